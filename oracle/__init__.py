@@ -1,0 +1,179 @@
+"""CPU oracle for the NVFP4 W4A16 sigmoid-top-k MoE decode layer.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (the CUDA library and its Python binding) never imports, links or
+runs anything here, and this package imports nothing from the product.
+
+The arithmetic lives in ``oracle.c`` (plain scalar C, FP64); this module only
+builds it with gcc, loads it with ctypes and marshals numpy arrays.  Every
+function of ``oracle.c`` cites the page passage it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, OpenMP)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c99",
+           "-D_DEFAULT_SOURCE", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
+        ("I", ctypes.c_int), ("S", ctypes.c_int), ("Is", ctypes.c_int),
+        ("normalize", ctypes.c_int), ("routed_scale", ctypes.c_double),
+        ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
+        ("w13", ctypes.c_void_p), ("w13_sf", ctypes.c_void_p), ("w13_gs", ctypes.c_void_p),
+        ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p),
+        ("sw13", ctypes.c_void_p), ("sw13_sf", ctypes.c_void_p), ("sw13_gs", ctypes.c_void_p),
+        ("sw2", ctypes.c_void_p), ("sw2_sf", ctypes.c_void_p), ("sw2_gs", ctypes.c_void_p),
+    ]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            d, i, vp = ctypes.c_double, ctypes.c_int, ctypes.c_void_p
+            L.orc_e2m1.restype = d
+            L.orc_e2m1.argtypes = [i]
+            L.orc_e4m3.restype = d
+            L.orc_e4m3.argtypes = [i]
+            L.orc_bf16_round.restype = d
+            L.orc_bf16_round.argtypes = [d]
+            L.orc_double_to_bf16.restype = ctypes.c_uint16
+            L.orc_double_to_bf16.argtypes = [d]
+            L.orc_bf16_to_double.restype = d
+            L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.orc_dequant.restype = None
+            L.orc_dequant.argtypes = [vp, vp, ctypes.c_float, i, i, vp]
+            L.orc_route.restype = i
+            L.orc_route.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp]
+            L.orc_forward.restype = i
+            L.orc_forward.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp, i]
+            L.orc_max_threads.restype = i
+            L.orc_max_threads.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class _Bound:
+    """Keeps the contiguous arrays alive while the C struct points at them."""
+
+    def __init__(self, layer: dict):
+        self.arrs = {}
+        for name, dt in [("router_w", np.float32), ("router_b", np.float32),
+                         ("w13", np.uint8), ("w13_sf", np.uint8), ("w13_gs", np.float32),
+                         ("w2", np.uint8), ("w2_sf", np.uint8), ("w2_gs", np.float32),
+                         ("sw13", np.uint8), ("sw13_sf", np.uint8), ("sw13_gs", np.float32),
+                         ("sw2", np.uint8), ("sw2_sf", np.uint8), ("sw2_gs", np.float32)]:
+            self.arrs[name] = _c(layer.get(name), dt)
+        c = layer["cfg"]
+        self.s = _Layer(H=c["H"], E=c["E"], k=c["k"], I=c["I"], S=c["S"], Is=c["Is"],
+                        normalize=int(c.get("normalize", 1)),
+                        routed_scale=float(c.get("routed_scale", 1.0)),
+                        **{n: _ptr(a) for n, a in self.arrs.items()})
+
+
+def e2m1(code: int) -> float:
+    return lib().orc_e2m1(int(code))
+
+
+def e4m3(code: int) -> float:
+    return lib().orc_e4m3(int(code))
+
+
+def bf16_round(v: float) -> float:
+    return lib().orc_bf16_round(float(v))
+
+
+def to_bf16_bits(v: float) -> int:
+    return int(lib().orc_double_to_bf16(float(v)))
+
+
+def bf16_bits_to_float(b: int) -> float:
+    return lib().orc_bf16_to_double(int(b))
+
+
+def dequant(codes: np.ndarray, sf: np.ndarray, gs: float) -> np.ndarray:
+    """[rows, cols/2] codes + [rows, cols/16] scales -> [rows, cols] FP32."""
+    codes = _c(codes, np.uint8)
+    sf = _c(sf, np.uint8)
+    rows, half = codes.shape
+    cols = half * 2
+    assert sf.shape == (rows, cols // 16)
+    out = np.empty((rows, cols), dtype=np.float32)
+    lib().orc_dequant(_ptr(codes), _ptr(sf), ctypes.c_float(gs), rows, cols, _ptr(out))
+    return out
+
+
+def route(layer: dict, x_bits: np.ndarray):
+    """Routing for T tokens -> (ids [T,k] int32, w [T,k] f64, scores [T,E] f64,
+    logits [T,E] f64)."""
+    b = _Bound(layer)
+    x = _c(x_bits, np.uint16)
+    T = x.shape[0]
+    c = layer["cfg"]
+    ids = np.empty((T, c["k"]), dtype=np.int32)
+    w = np.empty((T, c["k"]), dtype=np.float64)
+    s = np.empty((T, c["E"]), dtype=np.float64)
+    z = np.empty((T, c["E"]), dtype=np.float64)
+    rc = lib().orc_route(ctypes.byref(b.s), _ptr(x), T, _ptr(ids), _ptr(w), _ptr(s), _ptr(z))
+    if rc != 0:
+        raise MemoryError("oracle routing failed")
+    return ids, w, s, z
+
+
+def forward(layer: dict, x_bits: np.ndarray, nthreads: int | None = None):
+    """Full layer -> (out_bits [T,H] uint16, out_pre [T,H] f64, ids, w)."""
+    b = _Bound(layer)
+    x = _c(x_bits, np.uint16)
+    T = x.shape[0]
+    c = layer["cfg"]
+    out = np.empty((T, c["H"]), dtype=np.uint16)
+    pre = np.empty((T, c["H"]), dtype=np.float64)
+    ids = np.empty((T, c["k"]), dtype=np.int32)
+    w = np.empty((T, c["k"]), dtype=np.float64)
+    nt = nthreads if nthreads else max_threads()
+    rc = lib().orc_forward(ctypes.byref(b.s), _ptr(x), T, _ptr(out), _ptr(pre),
+                           _ptr(ids), _ptr(w), int(nt))
+    if rc != 0:
+        raise MemoryError("oracle forward failed")
+    return out, pre, ids, w
+
+
+def max_threads() -> int:
+    return int(lib().orc_max_threads())

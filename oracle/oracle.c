@@ -1,0 +1,362 @@
+/*
+ * oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, scalar FP64 evaluation of one decode step of a sigmoid-top-k
+ * Mixture-of-Experts layer whose experts are stored as NVFP4 weights and run
+ * weight-only (W4A16: BF16 activations, 4-bit weights).  Only tests, the smoke
+ * check and the CPU-baseline leg of the benchmark may load this library; the
+ * product path never does.  It shares no code, header, table or constant with
+ * the CUDA kernels: every decoder below is written from the number formats'
+ * definitions.
+ *
+ * Sources (pages are cited by title and section):
+ *  [FLINT]  "vLLM Day-0 support for Recursive's Flint" --
+ *           section "Flint model overview" (NVFP4 checkpoint run weight-only,
+ *           W4A16, BF16 activations), section "Flint model architecture"
+ *           (MoE bullet: 256 experts, sigmoid top-6 selection plus one shared
+ *           expert), section "Optimisation strategy" (small-batch MoE kernels
+ *           read only the selected experts' weights; the low-latency path folds
+ *           routing and the expert combine into the neighbouring GEMVs).
+ *  [INK2]   "Inkling 2 Small on vLLM: Day-0 Support" -- paragraph "Mixed-
+ *           precision MoE and Four-Over-Six NVFP4" (16-element blocks, block
+ *           maximum mapped to 6 or 4), section "vLLM integration and
+ *           optimisation" (SwiGLU between gate/up and down), section "Accuracy
+ *           evaluation" (the router runs in FP32; only reduction order may
+ *           differ from the reference numerics).
+ *  [ML4]    "Day 0 support for Mistral Large 4 on vLLM" -- "Highlights" and the
+ *           "Model architecture" table (128 routed experts, top-4, one shared
+ *           expert), section "Breakable CUDA graphs and fusions" (FP32 routing
+ *           GEMM).
+ *
+ * Readings where the pages are silent (the full list is kept in the design
+ * notes of the repository):
+ *  - NVFP4 = E2M1 codes, one E4M3 (fn variant) scale per 16 consecutive
+ *    elements along K, one FP32 tensor scale per (expert, matrix).
+ *  - Packing: K-major rows, element 2j in the low nibble of byte j, 2j+1 in the
+ *    high nibble.  Gate/up are one [2I, H] matrix: rows < I gate, rows >= I up.
+ *  - Dequantised weight = e2m1 * e4m3 * gs.  The first product is exact and the
+ *    whole product needs at most 30 significant bits, so it is exact in FP64;
+ *    the forward pass uses this exact value.  orc_dequant() returns it rounded
+ *    once to FP32 (round to nearest even).
+ *  - Router: logits in FP64 (the exact value of the FP32 router), score =
+ *    sigmoid(logit).  The top-k DECISION is taken on the FP32-rounded score
+ *    (the router's precision), descending, lowest expert index first on ties.
+ *    The weights use the FP64 scores, normalised to sum to 1 when asked, then
+ *    multiplied by the routed scale.
+ *  - Router bias, when present, is added to the logit (plain linear layer).
+ *  - Shared experts: ungated, weight 1, same NVFP4 format.
+ *  - SwiGLU: h = silu(gate) * up, silu(z) = z / (1 + exp(-z)); h is rounded to
+ *    BF16 (round to nearest even) before the down projection.
+ *  - Output: sum of routing-weighted routed outputs plus the shared outputs,
+ *    accumulated in FP64, rounded once to BF16.
+ *
+ * Build: gcc -O2 -fPIC -shared -fopenmp oracle.c -o liboracle.so -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* Number formats, written from their definitions.                           */
+/* ------------------------------------------------------------------------- */
+
+/* E2M1 (FP4): bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa.
+ * Exponent 0 is subnormal: value = m * 0.5.  Otherwise (1 + m/2) * 2^(e-1).
+ * The magnitudes are {0, 0.5, 1, 1.5, 2, 3, 4, 6}; 6 is the largest, matching
+ * the "scale the block maximum to 6" rule of [INK2] and 4 is representable. */
+double orc_e2m1(int code)
+{
+    int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
+}
+
+/* E4M3, "fn" variant (finite, no infinities): bit 7 sign, bits 6..3 exponent
+ * (bias 7), bits 2..0 mantissa.  Exponent 0 is subnormal: (m/8) * 2^-6.
+ * Exponent 15 with mantissa 7 is NaN (0x7F, 0xFF); everything else is finite,
+ * the largest magnitude being 1.75 * 2^8 = 448. */
+double orc_e4m3(int code)
+{
+    int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) mag = ldexp(m / 8.0, -6);
+    else mag = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* BF16 bits -> value (exact: a BF16 is the top half of an IEEE binary32). */
+double orc_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* Round a double to the nearest BF16 value (8 significant bits, exponent range
+ * of binary32, gradual underflow), ties to even, overflow to infinity.  Direct
+ * single rounding from FP64. */
+double orc_bf16_round(double v)
+{
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);             /* a in [2^(e-1), 2^e) */
+    int lead = e - 1;
+    if (lead < -126) lead = -126;           /* subnormal range: fixed quantum */
+    double quantum = ldexp(1.0, lead - 7);  /* 8 significant bits */
+    double n = a / quantum;                 /* exact: power-of-two scaling */
+    double r = nearbyint(n);                /* default mode: ties to even */
+    double res = r * quantum;
+    if (res >= 0x1p128) res = INFINITY;     /* beyond the largest BF16 */
+    return copysign(res, v);
+}
+
+uint16_t orc_double_to_bf16(double v)
+{
+    double r = orc_bf16_round(v);
+    float f = (float)r;       /* exact: r is a BF16 value (or inf/nan) */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if (isnan(v)) return (uint16_t)0x7FC0u;
+    return (uint16_t)(u >> 16);
+}
+
+/* Code nibble of element k in a K-major packed row (element 2j low nibble). */
+static inline int nib(const uint8_t *row, int k)
+{
+    uint8_t b = row[k >> 1];
+    return (k & 1) ? (b >> 4) : (b & 15);
+}
+
+/* Value tables filled from the closed forms above (speed only: the forward
+ * pass decodes ~10^9 elements for the largest layer). */
+static double tab_e2m1[16], tab_e4m3[256];
+static void fill_tables(void)
+{
+    static int done = 0;
+    if (done) return;
+    for (int c = 0; c < 16; ++c) tab_e2m1[c] = orc_e2m1(c);
+    for (int c = 0; c < 256; ++c) tab_e4m3[c] = orc_e4m3(c);
+    done = 1;
+}
+
+/* Exact dequantised weight W[r][k] = e2m1 * e4m3 * gs (FP64, exact). */
+static inline double wexact(const uint8_t *codes, const uint8_t *sf, double gs,
+                            int cols, int r, int k)
+{
+    const uint8_t *row = codes + (size_t)r * (cols / 2);
+    int sc = sf[(size_t)r * (cols / 16) + k / 16];
+    return tab_e2m1[nib(row, k)] * tab_e4m3[sc] * gs;
+}
+
+/* Dequantise a [rows, cols] NVFP4 matrix to FP32: one rounding of the exact
+ * product e2m1 * e4m3 * gs. */
+void orc_dequant(const uint8_t *codes, const uint8_t *sf, float gs,
+                 int rows, int cols, float *out)
+{
+    fill_tables();
+    for (int r = 0; r < rows; ++r)
+        for (int k = 0; k < cols; ++k)
+            out[(size_t)r * cols + k] = (float)wexact(codes, sf, (double)gs, cols, r, k);
+}
+
+/* ------------------------------------------------------------------------- */
+/* The layer.                                                                 */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int H, E, k, I, S, Is;      /* hidden, routed experts, top-k, expert inter, shared count, shared inter */
+    int normalize;              /* 1: routing weights normalised to sum to 1 */
+    double routed_scale;        /* multiplies the routed weights (1.0) */
+    const float *router_w;      /* [E, H] */
+    const float *router_b;      /* [E] or NULL */
+    const uint8_t *w13;         /* [E, 2I, H/2]  rows < I gate, rows >= I up */
+    const uint8_t *w13_sf;      /* [E, 2I, H/16] */
+    const float *w13_gs;        /* [E, 2] (gate, up) */
+    const uint8_t *w2;          /* [E, H, I/2] */
+    const uint8_t *w2_sf;       /* [E, H, I/16] */
+    const float *w2_gs;         /* [E] */
+    const uint8_t *sw13;        /* [S, 2Is, H/2] */
+    const uint8_t *sw13_sf;     /* [S, 2Is, H/16] */
+    const float *sw13_gs;       /* [S, 2] */
+    const uint8_t *sw2;         /* [S, H, Is/2] */
+    const uint8_t *sw2_sf;      /* [S, H, Is/16] */
+    const float *sw2_gs;        /* [S] */
+} orc_layer;
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* Router logits and sigmoid scores for one token ([FLINT] architecture: sigmoid
+ * scoring; [INK2] accuracy section and [ML4] fusions: FP32 router, whose exact
+ * value this is). */
+static void token_scores(const orc_layer *L, const uint16_t *xt, double *z, double *s)
+{
+    for (int e = 0; e < L->E; ++e) {
+        double acc = 0.0;
+        const float *wr = L->router_w + (size_t)e * L->H;
+        for (int h = 0; h < L->H; ++h) acc += orc_bf16_to_double(xt[h]) * (double)wr[h];
+        if (L->router_b) acc += (double)L->router_b[e];
+        z[e] = acc;
+        s[e] = sigmoid(acc);
+    }
+}
+
+/* Top-k by score: descending FP32-rounded score, lowest index first on ties.
+ * ids[j] in selection order; w[j] from the FP64 scores. */
+static void token_topk(const orc_layer *L, const double *s, int *ids, double *w)
+{
+    int E = L->E, K = L->k;
+    char *taken = (char *)calloc((size_t)E, 1);
+    for (int j = 0; j < K; ++j) {
+        int best = -1;
+        float bs = 0.0f;
+        for (int e = 0; e < E; ++e) {
+            if (taken[e]) continue;
+            float se = (float)s[e];
+            if (best < 0 || se > bs) { best = e; bs = se; }   /* strict: ties keep lower e */
+        }
+        taken[best] = 1;
+        ids[j] = best;
+    }
+    double sum = 0.0;
+    for (int j = 0; j < K; ++j) sum += s[ids[j]];
+    for (int j = 0; j < K; ++j) {
+        double wj = L->normalize ? s[ids[j]] / sum : s[ids[j]];
+        w[j] = wj * L->routed_scale;
+    }
+    free(taken);
+}
+
+/* Routing for T tokens: ids [T,k], w [T,k], optionally scores [T,E] (FP64
+ * sigmoid) and logits [T,E]. */
+int orc_route(const orc_layer *L, const uint16_t *x, int T, int *ids, double *w,
+              double *scores, double *logits)
+{
+    double *z = (double *)malloc(sizeof(double) * L->E);
+    double *s = (double *)malloc(sizeof(double) * L->E);
+    if (!z || !s) { free(z); free(s); return -1; }
+    for (int t = 0; t < T; ++t) {
+        token_scores(L, x + (size_t)t * L->H, z, s);
+        token_topk(L, s, ids + (size_t)t * L->k, w + (size_t)t * L->k);
+        if (scores) memcpy(scores + (size_t)t * L->E, s, sizeof(double) * L->E);
+        if (logits) memcpy(logits + (size_t)t * L->E, z, sizeof(double) * L->E);
+    }
+    free(z);
+    free(s);
+    return 0;
+}
+
+/* One expert MLP on one token ([INK2] integration section: SwiGLU between the
+ * gate/up and the down projection):
+ *   g_n = sum_k x_k Wg[n,k],  u_n = sum_k x_k Wu[n,k]
+ *   h_n = bf16(silu(g_n) * u_n)
+ *   y_m = sum_n h_n Wd[m,n]
+ * All weights are the exact dequantised values. */
+static void expert_mlp(int H, int I,
+                       const uint8_t *w13, const uint8_t *w13_sf, const float *w13_gs,
+                       const uint8_t *w2, const uint8_t *w2_sf, float w2_gs,
+                       const double *x, double *h, double *y)
+{
+    double gsg = (double)w13_gs[0], gsu = (double)w13_gs[1], gsd = (double)w2_gs;
+    for (int n = 0; n < I; ++n) {
+        double g = 0.0, u = 0.0;
+        for (int k = 0; k < H; ++k) {
+            g += x[k] * wexact(w13, w13_sf, gsg, H, n, k);
+            u += x[k] * wexact(w13, w13_sf, gsu, H, I + n, k);
+        }
+        double silu = g * sigmoid(g);
+        h[n] = orc_bf16_round(silu * u);
+    }
+    for (int m = 0; m < H; ++m) {
+        double acc = 0.0;
+        for (int n = 0; n < I; ++n) acc += h[n] * wexact(w2, w2_sf, gsd, I, m, n);
+        y[m] = acc;
+    }
+}
+
+/* Full decode step for T tokens.
+ *  out      [T,H] BF16 bits (required)
+ *  out_pre  [T,H] FP64 value before the final BF16 rounding (or NULL)
+ *  ids, w   [T,k] routing result (or NULL)
+ *  nthreads OpenMP threads for the per-(token, expert) work; the reduction is
+ *           in a fixed order, so the result does not depend on it.
+ * Per token: logits, sigmoid, top-k, normalise ([FLINT] architecture), the
+ * selected experts only ([FLINT] optimisation strategy) plus the shared
+ * experts, then the routing-weighted combine. */
+int orc_forward(const orc_layer *L, const uint16_t *x, int T, uint16_t *out,
+                double *out_pre, int *ids_out, double *w_out, int nthreads)
+{
+    int H = L->H, K = L->k, S = L->S, P = K + S;
+    fill_tables();
+    int Imax = L->I > L->Is ? L->I : L->Is;
+    int *ids = (int *)malloc(sizeof(int) * (size_t)T * K);
+    double *w = (double *)malloc(sizeof(double) * (size_t)T * K);
+    double *y = (double *)malloc(sizeof(double) * (size_t)T * P * H);
+    double *xd = (double *)malloc(sizeof(double) * (size_t)T * H);
+    if (!ids || !w || !y || !xd) { free(ids); free(w); free(y); free(xd); return -1; }
+    if (orc_route(L, x, T, ids, w, NULL, NULL) != 0) { free(ids); free(w); free(y); free(xd); return -1; }
+    for (size_t i = 0; i < (size_t)T * H; ++i) xd[i] = orc_bf16_to_double(x[i]);
+
+    int npairs = T * P;
+    int nt = nthreads > 0 ? nthreads : 1;
+    (void)nt;
+#ifdef _OPENMP
+    #pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+#endif
+    for (int pi = 0; pi < npairs; ++pi) {
+        int t = pi / P, j = pi % P;
+        double *h = (double *)malloc(sizeof(double) * (size_t)Imax);
+        double *yp = y + (size_t)pi * H;
+        const double *xt = xd + (size_t)t * H;
+        if (j < K) {
+            int e = ids[(size_t)t * K + j];
+            int I = L->I;
+            expert_mlp(H, I,
+                       L->w13 + (size_t)e * 2 * I * (H / 2), L->w13_sf + (size_t)e * 2 * I * (H / 16),
+                       L->w13_gs + 2 * (size_t)e,
+                       L->w2 + (size_t)e * H * (I / 2), L->w2_sf + (size_t)e * H * (I / 16),
+                       L->w2_gs[e], xt, h, yp);
+        } else {
+            int sidx = j - K, I = L->Is;
+            expert_mlp(H, I,
+                       L->sw13 + (size_t)sidx * 2 * I * (H / 2), L->sw13_sf + (size_t)sidx * 2 * I * (H / 16),
+                       L->sw13_gs + 2 * (size_t)sidx,
+                       L->sw2 + (size_t)sidx * H * (I / 2), L->sw2_sf + (size_t)sidx * H * (I / 16),
+                       L->sw2_gs[sidx], xt, h, yp);
+        }
+        free(h);
+    }
+
+    /* Combine, fixed order: routed experts in selection order, then shared. */
+    for (int t = 0; t < T; ++t) {
+        for (int m = 0; m < H; ++m) {
+            double acc = 0.0;
+            for (int j = 0; j < K; ++j)
+                acc += w[(size_t)t * K + j] * y[((size_t)t * P + j) * H + m];
+            for (int sidx = 0; sidx < S; ++sidx)
+                acc += y[((size_t)t * P + K + sidx) * H + m];
+            if (out_pre) out_pre[(size_t)t * H + m] = acc;
+            out[(size_t)t * H + m] = orc_double_to_bf16(acc);
+        }
+    }
+    if (ids_out) memcpy(ids_out, ids, sizeof(int) * (size_t)T * K);
+    if (w_out) memcpy(w_out, w, sizeof(double) * (size_t)T * K);
+    free(ids); free(w); free(y); free(xd);
+    return 0;
+}
+
+/* Threads the OpenMP runtime would use (1 without OpenMP). */
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

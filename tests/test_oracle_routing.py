@@ -1,0 +1,126 @@
+"""Pins for the oracle's router (no GPU).
+
+Sigmoid top-k with weights normalised to sum to 1 (Flint page, "Flint model
+architecture", MoE bullet), FP32 router decision (Inkling 2 Small page,
+"Accuracy evaluation").  Pinned by brute force over all k-subsets, by closed
+forms for the scores and weights, by the tie rule and by a permutation
+invariant.
+"""
+import itertools
+import math
+
+import numpy as np
+
+import gen
+
+
+def _router_layer(E, H, k, w, b=None, normalize=1, routed_scale=1.0):
+    c = dict(H=H, E=E, k=k, I=64, S=0, Is=64, normalize=normalize, routed_scale=routed_scale)
+    return {"cfg": c, "router_w": w.astype(np.float32), "router_b": b}
+
+
+def _bf16(a):
+    import torch
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bruteforce_topk_subsets(orc):
+    rng = np.random.default_rng(11)
+    E, H, k = 9, 32, 3
+    for trial in range(20):
+        w = rng.standard_normal((E, H)).astype(np.float32)
+        x = _bf16(rng.standard_normal((1, H)))
+        L = _router_layer(E, H, k, w)
+        ids, wt, s, z = orc.route(L, x)
+        best = max(itertools.combinations(range(E), k), key=lambda sub: sum(s[0][list(sub)]))
+        assert sorted(ids[0].tolist()) == sorted(best)
+        # selection order is descending score
+        assert all(s[0][ids[0][j]] >= s[0][ids[0][j + 1]] for j in range(k - 1))
+
+
+def test_scores_weights_closed_form(orc):
+    # x = one-hot 1.0 at h=0, router column 0 holds the logits -> z_e known exactly.
+    E, H, k = 6, 16, 3
+    zs = np.array([0.5, -1.0, 2.0, 0.25, 1.5, -0.75], np.float32)
+    w = np.zeros((E, H), np.float32)
+    w[:, 0] = zs
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x3F80                                   # BF16 1.0
+    L = _router_layer(E, H, k, w)
+    ids, wt, s, z = orc.route(L, x)
+    sig = [1 / (1 + math.exp(-float(v))) for v in zs]
+    assert np.allclose(s[0], sig, rtol=0, atol=1e-15)
+    assert ids[0].tolist() == [2, 4, 0]
+    tot = sig[2] + sig[4] + sig[0]
+    assert np.allclose(wt[0], [sig[2] / tot, sig[4] / tot, sig[0] / tot], rtol=0, atol=1e-15)
+    # bias adds to the logit
+    b = np.array([0, 0, -5, 0, 0, 3], np.float32)
+    ids, wt, s, z = orc.route(_router_layer(E, H, k, w, b), x)
+    assert np.allclose(z[0], zs.astype(np.float64) + b, rtol=0, atol=0)
+    assert ids[0].tolist() == [5, 4, 0]
+    # no normalisation: weights are the scores times the routed scale
+    ids, wt, s, z = orc.route(_router_layer(E, H, k, w, normalize=0, routed_scale=2.5), x)
+    assert np.allclose(wt[0], [2.5 * sig[2], 2.5 * sig[4], 2.5 * sig[0]], rtol=0, atol=1e-15)
+
+
+def test_ties_lowest_index_first(orc):
+    E, H, k = 8, 16, 2
+    w = np.zeros((E, H), np.float32)
+    w[:, 0] = [0.1, 0.3, 0.7, 0.2, 0.7, 0.7, 0.0, -1]   # experts 2, 4, 5 tie at the top
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x3F80
+    ids, *_ = orc.route(_router_layer(E, H, k, w), x)
+    assert ids[0].tolist() == [2, 4]
+
+
+def test_fp32_decision_precision(orc):
+    # Two logits whose FP64 sigmoids differ but round to the same FP32 score:
+    # the decision is taken on FP32 scores, so the lower index wins.
+    E, H, k = 3, 16, 1
+    z_hi, z_lo = 20.0, 19.5          # sigmoid -> 1 - 2e-9 vs 1 - 3.4e-9: both fl32 = 1.0
+    w = np.zeros((E, H), np.float32)
+    w[:, 0] = [z_lo, z_hi, -3.0]
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x3F80
+    ids, wt, s, _ = orc.route(_router_layer(E, H, k, w), x)
+    assert s[0][1] > s[0][0]
+    assert np.float32(s[0][1]) == np.float32(s[0][0])
+    assert ids[0].tolist() == [0]
+
+
+def test_weights_sum_to_one_and_permutation(orc):
+    c = gen.config(1)
+    R = gen.make_router(c, 5)
+    L = {"cfg": c, **R}
+    x = gen.make_x(c, 5, T=4)
+    ids, wt, s, z = orc.route(L, x)
+    assert np.allclose(wt.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    perm = np.random.default_rng(1).permutation(c["E"])        # new index p -> old perm[p]
+    Lp = {"cfg": c, "router_w": R["router_w"][perm], "router_b": None}
+    ids_p, wt_p, s_p, _ = orc.route(Lp, x)
+    inv = np.argsort(perm)
+    assert np.array_equal(perm[ids_p], ids)
+    assert np.array_equal(wt_p, wt)
+    assert np.array_equal(s_p[:, inv], s)
+
+
+def test_zipf_workload_popularity(orc):
+    """The skewed workload's router bias gives selection counts with a log-log
+    slope near -1.1 over the 64 most popular ranks."""
+    c = gen.config(3)
+    seed = 20261205
+    R = gen.make_router(c, seed)
+    L = {"cfg": c, **R}
+    counts = np.zeros(c["E"])
+    nb = 6
+    for b in range(nb):
+        ids, *_ = orc.route(L, gen.make_x(c, 1000 + b))
+        np.add.at(counts, ids.ravel(), 1)
+    perm = np.random.Generator(np.random.SFC64([seed, 3, 0])).permutation(c["E"])
+    byrank = np.zeros(c["E"])
+    byrank[perm] = counts
+    r = np.arange(1, 65)
+    y = byrank[:64]
+    m = y > 0
+    slope = np.polyfit(np.log(r[m]), np.log(y[m]), 1)[0]
+    assert -1.3 < slope < -0.9, slope
