@@ -1,0 +1,460 @@
+"""Benchmark of the NVFP4 W4A16 sigmoid-top-k MoE decode layer on GB300.
+
+One step = one decode step through every MoE layer of a Flint-shaped model:
+47 distinct layers (49 layers, the first two dense; "vLLM Day-0 support for
+Recursive's Flint", "Flint model architecture"), T tokens each, captured into
+one CUDA graph.  Metric: per-layer decode time and effective HBM GB/s over the
+bytes a layer must read (router, the selected experts and the shared expert,
+x and out).  The selected bytes are counted from the ids each layer returns.
+Distinct layers make every step read ~1 GB at T=1, far more than L2 (126 MB),
+so nothing is served from L2 across layers.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload flint1]
+  python bench.py --impl reference ...   (the CPU oracle, timed as the reference arm)
+
+Rank 0 prints one JSON line.  Under torchrun every rank runs its own layers
+(weak scaling, no collective on the data path) and the timed region is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode µs & effective HBM GB/s (selected-expert bytes) at T=1/8"
+WORKLOADS = {
+    # name: (config index, layers per step)
+    "flint1": (1, 47),
+    "flint8": (2, 47),
+    "ml4": (4, 6),
+    "zipf64": (3, 16),
+    "tiny": (0, 64),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="flint1", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0, help="override layers per step")
+    ap.add_argument("--secondary", default="flint8", help="second workload reported in the line ('' = none)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg_index: int, seconds: float, seed: int, want_out: bool = False):
+    """Time the oracle on whole-layer forwards of the workload until `seconds`
+    of CPU work have run.  -> dict(value GB/s, per_layer_s, layers, cores, ...)."""
+    import numpy as np
+    import gen
+    import oracle
+    c = gen.config(cfg_index)
+    router = gen.make_router(c, seed)
+    x = gen.make_x(c, seed)
+    ids, *_ = oracle.route({"cfg": c, **router}, x)
+    layer = {"cfg": c, **router, **gen.make_experts(c, seed, np.unique(ids))}
+    nthreads = oracle.max_threads()
+    pairs = c["T"] * (c["k"] + c["S"])
+    cores = min(nthreads, pairs)
+    n, t0, res = 0, time.perf_counter(), None
+    while True:
+        res = oracle.forward(layer, x, nthreads=nthreads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 10000:
+            break
+    U = len(np.unique(res[2]))
+    b = gen.selected_bytes(c, U)
+    out = {"value": b * n / el / 1e9, "per_layer_s": el / n, "layers": n, "cores": cores,
+           "selected_bytes": b, "seconds": el}
+    if want_out:
+        out["layer"], out["x"], out["result"] = layer, x, res
+    return out
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    ci, _ = WORKLOADS[args.workload]
+    import gen
+    c = gen.config(ci)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for w in range(args.warmup):
+        oracle_sample(ci, 0.0, gen.BASE_SEED + 100 + w)
+    total_b, layers, cores, el = 0.0, 0, 1, 0.0
+    for k in range(args.steps):
+        r = oracle_sample(ci, per_step, gen.BASE_SEED + 200 + k)
+        total_b += r["selected_bytes"] * r["layers"]
+        layers += r["layers"]
+        cores = r["cores"]
+        el += r["seconds"]     # oracle work only; input generation is not timed
+    gbs = total_b / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{c['name']}: T={c['T']} H={c['H']} E={c['E']} top-{c['k']} "
+                               f"I={c['I']} +{c['S']} shared, one layer per sample",
+                   "step": f"about {per_step:.1f} s of whole-layer oracle forwards"},
+        "us_per_layer": el * 1e6 / max(1, layers),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{layers} whole-layer FP64 forwards of the {c['name']} workload"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+class Chain:
+    """L distinct layers of one workload on the current GPU."""
+
+    def __init__(self, moe, torch, gen, ci, L, seed0):
+        self.c = gen.config(ci)
+        c = self.c
+        self.T, self.L = c["T"], L
+        self.layers, self.xs, self.outs, self.ids, self.ws = [], [], [], [], []
+        for l in range(L):
+            lay = gen.make_layer_torch(c, seed0 + l)
+            self.layers.append(moe.MoELayer(lay, max_tokens=self.T))
+            del lay
+            self.xs.append(gen.make_x_torch(c, seed0 + l))
+            self.outs.append(torch.empty((self.T, c["H"]), dtype=torch.bfloat16, device="cuda"))
+            self.ids.append(torch.empty((self.T, c["k"]), dtype=torch.int32, device="cuda"))
+            self.ws.append(torch.empty((self.T, c["k"]), dtype=torch.float32, device="cuda"))
+        torch.cuda.synchronize()
+
+    def enqueue(self, moe, stage=None):
+        for l in range(self.L):
+            h = self.layers[l].h
+            if stage is None:
+                moe.moe_decode_forward(h, self.xs[l], self.T, self.outs[l], self.ids[l], self.ws[l])
+            elif stage == "route":
+                moe.moe_stage_route(h, self.xs[l], self.T)
+            elif stage == "gate_up":
+                moe.moe_stage_gate_up(h, self.xs[l], self.T)
+            elif stage == "down":
+                moe.moe_stage_down(h, self.T)
+            elif stage == "combine":
+                moe.moe_stage_combine(h, self.T, self.outs[l], self.ids[l], self.ws[l])
+
+    def close(self):
+        for lay in self.layers:
+            lay.close()
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, stream, warmup, steps, sampler=None):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    return e0.elapsed_time(e1), clocks
+
+
+def byte_counts(gen, chain, np):
+    """Selected bytes per layer from the ids each layer returned, plus the
+    gate/up kernel's algorithmic bytes (weights of the slots, x in, h out)."""
+    c = chain.c
+    T, H, I, Is, S, k = c["T"], c["H"], c["I"], c["Is"], c["S"], c["k"]
+    sel, gu, Us = [], [], []
+    for l in range(chain.L):
+        U = len(np.unique(chain.ids[l].cpu().numpy()))
+        Us.append(U)
+        sel.append(gen.selected_bytes(c, U))
+        w13 = U * (2 * I * H // 2 + 2 * I * H // 16 + 8) + S * (2 * Is * H // 2 + 2 * Is * H // 16 + 8)
+        gu.append(w13 + T * H * 2 + T * (k + S) * max(I, Is) * 2)
+    return sel, gu, Us
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import gen
+    import nvfp4_weight_only_fp32_gb300 as moe
+    from nvfp4_weight_only_fp32_gb300 import build as moe_build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(ws, "nccl")
+    moe_build.build()
+    moe.lib()
+    dev = torch.device("cuda", local)
+    peak, peak_kind = peaks()
+    ci, L = WORKLOADS[args.workload]
+    L = args.layers or L
+    seed0 = gen.BASE_SEED + 1000 * (rank + 1) + 100 * ci
+    chain = Chain(moe, torch, gen, ci, L, seed0)
+    c = chain.c
+    stream = torch.cuda.Stream()
+
+    g_full = capture(torch, lambda: chain.enqueue(moe), stream)
+    sel, gu_bytes, Us = byte_counts(gen, chain, np)
+    barrier(dist)
+    sampler = ClockSampler(local)
+    ms, clocks = time_graph(torch, g_full, stream, args.warmup, args.steps, sampler)
+    barrier(dist)
+    ms_max = max_over_ranks(ms, dist, dev)
+    bytes_step = float(sum(sel))
+    total_bytes = sum_over_ranks(bytes_step * args.steps, dist, dev)
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    us_layer = ms * 1e3 / (args.steps * L)
+
+    # per-stage graphs: each kernel's average launch duration
+    stage_us = {}
+    for st in ("route", "gate_up", "down", "combine"):
+        g = capture(torch, lambda st=st: chain.enqueue(moe, st), stream)
+        sms, _ = time_graph(torch, g, stream, 3, max(5, args.steps // 2))
+        stage_us[st] = sms * 1e3 / (max(5, args.steps // 2) * L)
+        del g
+    gu_avg = float(np.mean(gu_bytes))
+    achieved = gu_avg / (stage_us["gate_up"] * 1e-6) / 1e9
+
+    # end to end through the host-buffer entry point (pinned memory)
+    T, H, k = c["T"], c["H"], c["k"]
+    xh = [chain.xs[l].cpu().pin_memory() for l in range(L)]
+    oh = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    ih = [torch.empty((T, k), dtype=torch.int32).pin_memory() for _ in range(L)]
+    wh = [torch.empty((T, k), dtype=torch.float32).pin_memory() for _ in range(L)]
+
+    def e2e_step():
+        for l in range(L):
+            moe.moe_decode_forward_host(chain.layers[l].h, xh[l], T, oh[l], ih[l], wh[l], stream)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_total = sum_over_ranks(bytes_step * args.steps, dist, dev)
+    e2e = {"value": e2e_total / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": L * T * H * 2,
+           "d2h_bytes_per_step": L * (T * H * 2 + T * k * 8),
+           "us_per_layer": e2e_ms * 1e3 / (args.steps * L)}
+    chain.close()
+    del chain, g_full
+    torch.cuda.empty_cache()
+
+    secondary = None
+    if args.secondary and args.secondary != args.workload and rank == 0:
+        si, sL = WORKLOADS[args.secondary]
+        ch2 = Chain(moe, torch, gen, si, sL, seed0 + 50000)
+        g2 = capture(torch, lambda: ch2.enqueue(moe), stream)
+        sel2, _, U2 = byte_counts(gen, ch2, np)
+        ms2, _ = time_graph(torch, g2, stream, args.warmup, args.steps)
+        us2 = ms2 * 1e3 / (args.steps * sL)
+        b2 = float(np.mean(sel2))
+        c2 = ch2.c
+        secondary = {"workload": f"{c2['name']}: T={c2['T']} H={c2['H']} E={c2['E']} top-{c2['k']} "
+                                 f"I={c2['I']} +{c2['S']} shared, {sL} layers per step",
+                     "us_per_layer": us2, "GBps": b2 / (us2 * 1e-6) / 1e9,
+                     "selected_bytes_per_layer": b2, "unique_experts_mean": float(np.mean(U2))}
+        ch2.close()
+        del g2
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r = oracle_sample(ci, args.cpu_seconds, gen.BASE_SEED + 7)
+        cpu = {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+               "sample": f"{r['layers']} whole-layer FP64 forwards of one {c['name']} layer "
+                         f"(T={c['T']}), {r['seconds']:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "w4a16(e2m1*e4m3 x bf16->f16 mma, fp32 acc)",
+            "data": "synthetic",
+            "config": {"workload": f"{c['name']}: T={c['T']} H={c['H']} E={c['E']} top-{c['k']} "
+                                   f"I={c['I']} +{c['S']} shared",
+                       "layers_per_step": L, "tokens_per_layer": c["T"],
+                       "l2": f"inputs larger than L2: {L} distinct layers, "
+                             f"{bytes_step / 1e6:.0f} MB selected bytes per step",
+                       "graph": "one CUDA graph per step, 4 kernels per layer chained with PDL"},
+            "us_per_layer": us_layer,
+            "selected_bytes_per_layer": bytes_step / L,
+            "unique_experts_mean": float(np.mean(Us)),
+            "frac_of_8TBps": value / 8000.0,
+            "stage_us": stage_us,
+            "roofline": {"bound": "hbm", "kernel": "gemv_kernel<gate/up>", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+                         "algorithmic_bytes_per_launch": gu_avg},
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": 4 * L * args.steps,
+            "cpu_baseline": cpu,
+        }
+        if secondary:
+            line["secondary"] = secondary
+        print(json.dumps(line), flush=True)
+    barrier(dist)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -206,3 +206,47 @@ def selected_bytes(c: dict, n_unique_routed: int) -> int:
     per_shared = 3 * Is * H // 2 + 3 * Is * H // 16 + 12
     router = E * H * 4 + (E * 4 if c.get("zipf") else 0)
     return router + n_unique_routed * per_routed + S * per_shared + T * H * 2 * 2
+
+
+def make_layer_torch(c: dict, seed: int, device="cuda") -> dict:
+    """The same recipe drawn with torch's generator on `device` (fast, for the
+    many distinct layer replicas a timing run needs; these replicas are never
+    compared with the oracle).  Returns canonical torch tensors."""
+    import torch
+    E, H, I, S, Is = c["E"], c["H"], c["I"], c["S"], c["Is"]
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+
+    def codes(*shape):
+        return torch.randint(0, 256, shape, dtype=torch.uint8, device=device, generator=g)
+
+    def scales(*shape):
+        u = torch.rand(shape, dtype=torch.float32, device=device, generator=g)
+        return (0.125 + 0.875 * u).to(torch.float8_e4m3fn).view(torch.uint8)
+
+    f32 = dict(dtype=torch.float32, device=device)
+    layer = {"cfg": dict(c)}
+    layer["router_w"] = torch.randn((E, H), generator=g, **f32) * (1.0 / math.sqrt(H))
+    layer["router_b"] = None
+    if c.get("zipf"):
+        perm = torch.randperm(E, generator=g, device=device).to(torch.float64) + 1.0
+        layer["router_b"] = (-ZIPF_ALPHA * ZIPF_S * torch.log(perm)).to(torch.float32)
+    layer.update({
+        "w13": codes(E, 2 * I, H // 2), "w13_sf": scales(E, 2 * I, H // 16),
+        "w13_gs": torch.full((E, 2), 1.0 / math.sqrt(H), **f32),
+        "w2": codes(E, H, I // 2), "w2_sf": scales(E, H, I // 16),
+        "w2_gs": torch.full((E,), 1.0 / math.sqrt(I), **f32),
+        "sw13": codes(S, 2 * Is, H // 2), "sw13_sf": scales(S, 2 * Is, H // 16),
+        "sw13_gs": torch.full((S, 2), 1.0 / math.sqrt(H), **f32),
+        "sw2": codes(S, H, Is // 2), "sw2_sf": scales(S, H, Is // 16),
+        "sw2_gs": torch.full((S,), 1.0 / math.sqrt(Is), **f32),
+    })
+    return layer
+
+
+def make_x_torch(c: dict, seed: int, T: int | None = None, device="cuda"):
+    import torch
+    T = c["T"] if T is None else T
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) + 7919)
+    return torch.randn((T, c["H"]), generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)

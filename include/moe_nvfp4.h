@@ -1,0 +1,203 @@
+/*
+ * moe_nvfp4.h -- C ABI of a GB300 (sm_103a) decode-step library for one
+ * sigmoid-top-k Mixture-of-Experts layer whose experts are NVFP4 weights run
+ * weight-only (W4A16: BF16 activations, 4-bit weights, FP32 accumulation).
+ *
+ * What the layer computes, per token t (sources are cited by page title and
+ * section):
+ *   a1  FP32 router GEMV      z[e] = sum_h x[t,h] * Wr[e,h] (+ b[e])
+ *         "Inkling 2 Small on vLLM: Day-0 Support", "Accuracy evaluation"
+ *         (FP32 router); "Day 0 support for Mistral Large 4 on vLLM",
+ *         "Breakable CUDA graphs and fusions" (FP32 routing GEMM).
+ *   a2  sigmoid top-k         s = sigmoid(z); the k largest s (lowest expert
+ *                             index first on ties); w = s_sel / sum(s_sel)
+ *         "vLLM Day-0 support for Recursive's Flint", "Flint model
+ *         architecture" (256 experts, sigmoid top-6 + one shared expert).
+ *   a3  gate/up + SwiGLU      h = bf16(silu(Wg x) * (Wu x)) for each selected
+ *                             expert and each shared expert
+ *   a4  down                  y = Wd h
+ *         Inkling 2 Small page, "vLLM integration and optimisation" (SwiGLU
+ *         between the gate/up and down projections); Flint page, "Optimisation
+ *         strategy" (the expert GEMVs read only the selected experts' weights).
+ *   a5  combine               out[t] = bf16(sum_j w_j y_j + sum_shared y_s)
+ *         Flint page, "Optimisation strategy" (routing and the expert combine
+ *         fused into the neighbouring GEMVs).
+ * Expert weights are NVFP4: E2M1 codes, one E4M3 (fn) scale per 16 elements
+ * along K (Inkling 2 Small page, "Mixed-precision MoE and Four-Over-Six
+ * NVFP4": 16-element blocks), one FP32 tensor scale per (expert, matrix).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless the name ends in _host.
+ *   - Integers are int32; BF16 tensors are arrays of uint16 bit patterns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - All work is enqueued asynchronously on `stream`; nothing here blocks the
+ *     host unless documented (moe_init, moe_check, moe_debug_dequant).
+ *   - Argument errors are detected on the host before anything is enqueued and
+ *     return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED; moe_last_error() then
+ *     names every reason.  The library never aborts, traps or prints.
+ *   - A handle may be used from one host thread at a time; different handles
+ *     are independent.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_layer moe_layer;   /* opaque handle */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, T out of range ... */
+    MOE_ERR_UNSUPPORTED = -2,   /* configuration outside what the kernels cover */
+    MOE_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_OOM = -4,           /* device allocation failed in moe_init */
+    MOE_ERR_TIMEOUT = -5,       /* a bounded in-kernel wait gave up */
+    MOE_ERR_DEVICE = -6         /* the sticky device error word was set */
+} moe_status;
+
+/* Layer configuration (host struct).
+ * Supported (anything else -> MOE_ERR_UNSUPPORTED with every reason listed;
+ * default-deny, as the Mistral Large 4 page's "Fail-stop" section describes
+ * for its specialised decode kernel):
+ *   hidden % 64 == 0, 64 <= hidden <= 16384
+ *   inter % 64 == 0 and shared_inter % 64 == 0 (when num_shared > 0), <= 16384
+ *   1 <= top_k <= 8, top_k <= num_experts <= 512
+ *   0 <= num_shared <= 2
+ *   1 <= max_tokens <= 64                                                     */
+typedef struct {
+    int hidden;             /* H */
+    int num_experts;        /* E routed experts */
+    int top_k;              /* k */
+    int inter;              /* I, routed expert intermediate size */
+    int num_shared;         /* S shared (always-on, weight 1) experts */
+    int shared_inter;       /* I of the shared experts */
+    int max_tokens;         /* largest T a call may pass; sizes the workspace */
+    int normalize_topk;     /* 1: routing weights normalised to sum to 1 */
+    float routed_scale;     /* multiplies every routed weight (1.0) */
+    int grouped_min_tokens; /* experts with at least this many tokens use the
+                               grouped tensor-core path when T > 8;
+                               0 = library default, < 0 = never */
+} moe_config;
+
+/* Weights in the canonical layout (device pointers, only read during
+ * moe_init; the caller may free them afterwards).
+ *   router_w  FP32 [E, H] row-major
+ *   router_b  FP32 [E] or NULL (added to the logit)
+ *   w13       uint8 [E, 2I, H/2]   E2M1 codes, row-major over K; element 2j in
+ *                                  the low nibble of byte j.  Rows 0..I-1 are
+ *                                  the gate projection, rows I..2I-1 the up one.
+ *   w13_sf    uint8 [E, 2I, H/16]  E4M3 (fn) block scales, one per 16 elements
+ *   w13_gs    FP32  [E, 2]         tensor scales (gate, up)
+ *   w2        uint8 [E, H, I/2]    down projection codes
+ *   w2_sf     uint8 [E, H, I/16]
+ *   w2_gs     FP32  [E]
+ *   sw13 ... sw2_gs: the same seven tensors for the shared experts, with E ->
+ *   num_shared and I -> shared_inter (NULL when num_shared == 0).
+ * Every pointer must be 16-byte aligned. */
+typedef struct {
+    const float *router_w;
+    const float *router_b;
+    const uint8_t *w13;
+    const uint8_t *w13_sf;
+    const float *w13_gs;
+    const uint8_t *w2;
+    const uint8_t *w2_sf;
+    const float *w2_gs;
+    const uint8_t *sw13;
+    const uint8_t *sw13_sf;
+    const float *sw13_gs;
+    const uint8_t *sw2;
+    const uint8_t *sw2_sf;
+    const float *sw2_gs;
+} moe_weights;
+
+/* Sizes a handle holds (for accounting). */
+typedef struct {
+    size_t weight_bytes;     /* repacked expert weights + router, device */
+    size_t workspace_bytes;  /* per-call scratch, device */
+    size_t expert_bytes;     /* bytes one routed expert's NVFP4 weights occupy */
+    size_t shared_bytes;     /* the same for one shared expert */
+    int max_slots;           /* worst-case number of distinct experts per call */
+    int sm_count;            /* SMs of the device the handle lives on */
+} moe_layer_info;
+
+/* Create a handle on the current device: validate `cfg` (default-deny), copy
+ * the router, repack every expert LOSSLESSLY into the kernels' streaming layout
+ * (the load-time repack of the Flint page, "Flint model overview": the NVFP4
+ * checkpoint is repacked without loss when it is loaded) and allocate the
+ * workspace for `max_tokens`.  Blocks until the repack has finished on
+ * `stream`.  On success *out owns all of it; release with moe_destroy. */
+moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream,
+                    moe_layer **out);
+
+/* Release a handle (synchronises its device first).  NULL is a no-op. */
+void moe_destroy(moe_layer *layer);
+
+/* One decode step, rows a1..a5 above, for T tokens (1 <= T <= max_tokens).
+ *   x         BF16 [T, H], 16-byte aligned, read only
+ *   out       BF16 [T, H], 16-byte aligned, written; must not alias x
+ *   topk_ids  int32 [T, k] or NULL: selected experts, descending score
+ *   topk_w    FP32  [T, k] or NULL: their routing weights (routed scale
+ *             applied)
+ * No host synchronisation; the launches form a chain of kernels that each
+ * start early (programmatic dependent launch) and wait for their inputs, so
+ * the call can be captured into a CUDA graph.  The handle's workspace is
+ * reused by every call: calls on one handle must be ordered on one stream. */
+moe_status moe_decode_forward(moe_layer *layer, const void *x, int T, void *out,
+                              int *topk_ids, float *topk_w, void *stream);
+
+/* The same step with HOST buffers (pinned memory for asynchronous copies):
+ * copies x_host to the device, runs moe_decode_forward, copies out and the
+ * routing result back.  Returns after enqueueing; the host buffers may be read
+ * after the stream has been synchronised. */
+moe_status moe_decode_forward_host(moe_layer *layer, const void *x_host, int T,
+                                   void *out_host, int *topk_ids_host,
+                                   float *topk_w_host, void *stream);
+
+/* The step split into its rows, for measurement.  moe_decode_forward is
+ * exactly moe_stage_route; moe_stage_gate_up; moe_stage_down;
+ * moe_stage_combine on one stream with the same T.
+ *   moe_stage_route     a1+a2: logits, sigmoid, top-k, weights, and the list
+ *                       of distinct selected experts with their tokens
+ *   moe_stage_gate_up   a3: gate/up GEMV + SwiGLU over the selected and the
+ *                       shared experts (BF16 intermediate in the workspace)
+ *   moe_stage_down      a4: down GEMV (FP32 per-expert outputs, workspace)
+ *   moe_stage_combine   a5: routing-weighted sum + shared, BF16 `out` */
+moe_status moe_stage_route(moe_layer *layer, const void *x, int T, void *stream);
+moe_status moe_stage_gate_up(moe_layer *layer, const void *x, int T, void *stream);
+moe_status moe_stage_down(moe_layer *layer, int T, void *stream);
+moe_status moe_stage_combine(moe_layer *layer, int T, void *out, int *topk_ids,
+                             float *topk_w, void *stream);
+
+/* Synchronise `stream`, then read and clear the handle's sticky device error
+ * word: MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (reason in
+ * moe_last_error()). */
+moe_status moe_check(moe_layer *layer, void *stream);
+
+/* Decode one repacked matrix back to the canonical row-major FP32 layout with
+ * the kernels' own decoder: value = fl32(e2m1 * e4m3 * gs), which must equal
+ * the canonical weights' exact dequantisation rounded once to FP32.
+ *   which   0 routed w13 [2I, H], 1 routed w2 [H, I],
+ *           2 shared w13 [2Is, H], 3 shared w2 [H, Is]
+ *   expert  routed expert id (which 0, 1) or shared index (which 2, 3)
+ *   dst     FP32 device buffer of rows*cols elements
+ * Synchronises `stream`. */
+moe_status moe_debug_dequant(moe_layer *layer, int which, int expert, float *dst,
+                             void *stream);
+
+/* Fill *info (host struct). */
+moe_status moe_get_info(const moe_layer *layer, moe_layer_info *info);
+
+/* Reasons for the last failure on this host thread ("" if none). */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

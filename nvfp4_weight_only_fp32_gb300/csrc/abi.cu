@@ -1,0 +1,476 @@
+// abi.cu -- the C ABI declared in include/moe_nvfp4.h: validation
+// (default-deny), the load-time repack, workspace management and the launch
+// sequence of one decode step.
+//
+// Default-deny start-up follows "Day 0 support for Mistral Large 4 on vLLM",
+// "Fail-stop": a configuration the kernels do not cover fails at start-up and
+// the error lists every reason, rather than running something unsupported.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_layer {
+    moe_config cfg;
+    int device;
+    int sm_count;
+    DevLayer d;
+    void *wmem;
+    size_t wbytes;
+    void *wsmem;
+    size_t wsbytes;
+    __nv_bfloat16 *x_stage;
+    __nv_bfloat16 *out_stage;
+    int *ids_stage;
+    float *w_stage;
+    std::vector<float> gs13_h, gs2_h, sgs13_h, sgs2_h;
+    size_t expert_bytes, shared_bytes;
+    float *router_b_slot;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+moe_status fail(moe_status st, const std::string &msg) {
+    g_err = msg;
+    return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char *what) {
+    g_err = std::string(what) + ": " + cudaGetErrorString(e);
+    return MOE_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+std::string join(const std::vector<std::string> &v) {
+    std::string s;
+    for (size_t i = 0; i < v.size(); ++i) {
+        if (i) s += "; ";
+        s += v[i];
+    }
+    return s;
+}
+
+std::vector<std::string> unsupported_reasons(const moe_config *c) {
+    std::vector<std::string> why;
+    auto chk = [&](bool ok, const char *msg) {
+        if (!ok) why.emplace_back(msg);
+    };
+    chk(c->hidden >= 64 && c->hidden <= 16384 && c->hidden % 64 == 0,
+        "hidden must be a multiple of 64 in [64, 16384]");
+    chk(c->inter >= 64 && c->inter <= 16384 && c->inter % 64 == 0,
+        "inter must be a multiple of 64 in [64, 16384]");
+    chk(c->num_shared >= 0 && c->num_shared <= kMaxShared, "num_shared must be 0, 1 or 2");
+    if (c->num_shared > 0)
+        chk(c->shared_inter >= 64 && c->shared_inter <= 16384 && c->shared_inter % 64 == 0,
+            "shared_inter must be a multiple of 64 in [64, 16384]");
+    chk(c->num_experts >= 1 && c->num_experts <= kMaxExperts, "num_experts must be in [1, 512]");
+    chk(c->top_k >= 1 && c->top_k <= kMaxTopK, "top_k must be in [1, 8]");
+    chk(c->top_k <= c->num_experts, "top_k must not exceed num_experts");
+    chk(c->max_tokens >= 1 && c->max_tokens <= kMaxTokens, "max_tokens must be in [1, 64]");
+    chk(c->normalize_topk == 0 || c->normalize_topk == 1, "normalize_topk must be 0 or 1");
+    chk(std::isfinite(c->routed_scale), "routed_scale must be finite");
+    return why;
+}
+
+bool is_device_ptr(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+struct Carver {
+    char *base;
+    size_t off = 0;
+    template <class T>
+    T *take(size_t count) {
+        off = (off + 255) & ~(size_t)255;
+        T *p = reinterpret_cast<T *>(base ? base + off : nullptr);
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+// Lay out (or measure, when base == nullptr) the weight block.
+void carve_weights(moe_layer *L, char *base) {
+    const moe_config &c = L->cfg;
+    DevLayer &d = L->d;
+    Carver cv{base};
+    const int E = c.num_experts, H = c.hidden, I = c.inter, S = c.num_shared;
+    const int Is = S > 0 ? c.shared_inter : I;
+    d.router_w = cv.take<float>((size_t)E * H);
+    d.router_b = nullptr;
+    L->router_b_slot = cv.take<float>(E);
+    d.e13_stride = repacked_bytes(2 * I, H);
+    d.e2_stride = repacked_bytes(H, I);
+    d.s13_stride = repacked_bytes(2 * Is, H);
+    d.s2_stride = repacked_bytes(H, Is);
+    d.w13r = cv.take<uint8_t>((size_t)E * d.e13_stride);
+    d.w2r = cv.take<uint8_t>((size_t)E * d.e2_stride);
+    d.gs13 = cv.take<float>((size_t)E * 2);
+    d.gs2 = cv.take<float>(E);
+    d.sw13r = cv.take<uint8_t>((size_t)S * d.s13_stride);
+    d.sw2r = cv.take<uint8_t>((size_t)S * d.s2_stride);
+    d.sgs13 = cv.take<float>((size_t)(S > 0 ? S : 1) * 2);
+    d.sgs2 = cv.take<float>(S > 0 ? S : 1);
+    L->wbytes = cv.off;
+}
+
+void carve_workspace(moe_layer *L, char *base) {
+    const moe_config &c = L->cfg;
+    DevLayer &d = L->d;
+    Carver cv{base};
+    const int Tm = c.max_tokens, E = c.num_experts, K = c.top_k, S = c.num_shared, H = c.hidden;
+    d.logits = cv.take<float>((size_t)Tm * E);
+    d.ids = cv.take<int>((size_t)Tm * K);
+    d.wsel = cv.take<float>((size_t)Tm * K);
+    d.xexp = cv.take<int>(Tm);
+    d.nslots = cv.take<int>(1);
+    d.slot_expert = cv.take<int>(d.max_slots);
+    d.slot_m = cv.take<int>(d.max_slots);
+    d.slot_p0 = cv.take<int>(d.max_slots);
+    d.pair_tok = cv.take<int>(d.max_pairs);
+    d.pair_w = cv.take<float>(d.max_pairs);
+    d.pair_of = cv.take<int>((size_t)Tm * (K + S));
+    d.hmax = cv.take<unsigned>(d.max_pairs);
+    d.h_ws = cv.take<__nv_bfloat16>((size_t)d.max_pairs * d.Imax);
+    d.y_ws = cv.take<float>((size_t)d.max_pairs * H);
+    d.ticket = cv.take<unsigned>(1);
+    d.err = cv.take<int>(1);
+    L->x_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
+    L->out_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
+    L->ids_stage = cv.take<int>((size_t)Tm * K);
+    L->w_stage = cv.take<float>((size_t)Tm * K);
+    L->wsbytes = cv.off;
+}
+
+moe_status check_call(moe_layer *L, int T) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer handle is NULL");
+    if (T < 1 || T > L->cfg.max_tokens)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "T=" + std::to_string(T) + " outside [1, max_tokens=" +
+                        std::to_string(L->cfg.max_tokens) + "]");
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_last_error(void) { return g_err.c_str(); }
+
+moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, moe_layer **out) {
+    g_err.clear();
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!cfg || !w) return fail(MOE_ERR_INVALID_ARG, "cfg or weights is NULL");
+    std::vector<std::string> why = unsupported_reasons(cfg);
+    if (!why.empty()) return fail(MOE_ERR_UNSUPPORTED, join(why));
+
+    const int S = cfg->num_shared;
+    std::vector<std::string> bad;
+    auto need = [&](const void *p, const char *name) {
+        if (!p) bad.push_back(std::string(name) + " is NULL");
+        else if (!aligned16(p)) bad.push_back(std::string(name) + " is not 16-byte aligned");
+        else if (!is_device_ptr(p)) bad.push_back(std::string(name) + " is not a device pointer");
+    };
+    need(w->router_w, "router_w");
+    if (w->router_b) need(w->router_b, "router_b");
+    need(w->w13, "w13");
+    need(w->w13_sf, "w13_sf");
+    need(w->w13_gs, "w13_gs");
+    need(w->w2, "w2");
+    need(w->w2_sf, "w2_sf");
+    need(w->w2_gs, "w2_gs");
+    if (S > 0) {
+        need(w->sw13, "sw13");
+        need(w->sw13_sf, "sw13_sf");
+        need(w->sw13_gs, "sw13_gs");
+        need(w->sw2, "sw2");
+        need(w->sw2_sf, "sw2_sf");
+        need(w->sw2_gs, "sw2_gs");
+    }
+    if (!bad.empty()) return fail(MOE_ERR_INVALID_ARG, join(bad));
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    moe_layer *L = new moe_layer();
+    L->cfg = *cfg;
+    if (L->cfg.grouped_min_tokens == 0) L->cfg.grouped_min_tokens = 8;
+    cudaError_t e = cudaGetDevice(&L->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->sm_count, cudaDevAttrMultiProcessorCount, L->device);
+    if (e != cudaSuccess) {
+        delete L;
+        return cuda_fail(e, "device query");
+    }
+    const int E = cfg->num_experts, H = cfg->hidden, I = cfg->inter, K = cfg->top_k;
+    const int Is = S > 0 ? cfg->shared_inter : I;
+    DevLayer &d = L->d;
+    d.H = H;
+    d.E = E;
+    d.k = K;
+    d.I = I;
+    d.S = S;
+    d.Is = Is;
+    d.normalize = cfg->normalize_topk;
+    d.routed_scale = cfg->routed_scale;
+    d.max_tokens = cfg->max_tokens;
+    d.max_slots = std::min(E, cfg->max_tokens * K) + S;
+    d.max_pairs = cfg->max_tokens * (K + S);
+    d.Imax = std::max(I, Is);
+
+    carve_weights(L, nullptr);
+    carve_workspace(L, nullptr);
+    e = cudaMalloc(&L->wmem, L->wbytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete L;
+        return fail(MOE_ERR_OOM, "cudaMalloc of " + std::to_string(L->wbytes) + " weight bytes failed");
+    }
+    e = cudaMalloc(&L->wsmem, L->wsbytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(L->wmem);
+        delete L;
+        return fail(MOE_ERR_OOM, "cudaMalloc of workspace failed");
+    }
+    carve_weights(L, static_cast<char *>(L->wmem));
+    carve_workspace(L, static_cast<char *>(L->wsmem));
+    L->expert_bytes = d.e13_stride + d.e2_stride;
+    L->shared_bytes = d.s13_stride + d.s2_stride;
+
+    auto cp = [&](const void *dst, const void *src, size_t n) {
+        if (e == cudaSuccess && n) e = cudaMemcpyAsync(const_cast<void *>(dst), src, n, cudaMemcpyDeviceToDevice, st);
+    };
+    cp(d.router_w, w->router_w, (size_t)E * H * sizeof(float));
+    if (w->router_b) {
+        cp(L->router_b_slot, w->router_b, (size_t)E * sizeof(float));
+        d.router_b = L->router_b_slot;
+    }
+    cp(d.gs13, w->w13_gs, (size_t)E * 2 * sizeof(float));
+    cp(d.gs2, w->w2_gs, (size_t)E * sizeof(float));
+    if (S > 0) {
+        cp(d.sgs13, w->sw13_gs, (size_t)S * 2 * sizeof(float));
+        cp(d.sgs2, w->sw2_gs, (size_t)S * sizeof(float));
+    }
+    if (e == cudaSuccess)
+        e = launch_repack(w->w13, w->w13_sf, E, 2 * I, H, true, const_cast<uint8_t *>(d.w13r), st);
+    if (e == cudaSuccess)
+        e = launch_repack(w->w2, w->w2_sf, E, H, I, false, const_cast<uint8_t *>(d.w2r), st);
+    if (e == cudaSuccess && S > 0)
+        e = launch_repack(w->sw13, w->sw13_sf, S, 2 * Is, H, true, const_cast<uint8_t *>(d.sw13r), st);
+    if (e == cudaSuccess && S > 0)
+        e = launch_repack(w->sw2, w->sw2_sf, S, H, Is, false, const_cast<uint8_t *>(d.sw2r), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L->wsmem, 0, L->wsbytes, st);
+    L->gs13_h.resize((size_t)E * 2);
+    L->gs2_h.resize(E);
+    L->sgs13_h.resize((size_t)S * 2);
+    L->sgs2_h.resize(S);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(L->gs13_h.data(), w->w13_gs, (size_t)E * 2 * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(L->gs2_h.data(), w->w2_gs, (size_t)E * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && S > 0)
+        e = cudaMemcpyAsync(L->sgs13_h.data(), w->sw13_gs, (size_t)S * 2 * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && S > 0)
+        e = cudaMemcpyAsync(L->sgs2_h.data(), w->sw2_gs, (size_t)S * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = prepare_kernels();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        moe_status rs = cuda_fail(e, "moe_init");
+        cudaFree(L->wmem);
+        cudaFree(L->wsmem);
+        delete L;
+        return rs;
+    }
+    *out = L;
+    return MOE_OK;
+}
+
+void moe_destroy(moe_layer *L) {
+    if (!L) return;
+    DeviceGuard g(L->device);
+    cudaDeviceSynchronize();
+    cudaFree(L->wmem);
+    cudaFree(L->wsmem);
+    delete L;
+}
+
+moe_status moe_stage_route(moe_layer *L, const void *x, int T, void *stream) {
+    moe_status rc = check_call(L, T);
+    if (rc != MOE_OK) return rc;
+    if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
+    DeviceGuard g(L->device);
+    cudaError_t e = launch_route(L->d, static_cast<const __nv_bfloat16 *>(x), T,
+                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router launch");
+}
+
+moe_status moe_stage_gate_up(moe_layer *L, const void *x, int T, void *stream) {
+    moe_status rc = check_call(L, T);
+    if (rc != MOE_OK) return rc;
+    if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
+    DeviceGuard g(L->device);
+    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, L->sm_count,
+                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gate/up launch");
+}
+
+moe_status moe_stage_down(moe_layer *L, int T, void *stream) {
+    moe_status rc = check_call(L, T);
+    if (rc != MOE_OK) return rc;
+    DeviceGuard g(L->device);
+    cudaError_t e = launch_down(L->d, T, L->sm_count, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");
+}
+
+moe_status moe_stage_combine(moe_layer *L, int T, void *out, int *topk_ids, float *topk_w,
+                             void *stream) {
+    moe_status rc = check_call(L, T);
+    if (rc != MOE_OK) return rc;
+    if (!out || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "out is NULL or not 16-byte aligned");
+    DeviceGuard g(L->device);
+    cudaError_t e = launch_combine(L->d, T, static_cast<__nv_bfloat16 *>(out), topk_ids, topk_w,
+                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
+}
+
+moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int *topk_ids,
+                              float *topk_w, void *stream) {
+    moe_status rc = check_call(L, T);
+    if (rc != MOE_OK) return rc;
+    if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
+    if (!out || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "out is NULL or not 16-byte aligned");
+    const size_t nb = (size_t)T * L->cfg.hidden * 2;
+    const char *xa = static_cast<const char *>(x), *oa = static_cast<const char *>(out);
+    if (xa < oa + nb && oa < xa + nb) return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
+    rc = moe_stage_route(L, x, T, stream);
+    if (rc == MOE_OK) rc = moe_stage_gate_up(L, x, T, stream);
+    if (rc == MOE_OK) rc = moe_stage_down(L, T, stream);
+    if (rc == MOE_OK) rc = moe_stage_combine(L, T, out, topk_ids, topk_w, stream);
+    return rc;
+}
+
+moe_status moe_decode_forward_host(moe_layer *L, const void *x_host, int T, void *out_host,
+                                   int *topk_ids_host, float *topk_w_host, void *stream) {
+    moe_status rc = check_call(L, T);
+    if (rc != MOE_OK) return rc;
+    if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host or out_host is NULL");
+    DeviceGuard g(L->device);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t nb = (size_t)T * L->cfg.hidden * 2;
+    const size_t nk = (size_t)T * L->cfg.top_k;
+    cudaError_t e = cudaMemcpyAsync(L->x_stage, x_host, nb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "x upload");
+    rc = moe_decode_forward(L, L->x_stage, T, L->out_stage, L->ids_stage, L->w_stage, stream);
+    if (rc != MOE_OK) return rc;
+    e = cudaMemcpyAsync(out_host, L->out_stage, nb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && topk_ids_host)
+        e = cudaMemcpyAsync(topk_ids_host, L->ids_stage, nk * sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && topk_w_host)
+        e = cudaMemcpyAsync(topk_w_host, L->w_stage, nk * sizeof(float), cudaMemcpyDeviceToHost, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "result download");
+}
+
+moe_status moe_check(moe_layer *L, void *stream) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer handle is NULL");
+    DeviceGuard g(L->device);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, L->d.err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "error word read");
+    if (word == 0) return MOE_OK;
+    int zero = 0;
+    cudaMemcpy(L->d.err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (word == 1) return fail(MOE_ERR_TIMEOUT, "an in-kernel wait gave up");
+    return fail(MOE_ERR_DEVICE, "device error word " + std::to_string(word));
+}
+
+moe_status moe_debug_dequant(moe_layer *L, int which, int expert, float *dst, void *stream) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer handle is NULL");
+    if (!dst) return fail(MOE_ERR_INVALID_ARG, "dst is NULL");
+    const DevLayer &d = L->d;
+    const uint8_t *rep = nullptr;
+    int rows = 0, cols = 0;
+    float ga = 0.f, gb = 0.f;
+    bool gu = false;
+    if (which == 0 || which == 1) {
+        if (expert < 0 || expert >= d.E) return fail(MOE_ERR_INVALID_ARG, "expert out of range");
+        if (which == 0) {
+            rep = d.w13r + (size_t)expert * d.e13_stride;
+            rows = 2 * d.I;
+            cols = d.H;
+            ga = L->gs13_h[2 * expert];
+            gb = L->gs13_h[2 * expert + 1];
+            gu = true;
+        } else {
+            rep = d.w2r + (size_t)expert * d.e2_stride;
+            rows = d.H;
+            cols = d.I;
+            ga = gb = L->gs2_h[expert];
+        }
+    } else if (which == 2 || which == 3) {
+        if (expert < 0 || expert >= d.S) return fail(MOE_ERR_INVALID_ARG, "shared index out of range");
+        if (which == 2) {
+            rep = d.sw13r + (size_t)expert * d.s13_stride;
+            rows = 2 * d.Is;
+            cols = d.H;
+            ga = L->sgs13_h[2 * expert];
+            gb = L->sgs13_h[2 * expert + 1];
+            gu = true;
+        } else {
+            rep = d.sw2r + (size_t)expert * d.s2_stride;
+            rows = d.H;
+            cols = d.Is;
+            ga = gb = L->sgs2_h[expert];
+        }
+    } else {
+        return fail(MOE_ERR_INVALID_ARG, "which must be 0..3");
+    }
+    DeviceGuard g(L->device);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_dequant(rep, ga, gb, rows, cols, gu, dst, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "dequant");
+}
+
+moe_status moe_get_info(const moe_layer *L, moe_layer_info *info) {
+    if (!L || !info) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    info->weight_bytes = L->wbytes;
+    info->workspace_bytes = L->wsbytes;
+    info->expert_bytes = L->expert_bytes;
+    info->shared_bytes = L->shared_bytes;
+    info->max_slots = L->d.max_slots;
+    info->sm_count = L->sm_count;
+    return MOE_OK;
+}
+
+}  // extern "C"

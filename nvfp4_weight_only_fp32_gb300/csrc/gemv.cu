@@ -1,0 +1,361 @@
+// gemv.cu -- rows a3 and a4: NVFP4 weight-only GEMVs over the selected
+// experts and the shared experts.
+//
+// Sources: "vLLM Day-0 support for Recursive's Flint", "Optimisation strategy"
+// (small-batch MoE kernels: the expert GEMVs read only the selected experts'
+// weights); "Inkling 2 Small on vLLM: Day-0 Support", "vLLM integration and
+// optimisation" (SwiGLU between the gate/up and the down projection; kernels
+// chained with programmatic dependent launch so that each one's prologue
+// overlaps the previous one's tail).
+//
+// Work decomposition.  A CTA (8 warps) owns one expert slot (blockIdx.y) and a
+// group of 16-row weight tiles (blockIdx.x).  With T <= 8, `ksplit` warps share
+// one tile by splitting K and add their partial sums in shared memory in a
+// fixed order (deterministic).  Each warp streams its chunks (576 B: one
+// 16-byte code load and one 8-byte scale load per lane) through a register
+// ring PD chunks deep, decodes E2M1 x E4M3 exactly into f16 A fragments
+// (cvt.rn.f16x2.e2m1x2, cvt.rn.f16x2.e4m3x2, one f16x2 multiply) and issues
+// mma.m16n8k16 with FP32 accumulators against the activations of the slot's
+// tokens (B, staged once per CTA in shared memory, f16 after an exact
+// power-of-two prescale).  The tensor core here only takes the multiply-adds
+// off the CUDA cores so that decoding keeps up with HBM; the kernel is bound
+// by the weight stream.
+//
+// gate/up epilogue: tile rows 0..7 are gate rows and 8..15 the matching up
+// rows, so lane (g, q) holds gate and up of intermediate row 8r+g for its two
+// token columns: h = bf16(silu(gate) * up) is written to the workspace, and
+// the row max |h| of each (expert, token) pair is published for the down
+// kernel's prescale.
+// down epilogue: y = gs * acc (FP32) per (pair, output row) into the workspace.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 32 * kGemvWarps;
+constexpr int kStageBudget = 96 * 1024;   // B staging budget when a slot has > 8 tokens
+
+__device__ __forceinline__ int hexp_of(unsigned bits) {
+    float v = __uint_as_float(bits);
+    return (v > 0.f && isfinite(v)) ? max(0, ilogbf(v) - 14) : 0;
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void load_chunk(const uint8_t *tbase, int c, int lane, uint4 &cw,
+                                           uint2 &sw) {
+    const uint8_t *ch = tbase + (size_t)c * kChunkBytes;
+    cw = ld_stream_v4(ch + 16 * lane);
+    sw = ld_stream_v2(ch + kCodeBytes + 8 * (lane >> 2));
+}
+
+// Stage chunks [kc0, kc0+nch) of the slot's B rows (m real rows, zero rows up
+// to mpad) into shared memory as f16, permuted within each 64-element chunk so
+// that lane (g, q) reads its B fragments of four blocks with two 16-byte loads:
+// element kk = 16kb + 8h + 2q + e of a chunk sits at half index 16q + 4kb + 2h + e.
+template <int MODE>
+__device__ __forceinline__ void stage_rows(const DevLayer &d, const __nv_bfloat16 *__restrict__ x,
+                                           bool shared, int m, int mpad, int p0, int kc0, int nch,
+                                           uint8_t *bsm, int row_stride) {
+    const int items = mpad * nch * 8;
+    for (int it = threadIdx.x; it < items; it += kThreads) {
+        const int j = it / (nch * 8);
+        const int rem = it - j * nch * 8;
+        const int cc = rem >> 3, part = rem & 7;
+        uint32_t *dst = reinterpret_cast<uint32_t *>(bsm + (size_t)j * row_stride + cc * 128 +
+                                                     (part >> 1) * 8 + (part & 1) * 4);
+        if (j < m) {
+            const __nv_bfloat16 *row;
+            int ex;
+            if (MODE == 0) {
+                const int tok = shared ? j : __ldcg(d.pair_tok + p0 + j);
+                row = x + (size_t)tok * d.H;
+                ex = __ldcg(d.xexp + tok);
+            } else {
+                const int p = p0 + j;
+                row = d.h_ws + (size_t)p * d.Imax;
+                ex = hexp_of(__ldcg(d.hmax + p));
+            }
+            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(row + (size_t)(kc0 + cc) * kChunkK + part * 8));
+            const float sc = pow2f(-ex);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                float lo = __uint_as_float(w[qq] << 16) * sc;
+                float hi = __uint_as_float(w[qq] & 0xFFFF0000u) * sc;
+                dst[qq * 8] = pack_f16x2(lo, hi);
+            }
+        } else {
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) dst[qq * 8] = 0u;
+        }
+    }
+}
+
+template <int PD>
+__device__ __forceinline__ void prefetch_ring(const uint8_t *tbase, int c_begin, int c_end, int lane,
+                                              uint4 (&cb)[PD], uint2 (&sb)[PD]) {
+#pragma unroll
+    for (int i = 0; i < PD; ++i)
+        if (c_begin + i < c_end) load_chunk(tbase, c_begin + i, lane, cb[i], sb[i]);
+}
+
+template <int MODE, int GMAX, int PD>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
+                                                        int T, int ksplit) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int s = blockIdx.y;
+    const int tpc = kGemvWarps / ksplit;
+    const int tl = warp / ksplit, ks = warp - tl * ksplit;
+    const int r = blockIdx.x * tpc + tl;
+    const bool shared = s < d.S;
+
+    int m = 0, p0 = 0, NT = 0, NC = 0;
+    float gsa = 0.f, gsb = 0.f;
+    const uint8_t *wbase = nullptr;
+    uint4 cb[PD];
+    uint2 sb[PD];
+
+    if (shared) {
+        // The shared experts do not depend on routing: start streaming them
+        // before waiting for the router.
+        m = T;
+        p0 = s * T;
+        if (MODE == 0) {
+            NT = d.Is / 8;
+            NC = d.H / kChunkK;
+            gsa = d.sgs13[2 * s];
+            gsb = d.sgs13[2 * s + 1];
+            wbase = d.sw13r + (size_t)s * d.s13_stride;
+        } else {
+            NT = d.H / 16;
+            NC = d.Is / kChunkK;
+            gsa = d.sgs2[s];
+            wbase = d.sw2r + (size_t)s * d.s2_stride;
+        }
+        if (r < NT)
+            prefetch_ring<PD>(wbase + (size_t)r * NC * kChunkBytes, ks * NC / ksplit,
+                              (ks + 1) * NC / ksplit, lane, cb, sb);
+    }
+    pdl_wait();
+    if (!shared) {
+        const int ns = __ldcg(d.nslots);
+        if (s >= ns) {
+            pdl_trigger();
+            return;
+        }
+        const int e = __ldcg(d.slot_expert + s);
+        m = __ldcg(d.slot_m + s);
+        p0 = __ldcg(d.slot_p0 + s);
+        if (MODE == 0) {
+            NT = d.I / 8;
+            NC = d.H / kChunkK;
+            gsa = d.gs13[2 * e];
+            gsb = d.gs13[2 * e + 1];
+            wbase = d.w13r + (size_t)e * d.e13_stride;
+        } else {
+            NT = d.H / 16;
+            NC = d.I / kChunkK;
+            gsa = d.gs2[e];
+            wbase = d.w2r + (size_t)e * d.e2_stride;
+        }
+        if (r < NT)
+            prefetch_ring<PD>(wbase + (size_t)r * NC * kChunkBytes, ks * NC / ksplit,
+                              (ks + 1) * NC / ksplit, lane, cb, sb);
+    }
+    pdl_trigger();
+    if (blockIdx.x * tpc >= NT) return;   // whole CTA beyond this slot's tiles
+
+    const bool active = r < NT;
+    const uint8_t *tbase = wbase + (size_t)(active ? r : 0) * NC * kChunkBytes;
+    const int c_begin = ks * NC / ksplit, c_end = (ks + 1) * NC / ksplit;
+    const int mpad = (m + 7) & ~7;
+    const int G = mpad >> 3;
+    int ncst = NC;
+    if (GMAX > 1) {
+        const int lim = (kStageBudget / mpad - 16) / 128;
+        if (lim < NC) ncst = max(PD, (lim / PD) * PD);
+    }
+    const int row_stride = ncst * 128 + 16;
+    float *red = reinterpret_cast<float *>(smem + (size_t)mpad * row_stride);
+
+    float acc[GMAX][4];
+#pragma unroll
+    for (int G2 = 0; G2 < GMAX; ++G2)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[G2][v] = 0.f;
+
+    for (int st0 = 0; st0 < NC; st0 += ncst) {
+        const int st1 = min(NC, st0 + ncst);
+        if (st0 > 0) __syncthreads();
+        stage_rows<MODE>(d, x, shared, m, mpad, p0, st0, st1 - st0, smem, row_stride);
+        __syncthreads();
+        if (active) {
+            const int lo = max(st0, c_begin), hi = min(st1, c_end);
+            const uint8_t *brow = smem + (size_t)g * row_stride + q * 32;
+            for (int cc = lo; cc < hi; cc += PD) {
+#pragma unroll
+                for (int i = 0; i < PD; ++i) {
+                    const int c = cc + i;
+                    if (c < hi) {
+                        uint32_t a[4][4];
+                        decode_chunk(cb[i], sb[i], a);
+                        const uint8_t *bp0 = brow + (c - st0) * 128;
+#pragma unroll
+                        for (int G2 = 0; G2 < GMAX; ++G2) {
+                            if (G2 < G) {
+                                const uint8_t *bp = bp0 + (size_t)G2 * 8 * row_stride;
+                                const uint4 b01 = lds128(bp);
+                                const uint4 b23 = lds128(bp + 16);
+                                mma_16816(acc[G2], a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
+                                mma_16816(acc[G2], a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
+                                mma_16816(acc[G2], a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
+                                mma_16816(acc[G2], a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                            }
+                        }
+                        const int cn = c + PD;
+                        if (cn < c_end) load_chunk(tbase, cn, lane, cb[i], sb[i]);
+                    }
+                }
+            }
+        }
+    }
+
+    if (ksplit > 1) {
+        // Fixed-order K reduction across the warps sharing a tile.
+        if (ks > 0) {
+            float *rp = red + (size_t)((tl * (ksplit - 1) + (ks - 1)) * 4) * 32;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) rp[v * 32 + lane] = acc[0][v];
+        }
+        __syncthreads();
+        if (ks == 0) {
+            for (int k2 = 1; k2 < ksplit; ++k2) {
+                const float *rp = red + (size_t)((tl * (ksplit - 1) + (k2 - 1)) * 4) * 32;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[0][v] += rp[v * 32 + lane];
+            }
+        }
+    }
+    if (ks != 0 || !active) return;
+
+    if (MODE == 0) {
+        const int n = 8 * r + g;
+#pragma unroll
+        for (int G2 = 0; G2 < GMAX; ++G2) {
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int col = 8 * G2 + 2 * q + e2;
+                const bool ok = G2 < G && col < m;
+                float habs = 0.f;
+                if (ok) {
+                    const int p = p0 + col;
+                    const int tok = shared ? col : __ldcg(d.pair_tok + p);
+                    const float sc = pow2f(__ldcg(d.xexp + tok));
+                    const float gt = acc[G2][e2] * gsa * sc;
+                    const float up = acc[G2][2 + e2] * gsb * sc;
+                    const float hv = gt / (1.0f + expf(-gt)) * up;
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                    d.h_ws[(size_t)p * d.Imax + n] = hb;
+                    habs = fabsf(__bfloat162float(hb));
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1)
+                    habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, off));
+                if (ok && g == 0) atomicMax(d.hmax + p0 + col, __float_as_uint(habs));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int G2 = 0; G2 < GMAX; ++G2) {
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int col = 8 * G2 + 2 * q + e2;
+                if (G2 < G && col < m) {
+                    const int p = p0 + col;
+                    const float sc = pow2f(hexp_of(__ldcg(d.hmax + p))) * gsa;
+                    float *yp = d.y_ws + (size_t)p * d.H + 16 * r + g;
+                    yp[0] = acc[G2][e2] * sc;
+                    yp[8] = acc[G2][2 + e2] * sc;
+                }
+            }
+        }
+    }
+}
+
+template <int MODE, int GMAX, int PD>
+cudaError_t launch_one(const DevLayer &d, const __nv_bfloat16 *x, int T, int ksplit, dim3 grid,
+                       size_t smem, cudaStream_t s) {
+    auto fn = gemv_kernel<MODE, GMAX, PD>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, d, x, T, ksplit);
+}
+
+template <int MODE>
+cudaError_t launch_stage(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s) {
+    const int slots = min(d.E, T * d.k) + d.S;
+    const int Iall = d.S > 0 ? max(d.I, d.Is) : d.I;
+    const int Imin = d.S > 0 ? min(d.I, d.Is) : d.I;
+    const int NT = MODE == 0 ? Iall / 8 : d.H / 16;
+    const int NCmax = MODE == 0 ? d.H / kChunkK : Iall / kChunkK;
+    const int NCmin = MODE == 0 ? d.H / kChunkK : Imin / kChunkK;
+    if (T <= 8) {
+        long tiles = (long)slots * NT;
+        int ksplit = 1;
+        while (ksplit < 4 && tiles * ksplit < 2048 && NCmin >= 4 * ksplit) ksplit *= 2;
+        const int tpc = kGemvWarps / ksplit;
+        dim3 grid((NT + tpc - 1) / tpc, slots);
+        size_t smem = (size_t)8 * (NCmax * 128 + 16) + (size_t)tpc * (ksplit - 1) * 4 * 32 * sizeof(float);
+        return launch_one<MODE, 1, 8>(d, x, T, ksplit, grid, smem, s);
+    }
+    dim3 grid((NT + kGemvWarps - 1) / kGemvWarps, slots);
+    return launch_one<MODE, 8, 4>(d, x, T, 1, grid, (size_t)kStageBudget, s);
+}
+
+template <int MODE, int GMAX, int PD>
+cudaError_t allow_smem(int bytes) {
+    return cudaFuncSetAttribute(gemv_kernel<MODE, GMAX, PD>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+cudaError_t prepare_kernels() {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = allow_smem<0, 1, 8>(optin);
+    if (e == cudaSuccess) e = allow_smem<1, 1, 8>(optin);
+    if (e == cudaSuccess) e = allow_smem<0, 8, 4>(optin);
+    if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
+    return e;
+}
+
+cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count,
+                           cudaStream_t s) {
+    (void)sm_count;
+    return launch_stage<0>(d, x, T, s);
+}
+
+cudaError_t launch_down(const DevLayer &d, int T, int sm_count, cudaStream_t s) {
+    (void)sm_count;
+    return launch_stage<1>(d, nullptr, T, s);
+}
+
+}  // namespace moe

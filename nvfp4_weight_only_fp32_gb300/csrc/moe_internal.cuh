@@ -1,0 +1,204 @@
+// moe_internal.cuh -- private declarations shared by the library's CUDA files.
+//
+// Streaming layout of the repacked NVFP4 weights (built once by moe_init):
+//
+//   A weight matrix is cut into tiles of 16 rows (the M of one
+//   mma.m16n8k16) and each tile's K range into chunks of 64 elements (four
+//   16-element NVFP4 blocks).  One chunk is 576 contiguous bytes:
+//
+//     bytes [0, 512)   codes.  Lane L = 4g + q of a warp owns bytes
+//                      [16L, 16L+16): word i (i = 0..3) holds the A-fragment
+//                      codes of block 4c+i for that lane, byte b of the word
+//                      being fragment register b:
+//                        b=0  row g,    k = 16(4c+i) + 2q + {0,1}
+//                        b=1  row g+8,  same k
+//                        b=2  row g,    k + 8
+//                        b=3  row g+8,  k + 8
+//                      (low nibble = the lower k, as in the canonical layout,
+//                      so each byte is a copy of one canonical byte).
+//     bytes [512, 576) E4M3 block scales: byte 8g + 2i + h is the scale of
+//                      row g + 8h for block 4c+i.
+//
+//   One warp therefore streams a chunk with one 16-byte load of codes and one
+//   8-byte load of scales per lane, and every loaded byte is used.
+//
+//   Gate/up (w13): tile r holds gate rows 8r..8r+7 as MMA rows 0..7 and the
+//   matching up rows as MMA rows 8..15, so SwiGLU pairs are lane-local in the
+//   accumulator.  Down (w2): tile r holds output rows 16r..16r+15.
+//   Offset of chunk c of tile r of expert e: ((e*NT + r)*NC + c) * 576.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "moe_nvfp4.h"
+
+namespace moe {
+
+constexpr int kBlockK = 16;        // NVFP4 block length along K
+constexpr int kChunkK = 64;        // K elements per streamed chunk
+constexpr int kChunkBytes = 576;   // 512 code bytes + 64 scale bytes
+constexpr int kCodeBytes = 512;
+constexpr int kGemvWarps = 8;      // warps per GEMV CTA
+constexpr int kMaxTokens = 64;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxExperts = 512;
+constexpr int kMaxShared = 2;
+constexpr int kRouteWarps = 4;     // experts per router CTA
+
+// Everything a kernel needs to know about a layer (passed by value).
+struct DevLayer {
+    int H, E, k, I, S, Is, normalize;
+    float routed_scale;
+    int max_tokens, max_slots, max_pairs, Imax;
+    const float *router_w;          // [E,H]
+    const float *router_b;          // [E] or null
+    const uint8_t *w13r;            // repacked, E experts
+    const uint8_t *w2r;
+    const float *gs13;              // [E,2]
+    const float *gs2;               // [E]
+    const uint8_t *sw13r;           // repacked, S shared experts
+    const uint8_t *sw2r;
+    const float *sgs13;             // [S,2]
+    const float *sgs2;              // [S]
+    size_t e13_stride, e2_stride;   // bytes per routed expert
+    size_t s13_stride, s2_stride;   // bytes per shared expert
+    // workspace (device)
+    float *logits;                  // [Tm, E]
+    int *ids;                       // [Tm, k]
+    float *wsel;                    // [Tm, k]
+    int *xexp;                      // [Tm]  power-of-two prescale of x rows
+    int *nslots;                    // [1]
+    int *slot_expert;               // [max_slots]  >=0 routed id, <0 -(shared+1)
+    int *slot_m;                    // [max_slots]  tokens on the slot
+    int *slot_p0;                   // [max_slots]  first pair of the slot
+    int *pair_tok;                  // [max_pairs]
+    float *pair_w;                  // [max_pairs]
+    int *pair_of;                   // [Tm, k+S]
+    unsigned *hmax;                 // [max_pairs]  max |h| bits per pair
+    __nv_bfloat16 *h_ws;            // [max_pairs, Imax]
+    float *y_ws;                    // [max_pairs, H]
+    unsigned *ticket;               // [1]
+    int *err;                       // [1] sticky device error word
+};
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (defined in the .cu files).
+// ---------------------------------------------------------------------------
+cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s);
+cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count,
+                           cudaStream_t s);
+cudaError_t launch_down(const DevLayer &d, int T, int sm_count, cudaStream_t s);
+cudaError_t launch_combine(const DevLayer &d, int T, __nv_bfloat16 *out, int *ids, float *w,
+                           cudaStream_t s);
+cudaError_t prepare_kernels();   // per device, once: shared-memory limits
+cudaError_t launch_repack(const uint8_t *codes, const uint8_t *sf, int n_mats, int rows, int cols,
+                          bool gate_up, uint8_t *dst, cudaStream_t s);
+cudaError_t launch_dequant(const uint8_t *rep, float gs_a, float gs_b, int rows, int cols,
+                           bool gate_up, float *dst, cudaStream_t s);
+
+// Chunk geometry.
+__host__ __device__ inline size_t repacked_bytes(int rows, int cols) {
+    return (size_t)(rows / 16) * (size_t)(cols / kChunkK) * kChunkBytes;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers (inline PTX).
+// ---------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Streaming loads of weights: read-only, not kept in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n"
+                 : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ float4 ld_f4(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+
+// Four E2M1 pairs (one byte each) -> four f16x2 (low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t &h0, uint32_t &h1,
+                                                uint32_t &h2, uint32_t &h3) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}\n"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(w));
+}
+
+// Two E4M3 bytes (low 16 bits of v) -> f16x2 (low byte -> low half).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}\n" : "=r"(r) : "r"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// D[16x8] += A[16x16] * B[16x8], f16 inputs, FP32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 r;
+    uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
+}
+
+// Decode one chunk's A fragments for one lane: 4 blocks x 4 registers.
+// a[i][b] = exact f16 products e2m1 * e4m3 (<= 6 significant bits, in range).
+__device__ __forceinline__ void decode_chunk(const uint4 &cw, const uint2 &sw,
+                                             uint32_t (&a)[4][4]) {
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t sp = (i < 2) ? (sw.x >> (16 * i)) : (sw.y >> (16 * (i - 2)));
+        uint32_t s2 = e4m3x2_to_f16x2(sp & 0xFFFFu);     // {s(row g), s(row g+8)}
+        uint32_t sg = __byte_perm(s2, 0, 0x1010);        // {s_g, s_g}
+        uint32_t sg8 = __byte_perm(s2, 0, 0x3232);       // {s_g8, s_g8}
+        uint32_t h0, h1, h2, h3;
+        e2m1x8_to_f16x2(words[i], h0, h1, h2, h3);
+        a[i][0] = hmul2(h0, sg);
+        a[i][1] = hmul2(h1, sg8);
+        a[i][2] = hmul2(h2, sg);
+        a[i][3] = hmul2(h3, sg8);
+    }
+}
+
+#endif  // __CUDACC__
+
+}  // namespace moe

@@ -1,0 +1,172 @@
+"""GPU vs oracle parity through the C ABI.
+
+Routing ids must match as sets (and in order where the scores are separated by
+the margin), weights within 1e-5 relative, outputs within
+|gpu - oracle| <= 1e-2 + 1e-2 |oracle| per element.  The five workloads run at
+their full sizes in the launch configuration the benchmark uses; smaller
+shapes cover several tiles with ragged ends, the degenerate cases and large
+activations."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from gpu_util import check_parity, load_moe, out_to_bits, run_gpu, x_to_device
+from moe_cases import guarded_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return load_moe()
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_workload_full_size(moe, orc, cfg):
+    layer, x, _ = guarded_case(cfg, gen.BASE_SEED + cfg)
+    gout, gids, gw = run_gpu(moe, layer, x)
+    check_parity(orc, layer, x, gout, gids, gw)
+
+
+def test_tiny_all_experts_real(moe, orc):
+    layer, x, _ = guarded_case(0, 7, T=8, full=True)
+    gout, gids, gw = run_gpu(moe, layer, x)
+    check_parity(orc, layer, x, gout, gids, gw)
+
+
+SHAPES = [
+    # H, E, k, I, S, Is, T
+    (64, 5, 1, 64, 0, 64, 1),
+    (192, 9, 3, 128, 1, 64, 3),
+    (320, 33, 4, 192, 2, 128, 7),
+    (128, 4, 4, 64, 1, 64, 8),        # every expert selected
+    (512, 40, 8, 256, 1, 256, 5),
+    (256, 17, 2, 320, 1, 192, 13),    # T > 8: grouped token path
+    (384, 64, 6, 128, 1, 128, 37),
+    (128, 8, 3, 64, 2, 64, 64),
+    (128, 1, 1, 64, 0, 64, 4),        # a single expert
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+def test_ragged_shapes(moe, orc, shape):
+    H, E, k, I, S, Is, T = shape
+    c = dict(name="ragged", T=T, H=H, E=E, k=k, I=I, S=S, Is=Is, zipf=False, normalize=1, routed_scale=1.0)
+    layer, x, _ = guarded_case(c, 1000 + H + E + T, full=True)
+    gout, gids, gw = run_gpu(moe, layer, x)
+    check_parity(orc, layer, x, gout, gids, gw)
+
+
+def test_no_normalisation_and_routed_scale(moe, orc):
+    c = gen.config(0, normalize=0, routed_scale=2.5)
+    layer, x, _ = guarded_case(c, 31, T=4, full=True)
+    gout, gids, gw = run_gpu(moe, layer, x)
+    check_parity(orc, layer, x, gout, gids, gw)
+
+
+def test_router_bias_zipf_small(moe, orc):
+    c = gen.config(3)
+    layer, x, _ = guarded_case(c, 77, T=16)
+    gout, gids, gw = run_gpu(moe, layer, x)
+    check_parity(orc, layer, x, gout, gids, gw)
+
+
+def test_large_activations_prescale(moe, orc):
+    """Activations far outside the f16 range (x * 2^20, so h ~ 2^40): the
+    kernels' power-of-two prescale must keep the result exact up to the usual
+    rounding.  The router rows are scaled by 2^-20 so the logits, hence the
+    routing, are exactly those of the unscaled input."""
+    layer, x, _ = guarded_case(0, 5, T=3, full=True)
+    xs = (x.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** 20)
+    xb = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    big = dict(layer)
+    big["router_w"] = layer["router_w"] * np.float32(2.0 ** -20)
+    gout, gids, gw = run_gpu(moe, big, xb)
+    err_abs, err_rel = check_parity(orc, big, xb, gout, gids, gw)
+    assert np.abs((gout.astype(np.uint32) << 16).view(np.float32)).max() > 1e9
+
+
+def test_zero_input(moe, orc):
+    layer, x, _ = guarded_case(0, 3, T=2, full=True)
+    xz = np.zeros_like(x)
+    gout, gids, gw = run_gpu(moe, layer, xz)
+    oout, _, oids, _ = orc.forward(layer, xz)
+    assert np.array_equal(gout, oout)
+
+
+def test_handle_reuse_varying_T_and_determinism(moe, orc):
+    layer, x, _ = guarded_case(2, 11, T=8)
+    L = moe.MoELayer(layer, max_tokens=8)
+    try:
+        first = None
+        for T in (8, 1, 5, 8):
+            gout, gids, gw = run_gpu(moe, layer, x[:T], layer_obj=L)
+            check_parity(orc, layer, x[:T], gout, gids, gw)
+            if T == 8:
+                if first is None:
+                    first = gout
+                else:
+                    assert np.array_equal(first, gout), "run-to-run difference"
+    finally:
+        L.close()
+
+
+def test_host_buffer_entry_point(moe, orc):
+    layer, x, _ = guarded_case(1, 13)
+    L = moe.MoELayer(layer, max_tokens=1)
+    try:
+        T, H, k = 1, layer["cfg"]["H"], layer["cfg"]["k"]
+        xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+        oh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        ih = torch.empty((T, k), dtype=torch.int32).pin_memory()
+        wh = torch.empty((T, k), dtype=torch.float32).pin_memory()
+        moe.moe_decode_forward_host(L.h, xh, T, oh, ih, wh)
+        torch.cuda.synchronize()
+        dout, dids, dw = run_gpu(moe, layer, x, layer_obj=L)
+        assert np.array_equal(out_to_bits(oh), dout)
+        assert np.array_equal(ih.numpy(), dids) and np.array_equal(wh.numpy(), dw)
+        check_parity(orc, layer, x, dout, dids, dw)
+    finally:
+        L.close()
+
+
+def test_stage_entry_points_equal_forward(moe, orc):
+    layer, x, _ = guarded_case(2, 17)
+    L = moe.MoELayer(layer, max_tokens=8)
+    try:
+        xd = x_to_device(x)
+        T, H, k = x.shape[0], layer["cfg"]["H"], layer["cfg"]["k"]
+        out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        moe.moe_stage_route(L.h, xd, T)
+        moe.moe_stage_gate_up(L.h, xd, T)
+        moe.moe_stage_down(L.h, T)
+        moe.moe_stage_combine(L.h, T, out, ids, w)
+        torch.cuda.synchronize()
+        fout, fids, fw = run_gpu(moe, layer, x, layer_obj=L)
+        assert np.array_equal(out_to_bits(out), fout)
+        assert np.array_equal(ids.cpu().numpy(), fids)
+    finally:
+        L.close()
+
+
+def test_invalid_calls_enqueue_nothing(moe):
+    layer, x, _ = guarded_case(0, 3, T=2, full=True)
+    L = moe.MoELayer(layer, max_tokens=2)
+    try:
+        xd = x_to_device(x)
+        out = torch.empty_like(xd)
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_decode_forward(L.h, xd, 3, out)
+        assert ei.value.status == moe.moe.MOE_ERR_INVALID_ARG
+        with pytest.raises(moe.MoEError):
+            moe.moe_decode_forward(L.h, xd, 0, out)
+        with pytest.raises(moe.MoEError):
+            moe.moe_decode_forward(L.h, xd, 2, xd)          # out aliases x
+        with pytest.raises(moe.MoEError):
+            moe.moe_decode_forward(L.h, xd.view(-1)[1:], 1, out)  # 2-byte offset: misaligned
+        assert moe.moe_check(L.h) == moe.MOE_OK
+    finally:
+        L.close()
