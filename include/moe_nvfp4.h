@@ -193,6 +193,32 @@ moe_status moe_debug_dequant(moe_layer *layer, int which, int expert, float *dst
 /* Fill *info (host struct). */
 moe_status moe_get_info(const moe_layer *layer, moe_layer_info *info);
 
+/* Routing only (rows a1 + a2) WITHOUT any device allocation, for callers that
+ * cannot call cudaMalloc where they route: an engine whose free device memory
+ * is already handed to its KV cache, code under an allocator that forbids raw
+ * cudaMalloc/cudaFree after start-up, or code that must avoid the implicit
+ * synchronisation an allocation may cause.  The pages have no counterpart to
+ * this entry point; it exists for such embedders.
+ *   router_w  FP32 [E, H] device, 16-byte aligned;  router_b FP32 [E] or NULL
+ *   x         BF16 [T, H] device, 16-byte aligned
+ *   topk_ids  int32 [T, k] device (written): selected experts, descending score
+ *   topk_w    FP32  [T, k] device (written): weights (normalised when
+ *             normalize_topk = 1, then times routed_scale)
+ * Same arithmetic and tie rule as moe_stage_route.  No handle is needed.
+ * Limits: 1 <= T <= 64, 1 <= E <= 512, 1 <= k <= min(8, E), hidden a multiple
+ * of 64 in [64, 16384]; anything else returns MOE_ERR_UNSUPPORTED naming the
+ * limit.  Scratch: a 128 KiB + 256 B static device array inside the library
+ * (every GPU that loads the library holds it until exit), shared by all calls
+ * on a device; calls whose kernels may overlap on the GPU (different streams or
+ * host threads on one device) race on it, so order them on one stream.  The
+ * first call on each device looks up that array's device address; make it
+ * before any stream capture.  Asynchronous on `stream`. */
+moe_status moe_route_topk_static(const float *router_w, const float *router_b,
+                                 int num_experts, int hidden, int top_k,
+                                 int normalize_topk, float routed_scale,
+                                 const void *x, int T, int *topk_ids,
+                                 float *topk_w, void *stream);
+
 /* Reasons for the last failure on this host thread ("" if none). */
 const char *moe_last_error(void);
 

@@ -182,6 +182,11 @@ moe_status check_call(moe_layer *L, int T) {
 
 }  // namespace
 
+namespace moe {
+// Lets other translation units report through moe_last_error().
+void record_error(const std::string &msg) { g_err = msg; }
+}  // namespace moe
+
 extern "C" {
 
 const char *moe_last_error(void) { return g_err.c_str(); }

@@ -28,6 +28,7 @@ EXPORTED = [
     "moe_init", "moe_destroy", "moe_decode_forward", "moe_decode_forward_host",
     "moe_stage_route", "moe_stage_gate_up", "moe_stage_down", "moe_stage_combine",
     "moe_check", "moe_debug_dequant", "moe_get_info", "moe_last_error",
+    "moe_route_topk_static",
 ]
 
 
@@ -94,6 +95,8 @@ def lib(path: str | None = None):
             L.moe_debug_dequant.restype = st
             L.moe_get_info.argtypes = [vp, ctypes.POINTER(moe_layer_info)]
             L.moe_get_info.restype = st
+            L.moe_route_topk_static.argtypes = [vp, vp, i, i, i, i, ctypes.c_float, vp, i, vp, vp, vp]
+            L.moe_route_topk_static.restype = st
             L.moe_last_error.argtypes = []
             L.moe_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -172,6 +175,16 @@ def moe_get_info(h) -> moe_layer_info:
     info = moe_layer_info()
     _check(lib().moe_get_info(h, ctypes.byref(info)))
     return info
+
+
+def moe_route_topk_static(router_w, router_b, num_experts, hidden, top_k, normalize_topk,
+                          routed_scale, x, T, topk_ids, topk_w, stream=None) -> None:
+    """Routing without any device allocation (scratch in a static device
+    array inside the library); see include/moe_nvfp4.h."""
+    _check(lib().moe_route_topk_static(_p(router_w), _p(router_b), int(num_experts), int(hidden),
+                                       int(top_k), int(normalize_topk), float(routed_scale), _p(x),
+                                       int(T), _p(topk_ids), _p(topk_w),
+                                       ctypes.c_void_p(_stream(stream))))
 
 
 # --- convenience wrapper ------------------------------------------------------
