@@ -259,13 +259,11 @@ class Chain:
             if stage is None:
                 moe.moe_decode_forward(h, self.xs[l], self.T, self.outs[l], self.ids[l], self.ws[l])
             elif stage == "route":
-                moe.moe_stage_route(h, self.xs[l], self.T)
+                moe.moe_stage_route(h, self.xs[l], self.T, self.ids[l], self.ws[l])
             elif stage == "gate_up":
                 moe.moe_stage_gate_up(h, self.xs[l], self.T)
             elif stage == "down":
-                moe.moe_stage_down(h, self.T)
-            elif stage == "combine":
-                moe.moe_stage_combine(h, self.T, self.outs[l], self.ids[l], self.ws[l])
+                moe.moe_stage_down(h, self.T, self.outs[l])
 
     def close(self):
         for lay in self.layers:
@@ -352,7 +350,7 @@ def run_gpu(args):
 
     # per-stage graphs: each kernel's average launch duration
     stage_us = {}
-    for st in ("route", "gate_up", "down", "combine"):
+    for st in ("route", "gate_up", "down"):
         g = capture(torch, lambda st=st: chain.enqueue(moe, st), stream)
         sms, _ = time_graph(torch, g, stream, 3, max(5, args.steps // 2))
         stage_us[st] = sms * 1e3 / (max(5, args.steps // 2) * L)
@@ -391,7 +389,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     secondary = None
-    if args.secondary and args.secondary != args.workload and rank == 0:
+    if args.secondary not in ("", "none") and args.secondary != args.workload and rank == 0:
         si, sL = WORKLOADS[args.secondary]
         ch2 = Chain(moe, torch, gen, si, sL, seed0 + 50000)
         g2 = capture(torch, lambda: ch2.enqueue(moe), stream)
@@ -425,7 +423,7 @@ def run_gpu(args):
                        "layers_per_step": L, "tokens_per_layer": c["T"],
                        "l2": f"inputs larger than L2: {L} distinct layers, "
                              f"{bytes_step / 1e6:.0f} MB selected bytes per step",
-                       "graph": "one CUDA graph per step, 4 kernels per layer chained with PDL"},
+                       "graph": "one CUDA graph per step, 3 kernels per layer chained with PDL"},
             "us_per_layer": us_layer,
             "selected_bytes_per_layer": bytes_step / L,
             "unique_experts_mean": float(np.mean(Us)),
@@ -437,7 +435,7 @@ def run_gpu(args):
                          "algorithmic_bytes_per_launch": gu_avg},
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": 4 * L * args.steps,
+            "gpu_launches": 3 * L * args.steps,
             "cpu_baseline": cpu,
         }
         if secondary:

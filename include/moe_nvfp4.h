@@ -82,6 +82,11 @@ typedef struct {
     int grouped_min_tokens; /* experts with at least this many tokens use the
                                grouped tensor-core path when T > 8;
                                0 = library default, < 0 = never */
+    int fused;              /* 0: moe_decode_forward runs the whole step as
+                               one launch when the shape allows it (T <= 8,
+                               H <= 4096, E <= 2 x SM count, activations fit
+                               in shared memory); < 0: always the three-kernel
+                               chain of the moe_stage_* entry points */
 } moe_config;
 
 /* Weights in the canonical layout (device pointers, only read during
@@ -124,6 +129,7 @@ typedef struct {
     size_t shared_bytes;     /* the same for one shared expert */
     int max_slots;           /* worst-case number of distinct experts per call */
     int sm_count;            /* SMs of the device the handle lives on */
+    int single_launch_max_tokens; /* largest T run as one launch (0: none) */
 } moe_layer_info;
 
 /* Create a handle on the current device: validate `cfg` (default-deny), copy
@@ -139,6 +145,11 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream,
 void moe_destroy(moe_layer *layer);
 
 /* One decode step, rows a1..a5 above, for T tokens (1 <= T <= max_tokens).
+ * Small steps run as ONE launch of one block per SM with two in-kernel grid
+ * barriers (all blocks must be resident together: do not share the GPU with
+ * work that fills every SM while it runs; a barrier wait that exceeds about a
+ * second gives up, and moe_check then reports MOE_ERR_TIMEOUT); otherwise as
+ * the chain moe_stage_route, moe_stage_gate_up, moe_stage_down.
  *   x         BF16 [T, H], 16-byte aligned, read only
  *   out       BF16 [T, H], 16-byte aligned, written; must not alias x
  *   topk_ids  int32 [T, k] or NULL: selected experts, descending score
@@ -159,20 +170,20 @@ moe_status moe_decode_forward_host(moe_layer *layer, const void *x_host, int T,
                                    void *out_host, int *topk_ids_host,
                                    float *topk_w_host, void *stream);
 
-/* The step split into its rows, for measurement.  moe_decode_forward is
- * exactly moe_stage_route; moe_stage_gate_up; moe_stage_down;
- * moe_stage_combine on one stream with the same T.
- *   moe_stage_route     a1+a2: logits, sigmoid, top-k, weights, and the list
- *                       of distinct selected experts with their tokens
+/* The step split into its kernels, for measurement.  moe_decode_forward is
+ * exactly moe_stage_route; moe_stage_gate_up; moe_stage_down on one stream
+ * with the same T.
+ *   moe_stage_route     a1+a2: logits, sigmoid, top-k, weights (also written
+ *                       to topk_ids / topk_w when not NULL), and the list of
+ *                       distinct selected experts with their tokens
  *   moe_stage_gate_up   a3: gate/up GEMV + SwiGLU over the selected and the
  *                       shared experts (BF16 intermediate in the workspace)
- *   moe_stage_down      a4: down GEMV (FP32 per-expert outputs, workspace)
- *   moe_stage_combine   a5: routing-weighted sum + shared, BF16 `out` */
-moe_status moe_stage_route(moe_layer *layer, const void *x, int T, void *stream);
+ *   moe_stage_down      a4+a5: down GEMV, then the routing-weighted combine
+ *                       with the shared experts into BF16 `out` */
+moe_status moe_stage_route(moe_layer *layer, const void *x, int T, int *topk_ids,
+                           float *topk_w, void *stream);
 moe_status moe_stage_gate_up(moe_layer *layer, const void *x, int T, void *stream);
-moe_status moe_stage_down(moe_layer *layer, int T, void *stream);
-moe_status moe_stage_combine(moe_layer *layer, int T, void *out, int *topk_ids,
-                             float *topk_w, void *stream);
+moe_status moe_stage_down(moe_layer *layer, int T, void *out, void *stream);
 
 /* Synchronise `stream`, then read and clear the handle's sticky device error
  * word: MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (reason in
@@ -189,6 +200,13 @@ moe_status moe_check(moe_layer *layer, void *stream);
  * Synchronises `stream`. */
 moe_status moe_debug_dequant(moe_layer *layer, int which, int expert, float *dst,
                              void *stream);
+
+/* Diagnostics: install a device buffer of 3 * blocks_per_kernel * 16 uint64
+ * that the traced build of the library (compiled with MOE_TRACE) fills with
+ * %globaltimer stamps at numbered phase points of its kernels (kernel 0
+ * router, 1 gate/up, 2 down; index [kernel][block][point]).  NULL detaches.
+ * The regular build returns MOE_ERR_UNSUPPORTED. */
+moe_status moe_trace_attach(moe_layer *layer, unsigned long long *buf, int blocks_per_kernel);
 
 /* Fill *info (host struct). */
 moe_status moe_get_info(const moe_layer *layer, moe_layer_info *info);

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe_nvfp4.so")
-SOURCES = ["abi.cu", "route.cu", "gemv.cu", "combine.cu", "repack.cu", "route_static.cu"]
+SOURCES = ["abi.cu", "route.cu", "gemv.cu", "fused.cu", "repack.cu", "route_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,24 +33,28 @@ def _flags(extra=()):
                    "-I", INCLUDE, "-I", CSRC, *extra]
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib_path) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib_path)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
         os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)] + [os.path.abspath(__file__)]
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          trace: bool = False) -> str:
+    """Build the library (trace=True: the phase-traced variant in _build/trace/)."""
+    out_dir = os.path.join(BUILD, "trace") if trace else BUILD
+    lib_path = os.path.join(out_dir, "libmoe_nvfp4.so")
+    if not force and not _stale(lib_path):
+        return lib_path
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DMOE_TRACE"] if trace else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = [cc, *_flags(extra), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,14 +65,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                trace="--trace" in sys.argv))

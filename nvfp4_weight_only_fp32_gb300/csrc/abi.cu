@@ -32,6 +32,8 @@ struct moe_layer {
     std::vector<float> gs13_h, gs2_h, sgs13_h, sgs2_h;
     size_t expert_bytes, shared_bytes;
     float *router_b_slot;
+    int optin_smem;
+    int fused_ok[kMaxTokens + 1];   // single-launch path usable for this T
 };
 
 namespace {
@@ -45,6 +47,7 @@ moe_status fail(moe_status st, const std::string &msg) {
 
 moe_status cuda_fail(cudaError_t e, const char *what) {
     g_err = std::string(what) + ": " + cudaGetErrorString(e);
+    cudaGetLastError();   // clear a non-sticky error so later CUDA calls do not report it
     return MOE_ERR_CUDA;
 }
 
@@ -163,7 +166,12 @@ void carve_workspace(moe_layer *L, char *base) {
     d.h_ws = cv.take<__nv_bfloat16>((size_t)d.max_pairs * d.Imax);
     d.y_ws = cv.take<float>((size_t)d.max_pairs * H);
     d.ticket = cv.take<unsigned>(1);
+    d.down_cnt = cv.take<unsigned>((size_t)H / 16);
     d.err = cv.take<int>(1);
+    d.hmax64 = cv.take<unsigned long long>(d.max_pairs);
+    d.epoch = cv.take<unsigned>(1);
+    d.bar_count = cv.take<unsigned>(1);
+    d.bar_gen = cv.take<unsigned>(1);
     L->x_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->out_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->ids_stage = cv.take<int>((size_t)Tm * K);
@@ -306,7 +314,14 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     if (e == cudaSuccess && S > 0)
         e = cudaMemcpyAsync(L->sgs2_h.data(), w->sw2_gs, (size_t)S * sizeof(float), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = prepare_kernels();
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->optin_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    for (int T = 0; T <= kMaxTokens; ++T) {
+        L->fused_ok[T] = 0;
+        if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&
+            fused_eligible(d, T, L->sm_count, (size_t)L->optin_smem))
+            L->fused_ok[T] = fused_blocks_per_sm(d, T) >= 2;
+    }
     if (e != cudaSuccess) {
         moe_status rs = cuda_fail(e, "moe_init");
         cudaFree(L->wmem);
@@ -327,12 +342,13 @@ void moe_destroy(moe_layer *L) {
     delete L;
 }
 
-moe_status moe_stage_route(moe_layer *L, const void *x, int T, void *stream) {
+moe_status moe_stage_route(moe_layer *L, const void *x, int T, int *topk_ids, float *topk_w,
+                           void *stream) {
     moe_status rc = check_call(L, T);
     if (rc != MOE_OK) return rc;
     if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
-    cudaError_t e = launch_route(L->d, static_cast<const __nv_bfloat16 *>(x), T,
+    cudaError_t e = launch_route(L->d, static_cast<const __nv_bfloat16 *>(x), T, topk_ids, topk_w,
                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router launch");
 }
@@ -342,28 +358,19 @@ moe_status moe_stage_gate_up(moe_layer *L, const void *x, int T, void *stream) {
     if (rc != MOE_OK) return rc;
     if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
-    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, L->sm_count,
+    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T,
                                    reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gate/up launch");
 }
 
-moe_status moe_stage_down(moe_layer *L, int T, void *stream) {
-    moe_status rc = check_call(L, T);
-    if (rc != MOE_OK) return rc;
-    DeviceGuard g(L->device);
-    cudaError_t e = launch_down(L->d, T, L->sm_count, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");
-}
-
-moe_status moe_stage_combine(moe_layer *L, int T, void *out, int *topk_ids, float *topk_w,
-                             void *stream) {
+moe_status moe_stage_down(moe_layer *L, int T, void *out, void *stream) {
     moe_status rc = check_call(L, T);
     if (rc != MOE_OK) return rc;
     if (!out || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "out is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
-    cudaError_t e = launch_combine(L->d, T, static_cast<__nv_bfloat16 *>(out), topk_ids, topk_w,
-                                   reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
+    cudaError_t e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out),
+                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");
 }
 
 moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int *topk_ids,
@@ -375,10 +382,16 @@ moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int
     const size_t nb = (size_t)T * L->cfg.hidden * 2;
     const char *xa = static_cast<const char *>(x), *oa = static_cast<const char *>(out);
     if (xa < oa + nb && oa < xa + nb) return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
-    rc = moe_stage_route(L, x, T, stream);
+    if (L->fused_ok[T]) {
+        DeviceGuard g(L->device);
+        cudaError_t e = launch_fused(L->d, static_cast<const __nv_bfloat16 *>(x), T,
+                                     static_cast<__nv_bfloat16 *>(out), topk_ids, topk_w, L->sm_count,
+                                     reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "single-launch layer");
+    }
+    rc = moe_stage_route(L, x, T, topk_ids, topk_w, stream);
     if (rc == MOE_OK) rc = moe_stage_gate_up(L, x, T, stream);
-    if (rc == MOE_OK) rc = moe_stage_down(L, T, stream);
-    if (rc == MOE_OK) rc = moe_stage_combine(L, T, out, topk_ids, topk_w, stream);
+    if (rc == MOE_OK) rc = moe_stage_down(L, T, out, stream);
     return rc;
 }
 
@@ -415,6 +428,8 @@ moe_status moe_check(moe_layer *L, void *stream) {
     if (word == 0) return MOE_OK;
     int zero = 0;
     cudaMemcpy(L->d.err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    // a wait that gave up leaves the grid barrier mid-way: reset it
+    cudaMemset(L->d.bar_count, 0, sizeof(unsigned));
     if (word == 1) return fail(MOE_ERR_TIMEOUT, "an in-kernel wait gave up");
     return fail(MOE_ERR_DEVICE, "device error word " + std::to_string(word));
 }
@@ -467,6 +482,19 @@ moe_status moe_debug_dequant(moe_layer *L, int which, int expert, float *dst, vo
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "dequant");
 }
 
+moe_status moe_trace_attach(moe_layer *L, unsigned long long *buf, int blocks_per_kernel) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer handle is NULL");
+#ifdef MOE_TRACE
+    L->d.trace = buf;
+    L->d.trace_blocks = buf ? blocks_per_kernel : 0;
+    return MOE_OK;
+#else
+    (void)buf;
+    (void)blocks_per_kernel;
+    return fail(MOE_ERR_UNSUPPORTED, "this library was built without MOE_TRACE");
+#endif
+}
+
 moe_status moe_get_info(const moe_layer *L, moe_layer_info *info) {
     if (!L || !info) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
     info->weight_bytes = L->wbytes;
@@ -475,6 +503,9 @@ moe_status moe_get_info(const moe_layer *L, moe_layer_info *info) {
     info->shared_bytes = L->shared_bytes;
     info->max_slots = L->d.max_slots;
     info->sm_count = L->sm_count;
+    info->single_launch_max_tokens = 0;
+    for (int T = 1; T <= L->cfg.max_tokens; ++T)
+        if (L->fused_ok[T]) info->single_launch_max_tokens = T;
     return MOE_OK;
 }
 

@@ -1,9 +1,10 @@
-// gemv.cu -- rows a3 and a4: NVFP4 weight-only GEMVs over the selected
-// experts and the shared experts.
+// gemv.cu -- rows a3, a4 and a5: NVFP4 weight-only GEMVs over the selected
+// experts and the shared experts, and the routing-weighted combine.
 //
 // Sources: "vLLM Day-0 support for Recursive's Flint", "Optimisation strategy"
 // (small-batch MoE kernels: the expert GEMVs read only the selected experts'
-// weights); "Inkling 2 Small on vLLM: Day-0 Support", "vLLM integration and
+// weights; the low-latency path folds the expert combine into the adjacent
+// GEMV); "Inkling 2 Small on vLLM: Day-0 Support", "vLLM integration and
 // optimisation" (SwiGLU between the gate/up and the down projection; kernels
 // chained with programmatic dependent launch so that each one's prologue
 // overlaps the previous one's tail).
@@ -21,12 +22,20 @@
 // off the CUDA cores so that decoding keeps up with HBM; the kernel is bound
 // by the weight stream.
 //
+// Prefetch before the programmatic-launch wait: gate/up streams the shared
+// experts' weights (they do not depend on routing); down streams every slot's
+// weights, because by the time it starts the router has finished (the gate/up
+// kernel released it only after waiting for the router), so only h is awaited.
+//
 // gate/up epilogue: tile rows 0..7 are gate rows and 8..15 the matching up
 // rows, so lane (g, q) holds gate and up of intermediate row 8r+g for its two
 // token columns: h = bf16(silu(gate) * up) is written to the workspace, and
 // the row max |h| of each (expert, token) pair is published for the down
 // kernel's prescale.
-// down epilogue: y = gs * acc (FP32) per (pair, output row) into the workspace.
+// down epilogue: y = gs * acc (FP32) per (pair, output row) into the
+// workspace; the CTA that finishes last among the slots of a row group (atomic
+// ticket, no spinning) sums sum_j w_j y_j + y_shared for those rows in a fixed
+// order and writes BF16 `out`.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -35,81 +44,72 @@ namespace {
 
 constexpr int kThreads = 32 * kGemvWarps;
 constexpr int kStageBudget = 96 * 1024;   // B staging budget when a slot has > 8 tokens
+constexpr int kMaxRows = 64;              // staged B rows (tokens of one slot)
 
 __device__ __forceinline__ int hexp_of(unsigned bits) {
     float v = __uint_as_float(bits);
     return (v > 0.f && isfinite(v)) ? max(0, ilogbf(v) - 14) : 0;
 }
 
-__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
+template <int PD>
+__device__ __forceinline__ void prefetch_ring(const uint8_t *tbase, int c_begin, int c_end, int lane,
+                                              uint4 (&cb)[PD], uint2 (&sb)[PD], uint64_t pol) {
+#pragma unroll
+    for (int i = 0; i < PD; ++i)
+        if (c_begin + i < c_end) load_chunk(tbase, c_begin + i, lane, cb[i], sb[i], pol);
 }
 
-__device__ __forceinline__ void load_chunk(const uint8_t *tbase, int c, int lane, uint4 &cw,
-                                           uint2 &sw) {
-    const uint8_t *ch = tbase + (size_t)c * kChunkBytes;
-    cw = ld_stream_v4(ch + 16 * lane);
-    sw = ld_stream_v2(ch + kCodeBytes + 8 * (lane >> 2));
-}
-
-// Stage chunks [kc0, kc0+nch) of the slot's B rows (m real rows, zero rows up
-// to mpad) into shared memory as f16, permuted within each 64-element chunk so
-// that lane (g, q) reads its B fragments of four blocks with two 16-byte loads:
-// element kk = 16kb + 8h + 2q + e of a chunk sits at half index 16q + 4kb + 2h + e.
-template <int MODE>
-__device__ __forceinline__ void stage_rows(const DevLayer &d, const __nv_bfloat16 *__restrict__ x,
-                                           bool shared, int m, int mpad, int p0, int kc0, int nch,
-                                           uint8_t *bsm, int row_stride) {
-    const int items = mpad * nch * 8;
-    for (int it = threadIdx.x; it < items; it += kThreads) {
-        const int j = it / (nch * 8);
-        const int rem = it - j * nch * 8;
-        const int cc = rem >> 3, part = rem & 7;
-        uint32_t *dst = reinterpret_cast<uint32_t *>(bsm + (size_t)j * row_stride + cc * 128 +
-                                                     (part >> 1) * 8 + (part & 1) * 4);
-        if (j < m) {
-            const __nv_bfloat16 *row;
-            int ex;
-            if (MODE == 0) {
-                const int tok = shared ? j : __ldcg(d.pair_tok + p0 + j);
-                row = x + (size_t)tok * d.H;
-                ex = __ldcg(d.xexp + tok);
-            } else {
-                const int p = p0 + j;
-                row = d.h_ws + (size_t)p * d.Imax;
-                ex = hexp_of(__ldcg(d.hmax + p));
-            }
-            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(row + (size_t)(kc0 + cc) * kChunkK + part * 8));
-            const float sc = pow2f(-ex);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Stage chunks [kc0, kc0+nch) of the slot's m real B rows into shared memory
+// as f16, permuted within each 64-element chunk so that lane (g, q) reads its B
+// fragments of four blocks with two 16-byte loads: element kk = 16kb + 8h +
+// 2q + e of a chunk sits at half index 16q + 4kb + 2h + e.  Row j comes from
+// s_src[j] scaled by s_scale[j] (an exact power of two).  Loads are issued four
+// at a time before any store.
+__device__ __forceinline__ void stage_rows(int m, int kc0, int nch, uint8_t *bsm, int row_stride,
+                                           const uint4 *const *s_src, const float *s_scale) {
+    const int per_row = nch * 8;
+    const int items = m * per_row;
+    for (int base = threadIdx.x; base < items; base += 4 * kThreads) {
+        uint4 v[4];
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                float lo = __uint_as_float(w[qq] << 16) * sc;
-                float hi = __uint_as_float(w[qq] & 0xFFFF0000u) * sc;
-                dst[qq * 8] = pack_f16x2(lo, hi);
+        for (int u = 0; u < 4; ++u) {
+            const int it = base + u * kThreads;
+            if (it < items) {
+                const int j = it / per_row, rem = it - j * per_row;
+                v[u] = __ldcg(s_src[j] + (size_t)kc0 * 8 + rem);
             }
-        } else {
+        }
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) dst[qq * 8] = 0u;
+        for (int u = 0; u < 4; ++u) {
+            const int it = base + u * kThreads;
+            if (it < items) {
+                const int j = it / per_row, rem = it - j * per_row;
+                const int cc = rem >> 3, part = rem & 7;
+                uint32_t *dst = reinterpret_cast<uint32_t *>(bsm + (size_t)j * row_stride + cc * 128 +
+                                                             (part >> 1) * 8 + (part & 1) * 4);
+                const float sc = s_scale[j];
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float lo = __uint_as_float(w[qq] << 16) * sc;
+                    const float hi = __uint_as_float(w[qq] & 0xFFFF0000u) * sc;
+                    dst[qq * 8] = pack_f16x2(lo, hi);
+                }
+            }
         }
     }
 }
 
-template <int PD>
-__device__ __forceinline__ void prefetch_ring(const uint8_t *tbase, int c_begin, int c_end, int lane,
-                                              uint4 (&cb)[PD], uint2 (&sb)[PD]) {
-#pragma unroll
-    for (int i = 0; i < PD; ++i)
-        if (c_begin + i < c_end) load_chunk(tbase, c_begin + i, lane, cb[i], sb[i]);
-}
-
 template <int MODE, int GMAX, int PD>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
-                                                        int T, int ksplit) {
+                                                        int T, int ksplit, __nv_bfloat16 *__restrict__ out) {
     extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ const uint4 *s_src[kMaxRows];
+    __shared__ float s_scale[kMaxRows];
+    __shared__ float s_unscale[kMaxRows];
+    __shared__ int s_last;
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int s = blockIdx.y;
@@ -117,62 +117,87 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     const int tl = warp / ksplit, ks = warp - tl * ksplit;
     const int r = blockIdx.x * tpc + tl;
     const bool shared = s < d.S;
+    const uint64_t pol = evict_first_policy();
 
-    int m = 0, p0 = 0, NT = 0, NC = 0;
+    int m = 0, p0 = 0, NT = 0, NC = 0, ns = 0;
     float gsa = 0.f, gsb = 0.f;
     const uint8_t *wbase = nullptr;
     uint4 cb[PD];
     uint2 sb[PD];
 
-    if (shared) {
-        // The shared experts do not depend on routing: start streaming them
-        // before waiting for the router.
-        m = T;
-        p0 = s * T;
+    MOE_TRACE_POINT(1 + MODE, 0);
+    auto slot_geometry = [&](int e) {
         if (MODE == 0) {
-            NT = d.Is / 8;
+            NT = (e < 0 ? d.Is : d.I) / 8;
             NC = d.H / kChunkK;
-            gsa = d.sgs13[2 * s];
-            gsb = d.sgs13[2 * s + 1];
-            wbase = d.sw13r + (size_t)s * d.s13_stride;
+            if (e < 0) {
+                const int si = -e - 1;
+                gsa = d.sgs13[2 * si];
+                gsb = d.sgs13[2 * si + 1];
+                wbase = d.sw13r + (size_t)si * d.s13_stride;
+            } else {
+                gsa = d.gs13[2 * e];
+                gsb = d.gs13[2 * e + 1];
+                wbase = d.w13r + (size_t)e * d.e13_stride;
+            }
         } else {
             NT = d.H / 16;
-            NC = d.Is / kChunkK;
-            gsa = d.sgs2[s];
-            wbase = d.sw2r + (size_t)s * d.s2_stride;
+            NC = (e < 0 ? d.Is : d.I) / kChunkK;
+            if (e < 0) {
+                const int si = -e - 1;
+                gsa = d.sgs2[si];
+                wbase = d.sw2r + (size_t)si * d.s2_stride;
+            } else {
+                gsa = d.gs2[e];
+                wbase = d.w2r + (size_t)e * d.e2_stride;
+            }
         }
-        if (r < NT)
-            prefetch_ring<PD>(wbase + (size_t)r * NC * kChunkBytes, ks * NC / ksplit,
-                              (ks + 1) * NC / ksplit, lane, cb, sb);
-    }
-    pdl_wait();
-    if (!shared) {
-        const int ns = __ldcg(d.nslots);
+    };
+
+    if (MODE == 0) {
+        if (shared) {
+            // Shared experts do not depend on routing: stream them now.
+            m = T;
+            p0 = s * T;
+            slot_geometry(-(s + 1));
+            if (r < NT)
+                prefetch_ring<PD>(wbase + (size_t)r * NC * kChunkBytes, ks * NC / ksplit,
+                                  (ks + 1) * NC / ksplit, lane, cb, sb, pol);
+        }
+        pdl_wait();
+        if (!shared) {
+            ns = __ldcg(d.nslots);
+            if (s >= ns) {
+                pdl_trigger();
+                return;
+            }
+            m = __ldcg(d.slot_m + s);
+            p0 = __ldcg(d.slot_p0 + s);
+            slot_geometry(__ldcg(d.slot_expert + s));
+            if (r < NT)
+                prefetch_ring<PD>(wbase + (size_t)r * NC * kChunkBytes, ks * NC / ksplit,
+                                  (ks + 1) * NC / ksplit, lane, cb, sb, pol);
+        }
+    } else {
+        // The router has completed before this kernel could start: its slot
+        // tables are final.  Stream this slot's weights, then wait for h.
+        ns = __ldcg(d.nslots);
         if (s >= ns) {
+            pdl_wait();
             pdl_trigger();
             return;
         }
-        const int e = __ldcg(d.slot_expert + s);
         m = __ldcg(d.slot_m + s);
         p0 = __ldcg(d.slot_p0 + s);
-        if (MODE == 0) {
-            NT = d.I / 8;
-            NC = d.H / kChunkK;
-            gsa = d.gs13[2 * e];
-            gsb = d.gs13[2 * e + 1];
-            wbase = d.w13r + (size_t)e * d.e13_stride;
-        } else {
-            NT = d.H / 16;
-            NC = d.I / kChunkK;
-            gsa = d.gs2[e];
-            wbase = d.w2r + (size_t)e * d.e2_stride;
-        }
+        slot_geometry(__ldcg(d.slot_expert + s));
         if (r < NT)
             prefetch_ring<PD>(wbase + (size_t)r * NC * kChunkBytes, ks * NC / ksplit,
-                              (ks + 1) * NC / ksplit, lane, cb, sb);
+                              (ks + 1) * NC / ksplit, lane, cb, sb, pol);
+        pdl_wait();
     }
     pdl_trigger();
-    if (blockIdx.x * tpc >= NT) return;   // whole CTA beyond this slot's tiles
+    MOE_TRACE_POINT(1 + MODE, 1);
+    if (blockIdx.x * tpc >= NT) return;   // whole CTA beyond this slot's tiles (gate/up only)
 
     const bool active = r < NT;
     const uint8_t *tbase = wbase + (size_t)(active ? r : 0) * NC * kChunkBytes;
@@ -187,6 +212,27 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     const int row_stride = ncst * 128 + 16;
     float *red = reinterpret_cast<float *>(smem + (size_t)mpad * row_stride);
 
+    // Per-row source pointers and exact power-of-two scales.
+    if (threadIdx.x < m) {
+        const int j = threadIdx.x;
+        int ex;
+        const __nv_bfloat16 *row;
+        if (MODE == 0) {
+            const int tok = shared ? j : __ldcg(d.pair_tok + p0 + j);
+            row = x + (size_t)tok * d.H;
+            ex = __ldcg(d.xexp + tok);
+        } else {
+            row = d.h_ws + (size_t)(p0 + j) * d.Imax;
+            ex = hexp_of(__ldcg(d.hmax + p0 + j));
+        }
+        s_src[j] = reinterpret_cast<const uint4 *>(row);
+        s_scale[j] = pow2f(-ex);
+        s_unscale[j] = pow2f(ex);
+    }
+    // Zero the padding rows once; no stage writes them.
+    for (int i = threadIdx.x; i < (mpad - m) * (row_stride / 16); i += kThreads)
+        reinterpret_cast<uint4 *>(smem + (size_t)m * row_stride)[i] = make_uint4(0u, 0u, 0u, 0u);
+
     float acc[GMAX][4];
 #pragma unroll
     for (int G2 = 0; G2 < GMAX; ++G2)
@@ -195,9 +241,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
 
     for (int st0 = 0; st0 < NC; st0 += ncst) {
         const int st1 = min(NC, st0 + ncst);
-        if (st0 > 0) __syncthreads();
-        stage_rows<MODE>(d, x, shared, m, mpad, p0, st0, st1 - st0, smem, row_stride);
         __syncthreads();
+        stage_rows(m, st0, st1 - st0, smem, row_stride, s_src, s_scale);
+        __syncthreads();
+        MOE_TRACE_POINT(1 + MODE, 2);
         if (active) {
             const int lo = max(st0, c_begin), hi = min(st1, c_end);
             const uint8_t *brow = smem + (size_t)g * row_stride + q * 32;
@@ -222,13 +269,14 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
                             }
                         }
                         const int cn = c + PD;
-                        if (cn < c_end) load_chunk(tbase, cn, lane, cb[i], sb[i]);
+                        if (cn < c_end) load_chunk(tbase, cn, lane, cb[i], sb[i], pol);
                     }
                 }
             }
         }
     }
 
+    MOE_TRACE_POINT(1 + MODE, 3);
     if (ksplit > 1) {
         // Fixed-order K reduction across the warps sharing a tile.
         if (ks > 0) {
@@ -245,9 +293,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
             }
         }
     }
-    if (ks != 0 || !active) return;
+    const bool writer = ks == 0 && active;
+    MOE_TRACE_POINT(1 + MODE, 4);
 
     if (MODE == 0) {
+        if (!writer) return;
         const int n = 8 * r + g;
 #pragma unroll
         for (int G2 = 0; G2 < GMAX; ++G2) {
@@ -258,8 +308,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
                 float habs = 0.f;
                 if (ok) {
                     const int p = p0 + col;
-                    const int tok = shared ? col : __ldcg(d.pair_tok + p);
-                    const float sc = pow2f(__ldcg(d.xexp + tok));
+                    const float sc = s_unscale[col];
                     const float gt = acc[G2][e2] * gsa * sc;
                     const float up = acc[G2][2 + e2] * gsb * sc;
                     const float hv = gt / (1.0f + expf(-gt)) * up;
@@ -273,7 +322,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
                 if (ok && g == 0) atomicMax(d.hmax + p0 + col, __float_as_uint(habs));
             }
         }
-    } else {
+        return;
+    }
+
+    // ---- down: write y, then the last slot CTA of this row group combines ----
+    if (writer) {
 #pragma unroll
         for (int G2 = 0; G2 < GMAX; ++G2) {
 #pragma unroll
@@ -281,7 +334,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
                 const int col = 8 * G2 + 2 * q + e2;
                 if (G2 < G && col < m) {
                     const int p = p0 + col;
-                    const float sc = pow2f(hexp_of(__ldcg(d.hmax + p))) * gsa;
+                    const float sc = s_unscale[col] * gsa;
                     float *yp = d.y_ws + (size_t)p * d.H + 16 * r + g;
                     yp[0] = acc[G2][e2] * sc;
                     yp[8] = acc[G2][2 + e2] * sc;
@@ -289,12 +342,53 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
             }
         }
     }
+    __syncthreads();
+    MOE_TRACE_POINT(2, 5);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(d.down_cnt + blockIdx.x, 1u) == (unsigned)(ns - 1);
+    }
+    __syncthreads();
+    MOE_TRACE_POINT(2, 6);
+    if (!s_last) return;
+    __threadfence();
+
+    const int K = d.k, P = d.k + d.S;
+    int *s_pair = reinterpret_cast<int *>(smem);                       // [T, P]
+    float *s_pw = reinterpret_cast<float *>(smem + (size_t)kMaxTokens * 16 * sizeof(int));
+    for (int i = threadIdx.x; i < T * P; i += kThreads) {
+        const int p = __ldcg(d.pair_of + i);
+        s_pair[i] = p;
+        s_pw[i] = (i % P) < K ? __ldcg(d.pair_w + p) : 1.0f;
+    }
+    __syncthreads();
+    const int row0 = blockIdx.x * tpc * 16;
+    const int nq = (min(d.H, row0 + tpc * 16) - row0) / 4;
+    for (int it = threadIdx.x; it < T * nq; it += kThreads) {
+        const int t = it / nq, m4 = row0 / 4 + (it - t * nq);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < P; ++j) {
+            const float w = s_pw[t * P + j];
+            const float4 y = __ldcg(reinterpret_cast<const float4 *>(d.y_ws + (size_t)s_pair[t * P + j] * d.H) + m4);
+            a.x = fmaf(w, y.x, a.x);
+            a.y = fmaf(w, y.y, a.y);
+            a.z = fmaf(w, y.z, a.z);
+            a.w = fmaf(w, y.w, a.w);
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t *>(&lo);
+        v.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(out + (size_t)t * d.H + 4 * m4) = v;
+    }
+    if (threadIdx.x == 0) d.down_cnt[blockIdx.x] = 0u;
+    MOE_TRACE_POINT(2, 7);
 }
 
 template <int MODE, int GMAX, int PD>
 cudaError_t launch_one(const DevLayer &d, const __nv_bfloat16 *x, int T, int ksplit, dim3 grid,
-                       size_t smem, cudaStream_t s) {
-    auto fn = gemv_kernel<MODE, GMAX, PD>;
+                       size_t smem, __nv_bfloat16 *out, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -305,36 +399,43 @@ cudaError_t launch_one(const DevLayer &d, const __nv_bfloat16 *x, int T, int ksp
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, d, x, T, ksplit);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MODE, GMAX, PD>, d, x, T, ksplit, out);
 }
 
 template <int MODE>
-cudaError_t launch_stage(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s) {
+cudaError_t launch_stage(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out,
+                         cudaStream_t s) {
     const int slots = min(d.E, T * d.k) + d.S;
     const int Iall = d.S > 0 ? max(d.I, d.Is) : d.I;
     const int Imin = d.S > 0 ? min(d.I, d.Is) : d.I;
     const int NT = MODE == 0 ? Iall / 8 : d.H / 16;
     const int NCmax = MODE == 0 ? d.H / kChunkK : Iall / kChunkK;
     const int NCmin = MODE == 0 ? d.H / kChunkK : Imin / kChunkK;
+    // the combine (down) needs room for the [T, k+S] pair table
+    const size_t combine_smem = (size_t)kMaxTokens * 16 * (sizeof(int) + sizeof(float));
     if (T <= 8) {
-        long tiles = (long)slots * NT;
+        const long tiles = (long)slots * NT;
         int ksplit = 1;
         while (ksplit < 4 && tiles * ksplit < 2048 && NCmin >= 4 * ksplit) ksplit *= 2;
         const int tpc = kGemvWarps / ksplit;
         dim3 grid((NT + tpc - 1) / tpc, slots);
         size_t smem = (size_t)8 * (NCmax * 128 + 16) + (size_t)tpc * (ksplit - 1) * 4 * 32 * sizeof(float);
-        return launch_one<MODE, 1, 8>(d, x, T, ksplit, grid, smem, s);
+        if (MODE == 1 && smem < combine_smem) smem = combine_smem;
+        return launch_one<MODE, 1, 8>(d, x, T, ksplit, grid, smem, out, s);
     }
     dim3 grid((NT + kGemvWarps - 1) / kGemvWarps, slots);
-    return launch_one<MODE, 8, 4>(d, x, T, 1, grid, (size_t)kStageBudget, s);
+    return launch_one<MODE, 8, 4>(d, x, T, 1, grid, (size_t)kStageBudget, out, s);
 }
 
 template <int MODE, int GMAX, int PD>
-cudaError_t allow_smem(int bytes) {
-    return cudaFuncSetAttribute(gemv_kernel<MODE, GMAX, PD>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+cudaError_t allow_smem(int optin) {
+    return allow_max_dynamic_smem(gemv_kernel<MODE, GMAX, PD>, optin);
 }
 
 }  // namespace
+
+cudaError_t prepare_route_kernel(int optin_bytes);
+cudaError_t prepare_fused_kernel(int optin_bytes);
 
 cudaError_t prepare_kernels() {
     int dev = 0, optin = 0;
@@ -344,18 +445,17 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = allow_smem<1, 1, 8>(optin);
     if (e == cudaSuccess) e = allow_smem<0, 8, 4>(optin);
     if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
+    if (e == cudaSuccess) e = prepare_route_kernel(optin);
+    if (e == cudaSuccess) e = prepare_fused_kernel(optin);
     return e;
 }
 
-cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count,
-                           cudaStream_t s) {
-    (void)sm_count;
-    return launch_stage<0>(d, x, T, s);
+cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s) {
+    return launch_stage<0>(d, x, T, nullptr, s);
 }
 
-cudaError_t launch_down(const DevLayer &d, int T, int sm_count, cudaStream_t s) {
-    (void)sm_count;
-    return launch_stage<1>(d, nullptr, T, s);
+cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s) {
+    return launch_stage<1>(d, nullptr, T, out, s);
 }
 
 }  // namespace moe

@@ -48,7 +48,7 @@ constexpr int kMaxTokens = 64;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxShared = 2;
-constexpr int kRouteWarps = 4;     // experts per router CTA
+constexpr int kRouteWarps = 8;     // experts per router CTA
 
 // Everything a kernel needs to know about a layer (passed by value).
 struct DevLayer {
@@ -83,23 +83,42 @@ struct DevLayer {
     __nv_bfloat16 *h_ws;            // [max_pairs, Imax]
     float *y_ws;                    // [max_pairs, H]
     unsigned *ticket;               // [1]
+    unsigned *down_cnt;             // [H/16] arrivals per down row group
     int *err;                       // [1] sticky device error word
+    unsigned long long *hmax64;     // [max_pairs] single-launch path: (epoch << 32) | max|h| bits
+    unsigned *epoch;                // [1] call counter of the single-launch path
+    unsigned *bar_count;            // [1] grid barrier arrivals
+    unsigned *bar_gen;              // [1] grid barrier generation
+    unsigned long long *trace;      // traced build only: phase timestamps
+    int trace_blocks;
 };
 
 // ---------------------------------------------------------------------------
 // Host-side launchers (defined in the .cu files).
 // ---------------------------------------------------------------------------
-cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s);
-cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count,
-                           cudaStream_t s);
-cudaError_t launch_down(const DevLayer &d, int T, int sm_count, cudaStream_t s);
-cudaError_t launch_combine(const DevLayer &d, int T, __nv_bfloat16 *out, int *ids, float *w,
-                           cudaStream_t s);
+cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out,
+                         float *w_out, cudaStream_t s);
+cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s);
+cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s);
 cudaError_t prepare_kernels();   // per device, once: shared-memory limits
+bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem);
+cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
+                         float *w, int sm_count, cudaStream_t s);
+int fused_blocks_per_sm(const DevLayer &d, int T);
 cudaError_t launch_repack(const uint8_t *codes, const uint8_t *sf, int n_mats, int rows, int cols,
                           bool gate_up, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t *rep, float gs_a, float gs_b, int rows, int cols,
                            bool gate_up, float *dst, cudaStream_t s);
+
+// Let `fn` use all the shared memory a block may opt in to, minus its static part.
+template <class F>
+inline cudaError_t allow_max_dynamic_smem(F fn, int optin_bytes) {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, fn);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin_bytes - (int)a.sharedSizeBytes);
+}
 
 // Chunk geometry.
 __host__ __device__ inline size_t repacked_bytes(int rows, int cols) {
@@ -111,6 +130,26 @@ __host__ __device__ inline size_t repacked_bytes(int rows, int cols) {
 // ---------------------------------------------------------------------------
 #if defined(__CUDACC__)
 
+// Phase tracing, compiled only into the traced build (-DMOE_TRACE): thread 0
+// of each block stores %globaltimer at numbered points into the buffer that
+// moe_trace_attach() installed in DevLayer ([kernel][block][16] u64).  In the
+// regular build every trace point is empty.
+#ifdef MOE_TRACE
+#define MOE_TRACE_POINT(kid, i)                                                                  \
+    do {                                                                                         \
+        if (threadIdx.x == 0 && d.trace) {                                                       \
+            unsigned long long t_;                                                               \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                               \
+            const int b_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
+            if (b_ < d.trace_blocks) d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = t_; \
+        }                                                                                        \
+    } while (0)
+#else
+#define MOE_TRACE_POINT(kid, i) \
+    do {                        \
+    } while (0)
+#endif
+
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
@@ -118,17 +157,24 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-// Streaming loads of weights: read-only, not kept in L1.
-__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+// Streaming loads of weights: read-only, not kept in L1, and first in line
+// for eviction from L2 (the weights are read once per call; code, activations
+// and the workspace should stay in L2 instead).
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p, uint64_t pol) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p), "l"(pol));
     return r;
 }
-__device__ __forceinline__ uint2 ld_stream_v2(const void *p) {
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p, uint64_t pol) {
     uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n"
-                 : "=r"(r.x), "=r"(r.y) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;\n"
+                 : "=r"(r.x), "=r"(r.y) : "l"(p), "l"(pol));
     return r;
 }
 __device__ __forceinline__ float4 ld_f4(const float *p) {
@@ -177,6 +223,42 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
     return r;
+}
+
+// Loads that must be issued where they stand (e.g. before a
+// griddepcontrol.wait): volatile asm keeps the compiler from sinking them.
+__device__ __forceinline__ float2 ld_nc_f2(const float *p) {
+    float2 r;
+    asm volatile("ld.global.nc.v2.f32 {%0,%1}, [%2];\n" : "=f"(r.x), "=f"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int exp_for_f16(float maxabs) {
+    // power of two 2^e such that maxabs * 2^-e < 2^15 (and >= 2^14 when
+    // maxabs > 0): f16 then holds every BF16 value of the row exactly except
+    // those below maxabs * 2^-32.
+    return (maxabs > 0.f && isfinite(maxabs)) ? ilogbf(maxabs) - 14 : 0;
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// One 576-byte chunk for one lane: 16 code bytes and the 8 scale bytes of its
+// row group.
+__device__ __forceinline__ void load_chunk(const uint8_t *tbase, int c, int lane, uint4 &cw,
+                                           uint2 &sw, uint64_t pol) {
+    const uint8_t *ch = tbase + (size_t)c * kChunkBytes;
+    cw = ld_stream_v4(ch + 16 * lane, pol);
+    sw = ld_stream_v2(ch + kCodeBytes + 8 * (lane >> 2), pol);
 }
 
 // Decode one chunk's A fragments for one lane: 4 blocks x 4 registers.

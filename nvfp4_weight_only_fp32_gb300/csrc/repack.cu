@@ -59,9 +59,10 @@ __global__ void dequant_kernel(const uint8_t *__restrict__ rep, float gs_a, floa
     if (warp >= NT * NC) return;
     const int r = warp / NC, c = warp % NC;
     const uint8_t *chunk = rep + (size_t)warp * kChunkBytes;
-    uint4 cw = ld_stream_v4(chunk + 16 * lane);
+    const uint64_t pol = evict_first_policy();
+    uint4 cw = ld_stream_v4(chunk + 16 * lane, pol);
     const int g = lane >> 2, q = lane & 3;
-    uint2 sw = ld_stream_v2(chunk + kCodeBytes + 8 * g);
+    uint2 sw = ld_stream_v2(chunk + kCodeBytes + 8 * g, pol);
     uint32_t a[4][4];
     decode_chunk(cw, sw, a);
 #pragma unroll

@@ -10,13 +10,14 @@
 // strategy" (the expert GEMVs read only the selected experts, which is what the
 // work list built here enables).
 //
-// One launch.  Each warp computes one expert's logits for every token (the
-// router row is streamed once with 16-byte loads; the first part is fetched
-// before the programmatic-launch wait because router weights do not depend on
-// the previous kernel).  The CTA that finishes last (atomic ticket, no
-// spinning) then runs sigmoid/top-k per token (one warp per token), counts the
-// tokens per expert with 64-bit token masks, scans them into slots (shared
-// experts first, then routed experts in ascending id) and numbers the
+// One launch of E/8 blocks.  Each warp owns one expert: its router row is
+// fetched into registers BEFORE the programmatic-launch wait (router weights
+// do not depend on the previous kernel), the tokens' activations are staged in
+// shared memory once per block, and the warp writes the FP32 logits of every
+// token.  The block that finishes last (atomic ticket, no spinning) loads all
+// logits into shared memory, runs sigmoid/top-k per token (one warp per token),
+// counts the tokens per expert with 64-bit token masks, scans them into slots
+// (shared experts first, then routed experts in ascending id) and numbers the
 // (expert, token) pairs so that each expert's pairs are contiguous.
 #include "moe_internal.cuh"
 
@@ -35,14 +36,13 @@ __device__ __forceinline__ void bf16x4_to_f(uint2 v, float &a, float &b, float &
     e = __uint_as_float(v.y & 0xFFFF0000u);
 }
 
-__device__ __forceinline__ void dot4_tokens(const float4 &w, const __nv_bfloat16 *__restrict__ x,
-                                            int H, int t0, int nt, int v, float (&acc)[kTokGroup]) {
+__device__ __forceinline__ void dot4(const float4 &w, const uint2 *__restrict__ xs, int H4, int nt, int v,
+                                     float (&acc)[kTokGroup]) {
 #pragma unroll
     for (int t = 0; t < kTokGroup; ++t) {
         if (t < nt) {
-            uint2 xb = __ldcg(reinterpret_cast<const uint2 *>(x + (size_t)(t0 + t) * H + 4 * v));
             float x0, x1, x2, x3;
-            bf16x4_to_f(xb, x0, x1, x2, x3);
+            bf16x4_to_f(xs[t * H4 + v], x0, x1, x2, x3);
             acc[t] = fmaf(x0, w.x, acc[t]);
             acc[t] = fmaf(x1, w.y, acc[t]);
             acc[t] = fmaf(x2, w.z, acc[t]);
@@ -55,56 +55,130 @@ __device__ __forceinline__ bool better(float s, int e, float bs, int be) {
     return s > bs || (s == bs && e < be);
 }
 
-__global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
-                                                         const __nv_bfloat16 *__restrict__ x, int T) {
+__global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
+                                                         int T, int tg, int *__restrict__ ids_out,
+                                                         float *__restrict__ w_out) {
+    extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = d.H, E = d.E, K = d.k, S = d.S;
     const int e = blockIdx.x * kRouteWarps + warp;
     const int nvec = H / 4;
     const float *wr = d.router_w + (size_t)(e < E ? e : 0) * H;
 
+    MOE_TRACE_POINT(0, 0);
     float4 pre[kPre];
 #pragma unroll
     for (int j = 0; j < kPre; ++j) {
-        int v = lane + 32 * j;
-        pre[j] = (e < E && v < nvec) ? ld_f4(wr + 4 * v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int v = lane + 32 * j;
+        if (e < E && v < nvec) {
+            // volatile loads: issued here, before the wait, not sunk past it
+            const float2 lo = ld_nc_f2(wr + 4 * v), hi = ld_nc_f2(wr + 4 * v + 2);
+            pre[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        } else {
+            pre[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     pdl_wait();
     pdl_trigger();
+    MOE_TRACE_POINT(0, 1);
 
-    if (e < E) {
-        const float bias = d.router_b ? d.router_b[e] : 0.f;
-        for (int t0 = 0; t0 < T; t0 += kTokGroup) {
-            const int nt = min(kTokGroup, T - t0);
-            float acc[kTokGroup];
+    __shared__ float s_rmax[kTokGroup];
+    uint2 *xs = reinterpret_cast<uint2 *>(smem);          // [tg][H/4] groups of 4 bf16
+    const float bias = (e < E && d.router_b) ? d.router_b[e] : 0.f;
+    for (int t0 = 0; t0 < T; t0 += tg) {
+        const int nt = min(tg, T - t0);
+        if (t0 > 0) __syncthreads();
+        if (threadIdx.x < kTokGroup) s_rmax[threadIdx.x] = 0.f;
+        // stage the group's activation rows (16-byte loads)
+        const int n16 = nt * H / 8;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t0 * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem);
+        __syncthreads();
+        for (int base = threadIdx.x; base < n16; base += 4 * kThreads) {
+            uint4 v[4];
 #pragma unroll
-            for (int t = 0; t < kTokGroup; ++t) acc[t] = 0.f;
+            for (int u = 0; u < 4; ++u)
+                if (base + u * kThreads < n16) v[u] = __ldcg(src + base + u * kThreads);
 #pragma unroll
-            for (int j = 0; j < kPre; ++j) {
-                int v = lane + 32 * j;
-                if (v < nvec) dot4_tokens(pre[j], x, H, t0, nt, v, acc);
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * kThreads;
+                if (i < n16) dst[i] = v[u];
+                if (blockIdx.x == 0) {
+                    // per-token max |x| for the GEMVs' power-of-two prescale
+                    float m = 0.f;
+                    if (i < n16) {
+                        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
+                                               fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
+                    }
+                    if ((H & 255) == 0) {
+                        // a row is a multiple of 32 items and a warp's items are
+                        // contiguous: the warp lies in one row, reduce it first
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                        const int i0 = i - lane;
+                        if (lane == 0 && i0 < n16)
+                            atomicMax(reinterpret_cast<int *>(&s_rmax[i0 / (H / 8)]), __float_as_int(m));
+                    } else if (i < n16) {
+                        atomicMax(reinterpret_cast<int *>(&s_rmax[i / (H / 8)]), __float_as_int(m));
+                    }
+                }
             }
-            for (int v = lane + 32 * kPre; v < nvec; v += 32)
-                dot4_tokens(ld_f4(wr + 4 * v), x, H, t0, nt, v, acc);
+        }
+        __syncthreads();
+        MOE_TRACE_POINT(0, 2);
+        if (blockIdx.x == 0 && threadIdx.x < nt) {
+            const float mx = s_rmax[threadIdx.x];
+            d.xexp[t0 + threadIdx.x] = (mx > 0.f && isfinite(mx)) ? max(0, ilogbf(mx) - 14) : 0;
+        }
+        if (e < E) {
+            const int H4 = nvec;
+#pragma unroll 1
+            for (int t = 0; t < nt; ++t) {
+                const uint2 *xr = xs + t * H4;
+                float a = 0.f;
 #pragma unroll
-            for (int t = 0; t < kTokGroup; ++t) {
-                float a = acc[t];
+                for (int j = 0; j < kPre; ++j) {
+                    const int v = lane + 32 * j;
+                    if (v < nvec) {
+                        float x0, x1, x2, x3;
+                        bf16x4_to_f(xr[v], x0, x1, x2, x3);
+                        a = fmaf(x0, pre[j].x, a);
+                        a = fmaf(x1, pre[j].y, a);
+                        a = fmaf(x2, pre[j].z, a);
+                        a = fmaf(x3, pre[j].w, a);
+                    }
+                }
+                for (int v = lane + 32 * kPre; v < nvec; v += 32) {
+                    const float4 w = ld_f4(wr + 4 * v);
+                    float x0, x1, x2, x3;
+                    bf16x4_to_f(xr[v], x0, x1, x2, x3);
+                    a = fmaf(x0, w.x, a);
+                    a = fmaf(x1, w.y, a);
+                    a = fmaf(x2, w.z, a);
+                    a = fmaf(x3, w.w, a);
+                }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-                if (lane == 0 && t < nt) d.logits[(size_t)(t0 + t) * E + e] = a + bias;
+                if (lane == 0) d.logits[(size_t)(t0 + t) * E + e] = a + bias;
             }
         }
     }
 
-    // ---- last CTA to finish builds the routing result and the work list ----
+    // ---- the block that finishes last builds the routing result ----
     __shared__ int s_last;
     __syncthreads();
+    MOE_TRACE_POINT(0, 3);
     if (threadIdx.x == 0) {
         __threadfence();
         unsigned tk = atomicAdd(d.ticket, 1u);
         s_last = (tk == gridDim.x - 1);
     }
     __syncthreads();
+    MOE_TRACE_POINT(0, 4);
     if (!s_last) return;
     __threadfence();
 
@@ -114,18 +188,29 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
     __shared__ int s_pbase[kMaxExperts];
     __shared__ int s_wsum_f[kRouteWarps], s_wsum_c[kRouteWarps];
 
+    float *s_logit = reinterpret_cast<float *>(smem);     // [T, E], reuses the staging area
+    for (int base = threadIdx.x; base < T * E; base += 4 * kThreads) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (base + u * kThreads < T * E) v[u] = __ldcg(d.logits + base + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (base + u * kThreads < T * E) s_logit[base + u * kThreads] = v[u];
+    }
     for (int i = threadIdx.x; i < E; i += kThreads) s_mask[i] = 0ull;
     __syncthreads();
+    MOE_TRACE_POINT(0, 5);
 
     // a2: sigmoid + top-k + weights, one warp per token.
     for (int t = warp; t < T; t += kRouteWarps) {
         float sc[kMaxExperts / 32];
 #pragma unroll
         for (int m = 0; m < kMaxExperts / 32; ++m) {
-            int ee = lane + 32 * m;
+            const int ee = lane + 32 * m;
             float s = -INFINITY;
             if (ee < E) {
-                float z = __ldcg(d.logits + (size_t)t * E + ee);
+                const float z = s_logit[t * E + ee];
                 s = isnan(z) ? -INFINITY : 1.0f / (1.0f + expf(-z));
             }
             sc[m] = s;
@@ -133,12 +218,13 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
         unsigned taken = 0u;
         float sel_s = 0.f;
         int sel_e = 0;
+#pragma unroll 1
         for (int j = 0; j < K; ++j) {
             float bs = -INFINITY;
             int be = 0x7fffffff;
 #pragma unroll
             for (int m = 0; m < kMaxExperts / 32; ++m) {
-                int ee = lane + 32 * m;
+                const int ee = lane + 32 * m;
                 if (ee < E && !(taken & (1u << m)) && better(sc[m], ee, bs, be)) {
                     bs = sc[m];
                     be = ee;
@@ -146,8 +232,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
-                float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
                 if (better(os, oe, bs, be)) {
                     bs = os;
                     be = oe;
@@ -169,20 +255,23 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
             s_w[t][lane] = w;
             d.ids[(size_t)t * K + lane] = sel_e;
             d.wsel[(size_t)t * K + lane] = w;
+            if (ids_out) ids_out[(size_t)t * K + lane] = sel_e;
+            if (w_out) w_out[(size_t)t * K + lane] = w;
             atomicOr(&s_mask[sel_e], 1ull << t);
         }
     }
     __syncthreads();
 
+    MOE_TRACE_POINT(0, 6);
     // Slots: shared experts first, then routed experts with >= 1 token in
     // ascending id.  Exclusive scans of (used?, token count) over experts.
     const int per = (E + kThreads - 1) / kThreads;
     const int e0 = threadIdx.x * per;
     int fsum = 0, csum = 0;
     for (int i = 0; i < per; ++i) {
-        int ee = e0 + i;
+        const int ee = e0 + i;
         if (ee < E) {
-            int c = __popcll(s_mask[ee]);
+            const int c = __popcll(s_mask[ee]);
             fsum += c > 0;
             csum += c;
         }
@@ -190,8 +279,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
     int finc = fsum, cinc = csum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        int a = __shfl_up_sync(0xffffffffu, finc, off);
-        int b = __shfl_up_sync(0xffffffffu, cinc, off);
+        const int a = __shfl_up_sync(0xffffffffu, finc, off);
+        const int b = __shfl_up_sync(0xffffffffu, cinc, off);
         if (lane >= off) {
             finc += a;
             cinc += b;
@@ -208,12 +297,12 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
         cbase += s_wsum_c[w];
     }
     for (int i = 0; i < per; ++i) {
-        int ee = e0 + i;
+        const int ee = e0 + i;
         if (ee < E) {
-            int c = __popcll(s_mask[ee]);
+            const int c = __popcll(s_mask[ee]);
             if (c > 0) {
-                int slot = S + fbase;
-                int p0 = S * T + cbase;
+                const int slot = S + fbase;
+                const int p0 = S * T + cbase;
                 d.slot_expert[slot] = ee;
                 d.slot_m[slot] = c;
                 d.slot_p0[slot] = p0;
@@ -234,58 +323,57 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d,
     // Pairs: an expert's tokens are numbered in ascending token order.
     const int P = K + S;
     for (int it = threadIdx.x; it < T * K; it += kThreads) {
-        int t = it / K, j = it % K;
-        int ee = s_ids[t][j];
-        unsigned long long below = (t == 0) ? 0ull : (s_mask[ee] & ((1ull << t) - 1ull));
-        int p = s_pbase[ee] + __popcll(below);
+        const int t = it / K, j = it % K;
+        const int ee = s_ids[t][j];
+        const unsigned long long below = (t == 0) ? 0ull : (s_mask[ee] & ((1ull << t) - 1ull));
+        const int p = s_pbase[ee] + __popcll(below);
         d.pair_tok[p] = t;
         d.pair_w[p] = s_w[t][j];
         d.pair_of[t * P + j] = p;
     }
     for (int it = threadIdx.x; it < T * S; it += kThreads) {
-        int sidx = it / T, t = it % T;
-        int p = sidx * T + t;
+        const int sidx = it / T, t = it % T;
+        const int p = sidx * T + t;
         d.pair_tok[p] = t;
         d.pair_w[p] = 1.0f;
         d.pair_of[t * P + K + sidx] = p;
     }
     for (int p = threadIdx.x; p < T * P; p += kThreads) d.hmax[p] = 0u;
-
-    // Power-of-two prescale of each activation row so that it fits the f16
-    // operands of the expert GEMVs exactly: max|x| * 2^-xexp < 2^15.
-    for (int t = warp; t < T; t += kRouteWarps) {
-        float mx = 0.f;
-        for (int v = lane; v < nvec; v += 32) {
-            uint2 xb = __ldcg(reinterpret_cast<const uint2 *>(x + (size_t)t * H + 4 * v));
-            float a, b, c, f;
-            bf16x4_to_f(xb, a, b, c, f);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a), fabsf(b)), fmaxf(fabsf(c), fabsf(f))));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (lane == 0) {
-            int ex = 0;
-            if (mx > 0.f && isfinite(mx)) ex = max(0, ilogbf(mx) - 14);
-            d.xexp[t] = ex;
-        }
-    }
     if (threadIdx.x == 0) *d.ticket = 0u;
+    MOE_TRACE_POINT(0, 7);
 }
 
 }  // namespace
 
-cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s) {
+size_t route_smem_bytes(const DevLayer &d, int T, int *tg_out) {
+    // staging of up to 8 activation rows, reused for the [T, E] logits
+    int tg = kTokGroup;
+    while (tg > 1 && (size_t)tg * d.H * 2 > 96 * 1024) --tg;
+    if (tg > T) tg = T;
+    if (tg_out) *tg_out = tg;
+    size_t a = (size_t)tg * d.H * 2, b = (size_t)T * d.E * 4;
+    return a > b ? a : b;
+}
+
+cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out, float *w_out,
+                         cudaStream_t s) {
+    int tg = 1;
+    const size_t smem = route_smem_bytes(d, T, &tg);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((d.E + kRouteWarps - 1) / kRouteWarps);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, route_kernel, d, x, T);
+    return cudaLaunchKernelEx(&cfg, route_kernel, d, x, T, tg, ids_out, w_out);
+}
+
+cudaError_t prepare_route_kernel(int optin_bytes) {
+    return allow_max_dynamic_smem(route_kernel, optin_bytes);
 }
 
 }  // namespace moe

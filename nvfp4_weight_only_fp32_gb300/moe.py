@@ -26,9 +26,9 @@ MOE_ERR_DEVICE = -6
 
 EXPORTED = [
     "moe_init", "moe_destroy", "moe_decode_forward", "moe_decode_forward_host",
-    "moe_stage_route", "moe_stage_gate_up", "moe_stage_down", "moe_stage_combine",
+    "moe_stage_route", "moe_stage_gate_up", "moe_stage_down",
     "moe_check", "moe_debug_dequant", "moe_get_info", "moe_last_error",
-    "moe_route_topk_static",
+    "moe_route_topk_static", "moe_trace_attach",
 ]
 
 
@@ -36,7 +36,8 @@ class moe_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("num_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("inter", ctypes.c_int), ("num_shared", ctypes.c_int), ("shared_inter", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("normalize_topk", ctypes.c_int),
-                ("routed_scale", ctypes.c_float), ("grouped_min_tokens", ctypes.c_int)]
+                ("routed_scale", ctypes.c_float), ("grouped_min_tokens", ctypes.c_int),
+                ("fused", ctypes.c_int)]
 
 
 class moe_weights(ctypes.Structure):
@@ -48,7 +49,8 @@ class moe_weights(ctypes.Structure):
 class moe_layer_info(ctypes.Structure):
     _fields_ = [("weight_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
                 ("expert_bytes", ctypes.c_size_t), ("shared_bytes", ctypes.c_size_t),
-                ("max_slots", ctypes.c_int), ("sm_count", ctypes.c_int)]
+                ("max_slots", ctypes.c_int), ("sm_count", ctypes.c_int),
+                ("single_launch_max_tokens", ctypes.c_int)]
 
 
 class MoEError(RuntimeError):
@@ -62,11 +64,12 @@ _lib = None
 
 
 def lib(path: str | None = None):
-    """Load the CUDA library (raises if it is missing)."""
+    """Load the CUDA library (raises if it is missing).  MOE_LIBRARY may name
+    another build of it (e.g. the traced build)."""
     global _lib
     with _lock:
         if _lib is None:
-            p = path or LIB_PATH
+            p = path or os.environ.get("MOE_LIBRARY") or LIB_PATH
             if not os.path.exists(p):
                 raise RuntimeError(
                     f"{p} is missing: build it with nvfp4_weight_only_fp32_gb300.build.build()")
@@ -81,14 +84,12 @@ def lib(path: str | None = None):
             L.moe_decode_forward.restype = st
             L.moe_decode_forward_host.argtypes = [vp, vp, i, vp, vp, vp, vp]
             L.moe_decode_forward_host.restype = st
-            L.moe_stage_route.argtypes = [vp, vp, i, vp]
+            L.moe_stage_route.argtypes = [vp, vp, i, vp, vp, vp]
             L.moe_stage_route.restype = st
             L.moe_stage_gate_up.argtypes = [vp, vp, i, vp]
             L.moe_stage_gate_up.restype = st
-            L.moe_stage_down.argtypes = [vp, i, vp]
+            L.moe_stage_down.argtypes = [vp, i, vp, vp]
             L.moe_stage_down.restype = st
-            L.moe_stage_combine.argtypes = [vp, i, vp, vp, vp, vp]
-            L.moe_stage_combine.restype = st
             L.moe_check.argtypes = [vp, vp]
             L.moe_check.restype = st
             L.moe_debug_dequant.argtypes = [vp, i, i, vp, vp]
@@ -97,6 +98,8 @@ def lib(path: str | None = None):
             L.moe_get_info.restype = st
             L.moe_route_topk_static.argtypes = [vp, vp, i, i, i, i, ctypes.c_float, vp, i, vp, vp, vp]
             L.moe_route_topk_static.restype = st
+            L.moe_trace_attach.argtypes = [vp, vp, i]
+            L.moe_trace_attach.restype = st
             L.moe_last_error.argtypes = []
             L.moe_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -145,21 +148,17 @@ def moe_decode_forward_host(h, x_host, T, out_host, ids_host=None, w_host=None, 
                                          _p(w_host), ctypes.c_void_p(_stream(stream))))
 
 
-def moe_stage_route(h, x, T, stream=None) -> None:
-    _check(lib().moe_stage_route(h, _p(x), int(T), ctypes.c_void_p(_stream(stream))))
+def moe_stage_route(h, x, T, topk_ids=None, topk_w=None, stream=None) -> None:
+    _check(lib().moe_stage_route(h, _p(x), int(T), _p(topk_ids), _p(topk_w),
+                                 ctypes.c_void_p(_stream(stream))))
 
 
 def moe_stage_gate_up(h, x, T, stream=None) -> None:
     _check(lib().moe_stage_gate_up(h, _p(x), int(T), ctypes.c_void_p(_stream(stream))))
 
 
-def moe_stage_down(h, T, stream=None) -> None:
-    _check(lib().moe_stage_down(h, int(T), ctypes.c_void_p(_stream(stream))))
-
-
-def moe_stage_combine(h, T, out, topk_ids=None, topk_w=None, stream=None) -> None:
-    _check(lib().moe_stage_combine(h, int(T), _p(out), _p(topk_ids), _p(topk_w),
-                                   ctypes.c_void_p(_stream(stream))))
+def moe_stage_down(h, T, out, stream=None) -> None:
+    _check(lib().moe_stage_down(h, int(T), _p(out), ctypes.c_void_p(_stream(stream))))
 
 
 def moe_check(h, stream=None) -> int:
@@ -175,6 +174,10 @@ def moe_get_info(h) -> moe_layer_info:
     info = moe_layer_info()
     _check(lib().moe_get_info(h, ctypes.byref(info)))
     return info
+
+
+def moe_trace_attach(h, buf, blocks_per_kernel) -> None:
+    _check(lib().moe_trace_attach(h, _p(buf), int(blocks_per_kernel)))
 
 
 def moe_route_topk_static(router_w, router_b, num_experts, hidden, top_k, normalize_topk,
@@ -207,13 +210,14 @@ def to_device(layer: dict, device="cuda") -> dict:
     return out
 
 
-def make_config(c: dict, max_tokens: int | None = None, grouped_min_tokens: int = 0) -> moe_config:
+def make_config(c: dict, max_tokens: int | None = None, grouped_min_tokens: int = 0,
+                fused: int = 0) -> moe_config:
     return moe_config(hidden=c["H"], num_experts=c["E"], top_k=c["k"], inter=c["I"],
                       num_shared=c["S"], shared_inter=c["Is"],
                       max_tokens=int(max_tokens if max_tokens else c["T"]),
                       normalize_topk=int(c.get("normalize", 1)),
                       routed_scale=float(c.get("routed_scale", 1.0)),
-                      grouped_min_tokens=int(grouped_min_tokens))
+                      grouped_min_tokens=int(grouped_min_tokens), fused=int(fused))
 
 
 class MoELayer:
@@ -224,13 +228,13 @@ class MoELayer:
     the inputs may be freed afterwards."""
 
     def __init__(self, layer: dict, max_tokens: int | None = None, grouped_min_tokens: int = 0,
-                 stream=None):
+                 stream=None, fused: int = 0):
         c = layer["cfg"]
         self.cfg = dict(c)
         self.max_tokens = int(max_tokens if max_tokens else c["T"])
         dev = to_device(layer)
         w = moe_weights(**{n: (None if t is None else t.data_ptr()) for n, t in dev.items()})
-        self._cfg = make_config(c, self.max_tokens, grouped_min_tokens)
+        self._cfg = make_config(c, self.max_tokens, grouped_min_tokens, fused)
         self.h = moe_init(self._cfg, w, stream)
         del dev
 

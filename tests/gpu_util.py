@@ -28,10 +28,10 @@ def out_to_bits(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run_gpu(moe, layer, x_bits, max_tokens=None, layer_obj=None, grouped_min_tokens=0):
+def run_gpu(moe, layer, x_bits, max_tokens=None, layer_obj=None, grouped_min_tokens=0, fused=0):
     own = layer_obj is None
     L = layer_obj or moe.MoELayer(layer, max_tokens=max_tokens or x_bits.shape[0],
-                                  grouped_min_tokens=grouped_min_tokens)
+                                  grouped_min_tokens=grouped_min_tokens, fused=fused)
     x = x_to_device(x_bits)
     out, ids, w = L.forward(x)
     torch.cuda.synchronize()

@@ -47,9 +47,10 @@ def test_struct_layout_matches_header(moe, tmp_path):
 #include <stddef.h>
 #include "moe_nvfp4.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_layer_info),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_layer_info),
          offsetof(moe_config, routed_scale), offsetof(moe_config, grouped_min_tokens),
-         offsetof(moe_weights, sw2_gs), offsetof(moe_layer_info, sm_count));
+         offsetof(moe_weights, sw2_gs), offsetof(moe_layer_info, sm_count),
+         offsetof(moe_config, fused), offsetof(moe_layer_info, single_launch_max_tokens));
   return 0; }
 ''')
     exe = tmp_path / "layout"
@@ -58,13 +59,14 @@ int main(void) {
     want = [ctypes.sizeof(moe.moe_config), ctypes.sizeof(moe.moe_weights),
             ctypes.sizeof(moe.moe_layer_info), moe.moe_config.routed_scale.offset,
             moe.moe_config.grouped_min_tokens.offset, moe.moe_weights.sw2_gs.offset,
-            moe.moe_layer_info.sm_count.offset]
+            moe.moe_layer_info.sm_count.offset, moe.moe_config.fused.offset,
+            moe.moe_layer_info.single_launch_max_tokens.offset]
     assert got == want
 
 
 def _cfg(moe, **kw):
     base = dict(hidden=2048, num_experts=256, top_k=6, inter=768, num_shared=1, shared_inter=768,
-                max_tokens=8, normalize_topk=1, routed_scale=1.0, grouped_min_tokens=0)
+                max_tokens=8, normalize_topk=1, routed_scale=1.0, grouped_min_tokens=0, fused=0)
     base.update(kw)
     return moe.moe_config(**base)
 
@@ -98,7 +100,7 @@ def test_null_and_host_pointers_rejected(moe):
 def test_calls_on_null_handle(moe):
     L = moe.lib()
     assert L.moe_decode_forward(None, None, 1, None, None, None, None) == moe.moe.MOE_ERR_INVALID_ARG
-    assert L.moe_stage_down(None, 1, None) == moe.moe.MOE_ERR_INVALID_ARG
+    assert L.moe_stage_down(None, 1, None, None) == moe.moe.MOE_ERR_INVALID_ARG
     assert L.moe_check(None, None) == moe.moe.MOE_ERR_INVALID_ARG
     assert L.moe_get_info(None, None) == moe.moe.MOE_ERR_INVALID_ARG
     L.moe_destroy(None)

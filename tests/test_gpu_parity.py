@@ -24,9 +24,33 @@ def moe():
 
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
 def test_workload_full_size(moe, orc, cfg):
+    """moe_decode_forward as the benchmark runs it (single launch where the
+    shape allows it)."""
     layer, x, _ = guarded_case(cfg, gen.BASE_SEED + cfg)
     gout, gids, gw = run_gpu(moe, layer, x)
     check_parity(orc, layer, x, gout, gids, gw)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2])
+def test_workload_three_kernel_chain(moe, orc, cfg):
+    """The same workloads through the moe_stage_* chain (fused = -1)."""
+    layer, x, _ = guarded_case(cfg, gen.BASE_SEED + 10 + cfg)
+    gout, gids, gw = run_gpu(moe, layer, x, fused=-1)
+    check_parity(orc, layer, x, gout, gids, gw)
+
+
+def test_single_launch_is_used_for_small_steps(moe):
+    layer = gen.make_layer(gen.config(1), 3, experts=[0])
+    L = moe.MoELayer(layer, max_tokens=8)
+    try:
+        assert L.info().single_launch_max_tokens >= 1
+    finally:
+        L.close()
+    L = moe.MoELayer(layer, max_tokens=8, fused=-1)
+    try:
+        assert L.info().single_launch_max_tokens == 0
+    finally:
+        L.close()
 
 
 def test_tiny_all_experts_real(moe, orc):
@@ -49,19 +73,21 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("fused", [0, -1], ids=["auto", "chain"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
-def test_ragged_shapes(moe, orc, shape):
+def test_ragged_shapes(moe, orc, shape, fused):
     H, E, k, I, S, Is, T = shape
     c = dict(name="ragged", T=T, H=H, E=E, k=k, I=I, S=S, Is=Is, zipf=False, normalize=1, routed_scale=1.0)
     layer, x, _ = guarded_case(c, 1000 + H + E + T, full=True)
-    gout, gids, gw = run_gpu(moe, layer, x)
+    gout, gids, gw = run_gpu(moe, layer, x, fused=fused)
     check_parity(orc, layer, x, gout, gids, gw)
 
 
-def test_no_normalisation_and_routed_scale(moe, orc):
+@pytest.mark.parametrize("fused", [0, -1], ids=["auto", "chain"])
+def test_no_normalisation_and_routed_scale(moe, orc, fused):
     c = gen.config(0, normalize=0, routed_scale=2.5)
     layer, x, _ = guarded_case(c, 31, T=4, full=True)
-    gout, gids, gw = run_gpu(moe, layer, x)
+    gout, gids, gw = run_gpu(moe, layer, x, fused=fused)
     check_parity(orc, layer, x, gout, gids, gw)
 
 
@@ -72,7 +98,8 @@ def test_router_bias_zipf_small(moe, orc):
     check_parity(orc, layer, x, gout, gids, gw)
 
 
-def test_large_activations_prescale(moe, orc):
+@pytest.mark.parametrize("fused", [0, -1], ids=["auto", "chain"])
+def test_large_activations_prescale(moe, orc, fused):
     """Activations far outside the f16 range (x * 2^20, so h ~ 2^40): the
     kernels' power-of-two prescale must keep the result exact up to the usual
     rounding.  The router rows are scaled by 2^-20 so the logits, hence the
@@ -82,22 +109,24 @@ def test_large_activations_prescale(moe, orc):
     xb = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     big = dict(layer)
     big["router_w"] = layer["router_w"] * np.float32(2.0 ** -20)
-    gout, gids, gw = run_gpu(moe, big, xb)
+    gout, gids, gw = run_gpu(moe, big, xb, fused=fused)
     err_abs, err_rel = check_parity(orc, big, xb, gout, gids, gw)
     assert np.abs((gout.astype(np.uint32) << 16).view(np.float32)).max() > 1e9
 
 
-def test_zero_input(moe, orc):
+@pytest.mark.parametrize("fused", [0, -1], ids=["auto", "chain"])
+def test_zero_input(moe, orc, fused):
     layer, x, _ = guarded_case(0, 3, T=2, full=True)
     xz = np.zeros_like(x)
-    gout, gids, gw = run_gpu(moe, layer, xz)
+    gout, gids, gw = run_gpu(moe, layer, xz, fused=fused)
     oout, _, oids, _ = orc.forward(layer, xz)
     assert np.array_equal(gout, oout)
 
 
-def test_handle_reuse_varying_T_and_determinism(moe, orc):
+@pytest.mark.parametrize("fused", [0, -1], ids=["auto", "chain"])
+def test_handle_reuse_varying_T_and_determinism(moe, orc, fused):
     layer, x, _ = guarded_case(2, 11, T=8)
-    L = moe.MoELayer(layer, max_tokens=8)
+    L = moe.MoELayer(layer, max_tokens=8, fused=fused)
     try:
         first = None
         for T in (8, 1, 5, 8):
@@ -131,23 +160,26 @@ def test_host_buffer_entry_point(moe, orc):
         L.close()
 
 
-def test_stage_entry_points_equal_forward(moe, orc):
+def test_stage_entry_points(moe, orc):
+    """moe_stage_route / _gate_up / _down called one by one equal the chained
+    forward of a handle built with fused = -1 bit for bit, and match the
+    oracle."""
     layer, x, _ = guarded_case(2, 17)
-    L = moe.MoELayer(layer, max_tokens=8)
+    L = moe.MoELayer(layer, max_tokens=8, fused=-1)
     try:
         xd = x_to_device(x)
         T, H, k = x.shape[0], layer["cfg"]["H"], layer["cfg"]["k"]
         out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
         ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
         w = torch.empty((T, k), dtype=torch.float32, device="cuda")
-        moe.moe_stage_route(L.h, xd, T)
+        moe.moe_stage_route(L.h, xd, T, ids, w)
         moe.moe_stage_gate_up(L.h, xd, T)
-        moe.moe_stage_down(L.h, T)
-        moe.moe_stage_combine(L.h, T, out, ids, w)
+        moe.moe_stage_down(L.h, T, out)
         torch.cuda.synchronize()
         fout, fids, fw = run_gpu(moe, layer, x, layer_obj=L)
         assert np.array_equal(out_to_bits(out), fout)
         assert np.array_equal(ids.cpu().numpy(), fids)
+        check_parity(orc, layer, x, fout, fids, fw)
     finally:
         L.close()
 
