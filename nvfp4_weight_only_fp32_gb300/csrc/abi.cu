@@ -171,7 +171,6 @@ void carve_workspace(moe_layer *L, char *base) {
     d.hmax64 = cv.take<unsigned long long>(d.max_pairs);
     d.epoch = cv.take<unsigned>(1);
     d.bar_count = cv.take<unsigned>(1);
-    d.bar_gen = cv.take<unsigned>(1);
     L->x_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->out_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->ids_stage = cv.take<int>((size_t)Tm * K);
@@ -320,7 +319,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
         L->fused_ok[T] = 0;
         if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&
             fused_eligible(d, T, L->sm_count, (size_t)L->optin_smem))
-            L->fused_ok[T] = fused_blocks_per_sm(d, T) >= 2;
+            L->fused_ok[T] = fused_blocks_per_sm(d, T) >= 1;
     }
     if (e != cudaSuccess) {
         moe_status rs = cuda_fail(e, "moe_init");
@@ -428,8 +427,12 @@ moe_status moe_check(moe_layer *L, void *stream) {
     if (word == 0) return MOE_OK;
     int zero = 0;
     cudaMemcpy(L->d.err, &zero, sizeof(int), cudaMemcpyHostToDevice);
-    // a wait that gave up leaves the grid barrier mid-way: reset it
+    // a wait that gave up may leave the single-launch path's barrier counter
+    // out of step with its call counter: restart both, and the per-pair
+    // maxima tagged with the call counter
     cudaMemset(L->d.bar_count, 0, sizeof(unsigned));
+    cudaMemset(L->d.epoch, 0, sizeof(unsigned));
+    cudaMemset(L->d.hmax64, 0, sizeof(unsigned long long) * L->d.max_pairs);
     if (word == 1) return fail(MOE_ERR_TIMEOUT, "an in-kernel wait gave up");
     return fail(MOE_ERR_DEVICE, "device error word " + std::to_string(word));
 }

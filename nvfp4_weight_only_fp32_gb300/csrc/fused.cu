@@ -9,42 +9,62 @@
 // resident, in-kernel waits that give up after a bound and set a sticky error
 // word -- section "Fail-stop").
 //
-// One block per SM (grid = SM count), at most half an SM each, so the next
-// layer's launch (programmatic dependent launch) becomes resident beside it and
-// runs its prologue early.  Phases:
-//   A  before griddepcontrol.wait: bulk-prefetch into L2 this block's router
-//      rows and its first shared-expert tiles (static weights).
-//   B  stage x (T rows) once as f16 with an exact per-row power-of-two
-//      prescale, compute this block's experts' FP32 logits, publish them and
-//      ARRIVE at grid barrier 1.
-//   C  pass 0: this block's shared-expert gate/up tiles (no routing needed)
-//      while the grid arrives; WAIT on barrier 1; pass 1: every block reads
-//      all logits and runs the same deterministic top-k and slot/pair
-//      numbering, then gate/up + SwiGLU over the selected experts' tiles,
-//      spread over all warps of all blocks.  h goes to the workspace with a
-//      per-pair max |h|.  Grid barrier 2.
-//   D  each block owns 16-row output tiles for ALL selected experts: stage h
-//      of a group of experts, down GEMV per (warp, expert), multiply by the
-//      routing weight and accumulate per token, reduce the warps in a fixed
-//      order and write BF16 out.  No further exchange.
-// The token index is the MMA's N coordinate throughout (T <= 8 = N), so B
-// fragments of x are shared by every expert and per-token results land in the
-// lane that owns the token.  The code is kept small on purpose: each phase
-// runs once per layer, so instruction fetch is on the critical path.
+// One block of 16 warps per SM (grid = SM count, all resident).  Weights move
+// from HBM to shared memory by bulk asynchronous copies (cp.async.bulk, the
+// 1-D TMA): every warp owns a ring of RW segments of up to CH 576-byte chunks,
+// one mbarrier per segment.  Lane 0 issues the copies; the warp decodes and
+// multiplies from shared memory.  A warp's segments form one list -- its
+// shared-expert gate/up units, then its routed gate/up units, then its down
+// pieces -- and lane 0 keeps the ring full along that list, across phase
+// boundaries: the down weights do not depend on h, so their copies are in
+// flight while gate/up still runs (for one token, a block's whole share of
+// the layer's selected weights fits in its rings and is requested right
+// after routing).
+//
+// Phases:
+//   A  before griddepcontrol.wait: copy this block's router rows into shared
+//      memory; start the rings on the shared-expert gate/up units (static
+//      weights); L2-prefetch this block's rows of the shared down weights.
+//   B  x (T rows) arrives by one bulk copy; it is staged as the f16 MMA
+//      operand with an exact per-row power-of-two prescale, and this block's
+//      experts' FP32 logits are published; ARRIVE at grid barrier 1.
+//   C  pass 0: shared-expert gate/up units (no routing needed) while the grid
+//      arrives; WAIT on barrier 1; every block runs the same deterministic
+//      top-k (two stages: per group of experts, then per token) and slot/pair
+//      numbering; pass 1: routed gate/up units.  SwiGLU in the epilogue; h
+//      goes to the workspace with a per-pair max |h|.  Grid barrier 2.
+//   D  each block owns 16-row output tiles for ALL slots: stage every pair's h
+//      as f16 (exact power-of-two prescale), down GEMV per (slot, K part) and
+//      warp, scale by the routing weight, reduce the warps in a fixed order
+//      and write BF16 out.  No further exchange.
+// The token index is the MMA's N coordinate throughout (T <= 8 = N), so the
+// B fragments of x are shared by every expert and per-token results land in
+// the lane that owns the token.
+//
+// Everything between the weight streams is a short serial step executed once
+// per layer, so the work split is planned on the host (tables indexed by the
+// slot count) and the device side uses shifts and incremental counters
+// instead of integer division.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kFT = 256;
-constexpr int kFW = 8;
-constexpr int kTF = 8;             // tokens (MMA N)
-constexpr int kRE = 2;             // router experts per block
-constexpr int kPD = 8;             // gate/up register ring depth (chunks)
-constexpr int kPD2 = 4;            // down register ring depth (chunks)
-constexpr int kSlotsF = kTF * kMaxTopK + kMaxShared;   // slots of a call with T <= 8
-constexpr unsigned kSpinLimit = 1u << 22;               // x ~256 ns: about a second
+constexpr int kFW = 16;                                  // warps per block
+constexpr int kFT = 32 * kFW;
+constexpr int kTF = 8;                                   // tokens (MMA N)
+constexpr int kREmax = 4;                                // router experts per block
+constexpr int kCHmax = 8;                                // chunks per ring segment
+constexpr int kCHmin = 4;
+constexpr int kRWmax = 6;                                // ring segments per warp
+constexpr int kSlotsF = kTF * kMaxTopK + kMaxShared;     // slots of a call with T <= 8
+constexpr int kPairsF = kTF * (kMaxTopK + kMaxShared);   // pairs of a call with T <= 8
+constexpr int kCandMax = 64;                             // top-k candidates per token
+constexpr int kM1max = 8;                                // experts per lane in a top-k group
+constexpr unsigned long long kWaitNs = 1000000000ull;    // in-kernel waits give up after ~1 s
 
 struct FusedArgs {
     const __nv_bfloat16 *x;
@@ -54,55 +74,125 @@ struct FusedArgs {
     float *w_out;
 };
 
-struct FusedSmem {
-    size_t xrow, logit_off, red_off, oacc_off, total;
+// Launch geometry and host-planned work split.
+// Dynamic shared memory: [phase-local region | rings].  The phase-local
+// region holds x as the f16 MMA operand (T+1 rows, the last one zero), the
+// router rows, the top-k candidates and x as copied (BF16) during phases
+// B/C, and the staged h rows (all pairs + a zero row) during phase D.
+struct FusedGeom {
+    int kRE, RW, CH;
+    int xrow, hrow;
+    int router_off, cand_off, xraw_off, ring_off, total;
+    int gpt, m1;                            // top-k: groups per token, experts per lane per group
+    int lks0;                               // log2 of the pass-0 K split
+    unsigned char lks1[kSlotsF + 1];        // log2 of the pass-1 K split, by slot count
+    unsigned char lksd[kSlotsF + 1];        // log2 of the down K split, by slot count
+    unsigned char spu[5];                   // gate/up segments per unit, by log2 K split
 };
 
-// [xs: 8 permuted f16 rows][logits T*E][red][oacc].  Phase D stages h over
-// [0, red_off).
-__host__ __device__ inline FusedSmem fused_smem_layout(int H, int E, int T) {
-    FusedSmem L;
-    L.xrow = (size_t)H * 2 + 16;
-    L.logit_off = (kTF * L.xrow + 15) & ~(size_t)15;
-    L.red_off = L.logit_off + (((size_t)T * E * 4 + 15) & ~(size_t)15);
-    L.oacc_off = L.red_off + (size_t)kFW * 4 * 32 * 4;
-    L.total = L.oacc_off + (size_t)kFW * 4 * 32 * 4;
-    return L;
-}
+inline size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
 
-// Grid barrier in two halves so that work can run between arriving and
-// waiting.  Sense by generation: the last block to arrive resets the counter
-// and bumps the generation.  Waits are bounded; on give-up the sticky error
-// word is set and false is returned.
-__device__ __forceinline__ unsigned gbar_arrive(unsigned *count, unsigned *gen, unsigned nblocks) {
-    unsigned my = 0;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        my = ld_acquire_gpu(gen);
-        __threadfence();
-        if (atomicAdd(count, 1u) == nblocks - 1) {
-            *count = 0u;
-            __threadfence();
-            atomicAdd(gen, 1u);
+// Groups of ks warps share a gate/up unit by splitting K; ks minimises the
+// chunks of the busiest warp plus one chunk's worth per unit (the epilogue).
+int choose_lks(int units, int NC, int G) {
+    int best = 0, bestc = 0x7fffffff;
+    for (int l = 0; (1 << l) <= kFW && NC % (1 << l) == 0; ++l) {
+        const int groups = G * (kFW >> l);
+        const int cost = (units + groups - 1) / groups * (NC / (1 << l) + 1);
+        if (cost < bestc) {
+            bestc = cost;
+            best = l;
         }
     }
-    return my;
+    return best;
 }
 
-__device__ __forceinline__ bool gbar_wait(unsigned *gen, unsigned my, int *err) {
+bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) {
+    g.kRE = (d.E + G - 1) / G;
+    g.xrow = d.H * 2 + 16;
+    g.hrow = d.Imax * 2 + 16;
+    // top-k groups: T * gpt tasks (at most one per warp), at most kCandMax
+    // candidates per token, at most kM1max experts per lane
+    g.gpt = std::max(1, std::min({kFW / T, (d.E + 31) / 32, kCandMax / d.k}));
+    g.m1 = (d.E + 32 * g.gpt - 1) / (32 * g.gpt);
+    if (g.m1 > kM1max) return false;
+    const size_t xs = (size_t)(T + 1) * g.xrow;
+    g.router_off = (int)up16(xs);
+    g.cand_off = g.router_off + (int)up16((size_t)g.kRE * d.H * 4);
+    g.xraw_off = g.cand_off + (int)up16((size_t)T * kCandMax * 8);
+    const size_t pB = (size_t)g.xraw_off + (size_t)T * d.H * 2;
+    const size_t pD = (size_t)(T * (d.k + d.S) + 1) * g.hrow;
+    const size_t P = (std::max(pB, pD) + 127) & ~(size_t)127;
+    g.ring_off = (int)P;
+    if ((long)dyn_max <= (long)P) return false;
+    const size_t per_warp = ((size_t)dyn_max - P) / kFW;
+    g.CH = (int)std::min<size_t>(kCHmax, per_warp / (2 * kChunkBytes));
+    if (g.CH < kCHmin) return false;
+    g.RW = (int)std::min<size_t>(kRWmax, per_warp / ((size_t)g.CH * kChunkBytes));
+    g.total = (int)(P + (size_t)kFW * g.RW * g.CH * kChunkBytes);
+    if (g.RW < 2) return false;
+    const int NC13 = d.H / kChunkK, NTs = d.Is / 8, NT13 = d.I / 8;
+    const int ncr = d.I / kChunkK, ncs = d.S > 0 ? d.Is / kChunkK : ncr;
+    g.lks0 = choose_lks(d.S * NTs, NC13, G);
+    for (int n = 0; n <= kSlotsF; ++n) {
+        g.lks1[n] = (unsigned char)choose_lks(std::max(0, n - d.S) * NT13, NC13, G);
+        int l = 0;
+        while (n * (2 << l) <= kFW && ncr % (2 << l) == 0 && ncs % (2 << l) == 0 && ncr / (2 << l) >= 2 &&
+               ncs / (2 << l) >= 2)
+            ++l;
+        g.lksd[n] = (unsigned char)l;
+    }
+    for (int l = 0; l < 5; ++l) g.spu[l] = (unsigned char)(((NC13 >> l) + g.CH - 1) / g.CH);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of an mbarrier; gives up after kWaitNs, setting the
+// sticky error word.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity, int *err) {
+    if (mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = gtimer();
+    while (!mbar_try_wait(b, parity)) {
+        if (gtimer() - t0 > kWaitNs) {
+            atomicExch(err, 1);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Grid barrier on a counter that only grows: every block adds 1 per barrier
+// (a release reduction, no round trip), and barrier b of call `epoch`
+// completes when the counter reaches G * (2 * epoch + b + 1) (modulo 2^32).
+// Every block arrives at both barriers of every call, also after a wait gave
+// up, so the counter stays in step with the call counter.
+__device__ __forceinline__ void gbar_arrive(unsigned *count) {
+    __syncthreads();
+    if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(count) : "memory");
+}
+
+__device__ __forceinline__ bool gbar_wait(const unsigned *count, unsigned target, int *err) {
     __shared__ int s_ok;
     if (threadIdx.x == 0) {
         int ok = 1;
-        unsigned it = 0;
-        while (ld_acquire_gpu(gen) == my) {
-            if (++it > kSpinLimit) {
-                atomicExch(err, 1);
-                ok = 0;
-                break;
+        if ((int)(ld_acquire_gpu(count) - target) < 0) {
+            const unsigned long long t0 = gtimer();
+            while ((int)(ld_acquire_gpu(count) - target) < 0) {
+                if (gtimer() - t0 > kWaitNs) {
+                    atomicExch(err, 1);
+                    ok = 0;
+                    break;
+                }
             }
-            __nanosleep(64);
         }
-        __threadfence();
         s_ok = ok;
     }
     __syncthreads();
@@ -111,34 +201,6 @@ __device__ __forceinline__ bool gbar_wait(unsigned *gen, unsigned my, int *err) 
 
 __device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// Elements of piece j (16 bytes, positions 8j..8j+7) of a permuted 64-element
-// chunk come in four pairs of consecutive elements starting at piece_pair(j, i).
-__device__ __forceinline__ int piece_pair(int j, int i) {
-    const int q = j >> 1, kb = 2 * (j & 1) + (i >> 1);
-    return 16 * kb + 8 * (i & 1) + 2 * q;
-}
-
-__device__ __forceinline__ float2 h2f(uint32_t v) {
-    return __half22float2(*reinterpret_cast<__half2 *>(&v));
-}
-
-__device__ __forceinline__ bool ranks_before(float s, int e, float bs, int be) {
-    return s > bs || (s == bs && e < be);
-}
-
-// decode + 4 MMAs of one chunk against the B row of this lane's column
-__device__ __forceinline__ void chunk_mma(const uint4 &cw, const uint2 &sw, const uint8_t *bp,
-                                          float (&acc)[4]) {
-    uint32_t a[4][4];
-    decode_chunk(cw, sw, a);
-    const uint4 b01 = lds128(bp);
-    const uint4 b23 = lds128(bp + 16);
-    mma_16816(acc, a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
-    mma_16816(acc, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
-    mma_16816(acc, a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
-    mma_16816(acc, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
 }
 
 __device__ __forceinline__ float silu_fast(float v) { return v * __fdividef(1.0f, 1.0f + __expf(-v)); }
@@ -152,241 +214,416 @@ __device__ __forceinline__ float hmax_read(const unsigned long long *hm, int p, 
     return (unsigned)(v >> 32) == epoch ? __uint_as_float((unsigned)v) : 0.f;
 }
 
-template <int XP>
-__global__ void __launch_bounds__(kFT, 2) fused_kernel(DevLayer d, FusedArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
+// On give-up: wait (bounded) for the copies a warp still has in flight
+// (segments n_con .. n_iss-1; lane 0 knows n_iss).
+__device__ __forceinline__ void drain_ring(uint64_t *bar, int RW, int n_con, int n_iss, int lane) {
+    if (lane != 0) return;
+    for (int j = n_con; j < n_iss; ++j) {
+        const unsigned long long t0 = gtimer();
+        while (!mbar_try_wait(bar + j % RW, (unsigned)((j / RW) & 1)) && gtimer() - t0 < kWaitNs) {
+        }
+    }
+}
+
+// decode + 4 MMAs of one chunk held in shared memory, against the B row of
+// this lane's column; blocks 0/2 and 1/3 go to two accumulators so that the
+// MMA dependency chain is half as long.
+__device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, const uint8_t *bp,
+                                               float (&a0)[4], float (&a1)[4]) {
+    const uint4 cw = lds128(ch + 16 * lane);
+    uint2 sw;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n"
+                 : "=r"(sw.x), "=r"(sw.y) : "r"(smem_u32(ch + kCodeBytes + 8 * (lane >> 2))));
+    uint32_t a[4][4];
+    decode_chunk(cw, sw, a);
+    const uint4 b01 = lds128(bp);
+    const uint4 b23 = lds128(bp + 16);
+    mma_16816(a0, a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
+    mma_16816(a1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
+    mma_16816(a0, a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
+    mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+}
+
+// One round of warp-wide selection among up to M items per lane: the largest
+// key, the lowest id among equal keys; the winning item is marked taken.
+// Keys: bits(sigmoid score) + 1 (order-preserving for scores in [0, 1]), 0
+// for NaN; ids of empty places are 0xffffffff.
+template <int M>
+__device__ __forceinline__ void select_round(const unsigned (&key)[M], const unsigned (&id)[M], unsigned &taken,
+                                             unsigned &mx, unsigned &win) {
+    unsigned bk = 0u, bi = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (!((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && id[i] < bi))) {
+            bk = key[i];
+            bi = id[i];
+        }
+    mx = __reduce_max_sync(0xffffffffu, bk);
+    win = __reduce_min_sync(0xffffffffu, bk == mx ? bi : 0xffffffffu);
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (id[i] == win) taken |= 1u << i;
+}
+
+// Per-block constants of the copy issuer, written once by thread 0.
+struct PumpCtx {
+    const uint8_t *w13r, *w2r, *sw13r, *sw2r;
+    size_t e13, e2, s13, s2;              // bytes per expert
+    uint64_t pol;
+    int NC13, ncr, ncs, RW, CH, G, c;
+};
+
+// Per-warp work plan and copy cursor (shared memory; the cursor is touched
+// by the warp's lane 0 only).
+//   gate/up pass p (0 shared experts, 1 routed): this warp's units are
+//   uu = u0 + i * stride, i < my, each unit being (slot lo + uu / NT, tile
+//   uu % NT) and this warp's K range [cb0, cb0 + cpw) of it, in spu segments.
+//   down: items (ri, r2), ri < nrt, r2 < perw: row tile c + ri * G, piece
+//   warp + 16 * r2 = (slot, K part) with 2^lksd parts per slot.
+struct WarpPlan {
+    int u0[2], stride[2], cpw[2], cb0[2], spu[2], my[2], NT[2], lo[2], lks[2];
+    int nrt, perw, lksd;
+    // copy cursor: phase, item, ring slot, segments issued
+    int cph, ci, sl, n_iss, routed;
+    int ri, r2;                          // down item (ri, r2) of the cursor
+    const uint8_t *src;                  // next chunk of the current item
+    int left;                            // chunks of the current item not yet issued
+};
+
+__device__ __forceinline__ void plan_pass(WarpPlan &w, int p, int units, int NT, int lo, int NC, int G, int c,
+                                          int warp, int lks, int spu) {
+    const int ngrp = kFW >> lks;
+    w.lks[p] = lks;
+    w.cpw[p] = NC >> lks;
+    w.cb0[p] = (warp & ((1 << lks) - 1)) * w.cpw[p];
+    w.stride[p] = G * ngrp;
+    w.u0[p] = c * ngrp + (warp >> lks);
+    int my = 0;
+#pragma unroll 1
+    for (int uu = w.u0[p]; uu < units; uu += w.stride[p]) ++my;
+    w.my[p] = my;
+    w.spu[p] = spu;
+    w.NT[p] = NT;
+    w.lo[p] = lo;
+}
+
+// Issue this warp's next segments while fewer than `limit` have been issued
+// and the next one is known (the routed phases need the routing).  Lane 0
+// only; one copy of this code serves every call site.
+__device__ __noinline__ void pump_fn(WarpPlan *wp, const PumpCtx *px, const int *slot_e, uint8_t *ring,
+                                     uint64_t *bar, int warp, int limit) {
+    const int RW = px->RW, CH = px->CH;
+    while (wp->n_iss < limit) {
+        if (wp->left == 0) {
+            // start the next item of the list
+            int cph = wp->cph;
+            if (cph >= 3 || (cph >= 1 && !wp->routed)) break;
+            const int items = cph < 2 ? wp->my[cph] : wp->nrt * wp->perw;
+            if (wp->ci >= items) {
+                wp->cph = cph + 1;
+                wp->ci = 0;
+                wp->ri = wp->r2 = 0;
+                continue;
+            }
+            if (cph < 2) {
+                const int uu = wp->u0[cph] + wp->ci * wp->stride[cph];
+                const int s = uu / wp->NT[cph], r = uu - s * wp->NT[cph];
+                const int e = slot_e[wp->lo[cph] + s];
+                const uint8_t *b = e < 0 ? px->sw13r + (size_t)(-e - 1) * px->s13 : px->w13r + (size_t)e * px->e13;
+                wp->src = b + ((size_t)r * px->NC13 + wp->cb0[cph]) * kChunkBytes;
+                wp->left = wp->cpw[cph];
+            } else {
+                const int rt = px->c + wp->ri * px->G;
+                const int pi = warp + kFW * wp->r2;
+                const int e = slot_e[pi >> wp->lksd], kp = pi & ((1 << wp->lksd) - 1);
+                const int ncd = e < 0 ? px->ncs : px->ncr, cpk = ncd >> wp->lksd;
+                const uint8_t *b = e < 0 ? px->sw2r + (size_t)(-e - 1) * px->s2 : px->w2r + (size_t)e * px->e2;
+                wp->src = b + ((size_t)rt * ncd + kp * cpk) * kChunkBytes;
+                wp->left = cpk;
+                if (++wp->r2 == wp->perw) {
+                    wp->r2 = 0;
+                    ++wp->ri;
+                }
+            }
+            ++wp->ci;
+        }
+        const int n = min(CH, wp->left);
+        const int sl = wp->sl;
+        fence_proxy_async();
+        mbar_expect_tx(bar + sl, (unsigned)(n * kChunkBytes));
+        bulk_g2s(ring + (size_t)sl * CH * kChunkBytes, wp->src, (unsigned)(n * kChunkBytes), bar + sl, px->pol);
+        wp->src += (size_t)n * kChunkBytes;
+        wp->left -= n;
+        wp->sl = sl + 1 == RW ? 0 : sl + 1;
+        ++wp->n_iss;
+    }
+}
+
+template <int QP>
+__global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, FusedGeom fg) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t s_bar[kFW][kRWmax];
+    __shared__ __align__(8) uint64_t s_rbar;   // router rows
+    __shared__ __align__(8) uint64_t s_xbar;   // x
+    __shared__ PumpCtx s_px;
+    __shared__ WarpPlan s_wp[kFW];
     __shared__ float s_tmax[kFW][kTF];
     __shared__ int s_xexp[kTF];
     __shared__ unsigned s_epoch;
+    __shared__ float s_rb[kREmax];
     __shared__ int s_ids[kTF][kMaxTopK];
     __shared__ float s_w[kTF][kMaxTopK];
     __shared__ __align__(4) unsigned char s_tokmask[kMaxExperts];
+    __shared__ short s_eslot[kMaxExperts];
     __shared__ int s_slot_e[kSlotsF];
     __shared__ int s_slot_mask[kSlotsF];
     __shared__ int s_slot_p0[kSlotsF];
-    __shared__ float s_pw[kTF * (kMaxTopK + kMaxShared)];
-    __shared__ int s_wsum[kFW][2];
+    __shared__ float s_pw[kPairsF];
+    __shared__ float s_hun[kPairsF + 1];
+    __shared__ __align__(16) int s_wsum[2][kFW];
     __shared__ int s_nslots;
-    __shared__ int s_grp[kSlotsF + 1];
-    __shared__ int s_ngrp;
-    __shared__ int s_rowidx[kFW][kTF];
-    __shared__ float s_rowunscale[64];
+    __shared__ float s_lpart[kFW][kREmax][kTF];
+    __shared__ __align__(16) float s_red[kFW][4][32];
 
     const int T = a.T, H = d.H, E = d.E, K = d.k, S = d.S;
     const int G = gridDim.x, c = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const FusedSmem SL = fused_smem_layout(H, E, T);
+    const int RW = fg.RW, CH = fg.CH, kRE = fg.kRE;
     uint8_t *xs = smem;
-    float *s_logit = reinterpret_cast<float *>(smem + SL.logit_off);
-    float *red = reinterpret_cast<float *>(smem + SL.red_off);
-    float *oacc = reinterpret_cast<float *>(smem + SL.oacc_off);
-    const int npieces = H / 8;               // 16-byte pieces per activation row
+    const float *s_router = reinterpret_cast<const float *>(smem + fg.router_off);
+    unsigned *s_cand = reinterpret_cast<unsigned *>(smem + fg.cand_off);   // [T][kCandMax][key, id]
+    const uint8_t *xraw = smem + fg.xraw_off;
+    uint8_t *ring = smem + fg.ring_off + (size_t)warp * RW * CH * kChunkBytes;
+    uint64_t *bar = s_bar[warp];
+    WarpPlan &wp = s_wp[warp];
     const int NC13 = H / kChunkK;            // gate/up chunks per tile
     const int NTs = d.Is / 8, NT13 = d.I / 8, NRT = H / 16;
 
     MOE_TRACE_POINT(0, 0);
-    const uint64_t pol = evict_first_policy();
-    // ---------------- A: bulk L2 prefetch of static weights ----------------
-    if (threadIdx.x < kRE) {
-        const int e = c + threadIdx.x * G;
-        if (e < E) prefetch_l2(d.router_w + (size_t)e * H, (unsigned)H * 4);
-    } else if (threadIdx.x == 32 && S > 0 && c < S * NTs) {
-        prefetch_l2(d.sw13r + (size_t)(c / NTs) * d.s13_stride + (size_t)(c % NTs) * NC13 * kChunkBytes,
-                    (unsigned)(NC13 * kChunkBytes));
-    } else if (threadIdx.x == 64 && S > 0 && c < NRT) {
-        prefetch_l2(d.sw2r + (size_t)c * (d.Is / kChunkK) * kChunkBytes, (unsigned)(d.Is / kChunkK * kChunkBytes));
-    }
-    pdl_wait();
-    pdl_trigger();
-    MOE_TRACE_POINT(0, 1);
-
-    // ---------------- B: x, logits ----------------
-    // router rows of this block's experts: the four element pairs of each of
-    // this thread's pieces (served from L2 by the prefetch above)
-    float2 wr[kRE][XP][4];
-#pragma unroll
-    for (int re = 0; re < kRE; ++re) {
-        const int e = c + re * G;
-#pragma unroll
-        for (int xp = 0; xp < XP; ++xp) {
-            const int P = threadIdx.x + xp * kFT;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                wr[re][xp][i] = (e < E && P < npieces)
-                                    ? ld_nc_f2(d.router_w + (size_t)e * H + (P >> 3) * kChunkK + piece_pair(P & 7, i))
-                                    : make_float2(0.f, 0.f);
-        }
-    }
-    if (threadIdx.x == 0) s_epoch = __ldcg(d.epoch);
+    // ---------------- A: static weights before the dependency wait ----------------
     if (threadIdx.x < S) {
         s_slot_e[threadIdx.x] = -(threadIdx.x + 1);
         s_slot_mask[threadIdx.x] = (1 << T) - 1;
         s_slot_p0[threadIdx.x] = threadIdx.x * T;
     }
-    {
-        // x rows -> registers, per-token max |x| -> exact power-of-two prescale
-        uint4 xv[kTF][XP];
-#pragma unroll
-        for (int t = 0; t < kTF; ++t)
-#pragma unroll
-            for (int xp = 0; xp < XP; ++xp) {
-                const int P = threadIdx.x + xp * kFT;
-                xv[t][xp] = (t < T && P < npieces)
-                                ? __ldcg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * H) + P)
-                                : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-        for (int t = 0; t < kTF; ++t) {
-            float m = 0.f;
-#pragma unroll
-            for (int xp = 0; xp < XP; ++xp) {
-                const uint32_t w4[4] = {xv[t][xp].x, xv[t][xp].y, xv[t][xp].z, xv[t][xp].w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[u] << 16)), fabsf(__uint_as_float(w4[u] & 0xFFFF0000u))));
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) s_tmax[warp][t] = m;
-        }
-        __syncthreads();
-        if (threadIdx.x < kTF) {
-            float m = 0.f;
-            for (int w = 0; w < kFW; ++w) m = fmaxf(m, s_tmax[w][threadIdx.x]);
-            s_xexp[threadIdx.x] = max(-100, exp_for_f16(m));
-        }
-        __syncthreads();
-        // x' = x * 2^-xexp as f16, permuted within each 64-element chunk
-        // (element 16kb + 8h + 2q + e at half 16q + 4kb + 2h + e); rows >= T zero
-#pragma unroll
-        for (int t = 0; t < kTF; ++t) {
-            const float sc = pow2f(-s_xexp[t]);
-#pragma unroll
-            for (int xp = 0; xp < XP; ++xp) {
-                const int P = threadIdx.x + xp * kFT;
-                if (P < npieces) {
-                    uint32_t *dst = reinterpret_cast<uint32_t *>(xs + (size_t)t * SL.xrow + (P >> 3) * 128 +
-                                                                 ((P & 7) >> 1) * 8 + (P & 1) * 4);
-                    const uint32_t w4[4] = {xv[t][xp].x, xv[t][xp].y, xv[t][xp].z, xv[t][xp].w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        dst[u * 8] = pack_f16x2(__uint_as_float(w4[u] << 16) * sc,
-                                                __uint_as_float(w4[u] & 0xFFFF0000u) * sc);
-                }
-            }
-        }
+    if (threadIdx.x == 0) {
+        s_px.w13r = d.w13r;
+        s_px.w2r = d.w2r;
+        s_px.sw13r = d.sw13r;
+        s_px.sw2r = d.sw2r;
+        s_px.e13 = d.e13_stride;
+        s_px.e2 = d.e2_stride;
+        s_px.s13 = d.s13_stride;
+        s_px.s2 = d.s2_stride;
+        s_px.pol = evict_first_policy();
+        s_px.NC13 = NC13;
+        s_px.ncr = d.I / kChunkK;
+        s_px.ncs = d.Is / kChunkK;
+        s_px.RW = RW;
+        s_px.CH = CH;
+        s_px.G = G;
+        s_px.c = c;
+        mbar_init(&s_rbar, 1);
+        mbar_init(&s_xbar, 1);
+    }
+    if (threadIdx.x >= 64 && threadIdx.x < 64 + kREmax) {
+        const int re = threadIdx.x - 64, e = c + re * G;
+        s_rb[re] = (re < kRE && e < E && d.router_b) ? d.router_b[e] : 0.f;
+    }
+    if (lane == 0) {
+        plan_pass(wp, 0, S * NTs, NTs, 0, NC13, G, c, warp, fg.lks0, fg.spu[fg.lks0]);
+        wp.my[1] = 0;
+        wp.nrt = wp.perw = 0;
+        wp.lksd = 0;
+        wp.cph = wp.ci = wp.n_iss = wp.sl = wp.routed = wp.ri = wp.r2 = wp.left = 0;
+        for (int i = 0; i < RW; ++i) mbar_init(bar + i, 1);
+        fence_proxy_async();
     }
     __syncthreads();
-    MOE_TRACE_POINT(0, 2);
-    // logits: this thread's permuted pieces against the matching router pairs
+    if (threadIdx.x == 0) {
+        // this block's router rows (static)
+        const int nre = min(kRE, (E - c + G - 1) / G);
+        mbar_expect_tx(&s_rbar, (unsigned)(nre * H * 4));
+#pragma unroll 1
+        for (int re = 0; re < nre; ++re)
+            bulk_g2s(smem + fg.router_off + (size_t)re * H * 4, d.router_w + (size_t)(c + re * G) * H,
+                     (unsigned)(H * 4), &s_rbar, s_px.pol);
+    } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S && c < NRT) {
+        const int si = threadIdx.x - 32, ncs = d.Is / kChunkK;
+        prefetch_l2(d.sw2r + (size_t)si * d.s2_stride + (size_t)c * ncs * kChunkBytes, (unsigned)(ncs * kChunkBytes));
+    }
+    if (lane == 0) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, RW);
+    pdl_wait();
+    pdl_trigger();
+    MOE_TRACE_POINT(0, 1);
+
+    // ---------------- B: x, logits ----------------
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        s_epoch = __ldcg(d.epoch);
+        // x (T rows, contiguous) in one bulk copy
+        mbar_expect_tx(&s_xbar, (unsigned)(T * H * 2));
+        bulk_g2s(smem + fg.xraw_off, a.x, (unsigned)(T * H * 2), &s_xbar, s_px.pol);
+    }
+    if (!mbar_wait(&s_xbar, 0u, d.err) || !mbar_wait(&s_rbar, 0u, d.err)) ok = false;
+    const int nq = H / 4;                    // 4-element quads of an activation row
+    // per-token max |x| -> exact power-of-two prescale for the f16 MMA operand
 #pragma unroll 1
     for (int t = 0; t < T; ++t) {
-        float acc[kRE];
+        float m = 0.f;
 #pragma unroll
-        for (int re = 0; re < kRE; ++re) acc[re] = 0.f;
-#pragma unroll
-        for (int xp = 0; xp < XP; ++xp) {
+        for (int xp = 0; xp < QP; ++xp) {
             const int P = threadIdx.x + xp * kFT;
-            if (P < npieces) {
-                const uint4 v = lds128(xs + (size_t)t * SL.xrow + (P >> 3) * 128 + (P & 7) * 16);
-                const float2 x0 = h2f(v.x), x1 = h2f(v.y), x2 = h2f(v.z), x3 = h2f(v.w);
+            if (P < nq) {
+                const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(v.x << 16)), fabsf(__uint_as_float(v.x & 0xFFFF0000u))),
+                                   fmaxf(fabsf(__uint_as_float(v.y << 16)), fabsf(__uint_as_float(v.y & 0xFFFF0000u)))));
+            }
+        }
+        // m >= 0 and not NaN (fmaxf drops NaN): its bits order as unsigned
+        m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+        if (lane == 0) s_tmax[warp][t] = m;
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        float m = 0.f;
 #pragma unroll
-                for (int re = 0; re < kRE; ++re) {
-                    float s = acc[re];
-                    s = fmaf(x0.x, wr[re][xp][0].x, s);
-                    s = fmaf(x0.y, wr[re][xp][0].y, s);
-                    s = fmaf(x1.x, wr[re][xp][1].x, s);
-                    s = fmaf(x1.y, wr[re][xp][1].y, s);
-                    s = fmaf(x2.x, wr[re][xp][2].x, s);
-                    s = fmaf(x2.y, wr[re][xp][2].y, s);
-                    s = fmaf(x3.x, wr[re][xp][3].x, s);
-                    s = fmaf(x3.y, wr[re][xp][3].y, s);
-                    acc[re] = s;
+        for (int w = 0; w < kFW; ++w) m = fmaxf(m, s_tmax[w][threadIdx.x]);
+        s_xexp[threadIdx.x] = max(-100, exp_for_f16(m));
+    }
+    // zero row T (the B column of absent tokens)
+    for (int i = threadIdx.x; i < fg.xrow / 16; i += kFT)
+        reinterpret_cast<uint4 *>(xs + (size_t)T * fg.xrow)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    MOE_TRACE_POINT(0, 2);
+    // x' = x * 2^-xexp as f16, permuted within each 64-element chunk (element
+    // 16kb + 8h + 2q + e sits at half 16q + 4kb + 2h + e: quad m of a chunk,
+    // elements 4m..4m+3, has kb = m/4, h = (m/2)%2 and q = 2(m%2) for its
+    // first pair, q + 1 for its second), and the FP32 logits of this block's
+    // experts from the exact FP32 values of x (fixed-order reductions: lanes
+    // by butterfly, then warps)
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+        const float sc = pow2f(-s_xexp[t]);
+        float acc[kREmax];
+#pragma unroll
+        for (int re = 0; re < kREmax; ++re) acc[re] = 0.f;
+#pragma unroll
+        for (int xp = 0; xp < QP; ++xp) {
+            const int P = threadIdx.x + xp * kFT;
+            if (P < nq) {
+                const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
+                const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+                const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+                const int m = P & 15, kb = m >> 2, hh = (m >> 1) & 1, q0 = 2 * (m & 1);
+                uint8_t *row = xs + (size_t)t * fg.xrow + (P >> 4) * 128;
+                *reinterpret_cast<uint32_t *>(row + 32 * q0 + 8 * kb + 4 * hh) = pack_f16x2(x0 * sc, x1 * sc);
+                *reinterpret_cast<uint32_t *>(row + 32 * (q0 + 1) + 8 * kb + 4 * hh) = pack_f16x2(x2 * sc, x3 * sc);
+#pragma unroll
+                for (int re = 0; re < kREmax; ++re) {
+                    if (re < kRE) {
+                        const float4 w4 = *reinterpret_cast<const float4 *>(s_router + (size_t)re * H + 4 * P);
+                        acc[re] = fmaf(x3, w4.w, fmaf(x2, w4.z, fmaf(x1, w4.y, fmaf(x0, w4.x, acc[re]))));
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int re = 0; re < kRE; ++re) {
-            float v = acc[re];
+        for (int re = 0; re < kREmax; ++re) {
+            if (re < kRE) {
+                float v = acc[re];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red[(warp * kRE + re) * kTF + t] = v;
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) s_lpart[warp][re][t] = v;
+            }
         }
     }
     __syncthreads();
-    if (threadIdx.x < kRE * kTF) {
+    if (threadIdx.x < kREmax * kTF) {
         const int re = threadIdx.x / kTF, t = threadIdx.x % kTF;
         const int e = c + re * G;
-        if (e < E && t < T) {
+        if (re < kRE && e < E && t < T) {
             float v = 0.f;
-            for (int w = 0; w < kFW; ++w) v += red[(w * kRE + re) * kTF + t];
-            v *= pow2f(s_xexp[t]);             // exact: undoes the prescale
-            if (d.router_b) v += d.router_b[e];
-            d.logits[(size_t)t * E + e] = v;
+#pragma unroll
+            for (int w = 0; w < kFW; ++w) v += s_lpart[w][re][t];
+            d.logits[(size_t)t * E + e] = v + s_rb[re];
         }
     }
-    const unsigned bar1 = gbar_arrive(d.bar_count, d.bar_gen, G);
+    gbar_arrive(d.bar_count);
     MOE_TRACE_POINT(0, 3);
 
     // ---------------- C: gate/up, pass 0 shared experts, pass 1 routed ----------------
-    uint4 cb[kPD];
-    uint2 sb[kPD];
-    int nslots = S;
+    const unsigned bar_base = (unsigned)G * 2u * s_epoch;
+    const uint8_t *xb = xs + (size_t)(g < T ? g : T) * fg.xrow + q * 32;
+    int n_con = 0, sl_c = 0;             // segments consumed by this warp; its ring slot
+    unsigned par_c = 0u;                 // and the slot's phase parity
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         if (pass == 1) {
             MOE_TRACE_POINT(0, 4);
-            if (!gbar_wait(d.bar_gen, bar1, d.err)) return;
+            ok = gbar_wait(d.bar_count, bar_base + (unsigned)G, d.err) && ok;
             MOE_TRACE_POINT(0, 5);
-            // routing, identical in every block
-            for (int i = threadIdx.x; i < T * E; i += kFT) s_logit[i] = __ldcg(d.logits + i);
+            if (!__syncthreads_and(ok)) {
+                ok = false;
+                break;
+            }
+            // routing, identical in every block.  Stage 1: warp w takes
+            // token w / gpt, expert group w % gpt (m1 experts per lane) and
+            // keeps its group's k best as candidates.
+            if (warp < T * fg.gpt) {
+                const int t = warp / fg.gpt, grp = warp - t * fg.gpt;
+                unsigned key[kM1max], id[kM1max], taken = 0u;
+#pragma unroll
+                for (int i = 0; i < kM1max; ++i) {
+                    const int ee = (grp * fg.m1 + i) * 32 + lane;
+                    key[i] = 0u;
+                    id[i] = 0xffffffffu;
+                    if (i < fg.m1 && ee < E) {
+                        const float z = __ldcg(d.logits + (size_t)t * E + ee);
+                        key[i] = isnan(z) ? 0u : __float_as_uint(__fdividef(1.0f, 1.0f + __expf(-z))) + 1u;
+                        id[i] = (unsigned)ee;
+                    }
+                }
+                __syncwarp();
+                MOE_TRACE_POINT(0, 13);
+#pragma unroll 1
+                for (int j = 0; j < K; ++j) {
+                    unsigned mx, win;
+                    select_round<kM1max>(key, id, taken, mx, win);
+                    if (lane == 0) {
+                        s_cand[((t * kCandMax) + grp * K + j) * 2] = mx;
+                        s_cand[((t * kCandMax) + grp * K + j) * 2 + 1] = win;
+                    }
+                }
+            }
             for (int i = threadIdx.x; i < E; i += kFT) s_tokmask[i] = 0;
             __syncthreads();
+            MOE_TRACE_POINT(0, 10);
+            // Stage 2: warp t merges token t's gpt * k candidates.
             if (warp < T) {
-                const int t = warp;
-                float sc[kMaxExperts / 32];
+                const int t = warp, nc = fg.gpt * K;
+                unsigned key[2], id[2], taken = 0u;
 #pragma unroll
-                for (int m = 0; m < kMaxExperts / 32; ++m) {
-                    const int ee = lane + 32 * m;
-                    float s = -INFINITY;
-                    if (ee < E) {
-                        const float z = s_logit[t * E + ee];
-                        s = isnan(z) ? -INFINITY : __fdividef(1.0f, 1.0f + __expf(-z));
-                    }
-                    sc[m] = s;
+                for (int i = 0; i < 2; ++i) {
+                    const int ci = lane + 32 * i;
+                    key[i] = ci < nc ? s_cand[(t * kCandMax + ci) * 2] : 0u;
+                    id[i] = ci < nc ? s_cand[(t * kCandMax + ci) * 2 + 1] : 0xffffffffu;
                 }
-                unsigned taken = 0u;
-                float sel_s = 0.f;
+                unsigned sel_key = 0u;
                 int sel_e = 0;
 #pragma unroll 1
                 for (int j = 0; j < K; ++j) {
-                    float bs = -INFINITY;
-                    int be = 0x7fffffff;
-#pragma unroll
-                    for (int m = 0; m < kMaxExperts / 32; ++m) {
-                        const int ee = lane + 32 * m;
-                        if (ee < E && !(taken & (1u << m)) && ranks_before(sc[m], ee, bs, be)) {
-                            bs = sc[m];
-                            be = ee;
-                        }
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                        if (ranks_before(os, oe, bs, be)) {
-                            bs = os;
-                            be = oe;
-                        }
-                    }
-                    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                    unsigned mx, win;
+                    select_round<2>(key, id, taken, mx, win);
                     if (lane == j) {
-                        sel_s = bs;
-                        sel_e = be;
+                        sel_key = mx;
+                        sel_e = (int)win;
                     }
                 }
+                const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
                 float sum = 0.f;
+#pragma unroll 1
                 for (int j = 0; j < K; ++j) sum += __shfl_sync(0xffffffffu, sel_s, j);
                 if (lane < K) {
                     const float w = (d.normalize ? sel_s / sum : sel_s) * d.routed_scale;
@@ -400,119 +637,107 @@ __global__ void __launch_bounds__(kFT, 2) fused_kernel(DevLayer d, FusedArgs a) 
                 }
             }
             __syncthreads();
-            // slots: shared first, then routed experts in ascending id; an
-            // expert's pairs are contiguous, tokens ascending
+            MOE_TRACE_POINT(0, 11);
+            // slots: shared first, then routed experts in ascending id (one
+            // expert per thread); an expert's pairs are contiguous, tokens
+            // ascending
             {
-                const int per = (E + kFT - 1) / kFT;
-                const int e0 = threadIdx.x * per;
-                int fsum = 0, csum = 0;
-                for (int i = 0; i < per; ++i)
-                    if (e0 + i < E) {
-                        const int cnt = __popc(s_tokmask[e0 + i]);
-                        fsum += cnt > 0;
-                        csum += cnt;
-                    }
-                int finc = fsum, cinc = csum;
+                const int e = threadIdx.x;
+                const int msk = e < E ? s_tokmask[e] : 0;
+                const int cnt = __popc(msk);
+                const unsigned flags = __ballot_sync(0xffffffffu, msk != 0);
+                int cinc = cnt;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
-                    const int x1 = __shfl_up_sync(0xffffffffu, finc, off);
-                    const int x2 = __shfl_up_sync(0xffffffffu, cinc, off);
-                    if (lane >= off) {
-                        finc += x1;
-                        cinc += x2;
-                    }
+                    const int v = __shfl_up_sync(0xffffffffu, cinc, off);
+                    if (lane >= off) cinc += v;
                 }
                 if (lane == 31) {
-                    s_wsum[warp][0] = finc;
-                    s_wsum[warp][1] = cinc;
+                    s_wsum[0][warp] = __popc(flags);
+                    s_wsum[1][warp] = cinc;
                 }
                 __syncthreads();
-                int fb = finc - fsum, cbse = cinc - csum;
-                for (int w = 0; w < warp; ++w) {
-                    fb += s_wsum[w][0];
-                    cbse += s_wsum[w][1];
-                }
-                for (int i = 0; i < per; ++i)
-                    if (e0 + i < E && s_tokmask[e0 + i]) {
-                        const int msk = s_tokmask[e0 + i];
-                        s_slot_e[S + fb] = e0 + i;
-                        s_slot_mask[S + fb] = msk;
-                        s_slot_p0[S + fb] = S * T + cbse;
-                        fb += 1;
-                        cbse += __popc(msk);
+                int fb = __popc(flags & ((1u << lane) - 1u)), cb = cinc - cnt;
+#pragma unroll
+                for (int w = 0; w < kFW; ++w)
+                    if (w < warp) {
+                        fb += s_wsum[0][w];
+                        cb += s_wsum[1][w];
                     }
-                if (threadIdx.x == kFT - 1) s_nslots = S + fb;
-                __syncthreads();
-                for (int it = threadIdx.x; it < T * K; it += kFT) {
-                    const int t = it / K, j = it % K, e = s_ids[t][j];
-                    int slot = S;
-                    while (s_slot_e[slot] != e) ++slot;     // <= T*k slots
-                    s_pw[s_slot_p0[slot] + __popc(s_slot_mask[slot] & ((1 << t) - 1))] = s_w[t][j];
+                if (msk) {
+                    s_slot_e[S + fb] = e;
+                    s_slot_mask[S + fb] = msk;
+                    s_slot_p0[S + fb] = S * T + cb;
+                    s_eslot[e] = (short)(S + fb);
                 }
-                for (int it = threadIdx.x; it < T * S; it += kFT) s_pw[it] = 1.0f;
+                if (threadIdx.x == kFT - 1) s_nslots = S + fb + (msk != 0);
                 __syncthreads();
+                if (threadIdx.x < T * K) {
+                    const int t = threadIdx.x / K, j = threadIdx.x - (threadIdx.x / K) * K, ee = s_ids[t][j];
+                    const int sl = s_eslot[ee];
+                    s_pw[s_slot_p0[sl] + __popc(s_slot_mask[sl] & ((1 << t) - 1))] = s_w[t][j];
+                }
+                if (threadIdx.x < T * S) s_pw[threadIdx.x] = 1.0f;
             }
-            nslots = s_nslots;
+            MOE_TRACE_POINT(0, 12);
+            if (lane == 0) {
+                const int ns = s_nslots, l1 = fg.lks1[ns], ld = fg.lksd[ns];
+                plan_pass(wp, 1, (ns - S) * NT13, NT13, S, NC13, G, c, warp, l1, fg.spu[l1]);
+                wp.lksd = ld;
+                wp.perw = warp < (ns << ld) ? ((ns << ld) - warp + kFW - 1) / kFW : 0;
+                wp.nrt = c < NRT ? (NRT - c + G - 1) / G : 0;
+                wp.routed = 1;
+                if (ok) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, n_con + RW);
+            }
+            __syncwarp();
             MOE_TRACE_POINT(0, 6);
         }
-        // units (slot, 16-row tile) of this pass; ks warps split a unit's K
-        const int slot_lo = pass == 0 ? 0 : S;
-        const int NT = pass == 0 ? NTs : NT13;
-        const int units = (pass == 0 ? S : nslots - S) * NT;
-        int ks = 1;
-        while (ks < kFW && NC13 % (2 * ks) == 0 && units * 2 * ks <= G * kFW) ks *= 2;
-        const int ngrp = kFW / ks, gi = warp / ks, kw = warp % ks;
-        const int cpw = NC13 / ks, cb0 = kw * cpw;
-        int R = cpw < kPD ? cpw : kPD;           // ring depth: divides cpw
-        while (cpw % R) --R;
-        const int stride = G * ngrp, u0 = c * ngrp + gi;
-        const int my_units = u0 < units ? (units - u0 + stride - 1) / stride : 0;
-        auto unit_base = [&](int ui) -> const uint8_t * {
-            const int uu = u0 + ui * stride;
-            const int e = s_slot_e[slot_lo + uu / NT], r = uu % NT;
-            const uint8_t *b = e < 0 ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
-            return b + (size_t)r * NC13 * kChunkBytes;
-        };
-        if (my_units > 0) {
-            const uint8_t *b0 = unit_base(0);
-#pragma unroll
-            for (int i = 0; i < kPD; ++i)
-                if (i < R) load_chunk(b0, cb0 + i, lane, cb[i], sb[i], pol);
-        }
-        const uint8_t *brow = xs + (size_t)g * SL.xrow + q * 32;
+        const int lks = wp.lks[pass], cpw = wp.cpw[pass], cb0 = wp.cb0[pass], spu = wp.spu[pass];
+        const int my = wp.my[pass], u0 = wp.u0[pass], ustride = wp.stride[pass], NT = wp.NT[pass];
+        const int lo = wp.lo[pass], ks = 1 << lks, gi = warp >> lks, kw = warp & (ks - 1);
         // every warp of a group has the same unit count, so the group's named
         // barrier (id 1 + gi) is reached by all of its warps together
 #pragma unroll 1
-        for (int ui = 0; ui < my_units; ++ui) {
-            const uint8_t *cur = unit_base(ui);
-            const uint8_t *nxt = ui + 1 < my_units ? unit_base(ui + 1) : nullptr;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ui = 0; ui < my; ++ui) {
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint8_t *bp = xb + cb0 * 128;
+            int left = cpw;
 #pragma unroll 1
-            for (int c0 = 0; c0 < cpw; c0 += R) {
-#pragma unroll
-                for (int i = 0; i < kPD; ++i) {
-                    if (i < R) {
-                        const int cc = c0 + i;
-                        chunk_mma(cb[i], sb[i], brow + (cb0 + cc) * 128, acc);
-                        const int cn = cc + R;
-                        if (cn < cpw) load_chunk(cur, cb0 + cn, lane, cb[i], sb[i], pol);
-                        else if (nxt) load_chunk(nxt, cb0 + cn - cpw, lane, cb[i], sb[i], pol);
-                    }
+            for (int p = 0; p < spu; ++p) {
+                const int n = min(CH, left);
+                if (ok && !mbar_wait(bar + sl_c, par_c, d.err)) ok = false;
+                if (ok) {
+                    const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
+#pragma unroll 1
+                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, a0, a1);
                 }
+                __syncwarp();
+                bp += n * 128;
+                left -= n;
+                ++n_con;
+                if (++sl_c == RW) {
+                    sl_c = 0;
+                    par_c ^= 1u;
+                }
+                if (lane == 0 && ok) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, n_con + RW);
             }
-            const int uu = u0 + ui * stride;
-            const int slot = slot_lo + uu / NT, r = uu % NT;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) a0[v] += a1[v];
+            const int uu = u0 + ui * ustride;
+            const int s = uu / NT, r = uu - s * NT, slot = lo + s;
             if (ks > 1) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) red[(warp * 4 + v) * 32 + lane] = acc[v];
+                for (int v = 0; v < 4; ++v) s_red[warp][v][lane] = a0[v];
                 asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
-                if (kw == 0)
+                if (kw == 0) {
+#pragma unroll 1
                     for (int w = 1; w < ks; ++w)
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) acc[v] += red[((warp + w) * 4 + v) * 32 + lane];
+                        for (int v = 0; v < 4; ++v) a0[v] += s_red[warp + w][v][lane];
+                }
                 asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
             }
-            if (kw == 0) {
+            if (kw == 0 && ok) {
                 // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row 8r+g
                 const int e = s_slot_e[slot];
                 const int msk = s_slot_mask[slot], p0 = s_slot_p0[slot];
@@ -526,8 +751,8 @@ __global__ void __launch_bounds__(kFT, 2) fused_kernel(DevLayer d, FusedArgs a) 
                     float habs = 0.f;
                     if (on) {
                         const float un = pow2f(s_xexp[t]);
-                        const float gt = acc[e2] * gsa * un, up = acc[2 + e2] * gsb * un;
-                        const __nv_bfloat16 hb = __float2bfloat16_rn(silu_fast(gt) * up);
+                        const float gt = a0[e2] * gsa * un, upv = a0[2 + e2] * gsb * un;
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(silu_fast(gt) * upv);
                         d.h_ws[(size_t)p * d.Imax + 8 * r + g] = hb;
                         habs = fabsf(__bfloat162float(hb));
                     }
@@ -540,146 +765,117 @@ __global__ void __launch_bounds__(kFT, 2) fused_kernel(DevLayer d, FusedArgs a) 
         }
     }
     MOE_TRACE_POINT(0, 7);
-
-    // ---------------- D plan: groups of experts whose h rows fit in smem ----------------
-    const size_t hrow = (size_t)d.Imax * 2 + 16;
-    const int rows_cap = (int)(SL.red_off / hrow) - 1;       // last row: zeros
-    if (threadIdx.x == 0) {
-        int ng = 0, s0 = 0;
-        while (s0 < nslots) {
-            int s1 = s0, rows = 0;
-            while (s1 < nslots && s1 - s0 < kFW && rows + __popc(s_slot_mask[s1]) <= rows_cap) {
-                rows += __popc(s_slot_mask[s1]);
-                ++s1;
-            }
-            s_grp[ng++] = s0;
-            s0 = s1;
-        }
-        s_grp[ng] = nslots;
-        s_ngrp = ng;
+    gbar_arrive(d.bar_count);
+    ok = gbar_wait(d.bar_count, bar_base + 2u * (unsigned)G, d.err) && ok;
+    if (!__syncthreads_and(ok)) {
+        drain_ring(bar, RW, n_con, lane == 0 ? wp.n_iss : 0, lane);
+        if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;
+        return;
     }
-    const unsigned bar2 = gbar_arrive(d.bar_count, d.bar_gen, G);
-    if (!gbar_wait(d.bar_gen, bar2, d.err)) return;
     MOE_TRACE_POINT(0, 8);
 
     // ---------------- D: down + combine, 16 output rows per tile ----------------
-    const int ngroups = s_ngrp;
+    // stage every pair's h as f16 with an exact power-of-two prescale (one
+    // warp per row, all of a lane's loads in flight); row npairs stays zero
+    // (the B column of tokens a slot does not serve)
+    const int npairs = T * (K + S);
     uint8_t *hs = smem;
-    uint4 db[kPD2];
-    uint2 dsb[kPD2];
+    if (threadIdx.x < npairs)
+        s_hun[threadIdx.x] = pow2f(max(-100, exp_for_f16(hmax_read(d.hmax64, threadIdx.x, s_epoch))));
+    for (int i = threadIdx.x; i < fg.hrow / 16; i += kFT)
+        reinterpret_cast<uint4 *>(hs + (size_t)npairs * fg.hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    {
+        const int pieces = d.Imax / 8;       // 16-byte pieces per h row
 #pragma unroll 1
-    for (int rt = c; rt < NRT; rt += G) {
+        for (int j = warp; j < npairs; j += kFW) {
+            const uint4 *srcrow = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)j * d.Imax);
+            const float sc = __fdividef(1.0f, s_hun[j]);   // exact: a power of two
+#pragma unroll 1
+            for (int P0 = 0; P0 < pieces; P0 += 128) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int P = P0 + lane + 32 * u;
+                    if (P < pieces) v[u] = __ldcg(srcrow + P);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int P = P0 + lane + 32 * u;
+                    if (P < pieces) {
+                        uint32_t *dst = reinterpret_cast<uint32_t *>(hs + (size_t)j * fg.hrow + (P >> 3) * 128 +
+                                                                     ((P & 7) >> 1) * 8 + (P & 1) * 4);
+                        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                        for (int uu = 0; uu < 4; ++uu)
+                            dst[uu * 8] = pack_f16x2(__uint_as_float(w4[uu] << 16) * sc,
+                                                     __uint_as_float(w4[uu] & 0xFFFF0000u) * sc);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    MOE_TRACE_POINT(0, 14);
+    const int nrt = wp.nrt, perw = wp.perw, lksd = wp.lksd;
+#pragma unroll 1
+    for (int ri = 0; ri < nrt; ++ri) {
+        const int rt = c + ri * G;
         float oa[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = threadIdx.x; i < (int)(hrow / 16); i += kFT)
-            reinterpret_cast<uint4 *>(hs + (size_t)rows_cap * hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
-        for (int gk = 0; gk < ngroups; ++gk) {
-            const int sa = s_grp[gk], sbnd = s_grp[gk + 1];
-            const int myslot = sa + warp < sbnd ? sa + warp : -1;
-            // this warp's weights do not depend on h: start them first
-            const uint8_t *src = nullptr;
-            int nc = 0;
-            if (myslot >= 0) {
-                const int e = s_slot_e[myslot];
-                const int I = e < 0 ? d.Is : d.I;
-                nc = I / kChunkK;
-                src = (e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride) +
-                      (size_t)rt * nc * kChunkBytes;
-#pragma unroll
-                for (int i = 0; i < kPD2; ++i)
-                    if (i < nc) load_chunk(src, i, lane, db[i], dsb[i], pol);
-            }
-            __syncthreads();
-            // row table: slot (sa + w), token column n -> staged row or the zero row
-            int nrows = 0;
-            for (int s2 = sa; s2 < sbnd; ++s2) nrows += __popc(s_slot_mask[s2]);
-            if (threadIdx.x < kFW * kTF) {
-                const int w = threadIdx.x / kTF, n = threadIdx.x % kTF;
-                int row = rows_cap;
-                if (sa + w < sbnd) {
-                    int base = 0;
-                    for (int s2 = sa; s2 < sa + w; ++s2) base += __popc(s_slot_mask[s2]);
-                    const int msk = s_slot_mask[sa + w];
-                    if (n < T && ((msk >> n) & 1)) row = base + __popc(msk & ((1 << n) - 1));
-                }
-                s_rowidx[w][n] = row;
-            }
-            const int p_first = s_slot_p0[sa];
-            if (threadIdx.x < nrows)
-                s_rowunscale[threadIdx.x] = pow2f(max(-100, exp_for_f16(hmax_read(d.hmax64, p_first + threadIdx.x, s_epoch))));
-            __syncthreads();
-            // stage the group's h rows (pairs p_first.. are contiguous) as f16
-            {
-                const int pieces = d.Imax / 8;
-                const int items = nrows * pieces;
+        for (int r2 = 0; r2 < perw; ++r2) {
+            const int pi = warp + kFW * r2;
+            const int slot = pi >> lksd, kp = pi & ((1 << lksd) - 1);
+            const int e = s_slot_e[slot];
+            const int msk = s_slot_mask[slot], p0 = s_slot_p0[slot];
+            const int cpk = (e < 0 ? d.Is : d.I) / kChunkK >> lksd;
+            const int row = ((msk >> g) & 1) ? p0 + __popc(msk & ((1 << g) - 1)) : npairs;
+            const uint8_t *bp = hs + (size_t)row * fg.hrow + q * 32 + kp * cpk * 128;
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            int left = cpk;
 #pragma unroll 1
-                for (int base = threadIdx.x; base < items; base += 2 * kFT) {
-                    uint4 v[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int it = base + u * kFT;
-                        if (it < items) {
-                            const int j = it / pieces;
-                            v[u] = __ldcg(reinterpret_cast<const uint4 *>(d.h_ws + (size_t)(p_first + j) * d.Imax) +
-                                          (it - j * pieces));
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int it = base + u * kFT;
-                        if (it < items) {
-                            const int j = it / pieces, P = it - j * pieces;
-                            uint32_t *dst = reinterpret_cast<uint32_t *>(hs + (size_t)j * hrow + (P >> 3) * 128 +
-                                                                         ((P & 7) >> 1) * 8 + (P & 1) * 4);
-                            const float sc = __fdividef(1.0f, s_rowunscale[j]);   // exact: a power of two
-                            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                            for (int uu = 0; uu < 4; ++uu)
-                                dst[uu * 8] = pack_f16x2(__uint_as_float(w4[uu] << 16) * sc,
-                                                         __uint_as_float(w4[uu] & 0xFFFF0000u) * sc);
-                        }
-                    }
-                }
-            }
-            __syncthreads();
-            if (myslot >= 0) {
-                const uint8_t *bp = hs + (size_t)s_rowidx[warp][g] * hrow + q * 32;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            while (left > 0) {
+                const int n = min(CH, left);
+                if (ok && !mbar_wait(bar + sl_c, par_c, d.err)) ok = false;
+                if (ok) {
+                    const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
-                for (int c0 = 0; c0 < nc; c0 += kPD2) {
-#pragma unroll
-                    for (int i = 0; i < kPD2; ++i) {
-                        const int cc = c0 + i;
-                        if (cc < nc) {
-                            chunk_mma(db[i], dsb[i], bp + cc * 128, acc);
-                            if (cc + kPD2 < nc) load_chunk(src, cc + kPD2, lane, db[i], dsb[i], pol);
-                        }
-                    }
+                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, a0, a1);
                 }
-                // y = gs * 2^hexp * acc, weighted into the per-token accumulator
-                const int e = s_slot_e[myslot];
-                const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
-                const int msk = s_slot_mask[myslot], p0 = s_slot_p0[myslot];
+                __syncwarp();
+                bp += n * 128;
+                left -= n;
+                ++n_con;
+                if (++sl_c == RW) {
+                    sl_c = 0;
+                    par_c ^= 1u;
+                }
+                if (lane == 0 && ok) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, n_con + RW);
+            }
+            // y = gs * 2^hexp * acc, weighted into the per-token accumulator
+            const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
 #pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int t = 2 * q + e2;
-                    if (t < T && ((msk >> t) & 1)) {
-                        const float wgt = s_pw[p0 + __popc(msk & ((1 << t) - 1))] * gs * s_rowunscale[s_rowidx[warp][t]];
-                        oa[e2] = fmaf(wgt, acc[e2], oa[e2]);
-                        oa[2 + e2] = fmaf(wgt, acc[2 + e2], oa[2 + e2]);
-                    }
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int t = 2 * q + e2;
+                if (t < T && ((msk >> t) & 1)) {
+                    const int p = p0 + __popc(msk & ((1 << t) - 1));
+                    const float wgt = s_pw[p] * gs * s_hun[p];
+                    oa[e2] = fmaf(wgt, a0[e2] + a1[e2], oa[e2]);
+                    oa[2 + e2] = fmaf(wgt, a0[2 + e2] + a1[2 + e2], oa[2 + e2]);
                 }
             }
         }
         // fixed-order reduction over warps, BF16 out
 #pragma unroll
-        for (int v = 0; v < 4; ++v) oacc[(warp * 4 + v) * 32 + lane] = oa[v];
+        for (int v = 0; v < 4; ++v) s_red[warp][v][lane] = oa[v];
         __syncthreads();
+        MOE_TRACE_POINT(0, 15);
         if (warp == 0) {
             float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
             for (int w = 0; w < kFW; ++w)
 #pragma unroll
-                for (int v = 0; v < 4; ++v) o[v] += oacc[(w * 4 + v) * 32 + lane];
+                for (int v = 0; v < 4; ++v) o[v] += s_red[w][v][lane];
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
                 const int t = 2 * q + e2;
@@ -689,59 +885,98 @@ __global__ void __launch_bounds__(kFT, 2) fused_kernel(DevLayer d, FusedArgs a) 
                 }
             }
         }
+        __syncthreads();
     }
+    if (!ok) drain_ring(bar, RW, n_con, lane == 0 ? wp.n_iss : 0, lane);
     MOE_TRACE_POINT(0, 9);
     if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;
 }
 
-}  // namespace
-
-// Largest T for which moe_decode_forward picks the single launch: above it the
-// three-kernel chain streams the weights faster (more warps per SM).
-constexpr int kFusedMaxT = 1;
-
-bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem) {
-    if (T < 1 || T > kFusedMaxT) return false;
-    if (d.E > kRE * sm_count) return false;
-    if (d.H / 8 > 2 * kFT) return false;                    // x pieces: at most two per thread
-    if (d.k * T + d.S > kSlotsF) return false;
-    const FusedSmem L = fused_smem_layout(d.H, d.E, T);
-    const size_t hrow = (size_t)d.Imax * 2 + 16;
-    if ((int)(L.red_off / hrow) - 1 < kTF) return false;    // one expert's 8 rows + the zero row
-    if (L.total + 8 * 1024 > optin_smem / 2) return false;  // two blocks per SM
-    return true;
-}
-
-cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
-                         float *w, int sm_count, cudaStream_t s) {
-    const FusedSmem L = fused_smem_layout(d.H, d.E, T);
-    FusedArgs a{x, T, out, ids, w};
+template <int QP>
+cudaError_t launch_q(const DevLayer &d, const FusedArgs &a, const FusedGeom &fg, int G, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sm_count);
+    cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(kFT);
-    cfg.dynamicSmemBytes = L.total;
+    cfg.dynamicSmemBytes = (size_t)fg.total;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (d.H / 8 > kFT) return cudaLaunchKernelEx(&cfg, fused_kernel<2>, d, a);
-    return cudaLaunchKernelEx(&cfg, fused_kernel<1>, d, a);
+    return cudaLaunchKernelEx(&cfg, fused_kernel<QP>, d, a, fg);
+}
+
+constexpr int kQPcount = 4;                  // x quads per thread: H <= 4 * 4 * 512 = 8192
+int g_dyn_max[kQPcount + 1];                 // dynamic shared memory a block may use
+
+int qp_of(int H) { return (H / 4 + kFT - 1) / kFT; }
+
+template <int QP>
+cudaError_t prepare_q(int optin) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<QP>);
+    if (e != cudaSuccess) return e;
+    g_dyn_max[QP] = optin - (int)fa.sharedSizeBytes;
+    return cudaFuncSetAttribute(fused_kernel<QP>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_dyn_max[QP]);
+}
+
+}  // namespace
+
+// Largest T for which moe_decode_forward picks the single launch.
+constexpr int kFusedMaxT = 8;
+
+bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem) {
+    (void)optin_smem;
+    if (T < 1 || T > kFusedMaxT) return false;
+    if (d.E > kREmax * sm_count) return false;
+    const int QP = qp_of(d.H);
+    if (QP < 1 || QP > kQPcount || g_dyn_max[QP] <= 0) return false;
+    if (d.k * T + d.S > kSlotsF) return false;
+    FusedGeom fg;
+    return fused_geometry(d, T, sm_count, g_dyn_max[QP], fg);
+}
+
+cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
+                         float *w, int sm_count, cudaStream_t s) {
+    const int QP = qp_of(d.H);
+    FusedGeom fg;
+    if (QP < 1 || QP > kQPcount || !fused_geometry(d, T, sm_count, g_dyn_max[QP], fg)) return cudaErrorInvalidValue;
+    FusedArgs a{x, T, out, ids, w};
+    switch (QP) {
+        case 1: return launch_q<1>(d, a, fg, sm_count, s);
+        case 2: return launch_q<2>(d, a, fg, sm_count, s);
+        case 3: return launch_q<3>(d, a, fg, sm_count, s);
+        default: return launch_q<4>(d, a, fg, sm_count, s);
+    }
 }
 
 cudaError_t prepare_fused_kernel(int optin_bytes) {
-    cudaError_t e = allow_max_dynamic_smem(fused_kernel<1>, optin_bytes / 2);
-    if (e == cudaSuccess) e = allow_max_dynamic_smem(fused_kernel<2>, optin_bytes / 2);
+    cudaError_t e = prepare_q<1>(optin_bytes);
+    if (e == cudaSuccess) e = prepare_q<2>(optin_bytes);
+    if (e == cudaSuccess) e = prepare_q<3>(optin_bytes);
+    if (e == cudaSuccess) e = prepare_q<4>(optin_bytes);
     return e;
 }
 
 int fused_blocks_per_sm(const DevLayer &d, int T) {
-    const FusedSmem L = fused_smem_layout(d.H, d.E, T);
+    const int QP = qp_of(d.H);
+    int sms = 0, dev = 0;
+    if (QP < 1 || QP > kQPcount || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    FusedGeom fg;
+    if (!fused_geometry(d, T, sms, g_dyn_max[QP], fg)) return 0;
     int n = 0;
-    cudaError_t e = d.H / 8 > kFT
-                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<2>, kFT, L.total)
-                        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kFT, L.total);
+    cudaError_t e;
+    switch (QP) {
+        case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kFT, fg.total); break;
+        case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<2>, kFT, fg.total); break;
+        case 3: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<3>, kFT, fg.total); break;
+        default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<4>, kFT, fg.total); break;
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return 0;

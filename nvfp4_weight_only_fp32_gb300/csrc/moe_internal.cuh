@@ -87,8 +87,7 @@ struct DevLayer {
     int *err;                       // [1] sticky device error word
     unsigned long long *hmax64;     // [max_pairs] single-launch path: (epoch << 32) | max|h| bits
     unsigned *epoch;                // [1] call counter of the single-launch path
-    unsigned *bar_count;            // [1] grid barrier arrivals
-    unsigned *bar_gen;              // [1] grid barrier generation
+    unsigned *bar_count;            // [1] grid barrier arrivals (2 * grid size per call)
     unsigned long long *trace;      // traced build only: phase timestamps
     int trace_blocks;
 };
@@ -259,6 +258,39 @@ __device__ __forceinline__ void load_chunk(const uint8_t *tbase, int c, int lane
     const uint8_t *ch = tbase + (size_t)c * kChunkBytes;
     cw = ld_stream_v4(ch + 16 * lane, pol);
     sw = ld_stream_v2(ch + kCodeBytes + 8 * (lane >> 2), pol);
+}
+
+// ---- mbarrier + bulk async copy (TMA, 1-D) ----
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *b, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok) : "r"(smem_u32(b)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// global -> shared bulk copy completing on mbarrier `b` (bytes % 16 == 0,
+// both addresses 16-byte aligned), with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *b,
+                                         uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;\n" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(b)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 // Decode one chunk's A fragments for one lane: 4 blocks x 4 registers.
