@@ -143,6 +143,7 @@ void carve_weights(moe_layer *L, char *base) {
     d.sw2r = cv.take<uint8_t>((size_t)S * d.s2_stride);
     d.sgs13 = cv.take<float>((size_t)(S > 0 ? S : 1) * 2);
     d.sgs2 = cv.take<float>(S > 0 ? S : 1);
+    d.gsp = cv.take<float4>((size_t)E + S);
     L->wbytes = cv.off;
 }
 
@@ -291,6 +292,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
         cp(d.sgs13, w->sw13_gs, (size_t)S * 2 * sizeof(float));
         cp(d.sgs2, w->sw2_gs, (size_t)S * sizeof(float));
     }
+    if (e == cudaSuccess) e = launch_pack_scales(d, st);
     if (e == cudaSuccess)
         e = launch_repack(w->w13, w->w13_sf, E, 2 * I, H, true, const_cast<uint8_t *>(d.w13r), st);
     if (e == cudaSuccess)

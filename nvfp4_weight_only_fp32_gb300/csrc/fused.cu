@@ -64,6 +64,7 @@ constexpr int kSlotsF = kTF * kMaxTopK + kMaxShared;     // slots of a call with
 constexpr int kPairsF = kTF * (kMaxTopK + kMaxShared);   // pairs of a call with T <= 8
 constexpr int kCandMax = 64;                             // top-k candidates per token
 constexpr int kM1max = 8;                                // experts per lane in a top-k group
+constexpr int kTabMax = 32;                              // copy-list items per warp
 constexpr unsigned long long kWaitNs = 1000000000ull;    // in-kernel waits give up after ~1 s
 
 struct FusedArgs {
@@ -78,16 +79,16 @@ struct FusedArgs {
 // Dynamic shared memory: [phase-local region | rings].  The phase-local
 // region holds x as the f16 MMA operand (T+1 rows, the last one zero), the
 // router rows, the top-k candidates and x as copied (BF16) during phases
-// B/C, and the staged h rows (all pairs + a zero row) during phase D.
+// B/C, and the staged h rows (all pairs + a zero row) during phase D; then
+// the packed per-expert global scales and router biases for the whole call.
 struct FusedGeom {
     int kRE, RW, CH;
     int xrow, hrow;
-    int router_off, cand_off, xraw_off, ring_off, total;
-    int gpt, m1;                            // top-k: groups per token, experts per lane per group
+    int router_off, cand_off, xraw_off, gs_off, ring_off, total;
+    int gpt, m1p;                           // top-k: groups per token, experts per lane per group (1, 2, 4, 8)
     int lks0;                               // log2 of the pass-0 K split
     unsigned char lks1[kSlotsF + 1];        // log2 of the pass-1 K split, by slot count
     unsigned char lksd[kSlotsF + 1];        // log2 of the down K split, by slot count
-    unsigned char spu[5];                   // gate/up segments per unit, by log2 K split
 };
 
 inline size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
@@ -114,15 +115,18 @@ bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) 
     // top-k groups: T * gpt tasks (at most one per warp), at most kCandMax
     // candidates per token, at most kM1max experts per lane
     g.gpt = std::max(1, std::min({kFW / T, (d.E + 31) / 32, kCandMax / d.k}));
-    g.m1 = (d.E + 32 * g.gpt - 1) / (32 * g.gpt);
-    if (g.m1 > kM1max) return false;
+    const int m1 = (d.E + 32 * g.gpt - 1) / (32 * g.gpt);
+    if (m1 > kM1max) return false;
+    g.m1p = 1;
+    while (g.m1p < m1) g.m1p *= 2;
     const size_t xs = (size_t)(T + 1) * g.xrow;
     g.router_off = (int)up16(xs);
     g.cand_off = g.router_off + (int)up16((size_t)g.kRE * d.H * 4);
     g.xraw_off = g.cand_off + (int)up16((size_t)T * kCandMax * 8);
     const size_t pB = (size_t)g.xraw_off + (size_t)T * d.H * 2;
     const size_t pD = (size_t)(T * (d.k + d.S) + 1) * g.hrow;
-    const size_t P = (std::max(pB, pD) + 127) & ~(size_t)127;
+    g.gs_off = (int)((std::max(pB, pD) + 15) & ~(size_t)15);
+    const size_t P = ((size_t)g.gs_off + (size_t)(d.E + d.S) * 16 + 127) & ~(size_t)127;
     g.ring_off = (int)P;
     if ((long)dyn_max <= (long)P) return false;
     const size_t per_warp = ((size_t)dyn_max - P) / kFW;
@@ -142,7 +146,15 @@ bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) 
             ++l;
         g.lksd[n] = (unsigned char)l;
     }
-    for (int l = 0; l < 5; ++l) g.spu[l] = (unsigned char)(((NC13 >> l) + g.CH - 1) / g.CH);
+    // every warp's copy list (units of both passes + down pieces) must fit
+    // its table, whatever the number of distinct experts
+    const int NRT = d.H / 16, nrt = (NRT + G - 1) / G;
+    const int my0 = (d.S * NTs + G * (kFW >> g.lks0) - 1) / (G * (kFW >> g.lks0));
+    for (int n = d.S + 1; n <= d.S + std::min(d.E, T * d.k); ++n) {
+        const int my1 = ((n - d.S) * NT13 + G * (kFW >> g.lks1[n]) - 1) / (G * (kFW >> g.lks1[n]));
+        const int perw = ((n << g.lksd[n]) + kFW - 1) / kFW;
+        if (my0 + my1 + nrt * perw > kTabMax) return false;
+    }
     return true;
 }
 
@@ -265,99 +277,38 @@ __device__ __forceinline__ void select_round(const unsigned (&key)[M], const uns
         if (id[i] == win) taken |= 1u << i;
 }
 
-// Per-block constants of the copy issuer, written once by thread 0.
-struct PumpCtx {
-    const uint8_t *w13r, *w2r, *sw13r, *sw2r;
-    size_t e13, e2, s13, s2;              // bytes per expert
-    uint64_t pol;
-    int NC13, ncr, ncs, RW, CH, G, c;
-};
-
-// Per-warp work plan and copy cursor (shared memory; the cursor is touched
-// by the warp's lane 0 only).
-//   gate/up pass p (0 shared experts, 1 routed): this warp's units are
-//   uu = u0 + i * stride, i < my, each unit being (slot lo + uu / NT, tile
-//   uu % NT) and this warp's K range [cb0, cb0 + cpw) of it, in spu segments.
-//   down: items (ri, r2), ri < nrt, r2 < perw: row tile c + ri * G, piece
-//   warp + 16 * r2 = (slot, K part) with 2^lksd parts per slot.
-struct WarpPlan {
-    int u0[2], stride[2], cpw[2], cb0[2], spu[2], my[2], NT[2], lo[2], lks[2];
-    int nrt, perw, lksd;
-    // copy cursor: phase, item, ring slot, segments issued
-    int cph, ci, sl, n_iss, routed;
-    int ri, r2;                          // down item (ri, r2) of the cursor
-    const uint8_t *src;                  // next chunk of the current item
-    int left;                            // chunks of the current item not yet issued
-};
-
-__device__ __forceinline__ void plan_pass(WarpPlan &w, int p, int units, int NT, int lo, int NC, int G, int c,
-                                          int warp, int lks, int spu) {
-    const int ngrp = kFW >> lks;
-    w.lks[p] = lks;
-    w.cpw[p] = NC >> lks;
-    w.cb0[p] = (warp & ((1 << lks) - 1)) * w.cpw[p];
-    w.stride[p] = G * ngrp;
-    w.u0[p] = c * ngrp + (warp >> lks);
-    int my = 0;
-#pragma unroll 1
-    for (int uu = w.u0[p]; uu < units; uu += w.stride[p]) ++my;
-    w.my[p] = my;
-    w.spu[p] = spu;
-    w.NT[p] = NT;
-    w.lo[p] = lo;
-}
-
-// Issue this warp's next segments while fewer than `limit` have been issued
-// and the next one is known (the routed phases need the routing).  Lane 0
-// only; one copy of this code serves every call site.
-__device__ __noinline__ void pump_fn(WarpPlan *wp, const PumpCtx *px, const int *slot_e, uint8_t *ring,
-                                     uint64_t *bar, int warp, int limit) {
-    const int RW = px->RW, CH = px->CH;
-    while (wp->n_iss < limit) {
-        if (wp->left == 0) {
-            // start the next item of the list
-            int cph = wp->cph;
-            if (cph >= 3 || (cph >= 1 && !wp->routed)) break;
-            const int items = cph < 2 ? wp->my[cph] : wp->nrt * wp->perw;
-            if (wp->ci >= items) {
-                wp->cph = cph + 1;
-                wp->ci = 0;
-                wp->ri = wp->r2 = 0;
-                continue;
-            }
-            if (cph < 2) {
-                const int uu = wp->u0[cph] + wp->ci * wp->stride[cph];
-                const int s = uu / wp->NT[cph], r = uu - s * wp->NT[cph];
-                const int e = slot_e[wp->lo[cph] + s];
-                const uint8_t *b = e < 0 ? px->sw13r + (size_t)(-e - 1) * px->s13 : px->w13r + (size_t)e * px->e13;
-                wp->src = b + ((size_t)r * px->NC13 + wp->cb0[cph]) * kChunkBytes;
-                wp->left = wp->cpw[cph];
-            } else {
-                const int rt = px->c + wp->ri * px->G;
-                const int pi = warp + kFW * wp->r2;
-                const int e = slot_e[pi >> wp->lksd], kp = pi & ((1 << wp->lksd) - 1);
-                const int ncd = e < 0 ? px->ncs : px->ncr, cpk = ncd >> wp->lksd;
-                const uint8_t *b = e < 0 ? px->sw2r + (size_t)(-e - 1) * px->s2 : px->w2r + (size_t)e * px->e2;
-                wp->src = b + ((size_t)rt * ncd + kp * cpk) * kChunkBytes;
-                wp->left = cpk;
-                if (++wp->r2 == wp->perw) {
-                    wp->r2 = 0;
-                    ++wp->ri;
-                }
-            }
-            ++wp->ci;
+// Stage 1 of the top-k for one (token t, expert group grp): lane L holds
+// experts (grp * M + i) * 32 + L, i < M; the group's k best (key, id) go to
+// the token's candidate list in selection order.
+template <int M>
+__device__ __forceinline__ void topk_group(const float *logits, int t, int grp, int E, int K, int lane,
+                                           unsigned *cand) {
+    unsigned key[M], id[M], taken = 0u;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const int ee = (grp * M + i) * 32 + lane;
+        key[i] = 0u;
+        id[i] = 0xffffffffu;
+        if (ee < E) {
+            const float z = __ldcg(logits + (size_t)t * E + ee);
+            key[i] = isnan(z) ? 0u : __float_as_uint(__fdividef(1.0f, 1.0f + __expf(-z))) + 1u;
+            id[i] = (unsigned)ee;
         }
-        const int n = min(CH, wp->left);
-        const int sl = wp->sl;
-        fence_proxy_async();
-        mbar_expect_tx(bar + sl, (unsigned)(n * kChunkBytes));
-        bulk_g2s(ring + (size_t)sl * CH * kChunkBytes, wp->src, (unsigned)(n * kChunkBytes), bar + sl, px->pol);
-        wp->src += (size_t)n * kChunkBytes;
-        wp->left -= n;
-        wp->sl = sl + 1 == RW ? 0 : sl + 1;
-        ++wp->n_iss;
+    }
+#pragma unroll 1
+    for (int j = 0; j < K; ++j) {
+        unsigned mx, win;
+        select_round<M>(key, id, taken, mx, win);
+        if (lane == 0) {
+            cand[(t * kCandMax + grp * K + j) * 2] = mx;
+            cand[(t * kCandMax + grp * K + j) * 2 + 1] = win;
+        }
     }
 }
+
+// Per-warp copy list: the warp's items (gate/up units of pass 0, of pass 1,
+// then down pieces) as (first byte, chunk count), filled by the warp's lanes
+// in parallel; lane 0 walks it, cutting items into segments of <= CH chunks.
 
 template <int QP>
 __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, FusedGeom fg) {
@@ -365,12 +316,11 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     __shared__ __align__(8) uint64_t s_bar[kFW][kRWmax];
     __shared__ __align__(8) uint64_t s_rbar;   // router rows
     __shared__ __align__(8) uint64_t s_xbar;   // x
-    __shared__ PumpCtx s_px;
-    __shared__ WarpPlan s_wp[kFW];
+    __shared__ const uint8_t *s_tab_src[kFW][kTabMax];
+    __shared__ int s_tab_n[kFW][kTabMax];
     __shared__ float s_tmax[kFW][kTF];
     __shared__ int s_xexp[kTF];
     __shared__ unsigned s_epoch;
-    __shared__ float s_rb[kREmax];
     __shared__ int s_ids[kTF][kMaxTopK];
     __shared__ float s_w[kTF][kMaxTopK];
     __shared__ __align__(4) unsigned char s_tokmask[kMaxExperts];
@@ -394,66 +344,103 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     const float *s_router = reinterpret_cast<const float *>(smem + fg.router_off);
     unsigned *s_cand = reinterpret_cast<unsigned *>(smem + fg.cand_off);   // [T][kCandMax][key, id]
     const uint8_t *xraw = smem + fg.xraw_off;
+    const float4 *s_gsp = reinterpret_cast<const float4 *>(smem + fg.gs_off);  // copy of d.gsp
     uint8_t *ring = smem + fg.ring_off + (size_t)warp * RW * CH * kChunkBytes;
     uint64_t *bar = s_bar[warp];
-    WarpPlan &wp = s_wp[warp];
     const int NC13 = H / kChunkK;            // gate/up chunks per tile
     const int NTs = d.Is / 8, NT13 = d.I / 8, NRT = H / 16;
+    const uint64_t pol = evict_first_policy();
+
+    // ---- the copy issuer (lane 0's registers; the other lanes' copies idle) ----
+    int n_iss = 0, it = 0, n_known = 0, left = 0, sl_p = 0;
+    const uint8_t *src = nullptr;
+    auto pump = [&](int limit) {
+        if (lane != 0) return;
+        while (n_iss < limit) {
+            if (left == 0) {
+                if (it >= n_known) break;
+                src = s_tab_src[warp][it];
+                left = s_tab_n[warp][it];
+                ++it;
+            }
+            const int n = min(CH, left);
+            fence_proxy_async();
+            mbar_expect_tx(bar + sl_p, (unsigned)(n * kChunkBytes));
+            bulk_g2s(ring + (size_t)sl_p * CH * kChunkBytes, src, (unsigned)(n * kChunkBytes), bar + sl_p, pol);
+            src += (size_t)n * kChunkBytes;
+            left -= n;
+            sl_p = sl_p + 1 == RW ? 0 : sl_p + 1;
+            ++n_iss;
+        }
+    };
+    // gate/up plan of one pass: groups of 2^lks warps share a unit (slot lo +
+    // uu / NT, tile uu % NT) by splitting its K range; this warp's units are
+    // uu = u0 + i * stride, i < my, and its K range [cb0, cb0 + cpw)
+    struct Pass {
+        int lks, cpw, cb0, stride, u0, my, NT, lo;
+    };
+    auto plan = [&](int units, int lks, int NT, int lo) {
+        Pass p;
+        const int ngrp = kFW >> lks;
+        p.lks = lks;
+        p.cpw = NC13 >> lks;
+        p.cb0 = (warp & ((1 << lks) - 1)) * p.cpw;
+        p.stride = G * ngrp;
+        p.u0 = c * ngrp + (warp >> lks);
+        p.my = p.u0 < units ? (units - p.u0 + p.stride - 1) / p.stride : 0;
+        p.NT = NT;
+        p.lo = lo;
+        return p;
+    };
+    // lanes fill table entries [base, base + p.my) with the units of pass p
+    auto fill_units = [&](const Pass &p, int base) {
+        for (int i = lane; i < p.my; i += 32) {
+            const int uu = p.u0 + i * p.stride;
+            const int s = uu / p.NT, r = uu - s * p.NT;
+            const int e = s_slot_e[p.lo + s];
+            const uint8_t *b = e < 0 ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
+            s_tab_src[warp][base + i] = b + ((size_t)r * NC13 + p.cb0) * kChunkBytes;
+            s_tab_n[warp][base + i] = p.cpw;
+        }
+    };
 
     MOE_TRACE_POINT(0, 0);
-    // ---------------- A: static weights before the dependency wait ----------------
+    MOE_TRACE_CLOCK(1, 0);
+    // ---------------- A: static data before the dependency wait ----------------
     if (threadIdx.x < S) {
-        s_slot_e[threadIdx.x] = -(threadIdx.x + 1);
-        s_slot_mask[threadIdx.x] = (1 << T) - 1;
-        s_slot_p0[threadIdx.x] = threadIdx.x * T;
+        const int si = threadIdx.x;
+        s_slot_e[si] = -(si + 1);
+        s_slot_mask[si] = (1 << T) - 1;
+        s_slot_p0[si] = si * T;
     }
     if (threadIdx.x == 0) {
-        s_px.w13r = d.w13r;
-        s_px.w2r = d.w2r;
-        s_px.sw13r = d.sw13r;
-        s_px.sw2r = d.sw2r;
-        s_px.e13 = d.e13_stride;
-        s_px.e2 = d.e2_stride;
-        s_px.s13 = d.s13_stride;
-        s_px.s2 = d.s2_stride;
-        s_px.pol = evict_first_policy();
-        s_px.NC13 = NC13;
-        s_px.ncr = d.I / kChunkK;
-        s_px.ncs = d.Is / kChunkK;
-        s_px.RW = RW;
-        s_px.CH = CH;
-        s_px.G = G;
-        s_px.c = c;
         mbar_init(&s_rbar, 1);
         mbar_init(&s_xbar, 1);
     }
-    if (threadIdx.x >= 64 && threadIdx.x < 64 + kREmax) {
-        const int re = threadIdx.x - 64, e = c + re * G;
-        s_rb[re] = (re < kRE && e < E && d.router_b) ? d.router_b[e] : 0.f;
-    }
     if (lane == 0) {
-        plan_pass(wp, 0, S * NTs, NTs, 0, NC13, G, c, warp, fg.lks0, fg.spu[fg.lks0]);
-        wp.my[1] = 0;
-        wp.nrt = wp.perw = 0;
-        wp.lksd = 0;
-        wp.cph = wp.ci = wp.n_iss = wp.sl = wp.routed = wp.ri = wp.r2 = wp.left = 0;
         for (int i = 0; i < RW; ++i) mbar_init(bar + i, 1);
         fence_proxy_async();
     }
+    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0);
     __syncthreads();
+    fill_units(p0, 0);
+    __syncwarp();
+    n_known = p0.my;
     if (threadIdx.x == 0) {
-        // this block's router rows (static)
+        // static data: this block's router rows; the packed global scales
+        // and router biases of all experts
         const int nre = min(kRE, (E - c + G - 1) / G);
-        mbar_expect_tx(&s_rbar, (unsigned)(nre * H * 4));
+        mbar_expect_tx(&s_rbar, (unsigned)(nre * H * 4 + (E + S) * 16));
+        bulk_g2s(smem + fg.gs_off, d.gsp, (unsigned)((E + S) * 16), &s_rbar, pol);
 #pragma unroll 1
         for (int re = 0; re < nre; ++re)
             bulk_g2s(smem + fg.router_off + (size_t)re * H * 4, d.router_w + (size_t)(c + re * G) * H,
-                     (unsigned)(H * 4), &s_rbar, s_px.pol);
+                     (unsigned)(H * 4), &s_rbar, pol);
     } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S && c < NRT) {
         const int si = threadIdx.x - 32, ncs = d.Is / kChunkK;
         prefetch_l2(d.sw2r + (size_t)si * d.s2_stride + (size_t)c * ncs * kChunkBytes, (unsigned)(ncs * kChunkBytes));
     }
-    if (lane == 0) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, RW);
+    pump(RW);
     pdl_wait();
     pdl_trigger();
     MOE_TRACE_POINT(0, 1);
@@ -464,7 +451,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         s_epoch = __ldcg(d.epoch);
         // x (T rows, contiguous) in one bulk copy
         mbar_expect_tx(&s_xbar, (unsigned)(T * H * 2));
-        bulk_g2s(smem + fg.xraw_off, a.x, (unsigned)(T * H * 2), &s_xbar, s_px.pol);
+        bulk_g2s(smem + fg.xraw_off, a.x, (unsigned)(T * H * 2), &s_xbar, pol);
     }
     if (!mbar_wait(&s_xbar, 0u, d.err) || !mbar_wait(&s_rbar, 0u, d.err)) ok = false;
     const int nq = H / 4;                    // 4-element quads of an activation row
@@ -547,7 +534,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             float v = 0.f;
 #pragma unroll
             for (int w = 0; w < kFW; ++w) v += s_lpart[w][re][t];
-            d.logits[(size_t)t * E + e] = v + s_rb[re];
+            d.logits[(size_t)t * E + e] = v + s_gsp[e].w;
         }
     }
     gbar_arrive(d.bar_count);
@@ -558,8 +545,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     const uint8_t *xb = xs + (size_t)(g < T ? g : T) * fg.xrow + q * 32;
     int n_con = 0, sl_c = 0;             // segments consumed by this warp; its ring slot
     unsigned par_c = 0u;                 // and the slot's phase parity
+    int nslots = S, lksd = 0, perw = 0, nrt = 0;
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
+        Pass pp = p0;
         if (pass == 1) {
             MOE_TRACE_POINT(0, 4);
             ok = gbar_wait(d.bar_count, bar_base + (unsigned)G, d.err) && ok;
@@ -573,28 +562,11 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             // keeps its group's k best as candidates.
             if (warp < T * fg.gpt) {
                 const int t = warp / fg.gpt, grp = warp - t * fg.gpt;
-                unsigned key[kM1max], id[kM1max], taken = 0u;
-#pragma unroll
-                for (int i = 0; i < kM1max; ++i) {
-                    const int ee = (grp * fg.m1 + i) * 32 + lane;
-                    key[i] = 0u;
-                    id[i] = 0xffffffffu;
-                    if (i < fg.m1 && ee < E) {
-                        const float z = __ldcg(d.logits + (size_t)t * E + ee);
-                        key[i] = isnan(z) ? 0u : __float_as_uint(__fdividef(1.0f, 1.0f + __expf(-z))) + 1u;
-                        id[i] = (unsigned)ee;
-                    }
-                }
-                __syncwarp();
-                MOE_TRACE_POINT(0, 13);
-#pragma unroll 1
-                for (int j = 0; j < K; ++j) {
-                    unsigned mx, win;
-                    select_round<kM1max>(key, id, taken, mx, win);
-                    if (lane == 0) {
-                        s_cand[((t * kCandMax) + grp * K + j) * 2] = mx;
-                        s_cand[((t * kCandMax) + grp * K + j) * 2 + 1] = win;
-                    }
+                switch (fg.m1p) {
+                    case 1: topk_group<1>(d.logits, t, grp, E, K, lane, s_cand); break;
+                    case 2: topk_group<2>(d.logits, t, grp, E, K, lane, s_cand); break;
+                    case 4: topk_group<4>(d.logits, t, grp, E, K, lane, s_cand); break;
+                    default: topk_group<8>(d.logits, t, grp, E, K, lane, s_cand); break;
                 }
             }
             for (int i = threadIdx.x; i < E; i += kFT) s_tokmask[i] = 0;
@@ -665,10 +637,11 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                         cb += s_wsum[1][w];
                     }
                 if (msk) {
-                    s_slot_e[S + fb] = e;
-                    s_slot_mask[S + fb] = msk;
-                    s_slot_p0[S + fb] = S * T + cb;
-                    s_eslot[e] = (short)(S + fb);
+                    const int sl = S + fb;
+                    s_slot_e[sl] = e;
+                    s_slot_mask[sl] = msk;
+                    s_slot_p0[sl] = S * T + cb;
+                    s_eslot[e] = (short)sl;
                 }
                 if (threadIdx.x == kFT - 1) s_nslots = S + fb + (msk != 0);
                 __syncthreads();
@@ -680,31 +653,39 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 if (threadIdx.x < T * S) s_pw[threadIdx.x] = 1.0f;
             }
             MOE_TRACE_POINT(0, 12);
-            if (lane == 0) {
-                const int ns = s_nslots, l1 = fg.lks1[ns], ld = fg.lksd[ns];
-                plan_pass(wp, 1, (ns - S) * NT13, NT13, S, NC13, G, c, warp, l1, fg.spu[l1]);
-                wp.lksd = ld;
-                wp.perw = warp < (ns << ld) ? ((ns << ld) - warp + kFW - 1) / kFW : 0;
-                wp.nrt = c < NRT ? (NRT - c + G - 1) / G : 0;
-                wp.routed = 1;
-                if (ok) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, n_con + RW);
+            // this warp's routed units and down pieces -> its copy list
+            nslots = s_nslots;
+            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S);
+            fill_units(pp, p0.my);
+            lksd = fg.lksd[nslots];
+            perw = warp < (nslots << lksd) ? ((nslots << lksd) - warp + kFW - 1) / kFW : 0;
+            nrt = c < NRT ? (NRT - c + G - 1) / G : 0;
+            for (int i = lane; i < nrt * perw; i += 32) {
+                const int ri = i / perw, r2 = i - ri * perw;
+                const int rt = c + ri * G, pi = warp + kFW * r2;
+                const int e = s_slot_e[pi >> lksd], kp = pi & ((1 << lksd) - 1);
+                const int ncd = (e < 0 ? d.Is : d.I) / kChunkK, cpk = ncd >> lksd;
+                const uint8_t *b = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
+                s_tab_src[warp][p0.my + pp.my + i] = b + ((size_t)rt * ncd + kp * cpk) * kChunkBytes;
+                s_tab_n[warp][p0.my + pp.my + i] = cpk;
             }
+            __syncwarp();
+            n_known = p0.my + pp.my + nrt * perw;
+            if (ok) pump(n_con + RW);
             __syncwarp();
             MOE_TRACE_POINT(0, 6);
         }
-        const int lks = wp.lks[pass], cpw = wp.cpw[pass], cb0 = wp.cb0[pass], spu = wp.spu[pass];
-        const int my = wp.my[pass], u0 = wp.u0[pass], ustride = wp.stride[pass], NT = wp.NT[pass];
-        const int lo = wp.lo[pass], ks = 1 << lks, gi = warp >> lks, kw = warp & (ks - 1);
+        const int ks = 1 << pp.lks, gi = warp >> pp.lks, kw = warp & (ks - 1);
         // every warp of a group has the same unit count, so the group's named
         // barrier (id 1 + gi) is reached by all of its warps together
 #pragma unroll 1
-        for (int ui = 0; ui < my; ++ui) {
+        for (int ui = 0; ui < pp.my; ++ui) {
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint8_t *bp = xb + cb0 * 128;
-            int left = cpw;
+            const uint8_t *bp = xb + pp.cb0 * 128;
+            int lft = pp.cpw;
 #pragma unroll 1
-            for (int p = 0; p < spu; ++p) {
-                const int n = min(CH, left);
+            while (lft > 0) {
+                const int n = min(CH, lft);
                 if (ok && !mbar_wait(bar + sl_c, par_c, d.err)) ok = false;
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
@@ -713,18 +694,18 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
                 __syncwarp();
                 bp += n * 128;
-                left -= n;
+                lft -= n;
                 ++n_con;
                 if (++sl_c == RW) {
                     sl_c = 0;
                     par_c ^= 1u;
                 }
-                if (lane == 0 && ok) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, n_con + RW);
+                if (ok) pump(n_con + RW);
             }
 #pragma unroll
             for (int v = 0; v < 4; ++v) a0[v] += a1[v];
-            const int uu = u0 + ui * ustride;
-            const int s = uu / NT, r = uu - s * NT, slot = lo + s;
+            const int uu = pp.u0 + ui * pp.stride;
+            const int s = uu / pp.NT, r = uu - s * pp.NT, slot = pp.lo + s;
             if (ks > 1) {
 #pragma unroll
                 for (int v = 0; v < 4; ++v) s_red[warp][v][lane] = a0[v];
@@ -739,15 +720,14 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             }
             if (kw == 0 && ok) {
                 // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row 8r+g
-                const int e = s_slot_e[slot];
-                const int msk = s_slot_mask[slot], p0 = s_slot_p0[slot];
-                const float gsa = e < 0 ? d.sgs13[2 * (-e - 1)] : d.gs13[2 * e];
-                const float gsb = e < 0 ? d.sgs13[2 * (-e - 1) + 1] : d.gs13[2 * e + 1];
+                const int e = s_slot_e[slot], msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
+                const float4 gsv = s_gsp[e < 0 ? E - e - 1 : e];
+                const float gsa = gsv.x, gsb = gsv.y;
 #pragma unroll
                 for (int e2 = 0; e2 < 2; ++e2) {
                     const int t = 2 * q + e2;
                     const bool on = t < T && ((msk >> t) & 1);
-                    const int p = p0 + __popc(msk & ((1 << t) - 1));
+                    const int p = p0s + __popc(msk & ((1 << t) - 1));
                     float habs = 0.f;
                     if (on) {
                         const float un = pow2f(s_xexp[t]);
@@ -768,7 +748,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     gbar_arrive(d.bar_count);
     ok = gbar_wait(d.bar_count, bar_base + 2u * (unsigned)G, d.err) && ok;
     if (!__syncthreads_and(ok)) {
-        drain_ring(bar, RW, n_con, lane == 0 ? wp.n_iss : 0, lane);
+        drain_ring(bar, RW, n_con, n_iss, lane);
         if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;
         return;
     }
@@ -817,7 +797,6 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     }
     __syncthreads();
     MOE_TRACE_POINT(0, 14);
-    const int nrt = wp.nrt, perw = wp.perw, lksd = wp.lksd;
 #pragma unroll 1
     for (int ri = 0; ri < nrt; ++ri) {
         const int rt = c + ri * G;
@@ -827,15 +806,16 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             const int pi = warp + kFW * r2;
             const int slot = pi >> lksd, kp = pi & ((1 << lksd) - 1);
             const int e = s_slot_e[slot];
-            const int msk = s_slot_mask[slot], p0 = s_slot_p0[slot];
+            const int msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
+            const float gs = s_gsp[e < 0 ? E - e - 1 : e].z;
             const int cpk = (e < 0 ? d.Is : d.I) / kChunkK >> lksd;
-            const int row = ((msk >> g) & 1) ? p0 + __popc(msk & ((1 << g) - 1)) : npairs;
+            const int row = ((msk >> g) & 1) ? p0s + __popc(msk & ((1 << g) - 1)) : npairs;
             const uint8_t *bp = hs + (size_t)row * fg.hrow + q * 32 + kp * cpk * 128;
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-            int left = cpk;
+            int lft = cpk;
 #pragma unroll 1
-            while (left > 0) {
-                const int n = min(CH, left);
+            while (lft > 0) {
+                const int n = min(CH, lft);
                 if (ok && !mbar_wait(bar + sl_c, par_c, d.err)) ok = false;
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
@@ -844,21 +824,20 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
                 __syncwarp();
                 bp += n * 128;
-                left -= n;
+                lft -= n;
                 ++n_con;
                 if (++sl_c == RW) {
                     sl_c = 0;
                     par_c ^= 1u;
                 }
-                if (lane == 0 && ok) pump_fn(&wp, &s_px, s_slot_e, ring, bar, warp, n_con + RW);
+                if (ok) pump(n_con + RW);
             }
             // y = gs * 2^hexp * acc, weighted into the per-token accumulator
-            const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
                 const int t = 2 * q + e2;
                 if (t < T && ((msk >> t) & 1)) {
-                    const int p = p0 + __popc(msk & ((1 << t) - 1));
+                    const int p = p0s + __popc(msk & ((1 << t) - 1));
                     const float wgt = s_pw[p] * gs * s_hun[p];
                     oa[e2] = fmaf(wgt, a0[e2] + a1[e2], oa[e2]);
                     oa[2 + e2] = fmaf(wgt, a0[2 + e2] + a1[2 + e2], oa[2 + e2]);
@@ -887,8 +866,9 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         }
         __syncthreads();
     }
-    if (!ok) drain_ring(bar, RW, n_con, lane == 0 ? wp.n_iss : 0, lane);
+    if (!ok) drain_ring(bar, RW, n_con, n_iss, lane);
     MOE_TRACE_POINT(0, 9);
+    MOE_TRACE_CLOCK(1, 9);
     if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;
 }
 

@@ -65,6 +65,8 @@ struct DevLayer {
     const uint8_t *sw2r;
     const float *sgs13;             // [S,2]
     const float *sgs2;              // [S]
+    const float4 *gsp;              // [E+S] per expert: gate gs, up gs, down gs, router bias
+                                    //   (routed experts first, then the shared ones; bias 0 for those)
     size_t e13_stride, e2_stride;   // bytes per routed expert
     size_t s13_stride, s2_stride;   // bytes per shared expert
     // workspace (device)
@@ -106,6 +108,7 @@ cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_
 int fused_blocks_per_sm(const DevLayer &d, int T);
 cudaError_t launch_repack(const uint8_t *codes, const uint8_t *sf, int n_mats, int rows, int cols,
                           bool gate_up, uint8_t *dst, cudaStream_t s);
+cudaError_t launch_pack_scales(const DevLayer &d, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t *rep, float gs_a, float gs_b, int rows, int cols,
                            bool gate_up, float *dst, cudaStream_t s);
 
@@ -143,8 +146,20 @@ __host__ __device__ inline size_t repacked_bytes(int rows, int cols) {
             if (b_ < d.trace_blocks) d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = t_; \
         }                                                                                        \
     } while (0)
+// SM cycle counter at a point, stored under kernel slot `kid` (pairs with
+// the timestamps of another slot to give the effective SM clock).
+#define MOE_TRACE_CLOCK(kid, i)                                                                  \
+    do {                                                                                         \
+        if (threadIdx.x == 0 && d.trace) {                                                       \
+            const int b_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
+            if (b_ < d.trace_blocks) d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = clock64(); \
+        }                                                                                        \
+    } while (0)
 #else
 #define MOE_TRACE_POINT(kid, i) \
+    do {                        \
+    } while (0)
+#define MOE_TRACE_CLOCK(kid, i) \
     do {                        \
     } while (0)
 #endif

@@ -81,7 +81,28 @@ __global__ void dequant_kernel(const uint8_t *__restrict__ rep, float gs_a, floa
     }
 }
 
+// One 16-byte record per expert (routed, then shared): the global scales of
+// gate, up and down and the router bias, so that a block fetches them all
+// with one bulk copy.
+__global__ void pack_scales_kernel(DevLayer d) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= d.E + d.S) return;
+    float4 v;
+    if (i < d.E) {
+        v = make_float4(d.gs13[2 * i], d.gs13[2 * i + 1], d.gs2[i], d.router_b ? d.router_b[i] : 0.f);
+    } else {
+        const int si = i - d.E;
+        v = make_float4(d.sgs13[2 * si], d.sgs13[2 * si + 1], d.sgs2[si], 0.f);
+    }
+    const_cast<float4 *>(d.gsp)[i] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_pack_scales(const DevLayer &d, cudaStream_t s) {
+    pack_scales_kernel<<<(d.E + d.S + 255) / 256, 256, 0, s>>>(d);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_repack(const uint8_t *codes, const uint8_t *sf, int n_mats, int rows, int cols,
                           bool gate_up, uint8_t *dst, cudaStream_t s) {
