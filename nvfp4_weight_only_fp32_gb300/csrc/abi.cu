@@ -172,6 +172,10 @@ void carve_workspace(moe_layer *L, char *base) {
     d.hmax64 = cv.take<unsigned long long>(d.max_pairs);
     d.epoch = cv.take<unsigned>(1);
     d.bar_count = cv.take<unsigned>(1);
+    d.nhot = cv.take<int>(1);
+    d.hot_slots = cv.take<int>(d.max_slots);
+    d.tg_ticket = cv.take<unsigned>(Tm);
+    d.emask = cv.take<unsigned long long>(E);
     L->x_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->out_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->ids_stage = cv.take<int>((size_t)Tm * K);
@@ -257,6 +261,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     d.max_slots = std::min(E, cfg->max_tokens * K) + S;
     d.max_pairs = cfg->max_tokens * (K + S);
     d.Imax = std::max(I, Is);
+    d.grouped_min = 0;   // set once the shape is known to suit the grouped kernels
 
     carve_weights(L, nullptr);
     carve_workspace(L, nullptr);
@@ -317,6 +322,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     if (e == cudaSuccess) e = prepare_kernels();
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->optin_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (L->cfg.grouped_min_tokens > 0 && grouped_supported(d)) d.grouped_min = L->cfg.grouped_min_tokens;
     for (int T = 0; T <= kMaxTokens; ++T) {
         L->fused_ok[T] = 0;
         if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&
@@ -359,8 +365,12 @@ moe_status moe_stage_gate_up(moe_layer *L, const void *x, int T, void *stream) {
     if (rc != MOE_OK) return rc;
     if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
-    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T,
-                                   reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, st);
+    // above 8 tokens the GEMV kernel leaves the slots with >= grouped_min
+    // tokens to the grouped tensor-core kernel
+    if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)
+        e = launch_grouped_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, L->sm_count, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gate/up launch");
 }
 
@@ -369,8 +379,10 @@ moe_status moe_stage_down(moe_layer *L, int T, void *out, void *stream) {
     if (rc != MOE_OK) return rc;
     if (!out || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "out is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
-    cudaError_t e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out),
-                                reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out), st);
+    if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)
+        e = launch_grouped_down(L->d, T, static_cast<__nv_bfloat16 *>(out), L->sm_count, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");
 }
 

@@ -256,27 +256,6 @@ __device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, cons
     mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
 }
 
-// One round of warp-wide selection among up to M items per lane: the largest
-// key, the lowest id among equal keys; the winning item is marked taken.
-// Keys: bits(sigmoid score) + 1 (order-preserving for scores in [0, 1]), 0
-// for NaN; ids of empty places are 0xffffffff.
-template <int M>
-__device__ __forceinline__ void select_round(const unsigned (&key)[M], const unsigned (&id)[M], unsigned &taken,
-                                             unsigned &mx, unsigned &win) {
-    unsigned bk = 0u, bi = 0xffffffffu;
-#pragma unroll
-    for (int i = 0; i < M; ++i)
-        if (!((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && id[i] < bi))) {
-            bk = key[i];
-            bi = id[i];
-        }
-    mx = __reduce_max_sync(0xffffffffu, bk);
-    win = __reduce_min_sync(0xffffffffu, bk == mx ? bi : 0xffffffffu);
-#pragma unroll
-    for (int i = 0; i < M; ++i)
-        if (id[i] == win) taken |= 1u << i;
-}
-
 // Stage 1 of the top-k for one (token t, expert group grp): lane L holds
 // experts (grp * M + i) * 32 + L, i < M; the group's k best (key, id) go to
 // the token's candidate list in selection order.
@@ -291,7 +270,7 @@ __device__ __forceinline__ void topk_group(const float *logits, int t, int grp, 
         id[i] = 0xffffffffu;
         if (ee < E) {
             const float z = __ldcg(logits + (size_t)t * E + ee);
-            key[i] = isnan(z) ? 0u : __float_as_uint(__fdividef(1.0f, 1.0f + __expf(-z))) + 1u;
+            key[i] = isnan(z) ? 0u : __float_as_uint(1.0f / (1.0f + expf(-z))) + 1u;
             id[i] = (unsigned)ee;
         }
     }

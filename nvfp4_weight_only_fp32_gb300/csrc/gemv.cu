@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     };
 
     if (MODE == 0) {
+        if (shared && GMAX > 1 && d.grouped_min > 0 && T >= d.grouped_min) return;   // grouped kernel's
         if (shared) {
             // Shared experts do not depend on routing: stream them now.
             m = T;
@@ -172,6 +173,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
                 return;
             }
             m = __ldcg(d.slot_m + s);
+            if (GMAX > 1 && d.grouped_min > 0 && m >= d.grouped_min) {   // grouped kernel's
+                pdl_trigger();
+                return;
+            }
             p0 = __ldcg(d.slot_p0 + s);
             slot_geometry(__ldcg(d.slot_expert + s));
             if (r < NT)
@@ -188,6 +193,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
             return;
         }
         m = __ldcg(d.slot_m + s);
+        if (GMAX > 1 && d.grouped_min > 0 && m >= d.grouped_min) return;   // grouped kernel's (and its ticket)
         p0 = __ldcg(d.slot_p0 + s);
         slot_geometry(__ldcg(d.slot_expert + s));
         if (r < NT)
@@ -353,35 +359,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     if (!s_last) return;
     __threadfence();
 
-    const int K = d.k, P = d.k + d.S;
     int *s_pair = reinterpret_cast<int *>(smem);                       // [T, P]
     float *s_pw = reinterpret_cast<float *>(smem + (size_t)kMaxTokens * 16 * sizeof(int));
-    for (int i = threadIdx.x; i < T * P; i += kThreads) {
-        const int p = __ldcg(d.pair_of + i);
-        s_pair[i] = p;
-        s_pw[i] = (i % P) < K ? __ldcg(d.pair_w + p) : 1.0f;
-    }
-    __syncthreads();
     const int row0 = blockIdx.x * tpc * 16;
-    const int nq = (min(d.H, row0 + tpc * 16) - row0) / 4;
-    for (int it = threadIdx.x; it < T * nq; it += kThreads) {
-        const int t = it / nq, m4 = row0 / 4 + (it - t * nq);
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < P; ++j) {
-            const float w = s_pw[t * P + j];
-            const float4 y = __ldcg(reinterpret_cast<const float4 *>(d.y_ws + (size_t)s_pair[t * P + j] * d.H) + m4);
-            a.x = fmaf(w, y.x, a.x);
-            a.y = fmaf(w, y.y, a.y);
-            a.z = fmaf(w, y.z, a.z);
-            a.w = fmaf(w, y.w, a.w);
-        }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
-        uint2 v;
-        v.x = *reinterpret_cast<uint32_t *>(&lo);
-        v.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(out + (size_t)t * d.H + 4 * m4) = v;
-    }
+    combine_rows(d, T, out, row0, min(d.H, row0 + tpc * 16) - row0, s_pair, s_pw, threadIdx.x, kThreads,
+                 [] { __syncthreads(); });
     if (threadIdx.x == 0) d.down_cnt[blockIdx.x] = 0u;
     MOE_TRACE_POINT(2, 7);
 }
@@ -447,6 +429,7 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
     if (e == cudaSuccess) e = prepare_route_kernel(optin);
     if (e == cudaSuccess) e = prepare_fused_kernel(optin);
+    if (e == cudaSuccess) e = prepare_grouped_kernels(optin);
     return e;
 }
 

@@ -1,0 +1,453 @@
+// grouped.cu -- row a6: the experts that many tokens selected (and the shared
+// experts) as dense tensor-core contractions, for steps with more than 8
+// tokens.
+//
+// Sources: "vLLM Day-0 support for Recursive's Flint", "Optimisation strategy"
+// (the GEMV kernels are the small-batch path; above it the MoE layer runs as
+// grouped GEMMs over the tokens each expert received); "Inkling 2 Small on
+// vLLM: Day-0 Support", "vLLM integration and optimisation" (SwiGLU between
+// gate/up and down; NVFP4 weights with 16-element E4M3 block scales).
+//
+// A work item is (hot slot, M-tile of 128 weight rows = 8 repacked 16-row
+// tiles); blocks loop over items.  Per 64-wide K chunk:
+//   warps 0-7   each decode one 16-row tile's 576-byte chunk (E2M1 x E4M3,
+//               exact in f16) straight into the A stage, laid out as the
+//               tensor core's K-major operand without swizzle: 8x8 core
+//               matrices of 128 contiguous bytes, K-adjacent ones 128 bytes
+//               apart (LBO), row-adjacent ones 1024 bytes apart (SBO);
+//   warps 8-11  stage the slot's m tokens (gate/up: x rows times 2^-xexp;
+//               down: h rows times 2^-hexp, both exact in f16) as the B
+//               operand in the same layout, rows >= m zero;
+//   warp 12     lane 0 issues four tcgen05.mma kind::f16 (M=128, N=m rounded
+//               up to 16, K=16) into a TMEM accumulator and commits them to
+//               the stage's "empty" mbarrier; after the last chunk a commit
+//               to the accumulator barrier.
+// Three stages ring between producers and the MMA issuer.  Warps 0-7 then
+// read the accumulator (tcgen05.ld, warp w owns TMEM lanes 32(w%4).. and
+// half of the columns) and run the epilogue:
+//   gate/up  rows 16j+r (r < 8) are gate, 16j+r+8 the matching up rows
+//            (the repacked tile order), so SwiGLU pairs lanes L and L+8;
+//            h = bf16(silu(g) * u) goes to the workspace with the per-pair
+//            max |h|, as in the GEMV path;
+//   down     y = gs * 2^hexp * acc into the FP32 workspace; the block that
+//            completes a 128-row group last (shared ticket with the GEMV
+//            down kernel) runs the routing-weighted combine for those rows.
+// Every mbarrier wait gives up after about a second (sticky error word and a
+// shared abort flag that releases the other roles); the TMEM columns are
+// released on every exit path.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kDecW = 8;                          // decode / epilogue warps
+constexpr int kStgW = 4;                          // B staging warps
+constexpr int kMmaW = kDecW + kStgW;              // MMA-issuing warp
+constexpr int kGW = kMmaW + 1;
+constexpr int kGT = 32 * kGW;
+constexpr int kNS = 3;                            // pipeline stages
+constexpr int kMT = 128;                          // weight rows per item (8 tiles)
+constexpr int kNmax = kMaxTokens;                 // tokens per slot
+constexpr uint32_t kLBO = 128;                    // K-adjacent core matrices
+constexpr uint32_t kSBO = 8 * 128;                // row-adjacent core matrices (8 K-groups per row group)
+constexpr int kAStage = kMT * kChunkK * 2;        // 16 KB
+constexpr int kBStage = kNmax * kChunkK * 2;      // 8 KB
+constexpr int kScratch = kMaxTokens * (kMaxTopK + kMaxShared) * 8;   // combine's pair table
+constexpr int kSmem = kNS * (kAStage + kBStage) + kScratch;
+constexpr uint32_t kTmemCols = 64;                // >= N, a power of two >= 32
+constexpr unsigned long long kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// No-swizzle K-major shared-memory operand descriptor (tcgen05): start
+// address, leading (K) and stride (row) byte offsets, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(kLBO >> 4) << 16) | ((uint64_t)(kSBO >> 4) << 32) |
+           (1ull << 46);
+}
+
+// Instruction descriptor: kind::f16, A = B = f16, D = f32, both K-major.
+__device__ __forceinline__ uint32_t instr_desc(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(b)) : "memory");
+}
+
+// Bounded wait; gives up (error word, abort flag) after kWaitNs or as soon
+// as another role has given up.
+__device__ __forceinline__ bool gwait(uint64_t *b, unsigned parity, volatile int *abort, int *err) {
+    if (mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = gtimer();
+    while (!mbar_try_wait(b, parity)) {
+        if (*abort) return false;
+        if (gtimer() - t0 > kWaitNs) {
+            *abort = 1;
+            atomicExch(err, 1);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+
+// 16 consecutive accumulator columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ int hexp_of(unsigned bits) {
+    const float v = __uint_as_float(bits);
+    return (v > 0.f && isfinite(v)) ? max(0, ilogbf(v) - 14) : 0;
+}
+
+template <int MODE>   // 0 gate/up + SwiGLU, 1 down + combine
+__global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x, int T,
+                                                         __nv_bfloat16 *__restrict__ out) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ __align__(8) uint64_t s_full[kNS], s_empty[kNS], s_accf, s_acce;
+    __shared__ uint32_t s_taddr;
+    __shared__ int s_abort;
+    __shared__ int s_last;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + kNS * kAStage;
+    int *s_pair = reinterpret_cast<int *>(smem + kNS * (kAStage + kBStage));
+    float *s_pw = reinterpret_cast<float *>(smem + kNS * (kAStage + kBStage) + kScratch / 2);
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&s_full[i], kDecW + kStgW);
+            mbar_init(&s_empty[i], 1);
+        }
+        mbar_init(&s_accf, 1);
+        mbar_init(&s_acce, kDecW);
+        s_abort = 0;
+        fence_proxy_async();
+    }
+    if (warp == kMmaW) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_taddr)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = s_taddr;
+
+    pdl_wait();
+    pdl_trigger();
+    const int nhot = __ldcg(d.nhot);
+    const int ns = __ldcg(d.nslots);
+    const int MTper = MODE == 0 ? d.I / 64 : d.H / kMT;   // M-tiles per routed slot (shared: Is / 64 for gate/up)
+    const int MTs = MODE == 0 ? d.Is / 64 : d.H / kMT;
+    // items: hot slots in order, each with its M-tiles; a shared slot has
+    // MTs tiles, a routed one MTper (equal for down)
+    int nitems = 0;
+    if (MODE == 0) {
+        // hot slots are listed in slot order and the shared ones come first
+        for (int h = 0; h < nhot; ++h) nitems += __ldcg(d.hot_slots + h) < d.S ? MTs : MTper;
+    } else {
+        nitems = nhot * MTper;
+    }
+    const uint64_t pol = evict_first_policy();
+
+    int gc = 0;        // chunks through the ring so far (all items of this block)
+    int nloc = 0;      // items of this block so far
+#pragma unroll 1
+    for (int it = blockIdx.x; it < nitems; it += gridDim.x, ++nloc) {
+        // (every role runs every item, so that the epilogue warps' named
+        // barriers stay matched; after an abort the waits return at once)
+        // item -> (hot slot, M-tile)
+        int h = 0, mt = it;
+        if (MODE == 0) {
+#pragma unroll 1
+            for (;; ++h) {
+                const int n = __ldcg(d.hot_slots + h) < d.S ? MTs : MTper;
+                if (mt < n) break;
+                mt -= n;
+            }
+        } else {
+            h = it / MTper;
+            mt = it - h * MTper;
+        }
+        const int slot = __ldcg(d.hot_slots + h);
+        const int e = __ldcg(d.slot_expert + slot);
+        const int m = __ldcg(d.slot_m + slot);
+        const int p0 = __ldcg(d.slot_p0 + slot);
+        const int N = (m + 15) & ~15;
+        const bool shared = e < 0;
+        const int Islot = shared ? d.Is : d.I;
+        const int NC = MODE == 0 ? d.H / kChunkK : Islot / kChunkK;     // K chunks
+        const uint8_t *wbase;
+        float gs0, gs1;
+        if (MODE == 0) {
+            wbase = shared ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
+            gs0 = shared ? d.sgs13[2 * (-e - 1)] : d.gs13[2 * e];
+            gs1 = shared ? d.sgs13[2 * (-e - 1) + 1] : d.gs13[2 * e + 1];
+        } else {
+            wbase = shared ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
+            gs0 = shared ? d.sgs2[-e - 1] : d.gs2[e];
+            gs1 = 0.f;
+        }
+
+        if (warp < kDecW) {
+            // ---- A producer: tile 8mt + warp, chunk by chunk ----
+            const uint8_t *tb = wbase + (size_t)(8 * mt + warp) * NC * kChunkBytes;
+            uint4 cw;
+            uint2 sw;
+            load_chunk(tb, 0, lane, cw, sw, pol);
+#pragma unroll 1
+            for (int c = 0; c < NC; ++c) {
+                const int gcc = gc + c, st = gcc % kNS;
+                uint4 ncw = cw;
+                uint2 nsw = sw;
+                if (c + 1 < NC) load_chunk(tb, c + 1, lane, ncw, nsw, pol);
+                if (!gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err)) break;
+                uint32_t a[4][4];
+                decode_chunk(cw, sw, a);
+                uint8_t *As = sA + (size_t)st * kAStage + g * 16 + q * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * kSBO + (2 * i + (b >> 1)) * kLBO) =
+                            a[i][b];
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_full[st]);
+                cw = ncw;
+                sw = nsw;
+            }
+        } else if (warp < kMmaW) {
+            // ---- B producer: the slot's m tokens, rows >= m zero ----
+            const int tb = threadIdx.x - 32 * kDecW;      // 0..127
+            const int kg = tb & 7;                        // K group of this thread's pieces
+            const uint4 *src[4];
+            float sc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int n = (tb >> 3) + 16 * u;
+                src[u] = nullptr;
+                sc[u] = 0.f;
+                if (n < m) {
+                    if (MODE == 0) {
+                        const int tok = shared ? n : __ldcg(d.pair_tok + p0 + n);
+                        src[u] = reinterpret_cast<const uint4 *>(x + (size_t)tok * d.H);
+                        sc[u] = pow2f(-__ldcg(d.xexp + tok));
+                    } else {
+                        src[u] = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)(p0 + n) * d.Imax);
+                        sc[u] = pow2f(-hexp_of(__ldcg(d.hmax + p0 + n)));
+                    }
+                }
+            }
+#pragma unroll 1
+            for (int c = 0; c < NC; ++c) {
+                const int gcc = gc + c, st = gcc % kNS;
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = src[u] ? __ldcg(src[u] + c * 8 + kg) : make_uint4(0u, 0u, 0u, 0u);
+                if (!gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err)) break;
+                uint8_t *Bs = sB + (size_t)st * kBStage;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int n = (tb >> 3) + 16 * u;
+                    if (n < N) {
+                        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                        uint4 o;
+                        uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
+                                               __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
+                        *reinterpret_cast<uint4 *>(Bs + (n >> 3) * kSBO + kg * kLBO + (n & 7) * 16) = o;
+                    }
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_full[st]);
+            }
+        } else if (lane == 0) {
+            // ---- MMA issuer ----
+            const uint32_t idesc = instr_desc(kMT, N);
+            bool go = gwait(&s_acce, ((unsigned)nloc & 1u) ^ 1u, abort, d.err);   // accumulator read out
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < NC && go; ++c) {
+                const int gcc = gc + c, st = gcc % kNS;
+                if (!gwait(&s_full[st], (unsigned)(gcc / kNS) & 1u, abort, d.err)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + (size_t)st * kAStage), b0 = smem_u32(sB + (size_t)st * kBStage);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t da = smem_desc(a0 + ks * 2 * kLBO), db = smem_desc(b0 + ks * 2 * kLBO);
+                    const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(taddr),
+                        "l"(da), "l"(db), "r"(idesc), "r"(acc)
+                        : "memory");
+                }
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                                 smem_u32(&s_empty[st]))
+                             : "memory");
+            }
+            if (go)
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                                 smem_u32(&s_accf))
+                             : "memory");
+        }
+        gc += NC;
+
+        // ---- epilogue: warps 0-7 ----
+        if (warp < kDecW) {
+            const bool ok = gwait(&s_accf, (unsigned)nloc & 1u, abort, d.err);
+            tc_fence_after();
+            const int qd = warp & 3, half = warp >> 2;
+            float v[32];
+            if (ok) {
+                const uint32_t ta = taddr + ((uint32_t)(32 * qd) << 16) + (uint32_t)(32 * half);
+                if (32 * half < N) {
+                    float t16[16];
+                    tmem_ld16(ta, t16);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = t16[i];
+                    if (32 * half + 16 < N) {
+                        tmem_ld16(ta + 16, t16);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[16 + i] = t16[i];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_acce);
+            if (ok && 32 * half < N) {
+                const int row = 32 * qd + lane;            // row of the M-tile
+                if (MODE == 0) {
+                    const int j = row >> 4, rr = row & 15;
+                    const int n_int = 8 * (8 * mt + j) + (rr & 7);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = 32 * half + i;
+                        const float up = __shfl_down_sync(0xffffffffu, v[i], 8);
+                        float habs = 0.f;
+                        if (col < m && rr < 8) {
+                            const int p = p0 + col;
+                            const int tok = shared ? col : __ldcg(d.pair_tok + p);
+                            const float un = pow2f(__ldcg(d.xexp + tok));
+                            const float gt = v[i] * gs0 * un, uv = up * gs1 * un;
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * uv);
+                            d.h_ws[(size_t)p * d.Imax + n_int] = hb;
+                            habs = fabsf(__bfloat162float(hb));
+                        }
+                        habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, 1));
+                        habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, 2));
+                        habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, 4));
+                        if (col < m && (lane & 15) == 0) atomicMax(d.hmax + p0 + col, __float_as_uint(habs));
+                    }
+                } else {
+                    const int orow = kMT * mt + row;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = 32 * half + i;
+                        if (col < m) {
+                            const int p = p0 + col;
+                            d.y_ws[(size_t)p * d.H + orow] = v[i] * gs0 * pow2f(hexp_of(__ldcg(d.hmax + p)));
+                        }
+                    }
+                }
+            }
+            if (MODE == 1) {
+                // ticket shared with the GEMV down kernel: ns arrivals per
+                // 128-row group; the last one combines those rows
+                asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    s_last = !*abort && atomicAdd(d.down_cnt + mt, 1u) == (unsigned)(ns - 1);
+                }
+                asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+                if (s_last) {
+                    __threadfence();
+                    combine_rows(d, T, out, kMT * mt, kMT, s_pair, s_pw, threadIdx.x, 32 * kDecW,
+                                 [] { asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory"); });
+                    if (threadIdx.x == 0) d.down_cnt[mt] = 0u;
+                }
+                asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+            }
+        }
+    }
+    // the issuer's last commit covers all of its MMAs: wait for it before
+    // the columns are released
+    if (warp == kMmaW && lane == 0 && nloc > 0 && !*abort)
+        gwait(&s_accf, (unsigned)(nloc - 1) & 1u, abort, d.err);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaW)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(kTmemCols) : "memory");
+}
+
+template <int MODE>
+cudaError_t launch_g(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int sm_count,
+                     cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sm_count);
+    cfg.blockDim = dim3(kGT);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_kernel<MODE>, d, x, T, out);
+}
+
+}  // namespace
+
+// Shapes the grouped kernels take: 128-row M-tiles of every matrix (I, Is
+// multiples of 64 for gate/up's interleaved tiles, H of 128 for down).
+bool grouped_supported(const DevLayer &d) {
+    return d.H % kMT == 0 && d.I % 64 == 0 && (d.S == 0 || d.Is % 64 == 0) && d.max_tokens <= kNmax;
+}
+
+cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s) {
+    return launch_g<0>(d, x, T, nullptr, sm_count, s);
+}
+
+cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, cudaStream_t s) {
+    return launch_g<1>(d, nullptr, T, out, sm_count, s);
+}
+
+cudaError_t prepare_grouped_kernels(int optin_bytes) {
+    (void)optin_bytes;
+    cudaError_t e = cudaFuncSetAttribute(grouped_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    return e;
+}
+
+}  // namespace moe

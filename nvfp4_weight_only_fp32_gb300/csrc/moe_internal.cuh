@@ -90,6 +90,11 @@ struct DevLayer {
     unsigned long long *hmax64;     // [max_pairs] single-launch path: (epoch << 32) | max|h| bits
     unsigned *epoch;                // [1] call counter of the single-launch path
     unsigned *bar_count;            // [1] grid barrier arrivals (2 * grid size per call)
+    int grouped_min;                // slots with >= this many tokens use the grouped kernels (0: none)
+    int *nhot;                      // [1] number of such slots
+    int *hot_slots;                 // [max_slots] their slot indices, ascending
+    unsigned *tg_ticket;            // [max_tokens] router: arrivals per token group
+    unsigned long long *emask;      // [E] router: tokens that selected each expert (bit t)
     unsigned long long *trace;      // traced build only: phase timestamps
     int trace_blocks;
 };
@@ -101,6 +106,10 @@ cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *
                          float *w_out, cudaStream_t s);
 cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s);
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s);
+bool grouped_supported(const DevLayer &d);
+cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s);
+cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, cudaStream_t s);
+cudaError_t prepare_grouped_kernels(int optin_bytes);
 cudaError_t prepare_kernels();   // per device, once: shared-memory limits
 bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem);
 cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
@@ -306,6 +315,64 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
 }
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// One round of warp-wide selection among up to M items per lane: the largest
+// key, the lowest id among equal keys; the winning item is marked taken.
+// Keys: bits(sigmoid score) + 1 (order-preserving for scores in [0, 1]), 0
+// for NaN; ids of empty places are 0xffffffff.
+template <int M>
+__device__ __forceinline__ void select_round(const unsigned (&key)[M], const unsigned (&id)[M], unsigned &taken,
+                                             unsigned &mx, unsigned &win) {
+    unsigned bk = 0u, bi = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (!((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && id[i] < bi))) {
+            bk = key[i];
+            bi = id[i];
+        }
+    mx = __reduce_max_sync(0xffffffffu, bk);
+    win = __reduce_min_sync(0xffffffffu, bk == mx ? bi : 0xffffffffu);
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (id[i] == win) taken |= 1u << i;
+}
+
+// Routing-weighted combine of output rows [row0, row0 + nrows) for all T
+// tokens: out[t, m] = bf16(sum_j w[t, j] * y[pair(t, j), m] + sum_s y[pair(t,
+// k + s), m]), FP32 in a fixed order (routed slots in selection order, then
+// the shared ones).  Run by threads tid = 0..nthr-1 of the calling block;
+// `sync` synchronises exactly those threads.  s_pair/s_pw: shared scratch of
+// T * (k + S) entries each.
+template <class Sync>
+__device__ __forceinline__ void combine_rows(const DevLayer &d, int T, __nv_bfloat16 *out, int row0, int nrows,
+                                             int *s_pair, float *s_pw, int tid, int nthr, Sync sync) {
+    const int K = d.k, P = d.k + d.S;
+    for (int i = tid; i < T * P; i += nthr) {
+        const int p = __ldcg(d.pair_of + i);
+        s_pair[i] = p;
+        s_pw[i] = (i % P) < K ? __ldcg(d.pair_w + p) : 1.0f;
+    }
+    sync();
+    const int nq = nrows / 4;
+    for (int it = tid; it < T * nq; it += nthr) {
+        const int t = it / nq, m4 = row0 / 4 + (it - t * nq);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < P; ++j) {
+            const float w = s_pw[t * P + j];
+            const float4 y = __ldcg(reinterpret_cast<const float4 *>(d.y_ws + (size_t)s_pair[t * P + j] * d.H) + m4);
+            a.x = fmaf(w, y.x, a.x);
+            a.y = fmaf(w, y.y, a.y);
+            a.z = fmaf(w, y.z, a.z);
+            a.w = fmaf(w, y.w, a.w);
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t *>(&lo);
+        v.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(out + (size_t)t * d.H + 4 * m4) = v;
+    }
 }
 
 // Decode one chunk's A fragments for one lane: 4 blocks x 4 registers.

@@ -1,6 +1,7 @@
 // route.cu -- rows a1 + a2: FP32 router GEMV, sigmoid, top-k with
 // lowest-index tie-break, weight normalisation, and the work list of the
-// distinct selected experts.
+// distinct selected experts (the three-kernel chain; the single launch has its
+// own copy of these steps).
 //
 // Sources: "Inkling 2 Small on vLLM: Day-0 Support", "Accuracy evaluation"
 // (the router runs in FP32); "Day 0 support for Mistral Large 4 on vLLM",
@@ -10,15 +11,20 @@
 // strategy" (the expert GEMVs read only the selected experts, which is what the
 // work list built here enables).
 //
-// One launch of E/8 blocks.  Each warp owns one expert: its router row is
-// fetched into registers BEFORE the programmatic-launch wait (router weights
-// do not depend on the previous kernel), the tokens' activations are staged in
-// shared memory once per block, and the warp writes the FP32 logits of every
-// token.  The block that finishes last (atomic ticket, no spinning) loads all
-// logits into shared memory, runs sigmoid/top-k per token (one warp per token),
-// counts the tokens per expert with 64-bit token masks, scans them into slots
-// (shared experts first, then routed experts in ascending id) and numbers the
-// (expert, token) pairs so that each expert's pairs are contiguous.
+// Grid: (E/8 expert groups) x (token groups of up to 8 tokens).  Each warp
+// owns one expert: its router row is fetched into registers BEFORE the
+// programmatic-launch wait (router weights do not depend on the previous
+// kernel); the block stages its token group's activations in shared memory
+// and the warp computes the FP32 logits of those tokens (one accumulator per
+// token, so the FMA chains run side by side).  Two tickets follow, with no
+// spinning:
+//   * the last expert group of a token group to finish runs sigmoid + top-k
+//     for those tokens (one warp per token) and ORs each token into a 64-bit
+//     mask per selected expert;
+//   * the last token group to finish turns the masks into slots (shared
+//     experts first, then routed experts in ascending id), numbers the
+//     (expert, token) pairs so that each expert's pairs are contiguous, lists
+//     the slots with many tokens for the grouped kernels, and clears the masks.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -36,25 +42,6 @@ __device__ __forceinline__ void bf16x4_to_f(uint2 v, float &a, float &b, float &
     e = __uint_as_float(v.y & 0xFFFF0000u);
 }
 
-__device__ __forceinline__ void dot4(const float4 &w, const uint2 *__restrict__ xs, int H4, int nt, int v,
-                                     float (&acc)[kTokGroup]) {
-#pragma unroll
-    for (int t = 0; t < kTokGroup; ++t) {
-        if (t < nt) {
-            float x0, x1, x2, x3;
-            bf16x4_to_f(xs[t * H4 + v], x0, x1, x2, x3);
-            acc[t] = fmaf(x0, w.x, acc[t]);
-            acc[t] = fmaf(x1, w.y, acc[t]);
-            acc[t] = fmaf(x2, w.z, acc[t]);
-            acc[t] = fmaf(x3, w.w, acc[t]);
-        }
-    }
-}
-
-__device__ __forceinline__ bool better(float s, int e, float bs, int be) {
-    return s > bs || (s == bs && e < be);
-}
-
 __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
                                                          int T, int tg, int *__restrict__ ids_out,
                                                          float *__restrict__ w_out) {
@@ -63,6 +50,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     const int H = d.H, E = d.E, K = d.k, S = d.S;
     const int e = blockIdx.x * kRouteWarps + warp;
     const int nvec = H / 4;
+    const int t0 = blockIdx.y * tg, nt = min(tg, T - t0);
     const float *wr = d.router_w + (size_t)(e < E ? e : 0) * H;
 
     MOE_TRACE_POINT(0, 0);
@@ -78,190 +66,171 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             pre[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    const float bias = (e < E && d.router_b) ? d.router_b[e] : 0.f;
     pdl_wait();
     pdl_trigger();
     MOE_TRACE_POINT(0, 1);
 
+    // ---- stage the token group's activation rows (16-byte loads, all in flight) ----
     __shared__ float s_rmax[kTokGroup];
-    uint2 *xs = reinterpret_cast<uint2 *>(smem);          // [tg][H/4] groups of 4 bf16
-    const float bias = (e < E && d.router_b) ? d.router_b[e] : 0.f;
-    for (int t0 = 0; t0 < T; t0 += tg) {
-        const int nt = min(tg, T - t0);
-        if (t0 > 0) __syncthreads();
-        if (threadIdx.x < kTokGroup) s_rmax[threadIdx.x] = 0.f;
-        // stage the group's activation rows (16-byte loads)
+    if (threadIdx.x < kTokGroup) s_rmax[threadIdx.x] = 0.f;
+    const uint2 *xs = reinterpret_cast<const uint2 *>(smem);     // [nt][H/4] groups of 4 bf16
+    {
         const int n16 = nt * H / 8;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t0 * H);
         uint4 *dst = reinterpret_cast<uint4 *>(smem);
         __syncthreads();
-        for (int base = threadIdx.x; base < n16; base += 4 * kThreads) {
-            uint4 v[4];
+#pragma unroll 1
+        for (int base = threadIdx.x; base < n16; base += 8 * kThreads) {
+            uint4 v[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
                 if (base + u * kThreads < n16) v[u] = __ldcg(src + base + u * kThreads);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int i = base + u * kThreads;
-                if (i < n16) dst[i] = v[u];
-                if (blockIdx.x == 0) {
-                    // per-token max |x| for the GEMVs' power-of-two prescale
-                    float m = 0.f;
-                    if (i < n16) {
+                if (i < n16) {
+                    dst[i] = v[u];
+                    if (blockIdx.x == 0) {
+                        // per-token max |x| for the GEMVs' power-of-two prescale
+                        float m = 0.f;
                         const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
                                                fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
-                    }
-                    if ((H & 255) == 0) {
-                        // a row is a multiple of 32 items and a warp's items are
-                        // contiguous: the warp lies in one row, reduce it first
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                        const int i0 = i - lane;
-                        if (lane == 0 && i0 < n16)
-                            atomicMax(reinterpret_cast<int *>(&s_rmax[i0 / (H / 8)]), __float_as_int(m));
-                    } else if (i < n16) {
                         atomicMax(reinterpret_cast<int *>(&s_rmax[i / (H / 8)]), __float_as_int(m));
                     }
                 }
             }
         }
         __syncthreads();
-        MOE_TRACE_POINT(0, 2);
-        if (blockIdx.x == 0 && threadIdx.x < nt) {
-            const float mx = s_rmax[threadIdx.x];
-            d.xexp[t0 + threadIdx.x] = (mx > 0.f && isfinite(mx)) ? max(0, ilogbf(mx) - 14) : 0;
-        }
-        if (e < E) {
-            const int H4 = nvec;
-#pragma unroll 1
-            for (int t = 0; t < nt; ++t) {
-                const uint2 *xr = xs + t * H4;
-                float a = 0.f;
+    }
+    MOE_TRACE_POINT(0, 2);
+    if (blockIdx.x == 0 && threadIdx.x < nt) {
+        const float mx = s_rmax[threadIdx.x];
+        d.xexp[t0 + threadIdx.x] = (mx > 0.f && isfinite(mx)) ? max(0, ilogbf(mx) - 14) : 0;
+    }
+    // ---- logits of the group's tokens for this warp's expert ----
+    if (e < E) {
+        float acc[kTokGroup];
 #pragma unroll
-                for (int j = 0; j < kPre; ++j) {
-                    const int v = lane + 32 * j;
-                    if (v < nvec) {
+        for (int t = 0; t < kTokGroup; ++t) acc[t] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) {
+            const int v = lane + 32 * j;
+            if (v < nvec) {
+#pragma unroll
+                for (int t = 0; t < kTokGroup; ++t) {
+                    if (t < nt) {
                         float x0, x1, x2, x3;
-                        bf16x4_to_f(xr[v], x0, x1, x2, x3);
-                        a = fmaf(x0, pre[j].x, a);
-                        a = fmaf(x1, pre[j].y, a);
-                        a = fmaf(x2, pre[j].z, a);
-                        a = fmaf(x3, pre[j].w, a);
+                        bf16x4_to_f(xs[t * nvec + v], x0, x1, x2, x3);
+                        acc[t] = fmaf(x3, pre[j].w, fmaf(x2, pre[j].z, fmaf(x1, pre[j].y, fmaf(x0, pre[j].x, acc[t]))));
                     }
                 }
-                for (int v = lane + 32 * kPre; v < nvec; v += 32) {
-                    const float4 w = ld_f4(wr + 4 * v);
-                    float x0, x1, x2, x3;
-                    bf16x4_to_f(xr[v], x0, x1, x2, x3);
-                    a = fmaf(x0, w.x, a);
-                    a = fmaf(x1, w.y, a);
-                    a = fmaf(x2, w.z, a);
-                    a = fmaf(x3, w.w, a);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-                if (lane == 0) d.logits[(size_t)(t0 + t) * E + e] = a + bias;
             }
+        }
+#pragma unroll 1
+        for (int v = lane + 32 * kPre; v < nvec; v += 32) {
+            const float4 w = ld_f4(wr + 4 * v);
+#pragma unroll
+            for (int t = 0; t < kTokGroup; ++t) {
+                if (t < nt) {
+                    float x0, x1, x2, x3;
+                    bf16x4_to_f(xs[t * nvec + v], x0, x1, x2, x3);
+                    acc[t] = fmaf(x3, w.w, fmaf(x2, w.z, fmaf(x1, w.y, fmaf(x0, w.x, acc[t]))));
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kTokGroup; ++t) {
+            float a = acc[t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+            if (lane == 0 && t < nt) d.logits[(size_t)(t0 + t) * E + e] = a + bias;
         }
     }
 
-    // ---- the block that finishes last builds the routing result ----
+    // ---- the last expert group of this token group: top-k of its tokens ----
     __shared__ int s_last;
     __syncthreads();
     MOE_TRACE_POINT(0, 3);
     if (threadIdx.x == 0) {
         __threadfence();
-        unsigned tk = atomicAdd(d.ticket, 1u);
-        s_last = (tk == gridDim.x - 1);
+        s_last = atomicAdd(d.tg_ticket + blockIdx.y, 1u) == gridDim.x - 1;
     }
     __syncthreads();
-    MOE_TRACE_POINT(0, 4);
     if (!s_last) return;
     __threadfence();
+    MOE_TRACE_POINT(0, 4);
+    if (warp < nt) {
+        // sigmoid scores as order-preserving keys: bits(score) + 1 for a
+        // number, 0 for NaN (ranked last); the winner of a round is the
+        // largest key, the lowest expert id among equal keys
+        const int t = t0 + warp;
+        unsigned key[kMaxExperts / 32], id[kMaxExperts / 32], taken = 0u;
+#pragma unroll
+        for (int m = 0; m < kMaxExperts / 32; ++m) {
+            const int ee = lane + 32 * m;
+            key[m] = 0u;
+            id[m] = 0xffffffffu;
+            if (ee < E) {
+                const float z = __ldcg(d.logits + (size_t)t * E + ee);
+                key[m] = isnan(z) ? 0u : __float_as_uint(1.0f / (1.0f + expf(-z))) + 1u;
+                id[m] = (unsigned)ee;
+            }
+        }
+        unsigned sel_key = 0u;
+        int sel_e = 0;
+#pragma unroll 1
+        for (int j = 0; j < K; ++j) {
+            unsigned mx, win;
+            select_round<kMaxExperts / 32>(key, id, taken, mx, win);
+            if (lane == j) {
+                sel_key = mx;
+                sel_e = (int)win;
+            }
+        }
+        // weights: normalised over the k selected scores (summed in selection order)
+        const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
+        float sum = 0.f;
+        for (int j = 0; j < K; ++j) sum += __shfl_sync(0xffffffffu, sel_s, j);
+        if (lane < K) {
+            const float w = (d.normalize ? sel_s / sum : sel_s) * d.routed_scale;
+            d.ids[(size_t)t * K + lane] = sel_e;
+            d.wsel[(size_t)t * K + lane] = w;
+            if (ids_out) ids_out[(size_t)t * K + lane] = sel_e;
+            if (w_out) w_out[(size_t)t * K + lane] = w;
+            atomicOr(d.emask + sel_e, 1ull << t);
+        }
+    }
+    // ---- the last token group: slots, pairs, hot list ----
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        d.tg_ticket[blockIdx.y] = 0u;
+        __threadfence();
+        s_last = atomicAdd(d.ticket, 1u) == gridDim.y - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    MOE_TRACE_POINT(0, 5);
 
     __shared__ int s_ids[kMaxTokens][kMaxTopK];
     __shared__ float s_w[kMaxTokens][kMaxTopK];
     __shared__ unsigned long long s_mask[kMaxExperts];
     __shared__ int s_pbase[kMaxExperts];
     __shared__ int s_wsum_f[kRouteWarps], s_wsum_c[kRouteWarps];
-
-    float *s_logit = reinterpret_cast<float *>(smem);     // [T, E], reuses the staging area
-    for (int base = threadIdx.x; base < T * E; base += 4 * kThreads) {
-        float v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (base + u * kThreads < T * E) v[u] = __ldcg(d.logits + base + u * kThreads);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (base + u * kThreads < T * E) s_logit[base + u * kThreads] = v[u];
+    __shared__ short s_slotm[kMaxTokens * kMaxTopK + kMaxShared];   // tokens per slot
+    for (int i = threadIdx.x; i < E; i += kThreads) {
+        s_mask[i] = __ldcg(d.emask + i);
+        d.emask[i] = 0ull;
     }
-    for (int i = threadIdx.x; i < E; i += kThreads) s_mask[i] = 0ull;
-    __syncthreads();
-    MOE_TRACE_POINT(0, 5);
-
-    // a2: sigmoid + top-k + weights, one warp per token.
-    for (int t = warp; t < T; t += kRouteWarps) {
-        float sc[kMaxExperts / 32];
-#pragma unroll
-        for (int m = 0; m < kMaxExperts / 32; ++m) {
-            const int ee = lane + 32 * m;
-            float s = -INFINITY;
-            if (ee < E) {
-                const float z = s_logit[t * E + ee];
-                s = isnan(z) ? -INFINITY : 1.0f / (1.0f + expf(-z));
-            }
-            sc[m] = s;
-        }
-        unsigned taken = 0u;
-        float sel_s = 0.f;
-        int sel_e = 0;
-#pragma unroll 1
-        for (int j = 0; j < K; ++j) {
-            float bs = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int m = 0; m < kMaxExperts / 32; ++m) {
-                const int ee = lane + 32 * m;
-                if (ee < E && !(taken & (1u << m)) && better(sc[m], ee, bs, be)) {
-                    bs = sc[m];
-                    be = ee;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (better(os, oe, bs, be)) {
-                    bs = os;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            if (lane == j) {
-                sel_s = bs;
-                sel_e = be;
-            }
-        }
-        // weights: normalised over the k selected scores (summed in selection order)
-        float sum = 0.f;
-        for (int j = 0; j < K; ++j) sum += __shfl_sync(0xffffffffu, sel_s, j);
-        if (lane < K) {
-            float w = d.normalize ? sel_s / sum : sel_s;
-            w *= d.routed_scale;
-            s_ids[t][lane] = sel_e;
-            s_w[t][lane] = w;
-            d.ids[(size_t)t * K + lane] = sel_e;
-            d.wsel[(size_t)t * K + lane] = w;
-            if (ids_out) ids_out[(size_t)t * K + lane] = sel_e;
-            if (w_out) w_out[(size_t)t * K + lane] = w;
-            atomicOr(&s_mask[sel_e], 1ull << t);
-        }
+    for (int i = threadIdx.x; i < T * K; i += kThreads) {
+        s_ids[i / K][i % K] = __ldcg(d.ids + i);
+        s_w[i / K][i % K] = __ldcg(d.wsel + i);
     }
     __syncthreads();
-
     MOE_TRACE_POINT(0, 6);
     // Slots: shared experts first, then routed experts with >= 1 token in
     // ascending id.  Exclusive scans of (used?, token count) over experts.
@@ -306,6 +275,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
                 d.slot_expert[slot] = ee;
                 d.slot_m[slot] = c;
                 d.slot_p0[slot] = p0;
+                s_slotm[slot] = (short)c;
                 s_pbase[ee] = p0;
                 fbase += 1;
                 cbase += c;
@@ -317,8 +287,24 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         d.slot_expert[threadIdx.x] = -(threadIdx.x + 1);
         d.slot_m[threadIdx.x] = T;
         d.slot_p0[threadIdx.x] = threadIdx.x * T;
+        s_slotm[threadIdx.x] = (short)T;
     }
     __syncthreads();
+    if (warp == 0) {
+        // slots with at least grouped_min tokens (in slot order) go to the
+        // grouped tensor-core kernels; the GEMV kernels skip them
+        int ns = S;
+        for (int w = 0; w < kRouteWarps; ++w) ns += s_wsum_f[w];
+        int nh = 0;
+        for (int b = 0; b < ns; b += 32) {
+            const int sl = b + lane;
+            const bool hot = d.grouped_min > 0 && sl < ns && s_slotm[sl] >= d.grouped_min;
+            const unsigned bal = __ballot_sync(0xffffffffu, hot);
+            if (hot) d.hot_slots[nh + __popc(bal & ((1u << lane) - 1u))] = sl;
+            nh += __popc(bal);
+        }
+        if (lane == 0) *d.nhot = nh;
+    }
 
     // Pairs: an expert's tokens are numbered in ascending token order.
     const int P = K + S;
@@ -346,13 +332,12 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 }  // namespace
 
 size_t route_smem_bytes(const DevLayer &d, int T, int *tg_out) {
-    // staging of up to 8 activation rows, reused for the [T, E] logits
+    // activation rows of one token group (at most 8, at most 96 KB)
     int tg = kTokGroup;
     while (tg > 1 && (size_t)tg * d.H * 2 > 96 * 1024) --tg;
     if (tg > T) tg = T;
     if (tg_out) *tg_out = tg;
-    size_t a = (size_t)tg * d.H * 2, b = (size_t)T * d.E * 4;
-    return a > b ? a : b;
+    return (size_t)tg * d.H * 2;
 }
 
 cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out, float *w_out,
@@ -360,7 +345,7 @@ cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *
     int tg = 1;
     const size_t smem = route_smem_bytes(d, T, &tg);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((d.E + kRouteWarps - 1) / kRouteWarps);
+    cfg.gridDim = dim3((d.E + kRouteWarps - 1) / kRouteWarps, (T + tg - 1) / tg);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
