@@ -41,11 +41,30 @@ WORKLOADS = {
     "tiny": (0, 64),
 }
 
+# DRAM bytes (read + write) per launch of the single-launch kernel, from one
+# ncu capture per workload (summaries under profiles/), valid only for the
+# kernel source they were taken on: reported as `traffic` while fused.cu
+# hashes to the value below, null otherwise.
+NCU_TRAFFIC = {
+    "flint1": {"bytes": 20753920, "fused_cu_sha256_16": "09c695b3065df2f3"},
+    "flint8": {"bytes": 124603136, "fused_cu_sha256_16": "09c695b3065df2f3"},
+}
+
+
+def ncu_traffic(workload: str):
+    import hashlib
+    rec = NCU_TRAFFIC.get(workload)
+    if not rec:
+        return None
+    with open(os.path.join(ROOT, "nvfp4_weight_only_fp32_gb300", "csrc", "fused.cu"), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec["bytes"] if sha == rec["fused_cu_sha256_16"] else None
+
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: enough for ~1.5 s)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="flint1", choices=sorted(WORKLOADS))
@@ -90,9 +109,11 @@ class ClockSampler:
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.time(), ln.strip()))
 
-    def stop(self):
+    def stop(self, t0: float | None = None, t1: float | None = None):
+        """Median SM clock and throttle reasons over the samples taken between
+        wall-clock times t0 and t1 (the timed region)."""
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -103,7 +124,9 @@ class ClockSampler:
         self.t.join(timeout=2)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
             f = [v.strip() for v in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -116,7 +139,8 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"],
+                    "samples": 0}
         sm.sort()
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
@@ -204,6 +228,8 @@ def run_reference(args):
     ci, _ = WORKLOADS[args.workload]
     import gen
     c = gen.config(ci)
+    if args.steps <= 0:
+        args.steps = 3        # each step is a bounded sample of CPU work
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
     for w in range(args.warmup):
         oracle_sample(ci, 0.0, gen.BASE_SEED + 100 + w)
@@ -290,14 +316,23 @@ def time_graph(torch, g, stream, warmup, steps, sampler=None):
     if sampler:
         sampler.start()
         time.sleep(0.3)
+    t0 = time.time()
     e0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(steps):
             g.replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
     return e0.elapsed_time(e1), clocks
+
+
+def auto_steps(torch, g, stream, warmup, target_s=1.5):
+    """Timed steps for a ~target_s timed region (so that the clock sampler,
+    at 200 ms, sees it), from a short calibration after the warm-up."""
+    ms, _ = time_graph(torch, g, stream, warmup, 3)
+    return int(min(20000, max(20, target_s * 1e3 / max(ms / 3, 1e-3))))
 
 
 def byte_counts(gen, chain, np):
@@ -338,6 +373,10 @@ def run_gpu(args):
 
     g_full = capture(torch, lambda: chain.enqueue(moe), stream)
     sel, gu_bytes, Us = byte_counts(gen, chain, np)
+    if args.steps <= 0:
+        args.steps = auto_steps(torch, g_full, stream, args.warmup)
+        if dist is not None:
+            args.steps = int(max_over_ranks(float(args.steps), dist, dev))
     barrier(dist)
     sampler = ClockSampler(local)
     ms, clocks = time_graph(torch, g_full, stream, args.warmup, args.steps, sampler)
@@ -439,7 +478,8 @@ def run_gpu(args):
             "frac_of_8TBps": value / 8000.0,
             "chain_stage_us": stage_us,
             "roofline": {"bound": "hbm", "kernel": rk_name, "achieved": achieved,
-                         "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": ncu_traffic(args.workload) if single else None,
                          "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
                          "algorithmic_bytes_per_launch": rk_bytes, "launch_us": rk_us},
             "clocks": clocks,

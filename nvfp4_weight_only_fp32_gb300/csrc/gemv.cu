@@ -47,8 +47,8 @@ constexpr int kStageBudget = 96 * 1024;   // B staging budget when a slot has > 
 constexpr int kMaxRows = 64;              // staged B rows (tokens of one slot)
 
 __device__ __forceinline__ int hexp_of(unsigned bits) {
-    float v = __uint_as_float(bits);
-    return (v > 0.f && isfinite(v)) ? max(0, ilogbf(v) - 14) : 0;
+    // exact power-of-two prescale of an h row from its max |h| (also upward)
+    return max(-100, exp_for_f16(__uint_as_float(bits)));
 }
 
 

@@ -113,8 +113,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 __device__ __forceinline__ int hexp_of(unsigned bits) {
-    const float v = __uint_as_float(bits);
-    return (v > 0.f && isfinite(v)) ? max(0, ilogbf(v) - 14) : 0;
+    // exact power-of-two prescale of an h row from its max |h| (also upward)
+    return max(-100, exp_for_f16(__uint_as_float(bits)));
 }
 
 template <int MODE>   // 0 gate/up + SwiGLU, 1 down + combine

@@ -262,9 +262,11 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
 }
 
 __device__ __forceinline__ int exp_for_f16(float maxabs) {
-    // power of two 2^e such that maxabs * 2^-e < 2^15 (and >= 2^14 when
-    // maxabs > 0): f16 then holds every BF16 value of the row exactly except
-    // those below maxabs * 2^-32.
+    // power of two 2^e such that maxabs * 2^-e lies in [2^14, 2^15) when
+    // maxabs > 0: f16 then holds every BF16 value of the row exactly except
+    // those below maxabs * 2^-31 (8 significant bits need an f16 exponent of
+    // at least -17).  Callers clamp e at -100 so that 2^-e stays a normal
+    // FP32 number.
     return (maxabs > 0.f && isfinite(maxabs)) ? ilogbf(maxabs) - 14 : 0;
 }
 

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     MOE_TRACE_POINT(0, 2);
     if (blockIdx.x == 0 && threadIdx.x < nt) {
         const float mx = s_rmax[threadIdx.x];
-        d.xexp[t0 + threadIdx.x] = (mx > 0.f && isfinite(mx)) ? max(0, ilogbf(mx) - 14) : 0;
+        d.xexp[t0 + threadIdx.x] = max(-100, exp_for_f16(mx));
     }
     // ---- logits of the group's tokens for this warp's expert ----
     if (e < E) {
