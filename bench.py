@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--secondary", default="flint8", help="second workload reported in the line ('' = none)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--grouped-min", type=int, default=0,
+                    help="grouped_min_tokens of the layers (0: library default, -1: GEMV kernels only)")
     return ap.parse_args()
 
 
@@ -264,14 +266,14 @@ def run_reference(args):
 class Chain:
     """L distinct layers of one workload on the current GPU."""
 
-    def __init__(self, moe, torch, gen, ci, L, seed0):
+    def __init__(self, moe, torch, gen, ci, L, seed0, grouped_min=0):
         self.c = gen.config(ci)
         c = self.c
         self.T, self.L = c["T"], L
         self.layers, self.xs, self.outs, self.ids, self.ws = [], [], [], [], []
         for l in range(L):
             lay = gen.make_layer_torch(c, seed0 + l)
-            self.layers.append(moe.MoELayer(lay, max_tokens=self.T))
+            self.layers.append(moe.MoELayer(lay, max_tokens=self.T, grouped_min_tokens=grouped_min))
             del lay
             self.xs.append(gen.make_x_torch(c, seed0 + l))
             self.outs.append(torch.empty((self.T, c["H"]), dtype=torch.bfloat16, device="cuda"))
@@ -367,7 +369,7 @@ def run_gpu(args):
     ci, L = WORKLOADS[args.workload]
     L = args.layers or L
     seed0 = gen.BASE_SEED + 1000 * (rank + 1) + 100 * ci
-    chain = Chain(moe, torch, gen, ci, L, seed0)
+    chain = Chain(moe, torch, gen, ci, L, seed0, args.grouped_min)
     c = chain.c
     stream = torch.cuda.Stream()
 

@@ -201,11 +201,13 @@ moe_status moe_check(moe_layer *layer, void *stream);
 moe_status moe_debug_dequant(moe_layer *layer, int which, int expert, float *dst,
                              void *stream);
 
-/* Diagnostics: install a device buffer of 3 * blocks_per_kernel * 16 uint64
+/* Diagnostics: install a device buffer of 5 * blocks_per_kernel * 16 uint64
  * that the traced build of the library (compiled with MOE_TRACE) fills with
  * %globaltimer stamps at numbered phase points of its kernels (kernel 0
- * router, 1 gate/up, 2 down; index [kernel][block][point]).  NULL detaches.
- * The regular build returns MOE_ERR_UNSUPPORTED. */
+ * router or the single launch, 1 gate/up GEMV (the single launch: SM cycle
+ * counts), 2 down GEMV, 3 grouped gate/up, 4 grouped down; index
+ * [kernel][block][point]).  NULL detaches.  The regular build returns
+ * MOE_ERR_UNSUPPORTED. */
 moe_status moe_trace_attach(moe_layer *layer, unsigned long long *buf, int blocks_per_kernel);
 
 /* Fill *info (host struct). */

@@ -322,7 +322,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     if (e == cudaSuccess) e = prepare_kernels();
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->optin_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (L->cfg.grouped_min_tokens > 0 && grouped_supported(d)) d.grouped_min = L->cfg.grouped_min_tokens;
+    if (L->cfg.grouped_min_tokens > 0 && grouped_supported(d, L->sm_count)) d.grouped_min = L->cfg.grouped_min_tokens;
     for (int T = 0; T <= kMaxTokens; ++T) {
         L->fused_ok[T] = 0;
         if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&

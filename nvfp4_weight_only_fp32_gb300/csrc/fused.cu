@@ -227,10 +227,10 @@ __device__ __forceinline__ float hmax_read(const unsigned long long *hm, int p, 
 }
 
 // On give-up: wait (bounded) for the copies a warp still has in flight
-// (segments n_con .. n_iss-1; lane 0 knows n_iss).
-__device__ __forceinline__ void drain_ring(uint64_t *bar, int RW, int n_con, int n_iss, int lane) {
+// (segments n_done .. n_iss-1: issued, never waited for; lane 0 knows n_iss).
+__device__ __forceinline__ void drain_ring(uint64_t *bar, int RW, int n_done, int n_iss, int lane) {
     if (lane != 0) return;
-    for (int j = n_con; j < n_iss; ++j) {
+    for (int j = n_done; j < n_iss; ++j) {
         const unsigned long long t0 = gtimer();
         while (!mbar_try_wait(bar + j % RW, (unsigned)((j / RW) & 1)) && gtimer() - t0 < kWaitNs) {
         }
@@ -524,6 +524,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     const uint8_t *xb = xs + (size_t)(g < T ? g : T) * fg.xrow + q * 32;
     int n_con = 0, sl_c = 0;             // segments consumed by this warp; its ring slot
     unsigned par_c = 0u;                 // and the slot's phase parity
+    int n_done = 0;                      // segments whose copies have landed (waited for)
     int nslots = S, lksd = 0, perw = 0, nrt = 0;
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
@@ -665,7 +666,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll 1
             while (lft > 0) {
                 const int n = min(CH, lft);
-                if (ok && !mbar_wait(bar + sl_c, par_c, d.err)) ok = false;
+                if (ok) {
+                    if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
+                    else ok = false;
+                }
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
@@ -727,7 +731,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     gbar_arrive(d.bar_count);
     ok = gbar_wait(d.bar_count, bar_base + 2u * (unsigned)G, d.err) && ok;
     if (!__syncthreads_and(ok)) {
-        drain_ring(bar, RW, n_con, n_iss, lane);
+        drain_ring(bar, RW, n_done, n_iss, lane);
         if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;
         return;
     }
@@ -795,7 +799,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll 1
             while (lft > 0) {
                 const int n = min(CH, lft);
-                if (ok && !mbar_wait(bar + sl_c, par_c, d.err)) ok = false;
+                if (ok) {
+                    if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
+                    else ok = false;
+                }
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
@@ -845,7 +852,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         }
         __syncthreads();
     }
-    if (!ok) drain_ring(bar, RW, n_con, n_iss, lane);
+    if (!ok) drain_ring(bar, RW, n_done, n_iss, lane);
     MOE_TRACE_POINT(0, 9);
     MOE_TRACE_CLOCK(1, 9);
     if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;

@@ -155,7 +155,13 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     };
 
     if (MODE == 0) {
-        if (shared && GMAX > 1 && d.grouped_min > 0 && T >= d.grouped_min) return;   // grouped kernel's
+        if (shared && GMAX > 1 && d.grouped_min > 0 && T >= d.grouped_min) {   // grouped kernel's
+            // every block waits before it leaves, so that "all blocks of this
+            // kernel released the next one" implies the router has finished
+            pdl_wait();
+            pdl_trigger();
+            return;
+        }
         if (shared) {
             // Shared experts do not depend on routing: stream them now.
             m = T;
@@ -193,7 +199,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
             return;
         }
         m = __ldcg(d.slot_m + s);
-        if (GMAX > 1 && d.grouped_min > 0 && m >= d.grouped_min) return;   // grouped kernel's (and its ticket)
+        if (GMAX > 1 && d.grouped_min > 0 && m >= d.grouped_min) {   // grouped kernel's (and its ticket)
+            pdl_wait();   // as above: h is complete once every block has released the next kernel
+            pdl_trigger();
+            return;
+        }
         p0 = __ldcg(d.slot_p0 + s);
         slot_geometry(__ldcg(d.slot_expert + s));
         if (r < NT)

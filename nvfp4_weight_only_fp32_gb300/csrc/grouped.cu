@@ -35,6 +35,8 @@
 // Every mbarrier wait gives up after about a second (sticky error word and a
 // shared abort flag that releases the other roles); the TMEM columns are
 // released on every exit path.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -54,7 +56,11 @@ constexpr uint32_t kSBO = 8 * 128;                // row-adjacent core matrices 
 constexpr int kAStage = kMT * kChunkK * 2;        // 16 KB
 constexpr int kBStage = kNmax * kChunkK * 2;      // 8 KB
 constexpr int kScratch = kMaxTokens * (kMaxTopK + kMaxShared) * 8;   // combine's pair table
-constexpr int kSmem = kNS * (kAStage + kBStage) + kScratch;
+constexpr int kCHA = 4;                           // chunks per raw-weight segment
+constexpr int kRWA = 4;                           // raw-weight segments per decode warp
+constexpr int kRawOff = kNS * (kAStage + kBStage) + kScratch;
+constexpr int kSmem = kRawOff + kDecW * kRWA * kCHA * kChunkBytes;
+constexpr int kMaxItems = 128;                    // work items per block
 constexpr uint32_t kTmemCols = 64;                // >= N, a power of two >= 32
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
@@ -122,9 +128,14 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                                                          __nv_bfloat16 *__restrict__ out) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_full[kNS], s_empty[kNS], s_accf, s_acce;
+    __shared__ __align__(8) uint64_t s_rbar[kDecW][kRWA];
     __shared__ uint32_t s_taddr;
     __shared__ int s_abort;
     __shared__ int s_last;
+    // this block's items: first byte of tile 8mt (warp w adds w tiles), K
+    // chunks, tokens, first pair, expert (< 0: shared), M-tile
+    __shared__ const uint8_t *s_it_base[kMaxItems];
+    __shared__ int s_it_nc[kMaxItems], s_it_m[kMaxItems], s_it_p0[kMaxItems], s_it_e[kMaxItems], s_it_mt[kMaxItems];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
@@ -132,7 +143,9 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
     uint8_t *sB = smem + kNS * kAStage;
     int *s_pair = reinterpret_cast<int *>(smem + kNS * (kAStage + kBStage));
     float *s_pw = reinterpret_cast<float *>(smem + kNS * (kAStage + kBStage) + kScratch / 2);
+    uint8_t *rraw = smem + kRawOff + (size_t)(warp < kDecW ? warp : 0) * kRWA * kCHA * kChunkBytes;
     volatile int *abort = &s_abort;
+    const uint64_t pol = evict_first_policy();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNS; ++i) {
@@ -141,6 +154,8 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
         }
         mbar_init(&s_accf, 1);
         mbar_init(&s_acce, kDecW);
+        for (int w = 0; w < kDecW; ++w)
+            for (int i = 0; i < kRWA; ++i) mbar_init(&s_rbar[w][i], 1);
         s_abort = 0;
         fence_proxy_async();
     }
@@ -150,97 +165,135 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
+    MOE_TRACE_POINT(3 + MODE, 0);
+    // The router's tables are final when this kernel starts (the GEMV kernel
+    // before it released it only after its own dependency wait), and what
+    // this kernel reads besides them is x (gate/up) or h (down: complete
+    // before the GEMV down kernel released it).  So it starts at once; it
+    // waits on its predecessor only at the end, which keeps the chain's
+    // completion order.
+    pdl_trigger();
+    const int nhot = __ldcg(d.nhot);
+    const int ns = __ldcg(d.nslots);
+    const int MTper = MODE == 0 ? d.I / 64 : d.H / kMT;   // M-tiles of a routed slot
+    const int MTs = MODE == 0 ? d.Is / 64 : d.H / kMT;    // of a shared slot
+    // items: hot slots in slot order (shared ones first), each with its M-tiles
+    int sh = 0;
+    if (MODE == 0)
+        for (int h = 0; h < nhot && h < d.S; ++h) sh += __ldcg(d.hot_slots + h) < d.S;
+    const int nitems = MODE == 0 ? sh * MTs + (nhot - sh) * MTper : nhot * MTper;
+    const int nmy = blockIdx.x < nitems ? min(kMaxItems, (nitems - blockIdx.x + gridDim.x - 1) / gridDim.x) : 0;
+    if (threadIdx.x < nmy) {
+        const int it = blockIdx.x + threadIdx.x * gridDim.x;
+        int h, mt;
+        if (MODE == 0 && it < sh * MTs) {
+            h = it / MTs;
+            mt = it - h * MTs;
+        } else {
+            const int i2 = MODE == 0 ? it - sh * MTs : it;
+            h = (MODE == 0 ? sh : 0) + i2 / MTper;
+            mt = i2 % MTper;
+        }
+        const int slot = __ldcg(d.hot_slots + h);
+        const int e = __ldcg(d.slot_expert + slot);
+        const bool shared = e < 0;
+        const int NC = MODE == 0 ? d.H / kChunkK : (shared ? d.Is : d.I) / kChunkK;
+        const uint8_t *wbase = MODE == 0 ? (shared ? d.sw13r + (size_t)(-e - 1) * d.s13_stride
+                                                   : d.w13r + (size_t)e * d.e13_stride)
+                                         : (shared ? d.sw2r + (size_t)(-e - 1) * d.s2_stride
+                                                   : d.w2r + (size_t)e * d.e2_stride);
+        s_it_base[threadIdx.x] = wbase + (size_t)(8 * mt) * NC * kChunkBytes;
+        s_it_nc[threadIdx.x] = NC;
+        s_it_m[threadIdx.x] = __ldcg(d.slot_m + slot);
+        s_it_p0[threadIdx.x] = __ldcg(d.slot_p0 + slot);
+        s_it_e[threadIdx.x] = e;
+        s_it_mt[threadIdx.x] = mt;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t taddr = s_taddr;
+    MOE_TRACE_POINT(3 + MODE, 1);
 
-    pdl_wait();
-    pdl_trigger();
-    const int nhot = __ldcg(d.nhot);
-    const int ns = __ldcg(d.nslots);
-    const int MTper = MODE == 0 ? d.I / 64 : d.H / kMT;   // M-tiles per routed slot (shared: Is / 64 for gate/up)
-    const int MTs = MODE == 0 ? d.Is / 64 : d.H / kMT;
-    // items: hot slots in order, each with its M-tiles; a shared slot has
-    // MTs tiles, a routed one MTper (equal for down)
-    int nitems = 0;
-    if (MODE == 0) {
-        // hot slots are listed in slot order and the shared ones come first
-        for (int h = 0; h < nhot; ++h) nitems += __ldcg(d.hot_slots + h) < d.S ? MTs : MTper;
-    } else {
-        nitems = nhot * MTper;
-    }
-    const uint64_t pol = evict_first_policy();
+    // ---- raw weight ring of a decode warp: its tile's chunks of every item,
+    // in segments of <= kCHA chunks, issued ahead across items (lane 0) ----
+    uint64_t *rbar = s_rbar[warp < kDecW ? warp : 0];
+    int ip = 0, cp = 0, n_iss = 0, n_done = 0;
+    auto rissue = [&](int limit) {
+        if (lane != 0) return;
+        while (n_iss < limit && ip < nmy) {
+            const int nc = s_it_nc[ip], n = min(kCHA, nc - cp), sl = n_iss % kRWA;
+            const uint8_t *src = s_it_base[ip] + ((size_t)warp * nc + cp) * kChunkBytes;
+            fence_proxy_async();
+            mbar_expect_tx(rbar + sl, (unsigned)(n * kChunkBytes));
+            bulk_g2s(rraw + (size_t)sl * kCHA * kChunkBytes, src, (unsigned)(n * kChunkBytes), rbar + sl, pol);
+            ++n_iss;
+            cp += n;
+            if (cp == nc) {
+                cp = 0;
+                ++ip;
+            }
+        }
+    };
+    if (warp < kDecW) rissue(kRWA);
 
-    int gc = 0;        // chunks through the ring so far (all items of this block)
-    int nloc = 0;      // items of this block so far
+    int gc = 0;        // chunks through the A/B stages so far
+    int jc = 0;        // raw segments consumed (decode warps)
 #pragma unroll 1
-    for (int it = blockIdx.x; it < nitems; it += gridDim.x, ++nloc) {
+    for (int li = 0; li < nmy; ++li) {
         // (every role runs every item, so that the epilogue warps' named
         // barriers stay matched; after an abort the waits return at once)
-        // item -> (hot slot, M-tile)
-        int h = 0, mt = it;
-        if (MODE == 0) {
-#pragma unroll 1
-            for (;; ++h) {
-                const int n = __ldcg(d.hot_slots + h) < d.S ? MTs : MTper;
-                if (mt < n) break;
-                mt -= n;
-            }
-        } else {
-            h = it / MTper;
-            mt = it - h * MTper;
-        }
-        const int slot = __ldcg(d.hot_slots + h);
-        const int e = __ldcg(d.slot_expert + slot);
-        const int m = __ldcg(d.slot_m + slot);
-        const int p0 = __ldcg(d.slot_p0 + slot);
+        const int NC = s_it_nc[li], m = s_it_m[li], p0 = s_it_p0[li], e = s_it_e[li], mt = s_it_mt[li];
         const int N = (m + 15) & ~15;
         const bool shared = e < 0;
-        const int Islot = shared ? d.Is : d.I;
-        const int NC = MODE == 0 ? d.H / kChunkK : Islot / kChunkK;     // K chunks
-        const uint8_t *wbase;
         float gs0, gs1;
         if (MODE == 0) {
-            wbase = shared ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
             gs0 = shared ? d.sgs13[2 * (-e - 1)] : d.gs13[2 * e];
             gs1 = shared ? d.sgs13[2 * (-e - 1) + 1] : d.gs13[2 * e + 1];
         } else {
-            wbase = shared ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
             gs0 = shared ? d.sgs2[-e - 1] : d.gs2[e];
             gs1 = 0.f;
         }
 
         if (warp < kDecW) {
-            // ---- A producer: tile 8mt + warp, chunk by chunk ----
-            const uint8_t *tb = wbase + (size_t)(8 * mt + warp) * NC * kChunkBytes;
-            uint4 cw;
-            uint2 sw;
-            load_chunk(tb, 0, lane, cw, sw, pol);
+            // ---- A producer: tile 8mt + warp, from the raw ring ----
+            int oc = 0, cseg = 0;
 #pragma unroll 1
             for (int c = 0; c < NC; ++c) {
                 const int gcc = gc + c, st = gcc % kNS;
-                uint4 ncw = cw;
-                uint2 nsw = sw;
-                if (c + 1 < NC) load_chunk(tb, c + 1, lane, ncw, nsw, pol);
-                if (!gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err)) break;
-                uint32_t a[4][4];
-                decode_chunk(cw, sw, a);
-                uint8_t *As = sA + (size_t)st * kAStage + g * 16 + q * 4;
+                if (oc == 0 && !*abort) {
+                    if (gwait(rbar + jc % kRWA, (unsigned)((jc / kRWA) & 1), abort, d.err)) n_done = jc + 1;
+                }
+                const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
+                if (go) {
+                    const uint8_t *ch = rraw + ((size_t)(jc % kRWA) * kCHA + oc) * kChunkBytes;
+                    const uint4 cw = lds128(ch + 16 * lane);
+                    uint2 sw;
+                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n"
+                                 : "=r"(sw.x), "=r"(sw.y) : "r"(smem_u32(ch + kCodeBytes + 8 * g)));
+                    uint32_t a[4][4];
+                    decode_chunk(cw, sw, a);
+                    uint8_t *As = sA + (size_t)st * kAStage + g * 16 + q * 4;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                    for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * kSBO + (2 * i + (b >> 1)) * kLBO) =
-                            a[i][b];
-                fence_proxy_async();
+                        for (int b = 0; b < 4; ++b)
+                            *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * kSBO + (2 * i + (b >> 1)) * kLBO) =
+                                a[i][b];
+                    fence_proxy_async();
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&s_full[st]);
-                cw = ncw;
-                sw = nsw;
+                if (go && lane == 0) mbar_arrive(&s_full[st]);
+                if (++oc == min(kCHA, NC - cseg)) {
+                    cseg += oc;
+                    oc = 0;
+                    ++jc;
+                    if (!*abort) rissue(jc + kRWA);
+                }
             }
         } else if (warp < kMmaW) {
-            // ---- B producer: the slot's m tokens, rows >= m zero ----
+            // ---- B producer: the slot's m tokens (rows >= m zero), one
+            // chunk of loads ahead ----
             const int tb = threadIdx.x - 32 * kDecW;      // 0..127
             const int kg = tb & 7;                        // K group of this thread's pieces
             const uint4 *src[4];
@@ -261,36 +314,44 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     }
                 }
             }
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = src[u] ? __ldcg(src[u] + kg) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
             for (int c = 0; c < NC; ++c) {
                 const int gcc = gc + c, st = gcc % kNS;
-                uint4 v[4];
+                uint4 vn[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = src[u] ? __ldcg(src[u] + c * 8 + kg) : make_uint4(0u, 0u, 0u, 0u);
-                if (!gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err)) break;
-                uint8_t *Bs = sB + (size_t)st * kBStage;
+                for (int u = 0; u < 4; ++u)
+                    vn[u] = (src[u] && c + 1 < NC) ? __ldcg(src[u] + (c + 1) * 8 + kg) : make_uint4(0u, 0u, 0u, 0u);
+                const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
+                if (go) {
+                    uint8_t *Bs = sB + (size_t)st * kBStage;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int n = (tb >> 3) + 16 * u;
-                    if (n < N) {
-                        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                        uint4 o;
-                        uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+                    for (int u = 0; u < 4; ++u) {
+                        const int n = (tb >> 3) + 16 * u;
+                        if (n < N) {
+                            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                            uint4 o;
+                            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
-                                               __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
-                        *reinterpret_cast<uint4 *>(Bs + (n >> 3) * kSBO + kg * kLBO + (n & 7) * 16) = o;
+                            for (int i = 0; i < 4; ++i)
+                                ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
+                                                   __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
+                            *reinterpret_cast<uint4 *>(Bs + (n >> 3) * kSBO + kg * kLBO + (n & 7) * 16) = o;
+                        }
                     }
+                    fence_proxy_async();
                 }
-                fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&s_full[st]);
+                if (go && lane == 0) mbar_arrive(&s_full[st]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = vn[u];
             }
         } else if (lane == 0) {
             // ---- MMA issuer ----
             const uint32_t idesc = instr_desc(kMT, N);
-            bool go = gwait(&s_acce, ((unsigned)nloc & 1u) ^ 1u, abort, d.err);   // accumulator read out
+            bool go = gwait(&s_acce, ((unsigned)li & 1u) ^ 1u, abort, d.err);   // accumulator read out
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < NC && go; ++c) {
@@ -321,10 +382,11 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                              : "memory");
         }
         gc += NC;
+        if (li == 0) MOE_TRACE_POINT(3 + MODE, 2);
 
         // ---- epilogue: warps 0-7 ----
         if (warp < kDecW) {
-            const bool ok = gwait(&s_accf, (unsigned)nloc & 1u, abort, d.err);
+            const bool ok = gwait(&s_accf, (unsigned)li & 1u, abort, d.err);
             tc_fence_after();
             const int qd = warp & 3, half = warp >> 2;
             float v[32];
@@ -400,15 +462,25 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
             }
         }
     }
+    MOE_TRACE_POINT(3 + MODE, 8);
     // the issuer's last commit covers all of its MMAs: wait for it before
-    // the columns are released
-    if (warp == kMmaW && lane == 0 && nloc > 0 && !*abort)
-        gwait(&s_accf, (unsigned)(nloc - 1) & 1u, abort, d.err);
+    // the columns are released; decode warps wait for raw copies never used
+    if (warp == kMmaW && lane == 0 && nmy > 0 && !*abort) gwait(&s_accf, (unsigned)(nmy - 1) & 1u, abort, d.err);
+    if (warp < kDecW && lane == 0) {
+        for (int j = n_done; j < n_iss; ++j) {
+            const unsigned long long t0 = gtimer();
+            while (!mbar_try_wait(rbar + j % kRWA, (unsigned)((j / kRWA) & 1)) && gtimer() - t0 < kWaitNs) {
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaW)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(kTmemCols) : "memory");
+    // completion order of the chain: this kernel ends after its predecessor
+    pdl_wait();
+    MOE_TRACE_POINT(3 + MODE, 9);
 }
 
 template <int MODE>
@@ -431,8 +503,12 @@ cudaError_t launch_g(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bflo
 
 // Shapes the grouped kernels take: 128-row M-tiles of every matrix (I, Is
 // multiples of 64 for gate/up's interleaved tiles, H of 128 for down).
-bool grouped_supported(const DevLayer &d) {
-    return d.H % kMT == 0 && d.I % 64 == 0 && (d.S == 0 || d.Is % 64 == 0) && d.max_tokens <= kNmax;
+bool grouped_supported(const DevLayer &d, int sm_count) {
+    if (!(d.H % kMT == 0 && d.I % 64 == 0 && (d.S == 0 || d.Is % 64 == 0) && d.max_tokens <= kNmax)) return false;
+    // every block's items must fit its item table
+    const int mt = std::max(std::max(d.I / 64, d.S > 0 ? d.Is / 64 : 0), d.H / kMT);
+    const long items = (long)d.max_slots * mt;
+    return (items + sm_count - 1) / sm_count <= kMaxItems;
 }
 
 cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s) {

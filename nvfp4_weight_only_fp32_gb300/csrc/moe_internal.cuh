@@ -106,7 +106,7 @@ cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *
                          float *w_out, cudaStream_t s);
 cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s);
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s);
-bool grouped_supported(const DevLayer &d);
+bool grouped_supported(const DevLayer &d, int sm_count);
 cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s);
 cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, cudaStream_t s);
 cudaError_t prepare_grouped_kernels(int optin_bytes);
