@@ -34,6 +34,7 @@ struct moe_layer {
     float *router_b_slot;
     int optin_smem;
     int fused_ok[kMaxTokens + 1];   // single-launch path usable for this T
+    int inject_stall = 0;           // moe_debug_inject: for the next single launch only
 };
 
 namespace {
@@ -262,6 +263,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     d.max_pairs = cfg->max_tokens * (K + S);
     d.Imax = std::max(I, Is);
     d.grouped_min = 0;   // set once the shape is known to suit the grouped kernels
+    d.debug_stall = 0;
 
     carve_weights(L, nullptr);
     carve_workspace(L, nullptr);
@@ -397,7 +399,10 @@ moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int
     if (xa < oa + nb && oa < xa + nb) return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
     if (L->fused_ok[T]) {
         DeviceGuard g(L->device);
-        cudaError_t e = launch_fused(L->d, static_cast<const __nv_bfloat16 *>(x), T,
+        DevLayer d = L->d;
+        d.debug_stall = L->inject_stall;
+        L->inject_stall = 0;
+        cudaError_t e = launch_fused(d, static_cast<const __nv_bfloat16 *>(x), T,
                                      static_cast<__nv_bfloat16 *>(out), topk_ids, topk_w, L->sm_count,
                                      reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MOE_OK : cuda_fail(e, "single-launch layer");
@@ -510,6 +515,14 @@ moe_status moe_trace_attach(moe_layer *L, unsigned long long *buf, int blocks_pe
     (void)blocks_per_kernel;
     return fail(MOE_ERR_UNSUPPORTED, "this library was built without MOE_TRACE");
 #endif
+}
+
+moe_status moe_debug_inject(moe_layer *L, int what, int value) {
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer handle is NULL");
+    if (what != MOE_INJECT_BARRIER_STALL) return fail(MOE_ERR_INVALID_ARG, "unknown injection " + std::to_string(what));
+    if (value < 0) return fail(MOE_ERR_INVALID_ARG, "injection value must be >= 0");
+    L->inject_stall = value;
+    return MOE_OK;
 }
 
 moe_status moe_get_info(const moe_layer *L, moe_layer_info *info) {

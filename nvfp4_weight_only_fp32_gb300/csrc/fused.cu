@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         Pass pp = p0;
         if (pass == 1) {
             MOE_TRACE_POINT(0, 4);
-            ok = gbar_wait(d.bar_count, bar_base + (unsigned)G, d.err) && ok;
+            ok = gbar_wait(d.bar_count, bar_base + (unsigned)(G + d.debug_stall), d.err) && ok;
             MOE_TRACE_POINT(0, 5);
             if (!__syncthreads_and(ok)) {
                 ok = false;

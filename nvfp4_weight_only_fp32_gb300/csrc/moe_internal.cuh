@@ -91,6 +91,7 @@ struct DevLayer {
     unsigned *epoch;                // [1] call counter of the single-launch path
     unsigned *bar_count;            // [1] grid barrier arrivals (2 * grid size per call)
     int grouped_min;                // slots with >= this many tokens use the grouped kernels (0: none)
+    int debug_stall;                // single launch: extra arrivals its first grid barrier waits for (test hook)
     int *nhot;                      // [1] number of such slots
     int *hot_slots;                 // [max_slots] their slot indices, ascending
     unsigned *tg_ticket;            // [max_tokens] router: arrivals per token group

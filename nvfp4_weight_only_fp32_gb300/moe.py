@@ -28,8 +28,10 @@ EXPORTED = [
     "moe_init", "moe_destroy", "moe_decode_forward", "moe_decode_forward_host",
     "moe_stage_route", "moe_stage_gate_up", "moe_stage_down",
     "moe_check", "moe_debug_dequant", "moe_get_info", "moe_last_error",
-    "moe_route_topk_static", "moe_trace_attach",
+    "moe_route_topk_static", "moe_trace_attach", "moe_debug_inject",
 ]
+
+MOE_INJECT_BARRIER_STALL = 1
 
 
 class moe_config(ctypes.Structure):
@@ -100,6 +102,8 @@ def lib(path: str | None = None):
             L.moe_route_topk_static.restype = st
             L.moe_trace_attach.argtypes = [vp, vp, i]
             L.moe_trace_attach.restype = st
+            L.moe_debug_inject.argtypes = [vp, i, i]
+            L.moe_debug_inject.restype = st
             L.moe_last_error.argtypes = []
             L.moe_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -174,6 +178,10 @@ def moe_get_info(h) -> moe_layer_info:
     info = moe_layer_info()
     _check(lib().moe_get_info(h, ctypes.byref(info)))
     return info
+
+
+def moe_debug_inject(h, what, value) -> None:
+    _check(lib().moe_debug_inject(h, int(what), int(value)))
 
 
 def moe_trace_attach(h, buf, blocks_per_kernel) -> None:
