@@ -203,17 +203,18 @@ moe_status moe_debug_dequant(moe_layer *layer, int which, int expert, float *dst
 
 /* Test hook for the fail-stop path (the pages' "Fail-stop" requirement of the
  * persistent decode kernel: in-kernel waits give up after a bound and report
- * instead of hanging).  what = MOE_INJECT_BARRIER_STALL: the NEXT
+ * instead of hanging).  what = MOE_INJECT_WAIT_STALL: the NEXT
  * moe_decode_forward call on this handle that runs as one launch makes its
- * first grid barrier wait for `value` (>= 1) arrivals more than there are
- * blocks -- a flag nothing sets.  That wait gives up after about one second,
- * sets the sticky error word and lets the call finish (its outputs are then
- * invalid); moe_check reports MOE_ERR_TIMEOUT and restores the handle, and
- * the call after that is correct again.  Nothing faults or traps.  The hook
- * is consumed by that one call; value 0 clears it.
+ * first grid-wide wait (every block polls the other blocks' router logits,
+ * which carry the call's tag) expect a tag `value` (>= 1) calls ahead --
+ * words nothing writes.  That wait gives up after about one second, sets the
+ * sticky error word and lets the call finish (its outputs are then invalid);
+ * moe_check reports MOE_ERR_TIMEOUT and restores the handle, and the call
+ * after that is correct again.  Nothing faults or traps.  The hook is
+ * consumed by that one call; value 0 clears it.
  * Errors: MOE_ERR_INVALID_ARG for a NULL handle, an unknown `what` or a
  * negative value. */
-#define MOE_INJECT_BARRIER_STALL 1
+#define MOE_INJECT_WAIT_STALL 1
 moe_status moe_debug_inject(moe_layer *layer, int what, int value);
 
 /* Diagnostics: install a device buffer of 5 * blocks_per_kernel * 16 uint64

@@ -170,9 +170,10 @@ void carve_workspace(moe_layer *L, char *base) {
     d.ticket = cv.take<unsigned>(1);
     d.down_cnt = cv.take<unsigned>((size_t)H / 16);
     d.err = cv.take<int>(1);
-    d.hmax64 = cv.take<unsigned long long>(d.max_pairs);
-    d.epoch = cv.take<unsigned>(1);
-    d.bar_count = cv.take<unsigned>(1);
+    const int Tf = std::min(Tm, 8);
+    d.logit_tag = cv.take<unsigned long long>((size_t)Tf * E);
+    d.h_tag = cv.take<unsigned long long>((size_t)Tf * (K + S) * (d.Imax / 2));
+    d.calls = cv.take<unsigned>(L->sm_count);
     d.nhot = cv.take<int>(1);
     d.hot_slots = cv.take<int>(d.max_slots);
     d.tg_ticket = cv.take<unsigned>(Tm);
@@ -446,12 +447,12 @@ moe_status moe_check(moe_layer *L, void *stream) {
     if (word == 0) return MOE_OK;
     int zero = 0;
     cudaMemcpy(L->d.err, &zero, sizeof(int), cudaMemcpyHostToDevice);
-    // a wait that gave up may leave the single-launch path's barrier counter
-    // out of step with its call counter: restart both, and the per-pair
-    // maxima tagged with the call counter
-    cudaMemset(L->d.bar_count, 0, sizeof(unsigned));
-    cudaMemset(L->d.epoch, 0, sizeof(unsigned));
-    cudaMemset(L->d.hmax64, 0, sizeof(unsigned long long) * L->d.max_pairs);
+    // restart the single-launch path's call counters and clear the words
+    // tagged with them
+    const int Tf = std::min(L->cfg.max_tokens, 8);
+    cudaMemset(L->d.calls, 0, sizeof(unsigned) * L->sm_count);
+    cudaMemset(L->d.logit_tag, 0, sizeof(unsigned long long) * Tf * L->d.E);
+    cudaMemset(L->d.h_tag, 0, sizeof(unsigned long long) * Tf * (L->d.k + L->d.S) * (L->d.Imax / 2));
     if (word == 1) return fail(MOE_ERR_TIMEOUT, "an in-kernel wait gave up");
     return fail(MOE_ERR_DEVICE, "device error word " + std::to_string(word));
 }
@@ -519,7 +520,7 @@ moe_status moe_trace_attach(moe_layer *L, unsigned long long *buf, int blocks_pe
 
 moe_status moe_debug_inject(moe_layer *L, int what, int value) {
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer handle is NULL");
-    if (what != MOE_INJECT_BARRIER_STALL) return fail(MOE_ERR_INVALID_ARG, "unknown injection " + std::to_string(what));
+    if (what != MOE_INJECT_WAIT_STALL) return fail(MOE_ERR_INVALID_ARG, "unknown injection " + std::to_string(what));
     if (value < 0) return fail(MOE_ERR_INVALID_ARG, "injection value must be >= 0");
     L->inject_stall = value;
     return MOE_OK;

@@ -62,9 +62,9 @@ constexpr int kCHmin = 4;
 constexpr int kRWmax = 6;                                // ring segments per warp
 constexpr int kSlotsF = kTF * kMaxTopK + kMaxShared;     // slots of a call with T <= 8
 constexpr int kPairsF = kTF * (kMaxTopK + kMaxShared);   // pairs of a call with T <= 8
-constexpr int kCandMax = 64;                             // top-k candidates per token
-constexpr int kM1max = 8;                                // experts per lane in a top-k group
+constexpr int kM1max = 8;                                // experts per lane in the top-k (E <= 256)
 constexpr int kTabMax = 32;                              // copy-list items per warp
+constexpr int kHU = 4;                                   // tagged h pieces in flight per lane
 constexpr unsigned long long kWaitNs = 1000000000ull;    // in-kernel waits give up after ~1 s
 
 struct FusedArgs {
@@ -78,14 +78,14 @@ struct FusedArgs {
 // Launch geometry and host-planned work split.
 // Dynamic shared memory: [phase-local region | rings].  The phase-local
 // region holds x as the f16 MMA operand (T+1 rows, the last one zero), the
-// router rows, the top-k candidates and x as copied (BF16) during phases
+// router rows and x as copied (BF16) during phases
 // B/C, and the staged h rows (all pairs + a zero row) during phase D; then
 // the packed per-expert global scales and router biases for the whole call.
 struct FusedGeom {
     int kRE, RW, CH;
     int xrow, hrow;
-    int router_off, cand_off, xraw_off, gs_off, ring_off, total;
-    int gpt, m1p;                           // top-k: groups per token, experts per lane per group (1, 2, 4, 8)
+    int router_off, xraw_off, gs_off, ring_off, total;
+    int m1p;                                // top-k: experts per lane (1, 2, 4, 8)
     int lks0;                               // log2 of the pass-0 K split
     unsigned char lks1[kSlotsF + 1];        // log2 of the pass-1 K split, by slot count
     unsigned char lksd[kSlotsF + 1];        // log2 of the down K split, by slot count
@@ -112,17 +112,12 @@ bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) 
     g.kRE = (d.E + G - 1) / G;
     g.xrow = d.H * 2 + 16;
     g.hrow = d.Imax * 2 + 16;
-    // top-k groups: T * gpt tasks (at most one per warp), at most kCandMax
-    // candidates per token, at most kM1max experts per lane
-    g.gpt = std::max(1, std::min({kFW / T, (d.E + 31) / 32, kCandMax / d.k}));
-    const int m1 = (d.E + 32 * g.gpt - 1) / (32 * g.gpt);
-    if (m1 > kM1max) return false;
     g.m1p = 1;
-    while (g.m1p < m1) g.m1p *= 2;
+    while (32 * g.m1p < d.E) g.m1p *= 2;
+    if (g.m1p > kM1max) return false;
     const size_t xs = (size_t)(T + 1) * g.xrow;
     g.router_off = (int)up16(xs);
-    g.cand_off = g.router_off + (int)up16((size_t)g.kRE * d.H * 4);
-    g.xraw_off = g.cand_off + (int)up16((size_t)T * kCandMax * 8);
+    g.xraw_off = g.router_off + (int)up16((size_t)g.kRE * d.H * 4);
     const size_t pB = (size_t)g.xraw_off + (size_t)T * d.H * 2;
     const size_t pD = (size_t)(T * (d.k + d.S) + 1) * g.hrow;
     g.gs_off = (int)((std::max(pB, pD) + 15) & ~(size_t)15);
@@ -181,50 +176,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity, int *err
     return true;
 }
 
-// Grid barrier on a counter that only grows: every block adds 1 per barrier
-// (a release reduction, no round trip), and barrier b of call `epoch`
-// completes when the counter reaches G * (2 * epoch + b + 1) (modulo 2^32).
-// Every block arrives at both barriers of every call, also after a wait gave
-// up, so the counter stays in step with the call counter.
-__device__ __forceinline__ void gbar_arrive(unsigned *count) {
-    __syncthreads();
-    if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(count) : "memory");
+// Words exchanged between the blocks of one call: (tag << 32) | payload,
+// written and read with relaxed gpu-scope accesses (each 64-bit word is
+// single-copy atomic).  The tag is the number of calls every block has
+// finished, plus one, so a word from an earlier call (or zeroed memory) never
+// matches and a reader simply polls the words it needs.
+__device__ __forceinline__ void st_tagged(unsigned long long *p, unsigned tag, unsigned payload) {
+    const unsigned long long v = ((unsigned long long)tag << 32) | payload;
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ bool gbar_wait(const unsigned *count, unsigned target, int *err) {
-    __shared__ int s_ok;
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        if ((int)(ld_acquire_gpu(count) - target) < 0) {
-            const unsigned long long t0 = gtimer();
-            while ((int)(ld_acquire_gpu(count) - target) < 0) {
-                if (gtimer() - t0 > kWaitNs) {
-                    atomicExch(err, 1);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        s_ok = ok;
-    }
-    __syncthreads();
-    return s_ok != 0;
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
+
+__device__ __forceinline__ void ld_tagged2(const unsigned long long *p, unsigned long long &a,
+                                           unsigned long long &b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];\n" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ bool tag_is(unsigned long long v, unsigned tag) { return (unsigned)(v >> 32) == tag; }
 
 __device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ float silu_fast(float v) { return v * __fdividef(1.0f, 1.0f + __expf(-v)); }
-
-__device__ __forceinline__ void hmax_publish(unsigned long long *hm, int p, unsigned epoch, float v) {
-    atomicMax(hm + p, ((unsigned long long)epoch << 32) | (unsigned long long)__float_as_uint(v));
-}
-
-__device__ __forceinline__ float hmax_read(const unsigned long long *hm, int p, unsigned epoch) {
-    const unsigned long long v = __ldcg(hm + p);
-    return (unsigned)(v >> 32) == epoch ? __uint_as_float((unsigned)v) : 0.f;
-}
 
 // On give-up: wait (bounded) for the copies a warp still has in flight
 // (segments n_done .. n_iss-1: issued, never waited for; lane 0 knows n_iss).
@@ -256,33 +235,41 @@ __device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, cons
     mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
 }
 
-// Stage 1 of the top-k for one (token t, expert group grp): lane L holds
-// experts (grp * M + i) * 32 + L, i < M; the group's k best (key, id) go to
-// the token's candidate list in selection order.
+// Top-k of token t from the tagged logits (polled until they carry `tag`):
+// lane L holds experts i * 32 + L, i < M; lane j < K ends with the j-th
+// choice's sort key.
 template <int M>
-__device__ __forceinline__ void topk_group(const float *logits, int t, int grp, int E, int K, int lane,
-                                           unsigned *cand) {
-    unsigned key[M], id[M], taken = 0u;
+__device__ __forceinline__ bool route_token(const unsigned long long *lt, int t, int E, int K, unsigned tag,
+                                            int lane, int *err, unsigned long long &sel, int &passes) {
+    unsigned long long v[M];
+    bool ok = true;
+    unsigned pend = 0u;
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (i * 32 + lane < E) pend |= 1u << i;
+    // every pass re-reads all pending words at once: one round trip each
+    const unsigned long long t0 = gtimer();
+    while (__any_sync(0xffffffffu, pend != 0u)) {
+        ++passes;
+#pragma unroll
+        for (int i = 0; i < M; ++i)
+            if ((pend >> i) & 1u) v[i] = ld_tagged(lt + (size_t)t * E + i * 32 + lane);
+#pragma unroll
+        for (int i = 0; i < M; ++i)
+            if (((pend >> i) & 1u) && tag_is(v[i], tag)) pend &= ~(1u << i);
+        if (pend && gtimer() - t0 > kWaitNs) {
+            atomicExch(err, 1);
+            ok = false;
+            pend = 0u;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        const int ee = (grp * M + i) * 32 + lane;
-        key[i] = 0u;
-        id[i] = 0xffffffffu;
-        if (ee < E) {
-            const float z = __ldcg(logits + (size_t)t * E + ee);
-            key[i] = isnan(z) ? 0u : __float_as_uint(1.0f / (1.0f + expf(-z))) + 1u;
-            id[i] = (unsigned)ee;
-        }
+        const int e = i * 32 + lane;
+        v[i] = e < E ? ((unsigned long long)sigmoid_key(__uint_as_float((unsigned)v[i])) << 32) | (unsigned)~e : 0ull;
     }
-#pragma unroll 1
-    for (int j = 0; j < K; ++j) {
-        unsigned mx, win;
-        select_round<M>(key, id, taken, mx, win);
-        if (lane == 0) {
-            cand[(t * kCandMax + grp * K + j) * 2] = mx;
-            cand[(t * kCandMax + grp * K + j) * 2 + 1] = win;
-        }
-    }
+    sel = warp_topk<M>(v, K, lane);
+    return ok;
 }
 
 // Per-warp copy list: the warp's items (gate/up units of pass 0, of pass 1,
@@ -299,7 +286,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     __shared__ int s_tab_n[kFW][kTabMax];
     __shared__ float s_tmax[kFW][kTF];
     __shared__ int s_xexp[kTF];
-    __shared__ unsigned s_epoch;
+    __shared__ unsigned s_tag;
     __shared__ int s_ids[kTF][kMaxTopK];
     __shared__ float s_w[kTF][kMaxTopK];
     __shared__ __align__(4) unsigned char s_tokmask[kMaxExperts];
@@ -321,7 +308,6 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     const int RW = fg.RW, CH = fg.CH, kRE = fg.kRE;
     uint8_t *xs = smem;
     const float *s_router = reinterpret_cast<const float *>(smem + fg.router_off);
-    unsigned *s_cand = reinterpret_cast<unsigned *>(smem + fg.cand_off);   // [T][kCandMax][key, id]
     const uint8_t *xraw = smem + fg.xraw_off;
     const float4 *s_gsp = reinterpret_cast<const float4 *>(smem + fg.gs_off);  // copy of d.gsp
     uint8_t *ring = smem + fg.ring_off + (size_t)warp * RW * CH * kChunkBytes;
@@ -392,6 +378,8 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         s_slot_mask[si] = (1 << T) - 1;
         s_slot_p0[si] = si * T;
     }
+    if (threadIdx.x < S * T) s_pw[threadIdx.x] = 1.0f;
+    if (threadIdx.x < E) s_tokmask[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
         mbar_init(&s_rbar, 1);
         mbar_init(&s_xbar, 1);
@@ -427,7 +415,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     // ---------------- B: x, logits ----------------
     bool ok = true;
     if (threadIdx.x == 0) {
-        s_epoch = __ldcg(d.epoch);
+        s_tag = __ldcg(d.calls + c) + 1u;
         // x (T rows, contiguous) in one bulk copy
         mbar_expect_tx(&s_xbar, (unsigned)(T * H * 2));
         bulk_g2s(smem + fg.xraw_off, a.x, (unsigned)(T * H * 2), &s_xbar, pol);
@@ -513,14 +501,12 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             float v = 0.f;
 #pragma unroll
             for (int w = 0; w < kFW; ++w) v += s_lpart[w][re][t];
-            d.logits[(size_t)t * E + e] = v + s_gsp[e].w;
+            st_tagged(d.logit_tag + (size_t)t * E + e, s_tag, __float_as_uint(v + s_gsp[e].w));
         }
     }
-    gbar_arrive(d.bar_count);
     MOE_TRACE_POINT(0, 3);
 
     // ---------------- C: gate/up, pass 0 shared experts, pass 1 routed ----------------
-    const unsigned bar_base = (unsigned)G * 2u * s_epoch;
     const uint8_t *xb = xs + (size_t)(g < T ? g : T) * fg.xrow + q * 32;
     int n_con = 0, sl_c = 0;             // segments consumed by this warp; its ring slot
     unsigned par_c = 0u;                 // and the slot's phase parity
@@ -531,69 +517,67 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         Pass pp = p0;
         if (pass == 1) {
             MOE_TRACE_POINT(0, 4);
-            ok = gbar_wait(d.bar_count, bar_base + (unsigned)(G + d.debug_stall), d.err) && ok;
-            MOE_TRACE_POINT(0, 5);
-            if (!__syncthreads_and(ok)) {
-                ok = false;
-                break;
-            }
-            // routing, identical in every block.  Stage 1: warp w takes
-            // token w / gpt, expert group w % gpt (m1 experts per lane) and
-            // keeps its group's k best as candidates.
-            if (warp < T * fg.gpt) {
-                const int t = warp / fg.gpt, grp = warp - t * fg.gpt;
-                switch (fg.m1p) {
-                    case 1: topk_group<1>(d.logits, t, grp, E, K, lane, s_cand); break;
-                    case 2: topk_group<2>(d.logits, t, grp, E, K, lane, s_cand); break;
-                    case 4: topk_group<4>(d.logits, t, grp, E, K, lane, s_cand); break;
-                    default: topk_group<8>(d.logits, t, grp, E, K, lane, s_cand); break;
-                }
-            }
-            for (int i = threadIdx.x; i < E; i += kFT) s_tokmask[i] = 0;
-            __syncthreads();
-            MOE_TRACE_POINT(0, 10);
-            // Stage 2: warp t merges token t's gpt * k candidates.
+            // routing, identical in every block, straight from the tagged
+            // logits (no grid barrier): warp t < T takes token t, lane L the
+            // experts i * 32 + L.  An expert's sort key is (bits(sigmoid) +
+            // 1) << 32 | ~id (a NaN logit: 0 << 32 | ~id): larger is better,
+            // ties in the score go to the lower id, all keys differ.
+            const unsigned ltag = s_tag + (unsigned)d.debug_stall;
+            int lpass = 0;
+            unsigned long long sel = 0ull;
             if (warp < T) {
-                const int t = warp, nc = fg.gpt * K;
-                unsigned key[2], id[2], taken = 0u;
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int ci = lane + 32 * i;
-                    key[i] = ci < nc ? s_cand[(t * kCandMax + ci) * 2] : 0u;
-                    id[i] = ci < nc ? s_cand[(t * kCandMax + ci) * 2 + 1] : 0xffffffffu;
+                switch (fg.m1p) {
+                    case 1: ok = route_token<1>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                    case 2: ok = route_token<2>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                    case 4: ok = route_token<4>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                    default: ok = route_token<8>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
                 }
-                unsigned sel_key = 0u;
-                int sel_e = 0;
-#pragma unroll 1
-                for (int j = 0; j < K; ++j) {
-                    unsigned mx, win;
-                    select_round<2>(key, id, taken, mx, win);
-                    if (lane == j) {
-                        sel_key = mx;
-                        sel_e = (int)win;
-                    }
-                }
+            }
+            const unsigned sel_key = (unsigned)(sel >> 32);
+            const int sel_e = (int)~(unsigned)sel;
+            MOE_TRACE_POINT(0, 10);
+            MOE_TRACE_VALUE(1, 2, lpass);
+            // weights (normalised in selection order); for one token the
+            // slots follow directly: routed slot S + (rank of the id among
+            // the k choices), one pair each
+            if (warp < T) {
+                const int t = warp;
                 const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
                 float sum = 0.f;
+                int rank = 0;
 #pragma unroll 1
-                for (int j = 0; j < K; ++j) sum += __shfl_sync(0xffffffffu, sel_s, j);
+                for (int j = 0; j < K; ++j) {
+                    sum += __shfl_sync(0xffffffffu, sel_s, j);
+                    rank += __shfl_sync(0xffffffffu, sel_e, j) < sel_e;
+                }
                 if (lane < K) {
                     const float w = (d.normalize ? sel_s / sum : sel_s) * d.routed_scale;
                     s_ids[t][lane] = sel_e;
                     s_w[t][lane] = w;
-                    atomicOr(reinterpret_cast<unsigned *>(s_tokmask) + (sel_e >> 2), 1u << (8 * (sel_e & 3) + t));
                     if (c == 0) {
                         if (a.ids_out) a.ids_out[t * K + lane] = sel_e;
                         if (a.w_out) a.w_out[t * K + lane] = w;
                     }
+                    if (T == 1) {
+                        s_slot_e[S + rank] = sel_e;
+                        s_slot_mask[S + rank] = 1;
+                        s_slot_p0[S + rank] = S + rank;
+                        s_pw[S + rank] = w;
+                    } else {
+                        atomicOr(reinterpret_cast<unsigned *>(s_tokmask) + (sel_e >> 2), 1u << (8 * (sel_e & 3) + t));
+                    }
                 }
+                if (T == 1 && lane == 0) s_nslots = S + K;
             }
-            __syncthreads();
+            if (!__syncthreads_and(ok)) {
+                ok = false;
+                break;
+            }
             MOE_TRACE_POINT(0, 11);
-            // slots: shared first, then routed experts in ascending id (one
-            // expert per thread); an expert's pairs are contiguous, tokens
-            // ascending
-            {
+            if (T > 1) {
+                // slots: shared first, then routed experts in ascending id
+                // (one expert per thread); an expert's pairs are contiguous,
+                // tokens ascending
                 const int e = threadIdx.x;
                 const int msk = e < E ? s_tokmask[e] : 0;
                 const int cnt = __popc(msk);
@@ -630,7 +614,6 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     const int sl = s_eslot[ee];
                     s_pw[s_slot_p0[sl] + __popc(s_slot_mask[sl] & ((1 << t) - 1))] = s_w[t][j];
                 }
-                if (threadIdx.x < T * S) s_pw[threadIdx.x] = 1.0f;
             }
             MOE_TRACE_POINT(0, 12);
             // this warp's routed units and down pieces -> its copy list
@@ -701,8 +684,9 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
                 asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
             }
-            if (kw == 0 && ok) {
-                // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row 8r+g
+            if (kw == 0 && __all_sync(0xffffffffu, ok)) {
+                // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row
+                // 8r+g; lanes g and g+1 publish one tagged word of two BF16
                 const int e = s_slot_e[slot], msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
                 const float4 gsv = s_gsp[e < 0 ? E - e - 1 : e];
                 const float gsa = gsv.x, gsb = gsv.y;
@@ -711,74 +695,105 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     const int t = 2 * q + e2;
                     const bool on = t < T && ((msk >> t) & 1);
                     const int p = p0s + __popc(msk & ((1 << t) - 1));
-                    float habs = 0.f;
+                    unsigned hbits = 0u;
                     if (on) {
                         const float un = pow2f(s_xexp[t]);
                         const float gt = a0[e2] * gsa * un, upv = a0[2 + e2] * gsb * un;
-                        const __nv_bfloat16 hb = __float2bfloat16_rn(silu_fast(gt) * upv);
-                        d.h_ws[(size_t)p * d.Imax + 8 * r + g] = hb;
-                        habs = fabsf(__bfloat162float(hb));
+                        hbits = __bfloat16_as_ushort(__float2bfloat16_rn(silu_fast(gt) * upv));
                     }
-#pragma unroll
-                    for (int off = 4; off < 32; off <<= 1)
-                        habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, off));
-                    if (g == 0 && on) hmax_publish(d.hmax64, p, s_epoch, habs);
+                    const unsigned hnext = __shfl_down_sync(0xffffffffu, hbits, 4);
+                    if (on && !(g & 1))
+                        st_tagged(d.h_tag + ((size_t)p * d.Imax + 8 * r + g) / 2, s_tag, hbits | (hnext << 16));
                 }
             }
         }
     }
     MOE_TRACE_POINT(0, 7);
-    gbar_arrive(d.bar_count);
-    ok = gbar_wait(d.bar_count, bar_base + 2u * (unsigned)G, d.err) && ok;
-    if (!__syncthreads_and(ok)) {
+    // every warp is done with x and its gate/up units before phase D reuses
+    // the shared memory; a block without output tiles is done
+    if (!__syncthreads_and(ok) || nrt == 0) {
         drain_ring(bar, RW, n_done, n_iss, lane);
-        if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;
+        MOE_TRACE_POINT(0, 9);
+        if (threadIdx.x == 0) d.calls[c] = s_tag;
         return;
     }
     MOE_TRACE_POINT(0, 8);
 
     // ---------------- D: down + combine, 16 output rows per tile ----------------
-    // stage every pair's h as f16 with an exact power-of-two prescale (one
-    // warp per row, all of a lane's loads in flight); row npairs stays zero
-    // (the B column of tokens a slot does not serve)
+    // gather every pair's h row from the tagged words (one warp per row,
+    // polling until each word carries this call's tag) into shared memory in
+    // the MMA operand order, then rescale it in place to f16 by the row's
+    // exact power-of-two prescale; row npairs stays zero (the B column of
+    // tokens a slot does not serve)
     const int npairs = T * (K + S);
     uint8_t *hs = smem;
-    if (threadIdx.x < npairs)
-        s_hun[threadIdx.x] = pow2f(max(-100, exp_for_f16(hmax_read(d.hmax64, threadIdx.x, s_epoch))));
+    int hpass = 0;
     for (int i = threadIdx.x; i < fg.hrow / 16; i += kFT)
         reinterpret_cast<uint4 *>(hs + (size_t)npairs * fg.hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();
-    {
-        const int pieces = d.Imax / 8;       // 16-byte pieces per h row
 #pragma unroll 1
-        for (int j = warp; j < npairs; j += kFW) {
-            const uint4 *srcrow = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)j * d.Imax);
-            const float sc = __fdividef(1.0f, s_hun[j]);   // exact: a power of two
+    for (int j = warp; j < npairs; j += kFW) {
+        const int n = j < S * T ? d.Is : d.I;           // the row's length
+        const int npc = n / 4;                           // 16-byte pieces of tagged words
+        const unsigned long long *src = d.h_tag + (size_t)j * (d.Imax / 2);
+        uint32_t *row = reinterpret_cast<uint32_t *>(hs + (size_t)j * fg.hrow);
+        float mx = 0.f;
 #pragma unroll 1
-            for (int P0 = 0; P0 < pieces; P0 += 128) {
-                uint4 v[4];
+        for (int P0 = 0; P0 < npc; P0 += 32 * kHU) {
+            unsigned long long v[kHU][2];
+            unsigned pend = 0u;          // pieces not yet carrying the tag
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int P = P0 + lane + 32 * u;
-                    if (P < pieces) v[u] = __ldcg(srcrow + P);
+            for (int u = 0; u < kHU; ++u)
+                if (P0 + lane + 32 * u < npc) pend |= 1u << u;
+            // every pass re-reads all pending pieces at once
+            const unsigned long long t0 = gtimer();
+            while (pend && ok) {
+                ++hpass;
+#pragma unroll
+                for (int u = 0; u < kHU; ++u)
+                    if ((pend >> u) & 1u) ld_tagged2(src + 2 * (P0 + lane + 32 * u), v[u][0], v[u][1]);
+#pragma unroll
+                for (int u = 0; u < kHU; ++u)
+                    if (((pend >> u) & 1u) && tag_is(v[u][0], s_tag) && tag_is(v[u][1], s_tag)) pend &= ~(1u << u);
+                if (pend && gtimer() - t0 > kWaitNs) {
+                    atomicExch(d.err, 1);
+                    ok = false;
                 }
+            }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int P = P0 + lane + 32 * u;
-                    if (P < pieces) {
-                        uint32_t *dst = reinterpret_cast<uint32_t *>(hs + (size_t)j * fg.hrow + (P >> 3) * 128 +
-                                                                     ((P & 7) >> 1) * 8 + (P & 1) * 4);
-                        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            for (int u = 0; u < kHU; ++u) {
+                const int P = P0 + lane + 32 * u;
+                if (P < npc) {
 #pragma unroll
-                        for (int uu = 0; uu < 4; ++uu)
-                            dst[uu * 8] = pack_f16x2(__uint_as_float(w4[uu] << 16) * sc,
-                                                     __uint_as_float(w4[uu] & 0xFFFF0000u) * sc);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const unsigned wv = (unsigned)v[u][h2];
+                        // word wi of the row (elements 2wi, 2wi+1) -> its
+                        // place in the operand order (as for x)
+                        const int wi = 2 * P + h2, l = wi & 31;
+                        row[(wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1)] = wv;
+                        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wv << 16)), fabsf(__uint_as_float(wv & 0xFFFF0000u))));
                     }
                 }
             }
         }
+        // mx >= 0 and not NaN (fmaxf drops NaN): its bits order as unsigned
+        mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
+        const int hx = max(-100, exp_for_f16(mx));
+        if (lane == 0) s_hun[j] = pow2f(hx);
+        const float sc = pow2f(-hx);
+        __syncwarp();
+#pragma unroll 1
+        for (int w = lane; w < n / 2; w += 32) {
+            const unsigned wv = row[w];
+            row[w] = pack_f16x2(__uint_as_float(wv << 16) * sc, __uint_as_float(wv & 0xFFFF0000u) * sc);
+        }
     }
-    __syncthreads();
+    MOE_TRACE_VALUE(1, 3, hpass);
+    if (!__syncthreads_and(ok)) {
+        drain_ring(bar, RW, n_done, n_iss, lane);
+        MOE_TRACE_POINT(0, 9);
+        if (threadIdx.x == 0) d.calls[c] = s_tag;
+        return;
+    }
     MOE_TRACE_POINT(0, 14);
 #pragma unroll 1
     for (int ri = 0; ri < nrt; ++ri) {
@@ -855,7 +870,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     if (!ok) drain_ring(bar, RW, n_done, n_iss, lane);
     MOE_TRACE_POINT(0, 9);
     MOE_TRACE_CLOCK(1, 9);
-    if (c == 0 && threadIdx.x == 0) *d.epoch = s_epoch + 1u;
+    if (threadIdx.x == 0) d.calls[c] = s_tag;
 }
 
 template <int QP>

@@ -87,11 +87,14 @@ struct DevLayer {
     unsigned *ticket;               // [1]
     unsigned *down_cnt;             // [H/16] arrivals per down row group
     int *err;                       // [1] sticky device error word
-    unsigned long long *hmax64;     // [max_pairs] single-launch path: (epoch << 32) | max|h| bits
-    unsigned *epoch;                // [1] call counter of the single-launch path
-    unsigned *bar_count;            // [1] grid barrier arrivals (2 * grid size per call)
+    // single-launch path: values exchanged between blocks carry the call's
+    // tag (calls finished + 1) in their upper 32 bits, so a reader polls the
+    // words themselves instead of waiting at a grid barrier
+    unsigned long long *logit_tag;  // [8, E] (tag << 32) | FP32 logit bits
+    unsigned long long *h_tag;      // [8 * (k + S), Imax / 2] (tag << 32) | two BF16 of h (even index low)
+    unsigned *calls;                // [grid size] calls each block has finished
     int grouped_min;                // slots with >= this many tokens use the grouped kernels (0: none)
-    int debug_stall;                // single launch: extra arrivals its first grid barrier waits for (test hook)
+    int debug_stall;                // single launch: added to the tag its logit wait expects (test hook)
     int *nhot;                      // [1] number of such slots
     int *hot_slots;                 // [max_slots] their slot indices, ascending
     unsigned *tg_ticket;            // [max_tokens] router: arrivals per token group
@@ -165,12 +168,24 @@ __host__ __device__ inline size_t repacked_bytes(int rows, int cols) {
             if (b_ < d.trace_blocks) d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = clock64(); \
         }                                                                                        \
     } while (0)
+// A value (a count) stored under kernel slot `kid`, from thread 0.
+#define MOE_TRACE_VALUE(kid, i, v)                                                               \
+    do {                                                                                         \
+        if (threadIdx.x == 0 && d.trace) {                                                       \
+            const int b_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
+            if (b_ < d.trace_blocks)                                                             \
+                d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = (unsigned long long)(v); \
+        }                                                                                        \
+    } while (0)
 #else
 #define MOE_TRACE_POINT(kid, i) \
     do {                        \
     } while (0)
 #define MOE_TRACE_CLOCK(kid, i) \
     do {                        \
+    } while (0)
+#define MOE_TRACE_VALUE(kid, i, v) \
+    do {                           \
     } while (0)
 #endif
 
@@ -320,25 +335,61 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
-// One round of warp-wide selection among up to M items per lane: the largest
-// key, the lowest id among equal keys; the winning item is marked taken.
-// Keys: bits(sigmoid score) + 1 (order-preserving for scores in [0, 1]), 0
-// for NaN; ids of empty places are 0xffffffff.
+// The router's sigmoid score in FP32: exp to ~2 ulp, then an approximate
+// reciprocal (~1 ulp; 0 once 1 + exp(-z) passes 2^126, where the score is
+// below 2^-126 anyway) -- branch-free, a few ulp from the correctly rounded
+// score.
+__device__ __forceinline__ float sigmoid_score(float z) { return __fdividef(1.0f, 1.0f + expf(-z)); }
+
+// Order-preserving key of an expert's sigmoid score: bits(score) + 1, or 0
+// for a NaN logit (scores are in [0, 1], so their bits order as unsigned).
+__device__ __forceinline__ unsigned sigmoid_key(float z) {
+    return isnan(z) ? 0u : __float_as_uint(sigmoid_score(z)) + 1u;
+}
+
+// Sort M (a power of two) 64-bit keys held by one lane, largest first
+// (bitonic network; every index is a compile-time constant, so the keys stay
+// in registers).
 template <int M>
-__device__ __forceinline__ void select_round(const unsigned (&key)[M], const unsigned (&id)[M], unsigned &taken,
-                                             unsigned &mx, unsigned &win) {
-    unsigned bk = 0u, bi = 0xffffffffu;
+__device__ __forceinline__ void sort_desc(unsigned long long (&c)[M]) {
 #pragma unroll
-    for (int i = 0; i < M; ++i)
-        if (!((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && id[i] < bi))) {
-            bk = key[i];
-            bi = id[i];
+    for (int k = 2; k <= M; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long a = c[i], b = c[l];
+                    const bool sw = (i & k) == 0 ? a < b : a > b;
+                    c[i] = sw ? b : a;
+                    c[l] = sw ? a : b;
+                }
+            }
+}
+
+// Warp-wide top-k over 64-bit sort keys, M per lane (all keys distinct; 0
+// marks an empty place and is never chosen while k <= the number of real
+// keys).  Each lane sorts its keys once; every round takes the largest head
+// (its high word, then among lanes holding that, its low word) and the lane
+// that held it moves its list up.  Lane j < k ends with the j-th choice.
+template <int M>
+__device__ __forceinline__ unsigned long long warp_topk(unsigned long long (&c)[M], int K, int lane) {
+    sort_desc<M>(c);
+    unsigned long long mine = 0ull;
+#pragma unroll 1
+    for (int j = 0; j < K; ++j) {
+        const unsigned hi = (unsigned)(c[0] >> 32), lo = (unsigned)c[0];
+        const unsigned mx = __reduce_max_sync(0xffffffffu, hi);
+        const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mx ? lo : 0u);
+        if (lane == j) mine = ((unsigned long long)mx << 32) | ml;
+        if (hi == mx && lo == ml) {
+#pragma unroll
+            for (int i = 0; i + 1 < M; ++i) c[i] = c[i + 1];
+            c[M - 1] = 0ull;
         }
-    mx = __reduce_max_sync(0xffffffffu, bk);
-    win = __reduce_min_sync(0xffffffffu, bk == mx ? bi : 0xffffffffu);
-#pragma unroll
-    for (int i = 0; i < M; ++i)
-        if (id[i] == win) taken |= 1u << i;
+    }
+    return mine;
 }
 
 // Routing-weighted combine of output rows [row0, row0 + nrows) for all T

@@ -42,6 +42,19 @@ __device__ __forceinline__ void bf16x4_to_f(uint2 v, float &a, float &b, float &
     e = __uint_as_float(v.y & 0xFFFF0000u);
 }
 
+// Top-k of one token's FP32 logits (lane L holds experts i * 32 + L, i < M)
+// by sort keys; lane j < k returns the j-th choice.
+template <int M>
+__device__ __forceinline__ unsigned long long token_topk(const float *z, int E, int K, int lane) {
+    unsigned long long c[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const int e = i * 32 + lane;
+        c[i] = e < E ? ((unsigned long long)sigmoid_key(__ldcg(z + e)) << 32) | (unsigned)~e : 0ull;
+    }
+    return warp_topk<M>(c, K, lane);
+}
+
 __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
                                                          int T, int tg, int *__restrict__ ids_out,
                                                          float *__restrict__ w_out) {
@@ -164,33 +177,20 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     __threadfence();
     MOE_TRACE_POINT(0, 4);
     if (warp < nt) {
-        // sigmoid scores as order-preserving keys: bits(score) + 1 for a
-        // number, 0 for NaN (ranked last); the winner of a round is the
-        // largest key, the lowest expert id among equal keys
+        // sort keys (bits(sigmoid) + 1) << 32 | ~id (a NaN logit: 0 << 32 |
+        // ~id): larger is better, ties in the score go to the lower id; lane
+        // j < k ends with the j-th choice
         const int t = t0 + warp;
-        unsigned key[kMaxExperts / 32], id[kMaxExperts / 32], taken = 0u;
-#pragma unroll
-        for (int m = 0; m < kMaxExperts / 32; ++m) {
-            const int ee = lane + 32 * m;
-            key[m] = 0u;
-            id[m] = 0xffffffffu;
-            if (ee < E) {
-                const float z = __ldcg(d.logits + (size_t)t * E + ee);
-                key[m] = isnan(z) ? 0u : __float_as_uint(1.0f / (1.0f + expf(-z))) + 1u;
-                id[m] = (unsigned)ee;
-            }
+        unsigned long long sel;
+        switch (d.E <= 32 ? 1 : d.E <= 64 ? 2 : d.E <= 128 ? 4 : d.E <= 256 ? 8 : 16) {
+            case 1: sel = token_topk<1>(d.logits + (size_t)t * E, E, K, lane); break;
+            case 2: sel = token_topk<2>(d.logits + (size_t)t * E, E, K, lane); break;
+            case 4: sel = token_topk<4>(d.logits + (size_t)t * E, E, K, lane); break;
+            case 8: sel = token_topk<8>(d.logits + (size_t)t * E, E, K, lane); break;
+            default: sel = token_topk<16>(d.logits + (size_t)t * E, E, K, lane); break;
         }
-        unsigned sel_key = 0u;
-        int sel_e = 0;
-#pragma unroll 1
-        for (int j = 0; j < K; ++j) {
-            unsigned mx, win;
-            select_round<kMaxExperts / 32>(key, id, taken, mx, win);
-            if (lane == j) {
-                sel_key = mx;
-                sel_e = (int)win;
-            }
-        }
+        const unsigned sel_key = (unsigned)(sel >> 32);
+        const int sel_e = (int)~(unsigned)sel;
         // weights: normalised over the k selected scores (summed in selection order)
         const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
         float sum = 0.f;

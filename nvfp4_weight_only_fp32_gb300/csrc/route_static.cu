@@ -113,7 +113,7 @@ route_static_kernel(const float *__restrict__ Wr, const float *__restrict__ bias
             float s = -INFINITY;
             if (ee < E) {
                 const float z = __ldcg(logits + (size_t)t * E + ee);
-                s = isnan(z) ? -INFINITY : 1.0f / (1.0f + expf(-z));
+                s = isnan(z) ? -INFINITY : moe::sigmoid_score(z);
             }
             sc[m] = s;
         }

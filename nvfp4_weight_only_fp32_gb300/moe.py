@@ -31,7 +31,7 @@ EXPORTED = [
     "moe_route_topk_static", "moe_trace_attach", "moe_debug_inject",
 ]
 
-MOE_INJECT_BARRIER_STALL = 1
+MOE_INJECT_WAIT_STALL = 1
 
 
 class moe_config(ctypes.Structure):

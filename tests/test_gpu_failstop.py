@@ -2,8 +2,9 @@
 
 The ML4 page's persistent decode kernel ("Specialized decode", "Fail-stop")
 bounds every in-kernel wait and reports instead of hanging.  Here the test
-hook makes one call's first grid barrier wait for one arrival more than
-there are blocks -- a flag nothing sets: the wait must give up after about a
+hook makes one call's first grid-wide wait (each block polls the router
+logits the other blocks publish, tagged with the call number) expect a tag
+one call ahead -- words nothing writes: the wait must give up after about a
 second, moe_check must report the timeout, and the next call on the same
 handle must be correct again."""
 import time
@@ -25,7 +26,7 @@ def moe():
     return load_moe()
 
 
-def test_grid_barrier_gives_up_and_the_handle_recovers(moe, orc):
+def test_grid_wait_gives_up_and_the_handle_recovers(moe, orc):
     import torch
     layer, x, _ = guarded_case(1, gen.BASE_SEED + 11, T=1)
     L = moe.MoELayer(layer, max_tokens=8)
@@ -38,7 +39,7 @@ def test_grid_barrier_gives_up_and_the_handle_recovers(moe, orc):
         assert moe.moe_check(L.h) == moe.MOE_OK
         good = out_to_bits(out)
         # the stalled call: returns (launch OK), the wait runs out on the GPU
-        moe.moe_debug_inject(L.h, moe.MOE_INJECT_BARRIER_STALL, 1)
+        moe.moe_debug_inject(L.h, moe.MOE_INJECT_WAIT_STALL, 1)
         t0 = time.time()
         L.forward(xd)
         rc = moe.moe_check(L.h)
@@ -62,7 +63,7 @@ def test_inject_rejects_bad_arguments(moe):
         with pytest.raises(moe.MoEError):
             moe.moe_debug_inject(L.h, 99, 1)
         with pytest.raises(moe.MoEError):
-            moe.moe_debug_inject(L.h, moe.MOE_INJECT_BARRIER_STALL, -1)
-        moe.moe_debug_inject(L.h, moe.MOE_INJECT_BARRIER_STALL, 0)
+            moe.moe_debug_inject(L.h, moe.MOE_INJECT_WAIT_STALL, -1)
+        moe.moe_debug_inject(L.h, moe.MOE_INJECT_WAIT_STALL, 0)
     finally:
         L.close()
