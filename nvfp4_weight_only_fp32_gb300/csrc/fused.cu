@@ -53,15 +53,26 @@ namespace moe {
 
 namespace {
 
+// Phase point i of the traced build: %globaltimer under kernel slot 0 (for
+// the order across blocks) and the SM clock under slot 3 (cycle-exact within
+// a block).
+#define FUSED_TRACE(i)           \
+    do {                         \
+        MOE_TRACE_POINT(0, (i)); \
+        MOE_TRACE_CLOCK(3, (i)); \
+    } while (0)
+
 constexpr int kFW = 16;                                  // warps per block
 constexpr int kFT = 32 * kFW;
 constexpr int kTF = 8;                                   // tokens (MMA N)
+constexpr int kPW = 8;                                   // warps of the shared-expert pass; the others route
 constexpr int kREmax = 4;                                // router experts per block
+static_assert(kTF * kREmax == 32, "the logit reduction gives each lane one (token, expert) value");
 constexpr int kCHmax = 8;                                // chunks per ring segment
 constexpr int kCHmin = 4;
 constexpr int kRWmax = 6;                                // ring segments per warp
-constexpr int kSlotsF = kTF * kMaxTopK + kMaxShared;     // slots of a call with T <= 8
-constexpr int kPairsF = kTF * (kMaxTopK + kMaxShared);   // pairs of a call with T <= 8
+constexpr int kSlotsF = kFusedSlots;                     // slots of a call with T <= 8
+constexpr int kPairsF = kFusedPairs;                     // pairs of a call with T <= 8
 constexpr int kM1max = 8;                                // experts per lane in the top-k (E <= 256)
 constexpr int kTabMax = 32;                              // copy-list items per warp
 constexpr int kHU = 4;                                   // tagged h pieces in flight per lane
@@ -95,10 +106,10 @@ inline size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
 
 // Groups of ks warps share a gate/up unit by splitting K; ks minimises the
 // chunks of the busiest warp plus one chunk's worth per unit (the epilogue).
-int choose_lks(int units, int NC, int G) {
+int choose_lks(int units, int NC, int G, int nw) {
     int best = 0, bestc = 0x7fffffff;
-    for (int l = 0; (1 << l) <= kFW && NC % (1 << l) == 0; ++l) {
-        const int groups = G * (kFW >> l);
+    for (int l = 0; (1 << l) <= nw && NC % (1 << l) == 0; ++l) {
+        const int groups = G * (nw >> l);
         const int cost = (units + groups - 1) / groups * (NC / (1 << l) + 1);
         if (cost < bestc) {
             bestc = cost;
@@ -132,9 +143,9 @@ bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) 
     if (g.RW < 2) return false;
     const int NC13 = d.H / kChunkK, NTs = d.Is / 8, NT13 = d.I / 8;
     const int ncr = d.I / kChunkK, ncs = d.S > 0 ? d.Is / kChunkK : ncr;
-    g.lks0 = choose_lks(d.S * NTs, NC13, G);
+    g.lks0 = choose_lks(d.S * NTs, NC13, G, kPW);
     for (int n = 0; n <= kSlotsF; ++n) {
-        g.lks1[n] = (unsigned char)choose_lks(std::max(0, n - d.S) * NT13, NC13, G);
+        g.lks1[n] = (unsigned char)choose_lks(std::max(0, n - d.S) * NT13, NC13, G, kFW);
         int l = 0;
         while (n * (2 << l) <= kFW && ncr % (2 << l) == 0 && ncs % (2 << l) == 0 && ncr / (2 << l) >= 2 &&
                ncs / (2 << l) >= 2)
@@ -144,7 +155,7 @@ bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) 
     // every warp's copy list (units of both passes + down pieces) must fit
     // its table, whatever the number of distinct experts
     const int NRT = d.H / 16, nrt = (NRT + G - 1) / G;
-    const int my0 = (d.S * NTs + G * (kFW >> g.lks0) - 1) / (G * (kFW >> g.lks0));
+    const int my0 = (d.S * NTs + G * (kPW >> g.lks0) - 1) / (G * (kPW >> g.lks0));
     for (int n = d.S + 1; n <= d.S + std::min(d.E, T * d.k); ++n) {
         const int my1 = ((n - d.S) * NT13 + G * (kFW >> g.lks1[n]) - 1) / (G * (kFW >> g.lks1[n]));
         const int perw = ((n << g.lksd[n]) + kFW - 1) / kFW;
@@ -298,7 +309,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     __shared__ float s_hun[kPairsF + 1];
     __shared__ __align__(16) int s_wsum[2][kFW];
     __shared__ int s_nslots;
-    __shared__ float s_lpart[kFW][kREmax][kTF];
+    __shared__ float s_lpart[kFW][kTF * kREmax];
     __shared__ __align__(16) float s_red[kFW][4][32];
 
     const int T = a.T, H = d.H, E = d.E, K = d.k, S = d.S;
@@ -344,15 +355,15 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     struct Pass {
         int lks, cpw, cb0, stride, u0, my, NT, lo;
     };
-    auto plan = [&](int units, int lks, int NT, int lo) {
+    auto plan = [&](int units, int lks, int NT, int lo, int nw) {
         Pass p;
-        const int ngrp = kFW >> lks;
+        const int ngrp = nw >> lks;
         p.lks = lks;
         p.cpw = NC13 >> lks;
         p.cb0 = (warp & ((1 << lks) - 1)) * p.cpw;
         p.stride = G * ngrp;
         p.u0 = c * ngrp + (warp >> lks);
-        p.my = p.u0 < units ? (units - p.u0 + p.stride - 1) / p.stride : 0;
+        p.my = warp < nw && p.u0 < units ? (units - p.u0 + p.stride - 1) / p.stride : 0;
         p.NT = NT;
         p.lo = lo;
         return p;
@@ -369,7 +380,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         }
     };
 
-    MOE_TRACE_POINT(0, 0);
+    FUSED_TRACE(0);
     MOE_TRACE_CLOCK(1, 0);
     // ---------------- A: static data before the dependency wait ----------------
     if (threadIdx.x < S) {
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         for (int i = 0; i < RW; ++i) mbar_init(bar + i, 1);
         fence_proxy_async();
     }
-    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0);
+    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW);
     __syncthreads();
     fill_units(p0, 0);
     __syncwarp();
@@ -410,7 +421,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     pump(RW);
     pdl_wait();
     pdl_trigger();
-    MOE_TRACE_POINT(0, 1);
+    FUSED_TRACE(1);
 
     // ---------------- B: x, logits ----------------
     bool ok = true;
@@ -422,22 +433,64 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     }
     if (!mbar_wait(&s_xbar, 0u, d.err) || !mbar_wait(&s_rbar, 0u, d.err)) ok = false;
     const int nq = H / 4;                    // 4-element quads of an activation row
-    // per-token max |x| -> exact power-of-two prescale for the f16 MMA operand
-#pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-        float m = 0.f;
+    // One pass over x for all tokens: this thread's max |x| per token and its
+    // partial FP32 logits (token t, expert c + re * G) from the exact FP32
+    // values of x; each router quad is read once for all tokens.
+    {
+        float mx[kTF], acc[kTF * kREmax];
+#pragma unroll
+        for (int t = 0; t < kTF; ++t) mx[t] = 0.f;
+#pragma unroll
+        for (int i = 0; i < kTF * kREmax; ++i) acc[i] = 0.f;
 #pragma unroll
         for (int xp = 0; xp < QP; ++xp) {
             const int P = threadIdx.x + xp * kFT;
             if (P < nq) {
-                const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
-                m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(v.x << 16)), fabsf(__uint_as_float(v.x & 0xFFFF0000u))),
-                                   fmaxf(fabsf(__uint_as_float(v.y << 16)), fabsf(__uint_as_float(v.y & 0xFFFF0000u)))));
+                float4 w4[kREmax];
+#pragma unroll
+                for (int re = 0; re < kREmax; ++re)
+                    if (re < kRE) w4[re] = *reinterpret_cast<const float4 *>(s_router + (size_t)re * H + 4 * P);
+#pragma unroll
+                for (int t = 0; t < kTF; ++t) {
+                    if (t < T) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
+                        const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+                        const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+                        mx[t] = fmaxf(mx[t], fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
+#pragma unroll
+                        for (int re = 0; re < kREmax; ++re)
+                            if (re < kRE)
+                                acc[t * kREmax + re] = fmaf(x3, w4[re].w, fmaf(x2, w4[re].z, fmaf(x1, w4[re].y,
+                                                            fmaf(x0, w4[re].x, acc[t * kREmax + re]))));
+                    }
+                }
             }
         }
-        // m >= 0 and not NaN (fmaxf drops NaN): its bits order as unsigned
-        m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
-        if (lane == 0) s_tmax[warp][t] = m;
+        // warp maxima per token (mx >= 0 and not NaN -- fmaxf drops NaN --
+        // so its bits order as unsigned)
+#pragma unroll
+        for (int t = 0; t < kTF; ++t) {
+            if (t < T) {
+                const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx[t])));
+                if (lane == 0) s_tmax[warp][t] = m;
+            }
+        }
+        // warp sums of the 32 partial logits by a transposing butterfly: at
+        // the step of distance w every lane keeps the half of its values
+        // selected by bit w of its lane index and adds the partner's copy of
+        // that half; lane L ends with value L (token L / kREmax, expert L %
+        // kREmax)
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+                const bool up = (lane & w) != 0;
+                const float send = up ? acc[i] : acc[i + w];
+                const float keep = up ? acc[i + w] : acc[i];
+                acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+        }
+        s_lpart[warp][lane] = acc[0];
     }
     __syncthreads();
     if (threadIdx.x < T) {
@@ -446,65 +499,46 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         for (int w = 0; w < kFW; ++w) m = fmaxf(m, s_tmax[w][threadIdx.x]);
         s_xexp[threadIdx.x] = max(-100, exp_for_f16(m));
     }
+    if (threadIdx.x < kTF * kREmax) {
+        // logits: the warps' sums in a fixed order, plus the router bias
+        const int t = threadIdx.x / kREmax, re = threadIdx.x % kREmax, e = c + re * G;
+        if (re < kRE && e < E && t < T) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kFW; ++w) v += s_lpart[w][threadIdx.x];
+            st_tagged(d.logit_tag + (size_t)t * E + e, s_tag, __float_as_uint(v + s_gsp[e].w));
+        }
+    }
     // zero row T (the B column of absent tokens)
     for (int i = threadIdx.x; i < fg.xrow / 16; i += kFT)
         reinterpret_cast<uint4 *>(xs + (size_t)T * fg.xrow)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-    MOE_TRACE_POINT(0, 2);
+    FUSED_TRACE(2);
     // x' = x * 2^-xexp as f16, permuted within each 64-element chunk (element
     // 16kb + 8h + 2q + e sits at half 16q + 4kb + 2h + e: quad m of a chunk,
     // elements 4m..4m+3, has kb = m/4, h = (m/2)%2 and q = 2(m%2) for its
-    // first pair, q + 1 for its second), and the FP32 logits of this block's
-    // experts from the exact FP32 values of x (fixed-order reductions: lanes
-    // by butterfly, then warps)
-#pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-        const float sc = pow2f(-s_xexp[t]);
-        float acc[kREmax];
+    // first pair, q + 1 for its second)
 #pragma unroll
-        for (int re = 0; re < kREmax; ++re) acc[re] = 0.f;
+    for (int xp = 0; xp < QP; ++xp) {
+        const int P = threadIdx.x + xp * kFT;
+        if (P < nq) {
+            const int m = P & 15, kb = m >> 2, hh = (m >> 1) & 1, q0 = 2 * (m & 1);
 #pragma unroll
-        for (int xp = 0; xp < QP; ++xp) {
-            const int P = threadIdx.x + xp * kFT;
-            if (P < nq) {
-                const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
-                const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
-                const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-                const int m = P & 15, kb = m >> 2, hh = (m >> 1) & 1, q0 = 2 * (m & 1);
-                uint8_t *row = xs + (size_t)t * fg.xrow + (P >> 4) * 128;
-                *reinterpret_cast<uint32_t *>(row + 32 * q0 + 8 * kb + 4 * hh) = pack_f16x2(x0 * sc, x1 * sc);
-                *reinterpret_cast<uint32_t *>(row + 32 * (q0 + 1) + 8 * kb + 4 * hh) = pack_f16x2(x2 * sc, x3 * sc);
-#pragma unroll
-                for (int re = 0; re < kREmax; ++re) {
-                    if (re < kRE) {
-                        const float4 w4 = *reinterpret_cast<const float4 *>(s_router + (size_t)re * H + 4 * P);
-                        acc[re] = fmaf(x3, w4.w, fmaf(x2, w4.z, fmaf(x1, w4.y, fmaf(x0, w4.x, acc[re]))));
-                    }
+            for (int t = 0; t < kTF; ++t) {
+                if (t < T) {
+                    const float sc = pow2f(-s_xexp[t]);
+                    const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
+                    const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+                    const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+                    uint8_t *row = xs + (size_t)t * fg.xrow + (P >> 4) * 128;
+                    *reinterpret_cast<uint32_t *>(row + 32 * q0 + 8 * kb + 4 * hh) = pack_f16x2(x0 * sc, x1 * sc);
+                    *reinterpret_cast<uint32_t *>(row + 32 * (q0 + 1) + 8 * kb + 4 * hh) = pack_f16x2(x2 * sc, x3 * sc);
                 }
-            }
-        }
-#pragma unroll
-        for (int re = 0; re < kREmax; ++re) {
-            if (re < kRE) {
-                float v = acc[re];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                if (lane == 0) s_lpart[warp][re][t] = v;
             }
         }
     }
     __syncthreads();
-    if (threadIdx.x < kREmax * kTF) {
-        const int re = threadIdx.x / kTF, t = threadIdx.x % kTF;
-        const int e = c + re * G;
-        if (re < kRE && e < E && t < T) {
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kFW; ++w) v += s_lpart[w][re][t];
-            st_tagged(d.logit_tag + (size_t)t * E + e, s_tag, __float_as_uint(v + s_gsp[e].w));
-        }
-    }
-    MOE_TRACE_POINT(0, 3);
+    FUSED_TRACE(3);
 
     // ---------------- C: gate/up, pass 0 shared experts, pass 1 routed ----------------
     const uint8_t *xb = xs + (size_t)(g < T ? g : T) * fg.xrow + q * 32;
@@ -515,65 +549,65 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         Pass pp = p0;
-        if (pass == 1) {
-            MOE_TRACE_POINT(0, 4);
+        if (pass == 0 && warp >= kPW && warp < kPW + T) {
             // routing, identical in every block, straight from the tagged
-            // logits (no grid barrier): warp t < T takes token t, lane L the
-            // experts i * 32 + L.  An expert's sort key is (bits(sigmoid) +
-            // 1) << 32 | ~id (a NaN logit: 0 << 32 | ~id): larger is better,
-            // ties in the score go to the lower id, all keys differ.
+            // logits (no grid barrier), while warps 0..kPW-1 run the shared
+            // experts: warp kPW + t takes token t, lane L the experts i * 32
+            // + L.  An expert's sort key is (bits(sigmoid) + 1) << 32 | ~id
+            // (a NaN logit: 0 << 32 | ~id): larger is better, ties in the
+            // score go to the lower id, all keys differ.
+            const int t = warp - kPW;
             const unsigned ltag = s_tag + (unsigned)d.debug_stall;
             int lpass = 0;
             unsigned long long sel = 0ull;
-            if (warp < T) {
-                switch (fg.m1p) {
-                    case 1: ok = route_token<1>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                    case 2: ok = route_token<2>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                    case 4: ok = route_token<4>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                    default: ok = route_token<8>(d.logit_tag, warp, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                }
+            switch (fg.m1p) {
+                case 1: ok = route_token<1>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                case 2: ok = route_token<2>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                case 4: ok = route_token<4>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                default: ok = route_token<8>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
             }
             const unsigned sel_key = (unsigned)(sel >> 32);
             const int sel_e = (int)~(unsigned)sel;
-            MOE_TRACE_POINT(0, 10);
-            MOE_TRACE_VALUE(1, 2, lpass);
+            MOE_TRACE_CLOCK_AT(3, 10, 32 * kPW);
+            MOE_TRACE_VALUE_AT(1, 2, 32 * kPW, lpass);
             // weights (normalised in selection order); for one token the
             // slots follow directly: routed slot S + (rank of the id among
             // the k choices), one pair each
-            if (warp < T) {
-                const int t = warp;
-                const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
-                float sum = 0.f;
-                int rank = 0;
+            const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
+            float sum = 0.f;
+            int rank = 0;
 #pragma unroll 1
-                for (int j = 0; j < K; ++j) {
-                    sum += __shfl_sync(0xffffffffu, sel_s, j);
-                    rank += __shfl_sync(0xffffffffu, sel_e, j) < sel_e;
-                }
-                if (lane < K) {
-                    const float w = (d.normalize ? sel_s / sum : sel_s) * d.routed_scale;
-                    s_ids[t][lane] = sel_e;
-                    s_w[t][lane] = w;
-                    if (c == 0) {
-                        if (a.ids_out) a.ids_out[t * K + lane] = sel_e;
-                        if (a.w_out) a.w_out[t * K + lane] = w;
-                    }
-                    if (T == 1) {
-                        s_slot_e[S + rank] = sel_e;
-                        s_slot_mask[S + rank] = 1;
-                        s_slot_p0[S + rank] = S + rank;
-                        s_pw[S + rank] = w;
-                    } else {
-                        atomicOr(reinterpret_cast<unsigned *>(s_tokmask) + (sel_e >> 2), 1u << (8 * (sel_e & 3) + t));
-                    }
-                }
-                if (T == 1 && lane == 0) s_nslots = S + K;
+            for (int j = 0; j < K; ++j) {
+                sum += __shfl_sync(0xffffffffu, sel_s, j);
+                rank += __shfl_sync(0xffffffffu, sel_e, j) < sel_e;
             }
+            if (lane < K) {
+                const float w = (d.normalize ? sel_s / sum : sel_s) * d.routed_scale;
+                s_ids[t][lane] = sel_e;
+                s_w[t][lane] = w;
+                if (c == 0) {
+                    if (a.ids_out) a.ids_out[t * K + lane] = sel_e;
+                    if (a.w_out) a.w_out[t * K + lane] = w;
+                }
+                if (T == 1) {
+                    s_slot_e[S + rank] = sel_e;
+                    s_slot_mask[S + rank] = 1;
+                    s_slot_p0[S + rank] = S + rank;
+                    s_pw[S + rank] = w;
+                } else {
+                    atomicOr(reinterpret_cast<unsigned *>(s_tokmask) + (sel_e >> 2), 1u << (8 * (sel_e & 3) + t));
+                }
+            }
+            if (T == 1 && lane == 0) s_nslots = S + K;
+            MOE_TRACE_CLOCK_AT(3, 5, 32 * kPW);
+        }
+        if (pass == 1) {
+            FUSED_TRACE(4);
             if (!__syncthreads_and(ok)) {
                 ok = false;
                 break;
             }
-            MOE_TRACE_POINT(0, 11);
+            FUSED_TRACE(11);
             if (T > 1) {
                 // slots: shared first, then routed experts in ascending id
                 // (one expert per thread); an expert's pairs are contiguous,
@@ -615,10 +649,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     s_pw[s_slot_p0[sl] + __popc(s_slot_mask[sl] & ((1 << t) - 1))] = s_w[t][j];
                 }
             }
-            MOE_TRACE_POINT(0, 12);
+            FUSED_TRACE(12);
             // this warp's routed units and down pieces -> its copy list
             nslots = s_nslots;
-            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S);
+            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW);
             fill_units(pp, p0.my);
             lksd = fg.lksd[nslots];
             perw = warp < (nslots << lksd) ? ((nslots << lksd) - warp + kFW - 1) / kFW : 0;
@@ -636,7 +670,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             n_known = p0.my + pp.my + nrt * perw;
             if (ok) pump(n_con + RW);
             __syncwarp();
-            MOE_TRACE_POINT(0, 6);
+            FUSED_TRACE(6);
         }
         const int ks = 1 << pp.lks, gi = warp >> pp.lks, kw = warp & (ks - 1);
         // every warp of a group has the same unit count, so the group's named
@@ -653,6 +687,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
                     else ok = false;
                 }
+                if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK(2, 4 * pass);
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
@@ -668,6 +703,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
                 if (ok) pump(n_con + RW);
             }
+            if (ui == 0) MOE_TRACE_CLOCK(2, 4 * pass + 1);
 #pragma unroll
             for (int v = 0; v < 4; ++v) a0[v] += a1[v];
             const int uu = pp.u0 + ui * pp.stride;
@@ -684,6 +720,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
                 asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
             }
+            if (ui == 0) MOE_TRACE_CLOCK(2, 4 * pass + 2);
             if (kw == 0 && __all_sync(0xffffffffu, ok)) {
                 // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row
                 // 8r+g; lanes g and g+1 publish one tagged word of two BF16
@@ -706,18 +743,19 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                         st_tagged(d.h_tag + ((size_t)p * d.Imax + 8 * r + g) / 2, s_tag, hbits | (hnext << 16));
                 }
             }
+            MOE_TRACE_CLOCK(2, 4 * pass + 3);
         }
     }
-    MOE_TRACE_POINT(0, 7);
+    FUSED_TRACE(7);
     // every warp is done with x and its gate/up units before phase D reuses
     // the shared memory; a block without output tiles is done
     if (!__syncthreads_and(ok) || nrt == 0) {
         drain_ring(bar, RW, n_done, n_iss, lane);
-        MOE_TRACE_POINT(0, 9);
+        FUSED_TRACE(9);
         if (threadIdx.x == 0) d.calls[c] = s_tag;
         return;
     }
-    MOE_TRACE_POINT(0, 8);
+    FUSED_TRACE(8);
 
     // ---------------- D: down + combine, 16 output rows per tile ----------------
     // gather every pair's h row from the tagged words (one warp per row,
@@ -790,11 +828,11 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     MOE_TRACE_VALUE(1, 3, hpass);
     if (!__syncthreads_and(ok)) {
         drain_ring(bar, RW, n_done, n_iss, lane);
-        MOE_TRACE_POINT(0, 9);
+        FUSED_TRACE(9);
         if (threadIdx.x == 0) d.calls[c] = s_tag;
         return;
     }
-    MOE_TRACE_POINT(0, 14);
+    FUSED_TRACE(14);
 #pragma unroll 1
     for (int ri = 0; ri < nrt; ++ri) {
         const int rt = c + ri * G;
@@ -818,6 +856,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
                     else ok = false;
                 }
+                if (ri == 0 && r2 == 0 && lft == cpk) MOE_TRACE_CLOCK(2, 10);
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
@@ -833,6 +872,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
                 if (ok) pump(n_con + RW);
             }
+            if (ri == 0) MOE_TRACE_CLOCK(2, 11);
             // y = gs * 2^hexp * acc, weighted into the per-token accumulator
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
@@ -849,7 +889,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll
         for (int v = 0; v < 4; ++v) s_red[warp][v][lane] = oa[v];
         __syncthreads();
-        MOE_TRACE_POINT(0, 15);
+        FUSED_TRACE(15);
         if (warp == 0) {
             float o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -868,7 +908,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         __syncthreads();
     }
     if (!ok) drain_ring(bar, RW, n_done, n_iss, lane);
-    MOE_TRACE_POINT(0, 9);
+    FUSED_TRACE(9);
     MOE_TRACE_CLOCK(1, 9);
     if (threadIdx.x == 0) d.calls[c] = s_tag;
 }

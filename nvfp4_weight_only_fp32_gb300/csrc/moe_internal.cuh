@@ -48,6 +48,8 @@ constexpr int kMaxTokens = 64;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxShared = 2;
+constexpr int kFusedSlots = 8 * kMaxTopK + kMaxShared;   // slots of a single-launch call (T <= 8)
+constexpr int kFusedPairs = 8 * (kMaxTopK + kMaxShared); // (token, expert) pairs of such a call
 constexpr int kRouteWarps = 8;     // experts per router CTA
 
 // Everything a kernel needs to know about a layer (passed by value).
@@ -145,49 +147,42 @@ __host__ __device__ inline size_t repacked_bytes(int rows, int cols) {
 // ---------------------------------------------------------------------------
 #if defined(__CUDACC__)
 
-// Phase tracing, compiled only into the traced build (-DMOE_TRACE): thread 0
-// of each block stores %globaltimer at numbered points into the buffer that
-// moe_trace_attach() installed in DevLayer ([kernel][block][16] u64).  In the
-// regular build every trace point is empty.
+// Phase tracing, compiled only into the traced build (-DMOE_TRACE): one
+// thread of each block (thread 0 unless named) stores %globaltimer, the SM
+// cycle counter or a count at numbered points into the buffer that
+// moe_trace_attach() installed in DevLayer ([kernel slot][block][16] u64).
+// In the regular build every trace point is empty.
 #ifdef MOE_TRACE
-#define MOE_TRACE_POINT(kid, i)                                                                  \
+#define MOE_TRACE_STORE_(kid, i, tid, val)                                                       \
     do {                                                                                         \
-        if (threadIdx.x == 0 && d.trace) {                                                       \
-            unsigned long long t_;                                                               \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                               \
-            const int b_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
-            if (b_ < d.trace_blocks) d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = t_; \
-        }                                                                                        \
-    } while (0)
-// SM cycle counter at a point, stored under kernel slot `kid` (pairs with
-// the timestamps of another slot to give the effective SM clock).
-#define MOE_TRACE_CLOCK(kid, i)                                                                  \
-    do {                                                                                         \
-        if (threadIdx.x == 0 && d.trace) {                                                       \
-            const int b_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
-            if (b_ < d.trace_blocks) d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = clock64(); \
-        }                                                                                        \
-    } while (0)
-// A value (a count) stored under kernel slot `kid`, from thread 0.
-#define MOE_TRACE_VALUE(kid, i, v)                                                               \
-    do {                                                                                         \
-        if (threadIdx.x == 0 && d.trace) {                                                       \
+        if (threadIdx.x == (tid) && d.trace) {                                                   \
             const int b_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
             if (b_ < d.trace_blocks)                                                             \
-                d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = (unsigned long long)(v); \
+                d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = (unsigned long long)(val); \
         }                                                                                        \
     } while (0)
+__device__ __forceinline__ unsigned long long moe_globaltimer_() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+#define MOE_TRACE_POINT_AT(kid, i, tid) MOE_TRACE_STORE_(kid, i, tid, moe_globaltimer_())
+#define MOE_TRACE_CLOCK_AT(kid, i, tid) MOE_TRACE_STORE_(kid, i, tid, clock64())
+#define MOE_TRACE_VALUE_AT(kid, i, tid, v) MOE_TRACE_STORE_(kid, i, tid, v)
 #else
-#define MOE_TRACE_POINT(kid, i) \
-    do {                        \
+#define MOE_TRACE_POINT_AT(kid, i, tid) \
+    do {                                \
     } while (0)
-#define MOE_TRACE_CLOCK(kid, i) \
-    do {                        \
+#define MOE_TRACE_CLOCK_AT(kid, i, tid) \
+    do {                                \
     } while (0)
-#define MOE_TRACE_VALUE(kid, i, v) \
-    do {                           \
+#define MOE_TRACE_VALUE_AT(kid, i, tid, v) \
+    do {                                   \
     } while (0)
 #endif
+#define MOE_TRACE_POINT(kid, i) MOE_TRACE_POINT_AT(kid, i, 0)
+#define MOE_TRACE_CLOCK(kid, i) MOE_TRACE_CLOCK_AT(kid, i, 0)
+#define MOE_TRACE_VALUE(kid, i, v) MOE_TRACE_VALUE_AT(kid, i, 0, v)
 
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -438,8 +433,10 @@ __device__ __forceinline__ void decode_chunk(const uint4 &cw, const uint2 &sw,
     for (int i = 0; i < 4; ++i) {
         uint32_t sp = (i < 2) ? (sw.x >> (16 * i)) : (sw.y >> (16 * (i - 2)));
         uint32_t s2 = e4m3x2_to_f16x2(sp & 0xFFFFu);     // {s(row g), s(row g+8)}
-        uint32_t sg = __byte_perm(s2, 0, 0x1010);        // {s_g, s_g}
-        uint32_t sg8 = __byte_perm(s2, 0, 0x3232);       // {s_g8, s_g8}
+        uint32_t sg, sg8;                                // {s_g, s_g}, {s_g8, s_g8}
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tmov.b32 %0, {lo, lo};\n\t"
+            "mov.b32 %1, {hi, hi};\n\t}\n"
+            : "=r"(sg), "=r"(sg8) : "r"(s2));
         uint32_t h0, h1, h2, h3;
         e2m1x8_to_f16x2(words[i], h0, h1, h2, h3);
         a[i][0] = hmul2(h0, sg);
