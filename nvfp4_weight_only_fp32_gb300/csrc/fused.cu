@@ -75,7 +75,7 @@ constexpr int kSlotsF = kFusedSlots;                     // slots of a call with
 constexpr int kPairsF = kFusedPairs;                     // pairs of a call with T <= 8
 constexpr int kM1max = 8;                                // experts per lane in the top-k (E <= 256)
 constexpr int kTabMax = 32;                              // copy-list items per warp
-constexpr int kHU = 4;                                   // tagged h pieces in flight per lane
+constexpr int kHU = 8;                                   // tagged h pieces in flight per lane
 constexpr unsigned long long kWaitNs = 1000000000ull;    // in-kernel waits give up after ~1 s
 
 struct FusedArgs {
@@ -230,7 +230,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *bar, int RW, int n_done, in
 // decode + 4 MMAs of one chunk held in shared memory, against the B row of
 // this lane's column; blocks 0/2 and 1/3 go to two accumulators so that the
 // MMA dependency chain is half as long.
-__device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, const uint8_t *bp,
+__device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, const uint8_t *bp, bool bon,
                                                float (&a0)[4], float (&a1)[4]) {
     const uint4 cw = lds128(ch + 16 * lane);
     uint2 sw;
@@ -238,8 +238,8 @@ __device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, cons
                  : "=r"(sw.x), "=r"(sw.y) : "r"(smem_u32(ch + kCodeBytes + 8 * (lane >> 2))));
     uint32_t a[4][4];
     decode_chunk(cw, sw, a);
-    const uint4 b01 = lds128(bp);
-    const uint4 b23 = lds128(bp + 16);
+    const uint4 b01 = bon ? lds128(bp) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 b23 = bon ? lds128(bp + 16) : make_uint4(0u, 0u, 0u, 0u);
     mma_16816(a0, a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
     mma_16816(a1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
     mma_16816(a0, a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     __shared__ int s_slot_mask[kSlotsF];
     __shared__ int s_slot_p0[kSlotsF];
     __shared__ float s_pw[kPairsF];
-    __shared__ float s_hun[kPairsF + 1];
+    __shared__ signed char s_hx[kPairsF][8];                 // h prescale exponents by pair and K part
     __shared__ __align__(16) int s_wsum[2][kFW];
     __shared__ int s_nslots;
     __shared__ float s_lpart[kFW][kTF * kREmax];
@@ -332,6 +332,9 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     const uint8_t *src = nullptr;
     auto pump = [&](int limit) {
         if (lane != 0) return;
+        // one proxy fence orders the warp's reads of the slots about to be
+        // refilled before all of this call's copies
+        if (n_iss < limit && (left > 0 || it < n_known)) fence_proxy_async();
         while (n_iss < limit) {
             if (left == 0) {
                 if (it >= n_known) break;
@@ -340,7 +343,6 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 ++it;
             }
             const int n = min(CH, left);
-            fence_proxy_async();
             mbar_expect_tx(bar + sl_p, (unsigned)(n * kChunkBytes));
             bulk_g2s(ring + (size_t)sl_p * CH * kChunkBytes, src, (unsigned)(n * kChunkBytes), bar + sl_p, pol);
             src += (size_t)n * kChunkBytes;
@@ -432,6 +434,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         bulk_g2s(smem + fg.xraw_off, a.x, (unsigned)(T * H * 2), &s_xbar, pol);
     }
     if (!mbar_wait(&s_xbar, 0u, d.err) || !mbar_wait(&s_rbar, 0u, d.err)) ok = false;
+    MOE_TRACE_CLOCK(2, 12);
     const int nq = H / 4;                    // 4-element quads of an activation row
     // One pass over x for all tokens: this thread's max |x| per token and its
     // partial FP32 logits (token t, expert c + re * G) from the exact FP32
@@ -492,7 +495,9 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         }
         s_lpart[warp][lane] = acc[0];
     }
+    MOE_TRACE_CLOCK(2, 13);
     __syncthreads();
+    MOE_TRACE_CLOCK(2, 9);
     if (threadIdx.x < T) {
         float m = 0.f;
 #pragma unroll
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     int n_con = 0, sl_c = 0;             // segments consumed by this warp; its ring slot
     unsigned par_c = 0u;                 // and the slot's phase parity
     int n_done = 0;                      // segments whose copies have landed (waited for)
-    int nslots = S, lksd = 0, perw = 0, nrt = 0;
+    int nslots = S, lksd = 0, perw = 0, nrt = 0, n_list = 0;
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         Pass pp = p0;
@@ -667,8 +672,11 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 s_tab_n[warp][p0.my + pp.my + i] = cpk;
             }
             __syncwarp();
-            n_known = p0.my + pp.my + nrt * perw;
+            MOE_TRACE_CLOCK(2, 14);
+            n_list = p0.my + pp.my + nrt * perw;
+            n_known = n_list;
             if (ok) pump(n_con + RW);
+            MOE_TRACE_CLOCK(2, 15);
             __syncwarp();
             FUSED_TRACE(6);
         }
@@ -691,7 +699,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
-                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, a0, a1);
+                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, true, a0, a1);
                 }
                 __syncwarp();
                 bp += n * 128;
@@ -758,30 +766,34 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     FUSED_TRACE(8);
 
     // ---------------- D: down + combine, 16 output rows per tile ----------------
-    // gather every pair's h row from the tagged words (one warp per row,
-    // polling until each word carries this call's tag) into shared memory in
-    // the MMA operand order, then rescale it in place to f16 by the row's
-    // exact power-of-two prescale; row npairs stays zero (the B column of
-    // tokens a slot does not serve)
-    const int npairs = T * (K + S);
+    // h comes from the tagged words (polled until they carry this call's tag)
+    // into shared memory in the MMA operand order, by tasks (pair p, K part
+    // kp): a task's pieces are all in flight at once (one pass for parts of
+    // up to 32 * kHU pieces), and its range is rescaled to f16 by an exact
+    // power-of-two prescale of its own.  For one or two tokens each warp
+    // gathers the tasks of its own down pieces and starts at once; for more
+    // tokens (the shared expert's slot alone has T rows) the tasks are spread
+    // evenly over the warps and the block waits for all of them.  The B
+    // column of a token a slot does not serve is zero.
     uint8_t *hs = smem;
+    const int npairs = T * (K + S);
     int hpass = 0;
-    for (int i = threadIdx.x; i < fg.hrow / 16; i += kFT)
-        reinterpret_cast<uint4 *>(hs + (size_t)npairs * fg.hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 1
-    for (int j = warp; j < npairs; j += kFW) {
-        const int n = j < S * T ? d.Is : d.I;           // the row's length
-        const int npc = n / 4;                           // 16-byte pieces of tagged words
-        const unsigned long long *src = d.h_tag + (size_t)j * (d.Imax / 2);
-        uint32_t *row = reinterpret_cast<uint32_t *>(hs + (size_t)j * fg.hrow);
+    FUSED_TRACE(14);
+    auto gather = [&](int p, int kp) {
+        const int cpk = (p < S * T ? d.Is : d.I) / kChunkK >> lksd;
+        const int npc = cpk * 16, pc0 = kp * npc;        // 16-byte pieces of the K part; the first
+        const unsigned long long *src = d.h_tag + (size_t)p * (d.Imax / 2) + 2 * pc0;
+        uint32_t *row = reinterpret_cast<uint32_t *>(hs + (size_t)p * fg.hrow);
         float mx = 0.f;
 #pragma unroll 1
         for (int P0 = 0; P0 < npc; P0 += 32 * kHU) {
             unsigned long long v[kHU][2];
             unsigned pend = 0u;          // pieces not yet carrying the tag
 #pragma unroll
-            for (int u = 0; u < kHU; ++u)
+            for (int u = 0; u < kHU; ++u) {
+                v[u][0] = v[u][1] = 0ull;
                 if (P0 + lane + 32 * u < npc) pend |= 1u << u;
+            }
             // every pass re-reads all pending pieces at once
             const unsigned long long t0 = gtimer();
             while (pend && ok) {
@@ -799,14 +811,13 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             }
 #pragma unroll
             for (int u = 0; u < kHU; ++u) {
-                const int P = P0 + lane + 32 * u;
-                if (P < npc) {
+                if (P0 + lane + 32 * u < npc) {
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const unsigned wv = (unsigned)v[u][h2];
                         // word wi of the row (elements 2wi, 2wi+1) -> its
                         // place in the operand order (as for x)
-                        const int wi = 2 * P + h2, l = wi & 31;
+                        const int wi = 2 * (pc0 + P0 + lane + 32 * u) + h2, l = wi & 31;
                         row[(wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1)] = wv;
                         mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wv << 16)), fabsf(__uint_as_float(wv & 0xFFFF0000u))));
                     }
@@ -816,23 +827,40 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         // mx >= 0 and not NaN (fmaxf drops NaN): its bits order as unsigned
         mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
         const int hx = max(-100, exp_for_f16(mx));
-        if (lane == 0) s_hun[j] = pow2f(hx);
+        if (lane == 0) s_hx[p][kp] = (signed char)hx;
         const float sc = pow2f(-hx);
-        __syncwarp();
+        // each lane rescales the words it wrote
 #pragma unroll 1
-        for (int w = lane; w < n / 2; w += 32) {
-            const unsigned wv = row[w];
-            row[w] = pack_f16x2(__uint_as_float(wv << 16) * sc, __uint_as_float(wv & 0xFFFF0000u) * sc);
+        for (int P = lane; P < npc; P += 32) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int wi = 2 * (pc0 + P) + h2, l = wi & 31;
+                uint32_t *w = row + (wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1);
+                const unsigned wv = *w;
+                *w = pack_f16x2(__uint_as_float(wv << 16) * sc, __uint_as_float(wv & 0xFFFF0000u) * sc);
+            }
+        }
+    };
+    if (T <= 2) {
+#pragma unroll 1
+        for (int r2 = 0; r2 < perw; ++r2) {
+            const int pi = warp + kFW * r2, slot = pi >> lksd;
+            const int ntok = __popc(s_slot_mask[slot]), p0s = s_slot_p0[slot];
+#pragma unroll 1
+            for (int k = 0; k < ntok; ++k) gather(p0s + k, pi & ((1 << lksd) - 1));
+        }
+        __syncwarp();
+    } else {
+#pragma unroll 1
+        for (int tk = warp; tk < (npairs << lksd); tk += kFW) gather(tk >> lksd, tk & ((1 << lksd) - 1));
+        if (!__syncthreads_and(ok)) {
+            drain_ring(bar, RW, n_done, n_iss, lane);
+            FUSED_TRACE(9);
+            if (threadIdx.x == 0) d.calls[c] = s_tag;
+            return;
         }
     }
     MOE_TRACE_VALUE(1, 3, hpass);
-    if (!__syncthreads_and(ok)) {
-        drain_ring(bar, RW, n_done, n_iss, lane);
-        FUSED_TRACE(9);
-        if (threadIdx.x == 0) d.calls[c] = s_tag;
-        return;
-    }
-    FUSED_TRACE(14);
 #pragma unroll 1
     for (int ri = 0; ri < nrt; ++ri) {
         const int rt = c + ri * G;
@@ -845,8 +873,9 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             const int msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
             const float gs = s_gsp[e < 0 ? E - e - 1 : e].z;
             const int cpk = (e < 0 ? d.Is : d.I) / kChunkK >> lksd;
-            const int row = ((msk >> g) & 1) ? p0s + __popc(msk & ((1 << g) - 1)) : npairs;
-            const uint8_t *bp = hs + (size_t)row * fg.hrow + q * 32 + kp * cpk * 128;
+            const bool bon = (msk >> g) & 1;
+            const uint8_t *bp = hs + (size_t)(bon ? p0s + __popc(msk & ((1 << g) - 1)) : 0) * fg.hrow + q * 32 +
+                                kp * cpk * 128;
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
             int lft = cpk;
 #pragma unroll 1
@@ -860,7 +889,8 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
-                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, a0, a1);
+                    for (int i = 0; i < n; ++i)
+                        chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, bon, a0, a1);
                 }
                 __syncwarp();
                 bp += n * 128;
@@ -878,8 +908,8 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             for (int e2 = 0; e2 < 2; ++e2) {
                 const int t = 2 * q + e2;
                 if (t < T && ((msk >> t) & 1)) {
-                    const int p = p0s + __popc(msk & ((1 << t) - 1));
-                    const float wgt = s_pw[p] * gs * s_hun[p];
+                    const int k = __popc(msk & ((1 << t) - 1));
+                    const float wgt = s_pw[p0s + k] * gs * pow2f(s_hx[p0s + k][kp]);
                     oa[e2] = fmaf(wgt, a0[e2] + a1[e2], oa[e2]);
                     oa[2 + e2] = fmaf(wgt, a0[2 + e2] + a1[2 + e2], oa[2 + e2]);
                 }
