@@ -659,6 +659,11 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             nslots = s_nslots;
             pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW);
             fill_units(pp, p0.my);
+            __syncwarp();
+            // the routed units' copies start before the down pieces are listed
+            n_known = p0.my + pp.my;
+            if (ok) pump(n_con + RW);
+            MOE_TRACE_CLOCK(4, 5);
             lksd = fg.lksd[nslots];
             perw = warp < (nslots << lksd) ? ((nslots << lksd) - warp + kFW - 1) / kFW : 0;
             nrt = c < NRT ? (NRT - c + G - 1) / G : 0;
