@@ -46,10 +46,9 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20753920, "fused_cu_sha256_16": "09c695b3065df2f3"},
-    "flint8": {"bytes": 124603136, "fused_cu_sha256_16": "09c695b3065df2f3"},
+    "flint1": {"bytes": 20772352, "fused_cu_sha256_16": "ea91cb6c646f7081"},
+    "flint8": {"bytes": 124616448, "fused_cu_sha256_16": "ea91cb6c646f7081"},
 }
-
 
 def ncu_traffic(workload: str):
     import hashlib
