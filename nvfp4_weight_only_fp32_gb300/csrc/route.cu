@@ -34,6 +34,7 @@ namespace {
 constexpr int kThreads = 32 * kRouteWarps;
 constexpr int kTokGroup = 8;
 constexpr int kPre = 16;    // float4 per lane fetched before the wait (2048 K)
+constexpr int kTail = 8;    // float4 per lane in flight for the rest of a longer row
 
 __device__ __forceinline__ void bf16x4_to_f(uint2 v, float &a, float &b, float &c, float &e) {
     a = __uint_as_float(v.x << 16);
@@ -143,15 +144,25 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
                 }
             }
         }
+        // the rest of a long row: kTail loads per lane in flight per round trip
 #pragma unroll 1
-        for (int v = lane + 32 * kPre; v < nvec; v += 32) {
-            const float4 w = ld_f4(wr + 4 * v);
+        for (int v0 = lane + 32 * kPre; v0 < nvec; v0 += 32 * kTail) {
+            float4 w[kTail];
 #pragma unroll
-            for (int t = 0; t < kTokGroup; ++t) {
-                if (t < nt) {
-                    float x0, x1, x2, x3;
-                    bf16x4_to_f(xs[t * nvec + v], x0, x1, x2, x3);
-                    acc[t] = fmaf(x3, w.w, fmaf(x2, w.z, fmaf(x1, w.y, fmaf(x0, w.x, acc[t]))));
+            for (int u = 0; u < kTail; ++u)
+                if (v0 + 32 * u < nvec) w[u] = ld_f4(wr + 4 * (v0 + 32 * u));
+#pragma unroll
+            for (int u = 0; u < kTail; ++u) {
+                const int v = v0 + 32 * u;
+                if (v < nvec) {
+#pragma unroll
+                    for (int t = 0; t < kTokGroup; ++t) {
+                        if (t < nt) {
+                            float x0, x1, x2, x3;
+                            bf16x4_to_f(xs[t * nvec + v], x0, x1, x2, x3);
+                            acc[t] = fmaf(x3, w[u].w, fmaf(x2, w[u].z, fmaf(x1, w[u].y, fmaf(x0, w[u].x, acc[t]))));
+                        }
+                    }
                 }
             }
         }

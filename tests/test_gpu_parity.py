@@ -70,6 +70,9 @@ SHAPES = [
     (384, 64, 6, 128, 1, 128, 37),
     (128, 8, 3, 64, 2, 64, 64),
     (128, 1, 1, 64, 0, 64, 4),        # a single expert
+    (192, 48, 5, 128, 2, 64, 2),      # two tokens: each warp gathers its own pieces' h
+    (256, 300, 6, 128, 1, 128, 2),    # more than 256 experts: the chain's router
+    (128, 256, 8, 64, 1, 128, 8),     # top-8 of 256 at T = 8, shared expert wider than the routed ones
 ]
 
 
@@ -137,6 +140,26 @@ def test_handle_reuse_varying_T_and_determinism(moe, orc, fused):
                     first = gout
                 else:
                     assert np.array_equal(first, gout), "run-to-run difference"
+    finally:
+        L.close()
+
+
+def test_many_calls_keep_tags_in_step(moe, orc):
+    """The single launch tags exchanged words with the call number: after a
+    long run of calls with changing T (stale words of larger steps stay
+    behind), every call still matches the oracle."""
+    layer, x, _ = guarded_case(0, 17, T=8, full=True)
+    L = moe.MoELayer(layer, max_tokens=8)
+    try:
+        xd = x_to_device(x)
+        for i in range(300):
+            T = (1, 8, 2, 5)[i % 4]
+            out, ids, w = L.forward(xd[:T])
+        torch.cuda.synchronize()
+        assert moe.moe_check(L.h) == moe.MOE_OK
+        for T in (8, 1):
+            gout, gids, gw = run_gpu(moe, layer, x[:T], layer_obj=L)
+            check_parity(orc, layer, x[:T], gout, gids, gw)
     finally:
         L.close()
 
