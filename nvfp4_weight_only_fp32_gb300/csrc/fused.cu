@@ -478,22 +478,35 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 if (lane == 0) s_tmax[warp][t] = m;
             }
         }
-        // warp sums of the 32 partial logits by a transposing butterfly: at
-        // the step of distance w every lane keeps the half of its values
-        // selected by bit w of its lane index and adds the partner's copy of
-        // that half; lane L ends with value L (token L / kREmax, expert L %
-        // kREmax)
+        if (T <= 2) {
+            // few values: a butterfly sum of each (the same pairing order)
 #pragma unroll
-        for (int w = 16; w >= 1; w >>= 1) {
+            for (int i = 0; i < 2 * kREmax; ++i) {
+                if (i < T * kREmax) {
+                    float v = acc[i];
 #pragma unroll
-            for (int i = 0; i < w; ++i) {
-                const bool up = (lane & w) != 0;
-                const float send = up ? acc[i] : acc[i + w];
-                const float keep = up ? acc[i + w] : acc[i];
-                acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                    for (int w = 16; w >= 1; w >>= 1) v += __shfl_xor_sync(0xffffffffu, v, w);
+                    if (lane == 0) s_lpart[warp][i] = v;
+                }
             }
+        } else {
+            // warp sums of the 32 partial logits by a transposing butterfly:
+            // at the step of distance w every lane keeps the half of its
+            // values selected by bit w of its lane index and adds the
+            // partner's copy of that half; lane L ends with value L (token L /
+            // kREmax, expert L % kREmax)
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+                for (int i = 0; i < w; ++i) {
+                    const bool up = (lane & w) != 0;
+                    const float send = up ? acc[i] : acc[i + w];
+                    const float keep = up ? acc[i + w] : acc[i];
+                    acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                }
+            }
+            s_lpart[warp][lane] = acc[0];
         }
-        s_lpart[warp][lane] = acc[0];
     }
     MOE_TRACE_CLOCK(2, 13);
     __syncthreads();
@@ -551,6 +564,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     unsigned par_c = 0u;                 // and the slot's phase parity
     int n_done = 0;                      // segments whose copies have landed (waited for)
     int nslots = S, lksd = 0, perw = 0, nrt = 0, n_list = 0;
+    const int nrt0 = c < NRT ? (NRT - c + G - 1) / G : 0;   // this block's output tiles
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         Pass pp = p0;
@@ -579,12 +593,21 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             // slots follow directly: routed slot S + (rank of the id among
             // the k choices), one pair each
             const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
-            float sum = 0.f;
+            float sv[kMaxTopK];
+            int ev[kMaxTopK];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                sv[j] = __shfl_sync(0xffffffffu, sel_s, j);
+                ev[j] = __shfl_sync(0xffffffffu, sel_e, j);
+            }
+            float sum = 0.f;                 // in selection order
             int rank = 0;
-#pragma unroll 1
-            for (int j = 0; j < K; ++j) {
-                sum += __shfl_sync(0xffffffffu, sel_s, j);
-                rank += __shfl_sync(0xffffffffu, sel_e, j) < sel_e;
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                if (j < K) {
+                    sum += sv[j];
+                    rank += ev[j] < sel_e;
+                }
             }
             if (lane < K) {
                 const float w = (d.normalize ? sel_s / sum : sel_s) * d.routed_scale;
@@ -666,9 +689,9 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             MOE_TRACE_CLOCK(4, 5);
             lksd = fg.lksd[nslots];
             perw = warp < (nslots << lksd) ? ((nslots << lksd) - warp + kFW - 1) / kFW : 0;
-            nrt = c < NRT ? (NRT - c + G - 1) / G : 0;
+            nrt = nrt0;
             for (int i = lane; i < nrt * perw; i += 32) {
-                const int ri = i / perw, r2 = i - ri * perw;
+                const int ri = nrt == 1 ? 0 : i / perw, r2 = i - ri * perw;
                 const int rt = c + ri * G, pi = warp + kFW * r2;
                 const int e = s_slot_e[pi >> lksd], kp = pi & ((1 << lksd) - 1);
                 const int ncd = (e < 0 ? d.Is : d.I) / kChunkK, cpk = ncd >> lksd;
