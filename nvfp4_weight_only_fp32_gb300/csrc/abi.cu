@@ -154,6 +154,8 @@ void carve_workspace(moe_layer *L, char *base) {
     Carver cv{base};
     const int Tm = c.max_tokens, E = c.num_experts, K = c.top_k, S = c.num_shared, H = c.hidden;
     d.logits = cv.take<float>((size_t)Tm * E);
+    d.lpart = cv.take<float>((size_t)kMaxKSplit * Tm * E);
+    d.xmaxb = cv.take<unsigned>(Tm);
     d.ids = cv.take<int>((size_t)Tm * K);
     d.wsel = cv.take<float>((size_t)Tm * K);
     d.xexp = cv.take<int>(Tm);
@@ -358,7 +360,7 @@ moe_status moe_stage_route(moe_layer *L, const void *x, int T, int *topk_ids, fl
     if (rc != MOE_OK) return rc;
     if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
-    cudaError_t e = launch_route(L->d, static_cast<const __nv_bfloat16 *>(x), T, topk_ids, topk_w,
+    cudaError_t e = launch_route(L->d, static_cast<const __nv_bfloat16 *>(x), T, topk_ids, topk_w, L->sm_count,
                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router launch");
 }

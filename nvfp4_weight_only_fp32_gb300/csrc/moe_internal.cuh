@@ -51,6 +51,7 @@ constexpr int kMaxShared = 2;
 constexpr int kFusedSlots = 8 * kMaxTopK + kMaxShared;   // slots of a single-launch call (T <= 8)
 constexpr int kFusedPairs = 8 * (kMaxTopK + kMaxShared); // (token, expert) pairs of such a call
 constexpr int kRouteWarps = 8;     // experts per router CTA
+constexpr int kMaxKSplit = 8;      // router: K splits of the rows (blocks along z)
 
 // Everything a kernel needs to know about a layer (passed by value).
 struct DevLayer {
@@ -73,6 +74,8 @@ struct DevLayer {
     size_t s13_stride, s2_stride;   // bytes per shared expert
     // workspace (device)
     float *logits;                  // [Tm, E]
+    float *lpart;                   // [kMaxKSplit, Tm, E] router partial sums by K range
+    unsigned *xmaxb;                // [Tm] router: max |x| bits per token (zero between calls)
     int *ids;                       // [Tm, k]
     float *wsel;                    // [Tm, k]
     int *xexp;                      // [Tm]  power-of-two prescale of x rows
@@ -109,7 +112,7 @@ struct DevLayer {
 // Host-side launchers (defined in the .cu files).
 // ---------------------------------------------------------------------------
 cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out,
-                         float *w_out, cudaStream_t s);
+                         float *w_out, int sm_count, cudaStream_t s);
 cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s);
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s);
 bool grouped_supported(const DevLayer &d, int sm_count);

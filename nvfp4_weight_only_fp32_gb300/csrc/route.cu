@@ -11,13 +11,16 @@
 // strategy" (the expert GEMVs read only the selected experts, which is what the
 // work list built here enables).
 //
-// Grid: (E/8 expert groups) x (token groups of up to 8 tokens).  Each warp
-// owns one expert: its router row is fetched into registers BEFORE the
-// programmatic-launch wait (router weights do not depend on the previous
-// kernel); the block stages its token group's activations in shared memory
-// and the warp computes the FP32 logits of those tokens (one accumulator per
-// token, so the FMA chains run side by side).  Two tickets follow, with no
-// spinning:
+// Grid: (E/8 expert groups) x (token groups of up to 8 tokens) x (K ranges:
+// the router rows are split along H until the grid covers the SMs).  Each
+// warp owns one expert and one K range: that part of its router row is
+// fetched into registers BEFORE the programmatic-launch wait (router weights
+// do not depend on the previous kernel); the block stages its token group's
+// activation columns in shared memory and the warp computes the FP32 partial
+// logits of those tokens (one accumulator per token, so the FMA chains run
+// side by side).  With several K ranges the partial sums go to the workspace
+// and the ticket's last block adds them in a fixed order.  Two tickets
+// follow, with no spinning:
 //   * the last expert group of a token group to finish runs sigmoid + top-k
 //     for those tokens (one warp per token) and ORs each token into a 64-bit
 //     mask per selected expert;
@@ -63,9 +66,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = d.H, E = d.E, K = d.k, S = d.S;
     const int e = blockIdx.x * kRouteWarps + warp;
-    const int nvec = H / 4;
+    // K split: block z takes columns [k0, k0 + Hk) of the router rows
+    const int KH = gridDim.z, Hk = H / KH, k0 = blockIdx.z * Hk;
+    const int nvec = Hk / 4;
     const int t0 = blockIdx.y * tg, nt = min(tg, T - t0);
-    const float *wr = d.router_w + (size_t)(e < E ? e : 0) * H;
+    const float *wr = d.router_w + (size_t)(e < E ? e : 0) * H + k0;
 
     MOE_TRACE_POINT(0, 0);
     float4 pre[kPre];
@@ -80,26 +85,29 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             pre[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    const float bias = (e < E && d.router_b) ? d.router_b[e] : 0.f;
+    const float bias = (e < E && d.router_b && KH == 1) ? d.router_b[e] : 0.f;
     pdl_wait();
     pdl_trigger();
     MOE_TRACE_POINT(0, 1);
 
-    // ---- stage the token group's activation rows (16-byte loads, all in flight) ----
+    // ---- stage the token group's activation columns [k0, k0 + Hk) (16-byte
+    // loads, all in flight) ----
     __shared__ float s_rmax[kTokGroup];
     if (threadIdx.x < kTokGroup) s_rmax[threadIdx.x] = 0.f;
-    const uint2 *xs = reinterpret_cast<const uint2 *>(smem);     // [nt][H/4] groups of 4 bf16
+    const uint2 *xs = reinterpret_cast<const uint2 *>(smem);     // [nt][Hk/4] groups of 4 bf16
     {
-        const int n16 = nt * H / 8;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t0 * H);
+        const int r16 = Hk / 8, n16 = nt * r16;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t0 * H + k0);
         uint4 *dst = reinterpret_cast<uint4 *>(smem);
         __syncthreads();
 #pragma unroll 1
         for (int base = threadIdx.x; base < n16; base += 8 * kThreads) {
             uint4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (base + u * kThreads < n16) v[u] = __ldcg(src + base + u * kThreads);
+            for (int u = 0; u < 8; ++u) {
+                const int i = base + u * kThreads;
+                if (i < n16) v[u] = __ldcg(src + (size_t)(i / r16) * (H / 8) + i % r16);
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int i = base + u * kThreads;
@@ -113,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
                         for (int q = 0; q < 4; ++q)
                             m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
                                                fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
-                        atomicMax(reinterpret_cast<int *>(&s_rmax[i / (H / 8)]), __float_as_int(m));
+                        atomicMax(reinterpret_cast<int *>(&s_rmax[i / r16]), __float_as_int(m));
                     }
                 }
             }
@@ -122,8 +130,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     }
     MOE_TRACE_POINT(0, 2);
     if (blockIdx.x == 0 && threadIdx.x < nt) {
-        const float mx = s_rmax[threadIdx.x];
-        d.xexp[t0 + threadIdx.x] = max(-100, exp_for_f16(mx));
+        // this K range's max; the exponent is taken from the whole row below
+        atomicMax(d.xmaxb + t0 + threadIdx.x, __float_as_uint(s_rmax[threadIdx.x]));
     }
     // ---- logits of the group's tokens for this warp's expert ----
     if (e < E) {
@@ -171,7 +179,10 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             float a = acc[t];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            if (lane == 0 && t < nt) d.logits[(size_t)(t0 + t) * E + e] = a + bias;
+            if (lane == 0 && t < nt) {
+                if (KH == 1) d.logits[(size_t)(t0 + t) * E + e] = a + bias;
+                else d.lpart[((size_t)blockIdx.z * d.max_tokens + t0 + t) * E + e] = a;
+            }
         }
     }
 
@@ -181,11 +192,21 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     MOE_TRACE_POINT(0, 3);
     if (threadIdx.x == 0) {
         __threadfence();
-        s_last = atomicAdd(d.tg_ticket + blockIdx.y, 1u) == gridDim.x - 1;
+        s_last = atomicAdd(d.tg_ticket + blockIdx.y, 1u) == gridDim.x * gridDim.z - 1;
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    if (KH > 1) {
+        // the token group's logits: the K ranges' sums in a fixed order
+        for (int i = threadIdx.x; i < nt * E; i += kThreads) {
+            const int t = i / E, ee = i - t * E;
+            float v = 0.f;
+            for (int z = 0; z < KH; ++z) v += __ldcg(d.lpart + ((size_t)z * d.max_tokens + t0 + t) * E + ee);
+            d.logits[(size_t)(t0 + t) * E + ee] = v + (d.router_b ? d.router_b[ee] : 0.f);
+        }
+        __syncthreads();
+    }
     MOE_TRACE_POINT(0, 4);
     if (warp < nt) {
         // sort keys (bits(sigmoid) + 1) << 32 | ~id (a NaN logit: 0 << 32 |
@@ -240,6 +261,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     for (int i = threadIdx.x; i < T * K; i += kThreads) {
         s_ids[i / K][i % K] = __ldcg(d.ids + i);
         s_w[i / K][i % K] = __ldcg(d.wsel + i);
+    }
+    // the tokens' power-of-two prescales from their whole-row maxima
+    for (int t = threadIdx.x; t < T; t += kThreads) {
+        d.xexp[t] = max(-100, exp_for_f16(__uint_as_float(__ldcg(d.xmaxb + t))));
+        d.xmaxb[t] = 0u;
     }
     __syncthreads();
     MOE_TRACE_POINT(0, 6);
@@ -342,21 +368,32 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 
 }  // namespace
 
-size_t route_smem_bytes(const DevLayer &d, int T, int *tg_out) {
-    // activation rows of one token group (at most 8, at most 96 KB)
+// K splits of the router rows: enough blocks for the SMs, K ranges of a
+// multiple of 64 columns, at most kMaxKSplit.
+int route_ksplit(const DevLayer &d, int T, int sm_count) {
+    const int gx = (d.E + kRouteWarps - 1) / kRouteWarps, gy = (T + kTokGroup - 1) / kTokGroup;
+    int kh = 1;
+    while (2 * kh <= kMaxKSplit && gx * gy * kh < sm_count && d.H % (64 * 2 * kh) == 0) kh *= 2;
+    return kh;
+}
+
+size_t route_smem_bytes(const DevLayer &d, int T, int kh, int *tg_out) {
+    // activation columns of one token group (at most 8 tokens, at most 96 KB)
+    const int Hk = d.H / kh;
     int tg = kTokGroup;
-    while (tg > 1 && (size_t)tg * d.H * 2 > 96 * 1024) --tg;
+    while (tg > 1 && (size_t)tg * Hk * 2 > 96 * 1024) --tg;
     if (tg > T) tg = T;
     if (tg_out) *tg_out = tg;
-    return (size_t)tg * d.H * 2;
+    return (size_t)tg * Hk * 2;
 }
 
 cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out, float *w_out,
-                         cudaStream_t s) {
+                         int sm_count, cudaStream_t s) {
     int tg = 1;
-    const size_t smem = route_smem_bytes(d, T, &tg);
+    const int kh = route_ksplit(d, T, sm_count);
+    const size_t smem = route_smem_bytes(d, T, kh, &tg);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((d.E + kRouteWarps - 1) / kRouteWarps, (T + tg - 1) / tg);
+    cfg.gridDim = dim3((d.E + kRouteWarps - 1) / kRouteWarps, (T + tg - 1) / tg, kh);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
