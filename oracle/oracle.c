@@ -39,10 +39,11 @@
  *    the forward pass uses this exact value.  orc_dequant() returns it rounded
  *    once to FP32 (round to nearest even).
  *  - Router: logits in FP64 (the exact value of the FP32 router), score =
- *    sigmoid(logit).  The top-k DECISION is taken on the FP32-rounded score
- *    (the router's precision), descending, lowest expert index first on ties.
- *    The weights use the FP64 scores, normalised to sum to 1 when asked, then
- *    multiplied by the routed scale.
+ *    sigmoid(logit).  Sigmoid is strictly increasing, so the top-k by score is
+ *    the top-k by logit; the DECISION is taken on the FP32-rounded logit (the
+ *    router's precision), descending, lowest expert index first on ties
+ *    (equal FP32 logits).  The weights use the FP64 scores, normalised to sum
+ *    to 1 when asked, then multiplied by the routed scale.
  *  - Router bias, when present, is added to the logit (plain linear layer).
  *  - Shared experts: ungated, weight 1, same NVFP4 format.
  *  - SwiGLU: h = silu(gate) * up, silu(z) = z / (1 + exp(-z)); h is rounded to
@@ -207,19 +208,19 @@ static void token_scores(const orc_layer *L, const uint16_t *xt, double *z, doub
     }
 }
 
-/* Top-k by score: descending FP32-rounded score, lowest index first on ties.
- * ids[j] in selection order; w[j] from the FP64 scores. */
-static void token_topk(const orc_layer *L, const double *s, int *ids, double *w)
+/* Top-k: descending FP32-rounded logit (the order of the scores), lowest
+ * index first on ties.  ids[j] in selection order; w[j] from the FP64 scores. */
+static void token_topk(const orc_layer *L, const double *z, const double *s, int *ids, double *w)
 {
     int E = L->E, K = L->k;
     char *taken = (char *)calloc((size_t)E, 1);
     for (int j = 0; j < K; ++j) {
         int best = -1;
-        float bs = 0.0f;
+        float bz = 0.0f;
         for (int e = 0; e < E; ++e) {
             if (taken[e]) continue;
-            float se = (float)s[e];
-            if (best < 0 || se > bs) { best = e; bs = se; }   /* strict: ties keep lower e */
+            float ze = (float)z[e];
+            if (best < 0 || ze > bz) { best = e; bz = ze; }   /* strict: ties keep lower e */
         }
         taken[best] = 1;
         ids[j] = best;
@@ -243,7 +244,7 @@ int orc_route(const orc_layer *L, const uint16_t *x, int T, int *ids, double *w,
     if (!z || !s) { free(z); free(s); return -1; }
     for (int t = 0; t < T; ++t) {
         token_scores(L, x + (size_t)t * L->H, z, s);
-        token_topk(L, s, ids + (size_t)t * L->k, w + (size_t)t * L->k);
+        token_topk(L, z, s, ids + (size_t)t * L->k, w + (size_t)t * L->k);
         if (scores) memcpy(scores + (size_t)t * L->E, s, sizeof(double) * L->E);
         if (logits) memcpy(logits + (size_t)t * L->E, z, sizeof(double) * L->E);
     }

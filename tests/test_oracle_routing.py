@@ -2,7 +2,8 @@
 
 Sigmoid top-k with weights normalised to sum to 1 (Flint page, "Flint model
 architecture", MoE bullet), FP32 router decision (Inkling 2 Small page,
-"Accuracy evaluation").  Pinned by brute force over all k-subsets, by closed
+"Accuracy evaluation"): sigmoid is strictly increasing, so the ranking is that
+of the FP32 logits.  Pinned by brute force over all k-subsets, by closed
 forms for the scores and weights, by the tie rule and by a permutation
 invariant.
 """
@@ -74,8 +75,9 @@ def test_ties_lowest_index_first(orc):
 
 
 def test_fp32_decision_precision(orc):
-    # Two logits whose FP64 sigmoids differ but round to the same FP32 score:
-    # the decision is taken on FP32 scores, so the lower index wins.
+    # The decision is taken on FP32 logits.  (1) Logits 20.0 and 19.5 whose
+    # sigmoids round to the same FP32 score (1.0) are distinct FP32 logits:
+    # the larger logit wins, as it does for the exact scores.
     E, H, k = 3, 16, 1
     z_hi, z_lo = 20.0, 19.5          # sigmoid -> 1 - 2e-9 vs 1 - 3.4e-9: both fl32 = 1.0
     w = np.zeros((E, H), np.float32)
@@ -85,6 +87,22 @@ def test_fp32_decision_precision(orc):
     ids, wt, s, _ = orc.route(_router_layer(E, H, k, w), x)
     assert s[0][1] > s[0][0]
     assert np.float32(s[0][1]) == np.float32(s[0][0])
+    assert ids[0].tolist() == [1]
+    # (2) FP64 logits 1 + 2^-30 (expert 1) and 1 (expert 0) round to the same
+    # FP32 logit: a tie, so the lower index wins although expert 1's exact
+    # score is larger.
+    E, k = 2, 1
+    w = np.zeros((E, H), np.float32)
+    w[0, 0] = 1.0
+    w[1, 0] = 1.0
+    w[1, 1] = 1.0
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x3F80                 # 1.0
+    x[0, 1] = 0x3080                 # 2^-30
+    ids, wt, s, z = orc.route(_router_layer(E, H, k, w), x)
+    assert z[0][1] == 1.0 + 2.0 ** -30 and z[0][0] == 1.0
+    assert s[0][1] > s[0][0]
+    assert np.float32(z[0][1]) == np.float32(z[0][0])
     assert ids[0].tolist() == [0]
 
 
