@@ -21,22 +21,24 @@
 // the layer's selected weights fits in its rings and is requested right
 // after routing).
 //
-// Phases:
-//   A  before griddepcontrol.wait: copy this block's router rows into shared
-//      memory; start the rings on the shared-expert gate/up units (static
-//      weights); L2-prefetch this block's rows of the shared down weights.
-//   B  x (T rows) arrives by one bulk copy; it is staged as the f16 MMA
-//      operand with an exact per-row power-of-two prescale, and this block's
-//      experts' FP32 logits are published; ARRIVE at grid barrier 1.
-//   C  pass 0: shared-expert gate/up units (no routing needed) while the grid
-//      arrives; WAIT on barrier 1; every block runs the same deterministic
-//      top-k (two stages: per group of experts, then per token) and slot/pair
-//      numbering; pass 1: routed gate/up units.  SwiGLU in the epilogue; h
-//      goes to the workspace with a per-pair max |h|.  Grid barrier 2.
-//   D  each block owns 16-row output tiles for ALL slots: stage every pair's h
-//      as f16 (exact power-of-two prescale), down GEMV per (slot, K part) and
-//      warp, scale by the routing weight, reduce the warps in a fixed order
-//      and write BF16 out.  No further exchange.
+// Phases (no grid barrier: values that cross blocks travel as words tagged
+// with the call number and are polled by their readers):
+//   A  before griddepcontrol.wait: copy this block's router rows and the
+//      packed global scales into shared memory; start the rings of the
+//      shared-expert pass; L2-prefetch this block's rows of the shared down
+//      weights.
+//   B  x (T rows) arrives by one bulk copy; one pass over it gives the
+//      per-token max |x| and this block's experts' FP32 logits, published as
+//      tagged words; the shared-expert warps stage x as the f16 MMA operand
+//      (exact per-row power-of-two prescale).
+//   C  pass 0: the shared-expert gate/up units, while one warp per token
+//      polls all logits and takes the top-k (the same in every block);
+//      pass 1: the routed gate/up units.  SwiGLU in the epilogue; h is
+//      published as tagged words.
+//   D  h is gathered from the tagged words as f16 (an exact power-of-two
+//      prescale per piece); each block owns 16-row output tiles for all
+//      slots: down GEMV per (slot, K part) and warp, routing weight, a
+//      fixed-order warp reduction, BF16 out.
 // The token index is the MMA's N coordinate throughout (T <= 8 = N), so the
 // B fragments of x are shared by every expert and per-token results land in
 // the lane that owns the token.
@@ -65,7 +67,8 @@ namespace {
 constexpr int kFW = 16;                                  // warps per block
 constexpr int kFT = 32 * kFW;
 constexpr int kTF = 8;                                   // tokens (MMA N)
-constexpr int kPW = 8;                                   // warps of the shared-expert pass; the others route
+constexpr int kPW = 8;                                   // warps of the shared-expert pass (see pass0_index)
+constexpr int kStageBar = 15;                            // named barrier of the x staging (the kPW pass-0 warps)
 constexpr int kREmax = 4;                                // router experts per block
 static_assert(kTF * kREmax == 32, "the logit reduction gives each lane one (token, expert) value");
 constexpr int kCHmax = 8;                                // chunks per ring segment
@@ -173,6 +176,19 @@ __device__ __forceinline__ unsigned long long gtimer() {
     return t;
 }
 
+// Warp roles while the block routes.  Warp w runs on SM sub-partition w % 4.
+// The routing warps (one per token) sit on sub-partitions 0 and 1 -- token t
+// on warp 4t for t < 4, on warp 4(t - 4) + 1 above -- and the shared-expert
+// pass on sub-partitions 2 and 3, so that the issue-bound decode of that pass
+// does not share a scheduler with the latency-bound routing.
+__device__ __forceinline__ int routed_token_of(int w) {
+    return (w & 3) == 0 ? (w >> 2) : (w & 3) == 1 ? 4 + (w >> 2) : -1;
+}
+// Index of warp w among the kPW warps of the shared-expert pass (kFW if none).
+__device__ __forceinline__ int pass0_index(int w) {
+    return (w & 3) >= 2 ? 2 * (w >> 2) + (w & 3) - 2 : kFW;
+}
+
 // Wait for phase `parity` of an mbarrier; gives up after kWaitNs, setting the
 // sticky error word.
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity, int *err) {
@@ -250,8 +266,8 @@ __device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, cons
 // lane L holds experts i * 32 + L, i < M; lane j < K ends with the j-th
 // choice's sort key.
 template <int M>
-__device__ __forceinline__ bool route_token(const unsigned long long *lt, int t, int E, int K, unsigned tag,
-                                            int lane, int *err, unsigned long long &sel, int &passes) {
+__device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned long long *lt, int t, int E, int K,
+                                            unsigned tag, int lane, int *err, unsigned long long &sel, int &passes) {
     unsigned long long v[M];
     bool ok = true;
     unsigned pend = 0u;
@@ -274,11 +290,13 @@ __device__ __forceinline__ bool route_token(const unsigned long long *lt, int t,
             pend = 0u;
         }
     }
+    MOE_TRACE_CLOCK_AT(4, 0, 0);
 #pragma unroll
     for (int i = 0; i < M; ++i) {
         const int e = i * 32 + lane;
-        v[i] = e < E ? ((unsigned long long)sigmoid_key(__uint_as_float((unsigned)v[i])) << 32) | (unsigned)~e : 0ull;
+        v[i] = e < E ? ((unsigned long long)logit_key(__uint_as_float((unsigned)v[i])) << 32) | (unsigned)~e : 0ull;
     }
+    MOE_TRACE_CLOCK_AT(4, 1, 0);
     sel = warp_topk<M>(v, K, lane);
     return ok;
 }
@@ -329,12 +347,18 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 
     // ---- the copy issuer (lane 0's registers; the other lanes' copies idle) ----
     int n_iss = 0, it = 0, n_known = 0, left = 0, sl_p = 0;
+#ifdef MOE_TRACE
+    bool trc = false;
+#else
+    constexpr bool trc = false;
+#endif
     const uint8_t *src = nullptr;
     auto pump = [&](int limit) {
         if (lane != 0) return;
         // one proxy fence orders the warp's reads of the slots about to be
         // refilled before all of this call's copies
         if (n_iss < limit && (left > 0 || it < n_known)) fence_proxy_async();
+        if (trc) MOE_TRACE_CLOCK(4, 7);
         while (n_iss < limit) {
             if (left == 0) {
                 if (it >= n_known) break;
@@ -352,20 +376,21 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         }
     };
     // gate/up plan of one pass: groups of 2^lks warps share a unit (slot lo +
-    // uu / NT, tile uu % NT) by splitting its K range; this warp's units are
-    // uu = u0 + i * stride, i < my, and its K range [cb0, cb0 + cpw)
+    // uu / NT, tile uu % NT) by splitting its K range; the warp with index vw
+    // among the pass's nw warps takes units uu = u0 + i * stride, i < my, and
+    // the K range [cb0, cb0 + cpw)
     struct Pass {
         int lks, cpw, cb0, stride, u0, my, NT, lo;
     };
-    auto plan = [&](int units, int lks, int NT, int lo, int nw) {
+    auto plan = [&](int units, int lks, int NT, int lo, int nw, int vw) {
         Pass p;
         const int ngrp = nw >> lks;
         p.lks = lks;
         p.cpw = NC13 >> lks;
-        p.cb0 = (warp & ((1 << lks) - 1)) * p.cpw;
+        p.cb0 = (vw & ((1 << lks) - 1)) * p.cpw;
         p.stride = G * ngrp;
-        p.u0 = c * ngrp + (warp >> lks);
-        p.my = warp < nw && p.u0 < units ? (units - p.u0 + p.stride - 1) / p.stride : 0;
+        p.u0 = c * ngrp + (vw >> lks);
+        p.my = vw < nw && p.u0 < units ? (units - p.u0 + p.stride - 1) / p.stride : 0;
         p.NT = NT;
         p.lo = lo;
         return p;
@@ -401,7 +426,8 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         for (int i = 0; i < RW; ++i) mbar_init(bar + i, 1);
         fence_proxy_async();
     }
-    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW);
+    const int v0 = pass0_index(warp), tok = routed_token_of(warp);
+    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW, v0);
     __syncthreads();
     fill_units(p0, 0);
     __syncwarp();
@@ -469,6 +495,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
             }
         }
+        MOE_TRACE_CLOCK(4, 9);
         // warp maxima per token (mx >= 0 and not NaN -- fmaxf drops NaN --
         // so its bits order as unsigned)
 #pragma unroll
@@ -478,6 +505,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 if (lane == 0) s_tmax[warp][t] = m;
             }
         }
+        MOE_TRACE_CLOCK(4, 10);
         if (T <= 2) {
             // few values: a butterfly sum of each (the same pairing order)
 #pragma unroll
@@ -527,6 +555,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             st_tagged(d.logit_tag + (size_t)t * E + e, s_tag, __float_as_uint(v + s_gsp[e].w));
         }
     }
+    MOE_TRACE_CLOCK(4, 12);
     // zero row T (the B column of absent tokens)
     for (int i = threadIdx.x; i < fg.xrow / 16; i += kFT)
         reinterpret_cast<uint4 *>(xs + (size_t)T * fg.xrow)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -535,11 +564,13 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     // x' = x * 2^-xexp as f16, permuted within each 64-element chunk (element
     // 16kb + 8h + 2q + e sits at half 16q + 4kb + 2h + e: quad m of a chunk,
     // elements 4m..4m+3, has kb = m/4, h = (m/2)%2 and q = 2(m%2) for its
-    // first pair, q + 1 for its second)
-#pragma unroll
-    for (int xp = 0; xp < QP; ++xp) {
-        const int P = threadIdx.x + xp * kFT;
-        if (P < nq) {
+    // first pair, q + 1 for its second).  Staged by the warps of the
+    // shared-expert pass alone; the routing warps start polling at once (the
+    // block barrier at the start of pass 1 orders the staging before their
+    // own use of x).
+    if (v0 < kPW) {
+#pragma unroll 1
+        for (int P = 32 * v0 + lane; P < nq; P += 32 * kPW) {
             const int m = P & 15, kb = m >> 2, hh = (m >> 1) & 1, q0 = 2 * (m & 1);
 #pragma unroll
             for (int t = 0; t < kTF; ++t) {
@@ -554,9 +585,9 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
             }
         }
+        asm volatile("bar.sync %0, %1;\n" ::"n"(kStageBar), "n"(32 * kPW) : "memory");
+        MOE_TRACE_CLOCK_AT(3, 3, 64);
     }
-    __syncthreads();
-    FUSED_TRACE(3);
 
     // ---------------- C: gate/up, pass 0 shared experts, pass 1 routed ----------------
     const uint8_t *xb = xs + (size_t)(g < T ? g : T) * fg.xrow + q * 32;
@@ -568,31 +599,31 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         Pass pp = p0;
-        if (pass == 0 && warp >= kPW && warp < kPW + T) {
+        if (pass == 0 && tok >= 0 && tok < T) {
             // routing, identical in every block, straight from the tagged
-            // logits (no grid barrier), while warps 0..kPW-1 run the shared
-            // experts: warp kPW + t takes token t, lane L the experts i * 32
-            // + L.  An expert's sort key is (bits(sigmoid) + 1) << 32 | ~id
-            // (a NaN logit: 0 << 32 | ~id): larger is better, ties in the
-            // score go to the lower id, all keys differ.
-            const int t = warp - kPW;
+            // logits (no grid barrier), while the pass-0 warps run the shared
+            // experts: one warp per token t (routed_token_of), lane L the
+            // experts i * 32 + L.  An expert's sort key is logit_key(logit) << 32 | ~id:
+            // larger is better, equal logits go to the lower id, all keys
+            // differ.
+            const int t = tok;
             const unsigned ltag = s_tag + (unsigned)d.debug_stall;
             int lpass = 0;
             unsigned long long sel = 0ull;
             switch (fg.m1p) {
-                case 1: ok = route_token<1>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                case 2: ok = route_token<2>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                case 4: ok = route_token<4>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                default: ok = route_token<8>(d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                case 1: ok = route_token<1>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                case 2: ok = route_token<2>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                case 4: ok = route_token<4>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                default: ok = route_token<8>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
             }
             const unsigned sel_key = (unsigned)(sel >> 32);
             const int sel_e = (int)~(unsigned)sel;
-            MOE_TRACE_CLOCK_AT(3, 10, 32 * kPW);
-            MOE_TRACE_VALUE_AT(1, 2, 32 * kPW, lpass);
+            MOE_TRACE_CLOCK_AT(3, 10, 0);
+            MOE_TRACE_VALUE_AT(1, 2, 0, lpass);
             // weights (normalised in selection order); for one token the
             // slots follow directly: routed slot S + (rank of the id among
             // the k choices), one pair each
-            const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
+            const float sel_s = key_score(sel_key);
             float sv[kMaxTopK];
             int ev[kMaxTopK];
 #pragma unroll
@@ -627,7 +658,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
             }
             if (T == 1 && lane == 0) s_nslots = S + K;
-            MOE_TRACE_CLOCK_AT(3, 5, 32 * kPW);
+            MOE_TRACE_CLOCK_AT(3, 5, 0);
         }
         if (pass == 1) {
             FUSED_TRACE(4);
@@ -680,12 +711,20 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             FUSED_TRACE(12);
             // this warp's routed units and down pieces -> its copy list
             nslots = s_nslots;
-            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW);
+            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW, warp);
+            MOE_TRACE_CLOCK(4, 3);
             fill_units(pp, p0.my);
             __syncwarp();
+            MOE_TRACE_CLOCK(4, 4);
             // the routed units' copies start before the down pieces are listed
             n_known = p0.my + pp.my;
+#ifdef MOE_TRACE
+            trc = true;
+#endif
             if (ok) pump(n_con + RW);
+#ifdef MOE_TRACE
+            trc = false;
+#endif
             MOE_TRACE_CLOCK(4, 5);
             lksd = fg.lksd[nslots];
             perw = warp < (nslots << lksd) ? ((nslots << lksd) - warp + kFW - 1) / kFW : 0;
@@ -708,7 +747,8 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             __syncwarp();
             FUSED_TRACE(6);
         }
-        const int ks = 1 << pp.lks, gi = warp >> pp.lks, kw = warp & (ks - 1);
+        const int vw = pass == 0 ? v0 : warp;         // index among the pass's warps
+        const int ks = 1 << pp.lks, gi = vw >> pp.lks, kw = vw & (ks - 1);
         // every warp of a group has the same unit count, so the group's named
         // barrier (id 1 + gi) is reached by all of its warps together
 #pragma unroll 1
@@ -723,7 +763,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
                     else ok = false;
                 }
-                if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK(2, 4 * pass);
+                if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK_AT(2, 4 * pass, pass == 0 ? 64 : 0);
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
 #pragma unroll 1
@@ -739,24 +779,24 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 }
                 if (ok) pump(n_con + RW);
             }
-            if (ui == 0) MOE_TRACE_CLOCK(2, 4 * pass + 1);
+            if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * pass + 1, pass == 0 ? 64 : 0);
 #pragma unroll
             for (int v = 0; v < 4; ++v) a0[v] += a1[v];
             const int uu = pp.u0 + ui * pp.stride;
             const int s = uu / pp.NT, r = uu - s * pp.NT, slot = pp.lo + s;
             if (ks > 1) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) s_red[warp][v][lane] = a0[v];
+                for (int v = 0; v < 4; ++v) s_red[vw][v][lane] = a0[v];
                 asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
                 if (kw == 0) {
 #pragma unroll 1
                     for (int w = 1; w < ks; ++w)
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) a0[v] += s_red[warp + w][v][lane];
+                        for (int v = 0; v < 4; ++v) a0[v] += s_red[vw + w][v][lane];
                 }
                 asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
             }
-            if (ui == 0) MOE_TRACE_CLOCK(2, 4 * pass + 2);
+            if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * pass + 2, pass == 0 ? 64 : 0);
             if (kw == 0 && __all_sync(0xffffffffu, ok)) {
                 // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row
                 // 8r+g; lanes g and g+1 publish one tagged word of two BF16
@@ -779,7 +819,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                         st_tagged(d.h_tag + ((size_t)p * d.Imax + 8 * r + g) / 2, s_tag, hbits | (hnext << 16));
                 }
             }
-            MOE_TRACE_CLOCK(2, 4 * pass + 3);
+            MOE_TRACE_CLOCK_AT(2, 4 * pass + 3, pass == 0 ? 64 : 0);
         }
     }
     FUSED_TRACE(7);

@@ -339,10 +339,21 @@ __device__ __forceinline__ void fence_proxy_async() {
 // score.
 __device__ __forceinline__ float sigmoid_score(float z) { return __fdividef(1.0f, 1.0f + expf(-z)); }
 
-// Order-preserving key of an expert's sigmoid score: bits(score) + 1, or 0
-// for a NaN logit (scores are in [0, 1], so their bits order as unsigned).
-__device__ __forceinline__ unsigned sigmoid_key(float z) {
-    return isnan(z) ? 0u : __float_as_uint(sigmoid_score(z)) + 1u;
+// The ranking key of an expert: its FP32 logit mapped to an unsigned integer
+// of the same order (sigmoid is strictly increasing, so this is the order of
+// the scores).  -0 and +0 share one key; a NaN logit gets 0, below every
+// number (the smallest key of a number, that of -inf, is 0x007FFFFF).
+__device__ __forceinline__ unsigned logit_key(float z) {
+    unsigned u = __float_as_uint(z);
+    if (u == 0x80000000u) u = 0u;
+    return isnan(z) ? 0u : (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The weight of a chosen expert: the sigmoid of the logit its key encodes
+// (NaN for key 0).
+__device__ __forceinline__ float key_score(unsigned key) {
+    const float z = __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+    return key ? sigmoid_score(z) : __int_as_float(0x7fc00000);
 }
 
 // Sort M (a power of two) 64-bit keys held by one lane, largest first

@@ -54,7 +54,7 @@ __device__ __forceinline__ unsigned long long token_topk(const float *z, int E, 
 #pragma unroll
     for (int i = 0; i < M; ++i) {
         const int e = i * 32 + lane;
-        c[i] = e < E ? ((unsigned long long)sigmoid_key(__ldcg(z + e)) << 32) | (unsigned)~e : 0ull;
+        c[i] = e < E ? ((unsigned long long)logit_key(__ldcg(z + e)) << 32) | (unsigned)~e : 0ull;
     }
     return warp_topk<M>(c, K, lane);
 }
@@ -209,9 +209,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     }
     MOE_TRACE_POINT(0, 4);
     if (warp < nt) {
-        // sort keys (bits(sigmoid) + 1) << 32 | ~id (a NaN logit: 0 << 32 |
-        // ~id): larger is better, ties in the score go to the lower id; lane
-        // j < k ends with the j-th choice
+        // sort keys logit_key(logit) << 32 | ~id: larger is better, equal
+        // logits go to the lower id; lane j < k ends with the j-th choice
         const int t = t0 + warp;
         unsigned long long sel;
         switch (d.E <= 32 ? 1 : d.E <= 64 ? 2 : d.E <= 128 ? 4 : d.E <= 256 ? 8 : 16) {
@@ -224,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         const unsigned sel_key = (unsigned)(sel >> 32);
         const int sel_e = (int)~(unsigned)sel;
         // weights: normalised over the k selected scores (summed in selection order)
-        const float sel_s = sel_key ? __uint_as_float(sel_key - 1u) : -INFINITY;
+        const float sel_s = key_score(sel_key);
         float sum = 0.f;
         for (int j = 0; j < K; ++j) sum += __shfl_sync(0xffffffffu, sel_s, j);
         if (lane < K) {

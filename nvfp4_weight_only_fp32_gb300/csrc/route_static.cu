@@ -48,7 +48,8 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kTokGroup = 8;
 constexpr int kMaxDevices = 64;
 
-__device__ __forceinline__ bool ranks_before(float s, int e, float bs, int be) {
+// Ranking on logit_key(logit): larger first, the lower id on equal keys.
+__device__ __forceinline__ bool ranks_before(unsigned s, int e, unsigned bs, int be) {
     return s > bs || (s == bs && e < be);
 }
 
@@ -106,22 +107,17 @@ route_static_kernel(const float *__restrict__ Wr, const float *__restrict__ bias
     __threadfence();
 
     for (int t = warp; t < T; t += kWarps) {
-        float sc[kStaticMaxExperts / 32];
+        unsigned sc[kStaticMaxExperts / 32];
 #pragma unroll
         for (int m = 0; m < kStaticMaxExperts / 32; ++m) {
             const int ee = lane + 32 * m;
-            float s = -INFINITY;
-            if (ee < E) {
-                const float z = __ldcg(logits + (size_t)t * E + ee);
-                s = isnan(z) ? -INFINITY : moe::sigmoid_score(z);
-            }
-            sc[m] = s;
+            sc[m] = ee < E ? moe::logit_key(__ldcg(logits + (size_t)t * E + ee)) : 0u;
         }
         unsigned taken = 0u;
-        float sel_s = 0.f;
+        unsigned sel_k = 0u;
         int sel_e = 0;
         for (int j = 0; j < K; ++j) {
-            float bs = -INFINITY;
+            unsigned bs = 0u;
             int be = 0x7fffffff;
 #pragma unroll
             for (int m = 0; m < kStaticMaxExperts / 32; ++m) {
@@ -133,7 +129,7 @@ route_static_kernel(const float *__restrict__ Wr, const float *__restrict__ bias
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
-                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+                const unsigned os = __shfl_xor_sync(0xffffffffu, bs, off);
                 const int oe = __shfl_xor_sync(0xffffffffu, be, off);
                 if (ranks_before(os, oe, bs, be)) {
                     bs = os;
@@ -142,10 +138,11 @@ route_static_kernel(const float *__restrict__ Wr, const float *__restrict__ bias
             }
             if ((be & 31) == lane) taken |= 1u << (be >> 5);
             if (lane == j) {
-                sel_s = bs;
+                sel_k = bs;
                 sel_e = be;
             }
         }
+        const float sel_s = moe::key_score(sel_k);
         float sum = 0.f;
         for (int j = 0; j < K; ++j) sum += __shfl_sync(0xffffffffu, sel_s, j);
         if (lane < K) {
