@@ -305,7 +305,11 @@ __device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned lo
 // then down pieces) as (first byte, chunk count), filled by the warp's lanes
 // in parallel; lane 0 walks it, cutting items into segments of <= CH chunks.
 
-template <int QP>
+// TT: 1, 2 or 8, the token count the code is specialised for (T == TT for 1
+// and 2, 3 <= T <= 8 for 8) -- a step that runs once per call runs from a
+// cold instruction cache, so the loops over tokens are only as long as T
+// needs.
+template <int TT>
 __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, FusedGeom fg) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[kFW][kRWmax];
@@ -466,32 +470,29 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     // partial FP32 logits (token t, expert c + re * G) from the exact FP32
     // values of x; each router quad is read once for all tokens.
     {
-        float mx[kTF], acc[kTF * kREmax];
+        float mx[TT], acc[TT * kREmax];
 #pragma unroll
-        for (int t = 0; t < kTF; ++t) mx[t] = 0.f;
+        for (int t = 0; t < TT; ++t) mx[t] = 0.f;
 #pragma unroll
-        for (int i = 0; i < kTF * kREmax; ++i) acc[i] = 0.f;
+        for (int i = 0; i < TT * kREmax; ++i) acc[i] = 0.f;
+#pragma unroll 1
+        for (int P = threadIdx.x; P < nq; P += kFT) {
+            float4 w4[kREmax];
 #pragma unroll
-        for (int xp = 0; xp < QP; ++xp) {
-            const int P = threadIdx.x + xp * kFT;
-            if (P < nq) {
-                float4 w4[kREmax];
+            for (int re = 0; re < kREmax; ++re)
+                if (re < kRE) w4[re] = *reinterpret_cast<const float4 *>(s_router + (size_t)re * H + 4 * P);
 #pragma unroll
-                for (int re = 0; re < kREmax; ++re)
-                    if (re < kRE) w4[re] = *reinterpret_cast<const float4 *>(s_router + (size_t)re * H + 4 * P);
+            for (int t = 0; t < TT; ++t) {
+                if (t < T) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
+                    const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+                    const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+                    mx[t] = fmaxf(mx[t], fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
 #pragma unroll
-                for (int t = 0; t < kTF; ++t) {
-                    if (t < T) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
-                        const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
-                        const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
-                        mx[t] = fmaxf(mx[t], fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))));
-#pragma unroll
-                        for (int re = 0; re < kREmax; ++re)
-                            if (re < kRE)
-                                acc[t * kREmax + re] = fmaf(x3, w4[re].w, fmaf(x2, w4[re].z, fmaf(x1, w4[re].y,
-                                                            fmaf(x0, w4[re].x, acc[t * kREmax + re]))));
-                    }
+                    for (int re = 0; re < kREmax; ++re)
+                        if (re < kRE)
+                            acc[t * kREmax + re] = fmaf(x3, w4[re].w, fmaf(x2, w4[re].z, fmaf(x1, w4[re].y,
+                                                        fmaf(x0, w4[re].x, acc[t * kREmax + re]))));
                 }
             }
         }
@@ -499,17 +500,17 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         // warp maxima per token (mx >= 0 and not NaN -- fmaxf drops NaN --
         // so its bits order as unsigned)
 #pragma unroll
-        for (int t = 0; t < kTF; ++t) {
+        for (int t = 0; t < TT; ++t) {
             if (t < T) {
                 const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx[t])));
                 if (lane == 0) s_tmax[warp][t] = m;
             }
         }
         MOE_TRACE_CLOCK(4, 10);
-        if (T <= 2) {
+        if constexpr (TT <= 2) {
             // few values: a butterfly sum of each (the same pairing order)
 #pragma unroll
-            for (int i = 0; i < 2 * kREmax; ++i) {
+            for (int i = 0; i < TT * kREmax; ++i) {
                 if (i < T * kREmax) {
                     float v = acc[i];
 #pragma unroll
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         for (int w = 0; w < kFW; ++w) m = fmaxf(m, s_tmax[w][threadIdx.x]);
         s_xexp[threadIdx.x] = max(-100, exp_for_f16(m));
     }
-    if (threadIdx.x < kTF * kREmax) {
+    if (threadIdx.x < TT * kREmax) {
         // logits: the warps' sums in a fixed order, plus the router bias
         const int t = threadIdx.x / kREmax, re = threadIdx.x % kREmax, e = c + re * G;
         if (re < kRE && e < E && t < T) {
@@ -573,7 +574,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         for (int P = 32 * v0 + lane; P < nq; P += 32 * kPW) {
             const int m = P & 15, kb = m >> 2, hh = (m >> 1) & 1, q0 = 2 * (m & 1);
 #pragma unroll
-            for (int t = 0; t < kTF; ++t) {
+            for (int t = 0; t < TT; ++t) {
                 if (t < T) {
                     const float sc = pow2f(-s_xexp[t]);
                     const uint2 v = *reinterpret_cast<const uint2 *>(xraw + ((size_t)t * H + 4 * P) * 2);
@@ -648,7 +649,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     if (a.ids_out) a.ids_out[t * K + lane] = sel_e;
                     if (a.w_out) a.w_out[t * K + lane] = w;
                 }
-                if (T == 1) {
+                if constexpr (TT == 1) {
                     s_slot_e[S + rank] = sel_e;
                     s_slot_mask[S + rank] = 1;
                     s_slot_p0[S + rank] = S + rank;
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     atomicOr(reinterpret_cast<unsigned *>(s_tokmask) + (sel_e >> 2), 1u << (8 * (sel_e & 3) + t));
                 }
             }
-            if (T == 1 && lane == 0) s_nslots = S + K;
+            if (TT == 1 && lane == 0) s_nslots = S + K;
             MOE_TRACE_CLOCK_AT(3, 5, 0);
         }
         if (pass == 1) {
@@ -667,7 +668,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 break;
             }
             FUSED_TRACE(11);
-            if (T > 1) {
+            if constexpr (TT > 1) {
                 // slots: shared first, then routed experts in ascending id
                 // (one expert per thread); an expert's pairs are contiguous,
                 // tokens ascending
@@ -909,7 +910,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             }
         }
     };
-    if (T <= 2) {
+    if constexpr (TT <= 2) {
 #pragma unroll 1
         for (int r2 = 0; r2 < perw; ++r2) {
             const int pi = warp + kFW * r2, slot = pi >> lksd;
@@ -1011,8 +1012,8 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     if (threadIdx.x == 0) d.calls[c] = s_tag;
 }
 
-template <int QP>
-cudaError_t launch_q(const DevLayer &d, const FusedArgs &a, const FusedGeom &fg, int G, cudaStream_t s) {
+template <int TT>
+cudaError_t launch_tt(const DevLayer &d, const FusedArgs &a, const FusedGeom &fg, int G, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(kFT);
@@ -1023,78 +1024,75 @@ cudaError_t launch_q(const DevLayer &d, const FusedArgs &a, const FusedGeom &fg,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_kernel<QP>, d, a, fg);
+    return cudaLaunchKernelEx(&cfg, fused_kernel<TT>, d, a, fg);
 }
 
-constexpr int kQPcount = 4;                  // x quads per thread: H <= 4 * 4 * 512 = 8192
-int g_dyn_max[kQPcount + 1];                 // dynamic shared memory a block may use
+// the kernel instance for T tokens: 0 (TT = 1), 1 (TT = 2), 2 (TT = 8)
+int inst_of(int T) { return T == 1 ? 0 : T == 2 ? 1 : 2; }
+constexpr int kInst = 3;
+int g_dyn_max[kInst];                        // dynamic shared memory a block may use, by instance
 
-int qp_of(int H) { return (H / 4 + kFT - 1) / kFT; }
-
-template <int QP>
-cudaError_t prepare_q(int optin) {
+template <int TT>
+cudaError_t prepare_tt(int optin) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<QP>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<TT>);
     if (e != cudaSuccess) return e;
-    g_dyn_max[QP] = optin - (int)fa.sharedSizeBytes;
-    return cudaFuncSetAttribute(fused_kernel<QP>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_dyn_max[QP]);
+    g_dyn_max[inst_of(TT)] = optin - (int)fa.sharedSizeBytes;
+    return cudaFuncSetAttribute(fused_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                g_dyn_max[inst_of(TT)]);
 }
 
 }  // namespace
 
 // Largest T for which moe_decode_forward picks the single launch.
 constexpr int kFusedMaxT = 8;
+constexpr int kMaxFusedH = 8192;             // hidden sizes the single launch takes
 
 bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem) {
     (void)optin_smem;
     if (T < 1 || T > kFusedMaxT) return false;
     if (d.E > kREmax * sm_count) return false;
-    const int QP = qp_of(d.H);
-    if (QP < 1 || QP > kQPcount || g_dyn_max[QP] <= 0) return false;
+    if (d.H > kMaxFusedH || g_dyn_max[inst_of(T)] <= 0) return false;
     if (d.k * T + d.S > kSlotsF) return false;
     FusedGeom fg;
-    return fused_geometry(d, T, sm_count, g_dyn_max[QP], fg);
+    return fused_geometry(d, T, sm_count, g_dyn_max[inst_of(T)], fg);
 }
 
 cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
                          float *w, int sm_count, cudaStream_t s) {
-    const int QP = qp_of(d.H);
     FusedGeom fg;
-    if (QP < 1 || QP > kQPcount || !fused_geometry(d, T, sm_count, g_dyn_max[QP], fg)) return cudaErrorInvalidValue;
+    if (T < 1 || T > kFusedMaxT || d.H > kMaxFusedH || !fused_geometry(d, T, sm_count, g_dyn_max[inst_of(T)], fg))
+        return cudaErrorInvalidValue;
     FusedArgs a{x, T, out, ids, w};
-    switch (QP) {
-        case 1: return launch_q<1>(d, a, fg, sm_count, s);
-        case 2: return launch_q<2>(d, a, fg, sm_count, s);
-        case 3: return launch_q<3>(d, a, fg, sm_count, s);
-        default: return launch_q<4>(d, a, fg, sm_count, s);
+    switch (inst_of(T)) {
+        case 0: return launch_tt<1>(d, a, fg, sm_count, s);
+        case 1: return launch_tt<2>(d, a, fg, sm_count, s);
+        default: return launch_tt<8>(d, a, fg, sm_count, s);
     }
 }
 
 cudaError_t prepare_fused_kernel(int optin_bytes) {
-    cudaError_t e = prepare_q<1>(optin_bytes);
-    if (e == cudaSuccess) e = prepare_q<2>(optin_bytes);
-    if (e == cudaSuccess) e = prepare_q<3>(optin_bytes);
-    if (e == cudaSuccess) e = prepare_q<4>(optin_bytes);
+    cudaError_t e = prepare_tt<1>(optin_bytes);
+    if (e == cudaSuccess) e = prepare_tt<2>(optin_bytes);
+    if (e == cudaSuccess) e = prepare_tt<8>(optin_bytes);
     return e;
 }
 
 int fused_blocks_per_sm(const DevLayer &d, int T) {
-    const int QP = qp_of(d.H);
     int sms = 0, dev = 0;
-    if (QP < 1 || QP > kQPcount || cudaGetDevice(&dev) != cudaSuccess ||
+    if (T < 1 || T > kFusedMaxT || d.H > kMaxFusedH || cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     FusedGeom fg;
-    if (!fused_geometry(d, T, sms, g_dyn_max[QP], fg)) return 0;
+    if (!fused_geometry(d, T, sms, g_dyn_max[inst_of(T)], fg)) return 0;
     int n = 0;
     cudaError_t e;
-    switch (QP) {
-        case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kFT, fg.total); break;
-        case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<2>, kFT, fg.total); break;
-        case 3: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<3>, kFT, fg.total); break;
-        default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<4>, kFT, fg.total); break;
+    switch (inst_of(T)) {
+        case 0: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kFT, fg.total); break;
+        case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<2>, kFT, fg.total); break;
+        default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<8>, kFT, fg.total); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
