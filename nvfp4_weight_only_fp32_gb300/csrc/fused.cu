@@ -98,7 +98,7 @@ struct FusedArgs {
 struct FusedGeom {
     int kRE, RW, CH;
     int xrow, hrow;
-    int router_off, xraw_off, gs_off, ring_off, total;
+    int router_off, xraw_off, hs_off, gs_off, ring_off, total;
     int m1p;                                // top-k: experts per lane (1, 2, 4, 8)
     int lks0;                               // log2 of the pass-0 K split
     unsigned char lks1[kSlotsF + 1];        // log2 of the pass-1 K split, by slot count
@@ -134,7 +134,11 @@ bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) 
     g.xraw_off = g.router_off + (int)up16((size_t)g.kRE * d.H * 4);
     const size_t pB = (size_t)g.xraw_off + (size_t)T * d.H * 2;
     const size_t pD = (size_t)(T * (d.k + d.S) + 1) * g.hrow;
-    g.gs_off = (int)((std::max(pB, pD) + 15) & ~(size_t)15);
+    // the staged h rows of phase D: for T <= 2 behind x (over the router rows
+    // and the copied x, both dead by then), so that a warp may gather and
+    // use its h while other warps still read x; else over x as well
+    g.hs_off = T <= 2 ? g.router_off : 0;
+    g.gs_off = (int)((std::max(pB, (size_t)g.hs_off + pD) + 15) & ~(size_t)15);
     const size_t P = ((size_t)g.gs_off + (size_t)(d.E + d.S) * 16 + 127) & ~(size_t)127;
     g.ring_off = (int)P;
     if ((long)dyn_max <= (long)P) return false;
@@ -743,7 +747,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             MOE_TRACE_CLOCK(2, 14);
             n_list = p0.my + pp.my + nrt * perw;
             n_known = n_list;
-            if (ok) pump(n_con + RW);
+            // a warp with routed units requests its down pieces as its ring
+            // frees up, so that the routed gate/up weights, on which h and
+            // hence every block's phase D wait, come first
+            if (ok && pp.my == 0) pump(n_con + RW);
             MOE_TRACE_CLOCK(2, 15);
             __syncwarp();
             FUSED_TRACE(6);
@@ -824,13 +831,25 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         }
     }
     FUSED_TRACE(7);
-    // every warp is done with x and its gate/up units before phase D reuses
-    // the shared memory; a block without output tiles is done
-    if (!__syncthreads_and(ok) || nrt == 0) {
-        drain_ring(bar, RW, n_done, n_iss, lane);
-        FUSED_TRACE(9);
-        if (threadIdx.x == 0) d.calls[c] = s_tag;
-        return;
+    // a block without output tiles is done.  For more than two tokens every
+    // warp must be done with x and its gate/up units before phase D reuses
+    // the shared memory; for one or two the h rows have a region of their
+    // own, and a warp that failed a wait skips its work but keeps to the
+    // block's barriers.
+    if constexpr (TT <= 2) {
+        if (nrt == 0) {
+            drain_ring(bar, RW, n_done, n_iss, lane);
+            FUSED_TRACE(9);
+            if (threadIdx.x == 0) d.calls[c] = s_tag;
+            return;
+        }
+    } else {
+        if (!__syncthreads_and(ok) || nrt == 0) {
+            drain_ring(bar, RW, n_done, n_iss, lane);
+            FUSED_TRACE(9);
+            if (threadIdx.x == 0) d.calls[c] = s_tag;
+            return;
+        }
     }
     FUSED_TRACE(8);
 
@@ -844,7 +863,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     // tokens (the shared expert's slot alone has T rows) the tasks are spread
     // evenly over the warps and the block waits for all of them.  The B
     // column of a token a slot does not serve is zero.
-    uint8_t *hs = smem;
+    uint8_t *hs = smem + fg.hs_off;
     const int npairs = T * (K + S);
     int hpass = 0;
     FUSED_TRACE(14);
@@ -853,7 +872,13 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         const int npc = cpk * 16, pc0 = kp * npc;        // 16-byte pieces of the K part; the first
         const unsigned long long *src = d.h_tag + (size_t)p * (d.Imax / 2) + 2 * pc0;
         uint32_t *row = reinterpret_cast<uint32_t *>(hs + (size_t)p * fg.hrow);
-        float mx = 0.f;
+        // one batch: the prescale follows from the registers and the words
+        // are written once, already as f16; else raw BF16 first, rescaled
+        // after the last batch
+        const bool one = npc <= 32 * kHU;
+        float mx = 0.f, sc = 1.f;
+        int hx = 0;
+        MOE_TRACE_CLOCK(4, 13);
 #pragma unroll 1
         for (int P0 = 0; P0 < npc; P0 += 32 * kHU) {
             unsigned long long v[kHU][2];
@@ -878,6 +903,21 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                     ok = false;
                 }
             }
+            MOE_TRACE_CLOCK(4, 14);
+            // pieces past the end hold zeros, which leave the maximum alone
+#pragma unroll
+            for (int u = 0; u < kHU; ++u)
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const unsigned wv = (unsigned)v[u][h2];
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wv << 16)), fabsf(__uint_as_float(wv & 0xFFFF0000u))));
+                }
+            if (one) {
+                // mx >= 0 and not NaN (fmaxf drops NaN): its bits order as unsigned
+                mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
+                hx = max(-100, exp_for_f16(mx));
+                sc = pow2f(-hx);
+            }
 #pragma unroll
             for (int u = 0; u < kHU; ++u) {
                 if (P0 + lane + 32 * u < npc) {
@@ -887,28 +927,32 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                         // word wi of the row (elements 2wi, 2wi+1) -> its
                         // place in the operand order (as for x)
                         const int wi = 2 * (pc0 + P0 + lane + 32 * u) + h2, l = wi & 31;
-                        row[(wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1)] = wv;
-                        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wv << 16)), fabsf(__uint_as_float(wv & 0xFFFF0000u))));
+                        row[(wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1)] =
+                            one ? pack_f16x2(__uint_as_float(wv << 16) * sc, __uint_as_float(wv & 0xFFFF0000u) * sc)
+                                : wv;
                     }
                 }
             }
         }
-        // mx >= 0 and not NaN (fmaxf drops NaN): its bits order as unsigned
-        mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
-        const int hx = max(-100, exp_for_f16(mx));
-        if (lane == 0) s_hx[p][kp] = (signed char)hx;
-        const float sc = pow2f(-hx);
-        // each lane rescales the words it wrote
+        MOE_TRACE_CLOCK(4, 15);
+        if (!one) {
+            mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
+            hx = max(-100, exp_for_f16(mx));
+            sc = pow2f(-hx);
+            // each lane rescales the words it wrote
 #pragma unroll 1
-        for (int P = lane; P < npc; P += 32) {
+            for (int P = lane; P < npc; P += 32) {
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int wi = 2 * (pc0 + P) + h2, l = wi & 31;
-                uint32_t *w = row + (wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1);
-                const unsigned wv = *w;
-                *w = pack_f16x2(__uint_as_float(wv << 16) * sc, __uint_as_float(wv & 0xFFFF0000u) * sc);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int wi = 2 * (pc0 + P) + h2, l = wi & 31;
+                    uint32_t *w = row + (wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1);
+                    const unsigned wv = *w;
+                    *w = pack_f16x2(__uint_as_float(wv << 16) * sc, __uint_as_float(wv & 0xFFFF0000u) * sc);
+                }
             }
         }
+        if (lane == 0) s_hx[p][kp] = (signed char)hx;
+        MOE_TRACE_CLOCK(4, 11);
     };
     if constexpr (TT <= 2) {
 #pragma unroll 1
