@@ -356,46 +356,32 @@ __device__ __forceinline__ float key_score(unsigned key) {
     return key ? sigmoid_score(z) : __int_as_float(0x7fc00000);
 }
 
-// Sort M (a power of two) 64-bit keys held by one lane, largest first
-// (bitonic network; every index is a compile-time constant, so the keys stay
-// in registers).
-template <int M>
-__device__ __forceinline__ void sort_desc(unsigned long long (&c)[M]) {
-#pragma unroll
-    for (int k = 2; k <= M; k <<= 1)
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1)
-#pragma unroll
-            for (int i = 0; i < M; ++i) {
-                const int l = i ^ j;
-                if (l > i) {
-                    const unsigned long long a = c[i], b = c[l];
-                    const bool sw = (i & k) == 0 ? a < b : a > b;
-                    c[i] = sw ? b : a;
-                    c[l] = sw ? a : b;
-                }
-            }
-}
-
-// Warp-wide top-k over 64-bit sort keys, M per lane (all keys distinct; 0
-// marks an empty place and is never chosen while k <= the number of real
-// keys).  Each lane sorts its keys once; every round takes the largest head
-// (its high word, then among lanes holding that, its low word) and the lane
-// that held it moves its list up.  Lane j < k ends with the j-th choice.
+// Warp-wide top-k over 64-bit sort keys, M per lane (M a power of two; all
+// keys distinct; 0 marks an empty place and is never chosen while k <= the
+// number of real keys).  Every round each lane takes the largest of its
+// keys (a pairwise tree), the warp takes the largest of those (its high
+// word, then among the lanes holding that, its low word) and the lane that
+// held it clears it.  Lane j < k ends with the j-th choice.  The code is
+// short on purpose: it runs once per call, from a cold instruction cache.
 template <int M>
 __device__ __forceinline__ unsigned long long warp_topk(unsigned long long (&c)[M], int K, int lane) {
-    sort_desc<M>(c);
     unsigned long long mine = 0ull;
 #pragma unroll 1
     for (int j = 0; j < K; ++j) {
-        const unsigned hi = (unsigned)(c[0] >> 32), lo = (unsigned)c[0];
+        unsigned long long t[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) t[i] = c[i];
+#pragma unroll
+        for (int w = M / 2; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) t[i] = t[i + w] > t[i] ? t[i + w] : t[i];
+        const unsigned hi = (unsigned)(t[0] >> 32), lo = (unsigned)t[0];
         const unsigned mx = __reduce_max_sync(0xffffffffu, hi);
         const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mx ? lo : 0u);
         if (lane == j) mine = ((unsigned long long)mx << 32) | ml;
         if (hi == mx && lo == ml) {
 #pragma unroll
-            for (int i = 0; i + 1 < M; ++i) c[i] = c[i + 1];
-            c[M - 1] = 0ull;
+            for (int i = 0; i < M; ++i) c[i] = c[i] == t[0] ? 0ull : c[i];
         }
     }
     return mine;
