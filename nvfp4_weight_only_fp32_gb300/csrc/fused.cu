@@ -108,12 +108,14 @@ struct FusedGeom {
 inline size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
 
 // Groups of ks warps share a gate/up unit by splitting K; ks minimises the
-// chunks of the busiest warp plus one chunk's worth per unit (the epilogue).
+// chunks of the busiest warp plus one chunk's worth per unit (the epilogue)
+// and, when K is split, two more per unit: the group's named barrier (where
+// its warps wait for the one whose data came last) and the reduction.
 int choose_lks(int units, int NC, int G, int nw) {
     int best = 0, bestc = 0x7fffffff;
     for (int l = 0; (1 << l) <= nw && NC % (1 << l) == 0; ++l) {
         const int groups = G * (nw >> l);
-        const int cost = (units + groups - 1) / groups * (NC / (1 << l) + 1);
+        const int cost = (units + groups - 1) / groups * (NC / (1 << l) + 1 + (l > 0 ? 2 : 0));
         if (cost < bestc) {
             bestc = cost;
             best = l;
