@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK_AT(2, 4 * pass, pass == 0 ? 64 : 0);
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
-#pragma unroll 1
+#pragma unroll 2
                     for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, true, a0, a1);
                 }
                 __syncwarp();
@@ -1003,7 +1003,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 if (ri == 0 && r2 == 0 && lft == cpk) MOE_TRACE_CLOCK(2, 10);
                 if (ok) {
                     const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
-#pragma unroll 1
+#pragma unroll 2
                     for (int i = 0; i < n; ++i)
                         chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, bon, a0, a1);
                 }
