@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
         reinterpret_cast<uint4 *>(smem + (size_t)m * row_stride)[i] = make_uint4(0u, 0u, 0u, 0u);
 
     float acc[GMAX][4];
+    float acc1[4] = {0.f, 0.f, 0.f, 0.f};   // one token group: blocks 1 and 3 (a chain half as long)
 #pragma unroll
     for (int G2 = 0; G2 < GMAX; ++G2)
 #pragma unroll
@@ -278,10 +279,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
                                 const uint8_t *bp = bp0 + (size_t)G2 * 8 * row_stride;
                                 const uint4 b01 = lds128(bp);
                                 const uint4 b23 = lds128(bp + 16);
+                                float(&ac1)[4] = GMAX == 1 ? acc1 : acc[G2];
                                 mma_16816(acc[G2], a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
-                                mma_16816(acc[G2], a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
+                                mma_16816(ac1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
                                 mma_16816(acc[G2], a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
-                                mma_16816(acc[G2], a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                                mma_16816(ac1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
                             }
                         }
                         const int cn = c + PD;
@@ -293,6 +295,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     }
 
     MOE_TRACE_POINT(1 + MODE, 3);
+    if (GMAX == 1) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[0][v] += acc1[v];
+    }
     if (ksplit > 1) {
         // Fixed-order K reduction across the warps sharing a tile.
         if (ks > 0) {
