@@ -71,6 +71,7 @@ constexpr int kPW = 8;                                   // warps of the shared-
 constexpr int kStageBar = 15;                            // named barrier of the x staging (the kPW pass-0 warps)
 constexpr int kREmax = 4;                                // router experts per block
 static_assert(kTF * kREmax == 32, "the logit reduction gives each lane one (token, expert) value");
+static_assert(kTF + kPW <= kFW, "routing warps and shared-expert warps are distinct");
 constexpr int kCHmax = 8;                                // chunks per ring segment
 constexpr int kCHmin = 4;
 constexpr int kRWmax = 6;                                // ring segments per warp
@@ -182,17 +183,23 @@ __device__ __forceinline__ unsigned long long gtimer() {
     return t;
 }
 
-// Warp roles while the block routes.  Warp w runs on SM sub-partition w % 4.
-// The routing warps (one per token) sit on sub-partitions 0 and 1 -- token t
-// on warp 4t for t < 4, on warp 4(t - 4) + 1 above -- and the shared-expert
-// pass on sub-partitions 2 and 3, so that the issue-bound decode of that pass
-// does not share a scheduler with the latency-bound routing.
+// Warp roles while the block routes (one routing warp per token).  Warp w
+// runs on SM sub-partition w % 4.  For one or two tokens (TT <= 2) token t's
+// warp is 4t, on sub-partition 0, and the shared-expert pass runs on the
+// warps of sub-partitions 2 and 3, so that its issue-bound decode does not
+// share a scheduler with the latency-bound routing.  For more tokens the
+// routing's compare-and-select work is the larger cost and is spread over all
+// four sub-partitions: token t on warp t, the pass on warps 8..15.
+template <int TT>
 __device__ __forceinline__ int routed_token_of(int w) {
-    return (w & 3) == 0 ? (w >> 2) : (w & 3) == 1 ? 4 + (w >> 2) : -1;
+    if (TT <= 2) return (w & 3) == 0 ? (w >> 2) : -1;
+    return w < kPW ? w : -1;
 }
 // Index of warp w among the kPW warps of the shared-expert pass (kFW if none).
+template <int TT>
 __device__ __forceinline__ int pass0_index(int w) {
-    return (w & 3) >= 2 ? 2 * (w >> 2) + (w & 3) - 2 : kFW;
+    if (TT <= 2) return (w & 3) >= 2 ? 2 * (w >> 2) + (w & 3) - 2 : kFW;
+    return w >= kFW - kPW ? w - (kFW - kPW) : kFW;
 }
 
 // Wait for phase `parity` of an mbarrier; gives up after kWaitNs, setting the
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         for (int i = 0; i < RW; ++i) mbar_init(bar + i, 1);
         fence_proxy_async();
     }
-    const int v0 = pass0_index(warp), tok = routed_token_of(warp);
+    const int v0 = pass0_index<TT>(warp), tok = routed_token_of<TT>(warp);
     const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW, v0);
     __syncthreads();
     fill_units(p0, 0);
