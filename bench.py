@@ -46,8 +46,8 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20772352, "fused_cu_sha256_16": "ea91cb6c646f7081"},
-    "flint8": {"bytes": 124616448, "fused_cu_sha256_16": "ea91cb6c646f7081"},
+    "flint1": {"bytes": 20775168, "fused_cu_sha256_16": "f86527a3cf135a13"},
+    "flint8": {"bytes": 124784128, "fused_cu_sha256_16": "f86527a3cf135a13"},
 }
 
 def ncu_traffic(workload: str):
