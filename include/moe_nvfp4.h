@@ -163,9 +163,12 @@ moe_status moe_decode_forward(moe_layer *layer, const void *x, int T, void *out,
                               int *topk_ids, float *topk_w, void *stream);
 
 /* The same step with HOST buffers (pinned memory for asynchronous copies):
- * copies x_host to the device, runs moe_decode_forward, copies out and the
- * routing result back.  Returns after enqueueing; the host buffers may be read
- * after the stream has been synchronised. */
+ * copies x_host to the device and runs moe_decode_forward; when out_host is
+ * pinned (page-locked and mapped, as cudaHostAlloc gives) and 16-byte
+ * aligned the kernels store the output straight into it through its device
+ * alias, otherwise it is copied back; the routing result (optional) is copied
+ * back.  Returns after enqueueing; the host buffers may be read after the
+ * stream has been synchronised. */
 moe_status moe_decode_forward_host(moe_layer *layer, const void *x_host, int T,
                                    void *out_host, int *topk_ids_host,
                                    float *topk_w_host, void *stream);

@@ -427,9 +427,17 @@ moe_status moe_decode_forward_host(moe_layer *L, const void *x_host, int T, void
     const size_t nk = (size_t)T * L->cfg.top_k;
     cudaError_t e = cudaMemcpyAsync(L->x_stage, x_host, nb, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "x upload");
-    rc = moe_decode_forward(L, L->x_stage, T, L->out_stage, L->ids_stage, L->w_stage, stream);
+    // pinned (page-locked, mapped) output: the kernels store straight into it
+    // through its device alias instead of a copy after them
+    void *out_dev = nullptr;
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer && aligned16(pa.devicePointer))
+        out_dev = pa.devicePointer;
+    cudaGetLastError();
+    rc = moe_decode_forward(L, L->x_stage, T, out_dev ? out_dev : L->out_stage, L->ids_stage, L->w_stage, stream);
     if (rc != MOE_OK) return rc;
-    e = cudaMemcpyAsync(out_host, L->out_stage, nb, cudaMemcpyDeviceToHost, st);
+    e = out_dev ? cudaSuccess : cudaMemcpyAsync(out_host, L->out_stage, nb, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && topk_ids_host)
         e = cudaMemcpyAsync(topk_ids_host, L->ids_stage, nk * sizeof(int), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && topk_w_host)

@@ -164,15 +164,20 @@ def test_many_calls_keep_tags_in_step(moe, orc):
         L.close()
 
 
-def test_host_buffer_entry_point(moe, orc):
-    layer, x, _ = guarded_case(1, 13)
-    L = moe.MoELayer(layer, max_tokens=1)
+@pytest.mark.parametrize("cfg,T,pinned", [(1, 1, True), (1, 1, False), (0, 12, True), (0, 12, False)])
+def test_host_buffer_entry_point(moe, orc, cfg, T, pinned):
+    """Host buffers: pinned output is written through its device alias (the
+    single launch at T=1, the chain's down kernel at T=12), pageable output
+    is copied back; both equal the device-buffer call bit for bit."""
+    layer, x, _ = guarded_case(cfg, 13, T=T)
+    L = moe.MoELayer(layer, max_tokens=T)
     try:
-        T, H, k = 1, layer["cfg"]["H"], layer["cfg"]["k"]
-        xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
-        oh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-        ih = torch.empty((T, k), dtype=torch.int32).pin_memory()
-        wh = torch.empty((T, k), dtype=torch.float32).pin_memory()
+        H, k = layer["cfg"]["H"], layer["cfg"]["k"]
+        pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+        xh = pin(torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16))
+        oh = pin(torch.full((T, H), 7.0, dtype=torch.bfloat16))
+        ih = pin(torch.empty((T, k), dtype=torch.int32))
+        wh = pin(torch.empty((T, k), dtype=torch.float32))
         moe.moe_decode_forward_host(L.h, xh, T, oh, ih, wh)
         torch.cuda.synchronize()
         dout, dids, dw = run_gpu(moe, layer, x, layer_obj=L)
