@@ -370,11 +370,13 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     constexpr bool trc = false;
 #endif
     const uint8_t *src = nullptr;
+    // No proxy fence before a refill: every shared-memory read of a slot
+    // being refilled has returned its data before the __syncwarp that
+    // precedes the call (the values fed MMAs issued before it), so the bulk
+    // copy's write cannot overtake a read -- the write-after-read order that
+    // mbarrier-synchronised bulk-copy pipelines rely on as well.
     auto pump = [&](int limit) {
         if (lane != 0) return;
-        // one proxy fence orders the warp's reads of the slots about to be
-        // refilled before all of this call's copies
-        if (n_iss < limit && (left > 0 || it < n_known)) fence_proxy_async();
         if (trc) MOE_TRACE_CLOCK(4, 7);
         while (n_iss < limit) {
             if (left == 0) {
