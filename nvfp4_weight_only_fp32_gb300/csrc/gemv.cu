@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     };
 
     if (MODE == 0) {
-        if (shared && GMAX > 1 && d.grouped_min > 0 && T >= d.grouped_min) {   // grouped kernel's
+        if (shared && T > 8 && d.grouped_min > 0 && T >= d.grouped_min) {   // grouped kernel's
             // every block waits before it leaves, so that "all blocks of this
             // kernel released the next one" implies the router has finished
             pdl_wait();
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
                 return;
             }
             m = __ldcg(d.slot_m + s);
-            if (GMAX > 1 && d.grouped_min > 0 && m >= d.grouped_min) {   // grouped kernel's
+            if (T > 8 && d.grouped_min > 0 && m >= d.grouped_min) {   // grouped kernel's
                 pdl_trigger();
                 return;
             }
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
             return;
         }
         m = __ldcg(d.slot_m + s);
-        if (GMAX > 1 && d.grouped_min > 0 && m >= d.grouped_min) {   // grouped kernel's (and its ticket)
+        if (T > 8 && d.grouped_min > 0 && m >= d.grouped_min) {   // grouped kernel's (and its ticket)
             pdl_wait();   // as above: h is complete once every block has released the next kernel
             pdl_trigger();
             return;
@@ -411,7 +411,10 @@ cudaError_t launch_stage(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_
     const int NCmin = MODE == 0 ? d.H / kChunkK : Imin / kChunkK;
     // the combine (down) needs room for the [T, k+S] pair table
     const size_t combine_smem = (size_t)kMaxTokens * 16 * (sizeof(int) + sizeof(float));
-    if (T <= 8) {
+    // at most 8 tokens per slot here: up to 8 tokens in all, or the grouped
+    // kernels take every slot with at least grouped_min <= 8 of them -- one
+    // token group, the 8-deep register ring
+    if (T <= 8 || (d.grouped_min > 0 && d.grouped_min <= 8)) {
         const long tiles = (long)slots * NT;
         int ksplit = 1;
         while (ksplit < 4 && tiles * ksplit < 2048 && NCmin >= 4 * ksplit) ksplit *= 2;
