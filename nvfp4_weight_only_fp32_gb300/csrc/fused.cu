@@ -397,7 +397,11 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     // gate/up plan of one pass: groups of 2^lks warps share a unit (slot lo +
     // uu / NT, tile uu % NT) by splitting its K range; the warp with index vw
     // among the pass's nw warps takes units uu = u0 + i * stride, i < my, and
-    // the K range [cb0, cb0 + cpw)
+    // the K range [cb0, cb0 + cpw).  With more units than groups, unit uu
+    // goes to group uu / G of block uu % G (modulo the stride), so every
+    // block gets the floor or the ceiling of units / G (the decode rate of
+    // an SM is shared by its warps); with fewer, a block's groups take
+    // consecutive units (measured slightly faster at one token).
     struct Pass {
         int lks, cpw, cb0, stride, u0, my, NT, lo;
     };
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         p.cpw = NC13 >> lks;
         p.cb0 = (vw & ((1 << lks) - 1)) * p.cpw;
         p.stride = G * ngrp;
-        p.u0 = c * ngrp + (vw >> lks);
+        p.u0 = units > p.stride ? (vw >> lks) * G + c : c * ngrp + (vw >> lks);
         p.my = vw < nw && p.u0 < units ? (units - p.u0 + p.stride - 1) / p.stride : 0;
         p.NT = NT;
         p.lo = lo;
