@@ -80,6 +80,7 @@ constexpr int kPairsF = kFusedPairs;                     // pairs of a call with
 constexpr int kM1max = 8;                                // experts per lane in the top-k (E <= 256)
 constexpr int kTabMax = 32;                              // copy-list items per warp
 constexpr int kHU = 8;                                   // tagged h pieces in flight per lane
+constexpr int kHU2 = 6;                                  // per task when two tasks share a poll
 constexpr unsigned long long kWaitNs = 1000000000ull;    // in-kernel waits give up after ~1 s
 
 struct FusedArgs {
@@ -969,6 +970,81 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         if (lane == 0) s_hx[p][kp] = (signed char)hx;
         MOE_TRACE_CLOCK(4, 11);
     };
+    // two tasks polled together (one round trip for both) when each has at
+    // most 32 * kHU2 pieces; else one after the other
+    auto gather2 = [&](int pa, int kpa, int pb, int kpb) {
+        const int pp2[2] = {pa, pb}, kk2[2] = {kpa, kpb};
+        int npc2[2], pc02[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            npc2[j] = ((pp2[j] < S * T ? d.Is : d.I) / kChunkK >> lksd) * 16;
+            pc02[j] = kk2[j] * npc2[j];
+        }
+        if (npc2[0] > 32 * kHU2 || npc2[1] > 32 * kHU2) {
+            gather(pa, kpa);
+            gather(pb, kpb);
+            return;
+        }
+        unsigned long long v[2][kHU2][2];
+        unsigned pend = 0u;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int u = 0; u < kHU2; ++u) {
+                v[j][u][0] = v[j][u][1] = 0ull;
+                if (lane + 32 * u < npc2[j]) pend |= 1u << (j * kHU2 + u);
+            }
+        const unsigned long long t0 = gtimer();
+        while (pend && ok) {
+            ++hpass;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int u = 0; u < kHU2; ++u)
+                    if ((pend >> (j * kHU2 + u)) & 1u)
+                        ld_tagged2(d.h_tag + (size_t)pp2[j] * (d.Imax / 2) + 2 * (pc02[j] + lane + 32 * u), v[j][u][0],
+                                   v[j][u][1]);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int u = 0; u < kHU2; ++u)
+                    if (((pend >> (j * kHU2 + u)) & 1u) && tag_is(v[j][u][0], s_tag) && tag_is(v[j][u][1], s_tag))
+                        pend &= ~(1u << (j * kHU2 + u));
+            if (pend && gtimer() - t0 > kWaitNs) {
+                atomicExch(d.err, 1);
+                ok = false;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = 0.f;
+#pragma unroll
+            for (int u = 0; u < kHU2; ++u)
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const unsigned wv = (unsigned)v[j][u][h2];
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wv << 16)), fabsf(__uint_as_float(wv & 0xFFFF0000u))));
+                }
+            // mx >= 0 and not NaN (fmaxf drops NaN): its bits order as unsigned
+            mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
+            const int hx = max(-100, exp_for_f16(mx));
+            const float sc = pow2f(-hx);
+            uint32_t *row = reinterpret_cast<uint32_t *>(hs + (size_t)pp2[j] * fg.hrow);
+#pragma unroll
+            for (int u = 0; u < kHU2; ++u) {
+                if (lane + 32 * u < npc2[j]) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const unsigned wv = (unsigned)v[j][u][h2];
+                        const int wi = 2 * (pc02[j] + lane + 32 * u) + h2, l = wi & 31;
+                        row[(wi & ~31) + 8 * (l & 3) + 2 * (l >> 3) + ((l >> 2) & 1)] =
+                            pack_f16x2(__uint_as_float(wv << 16) * sc, __uint_as_float(wv & 0xFFFF0000u) * sc);
+                    }
+                }
+            }
+            if (lane == 0) s_hx[pp2[j]][kk2[j]] = (signed char)hx;
+        }
+    };
     if constexpr (TT <= 2) {
 #pragma unroll 1
         for (int r2 = 0; r2 < perw; ++r2) {
@@ -980,7 +1056,13 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         __syncwarp();
     } else {
 #pragma unroll 1
-        for (int tk = warp; tk < (npairs << lksd); tk += kFW) gather(tk >> lksd, tk & ((1 << lksd) - 1));
+        for (int tk = warp; tk < (npairs << lksd); tk += 2 * kFW) {
+            const int tb = tk + kFW;
+            if (tb < (npairs << lksd))
+                gather2(tk >> lksd, tk & ((1 << lksd) - 1), tb >> lksd, tb & ((1 << lksd) - 1));
+            else
+                gather(tk >> lksd, tk & ((1 << lksd) - 1));
+        }
         if (!__syncthreads_and(ok)) {
             drain_ring(bar, RW, n_done, n_iss, lane);
             FUSED_TRACE(9);
