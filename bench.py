@@ -46,8 +46,8 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20775168, "fused_cu_sha256_16": "f86527a3cf135a13"},
-    "flint8": {"bytes": 124784128, "fused_cu_sha256_16": "f86527a3cf135a13"},
+    "flint1": {"bytes": 20774400, "fused_cu_sha256_16": "8dc53de3ac787ff5"},
+    "flint8": {"bytes": 124850944, "fused_cu_sha256_16": "8dc53de3ac787ff5"},
 }
 
 def ncu_traffic(workload: str):
