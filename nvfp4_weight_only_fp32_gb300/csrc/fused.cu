@@ -69,6 +69,9 @@ constexpr int kFT = 32 * kFW;
 constexpr int kTF = 8;                                   // tokens (MMA N)
 constexpr int kPW = 8;                                   // warps of the shared-expert pass (see pass0_index)
 constexpr int kStageBar = 15;                            // named barrier of the x staging (the kPW pass-0 warps)
+constexpr int kGroupBar1 = 1;                            // split-K groups of the routed pass: ids 1..8
+constexpr int kGroupBar0 = 9;                            // of the shared-expert pass: ids 9..12
+static_assert(kGroupBar1 + kFW / 2 <= kGroupBar0 && kGroupBar0 + kPW / 2 <= kStageBar, "named barrier ids overlap");
 constexpr int kREmax = 4;                                // router experts per block
 static_assert(kTF * kREmax == 32, "the logit reduction gives each lane one (token, expert) value");
 static_assert(kTF + kPW <= kFW, "routing warps and shared-expert warps are distinct");
@@ -617,6 +620,88 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     int n_done = 0;                      // segments whose copies have landed (waited for)
     int nslots = S, lksd = 0, perw = 0, nrt = 0, n_list = 0;
     const int nrt0 = c < NRT ? (NRT - c + G - 1) / G : 0;   // this block's output tiles
+    // gate/up units of a pass plan: vw is this warp's index among the pass's
+    // warps, tp the pass (0 shared experts, 1 routed), rb + vw the warp's
+    // row of the reduction scratch (the physical warp where the two passes
+    // may overlap)
+    auto run_units = [&](const Pass &pp, int vw, int tp, int rb) {
+        const int ks = 1 << pp.lks, gi = vw >> pp.lks, kw = vw & (ks - 1);
+        // every warp of a group has the same unit count, so the group's named
+        // barrier is reached by all of its warps together: id kGroupBar1 + gi
+        // in the routed pass (at most 8 groups), kGroupBar0 + gi in the
+        // shared-expert pass (at most 4), which the routed pass may overlap
+        const int gb = (tp == 0 ? kGroupBar0 : kGroupBar1) + gi;
+#pragma unroll 1
+        for (int ui = 0; ui < pp.my; ++ui) {
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint8_t *bp = xb + pp.cb0 * 128;
+            int lft = pp.cpw;
+#pragma unroll 1
+            while (lft > 0) {
+                const int n = min(CH, lft);
+                if (ok) {
+                    if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
+                    else ok = false;
+                }
+                if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK_AT(2, 4 * tp, tp == 0 ? 64 : 0);
+                if (ok) {
+                    const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
+#pragma unroll 2
+                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, true, a0, a1);
+                }
+                __syncwarp();
+                bp += n * 128;
+                lft -= n;
+                ++n_con;
+                if (++sl_c == RW) {
+                    sl_c = 0;
+                    par_c ^= 1u;
+                }
+                if (ok) pump(n_con + RW);
+            }
+            if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * tp + 1, tp == 0 ? 64 : 0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) a0[v] += a1[v];
+            const int uu = pp.u0 + ui * pp.stride;
+            const int s = uu / pp.NT, r = uu - s * pp.NT, slot = pp.lo + s;
+            if (ks > 1) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) s_red[rb + vw][v][lane] = a0[v];
+                asm volatile("bar.sync %0, %1;\n" ::"r"(gb), "r"(32 * ks) : "memory");
+                if (kw == 0) {
+#pragma unroll 1
+                    for (int w = 1; w < ks; ++w)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) a0[v] += s_red[rb + vw + w][v][lane];
+                }
+                asm volatile("bar.sync %0, %1;\n" ::"r"(gb), "r"(32 * ks) : "memory");
+            }
+            if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * tp + 2, tp == 0 ? 64 : 0);
+            if (kw == 0 && __all_sync(0xffffffffu, ok)) {
+                // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row
+                // 8r+g; lanes g and g+1 publish one tagged word of two BF16
+                const int e = s_slot_e[slot], msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
+                const float4 gsv = s_gsp[e < 0 ? E - e - 1 : e];
+                const float gsa = gsv.x, gsb = gsv.y;
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int t = 2 * q + e2;
+                    const bool on = t < T && ((msk >> t) & 1);
+                    const int p = p0s + __popc(msk & ((1 << t) - 1));
+                    unsigned hbits = 0u;
+                    if (on) {
+                        const float un = pow2f(s_xexp[t]);
+                        const float gt = a0[e2] * gsa * un, upv = a0[2 + e2] * gsb * un;
+                        hbits = __bfloat16_as_ushort(__float2bfloat16_rn(silu_fast(gt) * upv));
+                    }
+                    const unsigned hnext = __shfl_down_sync(0xffffffffu, hbits, 4);
+                    if (on && !(g & 1))
+                        st_tagged(d.h_tag + ((size_t)p * d.Imax + 8 * r + g) / 2, s_tag, hbits | (hnext << 16));
+                }
+            }
+            MOE_TRACE_CLOCK_AT(2, 4 * tp + 3, tp == 0 ? 64 : 0);
+        }
+    };
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
         Pass pp = p0;
@@ -771,79 +856,17 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             __syncwarp();
             FUSED_TRACE(6);
         }
-        const int vw = pass == 0 ? v0 : warp;         // index among the pass's warps
-        const int ks = 1 << pp.lks, gi = vw >> pp.lks, kw = vw & (ks - 1);
-        // every warp of a group has the same unit count, so the group's named
-        // barrier (id 1 + gi) is reached by all of its warps together
-#pragma unroll 1
-        for (int ui = 0; ui < pp.my; ++ui) {
-            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint8_t *bp = xb + pp.cb0 * 128;
-            int lft = pp.cpw;
-#pragma unroll 1
-            while (lft > 0) {
-                const int n = min(CH, lft);
-                if (ok) {
-                    if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
-                    else ok = false;
-                }
-                if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK_AT(2, 4 * pass, pass == 0 ? 64 : 0);
-                if (ok) {
-                    const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
-#pragma unroll 2
-                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, true, a0, a1);
-                }
-                __syncwarp();
-                bp += n * 128;
-                lft -= n;
-                ++n_con;
-                if (++sl_c == RW) {
-                    sl_c = 0;
-                    par_c ^= 1u;
-                }
-                if (ok) pump(n_con + RW);
+        if constexpr (TT > 2) {
+            // more tokens: the shared-expert units wait for the routing (whose
+            // compare-and-select work would share schedulers with their
+            // decode); their segments were requested first, so they run
+            // first in pass 1
+            if (pass == 1) {
+                run_units(p0, v0, 0, kFW - kPW);   // the pass-0 warps are kFW - kPW .. kFW - 1
+                run_units(pp, warp, 1, 0);
             }
-            if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * pass + 1, pass == 0 ? 64 : 0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) a0[v] += a1[v];
-            const int uu = pp.u0 + ui * pp.stride;
-            const int s = uu / pp.NT, r = uu - s * pp.NT, slot = pp.lo + s;
-            if (ks > 1) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) s_red[vw][v][lane] = a0[v];
-                asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
-                if (kw == 0) {
-#pragma unroll 1
-                    for (int w = 1; w < ks; ++w)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) a0[v] += s_red[vw + w][v][lane];
-                }
-                asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gi), "r"(32 * ks) : "memory");
-            }
-            if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * pass + 2, pass == 0 ? 64 : 0);
-            if (kw == 0 && __all_sync(0xffffffffu, ok)) {
-                // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row
-                // 8r+g; lanes g and g+1 publish one tagged word of two BF16
-                const int e = s_slot_e[slot], msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
-                const float4 gsv = s_gsp[e < 0 ? E - e - 1 : e];
-                const float gsa = gsv.x, gsb = gsv.y;
-#pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int t = 2 * q + e2;
-                    const bool on = t < T && ((msk >> t) & 1);
-                    const int p = p0s + __popc(msk & ((1 << t) - 1));
-                    unsigned hbits = 0u;
-                    if (on) {
-                        const float un = pow2f(s_xexp[t]);
-                        const float gt = a0[e2] * gsa * un, upv = a0[2 + e2] * gsb * un;
-                        hbits = __bfloat16_as_ushort(__float2bfloat16_rn(silu_fast(gt) * upv));
-                    }
-                    const unsigned hnext = __shfl_down_sync(0xffffffffu, hbits, 4);
-                    if (on && !(g & 1))
-                        st_tagged(d.h_tag + ((size_t)p * d.Imax + 8 * r + g) / 2, s_tag, hbits | (hnext << 16));
-                }
-            }
-            MOE_TRACE_CLOCK_AT(2, 4 * pass + 3, pass == 0 ? 64 : 0);
+        } else {
+            run_units(pp, pass == 0 ? v0 : warp, pass, 0);
         }
     }
     FUSED_TRACE(7);
