@@ -46,8 +46,8 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20774144, "fused_cu_sha256_16": "c019f0a18d850dd6"},
-    "flint8": {"bytes": 124694272, "fused_cu_sha256_16": "c019f0a18d850dd6"},
+    "flint1": {"bytes": 20774144, "fused_cu_sha256_16": "7c939201365def2d"},
+    "flint8": {"bytes": 124694272, "fused_cu_sha256_16": "7c939201365def2d"},
 }
 
 def ncu_traffic(workload: str):

@@ -31,10 +31,11 @@
 //      per-token max |x| and this block's experts' FP32 logits, published as
 //      tagged words; the shared-expert warps stage x as the f16 MMA operand
 //      (exact per-row power-of-two prescale).
-//   C  pass 0: the shared-expert gate/up units, while one warp per token
-//      polls all logits and takes the top-k (the same in every block);
-//      pass 1: the routed gate/up units.  SwiGLU in the epilogue; h is
-//      published as tagged words.
+//   C  pass 0: one warp per token polls all logits and takes the top-k (the
+//      same in every block) while, for one or two tokens, the shared-expert
+//      warps run their gate/up units (for more tokens those wait for pass 1,
+//      where they run first); pass 1: the routed gate/up units.  SwiGLU in
+//      the epilogue; h is published as tagged words.
 //   D  h is gathered from the tagged words as f16 (an exact power-of-two
 //      prescale per piece); each block owns 16-row output tiles for all
 //      slots: down GEMV per (slot, K part) and warp, routing weight, a
@@ -44,9 +45,9 @@
 // the lane that owns the token.
 //
 // Everything between the weight streams is a short serial step executed once
-// per layer, so the work split is planned on the host (tables indexed by the
-// slot count) and the device side uses shifts and incremental counters
-// instead of integer division.
+// per layer, from a cold instruction cache, so the work split is planned on
+// the host (tables indexed by the slot count) and the code of those steps is
+// kept short (one kernel instance per token-count class).
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -707,11 +708,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         Pass pp = p0;
         if (pass == 0 && tok >= 0 && tok < T) {
             // routing, identical in every block, straight from the tagged
-            // logits (no grid barrier), while the pass-0 warps run the shared
-            // experts: one warp per token t (routed_token_of), lane L the
-            // experts i * 32 + L.  An expert's sort key is logit_key(logit) << 32 | ~id:
-            // larger is better, equal logits go to the lower id, all keys
-            // differ.
+            // logits: one warp per token t (routed_token_of), lane L the
+            // experts i * 32 + L.  An expert's sort key is
+            // logit_key(logit) << 32 | ~id: larger is better, equal logits go
+            // to the lower id, all keys differ.
             const int t = tok;
             const unsigned ltag = s_tag + (unsigned)d.debug_stall;
             int lpass = 0;
