@@ -22,7 +22,7 @@
 //               up to 16, K=16) into a TMEM accumulator and commits them to
 //               the stage's "empty" mbarrier; after the last chunk a commit
 //               to the accumulator barrier.
-// Three stages ring between producers and the MMA issuer.  Warps 0-7 then
+// Four stages ring between producers and the MMA issuer.  Warps 0-7 then
 // read the accumulator (tcgen05.ld, warp w owns TMEM lanes 32(w%4).. and
 // half of the columns) and run the epilogue:
 //   gate/up  rows 16j+r (r < 8) are gate, 16j+r+8 the matching up rows
@@ -48,7 +48,8 @@ constexpr int kStgW = 4;                          // B staging warps
 constexpr int kMmaW = kDecW + kStgW;              // MMA-issuing warp
 constexpr int kGW = kMmaW + 1;
 constexpr int kGT = 32 * kGW;
-constexpr int kNS = 3;                            // pipeline stages
+constexpr int kNS = 4;                            // pipeline stages
+constexpr int kLA = 4;                            // B-operand chunks in flight (raw copies)
 constexpr int kMT = 128;                          // weight rows per item (8 tiles)
 constexpr int kNmax = kMaxTokens;                 // tokens per slot
 constexpr uint32_t kLBO = 128;                    // K-adjacent core matrices
@@ -59,7 +60,10 @@ constexpr int kScratch = kMaxTokens * (kMaxTopK + kMaxShared) * 8;   // combine'
 constexpr int kCHA = 4;                           // chunks per raw-weight segment
 constexpr int kRWA = 4;                           // raw-weight segments per decode warp
 constexpr int kRawOff = kNS * (kAStage + kBStage) + kScratch;
-constexpr int kSmem = kRawOff + kDecW * kRWA * kCHA * kChunkBytes;
+constexpr int kBRawOff = kRawOff + kDecW * kRWA * kCHA * kChunkBytes;
+constexpr int kBRawStage = kNmax * kChunkK * 2;   // one chunk of the slot's token rows, as stored (8 KB)
+constexpr int kSmem = kBRawOff + kLA * kBRawStage;
+static_assert((kLA & (kLA - 1)) == 0, "kLA is a power of two");
 constexpr int kMaxItems = 128;                    // work items per block
 constexpr uint32_t kTmemCols = 64;                // >= N, a power of two >= 32
 constexpr unsigned long long kWaitNs = 1000000000ull;
@@ -81,6 +85,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 __device__ __forceinline__ uint32_t instr_desc(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// 16-byte asynchronous copy global -> shared (L2 only), and its groups.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(b)) : "memory");
@@ -255,6 +268,24 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
             gs1 = 0.f;
         }
 
+        // The epilogue's per-column factor, loaded now so that its round trip
+        // overlaps the main loop: lane i of a decode warp holds the one of
+        // column 32 * half + i (gate/up: 2^xexp of the column's token; down:
+        // 2^hexp of the pair).  The router's tables, x's exponents and h's
+        // maxima are all final when this kernel starts.
+        float col_un = 0.f;
+        if (warp < kDecW) {
+            const int col = 32 * (warp >> 2) + lane;
+            if (col < m) {
+                if (MODE == 0) {
+                    const int tok = shared ? col : __ldcg(d.pair_tok + p0 + col);
+                    col_un = pow2f(__ldcg(d.xexp + tok));
+                } else {
+                    col_un = pow2f(hexp_of(__ldcg(d.hmax + p0 + col)));
+                }
+            }
+        }
+
         if (warp < kDecW) {
             // ---- A producer: tile 8mt + warp, from the raw ring ----
             int oc = 0, cseg = 0;
@@ -284,6 +315,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                 }
                 __syncwarp();
                 if (go && lane == 0) mbar_arrive(&s_full[st]);
+                if (li == 0 && c == 0) MOE_TRACE_POINT(3 + MODE, 3);
                 if (++oc == min(kCHA, NC - cseg)) {
                     cseg += oc;
                     oc = 0;
@@ -292,8 +324,11 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                 }
             }
         } else if (warp < kMmaW) {
-            // ---- B producer: the slot's m tokens (rows >= m zero), one
-            // chunk of loads ahead ----
+            // ---- B producer: the slot's m tokens (rows >= m zero).  Each
+            // thread copies its own pieces of chunk c + kLA - 1 ahead
+            // (cp.async into a raw ring; a thread reads back only what it
+            // copied itself, so its own group waits order it) and converts
+            // chunk c into the stage ----
             const int tb = threadIdx.x - 32 * kDecW;      // 0..127
             const int kg = tb & 7;                        // K group of this thread's pieces
             const uint4 *src[4];
@@ -314,16 +349,26 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     }
                 }
             }
-            uint4 v[4];
+            uint8_t *braw = smem + kBRawOff + kg * 16;
+            // one commit group per chunk index (empty past the end), so that
+            // "chunk c landed" is always "at most kLA - 1 groups pending"
+            auto bissue = [&](int c) {
+                if (c < NC) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = src[u] ? __ldcg(src[u] + kg) : make_uint4(0u, 0u, 0u, 0u);
+                    for (int u = 0; u < 4; ++u) {
+                        const int n = (tb >> 3) + 16 * u;
+                        if (src[u])
+                            cp_async16(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128, src[u] + c * 8 + kg);
+                    }
+                }
+                cp_async_commit();
+            };
+#pragma unroll
+            for (int j = 0; j < kLA; ++j) bissue(j);
 #pragma unroll 1
             for (int c = 0; c < NC; ++c) {
                 const int gcc = gc + c, st = gcc % kNS;
-                uint4 vn[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    vn[u] = (src[u] && c + 1 < NC) ? __ldcg(src[u] + (c + 1) * 8 + kg) : make_uint4(0u, 0u, 0u, 0u);
+                cp_async_wait<kLA - 1>();
                 const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
                 if (go) {
                     uint8_t *Bs = sB + (size_t)st * kBStage;
@@ -331,13 +376,16 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     for (int u = 0; u < 4; ++u) {
                         const int n = (tb >> 3) + 16 * u;
                         if (n < N) {
-                            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                            uint4 o;
-                            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+                            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                            if (src[u]) {
+                                const uint4 v = lds128(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128);
+                                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                                uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
-                                                   __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
+                                for (int i = 0; i < 4; ++i)
+                                    ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
+                                                       __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
+                            }
                             *reinterpret_cast<uint4 *>(Bs + (n >> 3) * kSBO + kg * kLBO + (n & 7) * 16) = o;
                         }
                     }
@@ -345,9 +393,10 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                 }
                 __syncwarp();
                 if (go && lane == 0) mbar_arrive(&s_full[st]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = vn[u];
+                if (li == 0 && c == 0) MOE_TRACE_POINT_AT(3 + MODE, 6, 32 * kDecW);
+                bissue(c + kLA);
             }
+            if (li == 0) MOE_TRACE_POINT_AT(3 + MODE, 7, 32 * kDecW);
         } else if (lane == 0) {
             // ---- MMA issuer ----
             const uint32_t idesc = instr_desc(kMT, N);
@@ -361,6 +410,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     break;
                 }
                 tc_fence_after();
+                if (li == 0 && c == 0) MOE_TRACE_POINT_AT(3 + MODE, 4, 32 * kMmaW);
                 const uint32_t a0 = smem_u32(sA + (size_t)st * kAStage), b0 = smem_u32(sB + (size_t)st * kBStage);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
@@ -380,6 +430,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
                                  smem_u32(&s_accf))
                              : "memory");
+            if (li == 0) MOE_TRACE_POINT_AT(3 + MODE, 5, 32 * kMmaW);
         }
         gc += NC;
         if (li == 0) MOE_TRACE_POINT(3 + MODE, 2);
@@ -388,6 +439,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
         if (warp < kDecW) {
             const bool ok = gwait(&s_accf, (unsigned)li & 1u, abort, d.err);
             tc_fence_after();
+            if (li == 0) MOE_TRACE_POINT(3 + MODE, 10);
             const int qd = warp & 3, half = warp >> 2;
             float v[32];
             if (ok) {
@@ -416,11 +468,10 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     for (int i = 0; i < 32; ++i) {
                         const int col = 32 * half + i;
                         const float up = __shfl_down_sync(0xffffffffu, v[i], 8);
+                        const float un = __shfl_sync(0xffffffffu, col_un, i);
                         float habs = 0.f;
                         if (col < m && rr < 8) {
                             const int p = p0 + col;
-                            const int tok = shared ? col : __ldcg(d.pair_tok + p);
-                            const float un = pow2f(__ldcg(d.xexp + tok));
                             const float gt = v[i] * gs0 * un, uv = up * gs1 * un;
                             const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * uv);
                             d.h_ws[(size_t)p * d.Imax + n_int] = hb;
@@ -436,10 +487,8 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int col = 32 * half + i;
-                        if (col < m) {
-                            const int p = p0 + col;
-                            d.y_ws[(size_t)p * d.H + orow] = v[i] * gs0 * pow2f(hexp_of(__ldcg(d.hmax + p)));
-                        }
+                        const float un = __shfl_sync(0xffffffffu, col_un, i);
+                        if (col < m) d.y_ws[(size_t)(p0 + col) * d.H + orow] = v[i] * gs0 * un;
                     }
                 }
             }
@@ -463,9 +512,11 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
         }
     }
     MOE_TRACE_POINT(3 + MODE, 8);
+    MOE_TRACE_VALUE(3 + MODE, 12, nmy);
     // the issuer's last commit covers all of its MMAs: wait for it before
     // the columns are released; decode warps wait for raw copies never used
     if (warp == kMmaW && lane == 0 && nmy > 0 && !*abort) gwait(&s_accf, (unsigned)(nmy - 1) & 1u, abort, d.err);
+    if (warp >= kDecW && warp < kMmaW) cp_async_wait_all();   // B copies (all landed or empty)
     if (warp < kDecW && lane == 0) {
         for (int j = n_done; j < n_iss; ++j) {
             const unsigned long long t0 = gtimer();

@@ -111,17 +111,25 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int i = base + u * kThreads;
-                if (i < n16) {
-                    dst[i] = v[u];
-                    if (blockIdx.x == 0) {
-                        // per-token max |x| for the GEMVs' power-of-two prescale
-                        float m = 0.f;
+                if (i < n16) dst[i] = v[u];
+                if (blockIdx.x == 0) {
+                    // per-token max |x| for the GEMVs' power-of-two prescale
+                    // (non-negative, so its bits order as unsigned integers)
+                    float m = 0.f;
+                    if (i < n16) {
                         const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
                                                fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
-                        atomicMax(reinterpret_cast<int *>(&s_rmax[i / r16]), __float_as_int(m));
+                    }
+                    if ((r16 & 31) == 0) {
+                        // a warp's 32 pieces are one token's (and all in
+                        // range or all out): one shared atomic per warp
+                        const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+                        if (lane == 0 && i < n16) atomicMax(reinterpret_cast<unsigned *>(&s_rmax[i / r16]), mw);
+                    } else if (i < n16) {
+                        atomicMax(reinterpret_cast<unsigned *>(&s_rmax[i / r16]), __float_as_uint(m));
                     }
                 }
             }
