@@ -329,13 +329,17 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
             // (cp.async into a raw ring; a thread reads back only what it
             // copied itself, so its own group waits order it) and converts
             // chunk c into the stage ----
+            // Thread tb takes K group kg of tokens nlo + 8 * nhi + 16 * u: the
+            // eight lanes of a quarter warp (one 16-byte store phase) write
+            // eight different token rows of one core matrix, so their
+            // stores hit eight different bank groups.
             const int tb = threadIdx.x - 32 * kDecW;      // 0..127
-            const int kg = tb & 7;                        // K group of this thread's pieces
+            const int nlo = tb & 7, kg = (tb >> 3) & 7, nhi = tb >> 6;
             const uint4 *src[4];
             float sc[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int n = (tb >> 3) + 16 * u;
+                const int n = nlo + 8 * nhi + 16 * u;
                 src[u] = nullptr;
                 sc[u] = 0.f;
                 if (n < m) {
@@ -349,14 +353,17 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     }
                 }
             }
-            uint8_t *braw = smem + kBRawOff + kg * 16;
+            // raw ring: token row n of a chunk is 128 bytes, its K groups
+            // XOR-swizzled by n % 8 (= nlo) so that a quarter warp's pieces
+            // fall in different bank groups here too
+            uint8_t *braw = smem + kBRawOff + ((kg ^ nlo) << 4);
             // one commit group per chunk index (empty past the end), so that
             // "chunk c landed" is always "at most kLA - 1 groups pending"
             auto bissue = [&](int c) {
                 if (c < NC) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int n = (tb >> 3) + 16 * u;
+                        const int n = nlo + 8 * nhi + 16 * u;
                         if (src[u])
                             cp_async16(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128, src[u] + c * 8 + kg);
                     }
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     uint8_t *Bs = sB + (size_t)st * kBStage;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int n = (tb >> 3) + 16 * u;
+                        const int n = nlo + 8 * nhi + 16 * u;
                         if (n < N) {
                             uint4 o = make_uint4(0u, 0u, 0u, 0u);
                             if (src[u]) {
