@@ -28,6 +28,8 @@
 //     experts first, then routed experts in ascending id), numbers the
 //     (expert, token) pairs so that each expert's pairs are contiguous, lists
 //     the slots with many tokens for the grouped kernels, and clears the masks.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -49,12 +51,12 @@ __device__ __forceinline__ void bf16x4_to_f(uint2 v, float &a, float &b, float &
 // Top-k of one token's FP32 logits (lane L holds experts i * 32 + L, i < M)
 // by sort keys; lane j < k returns the j-th choice.
 template <int M>
-__device__ __forceinline__ unsigned long long token_topk(const float *z, int E, int K, int lane) {
+__device__ __forceinline__ unsigned long long token_topk(const float *z, bool in_smem, int E, int K, int lane) {
     unsigned long long c[M];
 #pragma unroll
     for (int i = 0; i < M; ++i) {
         const int e = i * 32 + lane;
-        c[i] = e < E ? ((unsigned long long)logit_key(__ldcg(z + e)) << 32) | (unsigned)~e : 0ull;
+        c[i] = e < E ? ((unsigned long long)logit_key(in_smem ? z[e] : __ldcg(z + e)) << 32) | (unsigned)~e : 0ull;
     }
     return warp_topk<M>(c, K, lane);
 }
@@ -94,11 +96,13 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     // loads, all in flight) ----
     __shared__ float s_rmax[kTokGroup];
     if (threadIdx.x < kTokGroup) s_rmax[threadIdx.x] = 0.f;
-    const uint2 *xs = reinterpret_cast<const uint2 *>(smem);     // [nt][Hk/4] groups of 4 bf16
+    // x columns as FP32 (exact), so that the dot products below read them
+    // with one 16-byte load per four elements and no unpacking
+    const float4 *xs = reinterpret_cast<const float4 *>(smem);   // [nt][Hk/4]
     {
         const int r16 = Hk / 8, n16 = nt * r16;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t0 * H + k0);
-        uint4 *dst = reinterpret_cast<uint4 *>(smem);
+        float4 *dst = reinterpret_cast<float4 *>(smem);
         __syncthreads();
 #pragma unroll 1
         for (int base = threadIdx.x; base < n16; base += 8 * kThreads) {
@@ -111,7 +115,13 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int i = base + u * kThreads;
-                if (i < n16) dst[i] = v[u];
+                if (i < n16) {
+                    float a0, a1, a2, a3, b0, b1, b2, b3;
+                    bf16x4_to_f(make_uint2(v[u].x, v[u].y), a0, a1, a2, a3);
+                    bf16x4_to_f(make_uint2(v[u].z, v[u].w), b0, b1, b2, b3);
+                    dst[2 * i] = make_float4(a0, a1, a2, a3);
+                    dst[2 * i + 1] = make_float4(b0, b1, b2, b3);
+                }
                 if (blockIdx.x == 0) {
                     // per-token max |x| for the GEMVs' power-of-two prescale
                     // (non-negative, so its bits order as unsigned integers)
@@ -153,9 +163,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 #pragma unroll
                 for (int t = 0; t < kTokGroup; ++t) {
                     if (t < nt) {
-                        float x0, x1, x2, x3;
-                        bf16x4_to_f(xs[t * nvec + v], x0, x1, x2, x3);
-                        acc[t] = fmaf(x3, pre[j].w, fmaf(x2, pre[j].z, fmaf(x1, pre[j].y, fmaf(x0, pre[j].x, acc[t]))));
+                        const float4 xv = xs[t * nvec + v];
+                        acc[t] = fmaf(xv.w, pre[j].w, fmaf(xv.z, pre[j].z, fmaf(xv.y, pre[j].y, fmaf(xv.x, pre[j].x, acc[t]))));
                     }
                 }
             }
@@ -174,9 +183,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 #pragma unroll
                     for (int t = 0; t < kTokGroup; ++t) {
                         if (t < nt) {
-                            float x0, x1, x2, x3;
-                            bf16x4_to_f(xs[t * nvec + v], x0, x1, x2, x3);
-                            acc[t] = fmaf(x3, w[u].w, fmaf(x2, w[u].z, fmaf(x1, w[u].y, fmaf(x0, w[u].x, acc[t]))));
+                            const float4 xv = xs[t * nvec + v];
+                            acc[t] = fmaf(xv.w, w[u].w, fmaf(xv.z, w[u].z, fmaf(xv.y, w[u].y, fmaf(xv.x, w[u].x, acc[t]))));
                         }
                     }
                 }
@@ -196,6 +204,9 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 
     // ---- the last expert group of this token group: top-k of its tokens ----
     __shared__ int s_last;
+    __shared__ int s_ids[kMaxTokens][kMaxTopK];
+    __shared__ float s_w[kMaxTokens][kMaxTopK];
+    __shared__ unsigned long long s_mask[kMaxExperts];
     __syncthreads();
     MOE_TRACE_POINT(0, 3);
     if (threadIdx.x == 0) {
@@ -205,28 +216,46 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    // With one token group this block is also the last one overall: the
+    // choices and the expert masks stay in shared memory (no second ticket).
+    const bool one = gridDim.y == 1;
+    if (one)
+        for (int i = threadIdx.x; i < E; i += kThreads) s_mask[i] = 0ull;
+    float *s_lg = reinterpret_cast<float *>(smem);   // [nt][E]: x is no longer read
     if (KH > 1) {
-        // the token group's logits: the K ranges' sums in a fixed order
+        // the token group's logits: the K ranges' sums in a fixed order, the
+        // partial loads of an element in flight together; kept in shared
+        // memory for the top-k below
         for (int i = threadIdx.x; i < nt * E; i += kThreads) {
             const int t = i / E, ee = i - t * E;
+            float part[kMaxKSplit];
+#pragma unroll
+            for (int z = 0; z < kMaxKSplit; ++z)
+                part[z] = z < KH ? __ldcg(d.lpart + ((size_t)z * d.max_tokens + t0 + t) * E + ee) : 0.f;
             float v = 0.f;
-            for (int z = 0; z < KH; ++z) v += __ldcg(d.lpart + ((size_t)z * d.max_tokens + t0 + t) * E + ee);
-            d.logits[(size_t)(t0 + t) * E + ee] = v + (d.router_b ? d.router_b[ee] : 0.f);
+#pragma unroll
+            for (int z = 0; z < kMaxKSplit; ++z)
+                if (z < KH) v += part[z];
+            v += d.router_b ? d.router_b[ee] : 0.f;
+            s_lg[i] = v;
+            d.logits[(size_t)(t0 + t) * E + ee] = v;
         }
-        __syncthreads();
     }
+    __syncthreads();
     MOE_TRACE_POINT(0, 4);
     if (warp < nt) {
         // sort keys logit_key(logit) << 32 | ~id: larger is better, equal
         // logits go to the lower id; lane j < k ends with the j-th choice
         const int t = t0 + warp;
+        const bool lsm = KH > 1;
+        const float *zt = lsm ? s_lg + (size_t)warp * E : d.logits + (size_t)t * E;
         unsigned long long sel;
         switch (d.E <= 32 ? 1 : d.E <= 64 ? 2 : d.E <= 128 ? 4 : d.E <= 256 ? 8 : 16) {
-            case 1: sel = token_topk<1>(d.logits + (size_t)t * E, E, K, lane); break;
-            case 2: sel = token_topk<2>(d.logits + (size_t)t * E, E, K, lane); break;
-            case 4: sel = token_topk<4>(d.logits + (size_t)t * E, E, K, lane); break;
-            case 8: sel = token_topk<8>(d.logits + (size_t)t * E, E, K, lane); break;
-            default: sel = token_topk<16>(d.logits + (size_t)t * E, E, K, lane); break;
+            case 1: sel = token_topk<1>(zt, lsm, E, K, lane); break;
+            case 2: sel = token_topk<2>(zt, lsm, E, K, lane); break;
+            case 4: sel = token_topk<4>(zt, lsm, E, K, lane); break;
+            case 8: sel = token_topk<8>(zt, lsm, E, K, lane); break;
+            default: sel = token_topk<16>(zt, lsm, E, K, lane); break;
         }
         const unsigned sel_key = (unsigned)(sel >> 32);
         const int sel_e = (int)~(unsigned)sel;
@@ -240,34 +269,43 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             d.wsel[(size_t)t * K + lane] = w;
             if (ids_out) ids_out[(size_t)t * K + lane] = sel_e;
             if (w_out) w_out[(size_t)t * K + lane] = w;
-            atomicOr(d.emask + sel_e, 1ull << t);
+            if (one) {
+                s_ids[t][lane] = sel_e;
+                s_w[t][lane] = w;
+                atomicOr(s_mask + sel_e, 1ull << t);
+            } else {
+                atomicOr(d.emask + sel_e, 1ull << t);
+            }
         }
     }
     // ---- the last token group: slots, pairs, hot list ----
     __syncthreads();
-    if (threadIdx.x == 0) {
-        d.tg_ticket[blockIdx.y] = 0u;
+    if (!one) {
+        if (threadIdx.x == 0) {
+            d.tg_ticket[blockIdx.y] = 0u;
+            __threadfence();
+            s_last = atomicAdd(d.ticket, 1u) == gridDim.y - 1;
+        }
+        __syncthreads();
+        if (!s_last) return;
         __threadfence();
-        s_last = atomicAdd(d.ticket, 1u) == gridDim.y - 1;
+    } else if (threadIdx.x == 0) {
+        d.tg_ticket[0] = 0u;
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
     MOE_TRACE_POINT(0, 5);
 
-    __shared__ int s_ids[kMaxTokens][kMaxTopK];
-    __shared__ float s_w[kMaxTokens][kMaxTopK];
-    __shared__ unsigned long long s_mask[kMaxExperts];
     __shared__ int s_pbase[kMaxExperts];
     __shared__ int s_wsum_f[kRouteWarps], s_wsum_c[kRouteWarps];
     __shared__ short s_slotm[kMaxTokens * kMaxTopK + kMaxShared];   // tokens per slot
-    for (int i = threadIdx.x; i < E; i += kThreads) {
-        s_mask[i] = __ldcg(d.emask + i);
-        d.emask[i] = 0ull;
-    }
-    for (int i = threadIdx.x; i < T * K; i += kThreads) {
-        s_ids[i / K][i % K] = __ldcg(d.ids + i);
-        s_w[i / K][i % K] = __ldcg(d.wsel + i);
+    if (!one) {
+        for (int i = threadIdx.x; i < E; i += kThreads) {
+            s_mask[i] = __ldcg(d.emask + i);
+            d.emask[i] = 0ull;
+        }
+        for (int i = threadIdx.x; i < T * K; i += kThreads) {
+            s_ids[i / K][i % K] = __ldcg(d.ids + i);
+            s_w[i / K][i % K] = __ldcg(d.wsel + i);
+        }
     }
     // the tokens' power-of-two prescales from their whole-row maxima
     for (int t = threadIdx.x; t < T; t += kThreads) {
@@ -385,13 +423,14 @@ int route_ksplit(const DevLayer &d, int T, int sm_count) {
 }
 
 size_t route_smem_bytes(const DevLayer &d, int T, int kh, int *tg_out) {
-    // activation columns of one token group (at most 8 tokens, at most 96 KB)
+    // activation columns of one token group as FP32 (at most 8 tokens, at
+    // most 96 KB), later the group's logits
     const int Hk = d.H / kh;
     int tg = kTokGroup;
-    while (tg > 1 && (size_t)tg * Hk * 2 > 96 * 1024) --tg;
+    while (tg > 1 && (size_t)tg * Hk * 4 > 96 * 1024) --tg;
     if (tg > T) tg = T;
     if (tg_out) *tg_out = tg;
-    return (size_t)tg * Hk * 2;
+    return (size_t)tg * (size_t)std::max(Hk, d.E) * 4;
 }
 
 cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out, float *w_out,
