@@ -469,25 +469,36 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
             if (ok && 32 * half < N) {
                 const int row = 32 * qd + lane;            // row of the M-tile
                 if (MODE == 0) {
+                    // Two columns per step: lanes rr < 8 hold gate rows and
+                    // take column i (up from lane + 8), lanes rr >= 8 hold the
+                    // matching up rows and take column i + 1 (gate from
+                    // lane - 8), so every lane evaluates one SwiGLU.
                     const int j = row >> 4, rr = row & 15;
+                    const bool hi = rr >= 8;
                     const int n_int = 8 * (8 * mt + j) + (rr & 7);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = 32 * half + i;
-                        const float up = __shfl_down_sync(0xffffffffu, v[i], 8);
-                        const float un = __shfl_sync(0xffffffffu, col_un, i);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float from_hi = __shfl_down_sync(0xffffffffu, v[i], 8);
+                        const float from_lo = __shfl_up_sync(0xffffffffu, v[i + 1], 8);
+                        const float graw = hi ? from_lo : v[i], uraw = hi ? v[i + 1] : from_hi;
+                        const int ci = i + (hi ? 1 : 0);
+                        const int col = 32 * half + ci;
+                        const float un = __shfl_sync(0xffffffffu, col_un, ci);
                         float habs = 0.f;
-                        if (col < m && rr < 8) {
+                        if (col < m) {
                             const int p = p0 + col;
-                            const float gt = v[i] * gs0 * un, uv = up * gs1 * un;
+                            const float gt = graw * gs0 * un, uv = uraw * gs1 * un;
                             const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * uv);
                             d.h_ws[(size_t)p * d.Imax + n_int] = hb;
                             habs = fabsf(__bfloat162float(hb));
                         }
+                        // max over the 16 rows of each column: lanes 0-7 and
+                        // 16-23 hold column i, lanes 8-15 and 24-31 column i + 1
                         habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, 1));
                         habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, 2));
                         habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, 4));
-                        if (col < m && (lane & 15) == 0) atomicMax(d.hmax + p0 + col, __float_as_uint(habs));
+                        habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, 16));
+                        if (col < m && (lane & 23) == 0) atomicMax(d.hmax + p0 + col, __float_as_uint(habs));
                     }
                 } else {
                     const int orow = kMT * mt + row;
