@@ -73,6 +73,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grouped-min", type=int, default=0,
                     help="grouped_min_tokens of the layers (0: library default, -1: GEMV kernels only)")
+    ap.add_argument("--score-func", default="sigmoid", choices=["sigmoid", "softmax"],
+                    help="routing score of the measured workload's layers (softmax: the chain)")
     return ap.parse_args()
 
 
@@ -265,8 +267,8 @@ def run_reference(args):
 class Chain:
     """L distinct layers of one workload on the current GPU."""
 
-    def __init__(self, moe, torch, gen, ci, L, seed0, grouped_min=0):
-        self.c = gen.config(ci)
+    def __init__(self, moe, torch, gen, ci, L, seed0, grouped_min=0, score_func="sigmoid"):
+        self.c = gen.config(ci, score_func=score_func)
         c = self.c
         self.T, self.L = c["T"], L
         self.layers, self.xs, self.outs, self.ids, self.ws = [], [], [], [], []
@@ -368,7 +370,7 @@ def run_gpu(args):
     ci, L = WORKLOADS[args.workload]
     L = args.layers or L
     seed0 = gen.BASE_SEED + 1000 * (rank + 1) + 100 * ci
-    chain = Chain(moe, torch, gen, ci, L, seed0, args.grouped_min)
+    chain = Chain(moe, torch, gen, ci, L, seed0, args.grouped_min, args.score_func)
     c = chain.c
     stream = torch.cuda.Stream()
 
@@ -479,7 +481,8 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "w4a16(e2m1*e4m3 x bf16->f16 mma, fp32 acc)",
             "data": "synthetic",
             "config": {"workload": f"{c['name']}: T={c['T']} H={c['H']} E={c['E']} top-{c['k']} "
-                                   f"I={c['I']} +{c['S']} shared",
+                                   f"I={c['I']} +{c['S']} shared"
+                                   + ("" if args.score_func == "sigmoid" else f", {args.score_func} routing"),
                        "layers_per_step": L, "tokens_per_layer": c["T"],
                        "l2": f"inputs larger than L2: {L} distinct layers, "
                              f"{bytes_step / 1e6:.0f} MB selected bytes per step",

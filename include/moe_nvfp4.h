@@ -68,7 +68,8 @@ typedef enum {
  *   inter % 64 == 0 and shared_inter % 64 == 0 (when num_shared > 0), <= 16384
  *   1 <= top_k <= 8, top_k <= num_experts <= 512
  *   0 <= num_shared <= 2
- *   1 <= max_tokens <= 64                                                     */
+ *   1 <= max_tokens <= 64
+ *   normalize_topk in {0, 1}, score_func in {0, 1}, routed_scale finite      */
 typedef struct {
     int hidden;             /* H */
     int num_experts;        /* E routed experts */
@@ -87,6 +88,17 @@ typedef struct {
                                H <= 4096, E <= 2 x SM count, activations fit
                                in shared memory); < 0: always the three-kernel
                                chain of the moe_stage_* entry points */
+    int score_func;         /* routing score: 0 = sigmoid of each logit (Flint
+                               page, "Flint model architecture"); 1 = softmax
+                               over all experts' logits (Mistral Large 4 page,
+                               "Specialized decode": its softmax top-4 router).
+                               The top-k is the same for both (both scores
+                               increase with the logit); the weights are the
+                               chosen experts' scores, normalised to sum to 1
+                               when normalize_topk = 1 (for softmax:
+                               exp(z_j - z_max) / sum over the chosen of
+                               exp(z_i - z_max)), times routed_scale.  Softmax
+                               layers always run the three-kernel chain. */
 } moe_config;
 
 /* Weights in the canonical layout (device pointers, only read during

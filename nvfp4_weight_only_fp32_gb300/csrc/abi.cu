@@ -82,6 +82,7 @@ std::vector<std::string> unsupported_reasons(const moe_config *c) {
     chk(c->max_tokens >= 1 && c->max_tokens <= kMaxTokens, "max_tokens must be in [1, 64]");
     chk(c->normalize_topk == 0 || c->normalize_topk == 1, "normalize_topk must be 0 or 1");
     chk(std::isfinite(c->routed_scale), "routed_scale must be finite");
+    chk(c->score_func == 0 || c->score_func == 1, "score_func must be 0 (sigmoid) or 1 (softmax)");
     return why;
 }
 
@@ -261,6 +262,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     d.Is = Is;
     d.normalize = cfg->normalize_topk;
     d.routed_scale = cfg->routed_scale;
+    d.score_func = cfg->score_func;
     d.max_tokens = cfg->max_tokens;
     d.max_slots = std::min(E, cfg->max_tokens * K) + S;
     d.max_pairs = cfg->max_tokens * (K + S);
@@ -330,7 +332,8 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     if (L->cfg.grouped_min_tokens > 0 && grouped_supported(d, L->sm_count)) d.grouped_min = L->cfg.grouped_min_tokens;
     for (int T = 0; T <= kMaxTokens; ++T) {
         L->fused_ok[T] = 0;
-        if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&
+        // the single launch implements sigmoid routing only
+        if (e == cudaSuccess && cfg->fused >= 0 && cfg->score_func == 0 && T >= 1 && T <= cfg->max_tokens &&
             fused_eligible(d, T, L->sm_count, (size_t)L->optin_smem))
             L->fused_ok[T] = fused_blocks_per_sm(d, T) >= 1;
     }

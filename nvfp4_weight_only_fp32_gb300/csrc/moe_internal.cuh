@@ -106,6 +106,7 @@ struct DevLayer {
     unsigned long long *emask;      // [E] router: tokens that selected each expert (bit t)
     unsigned long long *trace;      // traced build only: phase timestamps
     int trace_blocks;
+    int score_func;                 // 0 sigmoid per expert, 1 softmax over all experts
 };
 
 // ---------------------------------------------------------------------------
@@ -347,6 +348,12 @@ __device__ __forceinline__ unsigned logit_key(float z) {
     unsigned u = __float_as_uint(z);
     if (u == 0x80000000u) u = 0u;
     return isnan(z) ? 0u : (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The FP32 logit a key encodes (NaN for key 0).
+__device__ __forceinline__ float key_logit(unsigned key) {
+    const float z = __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+    return key ? z : __int_as_float(0x7fc00000);
 }
 
 // The weight of a chosen expert: the sigmoid of the logit its key encodes

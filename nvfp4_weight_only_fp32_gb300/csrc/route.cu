@@ -1,11 +1,13 @@
-// route.cu -- rows a1 + a2: FP32 router GEMV, sigmoid, top-k with
-// lowest-index tie-break, weight normalisation, and the work list of the
-// distinct selected experts (the three-kernel chain; the single launch has its
-// own copy of these steps).
+// route.cu -- rows a1 + a2: FP32 router GEMV, sigmoid (or softmax) scores,
+// top-k with lowest-index tie-break, weight normalisation, and the work list of
+// the distinct selected experts (the three-kernel chain; the single launch has
+// its own copy of these steps, sigmoid only).
 //
 // Sources: "Inkling 2 Small on vLLM: Day-0 Support", "Accuracy evaluation"
 // (the router runs in FP32); "Day 0 support for Mistral Large 4 on vLLM",
 // "Breakable CUDA graphs and fusions" (FP32 routing GEMM);
+// "Day 0 support for Mistral Large 4 on vLLM", "Specialized decode" (its
+// fused layer runs a softmax top-4 router);
 // "vLLM Day-0 support for Recursive's Flint", "Flint model architecture"
 // (sigmoid top-6 over 256 experts plus one shared expert) and "Optimisation
 // strategy" (the expert GEMVs read only the selected experts, which is what the
@@ -59,6 +61,17 @@ __device__ __forceinline__ unsigned long long token_topk(const float *z, bool in
         c[i] = e < E ? ((unsigned long long)logit_key(in_smem ? z[e] : __ldcg(z + e)) << 32) | (unsigned)~e : 0ull;
     }
     return warp_topk<M>(c, K, lane);
+}
+
+// Softmax denominator of one token relative to its largest logit z0: the sum
+// over all experts of exp(z_e - z0), lane-strided, then across the warp; every
+// lane gets lane 0's total.
+__device__ __forceinline__ float softmax_den(const float *z, bool in_smem, int E, float z0, int lane) {
+    float acc = 0.f;
+    for (int e = lane; e < E; e += 32) acc += expf((in_smem ? z[e] : __ldcg(z + e)) - z0);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    return __shfl_sync(0xffffffffu, acc, 0);
 }
 
 __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
@@ -259,12 +272,20 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         }
         const unsigned sel_key = (unsigned)(sel >> 32);
         const int sel_e = (int)~(unsigned)sel;
-        // weights: normalised over the k selected scores (summed in selection order)
-        const float sel_s = key_score(sel_key);
+        // the choices' scores: the sigmoid of the logit, or (softmax routing)
+        // its exponential relative to the largest logit, lane 0's choice
+        const bool smax = d.score_func == 1;
+        const float zsel = key_logit(sel_key);
+        const float z0 = __shfl_sync(0xffffffffu, zsel, 0);
+        const float sel_s = smax ? expf(zsel - z0) : key_score(sel_key);
+        // weights: normalised over the k selected scores (summed in selection
+        // order); softmax scores without normalisation are divided by the sum
+        // over all experts
         float sum = 0.f;
         for (int j = 0; j < K; ++j) sum += __shfl_sync(0xffffffffu, sel_s, j);
+        const float den = smax && !d.normalize ? softmax_den(zt, lsm, E, z0, lane) : 1.f;
         if (lane < K) {
-            const float w = (d.normalize ? sel_s / sum : sel_s) * d.routed_scale;
+            const float w = (d.normalize ? sel_s / sum : sel_s / den) * d.routed_scale;
             d.ids[(size_t)t * K + lane] = sel_e;
             d.wsel[(size_t)t * K + lane] = w;
             if (ids_out) ids_out[(size_t)t * K + lane] = sel_e;

@@ -39,7 +39,9 @@ class moe_config(ctypes.Structure):
                 ("inter", ctypes.c_int), ("num_shared", ctypes.c_int), ("shared_inter", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("normalize_topk", ctypes.c_int),
                 ("routed_scale", ctypes.c_float), ("grouped_min_tokens", ctypes.c_int),
-                ("fused", ctypes.c_int)]
+                ("fused", ctypes.c_int), ("score_func", ctypes.c_int)]
+
+SCORE_FUNCS = {"sigmoid": 0, "softmax": 1}
 
 
 class moe_weights(ctypes.Structure):
@@ -225,7 +227,8 @@ def make_config(c: dict, max_tokens: int | None = None, grouped_min_tokens: int 
                       max_tokens=int(max_tokens if max_tokens else c["T"]),
                       normalize_topk=int(c.get("normalize", 1)),
                       routed_scale=float(c.get("routed_scale", 1.0)),
-                      grouped_min_tokens=int(grouped_min_tokens), fused=int(fused))
+                      grouped_min_tokens=int(grouped_min_tokens), fused=int(fused),
+                      score_func=SCORE_FUNCS[c.get("score_func", "sigmoid")])
 
 
 class MoELayer:

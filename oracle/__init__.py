@@ -49,6 +49,7 @@ class _Layer(ctypes.Structure):
         ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p),
         ("sw13", ctypes.c_void_p), ("sw13_sf", ctypes.c_void_p), ("sw13_gs", ctypes.c_void_p),
         ("sw2", ctypes.c_void_p), ("sw2_sf", ctypes.c_void_p), ("sw2_gs", ctypes.c_void_p),
+        ("score_func", ctypes.c_int),
     ]
 
 
@@ -105,7 +106,16 @@ class _Bound:
         self.s = _Layer(H=c["H"], E=c["E"], k=c["k"], I=c["I"], S=c["S"], Is=c["Is"],
                         normalize=int(c.get("normalize", 1)),
                         routed_scale=float(c.get("routed_scale", 1.0)),
+                        score_func=score_func_code(c),
                         **{n: _ptr(a) for n, a in self.arrs.items()})
+
+
+def score_func_code(c: dict) -> int:
+    """The layer's routing score: "sigmoid" (default) -> 0, "softmax" -> 1."""
+    f = c.get("score_func", "sigmoid")
+    if f not in ("sigmoid", "softmax"):
+        raise ValueError(f"unknown score_func {f!r}")
+    return 1 if f == "softmax" else 0
 
 
 def e2m1(code: int) -> float:

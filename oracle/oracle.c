@@ -26,7 +26,8 @@
  *  [ML4]    "Day 0 support for Mistral Large 4 on vLLM" -- "Highlights" and the
  *           "Model architecture" table (128 routed experts, top-4, one shared
  *           expert), section "Breakable CUDA graphs and fusions" (FP32 routing
- *           GEMM).
+ *           GEMM), section "Specialized decode" (its fused decode layer runs a
+ *           softmax top-4 router).
  *
  * Readings where the pages are silent (the full list is kept in the design
  * notes of the repository):
@@ -44,6 +45,12 @@
  *    router's precision), descending, lowest expert index first on ties
  *    (equal FP32 logits).  The weights use the FP64 scores, normalised to sum
  *    to 1 when asked, then multiplied by the routed scale.
+ *  - Softmax routing (score_func = 1, [ML4] specialized decode): score =
+ *    exp(z_e - z_max) / sum over all experts of exp(z - z_max), in FP64.  It
+ *    increases with the logit too, so the top-k decision is the same as with
+ *    sigmoid; the weights are the chosen experts' softmax scores, normalised
+ *    over the chosen ones when asked (then exp(z_j - z_max) / sum over the
+ *    chosen of exp(z_i - z_max)), times the routed scale.
  *  - Router bias, when present, is added to the logit (plain linear layer).
  *  - Shared experts: ungated, weight 1, same NVFP4 format.
  *  - SwiGLU: h = silu(gate) * up, silu(z) = z / (1 + exp(-z)); h is rounded to
@@ -189,13 +196,14 @@ typedef struct {
     const uint8_t *sw2;         /* [S, H, Is/2] */
     const uint8_t *sw2_sf;      /* [S, H, Is/16] */
     const float *sw2_gs;        /* [S] */
+    int score_func;             /* 0: sigmoid per expert; 1: softmax over all experts */
 } orc_layer;
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 
-/* Router logits and sigmoid scores for one token ([FLINT] architecture: sigmoid
- * scoring; [INK2] accuracy section and [ML4] fusions: FP32 router, whose exact
- * value this is). */
+/* Router logits and scores for one token ([FLINT] architecture: sigmoid
+ * scoring; [ML4] specialized decode: softmax scoring; [INK2] accuracy section
+ * and [ML4] fusions: FP32 router, whose exact value this is). */
 static void token_scores(const orc_layer *L, const uint16_t *xt, double *z, double *s)
 {
     for (int e = 0; e < L->E; ++e) {
@@ -205,6 +213,12 @@ static void token_scores(const orc_layer *L, const uint16_t *xt, double *z, doub
         if (L->router_b) acc += (double)L->router_b[e];
         z[e] = acc;
         s[e] = sigmoid(acc);
+    }
+    if (L->score_func == 1) {
+        double zmax = z[0], den = 0.0;
+        for (int e = 1; e < L->E; ++e) zmax = z[e] > zmax ? z[e] : zmax;
+        for (int e = 0; e < L->E; ++e) den += exp(z[e] - zmax);
+        for (int e = 0; e < L->E; ++e) s[e] = exp(z[e] - zmax) / den;
     }
 }
 

@@ -47,10 +47,11 @@ def test_struct_layout_matches_header(moe, tmp_path):
 #include <stddef.h>
 #include "moe_nvfp4.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_layer_info),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_layer_info),
          offsetof(moe_config, routed_scale), offsetof(moe_config, grouped_min_tokens),
          offsetof(moe_weights, sw2_gs), offsetof(moe_layer_info, sm_count),
-         offsetof(moe_config, fused), offsetof(moe_layer_info, single_launch_max_tokens));
+         offsetof(moe_config, fused), offsetof(moe_layer_info, single_launch_max_tokens),
+         offsetof(moe_config, score_func));
   return 0; }
 ''')
     exe = tmp_path / "layout"
@@ -60,7 +61,7 @@ int main(void) {
             ctypes.sizeof(moe.moe_layer_info), moe.moe_config.routed_scale.offset,
             moe.moe_config.grouped_min_tokens.offset, moe.moe_weights.sw2_gs.offset,
             moe.moe_layer_info.sm_count.offset, moe.moe_config.fused.offset,
-            moe.moe_layer_info.single_launch_max_tokens.offset]
+            moe.moe_layer_info.single_launch_max_tokens.offset, moe.moe_config.score_func.offset]
     assert got == want
 
 
@@ -74,11 +75,11 @@ def _cfg(moe, **kw):
 def test_default_deny_lists_every_reason(moe):
     L = moe.lib()
     h = ctypes.c_void_p()
-    bad = _cfg(moe, hidden=100, inter=0, top_k=9, max_tokens=65, num_shared=3)
+    bad = _cfg(moe, hidden=100, inter=0, top_k=9, max_tokens=65, num_shared=3, score_func=2)
     rc = L.moe_init(ctypes.byref(bad), ctypes.byref(moe.moe_weights()), None, ctypes.byref(h))
     assert rc == moe.moe.MOE_ERR_UNSUPPORTED
     msg = moe.last_error()
-    for frag in ("hidden", "inter", "top_k", "max_tokens", "num_shared"):
+    for frag in ("hidden", "inter", "top_k", "max_tokens", "num_shared", "score_func"):
         assert frag in msg, (frag, msg)
     assert not h.value
 

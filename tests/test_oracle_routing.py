@@ -142,3 +142,77 @@ def test_zipf_workload_popularity(orc):
     m = y > 0
     slope = np.polyfit(np.log(r[m]), np.log(y[m]), 1)[0]
     assert -1.3 < slope < -0.9, slope
+
+
+# ---- softmax routing (Mistral Large 4 page, "Specialized decode": softmax
+# top-4 router), score_func = "softmax" ----
+
+def _softmax_layer(E, H, k, w, b=None, normalize=1, routed_scale=1.0):
+    L = _router_layer(E, H, k, w, b, normalize, routed_scale)
+    L["cfg"]["score_func"] = "softmax"
+    return L
+
+
+def _onehot_x(H):
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x3F80                                   # BF16 1.0
+    return x
+
+
+def test_softmax_two_experts_is_the_logistic_of_the_difference(orc):
+    # softmax over two logits a, b gives 1 / (1 + e^(b - a)) and its complement
+    H = 16
+    for a, b in [(0.5, -1.25), (3.0, 2.75), (-4.0, 1.0)]:
+        w = np.zeros((2, H), np.float32)
+        w[:, 0] = [a, b]
+        ids, wt, s, z = orc.route(_softmax_layer(2, H, 2, w, normalize=0), _onehot_x(H))
+        p0 = 1.0 / (1.0 + math.exp(b - a))
+        assert abs(s[0][0] - p0) <= 1e-15 and abs(s[0][1] - (1.0 - p0)) <= 1e-15
+        hi = 0 if a > b else 1
+        assert ids[0].tolist() == [hi, 1 - hi]
+        assert abs(wt[0][0] - max(p0, 1 - p0)) <= 1e-15
+
+
+def test_softmax_normalised_top2_is_the_logistic_of_the_chosen_gap(orc):
+    # normalised over the chosen two, the weights only see their logit gap
+    E, H, k = 6, 16, 2
+    zs = np.array([0.5, -1.0, 2.0, 0.25, 1.5, -0.75], np.float32)
+    w = np.zeros((E, H), np.float32)
+    w[:, 0] = zs
+    ids, wt, s, z = orc.route(_softmax_layer(E, H, k, w), _onehot_x(H))
+    assert ids[0].tolist() == [2, 4]
+    p = 1.0 / (1.0 + math.exp(float(zs[4]) - float(zs[2])))
+    assert abs(wt[0][0] - p) <= 1e-15 and abs(wt[0][1] - (1.0 - p)) <= 1e-15
+    # unnormalised, all experts chosen: the scores are a distribution
+    ids, wt, s, z = orc.route(_softmax_layer(E, H, E, w, normalize=0, routed_scale=2.0), _onehot_x(H))
+    assert abs(wt[0].sum() - 2.0) <= 1e-14
+    assert np.all(np.diff(wt[0]) <= 0)
+
+
+def test_softmax_is_shift_invariant_and_sigmoid_is_not(orc):
+    rng = np.random.default_rng(5)
+    E, H, k = 12, 64, 3
+    w = (rng.standard_normal((E, H)) / 8).astype(np.float32)
+    x = _bf16(rng.standard_normal((2, H)))
+    shift = np.full(E, 1.5, np.float32)                  # the same bias on every logit
+    for norm in (0, 1):
+        a = orc.route(_softmax_layer(E, H, k, w, normalize=norm), x)
+        b = orc.route(_softmax_layer(E, H, k, w, shift, normalize=norm), x)
+        assert np.array_equal(a[0], b[0])
+        assert np.allclose(a[1], b[1], rtol=1e-12, atol=0)
+    a = orc.route(_router_layer(E, H, k, w, normalize=0), x)
+    b = orc.route(_router_layer(E, H, k, w, shift, normalize=0), x)
+    assert np.array_equal(a[0], b[0]) and not np.allclose(a[1], b[1], rtol=1e-3, atol=0)
+
+
+def test_softmax_selects_what_sigmoid_selects(orc):
+    rng = np.random.default_rng(9)
+    E, H, k = 40, 96, 5
+    for trial in range(10):
+        w = rng.standard_normal((E, H)).astype(np.float32)
+        x = _bf16(rng.standard_normal((3, H)))
+        ids_sig = orc.route(_router_layer(E, H, k, w), x)[0]
+        ids_sm, wt, s, z = orc.route(_softmax_layer(E, H, k, w), x)
+        assert np.array_equal(ids_sig, ids_sm)
+        assert np.allclose(s.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+        assert np.allclose(wt.sum(axis=1), 1.0, rtol=0, atol=1e-12)
