@@ -9,20 +9,22 @@
 // gate/up and down; NVFP4 weights with 16-element E4M3 block scales).
 //
 // A work item is (hot slot, M-tile of 128 weight rows = 8 repacked 16-row
-// tiles); blocks loop over items.  Per 64-wide K chunk:
-//   warps 0-7   each decode one 16-row tile's 576-byte chunk (E2M1 x E4M3,
-//               exact in f16) straight into the A stage, laid out as the
-//               tensor core's K-major operand without swizzle: 8x8 core
+// tiles); blocks loop over items.  Per stage of two 64-wide K chunks:
+//   warps 0-7   each decode one 16-row tile's two 576-byte chunks (E2M1 x
+//               E4M3, exact in f16) straight into the A stage, laid out as
+//               the tensor core's K-major operand without swizzle: 8x8 core
 //               matrices of 128 contiguous bytes, K-adjacent ones 128 bytes
-//               apart (LBO), row-adjacent ones 1024 bytes apart (SBO);
+//               apart (LBO), row-adjacent ones 2048 bytes apart (SBO: 16 K
+//               groups per row group);
 //   warps 8-11  stage the slot's m tokens (gate/up: x rows times 2^-xexp;
 //               down: h rows times 2^-hexp, both exact in f16) as the B
 //               operand in the same layout, rows >= m zero;
-//   warp 12     lane 0 issues four tcgen05.mma kind::f16 (M=128, N=m rounded
-//               up to 16, K=16) into a TMEM accumulator and commits them to
-//               the stage's "empty" mbarrier; after the last chunk a commit
-//               to the accumulator barrier.
-// Four stages ring between producers and the MMA issuer.  Warps 0-7 then
+//   warp 12     lane 0 issues eight tcgen05.mma kind::f16 (M=128, N=m
+//               rounded up to 16, K=16) into a TMEM accumulator and commits
+//               them to the stage's "empty" mbarrier; after the last stage a
+//               commit to the accumulator barrier.
+// Two stages ring between producers and the MMA issuer (an odd chunk count
+// leaves the last stage half full).  Warps 0-7 then
 // read the accumulator (tcgen05.ld, warp w owns TMEM lanes 32(w%4).. and
 // half of the columns) and run the epilogue:
 //   gate/up  rows 16j+r (r < 8) are gate, 16j+r+8 the matching up rows
@@ -48,14 +50,15 @@ constexpr int kStgW = 4;                          // B staging warps
 constexpr int kMmaW = kDecW + kStgW;              // MMA-issuing warp
 constexpr int kGW = kMmaW + 1;
 constexpr int kGT = 32 * kGW;
-constexpr int kNS = 4;                            // pipeline stages
+constexpr int kCPS = 2;                           // 64-wide K chunks per pipeline stage
+constexpr int kNS = 2;                            // pipeline stages
 constexpr int kLA = 4;                            // B-operand chunks in flight (raw copies)
 constexpr int kMT = 128;                          // weight rows per item (8 tiles)
 constexpr int kNmax = kMaxTokens;                 // tokens per slot
 constexpr uint32_t kLBO = 128;                    // K-adjacent core matrices
-constexpr uint32_t kSBO = 8 * 128;                // row-adjacent core matrices (8 K-groups per row group)
-constexpr int kAStage = kMT * kChunkK * 2;        // 16 KB
-constexpr int kBStage = kNmax * kChunkK * 2;      // 8 KB
+constexpr uint32_t kSBO = kCPS * 8 * 128;         // row-adjacent core matrices (8 K-groups per chunk)
+constexpr int kAStage = kMT * kChunkK * kCPS * 2; // 32 KB
+constexpr int kBStage = kNmax * kChunkK * kCPS * 2;   // 16 KB
 constexpr int kScratch = kMaxTokens * (kMaxTopK + kMaxShared) * 8;   // combine's pair table
 constexpr int kCHA = 4;                           // chunks per raw-weight segment
 constexpr int kRWA = 4;                           // raw-weight segments per decode warp
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
     };
     if (warp < kDecW) rissue(kRWA);
 
-    int gc = 0;        // chunks through the A/B stages so far
+    int gc = 0;        // stages (kCPS chunks each) through the A/B ring so far
     int jc = 0;        // raw segments consumed (decode warps)
 #pragma unroll 1
     for (int li = 0; li < nmy; ++li) {
@@ -290,38 +293,42 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
             // ---- A producer: tile 8mt + warp, from the raw ring ----
             int oc = 0, cseg = 0;
 #pragma unroll 1
-            for (int c = 0; c < NC; ++c) {
-                const int gcc = gc + c, st = gcc % kNS;
-                if (oc == 0 && !*abort) {
-                    if (gwait(rbar + jc % kRWA, (unsigned)((jc / kRWA) & 1), abort, d.err)) n_done = jc + 1;
-                }
+            for (int c0 = 0; c0 < NC; c0 += kCPS) {
+                const int gcc = gc + c0 / kCPS, st = gcc % kNS, nch = min(kCPS, NC - c0);
                 const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
-                if (go) {
-                    const uint8_t *ch = rraw + ((size_t)(jc % kRWA) * kCHA + oc) * kChunkBytes;
-                    const uint4 cw = lds128(ch + 16 * lane);
-                    uint2 sw;
-                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n"
-                                 : "=r"(sw.x), "=r"(sw.y) : "r"(smem_u32(ch + kCodeBytes + 8 * g)));
-                    uint32_t a[4][4];
-                    decode_chunk(cw, sw, a);
-                    uint8_t *As = sA + (size_t)st * kAStage + g * 16 + q * 4;
+#pragma unroll 1
+                for (int h = 0; h < nch; ++h) {
+                    if (oc == 0 && !*abort) {
+                        if (gwait(rbar + jc % kRWA, (unsigned)((jc / kRWA) & 1), abort, d.err)) n_done = jc + 1;
+                    }
+                    if (go) {
+                        const uint8_t *ch = rraw + ((size_t)(jc % kRWA) * kCHA + oc) * kChunkBytes;
+                        const uint4 cw = lds128(ch + 16 * lane);
+                        uint2 sw;
+                        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n"
+                                     : "=r"(sw.x), "=r"(sw.y) : "r"(smem_u32(ch + kCodeBytes + 8 * g)));
+                        uint32_t a[4][4];
+                        decode_chunk(cw, sw, a);
+                        // chunk h of the stage: K groups 8h .. 8h + 7
+                        uint8_t *As = sA + (size_t)st * kAStage + 8 * h * kLBO + g * 16 + q * 4;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                        for (int i = 0; i < 4; ++i)
 #pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * kSBO + (2 * i + (b >> 1)) * kLBO) =
-                                a[i][b];
-                    fence_proxy_async();
+                            for (int b = 0; b < 4; ++b)
+                                *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * kSBO +
+                                                              (2 * i + (b >> 1)) * kLBO) = a[i][b];
+                    }
+                    if (++oc == min(kCHA, NC - cseg)) {
+                        cseg += oc;
+                        oc = 0;
+                        ++jc;
+                        if (!*abort) rissue(jc + kRWA);
+                    }
                 }
+                if (go) fence_proxy_async();
                 __syncwarp();
                 if (go && lane == 0) mbar_arrive(&s_full[st]);
-                if (li == 0 && c == 0) MOE_TRACE_POINT(3 + MODE, 3);
-                if (++oc == min(kCHA, NC - cseg)) {
-                    cseg += oc;
-                    oc = 0;
-                    ++jc;
-                    if (!*abort) rissue(jc + kRWA);
-                }
+                if (li == 0 && c0 == 0) MOE_TRACE_POINT(3 + MODE, 3);
             }
         } else if (warp < kMmaW) {
             // ---- B producer: the slot's m tokens (rows >= m zero).  Each
@@ -373,35 +380,40 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
 #pragma unroll
             for (int j = 0; j < kLA; ++j) bissue(j);
 #pragma unroll 1
-            for (int c = 0; c < NC; ++c) {
-                const int gcc = gc + c, st = gcc % kNS;
-                cp_async_wait<kLA - 1>();
+            for (int c0 = 0; c0 < NC; c0 += kCPS) {
+                const int gcc = gc + c0 / kCPS, st = gcc % kNS, nch = min(kCPS, NC - c0);
                 const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
-                if (go) {
-                    uint8_t *Bs = sB + (size_t)st * kBStage;
+#pragma unroll 1
+                for (int h = 0; h < nch; ++h) {
+                    const int c = c0 + h;
+                    cp_async_wait<kLA - 1>();
+                    if (go) {
+                        // chunk h of the stage: K groups 8h .. 8h + 7
+                        uint8_t *Bs = sB + (size_t)st * kBStage + 8 * h * kLBO;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int n = nlo + 8 * nhi + 16 * u;
-                        if (n < N) {
-                            uint4 o = make_uint4(0u, 0u, 0u, 0u);
-                            if (src[u]) {
-                                const uint4 v = lds128(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128);
-                                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                                uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+                        for (int u = 0; u < 4; ++u) {
+                            const int n = nlo + 8 * nhi + 16 * u;
+                            if (n < N) {
+                                uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                                if (src[u]) {
+                                    const uint4 v = lds128(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128);
+                                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                                    uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
-                                                       __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
+                                    for (int i = 0; i < 4; ++i)
+                                        ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
+                                                           __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
+                                }
+                                *reinterpret_cast<uint4 *>(Bs + (n >> 3) * kSBO + kg * kLBO + (n & 7) * 16) = o;
                             }
-                            *reinterpret_cast<uint4 *>(Bs + (n >> 3) * kSBO + kg * kLBO + (n & 7) * 16) = o;
                         }
                     }
-                    fence_proxy_async();
+                    bissue(c + kLA);
                 }
+                if (go) fence_proxy_async();
                 __syncwarp();
                 if (go && lane == 0) mbar_arrive(&s_full[st]);
-                if (li == 0 && c == 0) MOE_TRACE_POINT_AT(3 + MODE, 6, 32 * kDecW);
-                bissue(c + kLA);
+                if (li == 0 && c0 == 0) MOE_TRACE_POINT_AT(3 + MODE, 6, 32 * kDecW);
             }
             if (li == 0) MOE_TRACE_POINT_AT(3 + MODE, 7, 32 * kDecW);
         } else if (lane == 0) {
@@ -410,19 +422,19 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
             bool go = gwait(&s_acce, ((unsigned)li & 1u) ^ 1u, abort, d.err);   // accumulator read out
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < NC && go; ++c) {
-                const int gcc = gc + c, st = gcc % kNS;
+            for (int c0 = 0; c0 < NC && go; c0 += kCPS) {
+                const int gcc = gc + c0 / kCPS, st = gcc % kNS, nch = min(kCPS, NC - c0);
                 if (!gwait(&s_full[st], (unsigned)(gcc / kNS) & 1u, abort, d.err)) {
                     go = false;
                     break;
                 }
                 tc_fence_after();
-                if (li == 0 && c == 0) MOE_TRACE_POINT_AT(3 + MODE, 4, 32 * kMmaW);
+                if (li == 0 && c0 == 0) MOE_TRACE_POINT_AT(3 + MODE, 4, 32 * kMmaW);
                 const uint32_t a0 = smem_u32(sA + (size_t)st * kAStage), b0 = smem_u32(sB + (size_t)st * kBStage);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll 1
+                for (int ks = 0; ks < 4 * nch; ++ks) {
                     const uint64_t da = smem_desc(a0 + ks * 2 * kLBO), db = smem_desc(b0 + ks * 2 * kLBO);
-                    const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+                    const uint32_t acc = (c0 > 0 || ks > 0) ? 1u : 0u;
                     asm volatile(
                         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(taddr),
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                              : "memory");
             if (li == 0) MOE_TRACE_POINT_AT(3 + MODE, 5, 32 * kMmaW);
         }
-        gc += NC;
+        gc += (NC + kCPS - 1) / kCPS;
         if (li == 0) MOE_TRACE_POINT(3 + MODE, 2);
 
         // ---- epilogue: warps 0-7 ----
