@@ -18,18 +18,21 @@
 // warp owns one expert and one K range: that part of its router row is
 // fetched into registers BEFORE the programmatic-launch wait (router weights
 // do not depend on the previous kernel); the block stages its token group's
-// activation columns in shared memory and the warp computes the FP32 partial
-// logits of those tokens (one accumulator per token, so the FMA chains run
-// side by side).  With several K ranges the partial sums go to the workspace
-// and the ticket's last block adds them in a fixed order.  Two tickets
-// follow, with no spinning:
-//   * the last expert group of a token group to finish runs sigmoid + top-k
-//     for those tokens (one warp per token) and ORs each token into a 64-bit
-//     mask per selected expert;
+// activation columns in shared memory (as FP32) and the warp computes the
+// FP32 partial logits of those tokens (one accumulator per token, so the FMA
+// chains run side by side).  With several K ranges the partial sums go to the
+// workspace and the ticket's last block adds them in a fixed order, into
+// shared memory.  Two tickets follow, with no spinning:
+//   * the last expert group of a token group to finish runs the scores and
+//     top-k for those tokens (one warp per token) and ORs each token into a
+//     64-bit mask per selected expert;
 //   * the last token group to finish turns the masks into slots (shared
 //     experts first, then routed experts in ascending id), numbers the
 //     (expert, token) pairs so that each expert's pairs are contiguous, lists
 //     the slots with many tokens for the grouped kernels, and clears the masks.
+// With a single token group the first ticket's last block is also the last
+// overall: it keeps the choices and masks in shared memory and skips the
+// second ticket.
 #include <algorithm>
 
 #include "moe_internal.cuh"
