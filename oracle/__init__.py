@@ -11,6 +11,7 @@ function of ``oracle.c`` cites the page passage it follows.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -25,18 +26,21 @@ _lock = threading.Lock()
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    """Compile oracle.c into oracle/_build/liboracle.so (gcc, OpenMP)."""
-    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
-    tmp = _LIB + f".tmp{os.getpid()}"
+def build(force: bool = False, plant: int = 0) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, OpenMP); with
+    `plant` > 0 a separate library with that deliberate mistake compiled in
+    (tests of the pins only)."""
+    out = _LIB if plant == 0 else os.path.join(os.path.dirname(_LIB), f"liboracle_plant{int(plant)}.so")
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c99",
-           "-D_DEFAULT_SOURCE", _SRC, "-o", tmp, "-lm"]
+           "-D_DEFAULT_SOURCE", f"-DORC_PLANT={int(plant)}", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB)
-    return _LIB
+    os.replace(tmp, out)
+    return out
 
 
 class _Layer(ctypes.Structure):
@@ -53,32 +57,56 @@ class _Layer(ctypes.Structure):
     ]
 
 
+def _load(path):
+    L = ctypes.CDLL(path)
+    _declare(L)
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
-            d, i, vp = ctypes.c_double, ctypes.c_int, ctypes.c_void_p
-            L.orc_e2m1.restype = d
-            L.orc_e2m1.argtypes = [i]
-            L.orc_e4m3.restype = d
-            L.orc_e4m3.argtypes = [i]
-            L.orc_bf16_round.restype = d
-            L.orc_bf16_round.argtypes = [d]
-            L.orc_double_to_bf16.restype = ctypes.c_uint16
-            L.orc_double_to_bf16.argtypes = [d]
-            L.orc_bf16_to_double.restype = d
-            L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
-            L.orc_dequant.restype = None
-            L.orc_dequant.argtypes = [vp, vp, ctypes.c_float, i, i, vp]
-            L.orc_route.restype = i
-            L.orc_route.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp]
-            L.orc_forward.restype = i
-            L.orc_forward.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp, i]
-            L.orc_max_threads.restype = i
-            L.orc_max_threads.argtypes = []
-            _lib = L
+            _lib = _load(build())
     return _lib
+
+
+@contextlib.contextmanager
+def planted(plant: int):
+    """Run the oracle with deliberate mistake `plant` compiled in (see the
+    ORC_PLANT list in oracle.c) inside the block; the regular library after."""
+    global _lib
+    regular = lib()
+    mutant = _load(build(plant=plant))
+    with _lock:
+        _lib = mutant
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = regular
+
+
+def _declare(L):
+    d, i, vp = ctypes.c_double, ctypes.c_int, ctypes.c_void_p
+    L.orc_e2m1.restype = d
+    L.orc_e2m1.argtypes = [i]
+    L.orc_e4m3.restype = d
+    L.orc_e4m3.argtypes = [i]
+    L.orc_bf16_round.restype = d
+    L.orc_bf16_round.argtypes = [d]
+    L.orc_double_to_bf16.restype = ctypes.c_uint16
+    L.orc_double_to_bf16.argtypes = [d]
+    L.orc_bf16_to_double.restype = d
+    L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.orc_dequant.restype = None
+    L.orc_dequant.argtypes = [vp, vp, ctypes.c_float, i, i, vp]
+    L.orc_route.restype = i
+    L.orc_route.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp]
+    L.orc_forward.restype = i
+    L.orc_forward.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp, i]
+    L.orc_max_threads.restype = i
+    L.orc_max_threads.argtypes = []
 
 
 def _ptr(a):

@@ -62,6 +62,16 @@
  */
 #include <math.h>
 #include <stdint.h>
+
+/* Test hook: a nonzero ORC_PLANT compiles exactly one deliberate mistake into
+ * a separate library, so that a test can show that the pins catch it:
+ *   1 softmax scores replaced by sigmoid, 2 normalisation ignored,
+ *   3 gate and up rows swapped, 4 shared experts dropped from the combine,
+ *   5 E2M1 subnormal (code 1) decoded as 1.0 instead of 0.5.
+ * The regular build plants nothing. */
+#ifndef ORC_PLANT
+#define ORC_PLANT 0
+#endif
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -79,7 +89,7 @@
 double orc_e2m1(int code)
 {
     int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
-    double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    double mag = (e == 0) ? (ORC_PLANT == 5 ? 1.0 : 0.5) * m : ldexp(1.0 + 0.5 * m, e - 1);
     return s ? -mag : mag;
 }
 
@@ -214,7 +224,7 @@ static void token_scores(const orc_layer *L, const uint16_t *xt, double *z, doub
         z[e] = acc;
         s[e] = sigmoid(acc);
     }
-    if (L->score_func == 1) {
+    if (L->score_func == 1 && ORC_PLANT != 1) {
         double zmax = z[0], den = 0.0;
         for (int e = 1; e < L->E; ++e) zmax = z[e] > zmax ? z[e] : zmax;
         for (int e = 0; e < L->E; ++e) den += exp(z[e] - zmax);
@@ -242,7 +252,7 @@ static void token_topk(const orc_layer *L, const double *z, const double *s, int
     double sum = 0.0;
     for (int j = 0; j < K; ++j) sum += s[ids[j]];
     for (int j = 0; j < K; ++j) {
-        double wj = L->normalize ? s[ids[j]] / sum : s[ids[j]];
+        double wj = (L->normalize && ORC_PLANT != 2) ? s[ids[j]] / sum : s[ids[j]];
         w[j] = wj * L->routed_scale;
     }
     free(taken);
@@ -282,8 +292,8 @@ static void expert_mlp(int H, int I,
     for (int n = 0; n < I; ++n) {
         double g = 0.0, u = 0.0;
         for (int k = 0; k < H; ++k) {
-            g += x[k] * wexact(w13, w13_sf, gsg, H, n, k);
-            u += x[k] * wexact(w13, w13_sf, gsu, H, I + n, k);
+            g += x[k] * wexact(w13, w13_sf, gsg, H, ORC_PLANT == 3 ? I + n : n, k);
+            u += x[k] * wexact(w13, w13_sf, gsu, H, ORC_PLANT == 3 ? n : I + n, k);
         }
         double silu = g * sigmoid(g);
         h[n] = orc_bf16_round(silu * u);
@@ -354,7 +364,7 @@ int orc_forward(const orc_layer *L, const uint16_t *x, int T, uint16_t *out,
             double acc = 0.0;
             for (int j = 0; j < K; ++j)
                 acc += w[(size_t)t * K + j] * y[((size_t)t * P + j) * H + m];
-            for (int sidx = 0; sidx < S; ++sidx)
+            for (int sidx = 0; sidx < (ORC_PLANT == 4 ? 0 : S); ++sidx)
                 acc += y[((size_t)t * P + K + sidx) * H + m];
             if (out_pre) out_pre[(size_t)t * H + m] = acc;
             out[(size_t)t * H + m] = orc_double_to_bf16(acc);

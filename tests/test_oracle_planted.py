@@ -1,0 +1,39 @@
+"""The pins catch plausible mistakes (no GPU).
+
+Each case compiles the oracle with one deliberate mistake (the ORC_PLANT list
+in oracle/oracle.c) into a separate library and runs, against it, the pins
+that should expose it: at least one of them must fail.  The regular library
+is restored afterwards, and every pin passes on it (the other test files)."""
+import pytest
+
+import test_oracle_formats as fmt
+import test_oracle_layer as lay
+import test_oracle_routing as rt
+
+CASES = [
+    (1, "softmax scores replaced by sigmoid",
+     [rt.test_softmax_two_experts_is_the_logistic_of_the_difference,
+      rt.test_softmax_is_shift_invariant_and_sigmoid_is_not]),
+    (2, "normalisation ignored",
+     [rt.test_scores_weights_closed_form, rt.test_weights_sum_to_one_and_permutation]),
+    (3, "gate and up rows swapped",
+     [lay.test_closed_form_tiny_layer, lay.test_closed_form_two_experts_and_shared]),
+    (4, "shared experts dropped from the combine",
+     [lay.test_shared_expert_only, lay.test_closed_form_two_experts_and_shared]),
+    (5, "E2M1 subnormal decoded as 1.0",
+     [fmt.test_e2m1_golden_file, fmt.test_e2m1_table_exhaustive]),
+]
+
+
+@pytest.mark.parametrize("plant,what,pins", CASES, ids=[c[1] for c in CASES])
+def test_planted_mistake_is_caught(orc, plant, what, pins):
+    caught = []
+    with orc.planted(plant):
+        for pin in pins:
+            try:
+                pin(orc)
+            except AssertionError:
+                caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake: {what}"
+    # and the regular oracle is back
+    assert orc.e2m1(1) == 0.5
