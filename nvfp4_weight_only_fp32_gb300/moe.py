@@ -235,8 +235,10 @@ class MoELayer:
     """One decode layer on the current CUDA device.
 
     `layer` is a dict of canonical tensors (numpy or torch) plus "cfg" with the
-    sizes H, E, k, I, S, Is; the weights are repacked into library memory, so
-    the inputs may be freed afterwards."""
+    sizes H, E, k, I, S, Is and, optionally, "normalize" (1), "routed_scale"
+    (1.0) and "score_func" ("sigmoid", or "softmax": the three-kernel chain);
+    the weights are repacked into library memory, so the inputs may be freed
+    afterwards."""
 
     def __init__(self, layer: dict, max_tokens: int | None = None, grouped_min_tokens: int = 0,
                  stream=None, fused: int = 0):
