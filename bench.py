@@ -69,6 +69,9 @@ def parse():
     ap.add_argument("--workload", default="flint1", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=0, help="override layers per step")
     ap.add_argument("--secondary", default="flint8", help="second workload reported in the line ('' = none)")
+    ap.add_argument("--extras", default="ml4,zipf64,zipf64-gemv,tiny",
+                    help="further workloads timed and reported under 'workloads' ('' = none); "
+                         "zipf64-gemv is zipf64 with the grouped kernels off")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grouped-min", type=int, default=0,
@@ -194,9 +197,10 @@ def barrier(dist):
 # ---------------------------------------------------------------------------
 # CPU oracle leg (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-def oracle_sample(cfg_index: int, seconds: float, seed: int, want_out: bool = False):
+def oracle_sample(cfg_index: int, seconds: float, seed: int, want_out: bool = False, threads: int = 0):
     """Time the oracle on whole-layer forwards of the workload until `seconds`
-    of CPU work have run.  -> dict(value GB/s, per_layer_s, layers, cores, ...)."""
+    of CPU work have run (threads: 0 = all host cores).
+    -> dict(value GB/s, per_layer_s, layers, cores, ...)."""
     import numpy as np
     import gen
     import oracle
@@ -205,7 +209,7 @@ def oracle_sample(cfg_index: int, seconds: float, seed: int, want_out: bool = Fa
     x = gen.make_x(c, seed)
     ids, *_ = oracle.route({"cfg": c, **router}, x)
     layer = {"cfg": c, **router, **gen.make_experts(c, seed, np.unique(ids))}
-    nthreads = oracle.max_threads()
+    nthreads = threads if threads > 0 else oracle.max_threads()
     pairs = c["T"] * (c["k"] + c["S"])
     cores = min(nthreads, pairs)
     n, t0, res = 0, time.perf_counter(), None
@@ -310,15 +314,24 @@ def capture(torch, fn, stream):
     return g
 
 
-def time_graph(torch, g, stream, warmup, steps, sampler=None):
+def time_graph(torch, g, stream, warmup, steps, sampler=None, clock_pass_steps=0):
+    """CUDA-event time of `steps` replays after `warmup` untimed ones.  With a
+    sampler, clocks are sampled from the start of an untimed pass of
+    `clock_pass_steps` replays of the same graph (long enough for the 200 ms
+    sampler, run just before) through the end of the timed region."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tc = None
     if sampler:
         sampler.start()
         time.sleep(0.3)
+        tc = time.time()
+        with torch.cuda.stream(stream):
+            for _ in range(clock_pass_steps):
+                g.replay()
     t0 = time.time()
     e0.record(stream)
     with torch.cuda.stream(stream):
@@ -327,7 +340,11 @@ def time_graph(torch, g, stream, warmup, steps, sampler=None):
     e1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
-    clocks = sampler.stop(t0, t1) if sampler else None
+    clocks = None
+    if sampler:
+        clocks = sampler.stop(tc, t1)
+        clocks["window"] = (f"{clock_pass_steps} untimed replays of the same graph just before the timed "
+                            f"region ({t0 - tc:.2f} s), then the timed region ({t1 - t0:.3f} s)")
     return e0.elapsed_time(e1), clocks
 
 
@@ -376,13 +393,15 @@ def run_gpu(args):
 
     g_full = capture(torch, lambda: chain.enqueue(moe), stream)
     sel, gu_bytes, Us = byte_counts(gen, chain, np)
+    long_steps = auto_steps(torch, g_full, stream, args.warmup)     # ~1.5 s of replays
     if args.steps <= 0:
-        args.steps = auto_steps(torch, g_full, stream, args.warmup)
+        args.steps = long_steps
         if dist is not None:
             args.steps = int(max_over_ranks(float(args.steps), dist, dev))
     barrier(dist)
     sampler = ClockSampler(local)
-    ms, clocks = time_graph(torch, g_full, stream, args.warmup, args.steps, sampler)
+    ms, clocks = time_graph(torch, g_full, stream, args.warmup, args.steps, sampler,
+                            clock_pass_steps=long_steps if args.steps < long_steps else 0)
     barrier(dist)
     ms_max = max_over_ranks(ms, dist, dev)
     bytes_step = float(sum(sel))
@@ -446,33 +465,77 @@ def run_gpu(args):
            "h2d_bytes_per_step": L * T * H * 2,
            "d2h_bytes_per_step": L * T * H * 2,
            "us_per_layer": e2e_ms * 1e3 / (args.steps * L), "mode": e2e_mode}
+    # cold single-layer latency: one call of the first layer right after
+    # writing a scratch buffer of twice the L2 size (its weights, x and the
+    # code's data are then not in L2), median of a few tries
+    scratch = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024,
+                          dtype=torch.float32, device=dev)
+    cold = []
+    for i in range(7):
+        with torch.cuda.stream(stream):
+            scratch.fill_(float(i))
+            e0.record(stream)
+            moe.moe_decode_forward(chain.layers[0].h, chain.xs[0], T, chain.outs[0], chain.ids[0], chain.ws[0],
+                                   stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        cold.append(e0.elapsed_time(e1) * 1e3)
+    del scratch
+    cold_us = sorted(cold)[len(cold) // 2]
     chain.close()
     del chain, g_full
     torch.cuda.empty_cache()
 
-    secondary = None
-    if args.secondary not in ("", "none") and args.secondary != args.workload and rank == 0:
-        si, sL = WORKLOADS[args.secondary]
-        ch2 = Chain(moe, torch, gen, si, sL, seed0 + 50000)
+    def other(name, grouped_min=0):
+        """Per-layer time of another workload: its own distinct layers in one
+        CUDA graph, timed like the main one (same warm-up and step count)."""
+        oi, oL = WORKLOADS[name]
+        ch2 = Chain(moe, torch, gen, oi, oL, seed0 + 50000 + 1000 * oi, grouped_min)
         g2 = capture(torch, lambda: ch2.enqueue(moe), stream)
         sel2, _, U2 = byte_counts(gen, ch2, np)
-        ms2, _ = time_graph(torch, g2, stream, args.warmup, args.steps)
-        us2 = ms2 * 1e3 / (args.steps * sL)
+        st2 = max(args.steps, 5)
+        ms2, _ = time_graph(torch, g2, stream, args.warmup, st2)
+        us2 = ms2 * 1e3 / (st2 * oL)
         b2 = float(np.mean(sel2))
         c2 = ch2.c
-        secondary = {"workload": f"{c2['name']}: T={c2['T']} H={c2['H']} E={c2['E']} top-{c2['k']} "
-                                 f"I={c2['I']} +{c2['S']} shared, {sL} layers per step",
-                     "us_per_layer": us2, "GBps": b2 / (us2 * 1e-6) / 1e9,
-                     "selected_bytes_per_layer": b2, "unique_experts_mean": float(np.mean(U2))}
+        one = ch2.layers[0].info().single_launch_max_tokens >= ch2.T
+        res = {"workload": f"{c2['name']}: T={c2['T']} H={c2['H']} E={c2['E']} top-{c2['k']} "
+                           f"I={c2['I']} +{c2['S']} shared, {oL} layers per step",
+               "us_per_layer": us2, "GBps": b2 / (us2 * 1e-6) / 1e9,
+               "frac_of_measured": b2 / (us2 * 1e-6) / 1e9 / peak,
+               "selected_bytes_per_layer": b2, "unique_experts_mean": float(np.mean(U2)),
+               "path": "single launch" if one else
+                       ("chain" + (", grouped kernels off" if grouped_min < 0 else
+                                   (", grouped tensor-core kernels for slots of >= 8 tokens" if c2["T"] > 8
+                                    else ""))),
+               "steps": st2}
         ch2.close()
         del g2
+        torch.cuda.empty_cache()
+        return res
+
+    secondary = None
+    workloads = {}
+    if rank == 0:
+        if args.secondary not in ("", "none") and args.secondary != args.workload:
+            secondary = other(args.secondary)
+        for name in [w for w in args.extras.split(",") if w]:
+            base = name[:-5] if name.endswith("-gemv") else name
+            if base == args.workload and not name.endswith("-gemv"):
+                continue
+            workloads[name] = other(base, -1 if name.endswith("-gemv") else 0)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_sample(ci, args.cpu_seconds, gen.BASE_SEED + 7)
+        r1 = oracle_sample(ci, max(2.0, args.cpu_seconds / 4), gen.BASE_SEED + 8, threads=1)
         cpu = {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
                "sample": f"{r['layers']} whole-layer FP64 forwards of one {c['name']} layer "
-                         f"(T={c['T']}), {r['seconds']:.1f} s"}
+                         f"(T={c['T']}), {r['seconds']:.1f} s",
+               "us_per_layer": r["per_layer_s"] * 1e6,
+               "single_thread": {"value": r1["value"], "unit": "GB/s", "cores": 1,
+                                 "us_per_layer": r1["per_layer_s"] * 1e6,
+                                 "sample": f"{r1['layers']} forwards, {r1['seconds']:.1f} s"}}
 
     if rank == 0:
         line = {
@@ -489,6 +552,7 @@ def run_gpu(args):
                        "graph": "one CUDA graph per step; " + ("one single-launch kernel per layer" if single else
                                                                        "3 kernels per layer chained with PDL")},
             "us_per_layer": us_layer,
+            "cold_us_per_layer": cold_us,
             "selected_bytes_per_layer": bytes_step / L,
             "unique_experts_mean": float(np.mean(Us)),
             "frac_of_8TBps": value / 8000.0,
@@ -505,6 +569,8 @@ def run_gpu(args):
         }
         if secondary:
             line["secondary"] = secondary
+        if workloads:
+            line["workloads"] = workloads
         print(json.dumps(line), flush=True)
     barrier(dist)
     if dist is not None:

@@ -85,9 +85,10 @@ typedef struct {
                                0 = library default, < 0 = never */
     int fused;              /* 0: moe_decode_forward runs the whole step as
                                one launch when the shape allows it (T <= 8,
-                               H <= 4096, E <= 2 x SM count, activations fit
-                               in shared memory); < 0: always the three-kernel
-                               chain of the moe_stage_* entry points */
+                               H <= 8192, E <= 256 and <= 4 x SM count, the
+                               activations and the weight rings fit in shared
+                               memory); < 0: always the three-kernel chain of
+                               the moe_stage_* entry points */
     int score_func;         /* routing score: 0 = sigmoid of each logit (Flint
                                page, "Flint model architecture"); 1 = softmax
                                over all experts' logits (Mistral Large 4 page,
@@ -97,8 +98,7 @@ typedef struct {
                                chosen experts' scores, normalised to sum to 1
                                when normalize_topk = 1 (for softmax:
                                exp(z_j - z_max) / sum over the chosen of
-                               exp(z_i - z_max)), times routed_scale.  Softmax
-                               layers always run the three-kernel chain. */
+                               exp(z_i - z_max)), times routed_scale. */
 } moe_config;
 
 /* Weights in the canonical layout (device pointers, only read during
@@ -157,11 +157,18 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream,
 void moe_destroy(moe_layer *layer);
 
 /* One decode step, rows a1..a5 above, for T tokens (1 <= T <= max_tokens).
- * Small steps run as ONE launch of one block per SM with two in-kernel grid
- * barriers (all blocks must be resident together: do not share the GPU with
- * work that fills every SM while it runs; a barrier wait that exceeds about a
- * second gives up, and moe_check then reports MOE_ERR_TIMEOUT); otherwise as
- * the chain moe_stage_route, moe_stage_gate_up, moe_stage_down.
+ * Small steps run as ONE launch of one block per SM.  It has no grid
+ * barrier: blocks hand the router logits and the SwiGLU output to each other
+ * as words tagged with the call number, and a reader polls the words it
+ * needs.  Every block must therefore get an SM while the others poll.  A
+ * kernel on another stream that holds SMs delays the blocks that wait for
+ * them; a wait that exceeds about a second gives up, the call's outputs are
+ * then invalid and moe_check reports MOE_ERR_TIMEOUT.  Otherwise the step
+ * runs as the chain moe_stage_route, moe_stage_gate_up, moe_stage_down.
+ * The call tags of one handle are 32-bit: the library restarts them (with
+ * the tagged words) after 2^31 single-launch calls made through this entry
+ * point; a CUDA graph that replays such a call needs moe_check (which
+ * restarts them too) at least every 2^31 replays.
  *   x         BF16 [T, H], 16-byte aligned, read only
  *   out       BF16 [T, H], 16-byte aligned, written; must not alias x
  *   topk_ids  int32 [T, k] or NULL: selected experts, descending score
@@ -202,7 +209,9 @@ moe_status moe_stage_down(moe_layer *layer, int T, void *out, void *stream);
 
 /* Synchronise `stream`, then read and clear the handle's sticky device error
  * word: MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (reason in
- * moe_last_error()). */
+ * moe_last_error()).  It also restarts the single launch's call tags (see
+ * moe_decode_forward), so no work of this handle may be in flight on another
+ * stream. */
 moe_status moe_check(moe_layer *layer, void *stream);
 
 /* Decode one repacked matrix back to the canonical row-major FP32 layout with
@@ -255,7 +264,11 @@ moe_status moe_get_info(const moe_layer *layer, moe_layer_info *info);
  *   topk_ids  int32 [T, k] device (written): selected experts, descending score
  *   topk_w    FP32  [T, k] device (written): weights (normalised when
  *             normalize_topk = 1, then times routed_scale)
- * Same arithmetic and tie rule as moe_stage_route.  No handle is needed.
+ * The score is always the sigmoid of the logit (there is no softmax option
+ * here); the choice and its order follow moe_stage_route's rule (FP32 logits,
+ * lowest index on ties).  Its logits are summed in another order than the
+ * handle path's, so the weights agree with that path to FP32 rounding (about
+ * 1e-6 relative), not bit for bit.  No handle is needed.
  * Limits: 1 <= T <= 64, 1 <= E <= 512, 1 <= k <= min(8, E), hidden a multiple
  * of 64 in [64, 16384]; anything else returns MOE_ERR_UNSUPPORTED naming the
  * limit.  Scratch: a 128 KiB + 256 B static device array inside the library

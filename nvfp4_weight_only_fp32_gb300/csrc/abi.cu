@@ -35,6 +35,7 @@ struct moe_layer {
     int optin_smem;
     int fused_ok[kMaxTokens + 1];   // single-launch path usable for this T
     int inject_stall = 0;           // moe_debug_inject: for the next single launch only
+    unsigned long long fused_calls = 0;   // single launches since the tags were last restarted
 };
 
 namespace {
@@ -188,6 +189,24 @@ void carve_workspace(moe_layer *L, char *base) {
     L->wsbytes = cv.off;
 }
 
+// The single launch tags the words its blocks exchange with the call number
+// (32 bits): restart the per-block call counters and clear the tagged words,
+// enqueued on `st` (stream order puts it after the last call and before the
+// next one).
+cudaError_t restart_tags(moe_layer *L, cudaStream_t st) {
+    const int Tf = std::min(L->cfg.max_tokens, 8);
+    cudaError_t e = cudaMemsetAsync(L->d.calls, 0, sizeof(unsigned) * L->sm_count, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L->d.logit_tag, 0, sizeof(unsigned long long) * Tf * L->d.E, st);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(L->d.h_tag, 0, sizeof(unsigned long long) * Tf * (L->d.k + L->d.S) * (L->d.Imax / 2), st);
+    L->fused_calls = 0;
+    return e;
+}
+
+// Restart the tags well before the 32-bit call number could wrap to a value
+// that words left from an early call still carry.
+constexpr unsigned long long kTagRestart = 1ull << 31;
+
 moe_status check_call(moe_layer *L, int T) {
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer handle is NULL");
     if (T < 1 || T > L->cfg.max_tokens)
@@ -332,8 +351,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     if (L->cfg.grouped_min_tokens > 0 && grouped_supported(d, L->sm_count)) d.grouped_min = L->cfg.grouped_min_tokens;
     for (int T = 0; T <= kMaxTokens; ++T) {
         L->fused_ok[T] = 0;
-        // the single launch implements sigmoid routing only
-        if (e == cudaSuccess && cfg->fused >= 0 && cfg->score_func == 0 && T >= 1 && T <= cfg->max_tokens &&
+        if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&
             fused_eligible(d, T, L->sm_count, (size_t)L->optin_smem))
             L->fused_ok[T] = fused_blocks_per_sm(d, T) >= 1;
     }
@@ -408,7 +426,10 @@ moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int
         DevLayer d = L->d;
         d.debug_stall = L->inject_stall;
         L->inject_stall = 0;
-        cudaError_t e = launch_fused(d, static_cast<const __nv_bfloat16 *>(x), T,
+        cudaError_t e = cudaSuccess;
+        if (++L->fused_calls >= kTagRestart) e = restart_tags(L, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "tag restart");
+        e = launch_fused(d, static_cast<const __nv_bfloat16 *>(x), T,
                                      static_cast<__nv_bfloat16 *>(out), topk_ids, topk_w, L->sm_count,
                                      reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MOE_OK : cuda_fail(e, "single-launch layer");
@@ -457,15 +478,15 @@ moe_status moe_check(moe_layer *L, void *stream) {
     int word = 0;
     e = cudaMemcpy(&word, L->d.err, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "error word read");
+    // restart the single-launch path's call counters and clear the words
+    // tagged with them (after a wait that gave up the blocks' counters may
+    // disagree; otherwise this bounds the count between checks)
+    e = restart_tags(L, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "tag restart");
     if (word == 0) return MOE_OK;
     int zero = 0;
     cudaMemcpy(L->d.err, &zero, sizeof(int), cudaMemcpyHostToDevice);
-    // restart the single-launch path's call counters and clear the words
-    // tagged with them
-    const int Tf = std::min(L->cfg.max_tokens, 8);
-    cudaMemset(L->d.calls, 0, sizeof(unsigned) * L->sm_count);
-    cudaMemset(L->d.logit_tag, 0, sizeof(unsigned long long) * Tf * L->d.E);
-    cudaMemset(L->d.h_tag, 0, sizeof(unsigned long long) * Tf * (L->d.k + L->d.S) * (L->d.Imax / 2));
     if (word == 1) return fail(MOE_ERR_TIMEOUT, "an in-kernel wait gave up");
     return fail(MOE_ERR_DEVICE, "device error word " + std::to_string(word));
 }

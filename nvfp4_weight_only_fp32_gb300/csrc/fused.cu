@@ -282,10 +282,14 @@ __device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, cons
 
 // Top-k of token t from the tagged logits (polled until they carry `tag`):
 // lane L holds experts i * 32 + L, i < M; lane j < K ends with the j-th
-// choice's sort key.
+// choice's sort key.  With `full_den` (softmax scores without normalisation
+// over the chosen) every lane also gets sum_e exp(z_e - z_max) over all
+// experts: the experts left after the top-k, then the chosen ones, each lane's
+// terms in index order, summed across the warp by a butterfly.
 template <int M>
 __device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned long long *lt, int t, int E, int K,
-                                            unsigned tag, int lane, int *err, unsigned long long &sel, int &passes) {
+                                            unsigned tag, int lane, int *err, unsigned long long &sel, int &passes,
+                                            bool full_den, float &den) {
     unsigned long long v[M];
     bool ok = true;
     unsigned pend = 0u;
@@ -316,6 +320,18 @@ __device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned lo
     }
     MOE_TRACE_CLOCK_AT(4, 1, 0);
     sel = warp_topk<M>(v, K, lane);
+    den = 1.f;
+    if (full_den) {
+        const float zmax = key_logit(__shfl_sync(0xffffffffu, (unsigned)(sel >> 32), 0));
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < M; ++i)
+            if (v[i]) acc += expf(key_logit((unsigned)(v[i] >> 32)) - zmax);
+        if (lane < K) acc += expf(key_logit((unsigned)(sel >> 32)) - zmax);
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+        den = acc;
+    }
     return ok;
 }
 
@@ -621,6 +637,26 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     int n_done = 0;                      // segments whose copies have landed (waited for)
     int nslots = S, lksd = 0, perw = 0, nrt = 0, n_list = 0;
     const int nrt0 = c < NRT ? (NRT - c + G - 1) / G : 0;   // this block's output tiles
+    // One ring segment of n chunks against the B rows at bp: wait for it,
+    // decode and multiply, release the slot and keep the ring full.
+    auto segment = [&](int n, const uint8_t *bp, bool bon, float (&a0)[4], float (&a1)[4]) {
+        if (ok) {
+            if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
+            else ok = false;
+        }
+        if (ok) {
+            const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
+#pragma unroll 2
+            for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, bon, a0, a1);
+        }
+        __syncwarp();
+        ++n_con;
+        if (++sl_c == RW) {
+            sl_c = 0;
+            par_c ^= 1u;
+        }
+        if (ok) pump(n_con + RW);
+    };
     // gate/up units of a pass plan: vw is this warp's index among the pass's
     // warps, tp the pass (0 shared experts, 1 routed), rb + vw the warp's
     // row of the reduction scratch (the physical warp where the two passes
@@ -640,25 +676,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll 1
             while (lft > 0) {
                 const int n = min(CH, lft);
-                if (ok) {
-                    if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
-                    else ok = false;
-                }
                 if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK_AT(2, 4 * tp, tp == 0 ? 64 : 0);
-                if (ok) {
-                    const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
-#pragma unroll 2
-                    for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, true, a0, a1);
-                }
-                __syncwarp();
+                segment(n, bp, true, a0, a1);
                 bp += n * 128;
                 lft -= n;
-                ++n_con;
-                if (++sl_c == RW) {
-                    sl_c = 0;
-                    par_c ^= 1u;
-                }
-                if (ok) pump(n_con + RW);
             }
             if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * tp + 1, tp == 0 ? 64 : 0);
 #pragma unroll
@@ -716,20 +737,31 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             const unsigned ltag = s_tag + (unsigned)d.debug_stall;
             int lpass = 0;
             unsigned long long sel = 0ull;
+            const bool smax = d.score_func == 1, fden = smax && !d.normalize;
+            float den = 1.f;
             switch (fg.m1p) {
-                case 1: ok = route_token<1>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                case 2: ok = route_token<2>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                case 4: ok = route_token<4>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
-                default: ok = route_token<8>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass) && ok; break;
+                case 1: ok = route_token<1>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
+                case 2: ok = route_token<2>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
+                case 4: ok = route_token<4>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
+                default: ok = route_token<8>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
             }
             const unsigned sel_key = (unsigned)(sel >> 32);
             const int sel_e = (int)~(unsigned)sel;
             MOE_TRACE_CLOCK_AT(3, 10, 0);
             MOE_TRACE_VALUE_AT(1, 2, 0, lpass);
-            // weights (normalised in selection order); for one token the
+            // scores: the sigmoid of the chosen logit, or (softmax routing)
+            // exp(z - z_max) over the full-softmax denominator (1 when the
+            // weights are normalised over the chosen, where it cancels).
+            // Weights are normalised in selection order; for one token the
             // slots follow directly: routed slot S + (rank of the id among
             // the k choices), one pair each
-            const float sel_s = key_score(sel_key);
+            float sel_s;
+            if (smax) {
+                const float zs = key_logit(sel_key);
+                sel_s = expf(zs - __shfl_sync(0xffffffffu, zs, 0)) / den;
+            } else {
+                sel_s = key_score(sel_key);
+            }
             float sv[kMaxTopK];
             int ev[kMaxTopK];
 #pragma unroll
@@ -1114,26 +1146,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll 1
             while (lft > 0) {
                 const int n = min(CH, lft);
-                if (ok) {
-                    if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
-                    else ok = false;
-                }
                 if (ri == 0 && r2 == 0 && lft == cpk) MOE_TRACE_CLOCK(2, 10);
-                if (ok) {
-                    const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
-#pragma unroll 2
-                    for (int i = 0; i < n; ++i)
-                        chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, bon, a0, a1);
-                }
-                __syncwarp();
+                segment(n, bp, bon, a0, a1);
                 bp += n * 128;
                 lft -= n;
-                ++n_con;
-                if (++sl_c == RW) {
-                    sl_c = 0;
-                    par_c ^= 1u;
-                }
-                if (ok) pump(n_con + RW);
             }
             if (ri == 0) MOE_TRACE_CLOCK(2, 11);
             // y = gs * 2^hexp * acc, weighted into the per-token accumulator

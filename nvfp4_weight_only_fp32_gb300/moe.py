@@ -236,7 +236,7 @@ class MoELayer:
 
     `layer` is a dict of canonical tensors (numpy or torch) plus "cfg" with the
     sizes H, E, k, I, S, Is and, optionally, "normalize" (1), "routed_scale"
-    (1.0) and "score_func" ("sigmoid", or "softmax": the three-kernel chain);
+    (1.0) and "score_func" ("sigmoid" or "softmax");
     the weights are repacked into library memory, so the inputs may be freed
     afterwards."""
 

@@ -8,15 +8,18 @@ the library.  This test calls it through the C ABI twice in a row -- a T=8
 Flint-shaped layer, then a T=64 layer with a router bias, the largest T the
 static scratch holds -- and checks each result against the routing that the
 handle-based entry point (moe_decode_forward) returns for the same inputs: ids
-exactly, weights within 1e-5 relative.  It also checks that sizes beyond the
-static limit are refused with a message naming the limit.  The file is named
-so that pytest collects it last."""
+exactly, weights within 1e-5 relative.  Each result is also checked against
+the oracle's routing of the same guarded inputs (the id set exactly, the order
+where neighbouring scores differ by at least the margin, weights within 1e-5
+relative).  It also checks that sizes beyond the static limit are refused with
+a message naming the limit.  The file is named so that pytest collects it
+last."""
 import numpy as np
 import pytest
 import torch
 
 from gpu_util import W_RTOL, load_moe, x_to_device
-from moe_cases import guarded_case
+from moe_cases import MARGIN, guarded_case, sorted_gaps_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +37,7 @@ def _handle_routing(moe, layer, x):
 def test_static_routing_matches_handle_path_twice():
     moe = load_moe()
     cases = [guarded_case(2, 9101), guarded_case(3, 9102)]
-    for layer, x, _ in cases:
+    for layer, x, info in cases:
         c = layer["cfg"]
         ref_ids, ref_w = _handle_routing(moe, layer, x)
         T, k = x.shape[0], c["k"]
@@ -48,6 +51,17 @@ def test_static_routing_matches_handle_path_twice():
         got_ids, got_w = ids.cpu().numpy(), w.cpu().numpy()
         assert np.array_equal(got_ids, ref_ids)
         assert np.all(np.abs(got_w - ref_w) <= W_RTOL * np.abs(ref_w) + 1e-12)
+        # against the oracle (FP64 routing of the same inputs)
+        oids, ow, scores = info["ids"], info["w"], info["scores"]
+        for t in range(T):
+            assert sorted(got_ids[t].tolist()) == sorted(oids[t].tolist()), (t, got_ids[t], oids[t])
+            ok = sorted_gaps_ok(scores[t], oids[t], MARGIN)
+            for j in range(len(ok)):
+                if ok[j] and (j == 0 or ok[j - 1]):
+                    assert got_ids[t][j] == oids[t][j], (t, j, got_ids[t], oids[t])
+            for j, e in enumerate(got_ids[t].tolist()):
+                jo = oids[t].tolist().index(e)
+                assert abs(got_w[t][j] - ow[t][jo]) <= W_RTOL * abs(ow[t][jo]) + 1e-12, (t, j)
 
 
 def test_static_routing_refuses_sizes_beyond_its_scratch():
