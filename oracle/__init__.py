@@ -54,7 +54,18 @@ class _Layer(ctypes.Structure):
         ("sw13", ctypes.c_void_p), ("sw13_sf", ctypes.c_void_p), ("sw13_gs", ctypes.c_void_p),
         ("sw2", ctypes.c_void_p), ("sw2_sf", ctypes.c_void_p), ("sw2_gs", ctypes.c_void_p),
         ("score_func", ctypes.c_int),
+        ("efmt", ctypes.c_int), ("sfmt", ctypes.c_int),
     ]
+
+
+# Expert weight formats (see oracle.c): name -> code.
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "fp8_block": 2, "mxfp8": 3}
+
+
+def format_code(name: str) -> int:
+    if name not in FORMATS:
+        raise ValueError(f"unknown expert format {name!r}")
+    return FORMATS[name]
 
 
 def _load(path):
@@ -101,6 +112,10 @@ def _declare(L):
     L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
     L.orc_dequant.restype = None
     L.orc_dequant.argtypes = [vp, vp, ctypes.c_float, i, i, vp]
+    L.orc_dequant_fmt.restype = None
+    L.orc_dequant_fmt.argtypes = [i, vp, vp, ctypes.c_float, i, i, vp]
+    L.orc_e8m0.restype = d
+    L.orc_e8m0.argtypes = [i]
     L.orc_route.restype = i
     L.orc_route.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp]
     L.orc_forward.restype = i
@@ -124,17 +139,22 @@ class _Bound:
 
     def __init__(self, layer: dict):
         self.arrs = {}
-        for name, dt in [("router_w", np.float32), ("router_b", np.float32),
-                         ("w13", np.uint8), ("w13_sf", np.uint8), ("w13_gs", np.float32),
-                         ("w2", np.uint8), ("w2_sf", np.uint8), ("w2_gs", np.float32),
-                         ("sw13", np.uint8), ("sw13_sf", np.uint8), ("sw13_gs", np.float32),
-                         ("sw2", np.uint8), ("sw2_sf", np.uint8), ("sw2_gs", np.float32)]:
-            self.arrs[name] = _c(layer.get(name), dt)
         c = layer["cfg"]
+        efmt = format_code(c.get("efmt", "nvfp4"))
+        sfmt = format_code(c.get("sfmt", "nvfp4"))
+        # FP8 block scales are FP32; every other scale is one byte per block
+        esf = np.float32 if efmt == FORMATS["fp8_block"] else np.uint8
+        ssf = np.float32 if sfmt == FORMATS["fp8_block"] else np.uint8
+        for name, dt in [("router_w", np.float32), ("router_b", np.float32),
+                         ("w13", np.uint8), ("w13_sf", esf), ("w13_gs", np.float32),
+                         ("w2", np.uint8), ("w2_sf", esf), ("w2_gs", np.float32),
+                         ("sw13", np.uint8), ("sw13_sf", ssf), ("sw13_gs", np.float32),
+                         ("sw2", np.uint8), ("sw2_sf", ssf), ("sw2_gs", np.float32)]:
+            self.arrs[name] = _c(layer.get(name), dt)
         self.s = _Layer(H=c["H"], E=c["E"], k=c["k"], I=c["I"], S=c["S"], Is=c["Is"],
                         normalize=int(c.get("normalize", 1)),
                         routed_scale=float(c.get("routed_scale", 1.0)),
-                        score_func=score_func_code(c),
+                        score_func=score_func_code(c), efmt=efmt, sfmt=sfmt,
                         **{n: _ptr(a) for n, a in self.arrs.items()})
 
 
@@ -152,6 +172,10 @@ def e2m1(code: int) -> float:
 
 def e4m3(code: int) -> float:
     return lib().orc_e4m3(int(code))
+
+
+def e8m0(code: int) -> float:
+    return lib().orc_e8m0(int(code))
 
 
 def bf16_round(v: float) -> float:
@@ -175,6 +199,19 @@ def dequant(codes: np.ndarray, sf: np.ndarray, gs: float) -> np.ndarray:
     assert sf.shape == (rows, cols // 16)
     out = np.empty((rows, cols), dtype=np.float32)
     lib().orc_dequant(_ptr(codes), _ptr(sf), ctypes.c_float(gs), rows, cols, _ptr(out))
+    return out
+
+
+def dequant_fmt(fmt: str, codes: np.ndarray, sf: np.ndarray, gs: float, rows: int, cols: int) -> np.ndarray:
+    """One [rows, cols] matrix of any expert format -> FP32 (gs: NVFP4 only).
+    codes: [rows, cols/2] (FP4) or [rows, cols] (FP8) bytes; sf: [rows,
+    cols/16] E4M3 (NVFP4), [rows, cols/32] E8M0 (MX), or FP32 [ceil(rows/128),
+    ceil(cols/128)] (FP8 block)."""
+    f = format_code(fmt)
+    codes = _c(codes, np.uint8)
+    sf = _c(sf, np.float32 if fmt == "fp8_block" else np.uint8)
+    out = np.empty((rows, cols), dtype=np.float32)
+    lib().orc_dequant_fmt(f, _ptr(codes), _ptr(sf), ctypes.c_float(gs), rows, cols, _ptr(out))
     return out
 
 

@@ -52,7 +52,22 @@
  *    over the chosen ones when asked (then exp(z_j - z_max) / sum over the
  *    chosen of exp(z_i - z_max)), times the routed scale.
  *  - Router bias, when present, is added to the logit (plain linear layer).
- *  - Shared experts: ungated, weight 1, same NVFP4 format.
+ *  - Shared experts: ungated, weight 1, by default in the same NVFP4 format.
+ *  - Other expert formats (the routed experts and the shared ones each have
+ *    one; element k of a row is the k-th along K, as above):
+ *      MXFP4  ([ML4] "MXFP4 experts at load, one layer at a time": E2M1 values
+ *             with one E8M0 scale per 32 values): W = e2m1 * 2^(s - 127), no
+ *             tensor scale; E8M0 code 255 is NaN.
+ *      FP8 block-scaled ([ML4] "Highlights": the NVFP4 checkpoint keeps its
+ *             shared experts in FP8 with block-scaled weights; the block is
+ *             not given, and the reading here is 128 x 128): E4M3 (fn) codes,
+ *             one byte per element, and one FP32 scale per 128 x 128 block of
+ *             the stored [rows, cols] matrix, row-major over the blocks
+ *             ([ceil(rows/128), ceil(cols/128)]): W = e4m3 * scale.
+ *      MXFP8  ([INK2] "Mixed-precision MoE and Four-Over-Six NVFP4": the last
+ *             8 layers' experts are MXFP8): E4M3 (fn) codes with one E8M0
+ *             scale per 32 values along K: W = e4m3 * 2^(s - 127).
+ *    Every product is exact in FP64 (at most 4 + 24 significant bits).
  *  - SwiGLU: h = silu(gate) * up, silu(z) = z / (1 + exp(-z)); h is rounded to
  *    BF16 (round to nearest even) before the down projection.
  *  - Output: sum of routing-weighted routed outputs plus the shared outputs,
@@ -67,7 +82,9 @@
  * a separate library, so that a test can show that the pins catch it:
  *   1 softmax scores replaced by sigmoid, 2 normalisation ignored,
  *   3 gate and up rows swapped, 4 shared experts dropped from the combine,
- *   5 E2M1 subnormal (code 1) decoded as 1.0 instead of 0.5.
+ *   5 E2M1 subnormal (code 1) decoded as 1.0 instead of 0.5,
+ *   6 MX scales taken per 16 elements instead of per 32,
+ *   7 FP8 block scales indexed with rows and columns swapped.
  * The regular build plants nothing. */
 #ifndef ORC_PLANT
 #define ORC_PLANT 0
@@ -145,6 +162,31 @@ uint16_t orc_double_to_bf16(double v)
     return (uint16_t)(u >> 16);
 }
 
+/* E8M0 (the MX block scale): an unsigned biased exponent, value 2^(c - 127);
+ * code 255 is NaN.  No sign, no mantissa. */
+double orc_e8m0(int code)
+{
+    if ((code & 255) == 255) return NAN;
+    return ldexp(1.0, (code & 255) - 127);
+}
+
+/* Expert weight formats. */
+enum { ORC_NVFP4 = 0, ORC_MXFP4 = 1, ORC_FP8_BLOCK = 2, ORC_MXFP8 = 3 };
+
+/* Bytes of the codes and of the scales of one [rows, cols] matrix. */
+size_t orc_codes_bytes(int fmt, int rows, int cols)
+{
+    return (fmt == ORC_NVFP4 || fmt == ORC_MXFP4) ? (size_t)rows * (cols / 2) : (size_t)rows * cols;
+}
+size_t orc_scale_bytes(int fmt, int rows, int cols)
+{
+    switch (fmt) {
+    case ORC_NVFP4: return (size_t)rows * (cols / 16);
+    case ORC_FP8_BLOCK: return (size_t)((rows + 127) / 128) * ((cols + 127) / 128) * sizeof(float);
+    default: return (size_t)rows * (cols / 32);
+    }
+}
+
 /* Code nibble of element k in a K-major packed row (element 2j low nibble). */
 static inline int nib(const uint8_t *row, int k)
 {
@@ -173,6 +215,28 @@ static inline double wexact(const uint8_t *codes, const uint8_t *sf, double gs,
     return tab_e2m1[nib(row, k)] * tab_e4m3[sc] * gs;
 }
 
+/* The same in any expert format (gs is used by NVFP4 only). */
+static inline double wexact_fmt(int fmt, const uint8_t *codes, const uint8_t *sf, double gs,
+                                int cols, int r, int k)
+{
+    const int mxb = ORC_PLANT == 6 ? 16 : 32;   /* elements per MX scale */
+    switch (fmt) {
+    case ORC_MXFP4:
+        return tab_e2m1[nib(codes + (size_t)r * (cols / 2), k)] *
+               orc_e8m0(sf[(size_t)r * (cols / 32) + k / mxb]);
+    case ORC_FP8_BLOCK: {
+        const float *bs = (const float *)sf;
+        const int nbc = (cols + 127) / 128;
+        const size_t bi = ORC_PLANT == 7 ? (size_t)(k / 128) * nbc + r / 128 : (size_t)(r / 128) * nbc + k / 128;
+        return tab_e4m3[codes[(size_t)r * cols + k]] * (double)bs[bi];
+    }
+    case ORC_MXFP8:
+        return tab_e4m3[codes[(size_t)r * cols + k]] * orc_e8m0(sf[(size_t)r * (cols / 32) + k / mxb]);
+    default:
+        return wexact(codes, sf, gs, cols, r, k);
+    }
+}
+
 /* Dequantise a [rows, cols] NVFP4 matrix to FP32: one rounding of the exact
  * product e2m1 * e4m3 * gs. */
 void orc_dequant(const uint8_t *codes, const uint8_t *sf, float gs,
@@ -182,6 +246,17 @@ void orc_dequant(const uint8_t *codes, const uint8_t *sf, float gs,
     for (int r = 0; r < rows; ++r)
         for (int k = 0; k < cols; ++k)
             out[(size_t)r * cols + k] = (float)wexact(codes, sf, (double)gs, cols, r, k);
+}
+
+/* Dequantise a [rows, cols] matrix of any expert format to FP32: one
+ * rounding of the exact value (gs: NVFP4 only). */
+void orc_dequant_fmt(int fmt, const uint8_t *codes, const uint8_t *sf, float gs,
+                     int rows, int cols, float *out)
+{
+    fill_tables();
+    for (int r = 0; r < rows; ++r)
+        for (int k = 0; k < cols; ++k)
+            out[(size_t)r * cols + k] = (float)wexact_fmt(fmt, codes, sf, (double)gs, cols, r, k);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -207,6 +282,7 @@ typedef struct {
     const uint8_t *sw2_sf;      /* [S, H, Is/16] */
     const float *sw2_gs;        /* [S] */
     int score_func;             /* 0: sigmoid per expert; 1: softmax over all experts */
+    int efmt, sfmt;             /* weight format of the routed / shared experts (ORC_*) */
 } orc_layer;
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
@@ -283,24 +359,27 @@ int orc_route(const orc_layer *L, const uint16_t *x, int T, int *ids, double *w,
  *   h_n = bf16(silu(g_n) * u_n)
  *   y_m = sum_n h_n Wd[m,n]
  * All weights are the exact dequantised values. */
-static void expert_mlp(int H, int I,
+static void expert_mlp(int fmt, int H, int I,
                        const uint8_t *w13, const uint8_t *w13_sf, const float *w13_gs,
-                       const uint8_t *w2, const uint8_t *w2_sf, float w2_gs,
+                       const uint8_t *w2, const uint8_t *w2_sf, const float *w2_gs,
                        const double *x, double *h, double *y)
 {
-    double gsg = (double)w13_gs[0], gsu = (double)w13_gs[1], gsd = (double)w2_gs;
+    /* tensor scales: NVFP4 only */
+    const int nv = fmt == ORC_NVFP4;
+    double gsg = nv ? (double)w13_gs[0] : 1.0, gsu = nv ? (double)w13_gs[1] : 1.0;
+    double gsd = nv ? (double)w2_gs[0] : 1.0;
     for (int n = 0; n < I; ++n) {
         double g = 0.0, u = 0.0;
         for (int k = 0; k < H; ++k) {
-            g += x[k] * wexact(w13, w13_sf, gsg, H, ORC_PLANT == 3 ? I + n : n, k);
-            u += x[k] * wexact(w13, w13_sf, gsu, H, ORC_PLANT == 3 ? n : I + n, k);
+            g += x[k] * wexact_fmt(fmt, w13, w13_sf, gsg, H, ORC_PLANT == 3 ? I + n : n, k);
+            u += x[k] * wexact_fmt(fmt, w13, w13_sf, gsu, H, ORC_PLANT == 3 ? n : I + n, k);
         }
         double silu = g * sigmoid(g);
         h[n] = orc_bf16_round(silu * u);
     }
     for (int m = 0; m < H; ++m) {
         double acc = 0.0;
-        for (int n = 0; n < I; ++n) acc += h[n] * wexact(w2, w2_sf, gsd, I, m, n);
+        for (int n = 0; n < I; ++n) acc += h[n] * wexact_fmt(fmt, w2, w2_sf, gsd, I, m, n);
         y[m] = acc;
     }
 }
@@ -341,19 +420,25 @@ int orc_forward(const orc_layer *L, const uint16_t *x, int T, uint16_t *out,
         const double *xt = xd + (size_t)t * H;
         if (j < K) {
             int e = ids[(size_t)t * K + j];
-            int I = L->I;
-            expert_mlp(H, I,
-                       L->w13 + (size_t)e * 2 * I * (H / 2), L->w13_sf + (size_t)e * 2 * I * (H / 16),
-                       L->w13_gs + 2 * (size_t)e,
-                       L->w2 + (size_t)e * H * (I / 2), L->w2_sf + (size_t)e * H * (I / 16),
-                       L->w2_gs[e], xt, h, yp);
+            int I = L->I, f = L->efmt;
+            int nv = f == ORC_NVFP4;
+            expert_mlp(f, H, I,
+                       L->w13 + (size_t)e * orc_codes_bytes(f, 2 * I, H),
+                       L->w13_sf + (size_t)e * orc_scale_bytes(f, 2 * I, H),
+                       nv ? L->w13_gs + 2 * (size_t)e : NULL,
+                       L->w2 + (size_t)e * orc_codes_bytes(f, H, I),
+                       L->w2_sf + (size_t)e * orc_scale_bytes(f, H, I),
+                       nv ? L->w2_gs + e : NULL, xt, h, yp);
         } else {
-            int sidx = j - K, I = L->Is;
-            expert_mlp(H, I,
-                       L->sw13 + (size_t)sidx * 2 * I * (H / 2), L->sw13_sf + (size_t)sidx * 2 * I * (H / 16),
-                       L->sw13_gs + 2 * (size_t)sidx,
-                       L->sw2 + (size_t)sidx * H * (I / 2), L->sw2_sf + (size_t)sidx * H * (I / 16),
-                       L->sw2_gs[sidx], xt, h, yp);
+            int sidx = j - K, I = L->Is, f = L->sfmt;
+            int nv = f == ORC_NVFP4;
+            expert_mlp(f, H, I,
+                       L->sw13 + (size_t)sidx * orc_codes_bytes(f, 2 * I, H),
+                       L->sw13_sf + (size_t)sidx * orc_scale_bytes(f, 2 * I, H),
+                       nv ? L->sw13_gs + 2 * (size_t)sidx : NULL,
+                       L->sw2 + (size_t)sidx * orc_codes_bytes(f, H, I),
+                       L->sw2_sf + (size_t)sidx * orc_scale_bytes(f, H, I),
+                       nv ? L->sw2_gs + sidx : NULL, xt, h, yp);
         }
         free(h);
     }

@@ -8,6 +8,7 @@ import pytest
 
 import test_oracle_formats as fmt
 import test_oracle_layer as lay
+import test_oracle_mxfp8 as mx
 import test_oracle_routing as rt
 
 CASES = [
@@ -22,6 +23,12 @@ CASES = [
      [lay.test_shared_expert_only, lay.test_closed_form_two_experts_and_shared]),
     (5, "E2M1 subnormal decoded as 1.0",
      [fmt.test_e2m1_golden_file, fmt.test_e2m1_table_exhaustive]),
+    (6, "MX scales taken per 16 elements instead of per 32",
+     [lambda orc: mx.test_dequant_matches_nvfp4_on_shared_values(orc, "mxfp4"),
+      lambda orc: mx.test_layer_matches_nvfp4_on_shared_values(orc, "mxfp8", "mxfp8")]),
+    (7, "FP8 block scales indexed with rows and columns swapped",
+     [lambda orc: mx.test_dequant_matches_nvfp4_on_shared_values(orc, "fp8_block"),
+      mx.test_fp8_block_single_expert_equals_dense_mlp]),
 ]
 
 
@@ -33,7 +40,7 @@ def test_planted_mistake_is_caught(orc, plant, what, pins):
             try:
                 pin(orc)
             except AssertionError:
-                caught.append(pin.__name__)
+                caught.append(getattr(pin, "__name__", "pin"))
     assert caught, f"no pin caught the planted mistake: {what}"
     # and the regular oracle is back
     assert orc.e2m1(1) == 0.5
