@@ -39,6 +39,10 @@ WORKLOADS = {
     "ml4": (4, 6),
     "zipf64": (3, 16),
     "tiny": (0, 64),
+    "ml4fp8s": (5, 6),        # ML4 with its FP8 block-scaled shared expert
+    "inkling": (6, 2),        # Inkling-2-Small-shaped, NVFP4 experts
+    "inkling_mx8": (7, 2),    # the same with MXFP8 experts
+    "flint_mx4": (8, 47),     # Flint-shaped, MXFP4 experts
 }
 
 # DRAM bytes (read + write) per launch of the single-launch kernel, from one
@@ -69,7 +73,7 @@ def parse():
     ap.add_argument("--workload", default="flint1", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=0, help="override layers per step")
     ap.add_argument("--secondary", default="flint8", help="second workload reported in the line ('' = none)")
-    ap.add_argument("--extras", default="ml4,zipf64,zipf64-gemv,tiny",
+    ap.add_argument("--extras", default="ml4,zipf64,zipf64-gemv,tiny,ml4fp8s,inkling,inkling_mx8,flint_mx4",
                     help="further workloads timed and reported under 'workloads' ('' = none); "
                          "zipf64-gemv is zipf64 with the grouped kernels off")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -500,14 +504,15 @@ def run_gpu(args):
         c2 = ch2.c
         one = ch2.layers[0].info().single_launch_max_tokens >= ch2.T
         res = {"workload": f"{c2['name']}: T={c2['T']} H={c2['H']} E={c2['E']} top-{c2['k']} "
-                           f"I={c2['I']} +{c2['S']} shared, {oL} layers per step",
+                           f"I={c2['I']} +{c2['S']} shared, experts {c2['efmt']}, shared {c2['sfmt']}, "
+                           f"{oL} layers per step",
                "us_per_layer": us2, "GBps": b2 / (us2 * 1e-6) / 1e9,
                "frac_of_measured": b2 / (us2 * 1e-6) / 1e9 / peak,
                "selected_bytes_per_layer": b2, "unique_experts_mean": float(np.mean(U2)),
                "path": "single launch" if one else
                        ("chain" + (", grouped kernels off" if grouped_min < 0 else
-                                   (", grouped tensor-core kernels for slots of >= 8 tokens" if c2["T"] > 8
-                                    else ""))),
+                                   (", grouped tensor-core kernels for slots of >= 8 tokens"
+                                    if c2["T"] > 8 and "fp8" not in c2["efmt"] + c2["sfmt"] else ""))),
                "steps": st2}
         ch2.close()
         del g2

@@ -60,6 +60,38 @@ typedef enum {
     MOE_ERR_DEVICE = -6         /* the sticky device error word was set */
 } moe_status;
 
+/* Expert weight formats (moe_config.expert_format / shared_format).  The
+ * codes and scales of a [rows, cols] matrix (cols = K, the input size):
+ *   MOE_FMT_NVFP4      codes uint8 [rows, cols/2] E2M1, element 2j in the low
+ *                      nibble of byte j; scales uint8 [rows, cols/16] E4M3
+ *                      (fn), one per 16 elements; one FP32 tensor scale per
+ *                      matrix (gate and up separately).  W = e2m1*e4m3*gs.
+ *   MOE_FMT_MXFP4      codes as NVFP4; scales uint8 [rows, cols/32] E8M0, one
+ *                      per 32 elements; no tensor scale.  W = e2m1*2^(s-127).
+ *                      "Day 0 support for Mistral Large 4 on vLLM", "MXFP4
+ *                      experts at load, one layer at a time".  Repacked
+ *                      exactly into the NVFP4 layout: the E8M0 codes of one
+ *                      matrix (of the gate or the up half) must span at most
+ *                      17 octaves, else moe_init returns MOE_ERR_UNSUPPORTED.
+ *   MOE_FMT_FP8_BLOCK  codes uint8 [rows, cols] E4M3 (fn); scales FP32
+ *                      [ceil(rows/128), ceil(cols/128)], one per 128 x 128
+ *                      block of the stored matrix, passed through the uint8
+ *                      scale pointer (16-byte aligned).  W = e4m3*scale.  The
+ *                      Mistral Large 4 page, "Highlights": its NVFP4
+ *                      checkpoint keeps the shared experts in block-scaled FP8
+ *                      (the page gives no block size; 128 x 128 is read).
+ *   MOE_FMT_MXFP8      codes as FP8_BLOCK; scales uint8 [rows, cols/32] E8M0.
+ *                      W = e4m3*2^(s-127).  "Inkling 2 Small on vLLM: Day-0
+ *                      Support", "Mixed-precision MoE and Four-Over-Six NVFP4"
+ *                      (its last eight layers' experts).
+ * The tensor-scale pointers (w13_gs, w2_gs, ...) are read for NVFP4 only and
+ * may be NULL otherwise.  Experts in an FP8 format run on the GEMV kernels
+ * and the single launch, never on the grouped tensor-core kernels. */
+#define MOE_FMT_NVFP4 0
+#define MOE_FMT_MXFP4 1
+#define MOE_FMT_FP8_BLOCK 2
+#define MOE_FMT_MXFP8 3
+
 /* Layer configuration (host struct).
  * Supported (anything else -> MOE_ERR_UNSUPPORTED with every reason listed;
  * default-deny, as the Mistral Large 4 page's "Fail-stop" section describes
@@ -69,7 +101,8 @@ typedef enum {
  *   1 <= top_k <= 8, top_k <= num_experts <= 512
  *   0 <= num_shared <= 2
  *   1 <= max_tokens <= 64
- *   normalize_topk in {0, 1}, score_func in {0, 1}, routed_scale finite      */
+ *   normalize_topk in {0, 1}, score_func in {0, 1}, routed_scale finite
+ *   expert_format, shared_format in MOE_FMT_*                                */
 typedef struct {
     int hidden;             /* H */
     int num_experts;        /* E routed experts */
@@ -99,10 +132,13 @@ typedef struct {
                                when normalize_topk = 1 (for softmax:
                                exp(z_j - z_max) / sum over the chosen of
                                exp(z_i - z_max)), times routed_scale. */
+    int expert_format;      /* MOE_FMT_* of the routed experts (0 = NVFP4) */
+    int shared_format;      /* MOE_FMT_* of the shared experts (0 = NVFP4) */
 } moe_config;
 
 /* Weights in the canonical layout (device pointers, only read during
- * moe_init; the caller may free them afterwards).
+ * moe_init; the caller may free them afterwards).  Shapes below are those of
+ * NVFP4; the other formats' codes and scales follow MOE_FMT_* above.
  *   router_w  FP32 [E, H] row-major
  *   router_b  FP32 [E] or NULL (added to the logit)
  *   w13       uint8 [E, 2I, H/2]   E2M1 codes, row-major over K; element 2j in
@@ -137,7 +173,7 @@ typedef struct {
 typedef struct {
     size_t weight_bytes;     /* repacked expert weights + router, device */
     size_t workspace_bytes;  /* per-call scratch, device */
-    size_t expert_bytes;     /* bytes one routed expert's NVFP4 weights occupy */
+    size_t expert_bytes;     /* bytes one routed expert's repacked weights occupy */
     size_t shared_bytes;     /* the same for one shared expert */
     int max_slots;           /* worst-case number of distinct experts per call */
     int sm_count;            /* SMs of the device the handle lives on */

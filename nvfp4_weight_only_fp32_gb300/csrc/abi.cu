@@ -84,6 +84,10 @@ std::vector<std::string> unsupported_reasons(const moe_config *c) {
     chk(c->normalize_topk == 0 || c->normalize_topk == 1, "normalize_topk must be 0 or 1");
     chk(std::isfinite(c->routed_scale), "routed_scale must be finite");
     chk(c->score_func == 0 || c->score_func == 1, "score_func must be 0 (sigmoid) or 1 (softmax)");
+    chk(c->expert_format >= MOE_FMT_NVFP4 && c->expert_format <= MOE_FMT_MXFP8,
+        "expert_format must be 0 (NVFP4), 1 (MXFP4), 2 (FP8 block) or 3 (MXFP8)");
+    chk(c->shared_format >= MOE_FMT_NVFP4 && c->shared_format <= MOE_FMT_MXFP8,
+        "shared_format must be 0 (NVFP4), 1 (MXFP4), 2 (FP8 block) or 3 (MXFP8)");
     return why;
 }
 
@@ -134,10 +138,10 @@ void carve_weights(moe_layer *L, char *base) {
     d.router_w = cv.take<float>((size_t)E * H);
     d.router_b = nullptr;
     L->router_b_slot = cv.take<float>(E);
-    d.e13_stride = repacked_bytes(2 * I, H);
-    d.e2_stride = repacked_bytes(H, I);
-    d.s13_stride = repacked_bytes(2 * Is, H);
-    d.s2_stride = repacked_bytes(H, Is);
+    d.e13_stride = repacked_bytes(2 * I, H, d.f8e);
+    d.e2_stride = repacked_bytes(H, I, d.f8e);
+    d.s13_stride = repacked_bytes(2 * Is, H, d.f8s);
+    d.s2_stride = repacked_bytes(H, Is, d.f8s);
     d.w13r = cv.take<uint8_t>((size_t)E * d.e13_stride);
     d.w2r = cv.take<uint8_t>((size_t)E * d.e2_stride);
     d.gs13 = cv.take<float>((size_t)E * 2);
@@ -187,6 +191,101 @@ void carve_workspace(moe_layer *L, char *base) {
     L->ids_stage = cv.take<int>((size_t)Tm * K);
     L->w_stage = cv.take<float>((size_t)Tm * K);
     L->wsbytes = cv.off;
+}
+
+bool is_f8(int fmt) { return fmt == MOE_FMT_FP8_BLOCK || fmt == MOE_FMT_MXFP8; }
+
+// Repack one expert group (n experts of intermediate size I) from the
+// caller's canonical tensors in format `fmt` into the library's chunks, and
+// set the group's tensor scales (device gs13 [n,2] / gs2 [n] and their host
+// copies): the caller's for NVFP4; 1 for the FP8 formats (their scales live
+// in the chunks); for MXFP4 the power of two by which each matrix half's
+// E8M0 scales are shifted into E4M3's range, exactly (the repack then is
+// NVFP4).  MXFP4 needs the E8M0 codes of one matrix half to span at most 17
+// octaves (the powers of two E4M3 holds) and no NaN code; otherwise the
+// reasons are appended to `why`.  Synchronises `st` for MXFP4.
+cudaError_t repack_group(int fmt, int n, int H, int I, const uint8_t *w13, const uint8_t *w13_sf,
+                         const float *w13_gs, const uint8_t *w2, const uint8_t *w2_sf, const float *w2_gs,
+                         uint8_t *d13, uint8_t *d2, float *gs13, float *gs2, std::vector<float> &gs13_h,
+                         std::vector<float> &gs2_h, const char *what, std::vector<std::string> &why,
+                         cudaStream_t st) {
+    gs13_h.assign((size_t)n * 2, 1.f);
+    gs2_h.assign((size_t)n, 1.f);
+    if (n <= 0) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    if (fmt == MOE_FMT_NVFP4) {
+        e = cudaMemcpyAsync(gs13, w13_gs, (size_t)n * 2 * sizeof(float), cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(gs2, w2_gs, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess) e = launch_repack(w13, w13_sf, n, 2 * I, H, true, d13, st);
+        if (e == cudaSuccess) e = launch_repack(w2, w2_sf, n, H, I, false, d2, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(gs13_h.data(), w13_gs, (size_t)n * 2 * sizeof(float), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(gs2_h.data(), w2_gs, (size_t)n * sizeof(float), cudaMemcpyDeviceToHost, st);
+        return e;
+    }
+    if (is_f8(fmt)) {
+        e = cudaMemcpyAsync(gs13, gs13_h.data(), (size_t)n * 2 * sizeof(float), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(gs2, gs2_h.data(), (size_t)n * sizeof(float), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = launch_repack_f8(w13, w13_sf, fmt, n, 2 * I, H, true, d13, st);
+        if (e == cudaSuccess) e = launch_repack_f8(w2, w2_sf, fmt, n, H, I, false, d2, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);   // the host ones above are read by the copies
+        return e;
+    }
+    // MXFP4: scale ranges -> offsets -> NVFP4 scales, then the NVFP4 repack
+    int *mm = nullptr, *offs = nullptr;
+    uint8_t *sf13 = nullptr, *sf2 = nullptr;
+    std::vector<int> mm_h((size_t)n * 2 * 3 * 2), offs_h((size_t)n * 2 * 2);
+    e = cudaMalloc(&mm, mm_h.size() * sizeof(int));
+    if (e == cudaSuccess) e = cudaMalloc(&offs, offs_h.size() * sizeof(int));
+    if (e == cudaSuccess) e = cudaMalloc(&sf13, (size_t)n * 2 * I * (H / 16));
+    if (e == cudaSuccess) e = cudaMalloc(&sf2, (size_t)n * H * (I / 16));
+    if (e == cudaSuccess) e = launch_mx_scale_range(w13_sf, n, 2 * I, H, true, mm, st);
+    if (e == cudaSuccess) e = launch_mx_scale_range(w2_sf, n, H, I, false, mm + (size_t)n * 2 * 3, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(mm_h.data(), mm, mm_h.size() * sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    bool bad = false;
+    if (e == cudaSuccess) {
+        for (int m = 0; m < 2; ++m) {        // 0 gate/up, 1 down
+            for (int x = 0; x < n; ++x) {
+                for (int h = 0; h < (m == 0 ? 2 : 1); ++h) {
+                    const int *r = mm_h.data() + (size_t)m * n * 2 * 3 + ((size_t)x * 2 + h) * 3;
+                    const char *mat = m == 0 ? (h == 0 ? "gate" : "up") : "down";
+                    if (r[2]) {
+                        why.push_back(std::string(what) + " expert " + std::to_string(x) + " " + mat +
+                                      ": E8M0 scale code 255 (NaN)");
+                        bad = true;
+                    } else if (r[1] - r[0] > 17) {
+                        why.push_back(std::string(what) + " expert " + std::to_string(x) + " " + mat +
+                                      ": E8M0 scales span " + std::to_string(r[1] - r[0]) +
+                                      " octaves (at most 17 convert exactly)");
+                        bad = true;
+                    }
+                    // the largest scale maps to 2^8, the largest power of two of E4M3
+                    const int off = r[1] - 127 - 8;
+                    offs_h[(size_t)m * n * 2 + (size_t)x * 2 + h] = off;
+                    const float g = ldexpf(1.f, off);
+                    if (m == 0) gs13_h[(size_t)x * 2 + h] = g;
+                    else gs2_h[x] = g;
+                }
+            }
+        }
+    }
+    if (e == cudaSuccess && !bad) {
+        e = cudaMemcpyAsync(offs, offs_h.data(), offs_h.size() * sizeof(int), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = launch_mx_to_nv_scales(w13_sf, offs, n, 2 * I, H, true, sf13, st);
+        if (e == cudaSuccess) e = launch_mx_to_nv_scales(w2_sf, offs + (size_t)n * 2, n, H, I, false, sf2, st);
+        if (e == cudaSuccess) e = launch_repack(w13, sf13, n, 2 * I, H, true, d13, st);
+        if (e == cudaSuccess) e = launch_repack(w2, sf2, n, H, I, false, d2, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(gs13, gs13_h.data(), (size_t)n * 2 * sizeof(float), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(gs2, gs2_h.data(), (size_t)n * sizeof(float), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    cudaFree(mm);
+    cudaFree(offs);
+    cudaFree(sf13);
+    cudaFree(sf2);
+    return e;
 }
 
 // The single launch tags the words its blocks exchange with the call number
@@ -246,17 +345,21 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     if (w->router_b) need(w->router_b, "router_b");
     need(w->w13, "w13");
     need(w->w13_sf, "w13_sf");
-    need(w->w13_gs, "w13_gs");
     need(w->w2, "w2");
     need(w->w2_sf, "w2_sf");
-    need(w->w2_gs, "w2_gs");
+    if (cfg->expert_format == MOE_FMT_NVFP4) {   // tensor scales: NVFP4 only
+        need(w->w13_gs, "w13_gs");
+        need(w->w2_gs, "w2_gs");
+    }
     if (S > 0) {
         need(w->sw13, "sw13");
         need(w->sw13_sf, "sw13_sf");
-        need(w->sw13_gs, "sw13_gs");
         need(w->sw2, "sw2");
         need(w->sw2_sf, "sw2_sf");
-        need(w->sw2_gs, "sw2_gs");
+        if (cfg->shared_format == MOE_FMT_NVFP4) {
+            need(w->sw13_gs, "sw13_gs");
+            need(w->sw2_gs, "sw2_gs");
+        }
     }
     if (!bad.empty()) return fail(MOE_ERR_INVALID_ARG, join(bad));
 
@@ -288,6 +391,8 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     d.Imax = std::max(I, Is);
     d.grouped_min = 0;   // set once the shape is known to suit the grouped kernels
     d.debug_stall = 0;
+    d.f8e = is_f8(cfg->expert_format);
+    d.f8s = S > 0 && is_f8(cfg->shared_format);
 
     carve_weights(L, nullptr);
     carve_workspace(L, nullptr);
@@ -317,38 +422,31 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
         cp(L->router_b_slot, w->router_b, (size_t)E * sizeof(float));
         d.router_b = L->router_b_slot;
     }
-    cp(d.gs13, w->w13_gs, (size_t)E * 2 * sizeof(float));
-    cp(d.gs2, w->w2_gs, (size_t)E * sizeof(float));
-    if (S > 0) {
-        cp(d.sgs13, w->sw13_gs, (size_t)S * 2 * sizeof(float));
-        cp(d.sgs2, w->sw2_gs, (size_t)S * sizeof(float));
+    std::vector<std::string> fmt_why;
+    if (e == cudaSuccess)
+        e = repack_group(cfg->expert_format, E, H, I, w->w13, w->w13_sf, w->w13_gs, w->w2, w->w2_sf, w->w2_gs,
+                         const_cast<uint8_t *>(d.w13r), const_cast<uint8_t *>(d.w2r), const_cast<float *>(d.gs13),
+                         const_cast<float *>(d.gs2), L->gs13_h, L->gs2_h, "routed", fmt_why, st);
+    if (e == cudaSuccess)
+        e = repack_group(cfg->shared_format, S, H, Is, w->sw13, w->sw13_sf, w->sw13_gs, w->sw2, w->sw2_sf,
+                         w->sw2_gs, const_cast<uint8_t *>(d.sw13r), const_cast<uint8_t *>(d.sw2r),
+                         const_cast<float *>(d.sgs13), const_cast<float *>(d.sgs2), L->sgs13_h, L->sgs2_h,
+                         "shared", fmt_why, st);
+    if (e == cudaSuccess && !fmt_why.empty()) {
+        cudaStreamSynchronize(st);
+        cudaFree(L->wmem);
+        cudaFree(L->wsmem);
+        delete L;
+        return fail(MOE_ERR_UNSUPPORTED, join(fmt_why));
     }
     if (e == cudaSuccess) e = launch_pack_scales(d, st);
-    if (e == cudaSuccess)
-        e = launch_repack(w->w13, w->w13_sf, E, 2 * I, H, true, const_cast<uint8_t *>(d.w13r), st);
-    if (e == cudaSuccess)
-        e = launch_repack(w->w2, w->w2_sf, E, H, I, false, const_cast<uint8_t *>(d.w2r), st);
-    if (e == cudaSuccess && S > 0)
-        e = launch_repack(w->sw13, w->sw13_sf, S, 2 * Is, H, true, const_cast<uint8_t *>(d.sw13r), st);
-    if (e == cudaSuccess && S > 0)
-        e = launch_repack(w->sw2, w->sw2_sf, S, H, Is, false, const_cast<uint8_t *>(d.sw2r), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L->wsmem, 0, L->wsbytes, st);
-    L->gs13_h.resize((size_t)E * 2);
-    L->gs2_h.resize(E);
-    L->sgs13_h.resize((size_t)S * 2);
-    L->sgs2_h.resize(S);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(L->gs13_h.data(), w->w13_gs, (size_t)E * 2 * sizeof(float), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(L->gs2_h.data(), w->w2_gs, (size_t)E * sizeof(float), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && S > 0)
-        e = cudaMemcpyAsync(L->sgs13_h.data(), w->sw13_gs, (size_t)S * 2 * sizeof(float), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && S > 0)
-        e = cudaMemcpyAsync(L->sgs2_h.data(), w->sw2_gs, (size_t)S * sizeof(float), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = prepare_kernels();
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->optin_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (L->cfg.grouped_min_tokens > 0 && grouped_supported(d, L->sm_count)) d.grouped_min = L->cfg.grouped_min_tokens;
+    // the grouped tensor-core kernels decode NVFP4 chunks only
+    if (L->cfg.grouped_min_tokens > 0 && !d.f8e && !d.f8s && grouped_supported(d, L->sm_count))
+        d.grouped_min = L->cfg.grouped_min_tokens;
     for (int T = 0; T <= kMaxTokens; ++T) {
         L->fused_ok[T] = 0;
         if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&
@@ -534,7 +632,9 @@ moe_status moe_debug_dequant(moe_layer *L, int which, int expert, float *dst, vo
     }
     DeviceGuard g(L->device);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_dequant(rep, ga, gb, rows, cols, gu, dst, st);
+    const bool f8 = which < 2 ? d.f8e : d.f8s;
+    cudaError_t e = f8 ? launch_dequant_f8(rep, rows, cols, gu, dst, st)
+                       : launch_dequant(rep, ga, gb, rows, cols, gu, dst, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "dequant");
 }

@@ -156,11 +156,12 @@ bool fused_geometry(const DevLayer &d, int T, int G, int dyn_max, FusedGeom &g) 
     g.RW = (int)std::min<size_t>(kRWmax, per_warp / ((size_t)g.CH * kChunkBytes));
     g.total = (int)(P + (size_t)kFW * g.RW * g.CH * kChunkBytes);
     if (g.RW < 2) return false;
-    const int NC13 = d.H / kChunkK, NTs = d.Is / 8, NT13 = d.I / 8;
+    const int NTs = d.Is / 8, NT13 = d.I / 8;
+    const int NC13s = chunks_of(d.H, d.f8s), NC13r = chunks_of(d.H, d.f8e);
     const int ncr = d.I / kChunkK, ncs = d.S > 0 ? d.Is / kChunkK : ncr;
-    g.lks0 = choose_lks(d.S * NTs, NC13, G, kPW);
+    g.lks0 = choose_lks(d.S * NTs, NC13s, G, kPW);
     for (int n = 0; n <= kSlotsF; ++n) {
-        g.lks1[n] = (unsigned char)choose_lks(std::max(0, n - d.S) * NT13, NC13, G, kFW);
+        g.lks1[n] = (unsigned char)choose_lks(std::max(0, n - d.S) * NT13, NC13r, G, kFW);
         int l = 0;
         while (n * (2 << l) <= kFW && ncr % (2 << l) == 0 && ncs % (2 << l) == 0 && ncr / (2 << l) >= 2 &&
                ncs / (2 << l) >= 2)
@@ -379,7 +380,6 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     const float4 *s_gsp = reinterpret_cast<const float4 *>(smem + fg.gs_off);  // copy of d.gsp
     uint8_t *ring = smem + fg.ring_off + (size_t)warp * RW * CH * kChunkBytes;
     uint64_t *bar = s_bar[warp];
-    const int NC13 = H / kChunkK;            // gate/up chunks per tile
     const int NTs = d.Is / 8, NT13 = d.I / 8, NRT = H / 16;
     const uint64_t pol = evict_first_policy();
 
@@ -423,14 +423,19 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     // block gets the floor or the ceiling of units / G (the decode rate of
     // an SM is shared by its warps); with fewer, a block's groups take
     // consecutive units (measured slightly faster at one token).
+    // nc: the pass's chunks per gate/up tile (H/64 NVFP4 chunks or H/32 F8
+    // chunks), f8: its experts' format
     struct Pass {
-        int lks, cpw, cb0, stride, u0, my, NT, lo;
+        int lks, cpw, cb0, stride, u0, my, NT, lo, nc;
+        bool f8;
     };
-    auto plan = [&](int units, int lks, int NT, int lo, int nw, int vw) {
+    auto plan = [&](int units, int lks, int NT, int lo, int nw, int vw, bool f8) {
         Pass p;
         const int ngrp = nw >> lks;
+        p.f8 = f8;
+        p.nc = chunks_of(H, f8);
         p.lks = lks;
-        p.cpw = NC13 >> lks;
+        p.cpw = p.nc >> lks;
         p.cb0 = (vw & ((1 << lks) - 1)) * p.cpw;
         p.stride = G * ngrp;
         p.u0 = units > p.stride ? (vw >> lks) * G + c : c * ngrp + (vw >> lks);
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             const int s = uu / p.NT, r = uu - s * p.NT;
             const int e = s_slot_e[p.lo + s];
             const uint8_t *b = e < 0 ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
-            s_tab_src[warp][base + i] = b + ((size_t)r * NC13 + p.cb0) * kChunkBytes;
+            s_tab_src[warp][base + i] = b + ((size_t)r * p.nc + p.cb0) * kChunkBytes;
             s_tab_n[warp][base + i] = p.cpw;
         }
     };
@@ -471,7 +476,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         fence_proxy_async();
     }
     const int v0 = pass0_index<TT>(warp), tok = routed_token_of<TT>(warp);
-    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW, v0);
+    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW, v0, d.f8s);
     __syncthreads();
     fill_units(p0, 0);
     __syncwarp();
@@ -487,7 +492,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             bulk_g2s(smem + fg.router_off + (size_t)re * H * 4, d.router_w + (size_t)(c + re * G) * H,
                      (unsigned)(H * 4), &s_rbar, pol);
     } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S && c < NRT) {
-        const int si = threadIdx.x - 32, ncs = d.Is / kChunkK;
+        const int si = threadIdx.x - 32, ncs = chunks_of(d.Is, d.f8s);
         prefetch_l2(d.sw2r + (size_t)si * d.s2_stride + (size_t)c * ncs * kChunkBytes, (unsigned)(ncs * kChunkBytes));
     }
     pump(RW);
@@ -639,15 +644,32 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     const int nrt0 = c < NRT ? (NRT - c + G - 1) / G : 0;   // this block's output tiles
     // One ring segment of n chunks against the B rows at bp: wait for it,
     // decode and multiply, release the slot and keep the ring full.
-    auto segment = [&](int n, const uint8_t *bp, bool bon, float (&a0)[4], float (&a1)[4]) {
+    // The segment holds chunks c0 .. c0 + n - 1 of its tile's K range; their
+    // B fragments are at bbase + b_offset(c) (F8 chunks: half a 64-element
+    // group each, scaled in FP32 after their two MMAs).
+    auto segment = [&](int n, const uint8_t *bbase, int c0, bool f8, bool bon, float (&a0)[4], float (&a1)[4]) {
         if (ok) {
             if (mbar_wait(bar + sl_c, par_c, d.err)) n_done = n_con + 1;
             else ok = false;
         }
         if (ok) {
             const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
+            if (f8) {
 #pragma unroll 2
-            for (int i = 0; i < n; ++i) chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bp + i * 128, bon, a0, a1);
+                for (int i = 0; i < n; ++i) {
+                    const uint8_t *ci = ch + (size_t)i * kChunkBytes;
+                    const uint4 cw = lds128(ci + 16 * lane);
+                    uint2 sw;
+                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n"
+                                 : "=r"(sw.x), "=r"(sw.y) : "r"(smem_u32(ci + kCodeBytes + 8 * (lane >> 2))));
+                    const uint4 b = bon ? lds128(bbase + b_offset(c0 + i, true)) : make_uint4(0u, 0u, 0u, 0u);
+                    chunk_mma_f8(cw, sw, b, (i & 1) ? a1 : a0);
+                }
+            } else {
+#pragma unroll 2
+                for (int i = 0; i < n; ++i)
+                    chunk_mma_smem(ch + (size_t)i * kChunkBytes, lane, bbase + (c0 + i) * 128, bon, a0, a1);
+            }
         }
         __syncwarp();
         ++n_con;
@@ -671,14 +693,14 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 #pragma unroll 1
         for (int ui = 0; ui < pp.my; ++ui) {
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint8_t *bp = xb + pp.cb0 * 128;
+            int c0 = pp.cb0;
             int lft = pp.cpw;
 #pragma unroll 1
             while (lft > 0) {
                 const int n = min(CH, lft);
                 if (ui == 0 && lft == pp.cpw) MOE_TRACE_CLOCK_AT(2, 4 * tp, tp == 0 ? 64 : 0);
-                segment(n, bp, true, a0, a1);
-                bp += n * 128;
+                segment(n, xb, c0, pp.f8, true, a0, a1);
+                c0 += n;
                 lft -= n;
             }
             if (ui == 0) MOE_TRACE_CLOCK_AT(2, 4 * tp + 1, tp == 0 ? 64 : 0);
@@ -849,7 +871,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             FUSED_TRACE(12);
             // this warp's routed units and down pieces -> its copy list
             nslots = s_nslots;
-            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW, warp);
+            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW, warp, d.f8e);
             MOE_TRACE_CLOCK(4, 3);
             fill_units(pp, p0.my);
             __syncwarp();
@@ -871,7 +893,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 const int ri = nrt == 1 ? 0 : i / perw, r2 = i - ri * perw;
                 const int rt = c + ri * G, pi = warp + kFW * r2;
                 const int e = s_slot_e[pi >> lksd], kp = pi & ((1 << lksd) - 1);
-                const int ncd = (e < 0 ? d.Is : d.I) / kChunkK, cpk = ncd >> lksd;
+                const int ncd = chunks_of(e < 0 ? d.Is : d.I, e < 0 ? d.f8s : d.f8e), cpk = ncd >> lksd;
                 const uint8_t *b = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
                 s_tab_src[warp][p0.my + pp.my + i] = b + ((size_t)rt * ncd + kp * cpk) * kChunkBytes;
                 s_tab_n[warp][p0.my + pp.my + i] = cpk;
@@ -1137,18 +1159,19 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             const int e = s_slot_e[slot];
             const int msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
             const float gs = s_gsp[e < 0 ? E - e - 1 : e].z;
-            const int cpk = (e < 0 ? d.Is : d.I) / kChunkK >> lksd;
+            const bool f8 = e < 0 ? d.f8s : d.f8e;
+            const int cpk = chunks_of(e < 0 ? d.Is : d.I, f8) >> lksd;
             const bool bon = (msk >> g) & 1;
-            const uint8_t *bp = hs + (size_t)(bon ? p0s + __popc(msk & ((1 << g) - 1)) : 0) * fg.hrow + q * 32 +
-                                kp * cpk * 128;
+            const uint8_t *bb = hs + (size_t)(bon ? p0s + __popc(msk & ((1 << g) - 1)) : 0) * fg.hrow + q * 32;
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            int c0 = kp * cpk;
             int lft = cpk;
 #pragma unroll 1
             while (lft > 0) {
                 const int n = min(CH, lft);
                 if (ri == 0 && r2 == 0 && lft == cpk) MOE_TRACE_CLOCK(2, 10);
-                segment(n, bp, bon, a0, a1);
-                bp += n * 128;
+                segment(n, bb, c0, f8, bon, a0, a1);
+                c0 += n;
                 lft -= n;
             }
             if (ri == 0) MOE_TRACE_CLOCK(2, 11);

@@ -119,17 +119,22 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     const bool shared = s < d.S;
     const uint64_t pol = evict_first_policy();
 
-    int m = 0, p0 = 0, NT = 0, NC = 0, ns = 0;
+    int m = 0, p0 = 0, NT = 0, NC = 0, NC64 = 0, ns = 0;
+    bool f8 = false;                 // the slot's expert is stored as F8 chunks
     float gsa = 0.f, gsb = 0.f;
     const uint8_t *wbase = nullptr;
     uint4 cb[PD];
     uint2 sb[PD];
 
     MOE_TRACE_POINT(1 + MODE, 0);
+    // NC: the slot's weight chunks per tile (in its format); NC64: 64-element
+    // groups of K (the granularity of the B staging)
     auto slot_geometry = [&](int e) {
+        f8 = e < 0 ? d.f8s : d.f8e;
         if (MODE == 0) {
             NT = (e < 0 ? d.Is : d.I) / 8;
-            NC = d.H / kChunkK;
+            NC64 = d.H / kChunkK;
+            NC = chunks_of(d.H, f8);
             if (e < 0) {
                 const int si = -e - 1;
                 gsa = d.sgs13[2 * si];
@@ -142,7 +147,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
             }
         } else {
             NT = d.H / 16;
-            NC = (e < 0 ? d.Is : d.I) / kChunkK;
+            NC64 = (e < 0 ? d.Is : d.I) / kChunkK;
+            NC = chunks_of(e < 0 ? d.Is : d.I, f8);
             if (e < 0) {
                 const int si = -e - 1;
                 gsa = d.sgs2[si];
@@ -220,11 +226,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     const int c_begin = ks * NC / ksplit, c_end = (ks + 1) * NC / ksplit;
     const int mpad = (m + 7) & ~7;
     const int G = mpad >> 3;
-    int ncst = NC;
+    int ncst = NC64;                 // 64-element groups staged at a time
     if (GMAX > 1) {
         const int lim = (kStageBudget / mpad - 16) / 128;
-        if (lim < NC) ncst = max(PD, (lim / PD) * PD);
+        if (lim < NC64) ncst = max(PD, (lim / PD) * PD);
     }
+    const int mult = f8 ? 2 : 1;     // weight chunks per 64-element group
     const int row_stride = ncst * 128 + 16;
     float *red = reinterpret_cast<float *>(smem + (size_t)mpad * row_stride);
 
@@ -256,34 +263,40 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
 #pragma unroll
         for (int v = 0; v < 4; ++v) acc[G2][v] = 0.f;
 
-    for (int st0 = 0; st0 < NC; st0 += ncst) {
-        const int st1 = min(NC, st0 + ncst);
+    for (int st0 = 0; st0 < NC64; st0 += ncst) {
+        const int st1 = min(NC64, st0 + ncst);
         __syncthreads();
         stage_rows(m, st0, st1 - st0, smem, row_stride, s_src, s_scale);
         __syncthreads();
         MOE_TRACE_POINT(1 + MODE, 2);
         if (active) {
-            const int lo = max(st0, c_begin), hi = min(st1, c_end);
+            const int lo = max(st0 * mult, c_begin), hi = min(st1 * mult, c_end);
             const uint8_t *brow = smem + (size_t)g * row_stride + q * 32;
             for (int cc = lo; cc < hi; cc += PD) {
 #pragma unroll
                 for (int i = 0; i < PD; ++i) {
                     const int c = cc + i;
                     if (c < hi) {
-                        uint32_t a[4][4];
-                        decode_chunk(cb[i], sb[i], a);
-                        const uint8_t *bp0 = brow + (c - st0) * 128;
+                        const uint8_t *bp0 = brow + b_offset(c - st0 * mult, f8);
+                        if (f8) {
 #pragma unroll
-                        for (int G2 = 0; G2 < GMAX; ++G2) {
-                            if (G2 < G) {
-                                const uint8_t *bp = bp0 + (size_t)G2 * 8 * row_stride;
-                                const uint4 b01 = lds128(bp);
-                                const uint4 b23 = lds128(bp + 16);
-                                float(&ac1)[4] = GMAX == 1 ? acc1 : acc[G2];
-                                mma_16816(acc[G2], a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
-                                mma_16816(ac1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
-                                mma_16816(acc[G2], a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
-                                mma_16816(ac1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                            for (int G2 = 0; G2 < GMAX; ++G2)
+                                if (G2 < G) chunk_mma_f8(cb[i], sb[i], lds128(bp0 + (size_t)G2 * 8 * row_stride), acc[G2]);
+                        } else {
+                            uint32_t a[4][4];
+                            decode_chunk(cb[i], sb[i], a);
+#pragma unroll
+                            for (int G2 = 0; G2 < GMAX; ++G2) {
+                                if (G2 < G) {
+                                    const uint8_t *bp = bp0 + (size_t)G2 * 8 * row_stride;
+                                    const uint4 b01 = lds128(bp);
+                                    const uint4 b23 = lds128(bp + 16);
+                                    float(&ac1)[4] = GMAX == 1 ? acc1 : acc[G2];
+                                    mma_16816(acc[G2], a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
+                                    mma_16816(ac1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
+                                    mma_16816(acc[G2], a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
+                                    mma_16816(ac1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                                }
                             }
                         }
                         const int cn = c + PD;

@@ -26,6 +26,18 @@
 //   matching up rows as MMA rows 8..15, so SwiGLU pairs are lane-local in the
 //   accumulator.  Down (w2): tile r holds output rows 16r..16r+15.
 //   Offset of chunk c of tile r of expert e: ((e*NT + r)*NC + c) * 576.
+//
+// FP8 experts (E4M3 codes with a scale per row and 32 elements: MXFP8, or the
+// FP32 scale of a 128 x 128 block) use "F8 chunks" of the same 576 bytes:
+// 16 rows x 32 K elements (two MMA K blocks kb = 0, 1).
+//     bytes [0, 512)   codes.  Lane L = 4g + q owns bytes [16L, 16L+16):
+//                      byte 8kb + 2j + e is element k = 16kb + 2q + e (+8
+//                      for j = 2, 3) of row g (j = 0, 2) or g+8 (j = 1, 3),
+//                      i.e. fragment register j of block kb, low byte first.
+//     bytes [512, 576) the FP32 scales of the 16 rows for these 32 elements:
+//                      bytes 8g + 4h hold the scale of row g + 8h.
+//   A tile has K/32 F8 chunks.  The same two loads per lane (16 code bytes at
+//   16L, 8 scale bytes at 512 + 8g) fetch a chunk in either format.
 #pragma once
 
 #include <cstddef>
@@ -40,6 +52,7 @@
 namespace moe {
 
 constexpr int kBlockK = 16;        // NVFP4 block length along K
+constexpr int kChunkK8 = 32;       // K elements per F8 chunk
 constexpr int kChunkK = 64;        // K elements per streamed chunk
 constexpr int kChunkBytes = 576;   // 512 code bytes + 64 scale bytes
 constexpr int kCodeBytes = 512;
@@ -107,7 +120,11 @@ struct DevLayer {
     unsigned long long *trace;      // traced build only: phase timestamps
     int trace_blocks;
     int score_func;                 // 0 sigmoid per expert, 1 softmax over all experts
+    int f8e, f8s;                   // routed / shared experts stored as F8 chunks
 };
+
+// Chunks per tile row of K elements, in the NVFP4 or the F8 chunk layout.
+__host__ __device__ inline int chunks_of(int K, bool f8) { return f8 ? K / kChunkK8 : K / kChunkK; }
 
 // ---------------------------------------------------------------------------
 // Host-side launchers (defined in the .cu files).
@@ -130,6 +147,22 @@ cudaError_t launch_repack(const uint8_t *codes, const uint8_t *sf, int n_mats, i
 cudaError_t launch_pack_scales(const DevLayer &d, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t *rep, float gs_a, float gs_b, int rows, int cols,
                            bool gate_up, float *dst, cudaStream_t s);
+// F8 chunks from E4M3 codes [n, rows, cols] and their scales: fmt 2 = FP32
+// per 128 x 128 block ([n, ceil(rows/128), ceil(cols/128)]), 3 = E8M0 per
+// 32 elements ([n, rows, cols/32]).
+cudaError_t launch_repack_f8(const uint8_t *codes, const void *sf, int fmt, int n_mats, int rows, int cols,
+                             bool gate_up, uint8_t *dst, cudaStream_t s);
+cudaError_t launch_dequant_f8(const uint8_t *rep, int rows, int cols, bool gate_up, float *dst, cudaStream_t s);
+// MXFP4 scales: per (matrix, half) the smallest and largest E8M0 code and
+// whether a NaN code (255) occurs -> mm[(mat * 2 + half) * 3 + {0,1,2}]
+// (half 1 only for gate/up: its up rows).
+cudaError_t launch_mx_scale_range(const uint8_t *sf, int n_mats, int rows, int cols, bool gate_up, int *mm,
+                                  cudaStream_t s);
+// MXFP4 scales -> the NVFP4 scales of the same weights: E8M0 code c of 32
+// elements -> the E4M3 code of 2^(c - 127 - off) for both of its 16-element
+// blocks, off = offs[mat * 2 + half] (the tensor scale becomes 2^off).
+cudaError_t launch_mx_to_nv_scales(const uint8_t *sf, const int *offs, int n_mats, int rows, int cols,
+                                   bool gate_up, uint8_t *dst, cudaStream_t s);
 
 // Let `fn` use all the shared memory a block may opt in to, minus its static part.
 template <class F>
@@ -142,8 +175,8 @@ inline cudaError_t allow_max_dynamic_smem(F fn, int optin_bytes) {
 }
 
 // Chunk geometry.
-__host__ __device__ inline size_t repacked_bytes(int rows, int cols) {
-    return (size_t)(rows / 16) * (size_t)(cols / kChunkK) * kChunkBytes;
+__host__ __device__ inline size_t repacked_bytes(int rows, int cols, bool f8 = false) {
+    return (size_t)(rows / 16) * (size_t)chunks_of(cols, f8) * kChunkBytes;
 }
 
 // ---------------------------------------------------------------------------
@@ -452,6 +485,38 @@ __device__ __forceinline__ void decode_chunk(const uint4 &cw, const uint2 &sw,
         a[i][3] = hmul2(h3, sg8);
     }
 }
+
+// Decode one F8 chunk's A fragments for one lane: 2 blocks x 4 registers of
+// exact f16 E4M3 values (every E4M3 value is an f16 value).
+__device__ __forceinline__ void decode_chunk_f8(const uint4 &cw, uint32_t (&a)[2][4]) {
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        a[w >> 1][2 * (w & 1)] = e4m3x2_to_f16x2(words[w] & 0xFFFFu);
+        a[w >> 1][2 * (w & 1) + 1] = e4m3x2_to_f16x2(words[w] >> 16);
+    }
+}
+
+// One F8 chunk against B (b: the lane's B fragments of the chunk's two K
+// blocks): both MMAs into a fresh accumulator, then FP32 scaling of rows g
+// (sw.x) and g+8 (sw.y) into acc.
+__device__ __forceinline__ void chunk_mma_f8(const uint4 &cw, const uint2 &sw, const uint4 &b, float (&acc)[4]) {
+    uint32_t a[2][4];
+    decode_chunk_f8(cw, a);
+    float t[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16816(t, a[0][0], a[0][1], a[0][2], a[0][3], b.x, b.y);
+    mma_16816(t, a[1][0], a[1][1], a[1][2], a[1][3], b.z, b.w);
+    const float sg = __uint_as_float(sw.x), sg8 = __uint_as_float(sw.y);
+    acc[0] = fmaf(sg, t[0], acc[0]);
+    acc[1] = fmaf(sg, t[1], acc[1]);
+    acc[2] = fmaf(sg8, t[2], acc[2]);
+    acc[3] = fmaf(sg8, t[3], acc[3]);
+}
+
+// Offset of the B fragments of chunk c (format chunks along K) in an operand
+// row laid out per 64 elements (128 bytes, lane q at 32q): an NVFP4 chunk is
+// one such group, an F8 chunk half of one (its K blocks 2(c%2), 2(c%2)+1).
+__device__ __forceinline__ int b_offset(int c, bool f8) { return f8 ? (c >> 1) * 128 + (c & 1) * 16 : c * 128; }
 
 #endif  // __CUDACC__
 

@@ -39,9 +39,12 @@ class moe_config(ctypes.Structure):
                 ("inter", ctypes.c_int), ("num_shared", ctypes.c_int), ("shared_inter", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("normalize_topk", ctypes.c_int),
                 ("routed_scale", ctypes.c_float), ("grouped_min_tokens", ctypes.c_int),
-                ("fused", ctypes.c_int), ("score_func", ctypes.c_int)]
+                ("fused", ctypes.c_int), ("score_func", ctypes.c_int),
+                ("expert_format", ctypes.c_int), ("shared_format", ctypes.c_int)]
 
 SCORE_FUNCS = {"sigmoid": 0, "softmax": 1}
+# expert weight formats (MOE_FMT_* of the header)
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "fp8_block": 2, "mxfp8": 3}
 
 
 class moe_weights(ctypes.Structure):
@@ -208,7 +211,8 @@ _NAMES = ("router_w", "router_b", "w13", "w13_sf", "w13_gs", "w2", "w2_sf", "w2_
 
 def to_device(layer: dict, device="cuda") -> dict:
     """Canonical numpy/torch tensors -> contiguous CUDA tensors (uint8 codes
-    and scales, float32 router and tensor scales)."""
+    and scales -- FP32 for block-scaled FP8 -- float32 router and tensor
+    scales)."""
     out = {}
     for n in _NAMES:
         a = layer.get(n)
@@ -228,7 +232,9 @@ def make_config(c: dict, max_tokens: int | None = None, grouped_min_tokens: int 
                       normalize_topk=int(c.get("normalize", 1)),
                       routed_scale=float(c.get("routed_scale", 1.0)),
                       grouped_min_tokens=int(grouped_min_tokens), fused=int(fused),
-                      score_func=SCORE_FUNCS[c.get("score_func", "sigmoid")])
+                      score_func=SCORE_FUNCS[c.get("score_func", "sigmoid")],
+                      expert_format=FORMATS[c.get("efmt", "nvfp4")],
+                      shared_format=FORMATS[c.get("sfmt", "nvfp4")])
 
 
 class MoELayer:
@@ -236,7 +242,8 @@ class MoELayer:
 
     `layer` is a dict of canonical tensors (numpy or torch) plus "cfg" with the
     sizes H, E, k, I, S, Is and, optionally, "normalize" (1), "routed_scale"
-    (1.0) and "score_func" ("sigmoid" or "softmax");
+    (1.0), "score_func" ("sigmoid" or "softmax") and the expert formats
+    "efmt" / "sfmt" ("nvfp4", "mxfp4", "fp8_block" or "mxfp8");
     the weights are repacked into library memory, so the inputs may be freed
     afterwards."""
 

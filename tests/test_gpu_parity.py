@@ -230,3 +230,44 @@ def test_invalid_calls_enqueue_nothing(moe):
         assert moe.moe_check(L.h) == moe.MOE_OK
     finally:
         L.close()
+
+
+def _wide_rows(orc, c, router, rng, T):
+    """T activation rows whose magnitudes span about 2^40 within each row:
+    sixteen elements ~N(0,1), the others ~N(0,1) * 2^-40 (BF16 holds both),
+    each row redrawn until its routing clears the margin (at most 200 draws)."""
+    from moe_cases import MARGIN
+    rows = []
+    for _ in range(200 * T):
+        if len(rows) == T:
+            break
+        v = rng.standard_normal(c["H"]) * 2.0 ** -40
+        big = rng.choice(c["H"], 16, replace=False)
+        v[big] = rng.standard_normal(16)
+        xb = gen.synth._to_bf16_bits(v.astype(np.float32))
+        _, _, s, _ = orc.route({"cfg": c, **router}, xb[None, :])
+        srt = np.sort(s[0])[::-1]
+        if srt[c["k"] - 1] - srt[c["k"]] >= MARGIN:
+            rows.append(xb)
+    assert len(rows) == T, "no admissible rows"
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+@pytest.mark.parametrize("fused", [0, -1], ids=["single", "chain"])
+def test_activation_rows_spanning_2_pow_40(moe, orc, T, fused):
+    """The exact power-of-two prescale of activation rows to f16 (row maximum
+    in [2^14, 2^15)) on rows spanning ~2^40: the large elements stay exact,
+    only elements far below the row maximum lose bits, and their share of
+    every dot product is far inside the tolerance."""
+    c = gen.config(2, T=T)
+    seed = gen.BASE_SEED + 70 + T
+    router = gen.make_router(c, seed)
+    x = _wide_rows(orc, c, router, np.random.default_rng(seed), T)
+    xv = (x.astype(np.uint32) << 16).view(np.float32)
+    a = np.abs(xv[xv != 0])
+    assert np.log2(a.max() / a.min()) > 38
+    ids, *_ = orc.route({"cfg": c, **router}, x)
+    layer = {"cfg": c, **router, **gen.make_experts(c, seed, np.unique(ids))}
+    gout, gids, gw = run_gpu(moe, layer, x, fused=fused)
+    check_parity(orc, layer, x, gout, gids, gw)
