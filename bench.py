@@ -73,9 +73,11 @@ def parse():
     ap.add_argument("--workload", default="flint1", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=0, help="override layers per step")
     ap.add_argument("--secondary", default="flint8", help="second workload reported in the line ('' = none)")
-    ap.add_argument("--extras", default="ml4,zipf64,zipf64-gemv,tiny,ml4fp8s,inkling,inkling_mx8,flint_mx4",
+    ap.add_argument("--extras", default="ml4,zipf64,zipf64-gemv,tiny,ml4fp8s,inkling,inkling_mx8,flint_mx4,"
+                                        "flint1-coop,flint8-coop",
                     help="further workloads timed and reported under 'workloads' ('' = none); "
-                         "zipf64-gemv is zipf64 with the grouped kernels off")
+                         "a '-gemv' suffix turns the grouped kernels off, '-coop' launches the single "
+                         "launch as a cooperative grid")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grouped-min", type=int, default=0,
@@ -275,14 +277,14 @@ def run_reference(args):
 class Chain:
     """L distinct layers of one workload on the current GPU."""
 
-    def __init__(self, moe, torch, gen, ci, L, seed0, grouped_min=0, score_func="sigmoid"):
+    def __init__(self, moe, torch, gen, ci, L, seed0, grouped_min=0, score_func="sigmoid", fused=0):
         self.c = gen.config(ci, score_func=score_func)
         c = self.c
         self.T, self.L = c["T"], L
         self.layers, self.xs, self.outs, self.ids, self.ws = [], [], [], [], []
         for l in range(L):
             lay = gen.make_layer_torch(c, seed0 + l)
-            self.layers.append(moe.MoELayer(lay, max_tokens=self.T, grouped_min_tokens=grouped_min))
+            self.layers.append(moe.MoELayer(lay, max_tokens=self.T, grouped_min_tokens=grouped_min, fused=fused))
             del lay
             self.xs.append(gen.make_x_torch(c, seed0 + l))
             self.outs.append(torch.empty((self.T, c["H"]), dtype=torch.bfloat16, device="cuda"))
@@ -490,11 +492,11 @@ def run_gpu(args):
     del chain, g_full
     torch.cuda.empty_cache()
 
-    def other(name, grouped_min=0):
+    def other(name, grouped_min=0, fused=0):
         """Per-layer time of another workload: its own distinct layers in one
         CUDA graph, timed like the main one (same warm-up and step count)."""
         oi, oL = WORKLOADS[name]
-        ch2 = Chain(moe, torch, gen, oi, oL, seed0 + 50000 + 1000 * oi, grouped_min)
+        ch2 = Chain(moe, torch, gen, oi, oL, seed0 + 50000 + 1000 * oi, grouped_min, fused=fused)
         g2 = capture(torch, lambda: ch2.enqueue(moe), stream)
         sel2, _, U2 = byte_counts(gen, ch2, np)
         st2 = max(args.steps, 5)
@@ -509,7 +511,7 @@ def run_gpu(args):
                "us_per_layer": us2, "GBps": b2 / (us2 * 1e-6) / 1e9,
                "frac_of_measured": b2 / (us2 * 1e-6) / 1e9 / peak,
                "selected_bytes_per_layer": b2, "unique_experts_mean": float(np.mean(U2)),
-               "path": "single launch" if one else
+               "path": ("single launch" + (", cooperative grid" if fused > 0 else "")) if one else
                        ("chain" + (", grouped kernels off" if grouped_min < 0 else
                                    (", grouped tensor-core kernels for slots of >= 8 tokens"
                                     if c2["T"] > 8 and "fp8" not in c2["efmt"] + c2["sfmt"] else ""))),
@@ -525,10 +527,12 @@ def run_gpu(args):
         if args.secondary not in ("", "none") and args.secondary != args.workload:
             secondary = other(args.secondary)
         for name in [w for w in args.extras.split(",") if w]:
-            base = name[:-5] if name.endswith("-gemv") else name
-            if base == args.workload and not name.endswith("-gemv"):
+            # "-gemv": the grouped kernels off; "-coop": the single launch as a
+            # cooperative grid
+            base = name.rsplit("-", 1)[0] if name.endswith(("-gemv", "-coop")) else name
+            if name == base == args.workload:
                 continue
-            workloads[name] = other(base, -1 if name.endswith("-gemv") else 0)
+            workloads[name] = other(base, -1 if name.endswith("-gemv") else 0, 1 if name.endswith("-coop") else 0)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

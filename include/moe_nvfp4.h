@@ -120,8 +120,12 @@ typedef struct {
                                one launch when the shape allows it (T <= 8,
                                H <= 8192, E <= 256 and <= 4 x SM count, the
                                activations and the weight rings fit in shared
-                               memory); < 0: always the three-kernel chain of
-                               the moe_stage_* entry points */
+                               memory); 1: the same, launched as a
+                               cooperative grid (the driver starts it only
+                               when every block can be resident, so kernels
+                               on other streams cannot keep a block waiting
+                               on the others); < 0: always the three-kernel
+                               chain of the moe_stage_* entry points */
     int score_func;         /* routing score: 0 = sigmoid of each logit (Flint
                                page, "Flint model architecture"); 1 = softmax
                                over all experts' logits (Mistral Large 4 page,

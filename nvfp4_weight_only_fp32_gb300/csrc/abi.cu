@@ -527,9 +527,8 @@ moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int
         cudaError_t e = cudaSuccess;
         if (++L->fused_calls >= kTagRestart) e = restart_tags(L, reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "tag restart");
-        e = launch_fused(d, static_cast<const __nv_bfloat16 *>(x), T,
-                                     static_cast<__nv_bfloat16 *>(out), topk_ids, topk_w, L->sm_count,
-                                     reinterpret_cast<cudaStream_t>(stream));
+        e = launch_fused(d, static_cast<const __nv_bfloat16 *>(x), T, static_cast<__nv_bfloat16 *>(out), topk_ids,
+                         topk_w, L->sm_count, L->cfg.fused > 0, reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MOE_OK : cuda_fail(e, "single-launch layer");
     }
     rc = moe_stage_route(L, x, T, topk_ids, topk_w, stream);

@@ -344,7 +344,9 @@ __device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned lo
 // and 2, 3 <= T <= 8 for 8) -- a step that runs once per call runs from a
 // cold instruction cache, so the loops over tokens are only as long as T
 // needs.
-template <int TT>
+// F8: the layer has experts in F8 chunks (the instance without it carries
+// no F8 code).
+template <int TT, bool F8>
 __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, FusedGeom fg) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[kFW][kRWmax];
@@ -476,7 +478,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         fence_proxy_async();
     }
     const int v0 = pass0_index<TT>(warp), tok = routed_token_of<TT>(warp);
-    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW, v0, d.f8s);
+    const Pass p0 = plan(S * NTs, fg.lks0, NTs, 0, kPW, v0, F8 && d.f8s);
     __syncthreads();
     fill_units(p0, 0);
     __syncwarp();
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             bulk_g2s(smem + fg.router_off + (size_t)re * H * 4, d.router_w + (size_t)(c + re * G) * H,
                      (unsigned)(H * 4), &s_rbar, pol);
     } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S && c < NRT) {
-        const int si = threadIdx.x - 32, ncs = chunks_of(d.Is, d.f8s);
+        const int si = threadIdx.x - 32, ncs = chunks_of(d.Is, F8 && d.f8s);
         prefetch_l2(d.sw2r + (size_t)si * d.s2_stride + (size_t)c * ncs * kChunkBytes, (unsigned)(ncs * kChunkBytes));
     }
     pump(RW);
@@ -654,7 +656,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
         }
         if (ok) {
             const uint8_t *ch = ring + (size_t)sl_c * CH * kChunkBytes;
-            if (f8) {
+            if (F8 && f8) {
 #pragma unroll 2
                 for (int i = 0; i < n; ++i) {
                     const uint8_t *ci = ch + (size_t)i * kChunkBytes;
@@ -871,7 +873,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             FUSED_TRACE(12);
             // this warp's routed units and down pieces -> its copy list
             nslots = s_nslots;
-            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW, warp, d.f8e);
+            pp = plan((nslots - S) * NT13, fg.lks1[nslots], NT13, S, kFW, warp, F8 && d.f8e);
             MOE_TRACE_CLOCK(4, 3);
             fill_units(pp, p0.my);
             __syncwarp();
@@ -893,7 +895,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
                 const int ri = nrt == 1 ? 0 : i / perw, r2 = i - ri * perw;
                 const int rt = c + ri * G, pi = warp + kFW * r2;
                 const int e = s_slot_e[pi >> lksd], kp = pi & ((1 << lksd) - 1);
-                const int ncd = chunks_of(e < 0 ? d.Is : d.I, e < 0 ? d.f8s : d.f8e), cpk = ncd >> lksd;
+                const int ncd = chunks_of(e < 0 ? d.Is : d.I, F8 && (e < 0 ? d.f8s : d.f8e)), cpk = ncd >> lksd;
                 const uint8_t *b = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
                 s_tab_src[warp][p0.my + pp.my + i] = b + ((size_t)rt * ncd + kp * cpk) * kChunkBytes;
                 s_tab_n[warp][p0.my + pp.my + i] = cpk;
@@ -1159,7 +1161,7 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             const int e = s_slot_e[slot];
             const int msk = s_slot_mask[slot], p0s = s_slot_p0[slot];
             const float gs = s_gsp[e < 0 ? E - e - 1 : e].z;
-            const bool f8 = e < 0 ? d.f8s : d.f8e;
+            const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
             const int cpk = chunks_of(e < 0 ? d.Is : d.I, f8) >> lksd;
             const bool bon = (msk >> g) & 1;
             const uint8_t *bb = hs + (size_t)(bon ? p0s + __popc(msk & ((1 << g) - 1)) : 0) * fg.hrow + q * 32;
@@ -1215,19 +1217,26 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     if (threadIdx.x == 0) d.calls[c] = s_tag;
 }
 
-template <int TT>
-cudaError_t launch_tt(const DevLayer &d, const FusedArgs &a, const FusedGeom &fg, int G, cudaStream_t s) {
+// coop: launch as a cooperative grid, which the driver starts only when all
+// its blocks can be resident at once (the blocks' exchanges then cannot wait
+// on a block that kernels of other streams keep off the GPU); the attribute is
+// combined with programmatic dependent launch.
+template <int TT, bool F8>
+cudaError_t launch_tt(const DevLayer &d, const FusedArgs &a, const FusedGeom &fg, int G, bool coop,
+                      cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(kFT);
     cfg.dynamicSmemBytes = (size_t)fg.total;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_kernel<TT>, d, a, fg);
+    cfg.numAttrs = coop ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, fused_kernel<TT, F8>, d, a, fg);
 }
 
 // the kernel instance for T tokens: 0 (TT = 1), 1 (TT = 2), 2 (TT = 8)
@@ -1237,12 +1246,17 @@ int g_dyn_max[kInst];                        // dynamic shared memory a block ma
 
 template <int TT>
 cudaError_t prepare_tt(int optin) {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<TT>);
+    cudaFuncAttributes fa, fb;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<TT, false>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, fused_kernel<TT, true>);
     if (e != cudaSuccess) return e;
-    g_dyn_max[inst_of(TT)] = optin - (int)fa.sharedSizeBytes;
-    return cudaFuncSetAttribute(fused_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                g_dyn_max[inst_of(TT)]);
+    g_dyn_max[inst_of(TT)] = optin - (int)std::max(fa.sharedSizeBytes, fb.sharedSizeBytes);
+    e = cudaFuncSetAttribute(fused_kernel<TT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             g_dyn_max[inst_of(TT)]);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fused_kernel<TT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g_dyn_max[inst_of(TT)]);
+    return e;
 }
 
 }  // namespace
@@ -1262,15 +1276,16 @@ bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem) {
 }
 
 cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
-                         float *w, int sm_count, cudaStream_t s) {
+                         float *w, int sm_count, bool coop, cudaStream_t s) {
     FusedGeom fg;
     if (T < 1 || T > kFusedMaxT || d.H > kMaxFusedH || !fused_geometry(d, T, sm_count, g_dyn_max[inst_of(T)], fg))
         return cudaErrorInvalidValue;
     FusedArgs a{x, T, out, ids, w};
+    const bool f8 = d.f8e || d.f8s;
     switch (inst_of(T)) {
-        case 0: return launch_tt<1>(d, a, fg, sm_count, s);
-        case 1: return launch_tt<2>(d, a, fg, sm_count, s);
-        default: return launch_tt<8>(d, a, fg, sm_count, s);
+        case 0: return f8 ? launch_tt<1, true>(d, a, fg, sm_count, coop, s) : launch_tt<1, false>(d, a, fg, sm_count, coop, s);
+        case 1: return f8 ? launch_tt<2, true>(d, a, fg, sm_count, coop, s) : launch_tt<2, false>(d, a, fg, sm_count, coop, s);
+        default: return f8 ? launch_tt<8, true>(d, a, fg, sm_count, coop, s) : launch_tt<8, false>(d, a, fg, sm_count, coop, s);
     }
 }
 
@@ -1292,10 +1307,11 @@ int fused_blocks_per_sm(const DevLayer &d, int T) {
     if (!fused_geometry(d, T, sms, g_dyn_max[inst_of(T)], fg)) return 0;
     int n = 0;
     cudaError_t e;
+    const bool f8 = d.f8e || d.f8s;
     switch (inst_of(T)) {
-        case 0: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<1>, kFT, fg.total); break;
-        case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<2>, kFT, fg.total); break;
-        default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fused_kernel<8>, kFT, fg.total); break;
+        case 0: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f8 ? fused_kernel<1, true> : fused_kernel<1, false>, kFT, fg.total); break;
+        case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f8 ? fused_kernel<2, true> : fused_kernel<2, false>, kFT, fg.total); break;
+        default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f8 ? fused_kernel<8, true> : fused_kernel<8, false>, kFT, fg.total); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();

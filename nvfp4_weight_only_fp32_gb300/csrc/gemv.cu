@@ -36,6 +36,8 @@
 // workspace; the CTA that finishes last among the slots of a row group (atomic
 // ticket, no spinning) sums sum_j w_j y_j + y_shared for those rows in a fixed
 // order and writes BF16 `out`.
+#include <type_traits>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -263,6 +265,44 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
 #pragma unroll
         for (int v = 0; v < 4; ++v) acc[G2][v] = 0.f;
 
+    // The chunk loop of one stage, one instance per chunk format (the
+    // format is uniform over a CTA's slot), so the NVFP4 loop carries no F8
+    // code.
+    auto run_chunks = [&](auto f8c, int lo, int hi, const uint8_t *brow, int cst0) {
+        constexpr bool F8 = decltype(f8c)::value;
+        for (int cc = lo; cc < hi; cc += PD) {
+#pragma unroll
+            for (int i = 0; i < PD; ++i) {
+                const int c = cc + i;
+                if (c < hi) {
+                    const uint8_t *bp0 = brow + b_offset(c - cst0, F8);
+                    if constexpr (F8) {
+#pragma unroll
+                        for (int G2 = 0; G2 < GMAX; ++G2)
+                            if (G2 < G) chunk_mma_f8(cb[i], sb[i], lds128(bp0 + (size_t)G2 * 8 * row_stride), acc[G2]);
+                    } else {
+                        uint32_t a[4][4];
+                        decode_chunk(cb[i], sb[i], a);
+#pragma unroll
+                        for (int G2 = 0; G2 < GMAX; ++G2) {
+                            if (G2 < G) {
+                                const uint8_t *bp = bp0 + (size_t)G2 * 8 * row_stride;
+                                const uint4 b01 = lds128(bp);
+                                const uint4 b23 = lds128(bp + 16);
+                                float(&ac1)[4] = GMAX == 1 ? acc1 : acc[G2];
+                                mma_16816(acc[G2], a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
+                                mma_16816(ac1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
+                                mma_16816(acc[G2], a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
+                                mma_16816(ac1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                            }
+                        }
+                    }
+                    const int cn = c + PD;
+                    if (cn < c_end) load_chunk(tbase, cn, lane, cb[i], sb[i], pol);
+                }
+            }
+        }
+    };
     for (int st0 = 0; st0 < NC64; st0 += ncst) {
         const int st1 = min(NC64, st0 + ncst);
         __syncthreads();
@@ -272,38 +312,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
         if (active) {
             const int lo = max(st0 * mult, c_begin), hi = min(st1 * mult, c_end);
             const uint8_t *brow = smem + (size_t)g * row_stride + q * 32;
-            for (int cc = lo; cc < hi; cc += PD) {
-#pragma unroll
-                for (int i = 0; i < PD; ++i) {
-                    const int c = cc + i;
-                    if (c < hi) {
-                        const uint8_t *bp0 = brow + b_offset(c - st0 * mult, f8);
-                        if (f8) {
-#pragma unroll
-                            for (int G2 = 0; G2 < GMAX; ++G2)
-                                if (G2 < G) chunk_mma_f8(cb[i], sb[i], lds128(bp0 + (size_t)G2 * 8 * row_stride), acc[G2]);
-                        } else {
-                            uint32_t a[4][4];
-                            decode_chunk(cb[i], sb[i], a);
-#pragma unroll
-                            for (int G2 = 0; G2 < GMAX; ++G2) {
-                                if (G2 < G) {
-                                    const uint8_t *bp = bp0 + (size_t)G2 * 8 * row_stride;
-                                    const uint4 b01 = lds128(bp);
-                                    const uint4 b23 = lds128(bp + 16);
-                                    float(&ac1)[4] = GMAX == 1 ? acc1 : acc[G2];
-                                    mma_16816(acc[G2], a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
-                                    mma_16816(ac1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
-                                    mma_16816(acc[G2], a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
-                                    mma_16816(ac1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
-                                }
-                            }
-                        }
-                        const int cn = c + PD;
-                        if (cn < c_end) load_chunk(tbase, cn, lane, cb[i], sb[i], pol);
-                    }
-                }
-            }
+            if (f8) run_chunks(std::true_type{}, lo, hi, brow, st0 * mult);
+            else run_chunks(std::false_type{}, lo, hi, brow, st0 * mult);
         }
     }
 
