@@ -23,7 +23,7 @@
 //               rounded up to 16, K=16) into a TMEM accumulator and commits
 //               them to the stage's "empty" mbarrier; after the last stage a
 //               commit to the accumulator barrier.
-// Two stages ring between producers and the MMA issuer (an odd chunk count
+// Three stages ring between producers and the MMA issuer (an odd chunk count
 // leaves the last stage half full).  Warps 0-7 then
 // read the accumulator (tcgen05.ld, warp w owns TMEM lanes 32(w%4).. and
 // half of the columns) and run the epilogue:
@@ -51,8 +51,8 @@ constexpr int kMmaW = kDecW + kStgW;              // MMA-issuing warp
 constexpr int kGW = kMmaW + 1;
 constexpr int kGT = 32 * kGW;
 constexpr int kCPS = 2;                           // 64-wide K chunks per pipeline stage
-constexpr int kNS = 2;                            // pipeline stages
-constexpr int kLA = 4;                            // B-operand chunks in flight (raw copies)
+constexpr int kNS = 3;                            // pipeline stages
+constexpr int kLA = 2;                            // B-operand chunks in flight (raw copies)
 constexpr int kMT = 128;                          // weight rows per item (8 tiles)
 constexpr int kNmax = kMaxTokens;                 // tokens per slot
 constexpr uint32_t kLBO = 128;                    // K-adjacent core matrices
@@ -61,7 +61,7 @@ constexpr int kAStage = kMT * kChunkK * kCPS * 2; // 32 KB
 constexpr int kBStage = kNmax * kChunkK * kCPS * 2;   // 16 KB
 constexpr int kScratch = kMaxTokens * (kMaxTopK + kMaxShared) * 8;   // combine's pair table
 constexpr int kCHA = 4;                           // chunks per raw-weight segment
-constexpr int kRWA = 4;                           // raw-weight segments per decode warp
+constexpr int kRWA = 3;                           // raw-weight segments per decode warp
 constexpr int kRawOff = kNS * (kAStage + kBStage) + kScratch;
 constexpr int kBRawOff = kRawOff + kDecW * kRWA * kCHA * kChunkBytes;
 constexpr int kBRawStage = kNmax * kChunkK * 2;   // one chunk of the slot's token rows, as stored (8 KB)
@@ -431,8 +431,9 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                 tc_fence_after();
                 if (li == 0 && c0 == 0) MOE_TRACE_POINT_AT(3 + MODE, 4, 32 * kMmaW);
                 const uint32_t a0 = smem_u32(sA + (size_t)st * kAStage), b0 = smem_u32(sB + (size_t)st * kBStage);
-#pragma unroll 1
-                for (int ks = 0; ks < 4 * nch; ++ks) {
+#pragma unroll
+                for (int ks = 0; ks < 4 * kCPS; ++ks) {
+                    if (ks >= 4 * nch) break;
                     const uint64_t da = smem_desc(a0 + ks * 2 * kLBO), db = smem_desc(b0 + ks * 2 * kLBO);
                     const uint32_t acc = (c0 > 0 || ks > 0) ? 1u : 0u;
                     asm volatile(
