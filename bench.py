@@ -50,8 +50,8 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20774144, "fused_cu_sha256_16": "7c939201365def2d"},
-    "flint8": {"bytes": 124694272, "fused_cu_sha256_16": "7c939201365def2d"},
+    "flint1": {"bytes": 20784896, "fused_cu_sha256_16": "41a5b9880e39a08a"},
+    "flint8": {"bytes": 124596224, "fused_cu_sha256_16": "41a5b9880e39a08a"},
 }
 
 def ncu_traffic(workload: str):
@@ -526,7 +526,7 @@ def run_gpu(args):
     if rank == 0:
         if args.secondary not in ("", "none") and args.secondary != args.workload:
             secondary = other(args.secondary)
-        for name in [w for w in args.extras.split(",") if w]:
+        for name in [w for w in args.extras.split(",") if w and w != "none"]:
             # "-gemv": the grouped kernels off; "-coop": the single launch as a
             # cooperative grid
             base = name.rsplit("-", 1)[0] if name.endswith(("-gemv", "-coop")) else name

@@ -14,7 +14,8 @@
 // one tile by splitting K and add their partial sums in shared memory in a
 // fixed order (deterministic).  Each warp streams its chunks (576 B: one
 // 16-byte code load and one 8-byte scale load per lane) through a register
-// ring PD chunks deep, decodes E2M1 x E4M3 exactly into f16 A fragments
+// ring PD chunks deep (8 for gate/up, 12 for down at up to 8 tokens),
+// decodes E2M1 x E4M3 exactly into f16 A fragments
 // (cvt.rn.f16x2.e2m1x2, cvt.rn.f16x2.e4m3x2, one f16x2 multiply) and issues
 // mma.m16n8k16 with FP32 accumulators against the activations of the slot's
 // tokens (B, staged once per CTA in shared memory, f16 after an exact
@@ -445,7 +446,10 @@ cudaError_t launch_stage(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_
         dim3 grid((NT + tpc - 1) / tpc, slots);
         size_t smem = (size_t)8 * (NCmax * 128 + 16) + (size_t)tpc * (ksplit - 1) * 4 * 32 * sizeof(float);
         if (MODE == 1 && smem < combine_smem) smem = combine_smem;
-        return launch_one<MODE, 1, 8>(d, x, T, ksplit, grid, smem, out, s);
+        // down: a 12-deep ring (measured faster on the ML4- and
+        // Inkling-shaped layers, the same occupancy); gate/up: 8 deep
+        if constexpr (MODE == 1) return launch_one<1, 1, 12>(d, x, T, ksplit, grid, smem, out, s);
+        else return launch_one<0, 1, 8>(d, x, T, ksplit, grid, smem, out, s);
     }
     dim3 grid((NT + kGemvWarps - 1) / kGemvWarps, slots);
     return launch_one<MODE, 8, 4>(d, x, T, 1, grid, (size_t)kStageBudget, out, s);
@@ -466,7 +470,7 @@ cudaError_t prepare_kernels() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e == cudaSuccess) e = allow_smem<0, 1, 8>(optin);
-    if (e == cudaSuccess) e = allow_smem<1, 1, 8>(optin);
+    if (e == cudaSuccess) e = allow_smem<1, 1, 12>(optin);
     if (e == cudaSuccess) e = allow_smem<0, 8, 4>(optin);
     if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
     if (e == cudaSuccess) e = prepare_route_kernel(optin);

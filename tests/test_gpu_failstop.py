@@ -26,9 +26,12 @@ def moe():
     return load_moe()
 
 
-def test_grid_wait_gives_up_and_the_handle_recovers(moe, orc):
+@pytest.mark.parametrize("T", [1, 8])
+def test_grid_wait_gives_up_and_the_handle_recovers(moe, orc, T):
+    """One token (the h exchange through tagged words) and eight (through
+    plain rows and per-slot counters, which the restart clears too)."""
     import torch
-    layer, x, _ = guarded_case(1, gen.BASE_SEED + 11, T=1)
+    layer, x, _ = guarded_case(1, gen.BASE_SEED + 11, T=T)
     L = moe.MoELayer(layer, max_tokens=8)
     try:
         assert L.info().single_launch_max_tokens >= 1
