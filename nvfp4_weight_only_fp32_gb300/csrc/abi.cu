@@ -490,7 +490,7 @@ moe_status moe_stage_gate_up(moe_layer *L, const void *x, int T, void *stream) {
     if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, st);
+    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, L->sm_count, L->optin_smem, st);
     // above 8 tokens the GEMV kernel leaves the slots with >= grouped_min
     // tokens to the grouped tensor-core kernel
     if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)

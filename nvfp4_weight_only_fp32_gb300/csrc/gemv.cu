@@ -23,6 +23,11 @@
 // off the CUDA cores so that decoding keeps up with HBM; the kernel is bound
 // by the weight stream.
 //
+// Gate/up at up to 8 tokens runs, where the shape allows it, as one wave of
+// 16-warp blocks that stage the step's activations once per SM and stream
+// units from every slot (gemv_up_wave_kernel below); the per-slot grid ran a
+// little over three waves of blocks, each staging the activations anew.
+//
 // Prefetch before the programmatic-launch wait: gate/up streams the shared
 // experts' weights (they do not depend on routing); down streams every slot's
 // weights, because by the time it starts the router has finished (the gate/up
@@ -37,6 +42,7 @@
 // workspace; the CTA that finishes last among the slots of a row group (atomic
 // ticket, no spinning) sums sum_j w_j y_j + y_shared for those rows in a fixed
 // order and writes BF16 `out`.
+#include <algorithm>
 #include <type_traits>
 
 #include "moe_internal.cuh"
@@ -69,15 +75,16 @@ __device__ __forceinline__ void prefetch_ring(const uint8_t *tbase, int c_begin,
 // 2q + e of a chunk sits at half index 16q + 4kb + 2h + e.  Row j comes from
 // s_src[j] scaled by s_scale[j] (an exact power of two).  Loads are issued four
 // at a time before any store.
+template <int NTHR = kThreads>   // threads of the block taking part
 __device__ __forceinline__ void stage_rows(int m, int kc0, int nch, uint8_t *bsm, int row_stride,
                                            const uint4 *const *s_src, const float *s_scale) {
     const int per_row = nch * 8;
     const int items = m * per_row;
-    for (int base = threadIdx.x; base < items; base += 4 * kThreads) {
+    for (int base = threadIdx.x; base < items; base += 4 * NTHR) {
         uint4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int it = base + u * kThreads;
+            const int it = base + u * NTHR;
             if (it < items) {
                 const int j = it / per_row, rem = it - j * per_row;
                 v[u] = __ldcg(s_src[j] + (size_t)kc0 * 8 + rem);
@@ -85,7 +92,7 @@ __device__ __forceinline__ void stage_rows(int m, int kc0, int nch, uint8_t *bsm
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int it = base + u * kThreads;
+            const int it = base + u * NTHR;
             if (it < items) {
                 const int j = it / per_row, rem = it - j * per_row;
                 const int cc = rem >> 3, part = rem & 7;
@@ -408,6 +415,219 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     MOE_TRACE_POINT(2, 7);
 }
 
+// ---------------------------------------------------------------------------
+// Gate/up for steps of at most 8 tokens, as one wave: one block of 16 warps
+// per SM stages the step's x rows once (all T tokens: the MMA's N = 8
+// columns are the tokens, so every slot uses the same B operand and picks
+// its own tokens' columns in the epilogue), then its warps stream gate/up
+// units -- (slot, 16-row tile, K part), shared slots first -- assigned round
+// robin over every warp of the grid, through an 8-deep register ring that
+// runs on from one unit into the next.  Groups of 2^lks warps split a
+// tile's K range and add their partial sums in shared memory in a fixed
+// order.  Epilogue per unit: SwiGLU of the slot's tokens, h (BF16) and the
+// per-pair max |h| as in the per-slot kernel.
+// ---------------------------------------------------------------------------
+constexpr int kUW = 16;                 // warps per block
+constexpr int kUT = 32 * kUW;
+constexpr int kUPD = 8;                 // ring depth (a unit's chunks are a multiple of it)
+constexpr int kUMax = 32;               // units per warp
+
+template <bool F8>
+__global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
+                                                              int T, int lks) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ const uint8_t *s_ub[kUW][kUMax];    // first chunk of the unit's K part
+    __shared__ short s_us[kUW][kUMax], s_ur[kUW][kUMax], s_uc[kUW][kUMax];   // slot, tile, chunks
+    __shared__ const uint4 *s_src[8];
+    __shared__ float s_scale[8];
+    __shared__ float s_unscale[8];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int H = d.H, S = d.S;
+    const int ks = 1 << lks, kw = warp & (ks - 1);
+    const int ngrp = gridDim.x * (kUW >> lks), gid = blockIdx.x * (kUW >> lks) + (warp >> lks);
+    const int NC64 = H / kChunkK, row_stride = NC64 * 128 + 16;
+    float *red = reinterpret_cast<float *>(smem + (size_t)(T + 1) * row_stride);   // [kUW][4][32]
+    const uint64_t pol = evict_first_policy();
+
+    MOE_TRACE_POINT(1, 0);
+    pdl_wait();     // the router's slot tables, x's exponents and the zeroed h maxima
+    pdl_trigger();
+    MOE_TRACE_POINT(1, 1);
+    const int ns = __ldcg(d.nslots);
+    const int NTs = d.Is / 8, NT13 = d.I / 8;
+    const int units = S * NTs + (ns - S) * NT13;
+    const int my = gid < units ? min(kUMax, (units - gid + ngrp - 1) / ngrp) : 0;
+    for (int i = lane; i < my; i += 32) {
+        const int u = gid + i * ngrp;
+        int sl, r;
+        if (u < S * NTs) {
+            sl = u / NTs;
+            r = u - sl * NTs;
+        } else {
+            const int v = u - S * NTs;
+            sl = S + v / NT13;
+            r = v - (sl - S) * NT13;
+        }
+        const int e = __ldcg(d.slot_expert + sl);
+        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+        const int nc = chunks_of(H, f8), cpw = nc >> lks;
+        const uint8_t *b = e < 0 ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
+        s_ub[warp][i] = b + ((size_t)r * nc + kw * cpw) * kChunkBytes;
+        s_us[warp][i] = (short)sl;
+        s_ur[warp][i] = (short)r;
+        s_uc[warp][i] = (short)cpw;
+    }
+    __syncwarp();
+    // the ring's first chunks, before the activations are staged
+    uint4 cb[kUPD];
+    uint2 sb[kUPD];
+    if (my > 0) {
+#pragma unroll
+        for (int i = 0; i < kUPD; ++i) load_chunk(s_ub[warp][0], i, lane, cb[i], sb[i], pol);
+    }
+    if (threadIdx.x < T) {
+        const int t = threadIdx.x;
+        const int ex = __ldcg(d.xexp + t);
+        s_src[t] = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+        s_scale[t] = pow2f(-ex);
+        s_unscale[t] = pow2f(ex);
+    }
+    for (int i = threadIdx.x; i < row_stride / 16; i += kUT)
+        reinterpret_cast<uint4 *>(smem + (size_t)T * row_stride)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    stage_rows<kUT>(T, 0, NC64, smem, row_stride, s_src, s_scale);
+    __syncthreads();
+    MOE_TRACE_POINT(1, 2);
+
+    const uint8_t *xb = smem + (size_t)(g < T ? g : T) * row_stride + q * 32;
+    int lu = 0, lc = kUPD;     // next chunk to load: unit lu, chunk lc
+#pragma unroll 1
+    for (int cu = 0; cu < my; ++cu) {
+        const int sl = s_us[warp][cu], cpw = s_uc[warp][cu];
+        const int e = __ldcg(d.slot_expert + sl);
+        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+        const int kc0 = kw * cpw;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int cc = 0; cc < cpw; cc += kUPD) {
+#pragma unroll
+            for (int i = 0; i < kUPD; ++i) {
+                const uint8_t *bp = xb + b_offset(kc0 + cc + i, f8);
+                if (F8 && f8) {
+                    chunk_mma_f8(cb[i], sb[i], lds128(bp), (i & 1) ? a1 : a0);
+                } else {
+                    uint32_t a[4][4];
+                    decode_chunk(cb[i], sb[i], a);
+                    const uint4 b01 = lds128(bp), b23 = lds128(bp + 16);
+                    mma_16816(a0, a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
+                    mma_16816(a1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
+                    mma_16816(a0, a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
+                    mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                }
+                // refill this slot with the chunk kUPD ahead (possibly of the next unit)
+                if (lu < my && lc >= s_uc[warp][lu]) {
+                    lc -= s_uc[warp][lu];
+                    ++lu;
+                }
+                if (lu < my) load_chunk(s_ub[warp][lu], lc, lane, cb[i], sb[i], pol);
+                ++lc;
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) a0[v] += a1[v];
+        if (ks > 1) {
+            // fixed-order K reduction within the group (named barrier 1 + group)
+            if (kw > 0) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) red[(warp * 4 + v) * 32 + lane] = a0[v];
+            }
+            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + (warp >> lks)), "r"(32 * ks) : "memory");
+            if (kw == 0) {
+#pragma unroll 1
+                for (int w = 1; w < ks; ++w)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) a0[v] += red[((warp + w) * 4 + v) * 32 + lane];
+            }
+            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + (warp >> lks)), "r"(32 * ks) : "memory");
+        }
+        if (kw != 0) continue;
+        // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row 8r + g;
+        // columns are tokens, a slot's pairs are its tokens in ascending order
+        const int r = s_ur[warp][cu];
+        const int m = __ldcg(d.slot_m + sl), p0 = __ldcg(d.slot_p0 + sl);
+        unsigned msk = 0u;
+        if (lane < m) msk = 1u << __ldcg(d.pair_tok + p0 + lane);
+        msk = __reduce_or_sync(0xffffffffu, msk);
+        float gsa, gsb;
+        if (e < 0) {
+            gsa = d.sgs13[2 * (-e - 1)];
+            gsb = d.sgs13[2 * (-e - 1) + 1];
+        } else {
+            gsa = d.gs13[2 * e];
+            gsb = d.gs13[2 * e + 1];
+        }
+        const int n = 8 * r + g;
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const int t = 2 * q + e2;
+            const bool on = t < T && ((msk >> t) & 1u);
+            const int p = p0 + __popc(msk & ((1u << t) - 1u));
+            float habs = 0.f;
+            if (on) {
+                const float sc = s_unscale[t];
+                const float gt = a0[e2] * gsa * sc;
+                const float up = a0[2 + e2] * gsb * sc;
+                const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                d.h_ws[(size_t)p * d.Imax + n] = hb;
+                habs = fabsf(__bfloat162float(hb));
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, off));
+            if (on && g == 0) atomicMax(d.hmax + p, __float_as_uint(habs));
+        }
+    }
+    MOE_TRACE_POINT(1, 3);
+}
+
+// The K split of the wave kernel: among 2^l <= 4 whose units per warp group
+// fit its table and whose chunks per unit are a whole number of ring turns,
+// the one with the fewest (chunks + a reduction) per group.  -1: the kernel
+// does not apply.
+int wave_lks(const DevLayer &d, int T, int sm_count) {
+    if (T > 8) return -1;
+    // units of one length: routed and shared experts in the same chunk format
+    // (an F8 tile has twice the chunks, and the round-robin assignment would
+    // leave the warps that draw one behind; measured slower)
+    if (d.S > 0 && d.f8e != d.f8s) return -1;
+    const int slots = std::min(d.E, T * d.k);
+    const long units = (long)d.S * (d.Is / 8) + (long)slots * (d.I / 8);
+    int best = -1;
+    long bestc = 0;
+    for (int l = 0; l <= 2; ++l) {
+        const long groups = (long)sm_count * (kUW >> l);
+        const long per = (units + groups - 1) / groups;
+        bool fits = per <= kUMax;
+        for (int f = 0; f < 2 && fits; ++f) {
+            const bool f8 = f == 0 ? d.f8e : (d.S > 0 && d.f8s);
+            const int nc = chunks_of(d.H, f8);
+            fits = nc % (1 << l) == 0 && (nc >> l) % kUPD == 0;
+        }
+        if (!fits) continue;
+        const long cost = per * ((chunks_of(d.H, d.f8e) >> l) + (l > 0 ? 2 : 0));
+        if (best < 0 || cost < bestc) {
+            best = l;
+            bestc = cost;
+        }
+    }
+    return best;
+}
+
+size_t wave_smem(const DevLayer &d, int T) {
+    return (size_t)(T + 1) * ((d.H / kChunkK) * 128 + 16) + (size_t)kUW * 4 * 32 * sizeof(float);
+}
+
 template <int MODE, int GMAX, int PD>
 cudaError_t launch_one(const DevLayer &d, const __nv_bfloat16 *x, int T, int ksplit, dim3 grid,
                        size_t smem, __nv_bfloat16 *out, cudaStream_t s) {
@@ -472,6 +692,8 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = allow_smem<0, 1, 8>(optin);
     if (e == cudaSuccess) e = allow_smem<1, 1, 12>(optin);
     if (e == cudaSuccess) e = allow_smem<0, 8, 4>(optin);
+    if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<false>, optin);
+    if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<true>, optin);
     if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
     if (e == cudaSuccess) e = prepare_route_kernel(optin);
     if (e == cudaSuccess) e = prepare_fused_kernel(optin);
@@ -479,7 +701,25 @@ cudaError_t prepare_kernels() {
     return e;
 }
 
-cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s) {
+cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, int optin_smem,
+                           cudaStream_t s) {
+    const int sms = sm_count;
+    const int lks = wave_lks(d, T, sms);
+    const size_t smem = wave_smem(d, T);
+    if (lks >= 0 && smem + 16 * 1024 <= (size_t)optin_smem) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(sms);
+        cfg.blockDim = dim3(kUT);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return (d.f8e || d.f8s) ? cudaLaunchKernelEx(&cfg, gemv_up_wave_kernel<true>, d, x, T, lks)
+                                : cudaLaunchKernelEx(&cfg, gemv_up_wave_kernel<false>, d, x, T, lks);
+    }
     return launch_stage<0>(d, x, T, nullptr, s);
 }
 

@@ -131,7 +131,10 @@ __host__ __device__ inline int chunks_of(int K, bool f8) { return f8 ? K / kChun
 // ---------------------------------------------------------------------------
 cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out,
                          float *w_out, int sm_count, cudaStream_t s);
-cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, cudaStream_t s);
+// gate/up: one wave of 16-warp blocks (one per SM) for steps of at most 8
+// tokens where the shape allows it, else the per-slot GEMV kernel
+cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, int optin_smem,
+                           cudaStream_t s);
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s);
 bool grouped_supported(const DevLayer &d, int sm_count);
 cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s);
