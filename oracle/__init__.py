@@ -55,6 +55,7 @@ class _Layer(ctypes.Structure):
         ("sw2", ctypes.c_void_p), ("sw2_sf", ctypes.c_void_p), ("sw2_gs", ctypes.c_void_p),
         ("score_func", ctypes.c_int),
         ("efmt", ctypes.c_int), ("sfmt", ctypes.c_int),
+        ("w4a4", ctypes.c_int),
     ]
 
 
@@ -116,6 +117,12 @@ def _declare(L):
     L.orc_dequant_fmt.argtypes = [i, vp, vp, ctypes.c_float, i, i, vp]
     L.orc_e8m0.restype = d
     L.orc_e8m0.argtypes = [i]
+    L.orc_quant_fos.restype = ctypes.c_float
+    L.orc_quant_fos.argtypes = [vp, i, vp, vp, vp, vp]
+    L.orc_e4m3_from_f32.restype = i
+    L.orc_e4m3_from_f32.argtypes = [ctypes.c_float]
+    L.orc_e2m1_from_f32.restype = i
+    L.orc_e2m1_from_f32.argtypes = [ctypes.c_float]
     L.orc_route.restype = i
     L.orc_route.argtypes = [ctypes.POINTER(_Layer), vp, i, vp, vp, vp, vp]
     L.orc_forward.restype = i
@@ -155,6 +162,7 @@ class _Bound:
                         normalize=int(c.get("normalize", 1)),
                         routed_scale=float(c.get("routed_scale", 1.0)),
                         score_func=score_func_code(c), efmt=efmt, sfmt=sfmt,
+                        w4a4=int(bool(c.get("w4a4", 0))),
                         **{n: _ptr(a) for n, a in self.arrs.items()})
 
 
@@ -213,6 +221,28 @@ def dequant_fmt(fmt: str, codes: np.ndarray, sf: np.ndarray, gs: float, rows: in
     out = np.empty((rows, cols), dtype=np.float32)
     lib().orc_dequant_fmt(f, _ptr(codes), _ptr(sf), ctypes.c_float(gs), rows, cols, _ptr(out))
     return out
+
+
+def quant_fos(row_bits: np.ndarray):
+    """Four-Over-Six NVFP4 quantisation of one BF16 row (length a multiple of
+    16) -> (codes [n] uint8 (one code per element), block scale codes [n/16],
+    choices [n/16] (4 or 6), global scale, dequantised [n] f64)."""
+    row = _c(row_bits, np.uint16)
+    n = row.shape[0]
+    codes = np.empty(n, np.uint8)
+    sf = np.empty(n // 16, np.uint8)
+    ch = np.empty(n // 16, np.uint8)
+    deq = np.empty(n, np.float64)
+    gs = lib().orc_quant_fos(_ptr(row), n, _ptr(codes), _ptr(sf), _ptr(ch), _ptr(deq))
+    return codes, sf, ch, float(gs), deq
+
+
+def e4m3_from_f32(v: float) -> int:
+    return int(lib().orc_e4m3_from_f32(float(v)))
+
+
+def e2m1_from_f32(v: float) -> int:
+    return int(lib().orc_e2m1_from_f32(float(v)))
 
 
 def route(layer: dict, x_bits: np.ndarray):

@@ -68,6 +68,29 @@
  *             8 layers' experts are MXFP8): E4M3 (fn) codes with one E8M0
  *             scale per 32 values along K: W = e4m3 * 2^(s - 127).
  *    Every product is exact in FP64 (at most 4 + 24 significant bits).
+ *  - W4A4 (activations quantised to NVFP4 with "Four Over Six" block scales,
+ *    [INK2] "Mixed-precision MoE and Four-Over-Six NVFP4": a per-token global
+ *    scale plus, for each 16-element block, the block maximum scaled to 6 and
+ *    to 4, keeping whichever reconstructs the block with the lower mean
+ *    absolute error; [INK2] "MoE with fused activation quantisation": the
+ *    tokens are quantised before gate/up and the SwiGLU output before down).
+ *    Reading of the steps the page leaves open, all in FP32 (the precision
+ *    the quantiser's decisions are taken in):
+ *      a  = max |v| over the row (v: the BF16 row, exact in FP32);
+ *      gs = a / 1792 (1792 = 4 * 448, so that the "4" candidate's largest
+ *           block scale is E4M3's largest value); gs = 1 for an all-zero row;
+ *      for each block b (16 consecutive elements) and c in {6, 4}:
+ *        s_c = e4m3(m_b / (c * gs))      m_b = max |v| in the block; E4M3
+ *                                        round to nearest even, saturating
+ *        q_k = e2m1(v_k / (s_c * gs))    E2M1 round to nearest even (on a tie
+ *                                        the code with mantissa bit 0),
+ *                                        saturating at 6; all zero if s_c = 0
+ *        r_k = e2m1(q_k) * s_c * gs      err_c = sum over k = 0..15 of
+ *                                        |v_k - r_k|, summed in that order
+ *      the block keeps c = 4 if err_4 < err_6, else c = 6 (ties go to 6, the
+ *      plain NVFP4 choice).  The dequantised activation is e2m1 * e4m3 * gs,
+ *      exact in FP64.  The router still reads the unquantised x; h is the
+ *      BF16 SwiGLU output as in W4A16, quantised per (token, expert) row.
  *  - SwiGLU: h = silu(gate) * up, silu(z) = z / (1 + exp(-z)); h is rounded to
  *    BF16 (round to nearest even) before the down projection.
  *  - Output: sum of routing-weighted routed outputs plus the shared outputs,
@@ -84,7 +107,9 @@
  *   3 gate and up rows swapped, 4 shared experts dropped from the combine,
  *   5 E2M1 subnormal (code 1) decoded as 1.0 instead of 0.5,
  *   6 MX scales taken per 16 elements instead of per 32,
- *   7 FP8 block scales indexed with rows and columns swapped.
+ *   7 FP8 block scales indexed with rows and columns swapped,
+ *   8 Four-Over-Six keeping the candidate with the larger error,
+ *   9 Four-Over-Six ties going to 4.
  * The regular build plants nothing. */
 #ifndef ORC_PLANT
 #define ORC_PLANT 0
@@ -248,6 +273,88 @@ void orc_dequant(const uint8_t *codes, const uint8_t *sf, float gs,
             out[(size_t)r * cols + k] = (float)wexact(codes, sf, (double)gs, cols, r, k);
 }
 
+/* ------------------------------------------------------------------------- */
+/* Four-Over-Six NVFP4 activation quantisation (FP32 decisions).             */
+/* ------------------------------------------------------------------------- */
+
+/* Round a non-negative FP32 value to the nearest E4M3 (fn) value, ties to
+ * even (mantissa bit 0), saturating at 448; returns the code. */
+int orc_e4m3_from_f32(float v)
+{
+    if (!(v > 0.0f)) return 0;                    /* zero (and NaN, not used) */
+    if (v >= 448.0f) return 0x7E;
+    int best = 0;
+    double bd = 1e300;
+    for (int c = 0; c <= 0x7E; ++c) {             /* every finite non-negative code */
+        double d = fabs(orc_e4m3(c) - (double)v);
+        /* nearest; on an exact tie the even code (codes ascend with the value,
+         * so the two candidates are adjacent and differ in mantissa bit 0) */
+        if (d < bd || (d == bd && (c & 1) == 0)) { bd = d; best = c; }
+    }
+    return best;
+}
+
+/* Round a FP32 value to the nearest E2M1 value, ties to even (mantissa bit
+ * 0), saturating at +-6; returns the 4-bit code. */
+int orc_e2m1_from_f32(float v)
+{
+    double a = fabs((double)v);
+    int best = 0;
+    double bd = 1e300;
+    for (int c = 0; c < 8; ++c) {
+        double d = fabs(orc_e2m1(c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) { bd = d; best = c; }
+    }
+    if (a > 6.0) best = 7;
+    return (v < 0.0f && best != 0) ? (best | 8) : best;
+}
+
+/* Quantise one row of n BF16 values (n % 16 == 0): codes (one nibble per
+ * byte, value = code), block scale codes [n/16] and choices [n/16] (4 or 6),
+ * the global scale returned; deq[n] (optional) the dequantised values. */
+float orc_quant_fos(const uint16_t *row, int n, uint8_t *codes, uint8_t *sf, uint8_t *choice, double *deq)
+{
+    float a = 0.0f;
+    for (int k = 0; k < n; ++k) {
+        float v = (float)orc_bf16_to_double(row[k]);
+        a = fabsf(v) > a ? fabsf(v) : a;
+    }
+    const float gs = a > 0.0f ? a / 1792.0f : 1.0f;
+    for (int b = 0; b < n / 16; ++b) {
+        float v[16], m = 0.0f;
+        for (int k = 0; k < 16; ++k) {
+            v[k] = (float)orc_bf16_to_double(row[16 * b + k]);
+            m = fabsf(v[k]) > m ? fabsf(v[k]) : m;
+        }
+        int sc_c[2], q_c[2][16];
+        float err[2];
+        const float cand[2] = {6.0f, 4.0f};
+        for (int i = 0; i < 2; ++i) {
+            const float cg = cand[i] * gs;
+            sc_c[i] = orc_e4m3_from_f32(m / cg);
+            const float s = (float)orc_e4m3(sc_c[i]);
+            const float d = s * gs;
+            float e = 0.0f;
+            for (int k = 0; k < 16; ++k) {
+                q_c[i][k] = s > 0.0f ? orc_e2m1_from_f32(v[k] / d) : 0;
+                const float r = (float)orc_e2m1(q_c[i][k]) * s * gs;
+                e += fabsf(v[k] - r);
+            }
+            err[i] = e;
+        }
+        int pick = (err[1] < err[0]) ? 1 : 0;                 /* ties: 6 */
+        if (ORC_PLANT == 8) pick = (err[1] > err[0]) ? 1 : 0;
+        if (ORC_PLANT == 9) pick = (err[1] <= err[0]) ? 1 : 0;
+        sf[b] = (uint8_t)sc_c[pick];
+        if (choice) choice[b] = (uint8_t)(pick ? 4 : 6);
+        for (int k = 0; k < 16; ++k) {
+            codes[16 * b + k] = (uint8_t)q_c[pick][k];
+            if (deq) deq[16 * b + k] = orc_e2m1(q_c[pick][k]) * orc_e4m3(sc_c[pick]) * (double)gs;
+        }
+    }
+    return gs;
+}
+
 /* Dequantise a [rows, cols] matrix of any expert format to FP32: one
  * rounding of the exact value (gs: NVFP4 only). */
 void orc_dequant_fmt(int fmt, const uint8_t *codes, const uint8_t *sf, float gs,
@@ -283,6 +390,7 @@ typedef struct {
     const float *sw2_gs;        /* [S] */
     int score_func;             /* 0: sigmoid per expert; 1: softmax over all experts */
     int efmt, sfmt;             /* weight format of the routed / shared experts (ORC_*) */
+    int w4a4;                   /* 1: activations quantised with Four-Over-Six NVFP4 */
 } orc_layer;
 
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
@@ -359,11 +467,28 @@ int orc_route(const orc_layer *L, const uint16_t *x, int T, int *ids, double *w,
  *   h_n = bf16(silu(g_n) * u_n)
  *   y_m = sum_n h_n Wd[m,n]
  * All weights are the exact dequantised values. */
+/* The W4A4 activation: the Four-Over-Six dequantised values of a row of
+ * doubles that are BF16 values (x rows, h rows). */
+static void quant_row(const double *v, int n, double *out)
+{
+    uint16_t *b = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n);
+    uint8_t *codes = (uint8_t *)malloc((size_t)n), *sf = (uint8_t *)malloc((size_t)n / 16 + 1);
+    for (int k = 0; k < n; ++k) b[k] = orc_double_to_bf16(v[k]);
+    orc_quant_fos(b, n, codes, sf, NULL, out);
+    free(b); free(codes); free(sf);
+}
+
 static void expert_mlp(int fmt, int H, int I,
                        const uint8_t *w13, const uint8_t *w13_sf, const float *w13_gs,
                        const uint8_t *w2, const uint8_t *w2_sf, const float *w2_gs,
-                       const double *x, double *h, double *y)
+                       const double *x, double *h, double *y, int w4a4)
 {
+    double *xq = NULL;
+    if (w4a4) {
+        xq = (double *)malloc(sizeof(double) * (size_t)H);
+        quant_row(x, H, xq);
+        x = xq;
+    }
     /* tensor scales: NVFP4 only */
     const int nv = fmt == ORC_NVFP4;
     double gsg = nv ? (double)w13_gs[0] : 1.0, gsu = nv ? (double)w13_gs[1] : 1.0;
@@ -384,6 +509,10 @@ static void expert_mlp(int fmt, int H, int I,
         }
         double silu = g * sigmoid(g);
         h[n] = orc_bf16_round(silu * u);
+    }
+    if (w4a4) {
+        quant_row(h, I, h);
+        free(xq);
     }
     for (int m = 0; m < H; ++m) {
         double acc = 0.0;
@@ -439,7 +568,7 @@ int orc_forward(const orc_layer *L, const uint16_t *x, int T, uint16_t *out,
                        nv ? L->w13_gs + 2 * (size_t)e : NULL,
                        L->w2 + (size_t)e * orc_codes_bytes(f, H, I),
                        L->w2_sf + (size_t)e * orc_scale_bytes(f, H, I),
-                       nv ? L->w2_gs + e : NULL, xt, h, yp);
+                       nv ? L->w2_gs + e : NULL, xt, h, yp, L->w4a4);
         } else {
             int sidx = j - K, I = L->Is, f = L->sfmt;
             int nv = f == ORC_NVFP4;
@@ -449,7 +578,7 @@ int orc_forward(const orc_layer *L, const uint16_t *x, int T, uint16_t *out,
                        nv ? L->sw13_gs + 2 * (size_t)sidx : NULL,
                        L->sw2 + (size_t)sidx * orc_codes_bytes(f, H, I),
                        L->sw2_sf + (size_t)sidx * orc_scale_bytes(f, H, I),
-                       nv ? L->sw2_gs + sidx : NULL, xt, h, yp);
+                       nv ? L->sw2_gs + sidx : NULL, xt, h, yp, L->w4a4);
         }
         free(h);
     }

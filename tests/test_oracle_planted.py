@@ -6,6 +6,7 @@ that should expose it: at least one of them must fail.  The regular library
 is restored afterwards, and every pin passes on it (the other test files)."""
 import pytest
 
+import test_oracle_fos as fos
 import test_oracle_formats as fmt
 import test_oracle_layer as lay
 import test_oracle_mxfp8 as mx
@@ -29,6 +30,10 @@ CASES = [
     (7, "FP8 block scales indexed with rows and columns swapped",
      [lambda orc: mx.test_dequant_matches_nvfp4_on_shared_values(orc, "fp8_block"),
       mx.test_fp8_block_single_expert_equals_dense_mlp]),
+    (8, "Four-Over-Six keeping the candidate with the larger error",
+     [fos.test_four_wins_where_it_is_exact, fos.test_six_wins_where_it_is_exact]),
+    (9, "Four-Over-Six ties going to 4",
+     [fos.test_tie_goes_to_six_and_zero_rows]),
 ]
 
 
