@@ -43,6 +43,8 @@ WORKLOADS = {
     "inkling": (6, 2),        # Inkling-2-Small-shaped, NVFP4 experts
     "inkling_mx8": (7, 2),    # the same with MXFP8 experts
     "flint_mx4": (8, 47),     # Flint-shaped, MXFP4 experts
+    "inkling_w4a4": (9, 2),   # Inkling-2-Small-shaped, W4A4 (Four-Over-Six activations)
+    "zipf64_w4a4": (10, 16),  # Zipf-routed Flint-shaped T=64, W4A4
 }
 
 # DRAM bytes (read + write) per launch of the single-launch kernel, from one
@@ -74,7 +76,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="override layers per step")
     ap.add_argument("--secondary", default="flint8", help="second workload reported in the line ('' = none)")
     ap.add_argument("--extras", default="ml4,zipf64,zipf64-gemv,tiny,ml4fp8s,inkling,inkling_mx8,flint_mx4,"
-                                        "flint1-coop,flint8-coop",
+                                        "inkling_w4a4,zipf64_w4a4,flint1-coop,flint8-coop",
                     help="further workloads timed and reported under 'workloads' ('' = none); "
                          "a '-gemv' suffix turns the grouped kernels off, '-coop' launches the single "
                          "launch as a cooperative grid")
@@ -507,7 +509,8 @@ def run_gpu(args):
         one = ch2.layers[0].info().single_launch_max_tokens >= ch2.T
         res = {"workload": f"{c2['name']}: T={c2['T']} H={c2['H']} E={c2['E']} top-{c2['k']} "
                            f"I={c2['I']} +{c2['S']} shared, experts {c2['efmt']}, shared {c2['sfmt']}, "
-                           f"{oL} layers per step",
+                           + ("W4A4 Four-Over-Six activations, " if c2.get("w4a4") else "")
+                           + f"{oL} layers per step",
                "us_per_layer": us2, "GBps": b2 / (us2 * 1e-6) / 1e9,
                "frac_of_measured": b2 / (us2 * 1e-6) / 1e9 / peak,
                "selected_bytes_per_layer": b2, "unique_experts_mean": float(np.mean(U2)),

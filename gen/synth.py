@@ -62,6 +62,9 @@ CONFIGS = {
     7: dict(name="inkling_mx8", T=8, H=4096, E=384, k=8, I=2560, S=0, Is=2560, zipf=False, efmt="mxfp8"),
     8: dict(name="flint_mx4", T=1, H=2048, E=256, k=6, I=768, S=1, Is=768, zipf=False, efmt="mxfp4",
             sfmt="mxfp4"),
+    # W4A4: activations quantised with Four-Over-Six NVFP4 before each GEMM
+    9: dict(name="inkling_w4a4", T=8, H=4096, E=384, k=8, I=2560, S=0, Is=2560, zipf=False, w4a4=1),
+    10: dict(name="zipf64_w4a4", T=64, H=2048, E=256, k=6, I=768, S=1, Is=768, zipf=True, w4a4=1),
 }
 
 FORMATS = ("nvfp4", "mxfp4", "fp8_block", "mxfp8")
@@ -94,6 +97,7 @@ def config(idx_or_name, **over) -> dict:
     c.setdefault("routed_scale", 1.0)
     c.setdefault("efmt", "nvfp4")
     c.setdefault("sfmt", "nvfp4")
+    c.setdefault("w4a4", 0)
     c.update(over)
     return c
 

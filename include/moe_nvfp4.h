@@ -102,7 +102,7 @@ typedef enum {
  *   0 <= num_shared <= 2
  *   1 <= max_tokens <= 64
  *   normalize_topk in {0, 1}, score_func in {0, 1}, routed_scale finite
- *   expert_format, shared_format in MOE_FMT_*                                */
+ *   expert_format, shared_format in MOE_FMT_*, w4a4 in {0, 1}                */
 typedef struct {
     int hidden;             /* H */
     int num_experts;        /* E routed experts */
@@ -138,6 +138,19 @@ typedef struct {
                                exp(z_i - z_max)), times routed_scale. */
     int expert_format;      /* MOE_FMT_* of the routed experts (0 = NVFP4) */
     int shared_format;      /* MOE_FMT_* of the shared experts (0 = NVFP4) */
+    int w4a4;               /* 1: W4A4 -- the tokens (before gate/up) and the
+                               SwiGLU output (before down) are quantised to
+                               NVFP4 with "Four Over Six" block scales
+                               ("Inkling 2 Small on vLLM: Day-0 Support",
+                               "Mixed-precision MoE and Four-Over-Six NVFP4"):
+                               a per-row global scale a / 1792 (a the row's
+                               max |v|), and per 16-element block the block
+                               maximum scaled to 6 and to 4, keeping the lower
+                               sum of absolute reconstruction errors (ties: 6),
+                               every step in FP32.  The router reads the
+                               unquantised x.  Such layers run the chain (no
+                               single launch); the GEMMs see the dequantised
+                               values, exact in f16, on the same kernels. */
 } moe_config;
 
 /* Weights in the canonical layout (device pointers, only read during
@@ -322,6 +335,20 @@ moe_status moe_route_topk_static(const float *router_w, const float *router_b,
                                  int normalize_topk, float routed_scale,
                                  const void *x, int T, int *topk_ids,
                                  float *topk_w, void *stream);
+
+/* The W4A4 activation quantiser on its own (moe_config.w4a4 applies it to
+ * the tokens and to the SwiGLU output): "Four Over Six" NVFP4 quantisation of
+ * `rows` rows of n BF16 values ("Inkling 2 Small on vLLM: Day-0 Support",
+ * "Mixed-precision MoE and Four-Over-Six NVFP4"), as described at
+ * moe_config.w4a4.
+ *   x    BF16 [rows, n] device, read
+ *   deq  BF16 [rows, n] device, written (may equal x): the dequantised values
+ *        without the global scale, e2m1 * e4m3 (exact in BF16)
+ *   gs   FP32 [rows] device, written: the rows' global scales (value =
+ *        deq * gs)
+ * n must be a positive multiple of 16, rows >= 0.  Asynchronous on
+ * `stream`; no handle is needed. */
+moe_status moe_quant_fos(const void *x, int rows, int n, void *deq, float *gs, void *stream);
 
 /* Reasons for the last failure on this host thread ("" if none). */
 const char *moe_last_error(void);

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe_nvfp4.so")
-SOURCES = ["abi.cu", "route.cu", "gemv.cu", "fused.cu", "grouped.cu", "repack.cu", "route_static.cu"]
+SOURCES = ["abi.cu", "route.cu", "gemv.cu", "fused.cu", "grouped.cu", "repack.cu", "route_static.cu", "quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

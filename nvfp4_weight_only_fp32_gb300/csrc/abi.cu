@@ -88,6 +88,7 @@ std::vector<std::string> unsupported_reasons(const moe_config *c) {
         "expert_format must be 0 (NVFP4), 1 (MXFP4), 2 (FP8 block) or 3 (MXFP8)");
     chk(c->shared_format >= MOE_FMT_NVFP4 && c->shared_format <= MOE_FMT_MXFP8,
         "shared_format must be 0 (NVFP4), 1 (MXFP4), 2 (FP8 block) or 3 (MXFP8)");
+    chk(c->w4a4 == 0 || c->w4a4 == 1, "w4a4 must be 0 or 1");
     return why;
 }
 
@@ -186,6 +187,9 @@ void carve_workspace(moe_layer *L, char *base) {
     d.hot_slots = cv.take<int>(d.max_slots);
     d.tg_ticket = cv.take<unsigned>(Tm);
     d.emask = cv.take<unsigned long long>(E);
+    d.xq = cv.take<__nv_bfloat16>((size_t)Tm * H);
+    d.gsx = cv.take<float>(Tm);
+    d.gsh = cv.take<float>(d.max_pairs);
     L->x_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->out_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->ids_stage = cv.take<int>((size_t)Tm * K);
@@ -393,6 +397,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     d.debug_stall = 0;
     d.f8e = is_f8(cfg->expert_format);
     d.f8s = S > 0 && is_f8(cfg->shared_format);
+    d.w4a4 = cfg->w4a4;
 
     carve_weights(L, nullptr);
     carve_workspace(L, nullptr);
@@ -449,7 +454,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
         d.grouped_min = L->cfg.grouped_min_tokens;
     for (int T = 0; T <= kMaxTokens; ++T) {
         L->fused_ok[T] = 0;
-        if (e == cudaSuccess && cfg->fused >= 0 && T >= 1 && T <= cfg->max_tokens &&
+        if (e == cudaSuccess && cfg->fused >= 0 && !cfg->w4a4 && T >= 1 && T <= cfg->max_tokens &&
             fused_eligible(d, T, L->sm_count, (size_t)L->optin_smem))
             L->fused_ok[T] = fused_blocks_per_sm(d, T) >= 1;
     }
@@ -490,11 +495,19 @@ moe_status moe_stage_gate_up(moe_layer *L, const void *x, int T, void *stream) {
     if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, L->sm_count, L->optin_smem, st);
+    const __nv_bfloat16 *xa = static_cast<const __nv_bfloat16 *>(x);
+    cudaError_t e = cudaSuccess;
+    if (L->d.w4a4) {
+        // W4A4: the tokens quantised first (their f16 prescale exponents
+        // replace the router's); gate/up reads the dequantised rows
+        e = launch_fos(xa, L->d.xq, T, L->cfg.hidden, L->cfg.hidden, 0, 0, L->d.gsx, L->d.xexp, nullptr, st);
+        xa = L->d.xq;
+    }
+    if (e == cudaSuccess) e = launch_gate_up(L->d, xa, T, L->sm_count, L->optin_smem, st);
     // above 8 tokens the GEMV kernel leaves the slots with >= grouped_min
     // tokens to the grouped tensor-core kernel
     if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)
-        e = launch_grouped_gate_up(L->d, static_cast<const __nv_bfloat16 *>(x), T, L->sm_count, st);
+        e = launch_grouped_gate_up(L->d, xa, T, L->sm_count, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gate/up launch");
 }
 
@@ -504,7 +517,15 @@ moe_status moe_stage_down(moe_layer *L, int T, void *out, void *stream) {
     if (!out || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "out is NULL or not 16-byte aligned");
     DeviceGuard g(L->device);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out), st);
+    cudaError_t e = cudaSuccess;
+    if (L->d.w4a4) {
+        // W4A4: the h rows quantised in place (the shared experts' pairs
+        // first, rows of Is; then the routed ones, rows of I); their maxima
+        // replace those the SwiGLU epilogue left for the down prescale
+        const DevLayer &d = L->d;
+        e = launch_fos(d.h_ws, d.h_ws, T * (d.k + d.S), d.Imax, d.I, d.S * T, d.Is, d.gsh, nullptr, d.hmax, st);
+    }
+    if (e == cudaSuccess) e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out), st);
     if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)
         e = launch_grouped_down(L->d, T, static_cast<__nv_bfloat16 *>(out), L->sm_count, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");
@@ -657,6 +678,17 @@ moe_status moe_debug_inject(moe_layer *L, int what, int value) {
     if (value < 0) return fail(MOE_ERR_INVALID_ARG, "injection value must be >= 0");
     L->inject_stall = value;
     return MOE_OK;
+}
+
+moe_status moe_quant_fos(const void *x, int rows, int n, void *deq, float *gs, void *stream) {
+    g_err.clear();
+    if (rows < 0 || n <= 0 || n % 16 != 0)
+        return fail(MOE_ERR_INVALID_ARG, "rows must be >= 0 and n a positive multiple of 16");
+    if (rows == 0) return MOE_OK;
+    if (!x || !deq || !gs) return fail(MOE_ERR_INVALID_ARG, "x, deq or gs is NULL");
+    cudaError_t e = launch_fos(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(deq), rows, n, n,
+                               0, 0, gs, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "quantiser launch");
 }
 
 moe_status moe_get_info(const moe_layer *L, moe_layer_info *info) {

@@ -249,18 +249,21 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
     if (threadIdx.x < m) {
         const int j = threadIdx.x;
         int ex;
+        float gq = 1.f;    // W4A4: the row's global scale
         const __nv_bfloat16 *row;
         if (MODE == 0) {
             const int tok = shared ? j : __ldcg(d.pair_tok + p0 + j);
             row = x + (size_t)tok * d.H;
             ex = __ldcg(d.xexp + tok);
+            if (d.w4a4) gq = __ldcg(d.gsx + tok);
         } else {
             row = d.h_ws + (size_t)(p0 + j) * d.Imax;
             ex = hexp_of(__ldcg(d.hmax + p0 + j));
+            if (d.w4a4) gq = __ldcg(d.gsh + p0 + j);
         }
         s_src[j] = reinterpret_cast<const uint4 *>(row);
         s_scale[j] = pow2f(-ex);
-        s_unscale[j] = pow2f(ex);
+        s_unscale[j] = pow2f(ex) * gq;
     }
     // Zero the padding rows once; no stage writes them.
     for (int i = threadIdx.x; i < (mpad - m) * (row_stride / 16); i += kThreads)
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
         const int ex = __ldcg(d.xexp + t);
         s_src[t] = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
         s_scale[t] = pow2f(-ex);
-        s_unscale[t] = pow2f(ex);
+        s_unscale[t] = pow2f(ex) * (d.w4a4 ? __ldcg(d.gsx + t) : 1.f);
     }
     for (int i = threadIdx.x; i < row_stride / 16; i += kUT)
         reinterpret_cast<uint4 *>(smem + (size_t)T * row_stride)[i] = make_uint4(0u, 0u, 0u, 0u);

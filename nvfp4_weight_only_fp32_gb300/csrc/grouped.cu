@@ -280,11 +280,12 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
         if (warp < kDecW) {
             const int col = 32 * (warp >> 2) + lane;
             if (col < m) {
+                // (W4A4: times the row's global scale)
                 if (MODE == 0) {
                     const int tok = shared ? col : __ldcg(d.pair_tok + p0 + col);
-                    col_un = pow2f(__ldcg(d.xexp + tok));
+                    col_un = pow2f(__ldcg(d.xexp + tok)) * (d.w4a4 ? __ldcg(d.gsx + tok) : 1.f);
                 } else {
-                    col_un = pow2f(hexp_of(__ldcg(d.hmax + p0 + col)));
+                    col_un = pow2f(hexp_of(__ldcg(d.hmax + p0 + col))) * (d.w4a4 ? __ldcg(d.gsh + p0 + col) : 1.f);
                 }
             }
         }

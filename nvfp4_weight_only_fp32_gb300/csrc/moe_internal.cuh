@@ -121,6 +121,10 @@ struct DevLayer {
     int trace_blocks;
     int score_func;                 // 0 sigmoid per expert, 1 softmax over all experts
     int f8e, f8s;                   // routed / shared experts stored as F8 chunks
+    int w4a4;                       // activations quantised (Four-Over-Six NVFP4) before each GEMM
+    __nv_bfloat16 *xq;              // [Tm, H] W4A4: the tokens' dequantised e2m1 * e4m3 values
+    float *gsx;                     // [Tm] W4A4: their global scales
+    float *gsh;                     // [max_pairs] W4A4: the h rows' global scales
 };
 
 // Chunks per tile row of K elements, in the NVFP4 or the F8 chunk layout.
@@ -156,6 +160,13 @@ cudaError_t launch_dequant(const uint8_t *rep, float gs_a, float gs_b, int rows,
 cudaError_t launch_repack_f8(const uint8_t *codes, const void *sf, int fmt, int n_mats, int rows, int cols,
                              bool gate_up, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_dequant_f8(const uint8_t *rep, int rows, int cols, bool gate_up, float *dst, cudaStream_t s);
+// Four-Over-Six NVFP4 quantisation of activation rows (quant.cu): rows of
+// `stride` elements, the first n_short of length len_short, the rest len_long;
+// writes the dequantised e2m1 * e4m3 values (BF16, exact) to dst (may be
+// src), the global scales, and (optional) the f16 prescale exponent and the
+// max |value| bits of each row.
+cudaError_t launch_fos(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int nrows, int stride, int len_long,
+                       int n_short, int len_short, float *gs, int *exp_out, unsigned *max_out, cudaStream_t s);
 // MXFP4 scales: per (matrix, half) the smallest and largest E8M0 code and
 // whether a NaN code (255) occurs -> mm[(mat * 2 + half) * 3 + {0,1,2}]
 // (half 1 only for gate/up: its up rows).

@@ -28,7 +28,7 @@ EXPORTED = [
     "moe_init", "moe_destroy", "moe_decode_forward", "moe_decode_forward_host",
     "moe_stage_route", "moe_stage_gate_up", "moe_stage_down",
     "moe_check", "moe_debug_dequant", "moe_get_info", "moe_last_error",
-    "moe_route_topk_static", "moe_trace_attach", "moe_debug_inject",
+    "moe_route_topk_static", "moe_trace_attach", "moe_debug_inject", "moe_quant_fos",
 ]
 
 MOE_INJECT_WAIT_STALL = 1
@@ -40,7 +40,7 @@ class moe_config(ctypes.Structure):
                 ("max_tokens", ctypes.c_int), ("normalize_topk", ctypes.c_int),
                 ("routed_scale", ctypes.c_float), ("grouped_min_tokens", ctypes.c_int),
                 ("fused", ctypes.c_int), ("score_func", ctypes.c_int),
-                ("expert_format", ctypes.c_int), ("shared_format", ctypes.c_int)]
+                ("expert_format", ctypes.c_int), ("shared_format", ctypes.c_int), ("w4a4", ctypes.c_int)]
 
 SCORE_FUNCS = {"sigmoid": 0, "softmax": 1}
 # expert weight formats (MOE_FMT_* of the header)
@@ -109,6 +109,8 @@ def lib(path: str | None = None):
             L.moe_trace_attach.restype = st
             L.moe_debug_inject.argtypes = [vp, i, i]
             L.moe_debug_inject.restype = st
+            L.moe_quant_fos.argtypes = [vp, i, i, vp, vp, vp]
+            L.moe_quant_fos.restype = st
             L.moe_last_error.argtypes = []
             L.moe_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -203,6 +205,10 @@ def moe_route_topk_static(router_w, router_b, num_experts, hidden, top_k, normal
                                        ctypes.c_void_p(_stream(stream))))
 
 
+def moe_quant_fos(x, rows, n, deq, gs, stream=None) -> None:
+    _check(lib().moe_quant_fos(_p(x), int(rows), int(n), _p(deq), _p(gs), ctypes.c_void_p(_stream(stream))))
+
+
 # --- convenience wrapper ------------------------------------------------------
 
 _NAMES = ("router_w", "router_b", "w13", "w13_sf", "w13_gs", "w2", "w2_sf", "w2_gs",
@@ -234,7 +240,8 @@ def make_config(c: dict, max_tokens: int | None = None, grouped_min_tokens: int 
                       grouped_min_tokens=int(grouped_min_tokens), fused=int(fused),
                       score_func=SCORE_FUNCS[c.get("score_func", "sigmoid")],
                       expert_format=FORMATS[c.get("efmt", "nvfp4")],
-                      shared_format=FORMATS[c.get("sfmt", "nvfp4")])
+                      shared_format=FORMATS[c.get("sfmt", "nvfp4")],
+                      w4a4=int(bool(c.get("w4a4", 0))))
 
 
 class MoELayer:
@@ -243,7 +250,7 @@ class MoELayer:
     `layer` is a dict of canonical tensors (numpy or torch) plus "cfg" with the
     sizes H, E, k, I, S, Is and, optionally, "normalize" (1), "routed_scale"
     (1.0), "score_func" ("sigmoid" or "softmax") and the expert formats
-    "efmt" / "sfmt" ("nvfp4", "mxfp4", "fp8_block" or "mxfp8");
+    "efmt" / "sfmt" ("nvfp4", "mxfp4", "fp8_block" or "mxfp8") and "w4a4" (0/1);
     the weights are repacked into library memory, so the inputs may be freed
     afterwards."""
 

@@ -36,7 +36,7 @@ def build(force: bool = False, plant: int = 0) -> str:
             and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
         return out
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c99",
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", "-std=c99",
            "-D_DEFAULT_SOURCE", f"-DORC_PLANT={int(plant)}", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)

@@ -96,7 +96,8 @@
  *  - Output: sum of routing-weighted routed outputs plus the shared outputs,
  *    accumulated in FP64, rounded once to BF16.
  *
- * Build: gcc -O2 -fPIC -shared -fopenmp oracle.c -o liboracle.so -lm
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared -fopenmp oracle.c -o liboracle.so -lm
+ * (no fused multiply-adds: the quantiser's FP32 steps are each rounded)
  */
 #include <math.h>
 #include <stdint.h>

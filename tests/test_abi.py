@@ -47,11 +47,11 @@ def test_struct_layout_matches_header(moe, tmp_path):
 #include <stddef.h>
 #include "moe_nvfp4.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_layer_info),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(moe_config), sizeof(moe_weights), sizeof(moe_layer_info),
          offsetof(moe_config, routed_scale), offsetof(moe_config, grouped_min_tokens),
          offsetof(moe_weights, sw2_gs), offsetof(moe_layer_info, sm_count),
          offsetof(moe_config, fused), offsetof(moe_layer_info, single_launch_max_tokens),
-         offsetof(moe_config, score_func));
+         offsetof(moe_config, score_func), offsetof(moe_config, expert_format), offsetof(moe_config, w4a4));
   return 0; }
 ''')
     exe = tmp_path / "layout"
@@ -61,7 +61,8 @@ int main(void) {
             ctypes.sizeof(moe.moe_layer_info), moe.moe_config.routed_scale.offset,
             moe.moe_config.grouped_min_tokens.offset, moe.moe_weights.sw2_gs.offset,
             moe.moe_layer_info.sm_count.offset, moe.moe_config.fused.offset,
-            moe.moe_layer_info.single_launch_max_tokens.offset, moe.moe_config.score_func.offset]
+            moe.moe_layer_info.single_launch_max_tokens.offset, moe.moe_config.score_func.offset,
+            moe.moe_config.expert_format.offset, moe.moe_config.w4a4.offset]
     assert got == want
 
 
@@ -75,11 +76,11 @@ def _cfg(moe, **kw):
 def test_default_deny_lists_every_reason(moe):
     L = moe.lib()
     h = ctypes.c_void_p()
-    bad = _cfg(moe, hidden=100, inter=0, top_k=9, max_tokens=65, num_shared=3, score_func=2)
+    bad = _cfg(moe, hidden=100, inter=0, top_k=9, max_tokens=65, num_shared=3, score_func=2, w4a4=2)
     rc = L.moe_init(ctypes.byref(bad), ctypes.byref(moe.moe_weights()), None, ctypes.byref(h))
     assert rc == moe.moe.MOE_ERR_UNSUPPORTED
     msg = moe.last_error()
-    for frag in ("hidden", "inter", "top_k", "max_tokens", "num_shared", "score_func"):
+    for frag in ("hidden", "inter", "top_k", "max_tokens", "num_shared", "score_func", "w4a4"):
         assert frag in msg, (frag, msg)
     assert not h.value
 
@@ -105,3 +106,13 @@ def test_calls_on_null_handle(moe):
     assert L.moe_check(None, None) == moe.moe.MOE_ERR_INVALID_ARG
     assert L.moe_get_info(None, None) == moe.moe.MOE_ERR_INVALID_ARG
     L.moe_destroy(None)
+
+
+def test_quantiser_arguments_checked_before_any_launch(moe):
+    L = moe.lib()
+    assert L.moe_quant_fos(None, 2, 24, None, None, None) == moe.moe.MOE_ERR_INVALID_ARG
+    assert "multiple of 16" in moe.last_error()
+    assert L.moe_quant_fos(None, -1, 32, None, None, None) == moe.moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quant_fos(None, 1, 32, None, None, None) == moe.moe.MOE_ERR_INVALID_ARG
+    assert "NULL" in moe.last_error()
+    assert L.moe_quant_fos(None, 0, 32, None, None, None) == moe.moe.MOE_OK    # nothing to do
