@@ -190,6 +190,11 @@ void carve_workspace(moe_layer *L, char *base) {
     d.xq = cv.take<__nv_bfloat16>((size_t)Tm * H);
     d.gsx = cv.take<float>(Tm);
     d.gsh = cv.take<float>(d.max_pairs);
+    const bool q4 = c.w4a4 != 0;   // the packed codes only for W4A4 layers
+    d.xq4 = cv.take<uint8_t>(q4 ? (size_t)Tm * H / 2 : 0);
+    d.xsf = cv.take<uint8_t>(q4 ? (size_t)Tm * H / 16 : 0);
+    d.hq4 = cv.take<uint8_t>(q4 ? (size_t)d.max_pairs * d.Imax / 2 : 0);
+    d.hsf = cv.take<uint8_t>(q4 ? (size_t)d.max_pairs * d.Imax / 16 : 0);
     L->x_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->out_stage = cv.take<__nv_bfloat16>((size_t)Tm * H);
     L->ids_stage = cv.take<int>((size_t)Tm * K);
@@ -500,7 +505,9 @@ moe_status moe_stage_gate_up(moe_layer *L, const void *x, int T, void *stream) {
     if (L->d.w4a4) {
         // W4A4: the tokens quantised first (their f16 prescale exponents
         // replace the router's); gate/up reads the dequantised rows
-        e = launch_fos(xa, L->d.xq, T, L->cfg.hidden, L->cfg.hidden, 0, 0, L->d.gsx, L->d.xexp, nullptr, st);
+        const int H = L->cfg.hidden;
+        e = launch_fos(xa, L->d.xq, T, H, H, 0, 0, L->d.gsx, L->d.xexp, nullptr, L->d.xq4, L->d.xsf, H / 2, H / 16,
+                       st);
         xa = L->d.xq;
     }
     if (e == cudaSuccess) e = launch_gate_up(L->d, xa, T, L->sm_count, L->optin_smem, st);
@@ -523,7 +530,8 @@ moe_status moe_stage_down(moe_layer *L, int T, void *out, void *stream) {
         // first, rows of Is; then the routed ones, rows of I); their maxima
         // replace those the SwiGLU epilogue left for the down prescale
         const DevLayer &d = L->d;
-        e = launch_fos(d.h_ws, d.h_ws, T * (d.k + d.S), d.Imax, d.I, d.S * T, d.Is, d.gsh, nullptr, d.hmax, st);
+        e = launch_fos(d.h_ws, d.h_ws, T * (d.k + d.S), d.Imax, d.I, d.S * T, d.Is, d.gsh, nullptr, d.hmax, d.hq4,
+                       d.hsf, d.Imax / 2, d.Imax / 16, st);
     }
     if (e == cudaSuccess) e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out), st);
     if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)
@@ -687,7 +695,8 @@ moe_status moe_quant_fos(const void *x, int rows, int n, void *deq, float *gs, v
     if (rows == 0) return MOE_OK;
     if (!x || !deq || !gs) return fail(MOE_ERR_INVALID_ARG, "x, deq or gs is NULL");
     cudaError_t e = launch_fos(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(deq), rows, n, n,
-                               0, 0, gs, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+                               0, 0, gs, nullptr, nullptr, nullptr, nullptr, 0, 0,
+                               reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "quantiser launch");
 }
 

@@ -56,20 +56,40 @@ constexpr int kLA = 2;                            // B-operand chunks in flight 
 constexpr int kMT = 128;                          // weight rows per item (8 tiles)
 constexpr int kNmax = kMaxTokens;                 // tokens per slot
 constexpr uint32_t kLBO = 128;                    // K-adjacent core matrices
-constexpr uint32_t kSBO = kCPS * 8 * 128;         // row-adjacent core matrices (8 K-groups per chunk)
-constexpr int kAStage = kMT * kChunkK * kCPS * 2; // 32 KB
-constexpr int kBStage = kNmax * kChunkK * kCPS * 2;   // 16 KB
 constexpr int kScratch = kMaxTokens * (kMaxTopK + kMaxShared) * 8;   // combine's pair table
 constexpr int kCHA = 4;                           // chunks per raw-weight segment
 constexpr int kRWA = 3;                           // raw-weight segments per decode warp
-constexpr int kRawOff = kNS * (kAStage + kBStage) + kScratch;
-constexpr int kBRawOff = kRawOff + kDecW * kRWA * kCHA * kChunkBytes;
-constexpr int kBRawStage = kNmax * kChunkK * 2;   // one chunk of the slot's token rows, as stored (8 KB)
-constexpr int kSmem = kBRawOff + kLA * kBRawStage;
 static_assert((kLA & (kLA - 1)) == 0, "kLA is a power of two");
 constexpr int kMaxItems = 128;                    // work items per block
-constexpr uint32_t kTmemCols = 64;                // >= N, a power of two >= 32
 constexpr unsigned long long kWaitNs = 1000000000ull;
+
+// Shared-memory and TMEM geometry.  f16 operands (W4A16): a 64-wide K chunk
+// of a row is 128 bytes, 8 core matrices.  E2M1 operands (W4A4, block-scaled
+// MMA): 32 bytes, 2 core matrices, plus one 32-bit word of four E4M3 scales
+// per row and chunk, staged in shared memory on the way to TMEM.
+template <bool FP4>
+struct Geo {
+    static constexpr int kRowB = FP4 ? 32 : kChunkK * 2;       // bytes of one row of a chunk
+    static constexpr uint32_t kSBO = kCPS * kRowB / 16 * 128;   // row-adjacent core matrices
+    static constexpr int kAStage = kMT * kRowB * kCPS;          // f16 32 KB, E2M1 8 KB
+    static constexpr int kBStage = kNmax * kRowB * kCPS;        // f16 16 KB, E2M1 4 KB
+    static constexpr int kSfStage = FP4 ? kCPS * kMT * 4 : 0;   // the A scale words of a stage
+    static constexpr int kScrOff = kNS * (kAStage + kBStage + kSfStage);
+    static constexpr int kRawOff = kScrOff + kScratch;
+    static constexpr int kBRawOff = kRawOff + kDecW * kRWA * kCHA * kChunkBytes;
+    // one chunk of the slot's token rows as stored: f16 path the BF16 rows
+    // (8 KB); E2M1 path the codes (2 KB, [K group][token][16 bytes]) and each
+    // B warp's own copy of the 64 tokens' scale words
+    static constexpr int kBRawStage = FP4 ? kNmax * 32 + kStgW * kNmax * 4 : kNmax * kChunkK * 2;
+    static constexpr int kSmem = kBRawOff + kLA * kBRawStage;
+    // TMEM: accumulator columns 0..63 (N <= 64); E2M1 path: per (stage,
+    // chunk) four columns of A scales from kSfaCol and four of B scales
+    // from kSfbCol (block-scaled MMAs take scale addresses that are
+    // multiples of four columns: row r at lane r % 32, column r / 32)
+    static constexpr uint32_t kSfaCol = 64, kSfbCol = kSfaCol + 4 * kNS * kCPS;
+    static constexpr uint32_t kTmemCols = FP4 ? 128 : 64;        // a power of two >= 32
+    static_assert(!FP4 || kSfbCol + 4 * kNS * kCPS <= kTmemCols, "scale columns fit the allocation");
+};
 
 __device__ __forceinline__ unsigned long long gtimer() {
     unsigned long long t;
@@ -79,8 +99,8 @@ __device__ __forceinline__ unsigned long long gtimer() {
 
 // No-swizzle K-major shared-memory operand descriptor (tcgen05): start
 // address, leading (K) and stride (row) byte offsets, descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(kLBO >> 4) << 16) | ((uint64_t)(kSBO >> 4) << 32) |
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(kLBO >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
            (1ull << 46);
 }
 
@@ -88,6 +108,29 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 __device__ __forceinline__ uint32_t instr_desc(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// Instruction descriptor: kind::mxf4nvf4 block-scaled, A = B = E2M1, scales
+// E4M3 (one per 16 elements: scale_vec::4X), D = f32, both K-major.
+__device__ __forceinline__ uint32_t instr_desc_fp4(int M, int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 7) << 27);
+}
+
+// Byte `b` of each of four words, in order.
+__device__ __forceinline__ uint32_t gather4(uint32_t a, uint32_t b0, uint32_t c, uint32_t d, uint32_t b) {
+    const uint32_t sel = b | ((b + 4) << 4);
+    return __byte_perm(__byte_perm(a, b0, sel), __byte_perm(c, d, sel), 0x5410);
+}
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// 32 lanes (this warp's quadrant) x 2 consecutive TMEM columns.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t v0, uint32_t v1) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};\n" ::"r"(taddr), "r"(v0), "r"(v1)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // 16-byte asynchronous copy global -> shared (L2 only), and its groups.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
@@ -139,9 +182,14 @@ __device__ __forceinline__ int hexp_of(unsigned bits) {
     return max(-100, exp_for_f16(__uint_as_float(bits)));
 }
 
-template <int MODE>   // 0 gate/up + SwiGLU, 1 down + combine
+// MODE 0 gate/up + SwiGLU, 1 down + combine; FP4: W4A4 layers, whose
+// activations are E2M1 codes with E4M3 block scales, multiplied by
+// tcgen05.mma kind::mxf4nvf4 (no decode: the weights' codes are only
+// rearranged into the operand layout, their scales go to TMEM).
+template <int MODE, bool FP4>
 __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x, int T,
                                                          __nv_bfloat16 *__restrict__ out) {
+    using G = Geo<FP4>;
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_full[kNS], s_empty[kNS], s_accf, s_acce;
     __shared__ __align__(8) uint64_t s_rbar[kDecW][kRWA];
@@ -156,10 +204,11 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     uint8_t *sA = smem;
-    uint8_t *sB = smem + kNS * kAStage;
-    int *s_pair = reinterpret_cast<int *>(smem + kNS * (kAStage + kBStage));
-    float *s_pw = reinterpret_cast<float *>(smem + kNS * (kAStage + kBStage) + kScratch / 2);
-    uint8_t *rraw = smem + kRawOff + (size_t)(warp < kDecW ? warp : 0) * kRWA * kCHA * kChunkBytes;
+    uint8_t *sB = smem + kNS * G::kAStage;
+    uint32_t *sSF = reinterpret_cast<uint32_t *>(smem + kNS * (G::kAStage + G::kBStage));   // FP4 only
+    int *s_pair = reinterpret_cast<int *>(smem + G::kScrOff);
+    float *s_pw = reinterpret_cast<float *>(smem + G::kScrOff + kScratch / 2);
+    uint8_t *rraw = smem + G::kRawOff + (size_t)(warp < kDecW ? warp : 0) * kRWA * kCHA * kChunkBytes;
     volatile int *abort = &s_abort;
     const uint64_t pol = evict_first_policy();
 
@@ -177,7 +226,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
     }
     if (warp == kMmaW) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_taddr)),
-                     "r"(kTmemCols)
+                     "r"(G::kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
@@ -260,7 +309,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
         // (every role runs every item, so that the epilogue warps' named
         // barriers stay matched; after an abort the waits return at once)
         const int NC = s_it_nc[li], m = s_it_m[li], p0 = s_it_p0[li], e = s_it_e[li], mt = s_it_mt[li];
-        const int N = (m + 15) & ~15;
+        const int N = FP4 ? kNmax : (m + 15) & ~15;   // E2M1 path: always the shape its layout was checked on
         const bool shared = e < 0;
         float gs0, gs1;
         if (MODE == 0) {
@@ -280,12 +329,16 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
         if (warp < kDecW) {
             const int col = 32 * (warp >> 2) + lane;
             if (col < m) {
-                // (W4A4: times the row's global scale)
+                // (W4A4: times the row's global scale; the E2M1 operands
+                // carry no power-of-two prescale)
                 if (MODE == 0) {
                     const int tok = shared ? col : __ldcg(d.pair_tok + p0 + col);
-                    col_un = pow2f(__ldcg(d.xexp + tok)) * (d.w4a4 ? __ldcg(d.gsx + tok) : 1.f);
+                    col_un = FP4 ? __ldcg(d.gsx + tok)
+                                 : pow2f(__ldcg(d.xexp + tok)) * (d.w4a4 ? __ldcg(d.gsx + tok) : 1.f);
                 } else {
-                    col_un = pow2f(hexp_of(__ldcg(d.hmax + p0 + col))) * (d.w4a4 ? __ldcg(d.gsh + p0 + col) : 1.f);
+                    col_un = FP4 ? __ldcg(d.gsh + p0 + col)
+                                 : pow2f(hexp_of(__ldcg(d.hmax + p0 + col))) *
+                                       (d.w4a4 ? __ldcg(d.gsh + p0 + col) : 1.f);
                 }
             }
         }
@@ -304,20 +357,48 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     }
                     if (go) {
                         const uint8_t *ch = rraw + ((size_t)(jc % kRWA) * kCHA + oc) * kChunkBytes;
-                        const uint4 cw = lds128(ch + 16 * lane);
                         uint2 sw;
                         asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n"
                                      : "=r"(sw.x), "=r"(sw.y) : "r"(smem_u32(ch + kCodeBytes + 8 * g)));
-                        uint32_t a[4][4];
-                        decode_chunk(cw, sw, a);
-                        // chunk h of the stage: K groups 8h .. 8h + 7
-                        uint8_t *As = sA + (size_t)st * kAStage + 8 * h * kLBO + g * 16 + q * 4;
+                        if constexpr (FP4) {
+                            // The quad's 64 bytes hold rows g and g + 8 of the
+                            // tile (lane 4g + p: bytes 16p..; its word i, byte
+                            // b: row g + 8(b & 1), K byte 8i + p + 4(b >> 1)).
+                            // Lane q writes row g + 8(q & 1), K bytes
+                            // 16(q >> 1) .. + 15: one core-matrix row.
+                            const uint8_t *qb = ch + 64 * g;
+                            const uint4 u0 = lds128(qb), u1 = lds128(qb + 16), u2 = lds128(qb + 32),
+                                        u3 = lds128(qb + 48);
+                            const uint32_t rb = q & 1, kb = q >> 1;
+                            const uint32_t a0 = kb ? u0.z : u0.x, a1 = kb ? u1.z : u1.x, a2 = kb ? u2.z : u2.x,
+                                           a3 = kb ? u3.z : u3.x;
+                            const uint32_t b0 = kb ? u0.w : u0.y, b1 = kb ? u1.w : u1.y, b2 = kb ? u2.w : u2.y,
+                                           b3 = kb ? u3.w : u3.y;
+                            uint4 o;
+                            o.x = gather4(a0, a1, a2, a3, rb);
+                            o.y = gather4(a0, a1, a2, a3, 2 | rb);
+                            o.z = gather4(b0, b1, b2, b3, rb);
+                            o.w = gather4(b0, b1, b2, b3, 2 | rb);
+                            *reinterpret_cast<uint4 *>(sA + (size_t)st * G::kAStage + (2 * warp + rb) * G::kSBO +
+                                                       (2 * h + kb) * kLBO + g * 16) = o;
+                            // the four K-block scales of rows g (lane q = 0)
+                            // and g + 8 (q = 1), byte j = K block j
+                            if (q < 2)
+                                sSF[(st * kCPS + h) * kMT + 16 * warp + g + 8 * q] =
+                                    __byte_perm(sw.x, sw.y, q ? 0x7531 : 0x6420);
+                        } else {
+                            const uint4 cw = lds128(ch + 16 * lane);
+                            uint32_t a[4][4];
+                            decode_chunk(cw, sw, a);
+                            // chunk h of the stage: K groups 8h .. 8h + 7
+                            uint8_t *As = sA + (size_t)st * G::kAStage + 8 * h * kLBO + g * 16 + q * 4;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                            for (int i = 0; i < 4; ++i)
 #pragma unroll
-                            for (int b = 0; b < 4; ++b)
-                                *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * kSBO +
-                                                              (2 * i + (b >> 1)) * kLBO) = a[i][b];
+                                for (int b = 0; b < 4; ++b)
+                                    *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * G::kSBO +
+                                                                  (2 * i + (b >> 1)) * kLBO) = a[i][b];
+                        }
                     }
                     if (++oc == min(kCHA, NC - cseg)) {
                         cseg += oc;
@@ -325,6 +406,25 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                         ++jc;
                         if (!*abort) rissue(jc + kRWA);
                     }
+                }
+                if constexpr (FP4) {
+                    // the stage's A scales to TMEM, in every lane quadrant:
+                    // quadrant warp % 4 gets columns 2(warp / 4), +1 (rows
+                    // 64(warp / 4) .. + 63) from the words all eight decode
+                    // warps staged (every decode warp passes this barrier
+                    // once per stage, aborted or not)
+                    asm volatile("bar.sync 2, %0;\n" ::"r"(32 * kDecW) : "memory");
+                    if (__all_sync(0xffffffffu, go)) {
+                        const int j0 = 2 * (warp >> 2);
+                        for (int h = 0; h < nch; ++h) {
+                            const uint32_t *w = sSF + (st * kCPS + h) * kMT;
+                            tmem_st2(taddr + ((uint32_t)(32 * (warp & 3)) << 16) + G::kSfaCol + 4 * (st * kCPS + h) +
+                                         j0,
+                                     w[32 * j0 + lane], w[32 * (j0 + 1) + lane]);
+                        }
+                        tmem_st_wait();
+                    }
+                    tc_fence_before();
                 }
                 if (go) fence_proxy_async();
                 __syncwarp();
@@ -337,89 +437,167 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
             // (cp.async into a raw ring; a thread reads back only what it
             // copied itself, so its own group waits order it) and converts
             // chunk c into the stage ----
-            // Thread tb takes K group kg of tokens nlo + 8 * nhi + 16 * u: the
-            // eight lanes of a quarter warp (one 16-byte store phase) write
-            // eight different token rows of one core matrix, so their
-            // stores hit eight different bank groups.
-            const int tb = threadIdx.x - 32 * kDecW;      // 0..127
-            const int nlo = tb & 7, kg = (tb >> 3) & 7, nhi = tb >> 6;
-            const uint4 *src[4];
-            float sc[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int n = nlo + 8 * nhi + 16 * u;
-                src[u] = nullptr;
-                sc[u] = 0.f;
+            if constexpr (FP4) {
+                // E2M1 path: thread tb copies K group kb = tb / 64 (16
+                // bytes) of token n = tb % 64 of each chunk, kLA - 1 chunks
+                // ahead, into the raw ring ([K group][token][16 bytes]) and
+                // from there into the stage (rows >= m zero); each B warp
+                // also copies the 64 tokens' scale words of the chunk (lane
+                // L: tokens L and L + 32) and writes them to TMEM in its own
+                // lane quadrant (columns: tokens 0-31, 32-63).
+                const int tb = threadIdx.x - 32 * kDecW;      // 0..127
+                const int n = tb & 63, kb = tb >> 6, wq = tb >> 5;
+                const uint8_t *csrc = nullptr;
+                const uint8_t *ssrc[2] = {nullptr, nullptr};
                 if (n < m) {
                     if (MODE == 0) {
                         const int tok = shared ? n : __ldcg(d.pair_tok + p0 + n);
-                        src[u] = reinterpret_cast<const uint4 *>(x + (size_t)tok * d.H);
-                        sc[u] = pow2f(-__ldcg(d.xexp + tok));
+                        csrc = d.xq4 + (size_t)tok * (d.H / 2) + 16 * kb;
                     } else {
-                        src[u] = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)(p0 + n) * d.Imax);
-                        sc[u] = pow2f(-hexp_of(__ldcg(d.hmax + p0 + n)));
+                        csrc = d.hq4 + (size_t)(p0 + n) * (d.Imax / 2) + 16 * kb;
                     }
                 }
-            }
-            // raw ring: token row n of a chunk is 128 bytes, its K groups
-            // XOR-swizzled by n % 8 (= nlo) so that a quarter warp's pieces
-            // fall in different bank groups here too
-            uint8_t *braw = smem + kBRawOff + ((kg ^ nlo) << 4);
-            // one commit group per chunk index (empty past the end), so that
-            // "chunk c landed" is always "at most kLA - 1 groups pending"
-            auto bissue = [&](int c) {
-                if (c < NC) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int n = nlo + 8 * nhi + 16 * u;
-                        if (src[u])
-                            cp_async16(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128, src[u] + c * 8 + kg);
-                    }
-                }
-                cp_async_commit();
-            };
-#pragma unroll
-            for (int j = 0; j < kLA; ++j) bissue(j);
-#pragma unroll 1
-            for (int c0 = 0; c0 < NC; c0 += kCPS) {
-                const int gcc = gc + c0 / kCPS, st = gcc % kNS, nch = min(kCPS, NC - c0);
-                const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
-#pragma unroll 1
-                for (int h = 0; h < nch; ++h) {
-                    const int c = c0 + h;
-                    cp_async_wait<kLA - 1>();
-                    if (go) {
-                        // chunk h of the stage: K groups 8h .. 8h + 7
-                        uint8_t *Bs = sB + (size_t)st * kBStage + 8 * h * kLBO;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int n = nlo + 8 * nhi + 16 * u;
-                            if (n < N) {
-                                uint4 o = make_uint4(0u, 0u, 0u, 0u);
-                                if (src[u]) {
-                                    const uint4 v = lds128(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128);
-                                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                                    uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i)
-                                        ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
-                                                           __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
-                                }
-                                *reinterpret_cast<uint4 *>(Bs + (n >> 3) * kSBO + kg * kLBO + (n & 7) * 16) = o;
-                            }
+                for (int u = 0; u < 2; ++u) {
+                    const int nn = lane + 32 * u;
+                    if (nn < m) {
+                        if (MODE == 0) {
+                            const int tok = shared ? nn : __ldcg(d.pair_tok + p0 + nn);
+                            ssrc[u] = d.xsf + (size_t)tok * (d.H / 16);
+                        } else {
+                            ssrc[u] = d.hsf + (size_t)(p0 + nn) * (d.Imax / 16);
                         }
                     }
-                    bissue(c + kLA);
                 }
-                if (go) fence_proxy_async();
-                __syncwarp();
-                if (go && lane == 0) mbar_arrive(&s_full[st]);
-                if (li == 0 && c0 == 0) MOE_TRACE_POINT_AT(3 + MODE, 6, 32 * kDecW);
+                uint8_t *braw = smem + G::kBRawOff;
+                auto bissue = [&](int c) {
+                    if (c < NC) {
+                        uint8_t *slot = braw + (size_t)(c & (kLA - 1)) * G::kBRawStage;
+                        if (csrc) cp_async16(slot + kb * (kNmax * 16) + n * 16, csrc + 32 * c);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            if (ssrc[u])
+                                cp_async4(slot + kNmax * 32 + wq * (kNmax * 4) + (lane + 32 * u) * 4, ssrc[u] + 4 * c);
+                    }
+                    cp_async_commit();
+                };
+#pragma unroll
+                for (int j = 0; j < kLA; ++j) bissue(j);
+#pragma unroll 1
+                for (int c0 = 0; c0 < NC; c0 += kCPS) {
+                    const int gcc = gc + c0 / kCPS, st = gcc % kNS, nch = min(kCPS, NC - c0);
+                    const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
+                    const bool gw = __all_sync(0xffffffffu, go);
+#pragma unroll 1
+                    for (int h = 0; h < nch; ++h) {
+                        const int c = c0 + h;
+                        cp_async_wait<kLA - 1>();
+                        const uint8_t *slot = braw + (size_t)(c & (kLA - 1)) * G::kBRawStage;
+                        if (go) {
+                            const uint4 v = csrc ? lds128(slot + kb * (kNmax * 16) + n * 16) : make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4 *>(sB + (size_t)st * G::kBStage + (n >> 3) * G::kSBO +
+                                                       (2 * h + kb) * kLBO + (n & 7) * 16) = v;
+                        }
+                        if (gw) {
+                            const uint32_t *sf = reinterpret_cast<const uint32_t *>(slot + kNmax * 32 + wq * (kNmax * 4));
+                            tmem_st2(taddr + ((uint32_t)(32 * wq) << 16) + G::kSfbCol + 4 * (st * kCPS + h),
+                                     ssrc[0] ? sf[lane] : 0u, ssrc[1] ? sf[lane + 32] : 0u);
+                        }
+                        bissue(c + kLA);
+                    }
+                    if (gw) tmem_st_wait();
+                    tc_fence_before();
+                    if (go) fence_proxy_async();
+                    __syncwarp();
+                    if (go && lane == 0) mbar_arrive(&s_full[st]);
+                    if (li == 0 && c0 == 0) MOE_TRACE_POINT_AT(3 + MODE, 6, 32 * kDecW);
+                }
+                if (li == 0) MOE_TRACE_POINT_AT(3 + MODE, 7, 32 * kDecW);
+            } else {
+                // Thread tb takes K group kg of tokens nlo + 8 * nhi + 16 * u:
+                // the eight lanes of a quarter warp (one 16-byte store phase)
+                // write eight different token rows of one core matrix, so
+                // their stores hit eight different bank groups.
+                const int tb = threadIdx.x - 32 * kDecW;      // 0..127
+                const int nlo = tb & 7, kg = (tb >> 3) & 7, nhi = tb >> 6;
+                const uint4 *src[4];
+                float sc[4];
+    #pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int n = nlo + 8 * nhi + 16 * u;
+                    src[u] = nullptr;
+                    sc[u] = 0.f;
+                    if (n < m) {
+                        if (MODE == 0) {
+                            const int tok = shared ? n : __ldcg(d.pair_tok + p0 + n);
+                            src[u] = reinterpret_cast<const uint4 *>(x + (size_t)tok * d.H);
+                            sc[u] = pow2f(-__ldcg(d.xexp + tok));
+                        } else {
+                            src[u] = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)(p0 + n) * d.Imax);
+                            sc[u] = pow2f(-hexp_of(__ldcg(d.hmax + p0 + n)));
+                        }
+                    }
+                }
+                // raw ring: token row n of a chunk is 128 bytes, its K groups
+                // XOR-swizzled by n % 8 (= nlo) so that a quarter warp's pieces
+                // fall in different bank groups here too
+                uint8_t *braw = smem + G::kBRawOff + ((kg ^ nlo) << 4);
+                // one commit group per chunk index (empty past the end), so that
+                // "chunk c landed" is always "at most kLA - 1 groups pending"
+                auto bissue = [&](int c) {
+                    if (c < NC) {
+    #pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int n = nlo + 8 * nhi + 16 * u;
+                            if (src[u])
+                                cp_async16(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128, src[u] + c * 8 + kg);
+                        }
+                    }
+                    cp_async_commit();
+                };
+    #pragma unroll
+                for (int j = 0; j < kLA; ++j) bissue(j);
+    #pragma unroll 1
+                for (int c0 = 0; c0 < NC; c0 += kCPS) {
+                    const int gcc = gc + c0 / kCPS, st = gcc % kNS, nch = min(kCPS, NC - c0);
+                    const bool go = gwait(&s_empty[st], ((unsigned)(gcc / kNS) & 1u) ^ 1u, abort, d.err);
+    #pragma unroll 1
+                    for (int h = 0; h < nch; ++h) {
+                        const int c = c0 + h;
+                        cp_async_wait<kLA - 1>();
+                        if (go) {
+                            // chunk h of the stage: K groups 8h .. 8h + 7
+                            uint8_t *Bs = sB + (size_t)st * G::kBStage + 8 * h * kLBO;
+    #pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int n = nlo + 8 * nhi + 16 * u;
+                                if (n < N) {
+                                    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                                    if (src[u]) {
+                                        const uint4 v = lds128(braw + (size_t)((c & (kLA - 1)) * kNmax + n) * 128);
+                                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                                        uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+    #pragma unroll
+                                        for (int i = 0; i < 4; ++i)
+                                            ow[i] = pack_f16x2(__uint_as_float(w4[i] << 16) * sc[u],
+                                                               __uint_as_float(w4[i] & 0xFFFF0000u) * sc[u]);
+                                    }
+                                    *reinterpret_cast<uint4 *>(Bs + (n >> 3) * G::kSBO + kg * kLBO + (n & 7) * 16) = o;
+                                }
+                            }
+                        }
+                        bissue(c + kLA);
+                    }
+                    if (go) fence_proxy_async();
+                    __syncwarp();
+                    if (go && lane == 0) mbar_arrive(&s_full[st]);
+                    if (li == 0 && c0 == 0) MOE_TRACE_POINT_AT(3 + MODE, 6, 32 * kDecW);
+                }
+                if (li == 0) MOE_TRACE_POINT_AT(3 + MODE, 7, 32 * kDecW);
             }
-            if (li == 0) MOE_TRACE_POINT_AT(3 + MODE, 7, 32 * kDecW);
         } else if (lane == 0) {
             // ---- MMA issuer ----
-            const uint32_t idesc = instr_desc(kMT, N);
+            const uint32_t idesc = FP4 ? instr_desc_fp4(kMT, N) : instr_desc(kMT, N);
             bool go = gwait(&s_acce, ((unsigned)li & 1u) ^ 1u, abort, d.err);   // accumulator read out
             tc_fence_after();
 #pragma unroll 1
@@ -431,17 +609,38 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                 }
                 tc_fence_after();
                 if (li == 0 && c0 == 0) MOE_TRACE_POINT_AT(3 + MODE, 4, 32 * kMmaW);
-                const uint32_t a0 = smem_u32(sA + (size_t)st * kAStage), b0 = smem_u32(sB + (size_t)st * kBStage);
+                const uint32_t a0 = smem_u32(sA + (size_t)st * G::kAStage),
+                               b0 = smem_u32(sB + (size_t)st * G::kBStage);
+                if constexpr (FP4) {
+                    // one K=64 MMA per chunk, its scales at the stage's columns
 #pragma unroll
-                for (int ks = 0; ks < 4 * kCPS; ++ks) {
-                    if (ks >= 4 * nch) break;
-                    const uint64_t da = smem_desc(a0 + ks * 2 * kLBO), db = smem_desc(b0 + ks * 2 * kLBO);
-                    const uint32_t acc = (c0 > 0 || ks > 0) ? 1u : 0u;
-                    asm volatile(
-                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(taddr),
-                        "l"(da), "l"(db), "r"(idesc), "r"(acc)
-                        : "memory");
+                    for (int h = 0; h < kCPS; ++h) {
+                        if (h >= nch) break;
+                        const uint64_t da = smem_desc(a0 + h * 2 * kLBO, G::kSBO),
+                                       db = smem_desc(b0 + h * 2 * kLBO, G::kSBO);
+                        const uint32_t acc = (c0 > 0 || h > 0) ? 1u : 0u;
+                        const uint32_t col = 4 * (st * kCPS + h);
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+                            "[%4], [%5], p;\n\t}\n" ::"r"(taddr),
+                            "l"(da), "l"(db), "r"(idesc), "r"(taddr + G::kSfaCol + col), "r"(taddr + G::kSfbCol + col),
+                            "r"(acc)
+                            : "memory");
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < 4 * kCPS; ++ks) {
+                        if (ks >= 4 * nch) break;
+                        const uint64_t da = smem_desc(a0 + ks * 2 * kLBO, G::kSBO),
+                                       db = smem_desc(b0 + ks * 2 * kLBO, G::kSBO);
+                        const uint32_t acc = (c0 > 0 || ks > 0) ? 1u : 0u;
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(taddr),
+                            "l"(da), "l"(db), "r"(idesc), "r"(acc)
+                            : "memory");
+                    }
                 }
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
                                  smem_u32(&s_empty[st]))
@@ -560,7 +759,8 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaW)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(G::kTmemCols)
+                     : "memory");
     // completion order of the chain: this kernel ends after its predecessor
     pdl_wait();
     MOE_TRACE_POINT(3 + MODE, 9);
@@ -572,14 +772,15 @@ cudaError_t launch_g(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bflo
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sm_count);
     cfg.blockDim = dim3(kGT);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = d.w4a4 ? Geo<true>::kSmem : Geo<false>::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_kernel<MODE>, d, x, T, out);
+    return d.w4a4 ? cudaLaunchKernelEx(&cfg, grouped_kernel<MODE, true>, d, x, T, out)
+                  : cudaLaunchKernelEx(&cfg, grouped_kernel<MODE, false>, d, x, T, out);
 }
 
 }  // namespace
@@ -604,8 +805,11 @@ cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, in
 
 cudaError_t prepare_grouped_kernels(int optin_bytes) {
     (void)optin_bytes;
-    cudaError_t e = cudaFuncSetAttribute(grouped_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    const int s0 = Geo<false>::kSmem, s1 = Geo<true>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(grouped_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s0);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, s0);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1);
     return e;
 }
 

@@ -125,6 +125,9 @@ struct DevLayer {
     __nv_bfloat16 *xq;              // [Tm, H] W4A4: the tokens' dequantised e2m1 * e4m3 values
     float *gsx;                     // [Tm] W4A4: their global scales
     float *gsh;                     // [max_pairs] W4A4: the h rows' global scales
+    uint8_t *xq4, *xsf;             // [Tm, H/2], [Tm, H/16] W4A4: the tokens' E2M1 codes (element 2j in
+                                    //   the low nibble) and E4M3 block scale codes
+    uint8_t *hq4, *hsf;             // [max_pairs, Imax/2], [max_pairs, Imax/16] the same for the h rows
 };
 
 // Chunks per tile row of K elements, in the NVFP4 or the F8 chunk layout.
@@ -166,7 +169,8 @@ cudaError_t launch_dequant_f8(const uint8_t *rep, int rows, int cols, bool gate_
 // src), the global scales, and (optional) the f16 prescale exponent and the
 // max |value| bits of each row.
 cudaError_t launch_fos(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int nrows, int stride, int len_long,
-                       int n_short, int len_short, float *gs, int *exp_out, unsigned *max_out, cudaStream_t s);
+                       int n_short, int len_short, float *gs, int *exp_out, unsigned *max_out, uint8_t *codes,
+                       uint8_t *sfc, int code_stride, int sf_stride, cudaStream_t s);
 // MXFP4 scales: per (matrix, half) the smallest and largest E8M0 code and
 // whether a NaN code (255) occurs -> mm[(mat * 2 + half) * 3 + {0,1,2}]
 // (half 1 only for gate/up: its up rows).

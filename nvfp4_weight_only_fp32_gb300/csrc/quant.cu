@@ -18,7 +18,9 @@
 //   the block keeps 4 if err_4 < err_6, else 6.
 // The row is written back as the exact products e2m1 * e4m3 (at most six
 // significant bits: exact in BF16) and the global scale gs goes to its own
-// array; the GEMM epilogues multiply by it.  The power-of-two prescale the
+// array; the GEMM epilogues multiply by it.  Optionally the codes themselves
+// are written too (E2M1 codes two per byte, element 2j in the low nibble, and
+// one E4M3 scale code per block), for the block-scaled tensor-core MMAs.  The power-of-two prescale the
 // kernels use for the f16 operand (exponent of the row's new maximum) and,
 // for h rows, the row maximum's bits are written as well.
 #include "moe_internal.cuh"
@@ -71,7 +73,8 @@ constexpr int kFosMaxThreads = 1024;
 // the row maximum is complete.
 __global__ void __launch_bounds__(kFosMaxThreads)
 fos_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int stride, int len_long, int n_short, int len_short,
-           float *__restrict__ gs_out, int *__restrict__ exp_out, unsigned *__restrict__ max_out) {
+           float *__restrict__ gs_out, int *__restrict__ exp_out, unsigned *__restrict__ max_out,
+           uint8_t *__restrict__ codes, uint8_t *__restrict__ sfc, int code_stride, int sf_stride) {
     // The next kernel may start at once: its own wait covers this kernel's
     // completion.  The rows come from the kernels before (the router's input,
     // the SwiGLU output), complete once this wait returns; it also orders
@@ -106,10 +109,12 @@ fos_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int stride, int len_lon
         for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float t[2], sv[2];
         int q[2];
+        uint32_t scode[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const float cg = __fmul_rn(i == 0 ? 6.0f : 4.0f, gs);
-            const float sc = e4m3_value(e4m3_code_rn(__fdiv_rn(m, cg)));
+            scode[i] = e4m3_code_rn(__fdiv_rn(m, cg));
+            const float sc = e4m3_value(scode[i]);
             const float dv = __fmul_rn(sc, gs);
             q[i] = sc > 0.f ? e2m1_code_rne(__fdiv_rn(v, dv)) : 0;
             const float rv = __fmul_rn(__fmul_rn(e2m1_value(q[i]), sc), gs);
@@ -130,6 +135,12 @@ fos_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int stride, int len_lon
             out[k] = __float2bfloat16_rn(w);
             newmax = fmaxf(newmax, fabsf(w));
         }
+        if (codes) {
+            const uint32_t c = (uint32_t)q[pick] & 15u;
+            const uint32_t hi = __shfl_down_sync(0xffffffffu, c, 1);
+            if (on && (lane & 1) == 0) codes[(size_t)r * code_stride + k / 2] = (uint8_t)(c | (hi << 4));
+            if (on && (lane & 15) == 0) sfc[(size_t)r * sf_stride + k / 16] = (uint8_t)scode[pick];
+        }
     }
     unsigned nm = __reduce_max_sync(0xffffffffu, __float_as_uint(newmax));
     __syncthreads();   // every warp has read s_red above
@@ -148,7 +159,8 @@ fos_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int stride, int len_lon
 }  // namespace
 
 cudaError_t launch_fos(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int nrows, int stride, int len_long,
-                       int n_short, int len_short, float *gs, int *exp_out, unsigned *max_out, cudaStream_t s) {
+                       int n_short, int len_short, float *gs, int *exp_out, unsigned *max_out, uint8_t *codes,
+                       uint8_t *sfc, int code_stride, int sf_stride, cudaStream_t s) {
     if (nrows <= 0) return cudaSuccess;
     const int len = n_short > 0 ? max(len_long, len_short) : len_long;
     cudaLaunchConfig_t cfg = {};
@@ -161,7 +173,7 @@ cudaError_t launch_fos(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int nrows, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fos_kernel, src, dst, stride, len_long, n_short, len_short, gs, exp_out,
-                              max_out);
+                              max_out, codes, sfc, code_stride, sf_stride);
 }
 
 }  // namespace moe
