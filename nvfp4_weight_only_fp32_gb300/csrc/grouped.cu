@@ -390,14 +390,23 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                             const uint4 cw = lds128(ch + 16 * lane);
                             uint32_t a[4][4];
                             decode_chunk(cw, sw, a);
-                            // chunk h of the stage: K groups 8h .. 8h + 7
-                            uint8_t *As = sA + (size_t)st * G::kAStage + 8 * h * kLBO + g * 16 + q * 4;
+                            // chunk h of the stage: K groups 8h .. 8h + 7.
+                            // a[i][b] is the MMA fragment of an 8x8 block (rows
+                            // + 8(b & 1), K group 2i + (b >> 1)): one stmatrix
+                            // per i stores four of them, lane t giving row t % 8
+                            // of block b = t / 8 (each block one 128-byte core
+                            // matrix).
+                            const int bt = lane >> 3;
+                            const uint32_t As = smem_u32(sA + (size_t)st * G::kAStage +
+                                                         (2 * warp + (bt & 1)) * G::kSBO +
+                                                         (8 * h + (bt >> 1)) * kLBO + (lane & 7) * 16);
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
-#pragma unroll
-                                for (int b = 0; b < 4; ++b)
-                                    *reinterpret_cast<uint32_t *>(As + (2 * warp + (b & 1)) * G::kSBO +
-                                                                  (2 * i + (b >> 1)) * kLBO) = a[i][b];
+                                asm volatile(
+                                    "stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                                        As + 2 * i * kLBO),
+                                    "r"(a[i][0]), "r"(a[i][1]), "r"(a[i][2]), "r"(a[i][3])
+                                    : "memory");
                         }
                     }
                     if (++oc == min(kCHA, NC - cseg)) {

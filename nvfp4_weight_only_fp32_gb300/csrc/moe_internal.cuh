@@ -211,7 +211,7 @@ __host__ __device__ inline size_t repacked_bytes(int rows, int cols, bool f8 = f
 #define MOE_TRACE_STORE_(kid, i, tid, val)                                                       \
     do {                                                                                         \
         if (threadIdx.x == (tid) && d.trace) {                                                   \
-            const int b_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
+            const int b_ = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;       \
             if (b_ < d.trace_blocks)                                                             \
                 d.trace[((size_t)(kid) * d.trace_blocks + b_) * 16 + (i)] = (unsigned long long)(val); \
         }                                                                                        \

@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
                 }
             }
         }
+        MOE_TRACE_POINT(0, 8);
 #pragma unroll
         for (int t = 0; t < kTokGroup; ++t) {
             float a = acc[t];
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         __threadfence();
         s_last = atomicAdd(d.tg_ticket + blockIdx.y, 1u) == gridDim.x * gridDim.z - 1;
     }
+    MOE_TRACE_POINT(0, 9);
     __syncthreads();
     if (!s_last) return;
     __threadfence();
@@ -239,22 +241,67 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         for (int i = threadIdx.x; i < E; i += kThreads) s_mask[i] = 0ull;
     float *s_lg = reinterpret_cast<float *>(smem);   // [nt][E]: x is no longer read
     if (KH > 1) {
-        // the token group's logits: the K ranges' sums in a fixed order, the
-        // partial loads of an element in flight together; kept in shared
-        // memory for the top-k below
-        for (int i = threadIdx.x; i < nt * E; i += kThreads) {
-            const int t = i / E, ee = i - t * E;
-            float part[kMaxKSplit];
+        // the token group's logits: the K ranges' sums in a fixed order; kept
+        // in shared memory for the top-k below.  One block reads all the
+        // partials, so the number of requests sets the time: four experts
+        // per 16-byte load when E allows, a thread's items kLgBatch at a time
+        // with all their partial loads in flight together.
+        if ((E & 3) == 0) {
+            constexpr int kLgBatch = 2;
+            const int nq = nt * E / 4;
+            const float4 *lp = reinterpret_cast<const float4 *>(d.lpart);
+#pragma unroll 1
+            for (int i0 = 0; i0 < nq; i0 += kLgBatch * kThreads) {
+                float4 part[kLgBatch][kMaxKSplit];
 #pragma unroll
-            for (int z = 0; z < kMaxKSplit; ++z)
-                part[z] = z < KH ? __ldcg(d.lpart + ((size_t)z * d.max_tokens + t0 + t) * E + ee) : 0.f;
-            float v = 0.f;
+                for (int r = 0; r < kLgBatch; ++r) {
+                    const int i = i0 + r * kThreads + threadIdx.x;
+                    const int t = (4 * i) / E, e4 = 4 * i - t * E;
 #pragma unroll
-            for (int z = 0; z < kMaxKSplit; ++z)
-                if (z < KH) v += part[z];
-            v += d.router_b ? d.router_b[ee] : 0.f;
-            s_lg[i] = v;
-            d.logits[(size_t)(t0 + t) * E + ee] = v;
+                    for (int z = 0; z < kMaxKSplit; ++z)
+                        part[r][z] = (z < KH && i < nq)
+                                         ? __ldcg(lp + (((size_t)z * d.max_tokens + t0 + t) * E + e4) / 4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int r = 0; r < kLgBatch; ++r) {
+                    const int i = i0 + r * kThreads + threadIdx.x;
+                    if (i < nq) {
+                        const int t = (4 * i) / E, e4 = 4 * i - t * E;
+                        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int z = 0; z < kMaxKSplit; ++z)
+                            if (z < KH) {
+                                v[0] += part[r][z].x;
+                                v[1] += part[r][z].y;
+                                v[2] += part[r][z].z;
+                                v[3] += part[r][z].w;
+                            }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            v[u] += d.router_b ? d.router_b[e4 + u] : 0.f;
+                            s_lg[4 * i + u] = v[u];
+                        }
+                        *reinterpret_cast<float4 *>(d.logits + (size_t)(t0 + t) * E + e4) =
+                            make_float4(v[0], v[1], v[2], v[3]);
+                    }
+                }
+            }
+        } else {
+            for (int i = threadIdx.x; i < nt * E; i += kThreads) {
+                const int t = i / E, ee = i - t * E;
+                float part[kMaxKSplit];
+#pragma unroll
+                for (int z = 0; z < kMaxKSplit; ++z)
+                    part[z] = z < KH ? __ldcg(d.lpart + ((size_t)z * d.max_tokens + t0 + t) * E + ee) : 0.f;
+                float v = 0.f;
+#pragma unroll
+                for (int z = 0; z < kMaxKSplit; ++z)
+                    if (z < KH) v += part[z];
+                v += d.router_b ? d.router_b[ee] : 0.f;
+                s_lg[i] = v;
+                d.logits[(size_t)(t0 + t) * E + ee] = v;
+            }
         }
     }
     __syncthreads();
@@ -273,6 +320,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             case 8: sel = token_topk<8>(zt, lsm, E, K, lane); break;
             default: sel = token_topk<16>(zt, lsm, E, K, lane); break;
         }
+        MOE_TRACE_POINT(0, 10);
         const unsigned sel_key = (unsigned)(sel >> 32);
         const int sel_e = (int)~(unsigned)sel;
         // the choices' scores: the sigmoid of the logit, or (softmax routing)
@@ -302,6 +350,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             }
         }
     }
+    MOE_TRACE_POINT(0, 11);
     // ---- the last token group: slots, pairs, hot list ----
     __syncthreads();
     if (!one) {
