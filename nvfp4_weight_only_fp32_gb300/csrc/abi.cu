@@ -533,7 +533,7 @@ moe_status moe_stage_down(moe_layer *L, int T, void *out, void *stream) {
         e = launch_fos(d.h_ws, d.h_ws, T * (d.k + d.S), d.Imax, d.I, d.S * T, d.Is, d.gsh, nullptr, d.hmax, d.hq4,
                        d.hsf, d.Imax / 2, d.Imax / 16, st);
     }
-    if (e == cudaSuccess) e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out), st);
+    if (e == cudaSuccess) e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out), L->sm_count, L->optin_smem, st);
     if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)
         e = launch_grouped_down(L->d, T, static_cast<__nv_bfloat16 *>(out), L->sm_count, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");

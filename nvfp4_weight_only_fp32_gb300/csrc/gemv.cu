@@ -594,6 +594,266 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
     MOE_TRACE_POINT(1, 3);
 }
 
+// ---------------------------------------------------------------------------
+// Down + combine for steps of at most 8 tokens, as one wave: one block of 16
+// warps per SM takes a contiguous range of (slot, 16-row output tile) units
+// in slot order -- a range spans few slots, whose h rows (the B operand: a
+// slot's pairs as columns) it stages once -- and its warp groups take the
+// range's units round robin, streaming them through an 8-deep register ring
+// that runs on from one unit into the next.  Groups of 2^lks warps split a
+// unit's K range (fixed-order reduction).  Epilogue per unit: y = gs * acc
+// into the workspace; after its last unit a warp takes the per-tile tickets
+// of its units (no spinning), and the unit that completed a tile last among
+// the slots combines that tile's 16 rows for all tokens.
+// ---------------------------------------------------------------------------
+constexpr int kDMaxSlots = 12;          // slots one block's units may span
+
+template <bool F8>
+__global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int T, int lks,
+                                                                __nv_bfloat16 *__restrict__ out) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ const uint8_t *s_ub[kUW][kUMax];    // first chunk of the unit's K part
+    __shared__ short s_us[kUW][kUMax], s_ur[kUW][kUMax], s_uc[kUW][kUMax];   // slot, tile, chunks
+    __shared__ const uint4 *s_src[kDMaxSlots][8];
+    __shared__ float s_scale[kDMaxSlots][8], s_un[kDMaxSlots][8];
+    __shared__ int s_off[kDMaxSlots], s_rs[kDMaxSlots], s_m[kDMaxSlots], s_p0[kDMaxSlots];
+    __shared__ int s_pair[8 * (kMaxTopK + kMaxShared)];
+    __shared__ float s_pw[8 * (kMaxTopK + kMaxShared)];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int H = d.H, K = d.k, P = d.k + d.S;
+    const int ks = 1 << lks, kw = warp & (ks - 1), ngb = kUW >> lks, gj = warp >> lks;
+    const int NTd = H / 16;
+    float *red = reinterpret_cast<float *>(smem);   // [kUW][4][32]
+    uint8_t *stage = smem + (size_t)kUW * 4 * 32 * sizeof(float);
+    const uint64_t pol = evict_first_policy();
+
+    MOE_TRACE_POINT(2, 0);
+    // The router has completed before this kernel could start (the gate/up
+    // kernel released it only after its own wait): the slot and pair tables
+    // are final.  List the units and stream their weights; wait for h after.
+    const int ns = __ldcg(d.nslots);
+    const long U = (long)ns * NTd;
+    const int ub0 = (int)(U * blockIdx.x / gridDim.x), ub1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+    const int sl_lo = ub0 / NTd, nsb = ub1 > ub0 ? (ub1 - 1) / NTd - sl_lo + 1 : 0;
+    const int my = ub0 + gj < ub1 ? min(kUMax, (ub1 - ub0 - gj + ngb - 1) / ngb) : 0;
+    for (int i = lane; i < my; i += 32) {
+        const int tu = ub0 + gj + i * ngb;
+        const int sl = tu / NTd, r = tu - sl * NTd;
+        const int e = __ldcg(d.slot_expert + sl);
+        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+        const int nc = chunks_of(e < 0 ? d.Is : d.I, f8), cpw = nc >> lks;
+        const uint8_t *b = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
+        s_ub[warp][i] = b + ((size_t)r * nc + kw * cpw) * kChunkBytes;
+        s_us[warp][i] = (short)(sl - sl_lo);
+        s_ur[warp][i] = (short)r;
+        s_uc[warp][i] = (short)cpw;
+    }
+    __syncwarp();
+    uint4 cb[kUPD];
+    uint2 sb[kUPD];
+    if (my > 0) {
+#pragma unroll
+        for (int i = 0; i < kUPD; ++i) load_chunk(s_ub[warp][0], i, lane, cb[i], sb[i], pol);
+    }
+    // the staged slots' geometry (8 rows each, rows >= m zero) and the
+    // combine's pair table
+    if (threadIdx.x < nsb) {
+        const int sl = sl_lo + threadIdx.x;
+        const int e = __ldcg(d.slot_expert + sl);
+        s_rs[threadIdx.x] = ((e < 0 ? d.Is : d.I) / kChunkK) * 128 + 16;
+        s_m[threadIdx.x] = __ldcg(d.slot_m + sl);
+        s_p0[threadIdx.x] = __ldcg(d.slot_p0 + sl);
+    }
+    for (int i = threadIdx.x; i < T * P; i += kUT) {
+        const int p = __ldcg(d.pair_of + i);
+        s_pair[i] = p;
+        s_pw[i] = (i % P) < K ? __ldcg(d.pair_w + p) : 1.0f;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int off = 0;
+        for (int j = 0; j < nsb; ++j) {
+            s_off[j] = off;
+            off += 8 * s_rs[j];
+        }
+    }
+    pdl_wait();     // h and its maxima
+    pdl_trigger();
+    MOE_TRACE_POINT(2, 1);
+    if (threadIdx.x < 8 * nsb) {
+        const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
+        if (c < s_m[j]) {
+            const int p = s_p0[j] + c;
+            const int ex = hexp_of(__ldcg(d.hmax + p));
+            s_src[j][c] = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)p * d.Imax);
+            s_scale[j][c] = pow2f(-ex);
+            s_un[j][c] = pow2f(ex) * (d.w4a4 ? __ldcg(d.gsh + p) : 1.f);
+        }
+    }
+    __syncthreads();
+    for (int j = 0; j < nsb; ++j) {
+        const int m = s_m[j], rs = s_rs[j];
+        uint8_t *reg = stage + s_off[j];
+        for (int i = threadIdx.x; i < (8 - m) * (rs / 16); i += kUT)
+            reinterpret_cast<uint4 *>(reg + (size_t)m * rs)[i] = make_uint4(0u, 0u, 0u, 0u);
+        stage_rows<kUT>(m, 0, (rs - 16) / 128, reg, rs, s_src[j], s_scale[j]);
+    }
+    __syncthreads();
+    MOE_TRACE_POINT(2, 2);
+
+    int lu = 0, lc = kUPD;     // next chunk to load: unit lu, chunk lc
+#pragma unroll 1
+    for (int cu = 0; cu < my; ++cu) {
+        const int sj = s_us[warp][cu], cpw = s_uc[warp][cu];
+        const int sl = sl_lo + sj;
+        const int e = __ldcg(d.slot_expert + sl);
+        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+        const int kc0 = kw * cpw;
+        const uint8_t *xb = stage + s_off[sj] + (size_t)g * s_rs[sj] + q * 32;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int cc = 0; cc < cpw; cc += kUPD) {
+#pragma unroll
+            for (int i = 0; i < kUPD; ++i) {
+                const uint8_t *bp = xb + b_offset(kc0 + cc + i, f8);
+                if (F8 && f8) {
+                    chunk_mma_f8(cb[i], sb[i], lds128(bp), (i & 1) ? a1 : a0);
+                } else {
+                    uint32_t a[4][4];
+                    decode_chunk(cb[i], sb[i], a);
+                    const uint4 b01 = lds128(bp), b23 = lds128(bp + 16);
+                    mma_16816(a0, a[0][0], a[0][1], a[0][2], a[0][3], b01.x, b01.y);
+                    mma_16816(a1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
+                    mma_16816(a0, a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
+                    mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                }
+                // refill this slot with the chunk kUPD ahead (possibly of the next unit)
+                if (lu < my && lc >= s_uc[warp][lu]) {
+                    lc -= s_uc[warp][lu];
+                    ++lu;
+                }
+                if (lu < my) load_chunk(s_ub[warp][lu], lc, lane, cb[i], sb[i], pol);
+                ++lc;
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) a0[v] += a1[v];
+        if (ks > 1) {
+            // fixed-order K reduction within the group (named barrier 1 + group)
+            if (kw > 0) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) red[(warp * 4 + v) * 32 + lane] = a0[v];
+            }
+            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gj), "r"(32 * ks) : "memory");
+            if (kw == 0) {
+#pragma unroll 1
+                for (int w = 1; w < ks; ++w)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) a0[v] += red[((warp + w) * 4 + v) * 32 + lane];
+            }
+            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gj), "r"(32 * ks) : "memory");
+        }
+        if (kw != 0) continue;
+        // y = gs * 2^hexp * acc for the slot's pairs (columns), rows 16r + g, + 8
+        const int r = s_ur[warp][cu], m = s_m[sj], p0 = s_p0[sj];
+        const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const int col = 2 * q + e2;
+            if (col < m) {
+                const float sc = s_un[sj][col] * gs;
+                float *yp = d.y_ws + (size_t)(p0 + col) * H + 16 * r + g;
+                yp[0] = a0[e2] * sc;
+                yp[8] = a0[2 + e2] * sc;
+            }
+        }
+    }
+    // Tickets after the warp's last unit, not after each (a fence and an
+    // atomic round trip per unit would stall the ring): after the warp's
+    // barrier every lane fences (ordering all of the warp's y stores before
+    // its ticket), then lane i takes the ticket of the warp's unit i; the
+    // warp combines the tiles it completed last among the slots.
+    if (kw == 0 && my > 0) {
+        __syncwarp();
+        __threadfence();
+        const bool lastu = lane < my && atomicAdd(d.down_cnt + s_ur[warp][lane], 1u) == (unsigned)(ns - 1);
+        unsigned lm = __ballot_sync(0xffffffffu, lastu);
+        if (lm) __threadfence();
+        while (lm) {
+            const int i = __ffs(lm) - 1;
+            lm &= lm - 1;
+            const int r = s_ur[warp][i];
+            // every slot's y of this tile is written: out rows 16r .. 16r + 15
+            if (lane < 4 * T) {
+                const int t = lane >> 2, m4 = 4 * r + (lane & 3);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < P; ++j) {
+                    const float w = s_pw[t * P + j];
+                    const float4 y = __ldcg(reinterpret_cast<const float4 *>(d.y_ws + (size_t)s_pair[t * P + j] * H) + m4);
+                    acc.x = fmaf(w, y.x, acc.x);
+                    acc.y = fmaf(w, y.y, acc.y);
+                    acc.z = fmaf(w, y.z, acc.z);
+                    acc.w = fmaf(w, y.w, acc.w);
+                }
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 v;
+                v.x = *reinterpret_cast<uint32_t *>(&lo);
+                v.y = *reinterpret_cast<uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(out + (size_t)t * H + 4 * m4) = v;
+            }
+            if (lane == 0) d.down_cnt[r] = 0u;
+        }
+    }
+    MOE_TRACE_POINT(2, 3);
+}
+
+// The K split of the down wave kernel (as wave_lks), or -1: at most 8
+// tokens, one chunk format, and a block's unit range must span at most
+// kDMaxSlots slots whose staged h rows fit its shared memory.
+int down_wave_lks(const DevLayer &d, int T, int sm_count, size_t optin) {
+    if (T > 8) return -1;
+    // NVFP4 chunks only: F8 layers measured slower here than per slot
+    if (d.f8e || (d.S > 0 && d.f8s)) return -1;
+    const int slots = std::min(d.E, T * d.k) + d.S;
+    const long U = (long)slots * (d.H / 16);
+    const long perb = (U + sm_count - 1) / sm_count;
+    const long span = perb / (d.H / 16) + 2;
+    if (span > kDMaxSlots) return -1;
+    const int NC64 = (d.S > 0 ? std::max(d.I, d.Is) : d.I) / kChunkK;
+    const size_t smem = (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * (NC64 * 128 + 16);
+    if (smem + 16 * 1024 > optin) return -1;
+    int best = -1;
+    long bestc = 0;
+    for (int l = 0; l <= 2; ++l) {
+        const long per = (perb + (kUW >> l) - 1) / (kUW >> l);
+        bool fits = per <= kUMax;
+        for (int f = 0; f < 2 && fits; ++f) {
+            if (f == 1 && d.S == 0) break;
+            const int nc = f == 0 ? chunks_of(d.I, d.f8e) : chunks_of(d.Is, d.f8s);
+            fits = nc % (1 << l) == 0 && (nc >> l) % kUPD == 0;
+        }
+        if (!fits) continue;
+        const long cost = per * ((chunks_of(d.I, d.f8e) >> l) + (l > 0 ? 2 : 0));
+        if (best < 0 || cost < bestc) {
+            best = l;
+            bestc = cost;
+        }
+    }
+    return best;
+}
+
+size_t down_wave_smem(const DevLayer &d, int T, int sm_count) {
+    const int slots = std::min(d.E, T * d.k) + d.S;
+    const long U = (long)slots * (d.H / 16);
+    const long perb = (U + sm_count - 1) / sm_count;
+    const long span = perb / (d.H / 16) + 2;
+    const int NC64 = (d.S > 0 ? std::max(d.I, d.Is) : d.I) / kChunkK;
+    return (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * (NC64 * 128 + 16);
+}
+
 // The K split of the wave kernel: among 2^l <= 4 whose units per warp group
 // fit its table and whose chunks per unit are a whole number of ring turns,
 // the one with the fewest (chunks + a reduction) per group.  -1: the kernel
@@ -697,6 +957,8 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = allow_smem<0, 8, 4>(optin);
     if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<false>, optin);
     if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<true>, optin);
+    if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_down_wave_kernel<false>, optin);
+    if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_down_wave_kernel<true>, optin);
     if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
     if (e == cudaSuccess) e = prepare_route_kernel(optin);
     if (e == cudaSuccess) e = prepare_fused_kernel(optin);
@@ -726,7 +988,23 @@ cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int
     return launch_stage<0>(d, x, T, nullptr, s);
 }
 
-cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s) {
+cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, int optin_smem,
+                        cudaStream_t s) {
+    const int lks = down_wave_lks(d, T, sm_count, (size_t)optin_smem);
+    if (lks >= 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(sm_count);
+        cfg.blockDim = dim3(kUT);
+        cfg.dynamicSmemBytes = down_wave_smem(d, T, sm_count);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return (d.f8e || d.f8s) ? cudaLaunchKernelEx(&cfg, gemv_down_wave_kernel<true>, d, T, lks, out)
+                                : cudaLaunchKernelEx(&cfg, gemv_down_wave_kernel<false>, d, T, lks, out);
+    }
     return launch_stage<1>(d, nullptr, T, out, s);
 }
 

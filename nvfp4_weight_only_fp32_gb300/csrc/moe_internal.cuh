@@ -142,7 +142,8 @@ cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *
 // tokens where the shape allows it, else the per-slot GEMV kernel
 cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, int optin_smem,
                            cudaStream_t s);
-cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, cudaStream_t s);
+cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, int optin_smem,
+                        cudaStream_t s);
 bool grouped_supported(const DevLayer &d, int sm_count);
 cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s);
 cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, cudaStream_t s);
