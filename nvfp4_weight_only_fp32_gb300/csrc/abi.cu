@@ -187,6 +187,7 @@ void carve_workspace(moe_layer *L, char *base) {
     d.hot_slots = cv.take<int>(d.max_slots);
     d.tg_ticket = cv.take<unsigned>(Tm);
     d.emask = cv.take<unsigned long long>(E);
+    d.wave_ctr = cv.take<unsigned>(2);
     d.xq = cv.take<__nv_bfloat16>((size_t)Tm * H);
     d.gsx = cv.take<float>(Tm);
     d.gsh = cv.take<float>(d.max_pairs);

@@ -423,9 +423,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(DevLayer d, const __nv_b
 // per SM stages the step's x rows once (all T tokens: the MMA's N = 8
 // columns are the tokens, so every slot uses the same B operand and picks
 // its own tokens' columns in the epilogue), then its warps stream gate/up
-// units -- (slot, 16-row tile, K part), shared slots first -- assigned round
-// robin over every warp of the grid, through an 8-deep register ring that
-// runs on from one unit into the next.  Groups of 2^lks warps split a
+// units -- (slot, 16-row tile, K part), shared slots first -- handed out by
+// an atomic counter as they ask, through an 8-deep register ring that runs
+// on from one unit into the next.  Groups of 2^lks warps split a
 // tile's K range and add their partial sums in shared memory in a fixed
 // order.  Epilogue per unit: SwiGLU of the slot's tokens, h (BF16) and the
 // per-pair max |h| as in the per-slot kernel.
@@ -435,12 +435,15 @@ constexpr int kUT = 32 * kUW;
 constexpr int kUPD = 8;                 // ring depth (a unit's chunks are a multiple of it)
 constexpr int kUMax = 32;               // units per warp
 
+constexpr int kWaveSlots = 8 * kMaxTopK + kMaxShared;   // slots of a step of <= 8 tokens
+
 template <bool F8>
 __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
                                                               int T, int lks) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ const uint8_t *s_ub[kUW][kUMax];    // first chunk of the unit's K part
-    __shared__ short s_us[kUW][kUMax], s_ur[kUW][kUMax], s_uc[kUW][kUMax];   // slot, tile, chunks
+    __shared__ const uint8_t *s_sb[kWaveSlots];   // the slot's gate/up weights
+    __shared__ int s_se[kWaveSlots];              // its expert (< 0: shared)
+    __shared__ int s_q[kUW][2];                   // a warp group's next units
     __shared__ const uint4 *s_src[8];
     __shared__ float s_scale[8];
     __shared__ float s_unscale[8];
@@ -448,47 +451,38 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int H = d.H, S = d.S;
-    const int ks = 1 << lks, kw = warp & (ks - 1);
-    const int ngrp = gridDim.x * (kUW >> lks), gid = blockIdx.x * (kUW >> lks) + (warp >> lks);
+    const int ks = 1 << lks, kw = warp & (ks - 1), gj = warp >> lks;
+    const bool leader = kw == 0 && lane == 0;
     const int NC64 = H / kChunkK, row_stride = NC64 * 128 + 16;
     float *red = reinterpret_cast<float *>(smem + (size_t)(T + 1) * row_stride);   // [kUW][4][32]
     const uint64_t pol = evict_first_policy();
+    // a group's barrier (its K split), or the warp's own for a group of one
+    auto gsync = [&] {
+        if (ks > 1) asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gj), "r"(32 * ks) : "memory");
+        else __syncwarp();
+    };
 
     MOE_TRACE_POINT(1, 0);
-    pdl_wait();     // the router's slot tables, x's exponents and the zeroed h maxima
+    pdl_wait();     // the router's slot tables, x's exponents, the zeroed h maxima and unit counter
     pdl_trigger();
     MOE_TRACE_POINT(1, 1);
     const int ns = __ldcg(d.nslots);
     const int NTs = d.Is / 8, NT13 = d.I / 8;
     const int units = S * NTs + (ns - S) * NT13;
-    const int my = gid < units ? min(kUMax, (units - gid + ngrp - 1) / ngrp) : 0;
-    for (int i = lane; i < my; i += 32) {
-        const int u = gid + i * ngrp;
-        int sl, r;
-        if (u < S * NTs) {
-            sl = u / NTs;
-            r = u - sl * NTs;
-        } else {
-            const int v = u - S * NTs;
-            sl = S + v / NT13;
-            r = v - (sl - S) * NT13;
-        }
-        const int e = __ldcg(d.slot_expert + sl);
-        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
-        const int nc = chunks_of(H, f8), cpw = nc >> lks;
-        const uint8_t *b = e < 0 ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
-        s_ub[warp][i] = b + ((size_t)r * nc + kw * cpw) * kChunkBytes;
-        s_us[warp][i] = (short)sl;
-        s_ur[warp][i] = (short)r;
-        s_uc[warp][i] = (short)cpw;
+    // Units -- (slot, 16-row tile), shared slots first -- are handed out in
+    // order by an atomic counter as each warp group asks for its next one, so
+    // that groups on SMs that stream faster take more of them.  A group
+    // knows its next unit one unit ahead (the ring reaches into it) and asks
+    // for the one after at the start of each unit.
+    if (leader) {
+        const int u0 = (int)atomicAdd(d.wave_ctr, 1u);
+        s_q[gj][0] = u0;
+        s_q[gj][1] = u0 < units ? (int)atomicAdd(d.wave_ctr, 1u) : units;
     }
-    __syncwarp();
-    // the ring's first chunks, before the activations are staged
-    uint4 cb[kUPD];
-    uint2 sb[kUPD];
-    if (my > 0) {
-#pragma unroll
-        for (int i = 0; i < kUPD; ++i) load_chunk(s_ub[warp][0], i, lane, cb[i], sb[i], pol);
+    for (int sl = threadIdx.x; sl < ns; sl += kUT) {
+        const int e = __ldcg(d.slot_expert + sl);
+        s_se[sl] = e;
+        s_sb[sl] = e < 0 ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
     }
     if (threadIdx.x < T) {
         const int t = threadIdx.x;
@@ -500,19 +494,47 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
     for (int i = threadIdx.x; i < row_stride / 16; i += kUT)
         reinterpret_cast<uint4 *>(smem + (size_t)T * row_stride)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
+    int cur = s_q[gj][0], nxt = s_q[gj][1];
+    // unit -> slot, tile, and the first chunk of this warp's K part
+    auto decode = [&](int u, int &sl, int &r, int &cpw, const uint8_t *&base, bool &f8) {
+        if (u < S * NTs) {
+            sl = u / NTs;
+            r = u - sl * NTs;
+        } else {
+            const int v = u - S * NTs;
+            sl = S + v / NT13;
+            r = v - (sl - S) * NT13;
+        }
+        const int e = s_se[sl];
+        f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+        const int nc = chunks_of(H, f8);
+        cpw = nc >> lks;
+        base = s_sb[sl] + ((size_t)r * nc + kw * cpw) * kChunkBytes;
+    };
+    int sl = 0, r = 0, cpw = 0, nsl = 0, nr = 0, ncpw = 0;
+    bool f8 = false, nf8 = false;
+    const uint8_t *base = nullptr, *nbase = nullptr;
+    uint4 cb[kUPD];
+    uint2 sb[kUPD];
+    if (cur < units) {
+        decode(cur, sl, r, cpw, base, f8);
+#pragma unroll
+        for (int i = 0; i < kUPD; ++i) load_chunk(base, i, lane, cb[i], sb[i], pol);
+    }
     stage_rows<kUT>(T, 0, NC64, smem, row_stride, s_src, s_scale);
     __syncthreads();
     MOE_TRACE_POINT(1, 2);
 
     const uint8_t *xb = smem + (size_t)(g < T ? g : T) * row_stride + q * 32;
-    int lu = 0, lc = kUPD;     // next chunk to load: unit lu, chunk lc
 #pragma unroll 1
-    for (int cu = 0; cu < my; ++cu) {
-        const int sl = s_us[warp][cu], cpw = s_uc[warp][cu];
-        const int e = __ldcg(d.slot_expert + sl);
-        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+    for (int it = 0; cur < units; ++it) {
+        if (nxt < units) decode(nxt, nsl, nr, ncpw, nbase, nf8);
+        // the unit after next, asked for now, published at this unit's end
+        unsigned grab = (unsigned)units;
+        if (leader && nxt < units) grab = atomicAdd(d.wave_ctr, 1u);
         const int kc0 = kw * cpw;
         float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+        int lc = kUPD;     // next chunk to load (of this unit while < cpw, then of the next)
 #pragma unroll 1
         for (int cc = 0; cc < cpw; cc += kUPD) {
 #pragma unroll
@@ -530,66 +552,73 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
                     mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
                 }
                 // refill this slot with the chunk kUPD ahead (possibly of the next unit)
-                if (lu < my && lc >= s_uc[warp][lu]) {
-                    lc -= s_uc[warp][lu];
-                    ++lu;
-                }
-                if (lu < my) load_chunk(s_ub[warp][lu], lc, lane, cb[i], sb[i], pol);
+                if (lc < cpw) load_chunk(base, lc, lane, cb[i], sb[i], pol);
+                else if (nxt < units) load_chunk(nbase, lc - cpw, lane, cb[i], sb[i], pol);
                 ++lc;
             }
         }
 #pragma unroll
         for (int v = 0; v < 4; ++v) a0[v] += a1[v];
+        if (leader && ks > 1) s_q[gj][it & 1] = (int)grab;
         if (ks > 1) {
             // fixed-order K reduction within the group (named barrier 1 + group)
             if (kw > 0) {
 #pragma unroll
                 for (int v = 0; v < 4; ++v) red[(warp * 4 + v) * 32 + lane] = a0[v];
             }
-            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + (warp >> lks)), "r"(32 * ks) : "memory");
+            gsync();
             if (kw == 0) {
 #pragma unroll 1
                 for (int w = 1; w < ks; ++w)
 #pragma unroll
                     for (int v = 0; v < 4; ++v) a0[v] += red[((warp + w) * 4 + v) * 32 + lane];
             }
-            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + (warp >> lks)), "r"(32 * ks) : "memory");
+            gsync();
         }
-        if (kw != 0) continue;
-        // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row 8r + g;
-        // columns are tokens, a slot's pairs are its tokens in ascending order
-        const int r = s_ur[warp][cu];
-        const int m = __ldcg(d.slot_m + sl), p0 = __ldcg(d.slot_p0 + sl);
-        unsigned msk = 0u;
-        if (lane < m) msk = 1u << __ldcg(d.pair_tok + p0 + lane);
-        msk = __reduce_or_sync(0xffffffffu, msk);
-        float gsa, gsb;
-        if (e < 0) {
-            gsa = d.sgs13[2 * (-e - 1)];
-            gsb = d.sgs13[2 * (-e - 1) + 1];
-        } else {
-            gsa = d.gs13[2 * e];
-            gsb = d.gs13[2 * e + 1];
-        }
-        const int n = 8 * r + g;
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int t = 2 * q + e2;
-            const bool on = t < T && ((msk >> t) & 1u);
-            const int p = p0 + __popc(msk & ((1u << t) - 1u));
-            float habs = 0.f;
-            if (on) {
-                const float sc = s_unscale[t];
-                const float gt = a0[e2] * gsa * sc;
-                const float up = a0[2 + e2] * gsb * sc;
-                const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
-                d.h_ws[(size_t)p * d.Imax + n] = hb;
-                habs = fabsf(__bfloat162float(hb));
+        const int n2 = ks > 1 ? s_q[gj][it & 1] : (int)__shfl_sync(0xffffffffu, grab, 0);
+        if (kw == 0) {
+            // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row 8r + g;
+            // columns are tokens, a slot's pairs are its tokens in ascending order
+            const int e = s_se[sl];
+            const int m = __ldcg(d.slot_m + sl), p0 = __ldcg(d.slot_p0 + sl);
+            unsigned msk = 0u;
+            if (lane < m) msk = 1u << __ldcg(d.pair_tok + p0 + lane);
+            msk = __reduce_or_sync(0xffffffffu, msk);
+            float gsa, gsb;
+            if (e < 0) {
+                gsa = d.sgs13[2 * (-e - 1)];
+                gsb = d.sgs13[2 * (-e - 1) + 1];
+            } else {
+                gsa = d.gs13[2 * e];
+                gsb = d.gs13[2 * e + 1];
             }
+            const int n = 8 * r + g;
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, off));
-            if (on && g == 0) atomicMax(d.hmax + p, __float_as_uint(habs));
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int t = 2 * q + e2;
+                const bool on = t < T && ((msk >> t) & 1u);
+                const int p = p0 + __popc(msk & ((1u << t) - 1u));
+                float habs = 0.f;
+                if (on) {
+                    const float sc = s_unscale[t];
+                    const float gt = a0[e2] * gsa * sc;
+                    const float up = a0[2 + e2] * gsb * sc;
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                    d.h_ws[(size_t)p * d.Imax + n] = hb;
+                    habs = fabsf(__bfloat162float(hb));
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, off));
+                if (on && g == 0) atomicMax(d.hmax + p, __float_as_uint(habs));
+            }
         }
+        cur = nxt;
+        sl = nsl;
+        r = nr;
+        cpw = ncpw;
+        base = nbase;
+        f8 = nf8;
+        nxt = n2;
     }
     MOE_TRACE_POINT(1, 3);
 }
@@ -854,10 +883,9 @@ size_t down_wave_smem(const DevLayer &d, int T, int sm_count) {
     return (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * (NC64 * 128 + 16);
 }
 
-// The K split of the wave kernel: among 2^l <= 4 whose units per warp group
-// fit its table and whose chunks per unit are a whole number of ring turns,
-// the one with the fewest (chunks + a reduction) per group.  -1: the kernel
-// does not apply.
+// The K split of the wave kernel: among 2^l <= 4 whose chunks per unit are a
+// whole number of ring turns, the one with the fewest (chunks + a reduction)
+// per group at an even share of the units.  -1: the kernel does not apply.
 int wave_lks(const DevLayer &d, int T, int sm_count) {
     if (T > 8) return -1;
     // units of one length: routed and shared experts in the same chunk format
@@ -868,10 +896,11 @@ int wave_lks(const DevLayer &d, int T, int sm_count) {
     const long units = (long)d.S * (d.Is / 8) + (long)slots * (d.I / 8);
     int best = -1;
     long bestc = 0;
+    if (slots + d.S > kWaveSlots) return -1;
     for (int l = 0; l <= 2; ++l) {
         const long groups = (long)sm_count * (kUW >> l);
         const long per = (units + groups - 1) / groups;
-        bool fits = per <= kUMax;
+        bool fits = true;
         for (int f = 0; f < 2 && fits; ++f) {
             const bool f8 = f == 0 ? d.f8e : (d.S > 0 && d.f8s);
             const int nc = chunks_of(d.H, f8);

@@ -117,6 +117,7 @@ struct DevLayer {
     int *hot_slots;                 // [max_slots] their slot indices, ascending
     unsigned *tg_ticket;            // [max_tokens] router: arrivals per token group
     unsigned long long *emask;      // [E] router: tokens that selected each expert (bit t)
+    unsigned *wave_ctr;             // [2] chain gate/up wave kernel: next unit to hand out (reset by the router)
     unsigned long long *trace;      // traced build only: phase timestamps
     int trace_blocks;
     int score_func;                 // 0 sigmoid per expert, 1 softmax over all experts

@@ -480,7 +480,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         d.pair_of[t * P + K + sidx] = p;
     }
     for (int p = threadIdx.x; p < T * P; p += kThreads) d.hmax[p] = 0u;
-    if (threadIdx.x == 0) *d.ticket = 0u;
+    if (threadIdx.x == 0) {
+        *d.ticket = 0u;
+        d.wave_ctr[0] = 0u;
+        d.wave_ctr[1] = 0u;
+    }
     MOE_TRACE_POINT(0, 7);
 }
 
