@@ -628,8 +628,8 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
 // warps per SM takes a contiguous range of (slot, 16-row output tile) units
 // in slot order -- a range spans few slots, whose h rows (the B operand: a
 // slot's pairs as columns) it stages once -- and its warp groups take the
-// range's units round robin, streaming them through an 8-deep register ring
-// that runs on from one unit into the next.  Groups of 2^lks warps split a
+// range's units as they ask (a shared counter), streaming them through an
+// 8-deep register ring that runs on from one unit into the next.  Groups of 2^lks warps split a
 // unit's K range (fixed-order reduction).  Epilogue per unit: y = gs * acc
 // into the workspace; after its last unit a warp takes the per-tile tickets
 // of its units (no spinning), and the unit that completed a tile last among
@@ -641,56 +641,48 @@ template <bool F8>
 __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int T, int lks,
                                                                 __nv_bfloat16 *__restrict__ out) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ const uint8_t *s_ub[kUW][kUMax];    // first chunk of the unit's K part
-    __shared__ short s_us[kUW][kUMax], s_ur[kUW][kUMax], s_uc[kUW][kUMax];   // slot, tile, chunks
     __shared__ const uint4 *s_src[kDMaxSlots][8];
     __shared__ float s_scale[kDMaxSlots][8], s_un[kDMaxSlots][8];
     __shared__ int s_off[kDMaxSlots], s_rs[kDMaxSlots], s_m[kDMaxSlots], s_p0[kDMaxSlots];
+    __shared__ int s_e[kDMaxSlots];
+    __shared__ const uint8_t *s_wb[kDMaxSlots];
     __shared__ int s_pair[8 * (kMaxTopK + kMaxShared)];
     __shared__ float s_pw[8 * (kMaxTopK + kMaxShared)];
+    __shared__ int s_ctr;                          // the block's next unit
+    __shared__ int s_q[kUW][2];                    // a warp group's next units
+    __shared__ short s_dr[kUW][kUMax];             // tiles whose y a warp wrote, tickets pending
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int H = d.H, K = d.k, P = d.k + d.S;
-    const int ks = 1 << lks, kw = warp & (ks - 1), ngb = kUW >> lks, gj = warp >> lks;
+    const int ks = 1 << lks, kw = warp & (ks - 1), gj = warp >> lks;
+    const bool leader = kw == 0 && lane == 0;
     const int NTd = H / 16;
     float *red = reinterpret_cast<float *>(smem);   // [kUW][4][32]
     uint8_t *stage = smem + (size_t)kUW * 4 * 32 * sizeof(float);
     const uint64_t pol = evict_first_policy();
+    auto gsync = [&] {
+        if (ks > 1) asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gj), "r"(32 * ks) : "memory");
+        else __syncwarp();
+    };
 
     MOE_TRACE_POINT(2, 0);
     // The router has completed before this kernel could start (the gate/up
     // kernel released it only after its own wait): the slot and pair tables
-    // are final.  List the units and stream their weights; wait for h after.
+    // are final.  Take the units and stream their weights; wait for h after.
     const int ns = __ldcg(d.nslots);
     const long U = (long)ns * NTd;
     const int ub0 = (int)(U * blockIdx.x / gridDim.x), ub1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
-    const int sl_lo = ub0 / NTd, nsb = ub1 > ub0 ? (ub1 - 1) / NTd - sl_lo + 1 : 0;
-    const int my = ub0 + gj < ub1 ? min(kUMax, (ub1 - ub0 - gj + ngb - 1) / ngb) : 0;
-    for (int i = lane; i < my; i += 32) {
-        const int tu = ub0 + gj + i * ngb;
-        const int sl = tu / NTd, r = tu - sl * NTd;
-        const int e = __ldcg(d.slot_expert + sl);
-        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
-        const int nc = chunks_of(e < 0 ? d.Is : d.I, f8), cpw = nc >> lks;
-        const uint8_t *b = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
-        s_ub[warp][i] = b + ((size_t)r * nc + kw * cpw) * kChunkBytes;
-        s_us[warp][i] = (short)(sl - sl_lo);
-        s_ur[warp][i] = (short)r;
-        s_uc[warp][i] = (short)cpw;
-    }
-    __syncwarp();
-    uint4 cb[kUPD];
-    uint2 sb[kUPD];
-    if (my > 0) {
-#pragma unroll
-        for (int i = 0; i < kUPD; ++i) load_chunk(s_ub[warp][0], i, lane, cb[i], sb[i], pol);
-    }
-    // the staged slots' geometry (8 rows each, rows >= m zero) and the
-    // combine's pair table
+    const int nu = ub1 - ub0;
+    const int sl_lo = ub0 / NTd, nsb = nu > 0 ? (ub1 - 1) / NTd - sl_lo + 1 : 0;
+    if (threadIdx.x == 0) s_ctr = 0;
+    // the staged slots' geometry (8 rows each, rows >= m zero) and weights,
+    // and the combine's pair table
     if (threadIdx.x < nsb) {
         const int sl = sl_lo + threadIdx.x;
         const int e = __ldcg(d.slot_expert + sl);
+        s_e[threadIdx.x] = e;
+        s_wb[threadIdx.x] = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
         s_rs[threadIdx.x] = ((e < 0 ? d.Is : d.I) / kChunkK) * 128 + 16;
         s_m[threadIdx.x] = __ldcg(d.slot_m + sl);
         s_p0[threadIdx.x] = __ldcg(d.slot_p0 + sl);
@@ -701,12 +693,44 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
         s_pw[i] = (i % P) < K ? __ldcg(d.pair_w + p) : 1.0f;
     }
     __syncthreads();
+    // The block's units are handed out by a shared counter as each warp
+    // group asks (one unit ahead, for the ring), so that its warps finish
+    // together.
+    if (leader) {
+        const int u0 = atomicAdd(&s_ctr, 1);
+        s_q[gj][0] = u0;
+        s_q[gj][1] = u0 < nu ? atomicAdd(&s_ctr, 1) : nu;
+    }
     if (threadIdx.x == 0) {
         int off = 0;
         for (int j = 0; j < nsb; ++j) {
             s_off[j] = off;
             off += 8 * s_rs[j];
         }
+    }
+    __syncthreads();
+    int cur = s_q[gj][0], nxt = s_q[gj][1];
+    // unit -> staged slot, tile, and the first chunk of this warp's K part
+    auto decode = [&](int u, int &sj, int &r, int &cpw, const uint8_t *&base, bool &f8) {
+        const int tu = ub0 + u;
+        const int sl = tu / NTd;
+        r = tu - sl * NTd;
+        sj = sl - sl_lo;
+        const int e = s_e[sj];
+        f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+        const int nc = chunks_of(e < 0 ? d.Is : d.I, f8);
+        cpw = nc >> lks;
+        base = s_wb[sj] + ((size_t)r * nc + kw * cpw) * kChunkBytes;
+    };
+    int sj = 0, r = 0, cpw = 0, nsj = 0, nr = 0, ncpw = 0;
+    bool f8 = false, nf8 = false;
+    const uint8_t *base = nullptr, *nbase = nullptr;
+    uint4 cb[kUPD];
+    uint2 sb[kUPD];
+    if (cur < nu) {
+        decode(cur, sj, r, cpw, base, f8);
+#pragma unroll
+        for (int i = 0; i < kUPD; ++i) load_chunk(base, i, lane, cb[i], sb[i], pol);
     }
     pdl_wait();     // h and its maxima
     pdl_trigger();
@@ -732,16 +756,58 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
     __syncthreads();
     MOE_TRACE_POINT(2, 2);
 
-    int lu = 0, lc = kUPD;     // next chunk to load: unit lu, chunk lc
+    // Tickets of the tiles in the warp's pending list: after the warp's
+    // barrier every lane fences (ordering all of the warp's y stores before
+    // its tickets), then lane i takes the ticket of entry i; the warp
+    // combines the tiles it completed last among the slots.  Taken after
+    // the warp's last unit, not after each (a fence and an atomic round trip
+    // per unit would stall the ring), or when the list is full.
+    int nd = 0;
+    auto tickets = [&]() {
+        __syncwarp();
+        __threadfence();
+        const bool lastu = lane < nd && atomicAdd(d.down_cnt + s_dr[warp][lane], 1u) == (unsigned)(ns - 1);
+        unsigned lm = __ballot_sync(0xffffffffu, lastu);
+        if (lm) __threadfence();
+        while (lm) {
+            const int i = __ffs(lm) - 1;
+            lm &= lm - 1;
+            const int rr = s_dr[warp][i];
+            // every slot's y of this tile is written: out rows 16rr .. 16rr + 15
+            if (lane < 4 * T) {
+                const int t = lane >> 2, m4 = 4 * rr + (lane & 3);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < P; ++j) {
+                    const float w = s_pw[t * P + j];
+                    const float4 y = __ldcg(reinterpret_cast<const float4 *>(d.y_ws + (size_t)s_pair[t * P + j] * H) + m4);
+                    acc.x = fmaf(w, y.x, acc.x);
+                    acc.y = fmaf(w, y.y, acc.y);
+                    acc.z = fmaf(w, y.z, acc.z);
+                    acc.w = fmaf(w, y.w, acc.w);
+                }
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 v;
+                v.x = *reinterpret_cast<uint32_t *>(&lo);
+                v.y = *reinterpret_cast<uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(out + (size_t)t * H + 4 * m4) = v;
+            }
+            if (lane == 0) d.down_cnt[rr] = 0u;
+        }
+        __syncwarp();
+        nd = 0;
+    };
+
 #pragma unroll 1
-    for (int cu = 0; cu < my; ++cu) {
-        const int sj = s_us[warp][cu], cpw = s_uc[warp][cu];
-        const int sl = sl_lo + sj;
-        const int e = __ldcg(d.slot_expert + sl);
-        const bool f8 = F8 && (e < 0 ? d.f8s : d.f8e);
+    for (int it = 0; cur < nu; ++it) {
+        if (nxt < nu) decode(nxt, nsj, nr, ncpw, nbase, nf8);
+        // the unit after next, asked for now, published at this unit's end
+        int grab = nu;
+        if (leader && nxt < nu) grab = atomicAdd(&s_ctr, 1);
         const int kc0 = kw * cpw;
         const uint8_t *xb = stage + s_off[sj] + (size_t)g * s_rs[sj] + q * 32;
         float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+        int lc = kUPD;     // next chunk to load (of this unit while < cpw, then of the next)
 #pragma unroll 1
         for (int cc = 0; cc < cpw; cc += kUPD) {
 #pragma unroll
@@ -759,83 +825,57 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
                     mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
                 }
                 // refill this slot with the chunk kUPD ahead (possibly of the next unit)
-                if (lu < my && lc >= s_uc[warp][lu]) {
-                    lc -= s_uc[warp][lu];
-                    ++lu;
-                }
-                if (lu < my) load_chunk(s_ub[warp][lu], lc, lane, cb[i], sb[i], pol);
+                if (lc < cpw) load_chunk(base, lc, lane, cb[i], sb[i], pol);
+                else if (nxt < nu) load_chunk(nbase, lc - cpw, lane, cb[i], sb[i], pol);
                 ++lc;
             }
         }
 #pragma unroll
         for (int v = 0; v < 4; ++v) a0[v] += a1[v];
+        if (leader && ks > 1) s_q[gj][it & 1] = grab;
         if (ks > 1) {
             // fixed-order K reduction within the group (named barrier 1 + group)
             if (kw > 0) {
 #pragma unroll
                 for (int v = 0; v < 4; ++v) red[(warp * 4 + v) * 32 + lane] = a0[v];
             }
-            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gj), "r"(32 * ks) : "memory");
+            gsync();
             if (kw == 0) {
 #pragma unroll 1
                 for (int w = 1; w < ks; ++w)
 #pragma unroll
                     for (int v = 0; v < 4; ++v) a0[v] += red[((warp + w) * 4 + v) * 32 + lane];
             }
-            asm volatile("bar.sync %0, %1;\n" ::"r"(1 + gj), "r"(32 * ks) : "memory");
+            gsync();
         }
-        if (kw != 0) continue;
-        // y = gs * 2^hexp * acc for the slot's pairs (columns), rows 16r + g, + 8
-        const int r = s_ur[warp][cu], m = s_m[sj], p0 = s_p0[sj];
-        const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
+        const int n2 = ks > 1 ? s_q[gj][it & 1] : __shfl_sync(0xffffffffu, grab, 0);
+        if (kw == 0) {
+            // y = gs * 2^hexp * acc for the slot's pairs (columns), rows 16r + g, + 8
+            const int e = s_e[sj], m = s_m[sj], p0 = s_p0[sj];
+            const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int col = 2 * q + e2;
-            if (col < m) {
-                const float sc = s_un[sj][col] * gs;
-                float *yp = d.y_ws + (size_t)(p0 + col) * H + 16 * r + g;
-                yp[0] = a0[e2] * sc;
-                yp[8] = a0[2 + e2] * sc;
-            }
-        }
-    }
-    // Tickets after the warp's last unit, not after each (a fence and an
-    // atomic round trip per unit would stall the ring): after the warp's
-    // barrier every lane fences (ordering all of the warp's y stores before
-    // its ticket), then lane i takes the ticket of the warp's unit i; the
-    // warp combines the tiles it completed last among the slots.
-    if (kw == 0 && my > 0) {
-        __syncwarp();
-        __threadfence();
-        const bool lastu = lane < my && atomicAdd(d.down_cnt + s_ur[warp][lane], 1u) == (unsigned)(ns - 1);
-        unsigned lm = __ballot_sync(0xffffffffu, lastu);
-        if (lm) __threadfence();
-        while (lm) {
-            const int i = __ffs(lm) - 1;
-            lm &= lm - 1;
-            const int r = s_ur[warp][i];
-            // every slot's y of this tile is written: out rows 16r .. 16r + 15
-            if (lane < 4 * T) {
-                const int t = lane >> 2, m4 = 4 * r + (lane & 3);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int j = 0; j < P; ++j) {
-                    const float w = s_pw[t * P + j];
-                    const float4 y = __ldcg(reinterpret_cast<const float4 *>(d.y_ws + (size_t)s_pair[t * P + j] * H) + m4);
-                    acc.x = fmaf(w, y.x, acc.x);
-                    acc.y = fmaf(w, y.y, acc.y);
-                    acc.z = fmaf(w, y.z, acc.z);
-                    acc.w = fmaf(w, y.w, acc.w);
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int col = 2 * q + e2;
+                if (col < m) {
+                    const float sc = s_un[sj][col] * gs;
+                    float *yp = d.y_ws + (size_t)(p0 + col) * H + 16 * r + g;
+                    yp[0] = a0[e2] * sc;
+                    yp[8] = a0[2 + e2] * sc;
                 }
-                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-                uint2 v;
-                v.x = *reinterpret_cast<uint32_t *>(&lo);
-                v.y = *reinterpret_cast<uint32_t *>(&hi);
-                *reinterpret_cast<uint2 *>(out + (size_t)t * H + 4 * m4) = v;
             }
-            if (lane == 0) d.down_cnt[r] = 0u;
+            if (lane == 0) s_dr[warp][nd] = (short)r;
+            ++nd;
+            if (nd == kUMax) tickets();
         }
+        cur = nxt;
+        sj = nsj;
+        r = nr;
+        cpw = ncpw;
+        base = nbase;
+        f8 = nf8;
+        nxt = n2;
     }
+    if (kw == 0 && nd > 0) tickets();
     MOE_TRACE_POINT(2, 3);
 }
 
@@ -858,7 +898,7 @@ int down_wave_lks(const DevLayer &d, int T, int sm_count, size_t optin) {
     long bestc = 0;
     for (int l = 0; l <= 2; ++l) {
         const long per = (perb + (kUW >> l) - 1) / (kUW >> l);
-        bool fits = per <= kUMax;
+        bool fits = true;
         for (int f = 0; f < 2 && fits; ++f) {
             if (f == 1 && d.S == 0) break;
             const int nc = f == 0 ? chunks_of(d.I, d.f8e) : chunks_of(d.Is, d.f8s);
