@@ -884,8 +884,6 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
 // kDMaxSlots slots whose staged h rows fit its shared memory.
 int down_wave_lks(const DevLayer &d, int T, int sm_count, size_t optin) {
     if (T > 8) return -1;
-    // NVFP4 chunks only: F8 layers measured slower here than per slot
-    if (d.f8e || (d.S > 0 && d.f8s)) return -1;
     const int slots = std::min(d.E, T * d.k) + d.S;
     const long U = (long)slots * (d.H / 16);
     const long perb = (U + sm_count - 1) / sm_count;
@@ -928,10 +926,8 @@ size_t down_wave_smem(const DevLayer &d, int T, int sm_count) {
 // per group at an even share of the units.  -1: the kernel does not apply.
 int wave_lks(const DevLayer &d, int T, int sm_count) {
     if (T > 8) return -1;
-    // units of one length: routed and shared experts in the same chunk format
-    // (an F8 tile has twice the chunks, and the round-robin assignment would
-    // leave the warps that draw one behind; measured slower)
-    if (d.S > 0 && d.f8e != d.f8s) return -1;
+    // (routed and shared experts may differ in chunk format: an F8 tile has
+    // twice the chunks, which the units handed out on demand absorb)
     const int slots = std::min(d.E, T * d.k);
     const long units = (long)d.S * (d.Is / 8) + (long)slots * (d.I / 8);
     int best = -1;
