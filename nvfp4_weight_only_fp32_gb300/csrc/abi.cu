@@ -185,6 +185,8 @@ void carve_workspace(moe_layer *L, char *base) {
     d.calls = cv.take<unsigned>(L->sm_count);
     d.nhot = cv.take<int>(1);
     d.hot_slots = cv.take<int>(d.max_slots);
+    d.ncold = cv.take<int>(1);
+    d.cold_slots = cv.take<int>(d.max_slots);
     d.tg_ticket = cv.take<unsigned>(Tm);
     d.emask = cv.take<unsigned long long>(E);
     d.wave_ctr = cv.take<unsigned>(2);
@@ -535,8 +537,11 @@ moe_status moe_stage_down(moe_layer *L, int T, void *out, void *stream) {
                        d.hsf, d.Imax / 2, d.Imax / 16, st);
     }
     if (e == cudaSuccess) e = launch_down(L->d, T, static_cast<__nv_bfloat16 *>(out), L->sm_count, L->optin_smem, st);
-    if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0)
-        e = launch_grouped_down(L->d, T, static_cast<__nv_bfloat16 *>(out), L->sm_count, st);
+    if (e == cudaSuccess && T > 8 && L->d.grouped_min > 0) {
+        DevLayer dd = L->d;
+        dd.tick16 = down_tile_tickets(L->d, T, L->sm_count, L->optin_smem) ? 1 : 0;
+        e = launch_grouped_down(dd, T, static_cast<__nv_bfloat16 *>(out), L->sm_count, st);
+    }
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");
 }
 

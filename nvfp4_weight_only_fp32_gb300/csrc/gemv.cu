@@ -624,30 +624,35 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
 }
 
 // ---------------------------------------------------------------------------
-// Down + combine for steps of at most 8 tokens, as one wave: one block of 16
-// warps per SM takes a contiguous range of (slot, 16-row output tile) units
-// in slot order -- a range spans few slots, whose h rows (the B operand: a
-// slot's pairs as columns) it stages once -- and its warp groups take the
-// range's units as they ask (a shared counter), streaming them through an
-// 8-deep register ring that runs on from one unit into the next.  Groups of 2^lks warps split a
-// unit's K range (fixed-order reduction).  Epilogue per unit: y = gs * acc
-// into the workspace; after its last unit a warp takes the per-tile tickets
-// of its units (no spinning), and the unit that completed a tile last among
-// the slots combines that tile's 16 rows for all tokens.
+// Wave kernels over a list of slots, each slot with its own B operand: down +
+// combine (MODE 1) for steps of at most 8 tokens (every slot) and, above 8
+// tokens, gate/up + SwiGLU (MODE 0) and down + combine over the routed slots
+// that the grouped kernels leave (fewer than grouped_min_tokens <= 8 tokens).
+// One block of 16 warps per SM takes a contiguous, slot-major range of
+// (slot, 16-row tile) units -- a range spans few slots, whose B rows (a
+// slot's tokens' x rows, or its pairs' h rows, at most 8) it stages once --
+// and its warp groups take the range's units as they ask (a shared counter),
+// streaming them through a PD-deep register ring that runs on from one unit
+// into the next.  Groups of 2^lks warps split a unit's K range (fixed-order
+// reduction).  Gate/up epilogue: SwiGLU into h with the per-pair max |h|, as
+// the per-slot kernel.  Down epilogue: y = gs * acc into the workspace; after
+// its last unit a warp takes the per-tile tickets of its units (no spinning),
+// and the unit that completed a tile last among the slots combines that
+// tile's 16 rows for all tokens.
 // ---------------------------------------------------------------------------
 constexpr int kDMaxSlots = 12;          // slots one block's units may span
 
-template <bool F8>
-__global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int T, int lks,
+template <int MODE, bool F8, int PD>
+__global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
+                                                                int T, int lks, int cold,
                                                                 __nv_bfloat16 *__restrict__ out) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ const uint4 *s_src[kDMaxSlots][8];
     __shared__ float s_scale[kDMaxSlots][8], s_un[kDMaxSlots][8];
-    __shared__ int s_off[kDMaxSlots], s_rs[kDMaxSlots], s_m[kDMaxSlots], s_p0[kDMaxSlots];
-    __shared__ int s_e[kDMaxSlots];
+    __shared__ int s_off[kDMaxSlots], s_rs[kDMaxSlots], s_m[kDMaxSlots], s_p0[kDMaxSlots], s_e[kDMaxSlots];
     __shared__ const uint8_t *s_wb[kDMaxSlots];
-    __shared__ int s_pair[8 * (kMaxTopK + kMaxShared)];
-    __shared__ float s_pw[8 * (kMaxTopK + kMaxShared)];
+    __shared__ int s_pair[MODE == 1 ? kMaxTokens * (kMaxTopK + kMaxShared) : 1];
+    __shared__ float s_pw[MODE == 1 ? kMaxTokens * (kMaxTopK + kMaxShared) : 1];
     __shared__ int s_ctr;                          // the block's next unit
     __shared__ int s_q[kUW][2];                    // a warp group's next units
     __shared__ short s_dr[kUW][kUMax];             // tiles whose y a warp wrote, tickets pending
@@ -657,7 +662,7 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
     const int H = d.H, K = d.k, P = d.k + d.S;
     const int ks = 1 << lks, kw = warp & (ks - 1), gj = warp >> lks;
     const bool leader = kw == 0 && lane == 0;
-    const int NTd = H / 16;
+    const int NT = MODE == 0 ? d.I / 8 : H / 16;   // units per slot (gate/up: routed slots only)
     float *red = reinterpret_cast<float *>(smem);   // [kUW][4][32]
     uint8_t *stage = smem + (size_t)kUW * 4 * 32 * sizeof(float);
     const uint64_t pol = evict_first_policy();
@@ -666,31 +671,45 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
         else __syncwarp();
     };
 
-    MOE_TRACE_POINT(2, 0);
-    // The router has completed before this kernel could start (the gate/up
-    // kernel released it only after its own wait): the slot and pair tables
-    // are final.  Take the units and stream their weights; wait for h after.
+    MOE_TRACE_POINT(1 + MODE, 0);
+    // Down: the router has completed before this kernel could start (the
+    // gate/up kernels released it only after their own waits), so the slot
+    // and pair tables are final: stream the weights, wait for h after.
+    // Gate/up: the router's tables come from the kernel before: wait first.
+    if (MODE == 0) {
+        pdl_wait();
+        pdl_trigger();
+    }
     const int ns = __ldcg(d.nslots);
-    const long U = (long)ns * NTd;
+    const int nlist = cold ? __ldcg(d.ncold) : ns;
+    const long U = (long)nlist * NT;
     const int ub0 = (int)(U * blockIdx.x / gridDim.x), ub1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
     const int nu = ub1 - ub0;
-    const int sl_lo = ub0 / NTd, nsb = nu > 0 ? (ub1 - 1) / NTd - sl_lo + 1 : 0;
+    const int ci_lo = ub0 / NT, nsb = nu > 0 ? (ub1 - 1) / NT - ci_lo + 1 : 0;
     if (threadIdx.x == 0) s_ctr = 0;
     // the staged slots' geometry (8 rows each, rows >= m zero) and weights,
     // and the combine's pair table
     if (threadIdx.x < nsb) {
-        const int sl = sl_lo + threadIdx.x;
+        const int ci = ci_lo + threadIdx.x;
+        const int sl = cold ? __ldcg(d.cold_slots + ci) : ci;
         const int e = __ldcg(d.slot_expert + sl);
         s_e[threadIdx.x] = e;
-        s_wb[threadIdx.x] = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
-        s_rs[threadIdx.x] = ((e < 0 ? d.Is : d.I) / kChunkK) * 128 + 16;
+        if (MODE == 0) {
+            s_wb[threadIdx.x] = e < 0 ? d.sw13r + (size_t)(-e - 1) * d.s13_stride : d.w13r + (size_t)e * d.e13_stride;
+            s_rs[threadIdx.x] = (H / kChunkK) * 128 + 16;
+        } else {
+            s_wb[threadIdx.x] = e < 0 ? d.sw2r + (size_t)(-e - 1) * d.s2_stride : d.w2r + (size_t)e * d.e2_stride;
+            s_rs[threadIdx.x] = ((e < 0 ? d.Is : d.I) / kChunkK) * 128 + 16;
+        }
         s_m[threadIdx.x] = __ldcg(d.slot_m + sl);
         s_p0[threadIdx.x] = __ldcg(d.slot_p0 + sl);
     }
-    for (int i = threadIdx.x; i < T * P; i += kUT) {
-        const int p = __ldcg(d.pair_of + i);
-        s_pair[i] = p;
-        s_pw[i] = (i % P) < K ? __ldcg(d.pair_w + p) : 1.0f;
+    if (MODE == 1) {
+        for (int i = threadIdx.x; i < T * P; i += kUT) {
+            const int p = __ldcg(d.pair_of + i);
+            s_pair[i] = p;
+            s_pw[i] = (i % P) < K ? __ldcg(d.pair_w + p) : 1.0f;
+        }
     }
     __syncthreads();
     // The block's units are handed out by a shared counter as each warp
@@ -713,36 +732,46 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
     // unit -> staged slot, tile, and the first chunk of this warp's K part
     auto decode = [&](int u, int &sj, int &r, int &cpw, const uint8_t *&base, bool &f8) {
         const int tu = ub0 + u;
-        const int sl = tu / NTd;
-        r = tu - sl * NTd;
-        sj = sl - sl_lo;
+        const int ci = tu / NT;
+        r = tu - ci * NT;
+        sj = ci - ci_lo;
         const int e = s_e[sj];
         f8 = F8 && (e < 0 ? d.f8s : d.f8e);
-        const int nc = chunks_of(e < 0 ? d.Is : d.I, f8);
+        const int nc = MODE == 0 ? chunks_of(H, f8) : chunks_of(e < 0 ? d.Is : d.I, f8);
         cpw = nc >> lks;
         base = s_wb[sj] + ((size_t)r * nc + kw * cpw) * kChunkBytes;
     };
     int sj = 0, r = 0, cpw = 0, nsj = 0, nr = 0, ncpw = 0;
     bool f8 = false, nf8 = false;
     const uint8_t *base = nullptr, *nbase = nullptr;
-    uint4 cb[kUPD];
-    uint2 sb[kUPD];
+    uint4 cb[PD];
+    uint2 sb[PD];
     if (cur < nu) {
         decode(cur, sj, r, cpw, base, f8);
 #pragma unroll
-        for (int i = 0; i < kUPD; ++i) load_chunk(base, i, lane, cb[i], sb[i], pol);
+        for (int i = 0; i < PD; ++i) load_chunk(base, i, lane, cb[i], sb[i], pol);
     }
-    pdl_wait();     // h and its maxima
-    pdl_trigger();
-    MOE_TRACE_POINT(2, 1);
+    if (MODE == 1) {
+        pdl_wait();     // h and its maxima
+        pdl_trigger();
+    }
+    MOE_TRACE_POINT(1 + MODE, 1);
     if (threadIdx.x < 8 * nsb) {
         const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
         if (c < s_m[j]) {
             const int p = s_p0[j] + c;
-            const int ex = hexp_of(__ldcg(d.hmax + p));
-            s_src[j][c] = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)p * d.Imax);
-            s_scale[j][c] = pow2f(-ex);
-            s_un[j][c] = pow2f(ex) * (d.w4a4 ? __ldcg(d.gsh + p) : 1.f);
+            if (MODE == 0) {
+                const int tok = __ldcg(d.pair_tok + p);
+                const int ex = __ldcg(d.xexp + tok);
+                s_src[j][c] = reinterpret_cast<const uint4 *>(x + (size_t)tok * H);
+                s_scale[j][c] = pow2f(-ex);
+                s_un[j][c] = pow2f(ex) * (d.w4a4 ? __ldcg(d.gsx + tok) : 1.f);
+            } else {
+                const int ex = hexp_of(__ldcg(d.hmax + p));
+                s_src[j][c] = reinterpret_cast<const uint4 *>(d.h_ws + (size_t)p * d.Imax);
+                s_scale[j][c] = pow2f(-ex);
+                s_un[j][c] = pow2f(ex) * (d.w4a4 ? __ldcg(d.gsh + p) : 1.f);
+            }
         }
     }
     __syncthreads();
@@ -754,14 +783,14 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
         stage_rows<kUT>(m, 0, (rs - 16) / 128, reg, rs, s_src[j], s_scale[j]);
     }
     __syncthreads();
-    MOE_TRACE_POINT(2, 2);
+    MOE_TRACE_POINT(1 + MODE, 2);
 
-    // Tickets of the tiles in the warp's pending list: after the warp's
-    // barrier every lane fences (ordering all of the warp's y stores before
-    // its tickets), then lane i takes the ticket of entry i; the warp
-    // combines the tiles it completed last among the slots.  Taken after
-    // the warp's last unit, not after each (a fence and an atomic round trip
-    // per unit would stall the ring), or when the list is full.
+    // Down: tickets of the tiles in the warp's pending list.  After the
+    // warp's barrier every lane fences (ordering all of the warp's y stores
+    // before its tickets), then lane i takes the ticket of entry i; the warp
+    // combines the tiles it completed last among the slots.  Taken after the
+    // warp's last unit, not after each (a fence and an atomic round trip per
+    // unit would stall the ring), or when the list is full.
     int nd = 0;
     auto tickets = [&]() {
         __syncwarp();
@@ -774,8 +803,8 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
             lm &= lm - 1;
             const int rr = s_dr[warp][i];
             // every slot's y of this tile is written: out rows 16rr .. 16rr + 15
-            if (lane < 4 * T) {
-                const int t = lane >> 2, m4 = 4 * rr + (lane & 3);
+            for (int it = lane; it < 4 * T; it += 32) {
+                const int t = it >> 2, m4 = 4 * rr + (it & 3);
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int j = 0; j < P; ++j) {
                     const float w = s_pw[t * P + j];
@@ -807,11 +836,11 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
         const int kc0 = kw * cpw;
         const uint8_t *xb = stage + s_off[sj] + (size_t)g * s_rs[sj] + q * 32;
         float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-        int lc = kUPD;     // next chunk to load (of this unit while < cpw, then of the next)
+        int lc = PD;       // next chunk to load (of this unit while < cpw, then of the next)
 #pragma unroll 1
-        for (int cc = 0; cc < cpw; cc += kUPD) {
+        for (int cc = 0; cc < cpw; cc += PD) {
 #pragma unroll
-            for (int i = 0; i < kUPD; ++i) {
+            for (int i = 0; i < PD; ++i) {
                 const uint8_t *bp = xb + b_offset(kc0 + cc + i, f8);
                 if (F8 && f8) {
                     chunk_mma_f8(cb[i], sb[i], lds128(bp), (i & 1) ? a1 : a0);
@@ -824,7 +853,7 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
                     mma_16816(a0, a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
                     mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
                 }
-                // refill this slot with the chunk kUPD ahead (possibly of the next unit)
+                // refill this slot with the chunk PD ahead (possibly of the next unit)
                 if (lc < cpw) load_chunk(base, lc, lane, cb[i], sb[i], pol);
                 else if (nxt < nu) load_chunk(nbase, lc - cpw, lane, cb[i], sb[i], pol);
                 ++lc;
@@ -850,22 +879,47 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
         }
         const int n2 = ks > 1 ? s_q[gj][it & 1] : __shfl_sync(0xffffffffu, grab, 0);
         if (kw == 0) {
-            // y = gs * 2^hexp * acc for the slot's pairs (columns), rows 16r + g, + 8
             const int e = s_e[sj], m = s_m[sj], p0 = s_p0[sj];
-            const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
+            if (MODE == 0) {
+                // SwiGLU: tile rows 0..7 gate, 8..15 up of intermediate row
+                // 8r + g; columns are the slot's pairs
+                const float gsa = e < 0 ? d.sgs13[2 * (-e - 1)] : d.gs13[2 * e];
+                const float gsb = e < 0 ? d.sgs13[2 * (-e - 1) + 1] : d.gs13[2 * e + 1];
+                const int n = 8 * r + g;
 #pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-                const int col = 2 * q + e2;
-                if (col < m) {
-                    const float sc = s_un[sj][col] * gs;
-                    float *yp = d.y_ws + (size_t)(p0 + col) * H + 16 * r + g;
-                    yp[0] = a0[e2] * sc;
-                    yp[8] = a0[2 + e2] * sc;
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int col = 2 * q + e2;
+                    const bool on = col < m;
+                    float habs = 0.f;
+                    if (on) {
+                        const float sc = s_un[sj][col];
+                        const float gt = a0[e2] * gsa * sc;
+                        const float up = a0[2 + e2] * gsb * sc;
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                        d.h_ws[(size_t)(p0 + col) * d.Imax + n] = hb;
+                        habs = fabsf(__bfloat162float(hb));
+                    }
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) habs = fmaxf(habs, __shfl_xor_sync(0xffffffffu, habs, off));
+                    if (on && g == 0) atomicMax(d.hmax + p0 + col, __float_as_uint(habs));
                 }
+            } else {
+                // y = gs * 2^hexp * acc for the slot's pairs (columns), rows 16r + g, + 8
+                const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int col = 2 * q + e2;
+                    if (col < m) {
+                        const float sc = s_un[sj][col] * gs;
+                        float *yp = d.y_ws + (size_t)(p0 + col) * H + 16 * r + g;
+                        yp[0] = a0[e2] * sc;
+                        yp[8] = a0[2 + e2] * sc;
+                    }
+                }
+                if (lane == 0) s_dr[warp][nd] = (short)r;
+                ++nd;
+                if (nd == kUMax) tickets();
             }
-            if (lane == 0) s_dr[warp][nd] = (short)r;
-            ++nd;
-            if (nd == kUMax) tickets();
         }
         cur = nxt;
         sj = nsj;
@@ -875,50 +929,96 @@ __global__ void __launch_bounds__(kUT, 1) gemv_down_wave_kernel(DevLayer d, int 
         f8 = nf8;
         nxt = n2;
     }
-    if (kw == 0 && nd > 0) tickets();
-    MOE_TRACE_POINT(2, 3);
+    if (MODE == 1 && kw == 0 && nd > 0) tickets();
+    MOE_TRACE_POINT(1 + MODE, 3);
 }
 
-// The K split of the down wave kernel (as wave_lks), or -1: at most 8
-// tokens, one chunk format, and a block's unit range must span at most
-// kDMaxSlots slots whose staged h rows fit its shared memory.
-int down_wave_lks(const DevLayer &d, int T, int sm_count, size_t optin) {
-    if (T > 8) return -1;
-    const int slots = std::min(d.E, T * d.k) + d.S;
-    const long U = (long)slots * (d.H / 16);
-    const long perb = (U + sm_count - 1) / sm_count;
-    const long span = perb / (d.H / 16) + 2;
-    if (span > kDMaxSlots) return -1;
-    const int NC64 = (d.S > 0 ? std::max(d.I, d.Is) : d.I) / kChunkK;
-    const size_t smem = (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * (NC64 * 128 + 16);
-    if (smem + 16 * 1024 > optin) return -1;
-    int best = -1;
-    long bestc = 0;
-    for (int l = 0; l <= 2; ++l) {
-        const long per = (perb + (kUW >> l) - 1) / (kUW >> l);
-        bool fits = true;
-        for (int f = 0; f < 2 && fits; ++f) {
-            if (f == 1 && d.S == 0) break;
-            const int nc = f == 0 ? chunks_of(d.I, d.f8e) : chunks_of(d.Is, d.f8s);
-            fits = nc % (1 << l) == 0 && (nc >> l) % kUPD == 0;
-        }
-        if (!fits) continue;
-        const long cost = per * ((chunks_of(d.I, d.f8e) >> l) + (l > 0 ? 2 : 0));
-        if (best < 0 || cost < bestc) {
-            best = l;
-            bestc = cost;
-        }
+// The slot wave kernel's geometry, or lks = -1 where it does not apply:
+// down (MODE 1) at up to 8 tokens over every slot; above 8 tokens (cold =
+// 1), gate/up and down over the routed slots below grouped_min_tokens, when
+// that threshold is at most 8 (their B rows fit the 8 staged rows).  A
+// block's range must span at most kDMaxSlots slots whose staged rows fit
+// its shared memory, and a unit's chunks must be whole turns of an 8- or
+// 6-deep ring; among the K splits 2^l <= 4, the fewest (chunks + a
+// reduction) per group at an even share of the units.
+struct SlotWave {
+    int lks = -1, pd = 0, cold = 0;
+    size_t smem = 0;
+};
+
+SlotWave slot_wave(const DevLayer &d, int MODE, int T, int sm_count, size_t optin) {
+    SlotWave w;
+    if (T > 8) {
+        if (!(d.grouped_min > 0 && d.grouped_min <= 8)) return w;
+        w.cold = 1;
+    } else if (MODE == 0) {
+        return w;
     }
-    return best;
+    const int slots = std::min(d.E, T * d.k) + (w.cold ? 0 : d.S);
+    const int NT = MODE == 0 ? d.I / 8 : d.H / 16;
+    const long U = (long)slots * NT;
+    const long perb = (U + sm_count - 1) / sm_count;
+    const long span = perb / NT + 2;
+    if (span > kDMaxSlots) return w;
+    const int rowb = MODE == 0 ? (d.H / kChunkK) * 128 + 16
+                               : ((!w.cold && d.S > 0 ? std::max(d.I, d.Is) : d.I) / kChunkK) * 128 + 16;
+    const size_t smem = (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * rowb;
+    if (smem + 16 * 1024 > optin) return w;
+    // chunk counts per tile of the formats present
+    int nc[2] = {MODE == 0 ? chunks_of(d.H, d.f8e) : chunks_of(d.I, d.f8e), 0};
+    const bool two = !w.cold && d.S > 0;
+    if (two) nc[1] = MODE == 0 ? chunks_of(d.H, d.f8s) : chunks_of(d.Is, d.f8s);
+    long bestc = 0;
+    for (int pd = 8; pd >= 6; pd -= 2) {
+        for (int l = 0; l <= 2; ++l) {
+            bool fits = true;
+            for (int f = 0; f < (two ? 2 : 1) && fits; ++f)
+                fits = nc[f] % (1 << l) == 0 && (nc[f] >> l) % pd == 0;
+            if (!fits) continue;
+            const long per = (perb + (kUW >> l) - 1) / (kUW >> l);
+            const long cost = per * ((nc[0] >> l) + (l > 0 ? 2 : 0));
+            if (w.lks < 0 || cost < bestc) {
+                w.lks = l;
+                w.pd = pd;
+                bestc = cost;
+            }
+        }
+        if (w.lks >= 0) break;   // the deeper ring where it fits
+    }
+    w.smem = smem;
+    return w;
 }
 
-size_t down_wave_smem(const DevLayer &d, int T, int sm_count) {
-    const int slots = std::min(d.E, T * d.k) + d.S;
-    const long U = (long)slots * (d.H / 16);
-    const long perb = (U + sm_count - 1) / sm_count;
-    const long span = perb / (d.H / 16) + 2;
-    const int NC64 = (d.S > 0 ? std::max(d.I, d.Is) : d.I) / kChunkK;
-    return (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * (NC64 * 128 + 16);
+template <int MODE, bool F8, int PD>
+cudaError_t launch_slot_wave(const DevLayer &d, const __nv_bfloat16 *x, int T, const SlotWave &w,
+                             __nv_bfloat16 *out, int sm_count, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sm_count);
+    cfg.blockDim = dim3(kUT);
+    cfg.dynamicSmemBytes = w.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_slot_wave_kernel<MODE, F8, PD>, d, x, T, w.lks, w.cold, out);
+}
+
+template <int MODE>
+cudaError_t launch_slot_wave_any(const DevLayer &d, const __nv_bfloat16 *x, int T, const SlotWave &w,
+                                 __nv_bfloat16 *out, int sm_count, cudaStream_t s) {
+    const bool f8 = d.f8e || d.f8s;
+    if (w.pd == 8)
+        return f8 ? launch_slot_wave<MODE, true, 8>(d, x, T, w, out, sm_count, s)
+                  : launch_slot_wave<MODE, false, 8>(d, x, T, w, out, sm_count, s);
+    return f8 ? launch_slot_wave<MODE, true, 6>(d, x, T, w, out, sm_count, s)
+              : launch_slot_wave<MODE, false, 6>(d, x, T, w, out, sm_count, s);
+}
+
+template <int MODE, bool F8, int PD>
+cudaError_t allow_slot_wave(int optin) {
+    return allow_max_dynamic_smem(gemv_slot_wave_kernel<MODE, F8, PD>, optin);
 }
 
 // The K split of the wave kernel: among 2^l <= 4 whose chunks per unit are a
@@ -1022,8 +1122,14 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = allow_smem<0, 8, 4>(optin);
     if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<false>, optin);
     if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<true>, optin);
-    if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_down_wave_kernel<false>, optin);
-    if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_down_wave_kernel<true>, optin);
+    if (e == cudaSuccess) e = allow_slot_wave<0, false, 8>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<0, true, 8>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<0, false, 6>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<0, true, 6>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, false, 8>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, true, 8>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, false, 6>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, true, 6>(optin);
     if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
     if (e == cudaSuccess) e = prepare_route_kernel(optin);
     if (e == cudaSuccess) e = prepare_fused_kernel(optin);
@@ -1050,27 +1156,20 @@ cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int
         return (d.f8e || d.f8s) ? cudaLaunchKernelEx(&cfg, gemv_up_wave_kernel<true>, d, x, T, lks)
                                 : cudaLaunchKernelEx(&cfg, gemv_up_wave_kernel<false>, d, x, T, lks);
     }
+    const SlotWave w = slot_wave(d, 0, T, sms, (size_t)optin_smem);
+    if (w.lks >= 0) return launch_slot_wave_any<0>(d, x, T, w, nullptr, sms, s);
     return launch_stage<0>(d, x, T, nullptr, s);
 }
 
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, int optin_smem,
                         cudaStream_t s) {
-    const int lks = down_wave_lks(d, T, sm_count, (size_t)optin_smem);
-    if (lks >= 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(sm_count);
-        cfg.blockDim = dim3(kUT);
-        cfg.dynamicSmemBytes = down_wave_smem(d, T, sm_count);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return (d.f8e || d.f8s) ? cudaLaunchKernelEx(&cfg, gemv_down_wave_kernel<true>, d, T, lks, out)
-                                : cudaLaunchKernelEx(&cfg, gemv_down_wave_kernel<false>, d, T, lks, out);
-    }
+    const SlotWave w = slot_wave(d, 1, T, sm_count, (size_t)optin_smem);
+    if (w.lks >= 0) return launch_slot_wave_any<1>(d, nullptr, T, w, out, sm_count, s);
     return launch_stage<1>(d, nullptr, T, out, s);
+}
+
+bool down_tile_tickets(const DevLayer &d, int T, int sm_count, int optin_smem) {
+    return slot_wave(d, 1, T, sm_count, (size_t)optin_smem).lks >= 0;
 }
 
 }  // namespace moe

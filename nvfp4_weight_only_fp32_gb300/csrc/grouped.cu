@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
     __shared__ uint32_t s_taddr;
     __shared__ int s_abort;
     __shared__ int s_last;
+    __shared__ int s_t16[kMT / 16];   // down: the 16-row tiles this item completed last
     // this block's items: first byte of tile 8mt (warp w adds w tiles), K
     // chunks, tokens, first pair, expert (< 0: shared), M-tile
     __shared__ const uint8_t *s_it_base[kMaxItems];
@@ -732,9 +733,9 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     }
                 }
             }
-            if (MODE == 1) {
-                // ticket shared with the GEMV down kernel: ns arrivals per
-                // 128-row group; the last one combines those rows
+            if (MODE == 1 && !d.tick16) {
+                // ticket shared with the per-slot GEMV down kernel: ns
+                // arrivals per 128-row group; the last one combines those rows
                 asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
                 if (threadIdx.x == 0) {
                     __threadfence();
@@ -748,6 +749,30 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                     if (threadIdx.x == 0) d.down_cnt[mt] = 0u;
                 }
                 asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+            } else if (MODE == 1) {
+                // tickets shared with the wave down kernel: ns arrivals per
+                // 16-row tile; the last one combines that tile's rows
+                asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+                if (threadIdx.x < kMT / 16) {
+                    __threadfence();
+                    const bool last = !*abort && atomicAdd(d.down_cnt + (kMT / 16) * mt + threadIdx.x, 1u) ==
+                                                     (unsigned)(ns - 1);
+                    s_t16[threadIdx.x] = last;
+                }
+                asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+                unsigned lm = 0u;
+#pragma unroll
+                for (int t16 = 0; t16 < kMT / 16; ++t16) lm |= (s_t16[t16] ? 1u : 0u) << t16;
+                asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+                if (lm) __threadfence();
+                while (lm) {
+                    const int t16 = __ffs(lm) - 1;
+                    lm &= lm - 1;
+                    combine_rows(d, T, out, kMT * mt + 16 * t16, 16, s_pair, s_pw, threadIdx.x, 32 * kDecW,
+                                 [] { asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory"); });
+                    asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
+                    if (threadIdx.x == 0) d.down_cnt[(kMT / 16) * mt + t16] = 0u;
+                }
             }
         }
     }

@@ -115,6 +115,10 @@ struct DevLayer {
     int debug_stall;                // single launch: added to the tag its logit wait expects (test hook)
     int *nhot;                      // [1] number of such slots
     int *hot_slots;                 // [max_slots] their slot indices, ascending
+    int tick16;                     // grouped down kernel: combine tickets per 16-row tile (beside the
+                                    //   wave down kernel) instead of per 128-row group; set per launch
+    int *ncold;                     // [1] routed slots below grouped_min_tokens (steps of > 8 tokens)
+    int *cold_slots;                // [max_slots] their slot indices, ascending
     unsigned *tg_ticket;            // [max_tokens] router: arrivals per token group
     unsigned long long *emask;      // [E] router: tokens that selected each expert (bit t)
     unsigned *wave_ctr;             // [2] chain gate/up wave kernel: next unit to hand out (reset by the router)
@@ -145,6 +149,7 @@ cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int
                            cudaStream_t s);
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, int optin_smem,
                         cudaStream_t s);
+bool down_tile_tickets(const DevLayer &d, int T, int sm_count, int optin_smem);
 bool grouped_supported(const DevLayer &d, int sm_count);
 cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s);
 cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, cudaStream_t s);

@@ -450,15 +450,23 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         // grouped tensor-core kernels; the GEMV kernels skip them
         int ns = S;
         for (int w = 0; w < kRouteWarps; ++w) ns += s_wsum_f[w];
-        int nh = 0;
+        // (and the routed ones below it, which the GEMV kernels take)
+        int nh = 0, nc = 0;
         for (int b = 0; b < ns; b += 32) {
             const int sl = b + lane;
             const bool hot = d.grouped_min > 0 && sl < ns && s_slotm[sl] >= d.grouped_min;
+            const bool cold = sl >= S && sl < ns && !hot;
             const unsigned bal = __ballot_sync(0xffffffffu, hot);
+            const unsigned bcl = __ballot_sync(0xffffffffu, cold);
             if (hot) d.hot_slots[nh + __popc(bal & ((1u << lane) - 1u))] = sl;
+            if (cold) d.cold_slots[nc + __popc(bcl & ((1u << lane) - 1u))] = sl;
             nh += __popc(bal);
+            nc += __popc(bcl);
         }
-        if (lane == 0) *d.nhot = nh;
+        if (lane == 0) {
+            *d.nhot = nh;
+            *d.ncold = nc;
+        }
     }
 
     // Pairs: an expert's tokens are numbered in ascending token order.
