@@ -460,6 +460,8 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, void *stream, m
     // the grouped tensor-core kernels decode NVFP4 chunks only
     if (L->cfg.grouped_min_tokens > 0 && !d.f8e && !d.f8s && grouped_supported(d, L->sm_count))
         d.grouped_min = L->cfg.grouped_min_tokens;
+    d.nsm = L->sm_count;
+    d.tau_max = cold_threshold_max(d, L->sm_count, L->optin_smem);
     for (int T = 0; T <= kMaxTokens; ++T) {
         L->fused_ok[T] = 0;
         if (e == cudaSuccess && cfg->fused >= 0 && !cfg->w4a4 && T >= 1 && T <= cfg->max_tokens &&

@@ -642,13 +642,14 @@ __global__ void __launch_bounds__(kUT, 1) gemv_up_wave_kernel(DevLayer d, const 
 // ---------------------------------------------------------------------------
 constexpr int kDMaxSlots = 12;          // slots one block's units may span
 
-template <int MODE, bool F8, int PD>
+template <int MODE, bool F8, int PD, int NG>
 __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, const __nv_bfloat16 *__restrict__ x,
                                                                 int T, int lks, int cold,
                                                                 __nv_bfloat16 *__restrict__ out) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ const uint4 *s_src[kDMaxSlots][8];
-    __shared__ float s_scale[kDMaxSlots][8], s_un[kDMaxSlots][8];
+    constexpr int RB = 8 * NG;                     // staged B rows per slot
+    __shared__ const uint4 *s_src[kDMaxSlots][RB];
+    __shared__ float s_scale[kDMaxSlots][RB], s_un[kDMaxSlots][RB];
     __shared__ int s_off[kDMaxSlots], s_rs[kDMaxSlots], s_m[kDMaxSlots], s_p0[kDMaxSlots], s_e[kDMaxSlots];
     __shared__ const uint8_t *s_wb[kDMaxSlots];
     __shared__ int s_pair[MODE == 1 ? kMaxTokens * (kMaxTopK + kMaxShared) : 1];
@@ -687,7 +688,7 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
     const int nu = ub1 - ub0;
     const int ci_lo = ub0 / NT, nsb = nu > 0 ? (ub1 - 1) / NT - ci_lo + 1 : 0;
     if (threadIdx.x == 0) s_ctr = 0;
-    // the staged slots' geometry (8 rows each, rows >= m zero) and weights,
+    // the staged slots' geometry (RB rows each, rows >= m zero) and weights,
     // and the combine's pair table
     if (threadIdx.x < nsb) {
         const int ci = ci_lo + threadIdx.x;
@@ -724,7 +725,7 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
         int off = 0;
         for (int j = 0; j < nsb; ++j) {
             s_off[j] = off;
-            off += 8 * s_rs[j];
+            off += RB * s_rs[j];
         }
     }
     __syncthreads();
@@ -756,8 +757,8 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
         pdl_trigger();
     }
     MOE_TRACE_POINT(1 + MODE, 1);
-    if (threadIdx.x < 8 * nsb) {
-        const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
+    if (threadIdx.x < RB * nsb) {
+        const int j = threadIdx.x / RB, c = threadIdx.x % RB;
         if (c < s_m[j]) {
             const int p = s_p0[j] + c;
             if (MODE == 0) {
@@ -778,7 +779,7 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
     for (int j = 0; j < nsb; ++j) {
         const int m = s_m[j], rs = s_rs[j];
         uint8_t *reg = stage + s_off[j];
-        for (int i = threadIdx.x; i < (8 - m) * (rs / 16); i += kUT)
+        for (int i = threadIdx.x; i < (RB - m) * (rs / 16); i += kUT)
             reinterpret_cast<uint4 *>(reg + (size_t)m * rs)[i] = make_uint4(0u, 0u, 0u, 0u);
         stage_rows<kUT>(m, 0, (rs - 16) / 128, reg, rs, s_src[j], s_scale[j]);
     }
@@ -835,7 +836,9 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
         if (leader && nxt < nu) grab = atomicAdd(&s_ctr, 1);
         const int kc0 = kw * cpw;
         const uint8_t *xb = stage + s_off[sj] + (size_t)g * s_rs[sj] + q * 32;
-        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+        const size_t gstr = (size_t)8 * s_rs[sj];   // the second token group's B rows
+        const bool two = NG > 1 && s_m[sj] > 8;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
         int lc = PD;       // next chunk to load (of this unit while < cpw, then of the next)
 #pragma unroll 1
         for (int cc = 0; cc < cpw; cc += PD) {
@@ -852,6 +855,13 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
                     mma_16816(a1, a[1][0], a[1][1], a[1][2], a[1][3], b01.z, b01.w);
                     mma_16816(a0, a[2][0], a[2][1], a[2][2], a[2][3], b23.x, b23.y);
                     mma_16816(a1, a[3][0], a[3][1], a[3][2], a[3][3], b23.z, b23.w);
+                    if (NG > 1 && two) {
+                        const uint4 c01 = lds128(bp + gstr), c23 = lds128(bp + gstr + 16);
+                        mma_16816(c1, a[0][0], a[0][1], a[0][2], a[0][3], c01.x, c01.y);
+                        mma_16816(c1, a[1][0], a[1][1], a[1][2], a[1][3], c01.z, c01.w);
+                        mma_16816(c1, a[2][0], a[2][1], a[2][2], a[2][3], c23.x, c23.y);
+                        mma_16816(c1, a[3][0], a[3][1], a[3][2], a[3][3], c23.z, c23.w);
+                    }
                 }
                 // refill this slot with the chunk PD ahead (possibly of the next unit)
                 if (lc < cpw) load_chunk(base, lc, lane, cb[i], sb[i], pol);
@@ -864,18 +874,22 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
         if (leader && ks > 1) s_q[gj][it & 1] = grab;
         if (ks > 1) {
             // fixed-order K reduction within the group (named barrier 1 + group)
-            if (kw > 0) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) red[(warp * 4 + v) * 32 + lane] = a0[v];
-            }
-            gsync();
-            if (kw == 0) {
+            for (int gg = 0; gg < NG; ++gg) {
+                float *av = gg == 0 ? a0 : c1;
+                if (kw > 0) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) red[(warp * 4 + v) * 32 + lane] = av[v];
+                }
+                gsync();
+                if (kw == 0) {
 #pragma unroll 1
-                for (int w = 1; w < ks; ++w)
+                    for (int w = 1; w < ks; ++w)
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) a0[v] += red[((warp + w) * 4 + v) * 32 + lane];
+                        for (int v = 0; v < 4; ++v) av[v] += red[((warp + w) * 4 + v) * 32 + lane];
+                }
+                gsync();
             }
-            gsync();
         }
         const int n2 = ks > 1 ? s_q[gj][it & 1] : __shfl_sync(0xffffffffu, grab, 0);
         if (kw == 0) {
@@ -887,14 +901,16 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
                 const float gsb = e < 0 ? d.sgs13[2 * (-e - 1) + 1] : d.gs13[2 * e + 1];
                 const int n = 8 * r + g;
 #pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int col = 2 * q + e2;
+                for (int e4 = 0; e4 < 2 * NG; ++e4) {
+                    const int e2 = e4 & 1, gg = e4 >> 1;
+                    const float *av = gg == 0 ? a0 : c1;
+                    const int col = 8 * gg + 2 * q + e2;
                     const bool on = col < m;
                     float habs = 0.f;
                     if (on) {
                         const float sc = s_un[sj][col];
-                        const float gt = a0[e2] * gsa * sc;
-                        const float up = a0[2 + e2] * gsb * sc;
+                        const float gt = av[e2] * gsa * sc;
+                        const float up = av[2 + e2] * gsb * sc;
                         const __nv_bfloat16 hb = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
                         d.h_ws[(size_t)(p0 + col) * d.Imax + n] = hb;
                         habs = fabsf(__bfloat162float(hb));
@@ -907,13 +923,15 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
                 // y = gs * 2^hexp * acc for the slot's pairs (columns), rows 16r + g, + 8
                 const float gs = e < 0 ? d.sgs2[-e - 1] : d.gs2[e];
 #pragma unroll
-                for (int e2 = 0; e2 < 2; ++e2) {
-                    const int col = 2 * q + e2;
+                for (int e4 = 0; e4 < 2 * NG; ++e4) {
+                    const int e2 = e4 & 1, gg = e4 >> 1;
+                    const float *av = gg == 0 ? a0 : c1;
+                    const int col = 8 * gg + 2 * q + e2;
                     if (col < m) {
                         const float sc = s_un[sj][col] * gs;
                         float *yp = d.y_ws + (size_t)(p0 + col) * H + 16 * r + g;
-                        yp[0] = a0[e2] * sc;
-                        yp[8] = a0[2 + e2] * sc;
+                        yp[0] = av[e2] * sc;
+                        yp[8] = av[2 + e2] * sc;
                     }
                 }
                 if (lane == 0) s_dr[warp][nd] = (short)r;
@@ -942,15 +960,17 @@ __global__ void __launch_bounds__(kUT, 1) gemv_slot_wave_kernel(DevLayer d, cons
 // 6-deep ring; among the K splits 2^l <= 4, the fewest (chunks + a
 // reduction) per group at an even share of the units.
 struct SlotWave {
-    int lks = -1, pd = 0, cold = 0;
+    int lks = -1, pd = 0, cold = 0, ng = 1;
     size_t smem = 0;
 };
 
 SlotWave slot_wave(const DevLayer &d, int MODE, int T, int sm_count, size_t optin) {
     SlotWave w;
     if (T > 8) {
-        if (!(d.grouped_min > 0 && d.grouped_min <= 8)) return w;
+        // the cold slots hold fewer than 16 tokens: two groups of 8 B rows
+        if (!(d.grouped_min > 0 && d.grouped_min <= 16) || d.f8e || d.f8s) return w;
         w.cold = 1;
+        w.ng = 2;
     } else if (MODE == 0) {
         return w;
     }
@@ -962,7 +982,7 @@ SlotWave slot_wave(const DevLayer &d, int MODE, int T, int sm_count, size_t opti
     if (span > kDMaxSlots) return w;
     const int rowb = MODE == 0 ? (d.H / kChunkK) * 128 + 16
                                : ((!w.cold && d.S > 0 ? std::max(d.I, d.Is) : d.I) / kChunkK) * 128 + 16;
-    const size_t smem = (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * rowb;
+    const size_t smem = (size_t)kUW * 4 * 32 * sizeof(float) + (size_t)span * 8 * w.ng * rowb;
     if (smem + 16 * 1024 > optin) return w;
     // chunk counts per tile of the formats present
     int nc[2] = {MODE == 0 ? chunks_of(d.H, d.f8e) : chunks_of(d.I, d.f8e), 0};
@@ -989,7 +1009,7 @@ SlotWave slot_wave(const DevLayer &d, int MODE, int T, int sm_count, size_t opti
     return w;
 }
 
-template <int MODE, bool F8, int PD>
+template <int MODE, bool F8, int PD, int NG>
 cudaError_t launch_slot_wave(const DevLayer &d, const __nv_bfloat16 *x, int T, const SlotWave &w,
                              __nv_bfloat16 *out, int sm_count, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -1002,23 +1022,32 @@ cudaError_t launch_slot_wave(const DevLayer &d, const __nv_bfloat16 *x, int T, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_slot_wave_kernel<MODE, F8, PD>, d, x, T, w.lks, w.cold, out);
+    return cudaLaunchKernelEx(&cfg, gemv_slot_wave_kernel<MODE, F8, PD, NG>, d, x, T, w.lks, w.cold, out);
 }
 
-template <int MODE>
-cudaError_t launch_slot_wave_any(const DevLayer &d, const __nv_bfloat16 *x, int T, const SlotWave &w,
+// (instances: down at up to 8 tokens in both chunk families, one token
+// group; the cold slots above 8 tokens NVFP4 only -- the grouped kernels,
+// hence the cold slots, exist only for NVFP4 layers -- two token groups)
+cudaError_t launch_slot_wave_any(int MODE, const DevLayer &d, const __nv_bfloat16 *x, int T, const SlotWave &w,
                                  __nv_bfloat16 *out, int sm_count, cudaStream_t s) {
     const bool f8 = d.f8e || d.f8s;
+    if (w.ng == 2) {
+        if (MODE == 0)
+            return w.pd == 8 ? launch_slot_wave<0, false, 8, 2>(d, x, T, w, out, sm_count, s)
+                             : launch_slot_wave<0, false, 6, 2>(d, x, T, w, out, sm_count, s);
+        return w.pd == 8 ? launch_slot_wave<1, false, 8, 2>(d, x, T, w, out, sm_count, s)
+                         : launch_slot_wave<1, false, 6, 2>(d, x, T, w, out, sm_count, s);
+    }
     if (w.pd == 8)
-        return f8 ? launch_slot_wave<MODE, true, 8>(d, x, T, w, out, sm_count, s)
-                  : launch_slot_wave<MODE, false, 8>(d, x, T, w, out, sm_count, s);
-    return f8 ? launch_slot_wave<MODE, true, 6>(d, x, T, w, out, sm_count, s)
-              : launch_slot_wave<MODE, false, 6>(d, x, T, w, out, sm_count, s);
+        return f8 ? launch_slot_wave<1, true, 8, 1>(d, x, T, w, out, sm_count, s)
+                  : launch_slot_wave<1, false, 8, 1>(d, x, T, w, out, sm_count, s);
+    return f8 ? launch_slot_wave<1, true, 6, 1>(d, x, T, w, out, sm_count, s)
+              : launch_slot_wave<1, false, 6, 1>(d, x, T, w, out, sm_count, s);
 }
 
-template <int MODE, bool F8, int PD>
+template <int MODE, bool F8, int PD, int NG>
 cudaError_t allow_slot_wave(int optin) {
-    return allow_max_dynamic_smem(gemv_slot_wave_kernel<MODE, F8, PD>, optin);
+    return allow_max_dynamic_smem(gemv_slot_wave_kernel<MODE, F8, PD, NG>, optin);
 }
 
 // The K split of the wave kernel: among 2^l <= 4 whose chunks per unit are a
@@ -1122,14 +1151,14 @@ cudaError_t prepare_kernels() {
     if (e == cudaSuccess) e = allow_smem<0, 8, 4>(optin);
     if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<false>, optin);
     if (e == cudaSuccess) e = allow_max_dynamic_smem(gemv_up_wave_kernel<true>, optin);
-    if (e == cudaSuccess) e = allow_slot_wave<0, false, 8>(optin);
-    if (e == cudaSuccess) e = allow_slot_wave<0, true, 8>(optin);
-    if (e == cudaSuccess) e = allow_slot_wave<0, false, 6>(optin);
-    if (e == cudaSuccess) e = allow_slot_wave<0, true, 6>(optin);
-    if (e == cudaSuccess) e = allow_slot_wave<1, false, 8>(optin);
-    if (e == cudaSuccess) e = allow_slot_wave<1, true, 8>(optin);
-    if (e == cudaSuccess) e = allow_slot_wave<1, false, 6>(optin);
-    if (e == cudaSuccess) e = allow_slot_wave<1, true, 6>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<0, false, 8, 2>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<0, false, 6, 2>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, false, 8, 2>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, false, 6, 2>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, false, 8, 1>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, true, 8, 1>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, false, 6, 1>(optin);
+    if (e == cudaSuccess) e = allow_slot_wave<1, true, 6, 1>(optin);
     if (e == cudaSuccess) e = allow_smem<1, 8, 4>(optin);
     if (e == cudaSuccess) e = prepare_route_kernel(optin);
     if (e == cudaSuccess) e = prepare_fused_kernel(optin);
@@ -1157,19 +1186,30 @@ cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int
                                 : cudaLaunchKernelEx(&cfg, gemv_up_wave_kernel<false>, d, x, T, lks);
     }
     const SlotWave w = slot_wave(d, 0, T, sms, (size_t)optin_smem);
-    if (w.lks >= 0) return launch_slot_wave_any<0>(d, x, T, w, nullptr, sms, s);
+    if (w.lks >= 0) return launch_slot_wave_any(0, d, x, T, w, nullptr, sms, s);
     return launch_stage<0>(d, x, T, nullptr, s);
 }
 
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, int optin_smem,
                         cudaStream_t s) {
     const SlotWave w = slot_wave(d, 1, T, sm_count, (size_t)optin_smem);
-    if (w.lks >= 0) return launch_slot_wave_any<1>(d, nullptr, T, w, out, sm_count, s);
+    if (w.lks >= 0) return launch_slot_wave_any(1, d, nullptr, T, w, out, sm_count, s);
     return launch_stage<1>(d, nullptr, T, out, s);
 }
 
 bool down_tile_tickets(const DevLayer &d, int T, int sm_count, int optin_smem) {
     return slot_wave(d, 1, T, sm_count, (size_t)optin_smem).lks >= 0;
+}
+
+// Above 8 tokens both wave kernels take cold slots of up to 15 tokens (at
+// max_tokens, hence at every smaller step): the router may then raise the
+// grouped threshold up to 16 so that the grouped kernels' items fit one per
+// block.  Otherwise the threshold stays grouped_min_tokens.
+int cold_threshold_max(const DevLayer &d, int sm_count, int optin_smem) {
+    if (d.max_tokens <= 8 || d.grouped_min <= 0) return d.grouped_min;
+    const bool ok = slot_wave(d, 0, d.max_tokens, sm_count, (size_t)optin_smem).lks >= 0 &&
+                    slot_wave(d, 1, d.max_tokens, sm_count, (size_t)optin_smem).lks >= 0;
+    return ok ? std::max(d.grouped_min, 16) : d.grouped_min;
 }
 
 }  // namespace moe

@@ -766,12 +766,17 @@ __global__ void __launch_bounds__(kGT, 1) grouped_kernel(DevLayer d, const __nv_
                 asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
                 if (lm) __threadfence();
                 while (lm) {
-                    const int t16 = __ffs(lm) - 1;
-                    lm &= lm - 1;
-                    combine_rows(d, T, out, kMT * mt + 16 * t16, 16, s_pair, s_pw, threadIdx.x, 32 * kDecW,
+                    // one combine per run of consecutive tiles (usually all
+                    // eight: this kernel runs after the GEMV down kernel)
+                    const int t0 = __ffs(lm) - 1;
+                    int t1 = t0;
+                    while (t1 + 1 < kMT / 16 && ((lm >> (t1 + 1)) & 1u)) ++t1;
+                    lm &= ~(((2u << t1) - 1u) & ~((1u << t0) - 1u));
+                    combine_rows(d, T, out, kMT * mt + 16 * t0, 16 * (t1 - t0 + 1), s_pair, s_pw, threadIdx.x,
+                                 32 * kDecW,
                                  [] { asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory"); });
                     asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kDecW) : "memory");
-                    if (threadIdx.x == 0) d.down_cnt[(kMT / 16) * mt + t16] = 0u;
+                    if (threadIdx.x <= t1 - t0) d.down_cnt[(kMT / 16) * mt + t0 + threadIdx.x] = 0u;
                 }
             }
         }

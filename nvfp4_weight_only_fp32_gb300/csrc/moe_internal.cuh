@@ -117,7 +117,9 @@ struct DevLayer {
     int *hot_slots;                 // [max_slots] their slot indices, ascending
     int tick16;                     // grouped down kernel: combine tickets per 16-row tile (beside the
                                     //   wave down kernel) instead of per 128-row group; set per launch
-    int *ncold;                     // [1] routed slots below grouped_min_tokens (steps of > 8 tokens)
+    int nsm;                        // SMs (the grouped kernels' blocks)
+    int tau_max;                    // highest grouped threshold the router may raise to (>= grouped_min)
+    int *ncold;                     // [1] routed slots below the grouped threshold (steps of > 8 tokens)
     int *cold_slots;                // [max_slots] their slot indices, ascending
     unsigned *tg_ticket;            // [max_tokens] router: arrivals per token group
     unsigned long long *emask;      // [E] router: tokens that selected each expert (bit t)
@@ -150,6 +152,7 @@ cudaError_t launch_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int
 cudaError_t launch_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, int optin_smem,
                         cudaStream_t s);
 bool down_tile_tickets(const DevLayer &d, int T, int sm_count, int optin_smem);
+int cold_threshold_max(const DevLayer &d, int sm_count, int optin_smem);
 bool grouped_supported(const DevLayer &d, int sm_count);
 cudaError_t launch_grouped_gate_up(const DevLayer &d, const __nv_bfloat16 *x, int T, int sm_count, cudaStream_t s);
 cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, int sm_count, cudaStream_t s);

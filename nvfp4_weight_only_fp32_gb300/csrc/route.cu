@@ -450,11 +450,40 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         // grouped tensor-core kernels; the GEMV kernels skip them
         int ns = S;
         for (int w = 0; w < kRouteWarps; ++w) ns += s_wsum_f[w];
-        // (and the routed ones below it, which the GEMV kernels take)
+        // (and the routed ones below it, which the GEMV kernels take).  Where
+        // the GEMV kernels take slots of up to 15 tokens, a routed slot's
+        // threshold is raised from grouped_min (up to 16) until the grouped
+        // kernels' items fit one per block: their time is that of the block
+        // with the most items, the GEMV kernels' units are handed out on demand.
+        int tau = d.grouped_min;
+        if (T > 8 && d.tau_max > d.grouped_min) {
+            // routed slots by token count (counts of 16 and more together)
+            __shared__ int s_hist[17];
+            if (lane < 17) s_hist[lane] = 0;
+            __syncwarp();
+            for (int sl = S + lane; sl < ns; sl += 32) {
+                const int m = s_slotm[sl];
+                if (m >= d.grouped_min) atomicAdd(&s_hist[min(m, 16)], 1);
+            }
+            __syncwarp();
+            int shot = 0;   // shared slots stay hot at grouped_min
+            for (int j = 0; j < S; ++j) shot += s_slotm[j] >= d.grouped_min;
+            int cnt = 0;    // routed slots with at least cand tokens
+            for (int b = 16; b >= d.tau_max; --b) cnt += s_hist[b];
+            // from the top: the smallest threshold whose items still fit
+            tau = d.tau_max;
+            for (int cand = d.tau_max; cand >= d.grouped_min; --cand) {
+                const long up = (long)cnt * (d.I / 64) + (long)shot * (d.Is / 64);
+                const long dn = (long)(cnt + shot) * (d.H / 128);
+                if (up > d.nsm || dn > d.nsm) break;
+                tau = cand;
+                if (cand > d.grouped_min) cnt += s_hist[cand - 1];
+            }
+        }
         int nh = 0, nc = 0;
         for (int b = 0; b < ns; b += 32) {
             const int sl = b + lane;
-            const bool hot = d.grouped_min > 0 && sl < ns && s_slotm[sl] >= d.grouped_min;
+            const bool hot = d.grouped_min > 0 && sl < ns && s_slotm[sl] >= (sl < S ? d.grouped_min : tau);
             const bool cold = sl >= S && sl < ns && !hot;
             const unsigned bal = __ballot_sync(0xffffffffu, hot);
             const unsigned bcl = __ballot_sync(0xffffffffu, cold);
