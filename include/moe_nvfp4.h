@@ -115,7 +115,12 @@ typedef struct {
     float routed_scale;     /* multiplies every routed weight (1.0) */
     int grouped_min_tokens; /* experts with at least this many tokens use the
                                grouped tensor-core path when T > 8;
-                               0 = library default, < 0 = never */
+                               0 = library default (8), < 0 = never.  For a
+                               routed expert the library may raise the
+                               threshold per step, up to 16, so that the
+                               grouped kernels get at most one item per SM
+                               (the GEMV kernels take the rest); results do
+                               not depend on the split beyond FP32 rounding */
     int fused;              /* 0: moe_decode_forward runs the whole step as
                                one launch when the shape allows it (T <= 8,
                                H <= 8192, E <= 256 and <= 4 x SM count, the
