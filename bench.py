@@ -79,7 +79,7 @@ def parse():
                                         "inkling_w4a4,zipf64_w4a4,flint1-coop,flint8-coop",
                     help="further workloads timed and reported under 'workloads' ('' = none); "
                          "a '-gemv' suffix turns the grouped kernels off, '-coop' launches the single "
-                         "launch as a cooperative grid")
+                         "launch as a cooperative grid, '-chain' runs the three-kernel chain instead")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grouped-min", type=int, default=0,
@@ -531,11 +531,12 @@ def run_gpu(args):
             secondary = other(args.secondary)
         for name in [w for w in args.extras.split(",") if w and w != "none"]:
             # "-gemv": the grouped kernels off; "-coop": the single launch as a
-            # cooperative grid
-            base = name.rsplit("-", 1)[0] if name.endswith(("-gemv", "-coop")) else name
+            # cooperative grid; "-chain": the three-kernel chain, no single launch
+            base = name.rsplit("-", 1)[0] if name.endswith(("-gemv", "-coop", "-chain")) else name
             if name == base == args.workload:
                 continue
-            workloads[name] = other(base, -1 if name.endswith("-gemv") else 0, 1 if name.endswith("-coop") else 0)
+            fused = 1 if name.endswith("-coop") else (-1 if name.endswith("-chain") else 0)
+            workloads[name] = other(base, -1 if name.endswith("-gemv") else 0, fused)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
