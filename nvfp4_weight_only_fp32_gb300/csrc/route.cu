@@ -350,6 +350,13 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             }
         }
     }
+    // this token group's power-of-two prescales from their whole-row maxima
+    // (every block of the group has added its part before the ticket above)
+    if (threadIdx.x < nt) {
+        const int t = t0 + threadIdx.x;
+        d.xexp[t] = max(-100, exp_for_f16(__uint_as_float(__ldcg(d.xmaxb + t))));
+        d.xmaxb[t] = 0u;
+    }
     MOE_TRACE_POINT(0, 11);
     // ---- the last token group: slots, pairs, hot list ----
     __syncthreads();
@@ -379,11 +386,6 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
             s_ids[i / K][i % K] = __ldcg(d.ids + i);
             s_w[i / K][i % K] = __ldcg(d.wsel + i);
         }
-    }
-    // the tokens' power-of-two prescales from their whole-row maxima
-    for (int t = threadIdx.x; t < T; t += kThreads) {
-        d.xexp[t] = max(-100, exp_for_f16(__uint_as_float(__ldcg(d.xmaxb + t))));
-        d.xmaxb[t] = 0u;
     }
     __syncthreads();
     MOE_TRACE_POINT(0, 6);
