@@ -348,13 +348,14 @@ moe_status moe_route_topk_static(const float *router_w, const float *router_b,
  * `rows` rows of n BF16 values ("Inkling 2 Small on vLLM: Day-0 Support",
  * "Mixed-precision MoE and Four-Over-Six NVFP4"), as described at
  * moe_config.w4a4.
- *   x    BF16 [rows, n] device, read
- *   deq  BF16 [rows, n] device, written (may equal x): the dequantised values
+ *   x    BF16 [rows, n] device, 8-byte aligned, read
+ *   deq  BF16 [rows, n] device, 8-byte aligned, written (may equal x): the dequantised values
  *        without the global scale, e2m1 * e4m3 (exact in BF16)
  *   gs   FP32 [rows] device, written: the rows' global scales (value =
  *        deq * gs)
- * n must be a positive multiple of 16, rows >= 0.  Asynchronous on
- * `stream`; no handle is needed. */
+ * n must be a positive multiple of 16, rows >= 0; a NULL or misaligned
+ * pointer returns MOE_ERR_INVALID_ARG.  A row is split over a cluster of up
+ * to 8 CTAs.  Asynchronous on `stream`; no handle is needed. */
 moe_status moe_quant_fos(const void *x, int rows, int n, void *deq, float *gs, void *stream);
 
 /* Reasons for the last failure on this host thread ("" if none). */

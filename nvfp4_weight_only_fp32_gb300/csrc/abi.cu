@@ -702,6 +702,8 @@ moe_status moe_quant_fos(const void *x, int rows, int n, void *deq, float *gs, v
         return fail(MOE_ERR_INVALID_ARG, "rows must be >= 0 and n a positive multiple of 16");
     if (rows == 0) return MOE_OK;
     if (!x || !deq || !gs) return fail(MOE_ERR_INVALID_ARG, "x, deq or gs is NULL");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(deq)) % 8 != 0)
+        return fail(MOE_ERR_INVALID_ARG, "x and deq must be 8-byte aligned");
     cudaError_t e = launch_fos(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(deq), rows, n, n,
                                0, 0, gs, nullptr, nullptr, nullptr, nullptr, 0, 0,
                                reinterpret_cast<cudaStream_t>(stream));

@@ -116,3 +116,6 @@ def test_quantiser_arguments_checked_before_any_launch(moe):
     assert L.moe_quant_fos(None, 1, 32, None, None, None) == moe.moe.MOE_ERR_INVALID_ARG
     assert "NULL" in moe.last_error()
     assert L.moe_quant_fos(None, 0, 32, None, None, None) == moe.moe.MOE_OK    # nothing to do
+    # a pointer off the 8-byte grid is refused before anything touches it
+    assert L.moe_quant_fos(0x1004, 1, 32, 0x2000, 0x3000, None) == moe.moe.MOE_ERR_INVALID_ARG
+    assert "8-byte aligned" in moe.last_error()

@@ -73,7 +73,9 @@ def _rows(kind: str, n: int, rng: np.random.Generator) -> np.ndarray:
 KINDS = ["normal", "wide", "grid", "midpoints", "sparse", "huge", "tiny"]
 
 
-@pytest.mark.parametrize("n", [16, 48, 768, 2560, 7168])
+# 1040, 4112 and 40960 split a row over 4 and 8 CTAs with a shorter last
+# share; 40960 takes two rounds of 1024 threads in each of its 8 CTAs
+@pytest.mark.parametrize("n", [16, 48, 768, 1040, 2560, 4112, 7168, 40960])
 @pytest.mark.parametrize("kind", KINDS)
 def test_quantiser_bit_exact(moe, kind, n):
     rng = np.random.default_rng(1000 * KINDS.index(kind) + n)
