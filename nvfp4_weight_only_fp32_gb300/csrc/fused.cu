@@ -227,6 +227,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, unsigned parity, int *err
 // single-copy atomic).  The tag is the number of calls every block has
 // finished, plus one, so a word from an earlier call (or zeroed memory) never
 // matches and a reader simply polls the words it needs.
+// 8-byte asynchronous copy global -> shared
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(__cvta_generic_to_global(src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_tagged(unsigned long long *p, unsigned tag, unsigned payload) {
     const unsigned long long v = ((unsigned long long)tag << 32) | payload;
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
@@ -287,7 +293,7 @@ __device__ __forceinline__ void chunk_mma_smem(const uint8_t *ch, int lane, cons
 // over the chosen) every lane also gets sum_e exp(z_e - z_max) over all
 // experts: the experts left after the top-k, then the chosen ones, each lane's
 // terms in index order, summed across the warp by a butterfly.
-template <int M>
+template <int M, bool SORTED>
 __device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned long long *lt, int t, int E, int K,
                                             unsigned tag, int lane, int *err, unsigned long long &sel, int &passes,
                                             bool full_den, float &den) {
@@ -320,14 +326,28 @@ __device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned lo
         v[i] = e < E ? ((unsigned long long)logit_key(__uint_as_float((unsigned)v[i])) << 32) | (unsigned)~e : 0ull;
     }
     MOE_TRACE_CLOCK_AT(4, 1, 0);
-    sel = warp_topk<M>(v, K, lane);
+    // the sorted top-k for one or two tokens (measured faster there; slower
+    // at eight, where eight warps route at once) on a copy, so that v keeps
+    // the index order: a lane's chosen keys are larger than every key it has
+    // left (rest[0]); the tree form clears the chosen keys in v
+    unsigned long long rest[M];
+    if constexpr (SORTED) {
+#pragma unroll
+        for (int i = 0; i < M; ++i) rest[i] = v[i];
+        sel = warp_topk_sorted<M>(rest, K, lane);
+    } else {
+        sel = warp_topk_tree<M>(v, K, lane);
+    }
     den = 1.f;
     if (full_den) {
         const float zmax = key_logit(__shfl_sync(0xffffffffu, (unsigned)(sel >> 32), 0));
         float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < M; ++i)
-            if (v[i]) acc += expf(key_logit((unsigned)(v[i] >> 32)) - zmax);
+        for (int i = 0; i < M; ++i) {
+            bool left = v[i] != 0ull;
+            if constexpr (SORTED) left = left && v[i] <= rest[0];
+            if (left) acc += expf(key_logit((unsigned)(v[i] >> 32)) - zmax);
+        }
         if (lane < K) acc += expf(key_logit((unsigned)(sel >> 32)) - zmax);
 #pragma unroll
         for (int w = 16; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
@@ -351,7 +371,6 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[kFW][kRWmax];
     __shared__ __align__(8) uint64_t s_rbar;   // router rows
-    __shared__ __align__(8) uint64_t s_xbar;   // x
     __shared__ const uint8_t *s_tab_src[kFW][kTabMax];
     __shared__ int s_tab_n[kFW][kTabMax];
     __shared__ float s_tmax[kFW][kTF];
@@ -471,7 +490,6 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     if (threadIdx.x < E) s_tokmask[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
         mbar_init(&s_rbar, 1);
-        mbar_init(&s_xbar, 1);
     }
     if (lane == 0) {
         for (int i = 0; i < RW; ++i) mbar_init(bar + i, 1);
@@ -504,15 +522,20 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
 
     // ---------------- B: x, logits ----------------
     bool ok = true;
-    if (threadIdx.x == 0) {
-        s_tag = __ldcg(d.calls + c) + 1u;
-        // x (T rows, contiguous) in one bulk copy
-        mbar_expect_tx(&s_xbar, (unsigned)(T * H * 2));
-        bulk_g2s(smem + fg.xraw_off, a.x, (unsigned)(T * H * 2), &s_xbar, pol);
-    }
-    if (!mbar_wait(&s_xbar, 0u, d.err) || !mbar_wait(&s_rbar, 0u, d.err)) ok = false;
-    MOE_TRACE_CLOCK(2, 12);
     const int nq = H / 4;                    // 4-element quads of an activation row
+    if (threadIdx.x == 0) s_tag = __ldcg(d.calls + c) + 1u;
+    // x: each thread copies the quads it reads in the pass below (quads
+    // threadIdx.x + i * kFT of every token) with 8-byte asynchronous copies,
+    // so that only its own copies stand between it and its first use (a
+    // single bulk copy of all rows took longer to land)
+#pragma unroll 1
+    for (int P = threadIdx.x; P < nq; P += kFT)
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+            if (t < T) cp_async8(smem + fg.xraw_off + ((size_t)t * H + 4 * P) * 2, a.x + (size_t)t * H + 4 * P);
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    if (!mbar_wait(&s_rbar, 0u, d.err)) ok = false;
+    MOE_TRACE_CLOCK(2, 12);
     // One pass over x for all tokens: this thread's max |x| per token and its
     // partial FP32 logits (token t, expert c + re * G) from the exact FP32
     // values of x; each router quad is read once for all tokens.
@@ -764,10 +787,10 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
             const bool smax = d.score_func == 1, fden = smax && !d.normalize;
             float den = 1.f;
             switch (fg.m1p) {
-                case 1: ok = route_token<1>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
-                case 2: ok = route_token<2>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
-                case 4: ok = route_token<4>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
-                default: ok = route_token<8>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
+                case 1: ok = route_token<1, (TT <= 2)>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
+                case 2: ok = route_token<2, (TT <= 2)>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
+                case 4: ok = route_token<4, (TT <= 2)>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
+                default: ok = route_token<8, (TT <= 2)>(d, d.logit_tag, t, E, K, ltag, lane, d.err, sel, lpass, fden, den) && ok; break;
             }
             const unsigned sel_key = (unsigned)(sel >> 32);
             const int sel_e = (int)~(unsigned)sel;

@@ -424,15 +424,48 @@ __device__ __forceinline__ float key_score(unsigned key) {
     return key ? sigmoid_score(z) : __int_as_float(0x7fc00000);
 }
 
-// Warp-wide top-k over 64-bit sort keys, M per lane (M a power of two; all
-// keys distinct; 0 marks an empty place and is never chosen while k <= the
-// number of real keys).  Every round each lane takes the largest of its
-// keys (a pairwise tree), the warp takes the largest of those (its high
-// word, then among the lanes holding that, its low word) and the lane that
-// held it clears it.  Lane j < k ends with the j-th choice.  The code is
-// short on purpose: it runs once per call, from a cold instruction cache.
+// c[i] >= c[j] afterwards
+__device__ __forceinline__ void key_cx(unsigned long long &a, unsigned long long &b) {
+    const bool sw = b > a;
+    const unsigned long long x = sw ? b : a, y = sw ? a : b;
+    a = x;
+    b = y;
+}
+
+// Descending sort of M = 1, 2, 4 or 8 keys: Batcher's odd-even merge sort
+// network (for 8: 19 comparators in 6 levels).
 template <int M>
-__device__ __forceinline__ unsigned long long warp_topk(unsigned long long (&c)[M], int K, int lane) {
+__device__ __forceinline__ void sort_keys_desc(unsigned long long (&c)[M]) {
+    if constexpr (M == 2) {
+        key_cx(c[0], c[1]);
+    } else if constexpr (M == 4) {
+        key_cx(c[0], c[1]); key_cx(c[2], c[3]);
+        key_cx(c[0], c[2]); key_cx(c[1], c[3]);
+        key_cx(c[1], c[2]);
+    } else if constexpr (M == 8) {
+        key_cx(c[0], c[1]); key_cx(c[2], c[3]); key_cx(c[4], c[5]); key_cx(c[6], c[7]);
+        key_cx(c[0], c[2]); key_cx(c[1], c[3]); key_cx(c[4], c[6]); key_cx(c[5], c[7]);
+        key_cx(c[1], c[2]); key_cx(c[5], c[6]);
+        key_cx(c[0], c[4]); key_cx(c[1], c[5]); key_cx(c[2], c[6]); key_cx(c[3], c[7]);
+        key_cx(c[2], c[4]); key_cx(c[3], c[5]);
+        key_cx(c[1], c[2]); key_cx(c[3], c[4]); key_cx(c[5], c[6]);
+    } else {
+        static_assert(M == 1, "1, 2, 4 or 8 keys per lane");
+    }
+}
+
+// Warp-wide top-k over 64-bit sort keys, M per lane (M a power of two up to
+// 16; all keys distinct; 0 marks an empty place and is never chosen while
+// k <= the number of real keys).  Every round the warp takes the largest of
+// the lanes' largest keys (its high word, then among the lanes holding that,
+// its low word) and the lane that held it drops it.  Lane j < k ends with
+// the j-th choice.
+// Tree form: a round takes each lane's largest by a pairwise tree and the
+// winner clears it in place (c ends with the chosen keys zeroed, the rest
+// where they were).  Short code: it runs once per call, from a cold
+// instruction cache.
+template <int M>
+__device__ __forceinline__ unsigned long long warp_topk_tree(unsigned long long (&c)[M], int K, int lane) {
     unsigned long long mine = 0ull;
 #pragma unroll 1
     for (int j = 0; j < K; ++j) {
@@ -451,6 +484,28 @@ __device__ __forceinline__ unsigned long long warp_topk(unsigned long long (&c)[
 #pragma unroll
             for (int i = 0; i < M; ++i) c[i] = c[i] == t[0] ? 0ull : c[i];
         }
+    }
+    return mine;
+}
+
+// Sorted form (M <= 8): each lane first sorts its keys, largest first, so
+// that a round's candidate is its first key and dropping it moves the
+// others up by one (shorter rounds, a longer prologue); c ends with the
+// lane's keys not chosen, largest first.
+template <int M>
+__device__ __forceinline__ unsigned long long warp_topk_sorted(unsigned long long (&c)[M], int K, int lane) {
+    sort_keys_desc<M>(c);
+    unsigned long long mine = 0ull;
+#pragma unroll 1
+    for (int j = 0; j < K; ++j) {
+        const unsigned hi = (unsigned)(c[0] >> 32), lo = (unsigned)c[0];
+        const unsigned mx = __reduce_max_sync(0xffffffffu, hi);
+        const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mx ? lo : 0u);
+        if (lane == j) mine = ((unsigned long long)mx << 32) | ml;
+        const bool won = hi == mx && lo == ml;
+#pragma unroll
+        for (int i = 0; i + 1 < M; ++i) c[i] = won ? c[i + 1] : c[i];
+        c[M - 1] = won ? 0ull : c[M - 1];
     }
     return mine;
 }

@@ -63,7 +63,8 @@ __device__ __forceinline__ unsigned long long token_topk(const float *z, bool in
         const int e = i * 32 + lane;
         c[i] = e < E ? ((unsigned long long)logit_key(in_smem ? z[e] : __ldcg(z + e)) << 32) | (unsigned)~e : 0ull;
     }
-    return warp_topk<M>(c, K, lane);
+    if constexpr (M <= 8) return warp_topk_sorted<M>(c, K, lane);
+    else return warp_topk_tree<M>(c, K, lane);
 }
 
 // Softmax denominator of one token relative to its largest logit z0: the sum
