@@ -43,8 +43,11 @@ namespace {
 
 constexpr int kThreads = 32 * kRouteWarps;
 constexpr int kTokGroup = 8;
-constexpr int kPre = 16;    // float4 per lane fetched before the wait (2048 K)
-constexpr int kTail = 8;    // float4 per lane in flight for the rest of a longer row
+constexpr int kEPT = 4;                                  // experts per thread (a block half's)
+constexpr int kRouteHalfWarps = kRouteWarps / 2;
+constexpr int kHalfThreads = 32 * kRouteHalfWarps;
+constexpr int kPre = 4;     // 4-column groups per thread fetched before the wait (2048 K)
+static_assert(kRouteWarps == 2 * kEPT, "two halves of four experts");
 
 __device__ __forceinline__ void bf16x4_to_f(uint2 v, float &a, float &b, float &c, float &e) {
     a = __uint_as_float(v.x << 16);
@@ -84,27 +87,37 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = d.H, E = d.E, K = d.k, S = d.S;
-    const int e = blockIdx.x * kRouteWarps + warp;
+    // this block's experts: e0 .. e0 + kRouteWarps - 1
+    const int e0 = blockIdx.x * kRouteWarps;
     // K split: block z takes columns [k0, k0 + Hk) of the router rows
     const int KH = gridDim.z, Hk = H / KH, k0 = blockIdx.z * Hk;
     const int nvec = Hk / 4;
     const int t0 = blockIdx.y * tg, nt = min(tg, T - t0);
-    const float *wr = d.router_w + (size_t)(e < E ? e : 0) * H + k0;
 
     MOE_TRACE_POINT(0, 0);
-    float4 pre[kPre];
+    // The block's threads form two halves (warps 0-3 and 4-7), half h taking
+    // experts e0 + 4h .. e0 + 4h + 3; thread i of a half takes the 4-column
+    // groups v = i + 128 j of the K range for its four experts, so that each
+    // x group it reads from shared memory serves four experts.  The first
+    // kPre groups' router columns are loaded before the dependency wait.
+    const int half = warp / kRouteHalfWarps, hi_ = threadIdx.x % (32 * kRouteHalfWarps);
+    const int eh = e0 + kEPT * half;
+    float4 pre[kPre][kEPT];
 #pragma unroll
     for (int j = 0; j < kPre; ++j) {
-        const int v = lane + 32 * j;
-        if (e < E && v < nvec) {
-            // volatile loads: issued here, before the wait, not sunk past it
-            const float2 lo = ld_nc_f2(wr + 4 * v), hi = ld_nc_f2(wr + 4 * v + 2);
-            pre[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
-        } else {
-            pre[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int v = hi_ + kHalfThreads * j;
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i) {
+            if (eh + i < E && v < nvec) {
+                // volatile loads: issued here, before the wait, not sunk past it
+                const float *wr = d.router_w + (size_t)(eh + i) * H + k0 + 4 * v;
+                const float2 lo = ld_nc_f2(wr), hi = ld_nc_f2(wr + 2);
+                pre[j][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+                pre[j][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     }
-    const float bias = (e < E && d.router_b && KH == 1) ? d.router_b[e] : 0.f;
     pdl_wait();
     pdl_trigger();
     MOE_TRACE_POINT(0, 1);
@@ -168,54 +181,73 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         // this K range's max; the exponent is taken from the whole row below
         atomicMax(d.xmaxb + t0 + threadIdx.x, __float_as_uint(s_rmax[threadIdx.x]));
     }
-    // ---- logits of the group's tokens for this warp's expert ----
-    if (e < E) {
-        float acc[kTokGroup];
+    // ---- logits of the group's tokens for the block's experts ----
+    {
+        // acc[i][t]: expert eh + i, token t0 + t, over this thread's columns
+        float acc[kEPT][kTokGroup];
 #pragma unroll
-        for (int t = 0; t < kTokGroup; ++t) acc[t] = 0.f;
+        for (int i = 0; i < kEPT; ++i)
+#pragma unroll
+            for (int t = 0; t < kTokGroup; ++t) acc[i][t] = 0.f;
+        auto group = [&](int v, const float4 (&w)[kEPT]) {
+#pragma unroll
+            for (int t = 0; t < kTokGroup; ++t) {
+                if (t < nt) {
+                    const float4 xv = xs[t * nvec + v];
+#pragma unroll
+                    for (int i = 0; i < kEPT; ++i)
+                        acc[i][t] = fmaf(xv.w, w[i].w, fmaf(xv.z, w[i].z, fmaf(xv.y, w[i].y, fmaf(xv.x, w[i].x, acc[i][t]))));
+                }
+            }
+        };
 #pragma unroll
         for (int j = 0; j < kPre; ++j) {
-            const int v = lane + 32 * j;
-            if (v < nvec) {
-#pragma unroll
-                for (int t = 0; t < kTokGroup; ++t) {
-                    if (t < nt) {
-                        const float4 xv = xs[t * nvec + v];
-                        acc[t] = fmaf(xv.w, pre[j].w, fmaf(xv.z, pre[j].z, fmaf(xv.y, pre[j].y, fmaf(xv.x, pre[j].x, acc[t]))));
-                    }
-                }
-            }
+            const int v = hi_ + kHalfThreads * j;
+            if (v < nvec) group(v, pre[j]);
         }
-        // the rest of a long row: kTail loads per lane in flight per round trip
+        // the rest of a longer K range, one column group at a time
 #pragma unroll 1
-        for (int v0 = lane + 32 * kPre; v0 < nvec; v0 += 32 * kTail) {
-            float4 w[kTail];
+        for (int v = hi_ + kHalfThreads * kPre; v < nvec; v += kHalfThreads) {
+            float4 w[kEPT];
 #pragma unroll
-            for (int u = 0; u < kTail; ++u)
-                if (v0 + 32 * u < nvec) w[u] = ld_f4(wr + 4 * (v0 + 32 * u));
-#pragma unroll
-            for (int u = 0; u < kTail; ++u) {
-                const int v = v0 + 32 * u;
-                if (v < nvec) {
-#pragma unroll
-                    for (int t = 0; t < kTokGroup; ++t) {
-                        if (t < nt) {
-                            const float4 xv = xs[t * nvec + v];
-                            acc[t] = fmaf(xv.w, w[u].w, fmaf(xv.z, w[u].z, fmaf(xv.y, w[u].y, fmaf(xv.x, w[u].x, acc[t]))));
-                        }
-                    }
-                }
-            }
+            for (int i = 0; i < kEPT; ++i)
+                w[i] = eh + i < E ? ld_f4(d.router_w + (size_t)(eh + i) * H + k0 + 4 * v) : make_float4(0.f, 0.f, 0.f, 0.f);
+            group(v, w);
         }
         MOE_TRACE_POINT(0, 8);
+        // warp sums of the 32 values by a transposing butterfly: at the step
+        // of distance w every lane keeps the half of its values selected by
+        // bit w of its lane index and adds the partner's copy of that half;
+        // lane L ends with value L (expert eh + L / 8, token L % 8)
+        float *s_part = reinterpret_cast<float *>(smem + (size_t)nt * nvec * 16);   // [kRouteWarps][32]
+        static_assert(kEPT * kTokGroup == 32, "one value per lane");
+        {
+            float a[32];
 #pragma unroll
-        for (int t = 0; t < kTokGroup; ++t) {
-            float a = acc[t];
+            for (int u = 0; u < 32; ++u) a[u] = acc[u / kTokGroup][u % kTokGroup];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            if (lane == 0 && t < nt) {
-                if (KH == 1) d.logits[(size_t)(t0 + t) * E + e] = a + bias;
-                else d.lpart[((size_t)blockIdx.z * d.max_tokens + t0 + t) * E + e] = a;
+            for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+                for (int u = 0; u < w; ++u) {
+                    const bool up = (lane & w) != 0;
+                    const float send = up ? a[u] : a[u + w];
+                    const float keep = up ? a[u + w] : a[u];
+                    a[u] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                }
+            }
+            s_part[warp * 32 + lane] = a[0];
+        }
+        __syncthreads();
+        if (threadIdx.x < kRouteWarps * kTokGroup) {
+            // the sums of a half's warps in a fixed order
+            const int i = threadIdx.x / kTokGroup, t = threadIdx.x % kTokGroup, e = e0 + i;
+            const int h = i / kEPT, u = (i % kEPT) * kTokGroup + t;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kRouteHalfWarps; ++w) v += s_part[(h * kRouteHalfWarps + w) * 32 + u];
+            if (e < E && t < nt) {
+                if (KH == 1) d.logits[(size_t)(t0 + t) * E + e] = v + (d.router_b ? d.router_b[e] : 0.f);
+                else d.lpart[((size_t)blockIdx.z * d.max_tokens + t0 + t) * E + e] = v;
             }
         }
     }
@@ -393,10 +425,10 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     // Slots: shared experts first, then routed experts with >= 1 token in
     // ascending id.  Exclusive scans of (used?, token count) over experts.
     const int per = (E + kThreads - 1) / kThreads;
-    const int e0 = threadIdx.x * per;
+    const int eb = threadIdx.x * per;
     int fsum = 0, csum = 0;
     for (int i = 0; i < per; ++i) {
-        const int ee = e0 + i;
+        const int ee = eb + i;
         if (ee < E) {
             const int c = __popcll(s_mask[ee]);
             fsum += c > 0;
@@ -424,7 +456,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         cbase += s_wsum_c[w];
     }
     for (int i = 0; i < per; ++i) {
-        const int ee = e0 + i;
+        const int ee = eb + i;
         if (ee < E) {
             const int c = __popcll(s_mask[ee]);
             if (c > 0) {
@@ -541,13 +573,14 @@ int route_ksplit(const DevLayer &d, int T, int sm_count) {
 
 size_t route_smem_bytes(const DevLayer &d, int T, int kh, int *tg_out) {
     // activation columns of one token group as FP32 (at most 8 tokens, at
-    // most 96 KB), later the group's logits
+    // most 96 KB), later the group's logits,
     const int Hk = d.H / kh;
     int tg = kTokGroup;
     while (tg > 1 && (size_t)tg * Hk * 4 > 96 * 1024) --tg;
     if (tg > T) tg = T;
     if (tg_out) *tg_out = tg;
-    return (size_t)tg * (size_t)std::max(Hk, d.E) * 4;
+    // plus the warps' partial logits [kRouteWarps][32] behind the columns
+    return (size_t)tg * (size_t)std::max(Hk, d.E) * 4 + (size_t)kRouteWarps * 32 * 4;
 }
 
 cudaError_t launch_route(const DevLayer &d, const __nv_bfloat16 *x, int T, int *ids_out, float *w_out,
