@@ -49,6 +49,12 @@ constexpr int kHalfThreads = 32 * kRouteHalfWarps;
 constexpr int kPre = 4;     // 4-column groups per thread fetched before the wait (2048 K)
 static_assert(kRouteWarps == 2 * kEPT, "two halves of four experts");
 
+// 16-byte asynchronous copy global -> shared (L2 only)
+__device__ __forceinline__ void cp_async16_cg(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(__cvta_generic_to_global(src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bf16x4_to_f(uint2 v, float &a, float &b, float &c, float &e) {
     a = __uint_as_float(v.x << 16);
     b = __uint_as_float(v.x & 0xFFFF0000u);
@@ -126,55 +132,43 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
     // loads, all in flight) ----
     __shared__ float s_rmax[kTokGroup];
     if (threadIdx.x < kTokGroup) s_rmax[threadIdx.x] = 0.f;
-    // x columns as FP32 (exact), so that the dot products below read them
-    // with one 16-byte load per four elements and no unpacking
-    const float4 *xs = reinterpret_cast<const float4 *>(smem);   // [nt][Hk/4]
+    // x columns as BF16, copied by 16-byte asynchronous copies (all in
+    // flight, no register round trip); the dot products below unpack them
+    const uint2 *xs = reinterpret_cast<const uint2 *>(smem);   // [nt][Hk/4] groups of four
     {
         const int r16 = Hk / 8, n16 = nt * r16;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t0 * H + k0);
-        float4 *dst = reinterpret_cast<float4 *>(smem);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n16; i += kThreads)
+            cp_async16_cg(smem + (size_t)16 * i, src + (size_t)(i / r16) * (H / 8) + i % r16);
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
         __syncthreads();
+        if (blockIdx.x == 0) {
+            // per-token max |x| for the GEMVs' power-of-two prescale
+            // (non-negative, so its bits order as unsigned integers)
 #pragma unroll 1
-        for (int base = threadIdx.x; base < n16; base += 8 * kThreads) {
-            uint4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = base + u * kThreads;
-                if (i < n16) v[u] = __ldcg(src + (size_t)(i / r16) * (H / 8) + i % r16);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = base + u * kThreads;
+            for (int i0 = 0; i0 < n16; i0 += kThreads) {
+                const int i = i0 + threadIdx.x;
+                float m = 0.f;
                 if (i < n16) {
-                    float a0, a1, a2, a3, b0, b1, b2, b3;
-                    bf16x4_to_f(make_uint2(v[u].x, v[u].y), a0, a1, a2, a3);
-                    bf16x4_to_f(make_uint2(v[u].z, v[u].w), b0, b1, b2, b3);
-                    dst[2 * i] = make_float4(a0, a1, a2, a3);
-                    dst[2 * i + 1] = make_float4(b0, b1, b2, b3);
-                }
-                if (blockIdx.x == 0) {
-                    // per-token max |x| for the GEMVs' power-of-two prescale
-                    // (non-negative, so its bits order as unsigned integers)
-                    float m = 0.f;
-                    if (i < n16) {
-                        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    const uint4 v = reinterpret_cast<const uint4 *>(smem)[i];
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
-                                               fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
-                    }
-                    if ((r16 & 31) == 0) {
-                        // a warp's 32 pieces are one token's (and all in
-                        // range or all out): one shared atomic per warp
-                        const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-                        if (lane == 0 && i < n16) atomicMax(reinterpret_cast<unsigned *>(&s_rmax[i / r16]), mw);
-                    } else if (i < n16) {
-                        atomicMax(reinterpret_cast<unsigned *>(&s_rmax[i / r16]), __float_as_uint(m));
-                    }
+                    for (int q = 0; q < 4; ++q)
+                        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
+                                           fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
+                }
+                if ((r16 & 31) == 0) {
+                    // a warp's 32 pieces are one token's (and all in range or
+                    // all out): one shared atomic per warp
+                    const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+                    if (lane == 0 && i < n16) atomicMax(reinterpret_cast<unsigned *>(&s_rmax[i / r16]), mw);
+                } else if (i < n16) {
+                    atomicMax(reinterpret_cast<unsigned *>(&s_rmax[i / r16]), __float_as_uint(m));
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
     }
     MOE_TRACE_POINT(0, 2);
     if (blockIdx.x == 0 && threadIdx.x < nt) {
@@ -193,7 +187,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
 #pragma unroll
             for (int t = 0; t < kTokGroup; ++t) {
                 if (t < nt) {
-                    const float4 xv = xs[t * nvec + v];
+                    float4 xv;
+                    bf16x4_to_f(xs[t * nvec + v], xv.x, xv.y, xv.z, xv.w);
 #pragma unroll
                     for (int i = 0; i < kEPT; ++i)
                         acc[i][t] = fmaf(xv.w, w[i].w, fmaf(xv.z, w[i].z, fmaf(xv.y, w[i].y, fmaf(xv.x, w[i].x, acc[i][t]))));
@@ -219,7 +214,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         // of distance w every lane keeps the half of its values selected by
         // bit w of its lane index and adds the partner's copy of that half;
         // lane L ends with value L (expert eh + L / 8, token L % 8)
-        float *s_part = reinterpret_cast<float *>(smem + (size_t)nt * nvec * 16);   // [kRouteWarps][32]
+        float *s_part = reinterpret_cast<float *>(smem + (size_t)nt * nvec * 8);   // [kRouteWarps][32]
         static_assert(kEPT * kTokGroup == 32, "one value per lane");
         {
             float a[32];
@@ -450,6 +445,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         s_wsum_c[warp] = cinc;
     }
     __syncthreads();
+    MOE_TRACE_POINT(0, 12);
     int fbase = finc - fsum, cbase = cinc - csum;
     for (int w = 0; w < warp; ++w) {
         fbase += s_wsum_f[w];
@@ -480,6 +476,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         s_slotm[threadIdx.x] = (short)T;
     }
     __syncthreads();
+    MOE_TRACE_POINT(0, 13);
     if (warp == 0) {
         // slots with at least grouped_min tokens (in slot order) go to the
         // grouped tensor-core kernels; the GEMV kernels skip them
@@ -533,6 +530,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         }
     }
 
+    MOE_TRACE_POINT(0, 14);
     // Pairs: an expert's tokens are numbered in ascending token order.
     const int P = K + S;
     for (int it = threadIdx.x; it < T * K; it += kThreads) {
@@ -551,6 +549,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         d.pair_w[p] = 1.0f;
         d.pair_of[t * P + K + sidx] = p;
     }
+    MOE_TRACE_POINT(0, 15);
     for (int p = threadIdx.x; p < T * P; p += kThreads) d.hmax[p] = 0u;
     if (threadIdx.x == 0) {
         *d.ticket = 0u;
