@@ -489,19 +489,26 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         // with the most items, the GEMV kernels' units are handed out on demand.
         int tau = d.grouped_min;
         if (T > 8 && d.tau_max > d.grouped_min) {
-            // routed slots by token count (counts of 16 and more together)
+            // routed slots by token count (counts of 16 and more together):
+            // lane b < 17 ends with the number of count b.  Per 32 slots the
+            // lanes of one count meet in a match and the lowest of them adds
+            // them up (one writer per entry).
             __shared__ int s_hist[17];
             if (lane < 17) s_hist[lane] = 0;
             __syncwarp();
-            for (int sl = S + lane; sl < ns; sl += 32) {
-                const int m = s_slotm[sl];
-                if (m >= d.grouped_min) atomicAdd(&s_hist[min(m, 16)], 1);
+            for (int b0 = S; b0 < ns; b0 += 32) {
+                const int sl = b0 + lane;
+                const int m = sl < ns ? s_slotm[sl] : 0;
+                const int bin = sl < ns && m >= d.grouped_min ? min(m, 16) : -1;
+                const unsigned mm = __match_any_sync(0xffffffffu, bin);
+                if (bin >= 0 && lane == __ffs(mm) - 1) s_hist[bin] += __popc(mm);
+                __syncwarp();
             }
-            __syncwarp();
+            const int h = lane < 17 ? s_hist[lane] : 0;
             int shot = 0;   // shared slots stay hot at grouped_min
             for (int j = 0; j < S; ++j) shot += s_slotm[j] >= d.grouped_min;
-            int cnt = 0;    // routed slots with at least cand tokens
-            for (int b = 16; b >= d.tau_max; --b) cnt += s_hist[b];
+            // routed slots with at least cand tokens
+            int cnt = __reduce_add_sync(0xffffffffu, lane >= d.tau_max ? h : 0);
             // from the top: the smallest threshold whose items still fit
             tau = d.tau_max;
             for (int cand = d.tau_max; cand >= d.grouped_min; --cand) {
@@ -509,7 +516,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
                 const long dn = (long)(cnt + shot) * (d.H / 128);
                 if (up > d.nsm || dn > d.nsm) break;
                 tau = cand;
-                if (cand > d.grouped_min) cnt += s_hist[cand - 1];
+                if (cand > d.grouped_min) cnt += __shfl_sync(0xffffffffu, h, cand - 1);
             }
         }
         int nh = 0, nc = 0;
