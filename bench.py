@@ -52,8 +52,8 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20784896, "fused_cu_sha256_16": "41a5b9880e39a08a"},
-    "flint8": {"bytes": 124596224, "fused_cu_sha256_16": "41a5b9880e39a08a"},
+    "flint1": {"bytes": 20787456, "fused_cu_sha256_16": "619630a753dd442b"},
+    "flint8": {"bytes": 124407040, "fused_cu_sha256_16": "619630a753dd442b"},
 }
 
 def ncu_traffic(workload: str):
