@@ -52,8 +52,8 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20787456, "fused_cu_sha256_16": "619630a753dd442b"},
-    "flint8": {"bytes": 124407040, "fused_cu_sha256_16": "619630a753dd442b"},
+    "flint1": {"bytes": 20788736, "fused_cu_sha256_16": "48887d91ca152f48"},
+    "flint8": {"bytes": 124297472, "fused_cu_sha256_16": "48887d91ca152f48"},
 }
 
 def ncu_traffic(workload: str):

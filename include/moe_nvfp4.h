@@ -244,8 +244,12 @@ moe_status moe_decode_forward(moe_layer *layer, const void *x, int T, void *out,
  * pinned (page-locked and mapped, as cudaHostAlloc gives) and 16-byte
  * aligned the kernels store the output straight into it through its device
  * alias, otherwise it is copied back; the routing result (optional) is copied
- * back.  Returns after enqueueing; the host buffers may be read after the
- * stream has been synchronised. */
+ * back.  When the step takes the single launch with one or two tokens and
+ * x_host is pinned, mapped, 16-byte aligned and apart from out_host, the
+ * kernel reads x_host in place through its device alias instead of a copy
+ * (no copy then stands between two layers' kernels); x_host must then stay
+ * unchanged until the stream reaches the call.  Returns after enqueueing;
+ * the host buffers may be read after the stream has been synchronised. */
 moe_status moe_decode_forward_host(moe_layer *layer, const void *x_host, int T,
                                    void *out_host, int *topk_ids_host,
                                    float *topk_w_host, void *stream);

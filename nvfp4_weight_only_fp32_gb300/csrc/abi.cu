@@ -547,6 +547,22 @@ moe_status moe_stage_down(moe_layer *L, int T, void *out, void *stream) {
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "down launch");
 }
 
+// The single launch for one call (L->fused_ok[T]); x_sys: x is the device
+// alias of pinned host memory.
+static moe_status forward_fused(moe_layer *L, const void *x, int T, void *out, int *topk_ids, float *topk_w,
+                                void *stream, bool x_sys) {
+    DeviceGuard g(L->device);
+    DevLayer d = L->d;
+    d.debug_stall = L->inject_stall;
+    L->inject_stall = 0;
+    cudaError_t e = cudaSuccess;
+    if (++L->fused_calls >= kTagRestart) e = restart_tags(L, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tag restart");
+    e = launch_fused(d, static_cast<const __nv_bfloat16 *>(x), T, static_cast<__nv_bfloat16 *>(out), topk_ids, topk_w,
+                     L->sm_count, L->cfg.fused > 0, reinterpret_cast<cudaStream_t>(stream), x_sys);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "single-launch layer");
+}
+
 moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int *topk_ids,
                               float *topk_w, void *stream) {
     moe_status rc = check_call(L, T);
@@ -556,18 +572,7 @@ moe_status moe_decode_forward(moe_layer *L, const void *x, int T, void *out, int
     const size_t nb = (size_t)T * L->cfg.hidden * 2;
     const char *xa = static_cast<const char *>(x), *oa = static_cast<const char *>(out);
     if (xa < oa + nb && oa < xa + nb) return fail(MOE_ERR_INVALID_ARG, "out overlaps x");
-    if (L->fused_ok[T]) {
-        DeviceGuard g(L->device);
-        DevLayer d = L->d;
-        d.debug_stall = L->inject_stall;
-        L->inject_stall = 0;
-        cudaError_t e = cudaSuccess;
-        if (++L->fused_calls >= kTagRestart) e = restart_tags(L, reinterpret_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e, "tag restart");
-        e = launch_fused(d, static_cast<const __nv_bfloat16 *>(x), T, static_cast<__nv_bfloat16 *>(out), topk_ids,
-                         topk_w, L->sm_count, L->cfg.fused > 0, reinterpret_cast<cudaStream_t>(stream));
-        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "single-launch layer");
-    }
+    if (L->fused_ok[T]) return forward_fused(L, x, T, out, topk_ids, topk_w, stream, false);
     rc = moe_stage_route(L, x, T, topk_ids, topk_w, stream);
     if (rc == MOE_OK) rc = moe_stage_gate_up(L, x, T, stream);
     if (rc == MOE_OK) rc = moe_stage_down(L, T, out, stream);
@@ -583,18 +588,33 @@ moe_status moe_decode_forward_host(moe_layer *L, const void *x_host, int T, void
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t nb = (size_t)T * L->cfg.hidden * 2;
     const size_t nk = (size_t)T * L->cfg.top_k;
-    cudaError_t e = cudaMemcpyAsync(L->x_stage, x_host, nb, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_fail(e, "x upload");
-    // pinned (page-locked, mapped) output: the kernels store straight into it
-    // through its device alias instead of a copy after them
-    void *out_dev = nullptr;
-    cudaPointerAttributes pa;
-    if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
-        pa.devicePointer && aligned16(pa.devicePointer))
-        out_dev = pa.devicePointer;
-    cudaGetLastError();
-    rc = moe_decode_forward(L, L->x_stage, T, out_dev ? out_dev : L->out_stage, L->ids_stage, L->w_stage, stream);
+    // pinned (page-locked, mapped) host buffers: their device aliases
+    auto alias = [](const void *p) -> void * {
+        cudaPointerAttributes pa;
+        void *dev = nullptr;
+        if (cudaPointerGetAttributes(&pa, p) == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+            aligned16(pa.devicePointer))
+            dev = pa.devicePointer;
+        cudaGetLastError();
+        return dev;
+    };
+    // the kernels store the output straight into a pinned out_host instead of
+    // a copy after them; the single launch of one or two tokens also reads a
+    // pinned x_host in place (each block reads the rows once), so that no copy
+    // stands between two layers' kernels
+    void *out_dev = alias(out_host);
+    const char *xa = static_cast<const char *>(x_host), *oa = static_cast<const char *>(out_host);
+    const bool apart = !(xa < oa + nb && oa < xa + nb);
+    const void *x_dev = L->fused_ok[T] && T <= 2 && apart ? alias(x_host) : nullptr;
+    if (x_dev) {
+        rc = forward_fused(L, x_dev, T, out_dev ? out_dev : L->out_stage, L->ids_stage, L->w_stage, stream, true);
+    } else {
+        cudaError_t e = cudaMemcpyAsync(L->x_stage, x_host, nb, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "x upload");
+        rc = moe_decode_forward(L, L->x_stage, T, out_dev ? out_dev : L->out_stage, L->ids_stage, L->w_stage, stream);
+    }
     if (rc != MOE_OK) return rc;
+    cudaError_t e;
     e = out_dev ? cudaSuccess : cudaMemcpyAsync(out_host, L->out_stage, nb, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && topk_ids_host)
         e = cudaMemcpyAsync(topk_ids_host, L->ids_stage, nk * sizeof(int), cudaMemcpyDeviceToHost, st);

@@ -93,6 +93,7 @@ struct FusedArgs {
     __nv_bfloat16 *out;
     int *ids_out;
     float *w_out;
+    int x_sys;   // x is the device alias of pinned host memory: read by plain loads
 };
 
 // Launch geometry and host-planned work split.
@@ -528,12 +529,28 @@ __global__ void __launch_bounds__(kFT, 1) fused_kernel(DevLayer d, FusedArgs a, 
     // threadIdx.x + i * kFT of every token) with 8-byte asynchronous copies,
     // so that only its own copies stand between it and its first use (a
     // single bulk copy of all rows took longer to land)
+    if (TT <= 2 && a.x_sys) {
+        // x in pinned host memory, through its device alias: plain loads
+        // (taken for one or two tokens only; the instance for more carries
+        // none of this code)
 #pragma unroll 1
-    for (int P = threadIdx.x; P < nq; P += kFT)
+        for (int P = threadIdx.x; P < nq; P += kFT) {
+            uint2 v[TT];
 #pragma unroll
-        for (int t = 0; t < TT; ++t)
-            if (t < T) cp_async8(smem + fg.xraw_off + ((size_t)t * H + 4 * P) * 2, a.x + (size_t)t * H + 4 * P);
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
+            for (int t = 0; t < TT; ++t)
+                if (t < T) v[t] = *reinterpret_cast<const uint2 *>(a.x + (size_t)t * H + 4 * P);
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+                if (t < T) *reinterpret_cast<uint2 *>(smem + fg.xraw_off + ((size_t)t * H + 4 * P) * 2) = v[t];
+        }
+    } else {
+#pragma unroll 1
+        for (int P = threadIdx.x; P < nq; P += kFT)
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+                if (t < T) cp_async8(smem + fg.xraw_off + ((size_t)t * H + 4 * P) * 2, a.x + (size_t)t * H + 4 * P);
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+    }
     if (!mbar_wait(&s_rbar, 0u, d.err)) ok = false;
     MOE_TRACE_CLOCK(2, 12);
     // One pass over x for all tokens: this thread's max |x| per token and its
@@ -1331,11 +1348,11 @@ bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem) {
 }
 
 cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
-                         float *w, int sm_count, bool coop, cudaStream_t s) {
+                         float *w, int sm_count, bool coop, cudaStream_t s, bool x_sys) {
     FusedGeom fg;
     if (T < 1 || T > kFusedMaxT || d.H > kMaxFusedH || !fused_geometry(d, T, sm_count, g_dyn_max[inst_of(T)], fg))
         return cudaErrorInvalidValue;
-    FusedArgs a{x, T, out, ids, w};
+    FusedArgs a{x, T, out, ids, w, x_sys ? 1 : 0};
     const bool f8 = d.f8e || d.f8s;
     switch (inst_of(T)) {
         case 0: return f8 ? launch_tt<1, true>(d, a, fg, sm_count, coop, s) : launch_tt<1, false>(d, a, fg, sm_count, coop, s);

@@ -159,8 +159,9 @@ cudaError_t launch_grouped_down(const DevLayer &d, int T, __nv_bfloat16 *out, in
 cudaError_t prepare_grouped_kernels(int optin_bytes);
 cudaError_t prepare_kernels();   // per device, once: shared-memory limits
 bool fused_eligible(const DevLayer &d, int T, int sm_count, size_t optin_smem);
+// x_sys: x is the device alias of pinned host memory (read by plain loads)
 cudaError_t launch_fused(const DevLayer &d, const __nv_bfloat16 *x, int T, __nv_bfloat16 *out, int *ids,
-                         float *w, int sm_count, bool coop, cudaStream_t s);
+                         float *w, int sm_count, bool coop, cudaStream_t s, bool x_sys = false);
 int fused_blocks_per_sm(const DevLayer &d, int T);
 cudaError_t launch_repack(const uint8_t *codes, const uint8_t *sf, int n_mats, int rows, int cols,
                           bool gate_up, uint8_t *dst, cudaStream_t s);

@@ -164,11 +164,14 @@ def test_many_calls_keep_tags_in_step(moe, orc):
         L.close()
 
 
-@pytest.mark.parametrize("cfg,T,pinned", [(1, 1, True), (1, 1, False), (0, 12, True), (0, 12, False)])
+@pytest.mark.parametrize("cfg,T,pinned", [(1, 1, True), (1, 1, False), (1, 2, True), (1, 8, True), (0, 12, True),
+                                          (0, 12, False)])
 def test_host_buffer_entry_point(moe, orc, cfg, T, pinned):
     """Host buffers: pinned output is written through its device alias (the
-    single launch at T=1, the chain's down kernel at T=12), pageable output
-    is copied back; both equal the device-buffer call bit for bit."""
+    single launch at T=1, 2 and 8, the chain's down kernel at T=12), pageable
+    output is copied back; a pinned x is read in place by the single launch
+    at T <= 2 and copied up otherwise; all equal the device-buffer call bit
+    for bit."""
     layer, x, _ = guarded_case(cfg, 13, T=T)
     L = moe.MoELayer(layer, max_tokens=T)
     try:
