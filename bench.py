@@ -447,8 +447,10 @@ def run_gpu(args):
             moe.moe_decode_forward_host(chain.layers[l].h, xh[l], T, oh[l], None, None, stream)
 
     # the step's host-buffer calls captured once into a CUDA graph, as a
-    # decode loop runs them (the copies stay in the graph, so every replay
-    # moves x up and the output down); eager calls if capture is refused
+    # decode loop runs them: every replay moves x up (a copy, or at one or
+    # two tokens the kernel's own reads of the pinned rows) and the output
+    # down (the kernels' stores into the pinned rows); eager calls if capture
+    # is refused
     try:
         g_e2e = capture(torch, e2e_step, stream)
         e2e_run, e2e_mode = g_e2e.replay, "CUDA graph of the host-buffer calls"
