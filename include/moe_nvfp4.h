@@ -258,7 +258,10 @@ moe_status moe_decode_forward_host(moe_layer *layer, const void *x_host, int T,
  * exactly moe_stage_route; moe_stage_gate_up; moe_stage_down on one stream
  * with the same T.  Each of the last two consumes the state that the calls
  * before it in this order left in the handle's workspace (the routing, its
- * work counters, h): call the three in order, once each per step.
+ * work counters, h): call the three in order, once each per step.  With
+ * moe_config.w4a4 set, moe_stage_gate_up must follow moe_stage_route on the
+ * stream with no other work between them and with the same, unchanged x:
+ * its token quantiser reads x while the router still runs.
  *   moe_stage_route     a1+a2: logits, sigmoid, top-k, weights (also written
  *                       to topk_ids / topk_w when not NULL), and the list of
  *                       distinct selected experts with their tokens

@@ -508,11 +508,14 @@ moe_status moe_stage_gate_up(moe_layer *L, const void *x, int T, void *stream) {
     const __nv_bfloat16 *xa = static_cast<const __nv_bfloat16 *>(x);
     cudaError_t e = cudaSuccess;
     if (L->d.w4a4) {
-        // W4A4: the tokens quantised first (their f16 prescale exponents
-        // replace the router's); gate/up reads the dequantised rows
+        // W4A4: the tokens quantised first (their f16 prescale exponents are
+        // the only ones: the router leaves them out); gate/up reads the
+        // dequantised rows.  The router's launch comes right before this one
+        // (the stages run in order), so the quantiser runs beside it and
+        // waits for it at its end.
         const int H = L->cfg.hidden;
         e = launch_fos(xa, L->d.xq, T, H, H, 0, 0, L->d.gsx, L->d.xexp, nullptr, L->d.xq4, L->d.xsf, H / 2, H / 16,
-                       st);
+                       st, true);
         xa = L->d.xq;
     }
     if (e == cudaSuccess) e = launch_gate_up(L->d, xa, T, L->sm_count, L->optin_smem, st);

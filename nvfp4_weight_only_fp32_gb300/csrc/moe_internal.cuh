@@ -178,10 +178,13 @@ cudaError_t launch_dequant_f8(const uint8_t *rep, int rows, int cols, bool gate_
 // `stride` elements, the first n_short of length len_short, the rest len_long;
 // writes the dequantised e2m1 * e4m3 values (BF16, exact) to dst (may be
 // src), the global scales, and (optional) the f16 prescale exponent and the
-// max |value| bits of each row.
+// max |value| bits of each row.  wait_late: only right after the router's
+// launch (which releases its dependents once its own dependency wait has
+// returned), for rows the router reads as well: the rows are read at once
+// and the dependency wait comes last.
 cudaError_t launch_fos(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int nrows, int stride, int len_long,
                        int n_short, int len_short, float *gs, int *exp_out, unsigned *max_out, uint8_t *codes,
-                       uint8_t *sfc, int code_stride, int sf_stride, cudaStream_t s);
+                       uint8_t *sfc, int code_stride, int sf_stride, cudaStream_t s, bool wait_late = false);
 // MXFP4 scales: per (matrix, half) the smallest and largest E8M0 code and
 // whether a NaN code (255) occurs -> mm[(mat * 2 + half) * 3 + {0,1,2}]
 // (half 1 only for gate/up: its up rows).

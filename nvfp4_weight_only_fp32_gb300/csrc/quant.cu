@@ -116,14 +116,17 @@ __device__ __forceinline__ void fos_candidate(const float (&v)[4], float m, floa
 __global__ void __launch_bounds__(kFosMaxThreads)
 fos_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int S, int stride, int len_long, int n_short,
            int len_short, float *__restrict__ gs_out, int *__restrict__ exp_out, unsigned *__restrict__ max_out,
-           uint8_t *__restrict__ codes, uint8_t *__restrict__ sfc, int code_stride, int sf_stride) {
+           uint8_t *__restrict__ codes, uint8_t *__restrict__ sfc, int code_stride, int sf_stride, int wait_late) {
     // The next kernel may start at once: its own wait covers this kernel's
-    // completion.  The rows come from the kernels before (the router's input,
-    // the SwiGLU output), complete once this wait returns; it also orders
-    // the writes below after those of the router (x's exponents) and of the
-    // SwiGLU epilogue (h maxima).
+    // completion.  The rows come from the kernels before (the SwiGLU output),
+    // complete once the wait returns; it also orders the writes below after
+    // those of the SwiGLU epilogue (h maxima).  With wait_late (the tokens,
+    // launched right after the router, which releases its dependents only
+    // once its own wait has returned: the tokens are complete by then) the
+    // work runs beside the router and the wait comes last, so that this grid
+    // still completes after the router's.
     pdl_trigger();
-    pdl_wait();
+    if (!wait_late) pdl_wait();
     __shared__ unsigned s_red[kFosMaxThreads / 32];
     __shared__ unsigned s_part[kFosMaxCluster];   // rank 0: each CTA's maximum of the written values
     __shared__ unsigned s_amax;                    // this CTA's maximum of the values read
@@ -244,6 +247,7 @@ fos_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int S, int stride, int 
         if (exp_out) exp_out[r] = max(-100, exp_for_f16(__uint_as_float(nm)));
         if (max_out) max_out[r] = nm;
     }
+    if (wait_late) pdl_wait();
 }
 
 }  // namespace
@@ -261,7 +265,7 @@ static int fos_split(int nrows, int len) {
 
 cudaError_t launch_fos(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int nrows, int stride, int len_long,
                        int n_short, int len_short, float *gs, int *exp_out, unsigned *max_out, uint8_t *codes,
-                       uint8_t *sfc, int code_stride, int sf_stride, cudaStream_t s) {
+                       uint8_t *sfc, int code_stride, int sf_stride, cudaStream_t s, bool wait_late) {
     if (nrows <= 0) return cudaSuccess;
     const int len = n_short > 0 ? max(len_long, len_short) : len_long;
     const int S = fos_split(nrows, len);
@@ -280,7 +284,7 @@ cudaError_t launch_fos(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int nrows, 
     cfg.attrs = attr;
     cfg.numAttrs = S > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, fos_kernel, src, dst, S, stride, len_long, n_short, len_short, gs, exp_out,
-                              max_out, codes, sfc, code_stride, sf_stride);
+                              max_out, codes, sfc, code_stride, sf_stride, wait_late ? 1 : 0);
 }
 
 }  // namespace moe

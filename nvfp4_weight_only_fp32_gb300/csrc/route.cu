@@ -379,10 +379,12 @@ __global__ void __launch_bounds__(kThreads) route_kernel(DevLayer d, const __nv_
         }
     }
     // this token group's power-of-two prescales from their whole-row maxima
-    // (every block of the group has added its part before the ticket above)
+    // (every block of the group has added its part before the ticket above);
+    // with W4A4 the quantiser, running beside this kernel, writes them from
+    // the quantised rows
     if (threadIdx.x < nt) {
         const int t = t0 + threadIdx.x;
-        d.xexp[t] = max(-100, exp_for_f16(__uint_as_float(__ldcg(d.xmaxb + t))));
+        if (!d.w4a4) d.xexp[t] = max(-100, exp_for_f16(__uint_as_float(__ldcg(d.xmaxb + t))));
         d.xmaxb[t] = 0u;
     }
     MOE_TRACE_POINT(0, 11);
