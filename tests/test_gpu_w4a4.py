@@ -169,3 +169,36 @@ def test_w4a4_workloads_full_size(moe, orc, cfg):
     layer, x, _ = guarded_case(cfg, gen.BASE_SEED + 90 + cfg)
     gout, gids, gw = run_gpu(moe, layer, x)
     check_parity(orc, layer, x, gout, gids, gw)
+
+
+@pytest.mark.parametrize("T", [5, 37])
+def test_w4a4_stage_entry_points_repeat(moe, orc, T):
+    """The stages called one by one, twice in a row on one handle, equal the
+    chained forward bit for bit: the token quantiser reads x while the router
+    still runs and waits for it last, and a second step's quantiser must not
+    overtake the first step's consumers of its outputs."""
+    c = dict(name="w4a4", T=T, H=320, E=33, k=4, I=192, S=1, Is=128, zipf=False, normalize=1, routed_scale=1.0,
+             w4a4=1)
+    layer, x, _ = guarded_case(c, 9300 + T)
+    L = moe.MoELayer(layer, max_tokens=T, grouped_min_tokens=2)
+    try:
+        xd = x_to_device(x)
+        H, k = layer["cfg"]["H"], layer["cfg"]["k"]
+        outs = []
+        for _ in range(2):
+            out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+            ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+            w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+            moe.moe_stage_route(L.h, xd, T, ids, w)
+            moe.moe_stage_gate_up(L.h, xd, T)
+            moe.moe_stage_down(L.h, T, out)
+            outs.append((out, ids, w))
+        torch.cuda.synchronize()
+        fout, fids, fw = run_gpu(moe, layer, x, layer_obj=L)
+        for out, ids, w in outs:
+            assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), fout)
+            assert np.array_equal(ids.cpu().numpy(), fids)
+            assert np.array_equal(w.cpu().numpy(), fw)
+        check_parity(orc, layer, x, fout, fids, fw)
+    finally:
+        L.close()
