@@ -52,8 +52,8 @@ WORKLOADS = {
 # kernel source they were taken on: reported as `traffic` while fused.cu
 # hashes to the value below, null otherwise.
 NCU_TRAFFIC = {
-    "flint1": {"bytes": 20788736, "fused_cu_sha256_16": "48887d91ca152f48"},
-    "flint8": {"bytes": 124297472, "fused_cu_sha256_16": "48887d91ca152f48"},
+    "flint1": {"bytes": 20788736, "fused_cu_sha256_16": "3fd6c6f8882e58a0"},
+    "flint8": {"bytes": 124420864, "fused_cu_sha256_16": "3fd6c6f8882e58a0"},
 }
 
 def ncu_traffic(workload: str):

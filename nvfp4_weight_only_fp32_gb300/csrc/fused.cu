@@ -327,17 +327,17 @@ __device__ __forceinline__ bool route_token(const DevLayer &d, const unsigned lo
         v[i] = e < E ? ((unsigned long long)logit_key(__uint_as_float((unsigned)v[i])) << 32) | (unsigned)~e : 0ull;
     }
     MOE_TRACE_CLOCK_AT(4, 1, 0);
-    // the sorted top-k for one or two tokens (measured faster there; slower
-    // at eight, where eight warps route at once) on a copy, so that v keeps
-    // the index order: a lane's chosen keys are larger than every key it has
-    // left (rest[0]); the tree form clears the chosen keys in v
+    // the sorted top-k: for one or two tokens on a copy, so that v keeps the
+    // index order (a lane's chosen keys are larger than every key it has
+    // left, rest[0]); for more tokens in place (v ends with the keys not
+    // chosen, largest first)
     unsigned long long rest[M];
     if constexpr (SORTED) {
 #pragma unroll
         for (int i = 0; i < M; ++i) rest[i] = v[i];
         sel = warp_topk_sorted<M>(rest, K, lane);
     } else {
-        sel = warp_topk_tree<M>(v, K, lane);
+        sel = warp_topk_sorted<M>(v, K, lane);
     }
     den = 1.f;
     if (full_den) {
