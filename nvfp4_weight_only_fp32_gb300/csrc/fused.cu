@@ -27,7 +27,9 @@
 //      packed global scales into shared memory; start the rings of the
 //      shared-expert pass; L2-prefetch this block's rows of the shared down
 //      weights.
-//   B  x (T rows) arrives by one bulk copy; one pass over it gives the
+//   B  x (T rows) arrives by each thread's own asynchronous copies of the
+//      quads it reads (plain loads from pinned host memory when x lives
+//      there); one pass over it gives the
 //      per-token max |x| and this block's experts' FP32 logits, published as
 //      tagged words; the shared-expert warps stage x as the f16 MMA operand
 //      (exact per-row power-of-two prescale).

@@ -14,13 +14,16 @@
 // work list built here enables).
 //
 // Grid: (E/8 expert groups) x (token groups of up to 8 tokens) x (K ranges:
-// the router rows are split along H until the grid covers the SMs).  Each
-// warp owns one expert and one K range: that part of its router row is
-// fetched into registers BEFORE the programmatic-launch wait (router weights
-// do not depend on the previous kernel); the block stages its token group's
-// activation columns in shared memory (as FP32) and the warp computes the
-// FP32 partial logits of those tokens (one accumulator per token, so the FMA
-// chains run side by side).  With several K ranges the partial sums go to the
+// the router rows are split along H until the grid covers the SMs).  A
+// block's threads form two halves of four experts; a thread takes 4-column
+// groups of the K range for its half's four experts, whose router columns it
+// fetches into registers BEFORE the programmatic-launch wait (router weights
+// do not depend on the previous kernel).  The block stages its token group's
+// activation columns in shared memory (BF16, by asynchronous copies) and each
+// x group a thread reads there serves four experts' FP32 partial logits (one
+// accumulator per expert and token, so the FMA chains run side by side); a
+// transposing butterfly and a fixed-order sum over a half's warps give the
+// logits.  With several K ranges the partial sums go to the
 // workspace and the ticket's last block adds them in a fixed order, into
 // shared memory.  Two tickets follow, with no spinning:
 //   * the last expert group of a token group to finish runs the scores and
