@@ -252,13 +252,17 @@ fos_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int S, int stride, int 
 
 }  // namespace
 
+// GB300's SM count, for the split heuristic below only: any value gives the
+// same results (no device query in the launch path, which may be captured).
+constexpr int kFosSmsHint = 152;
+
 // The cluster size: the fewest CTAs per row (1, 2, 4 or 8) that give at
-// least 2 x 152 CTAs in all, or blocks of at most 32 16-element runs (128
+// least two CTAs per SM in all, or blocks of at most 32 16-element runs (128
 // threads) per CTA.
 static int fos_split(int nrows, int len) {
     const int nblk = len / 16;
     int S = 1;
-    while (S < kFosMaxCluster && (long long)nrows * S < 2 * 152 && (nblk + S - 1) / S > 32) S *= 2;
+    while (S < kFosMaxCluster && (long long)nrows * S < 2LL * kFosSmsHint && (nblk + S - 1) / S > 32) S *= 2;
     while (S < kFosMaxCluster && (nblk + S - 1) / S > kFosMaxThreads / 4) S *= 2;
     return S;
 }
